@@ -1,0 +1,275 @@
+/*
+ * nfo.c -- fp64 CPU oracle for the normalization-fused bf16 GEMM.
+ *
+ * TEST INFRASTRUCTURE: only tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load it.  It shares no code with the CUDA library.
+ *
+ * Each function writes out the plain definition of its operation in double
+ * precision: widen the bf16 inputs exactly, form the product with plain
+ * loops, then apply the normalization as defined, with no blocking, no fusion
+ * and no reordering beyond what the definition states.
+ *
+ * Definitions followed ("Towards Free Normalization: Fusing Normalization
+ * into GEMM and Attention Kernels"):
+ *   - §2, Lazy Pre-Norm: C = rmsnorm(A) @ B, with rmsnorm(A) = A * rstd(A)
+ *     row-wise and rstd(A) = rsqrt(sum(A^2 over the row) / row length + eps).
+ *   - §3, Multi-CTA Norm: C = norm(A @ B), the norm taken over each full
+ *     output row of length N.
+ *   - LayerNorm as torch.nn.LayerNorm (linked from the blog's Introduction):
+ *     biased variance (divide by N), eps inside the square root, then
+ *     elementwise gain gamma and bias beta.
+ *   - RMSNorm with a gain: y = x / sqrt(mean(x^2) + eps) * gamma (the
+ *     FusedRMSNorm+MatMul article, §3.1 "数学原理重述").
+ */
+#include "nfo.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> double, exact (bf16 is the top half of an fp32). */
+static double bf16_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int check_rows(const int64_t* rows, int64_t nrows, int64_t M) {
+    if (!rows) return 0;
+    if (nrows < 0) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return -1;
+    return 0;
+}
+
+static int64_t row_count(const int64_t* rows, int64_t nrows, int64_t M) {
+    return rows ? nrows : M;
+}
+
+static int64_t row_index(const int64_t* rows, int64_t r) {
+    return rows ? rows[r] : r;
+}
+
+/* z[j] = sum_k x[k] * W[k][j] for one row x of length K (fp64). */
+static void row_times_w(const double* x, const uint16_t* W, int64_t N, int64_t K,
+                        double* z) {
+    for (int64_t j = 0; j < N; ++j) z[j] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double xk = x[k];
+        const uint16_t* wk = W + k * N;
+        for (int64_t j = 0; j < N; ++j) z[j] += xk * bf16_to_double(wk[j]);
+    }
+}
+
+static void load_row(const uint16_t* A, int64_t i, int64_t len, double* out) {
+    const uint16_t* a = A + i * len;
+    for (int64_t k = 0; k < len; ++k) out[k] = bf16_to_double(a[k]);
+}
+
+/* LayerNorm of one row v (length n) as torch.nn.LayerNorm defines it:
+ * two passes, biased variance, eps inside the root. */
+static void layernorm_row(const double* v, int64_t n, const uint16_t* gamma,
+                          const uint16_t* beta, double eps, double* y,
+                          double* mean_out, double* rstd_out) {
+    double s = 0.0;
+    for (int64_t j = 0; j < n; ++j) s += v[j];
+    const double mu = s / (double)n;
+    double ss = 0.0;
+    for (int64_t j = 0; j < n; ++j) ss += (v[j] - mu) * (v[j] - mu);
+    const double var = ss / (double)n;
+    const double rstd = 1.0 / sqrt(var + eps);
+    for (int64_t j = 0; j < n; ++j) {
+        double t = (v[j] - mu) * rstd;
+        if (gamma) t *= bf16_to_double(gamma[j]);
+        if (beta) t += bf16_to_double(beta[j]);
+        y[j] = t;
+    }
+    if (mean_out) *mean_out = mu;
+    if (rstd_out) *rstd_out = rstd;
+}
+
+/* RMSNorm of one row v (length n): v / sqrt(mean(v^2) + eps) * gamma. */
+static void rmsnorm_row(const double* v, int64_t n, const uint16_t* gamma,
+                        double eps, double* y, double* rstd_out) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < n; ++j) ss += v[j] * v[j];
+    const double rstd = 1.0 / sqrt(ss / (double)n + eps);
+    for (int64_t j = 0; j < n; ++j) {
+        double t = v[j] * rstd;
+        if (gamma) t *= bf16_to_double(gamma[j]);
+        y[j] = t;
+    }
+    if (rstd_out) *rstd_out = rstd;
+}
+
+int nfo_gemm_plain(const uint16_t* X, const uint16_t* W, int64_t M, int64_t N,
+                   int64_t K, const int64_t* rows, int64_t nrows, double* Y) {
+    if (!X || !W || !Y || M < 0 || N <= 0 || K <= 0) return -1;
+    if (check_rows(rows, nrows, M)) return -1;
+    const int64_t R = row_count(rows, nrows, M);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* x = (double*)malloc(sizeof(double) * (size_t)K);
+        if (!x) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!x) continue;
+            load_row(X, row_index(rows, r), K, x);
+            row_times_w(x, W, N, K, Y + r * N);
+        }
+        free(x);
+    }
+    return bad ? -1 : 0;
+}
+
+int nfo_gemm_prenorm_rms(const uint16_t* X, const uint16_t* W, int64_t M,
+                         int64_t N, int64_t K, double eps, const int64_t* rows,
+                         int64_t nrows, double* Y, double* rstd_out) {
+    if (!X || !W || !Y || M < 0 || N <= 0 || K <= 0 || !(eps >= 0.0)) return -1;
+    if (check_rows(rows, nrows, M)) return -1;
+    const int64_t R = row_count(rows, nrows, M);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* x = (double*)malloc(sizeof(double) * (size_t)K);
+        if (!x) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!x) continue;
+            load_row(X, row_index(rows, r), K, x);
+            /* rstd over the full row of X (length K) ... */
+            double ss = 0.0;
+            for (int64_t k = 0; k < K; ++k) ss += x[k] * x[k];
+            const double rstd = 1.0 / sqrt(ss / (double)K + eps);
+            /* ... rmsnorm(X) materialised in fp64 ... */
+            for (int64_t k = 0; k < K; ++k) x[k] *= rstd;
+            /* ... then the product with W. */
+            row_times_w(x, W, N, K, Y + r * N);
+            if (rstd_out) rstd_out[r] = rstd;
+        }
+        free(x);
+    }
+    return bad ? -1 : 0;
+}
+
+int nfo_gemm_postnorm_ln(const uint16_t* X, const uint16_t* W,
+                         const uint16_t* gamma, const uint16_t* beta,
+                         int64_t M, int64_t N, int64_t K, double eps,
+                         const int64_t* rows, int64_t nrows, double* Y,
+                         double* mean_out, double* rstd_out) {
+    if (!X || !W || !Y || M < 0 || N <= 0 || K <= 0 || !(eps >= 0.0)) return -1;
+    if (check_rows(rows, nrows, M)) return -1;
+    const int64_t R = row_count(rows, nrows, M);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* x = (double*)malloc(sizeof(double) * (size_t)K);
+        double* z = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!x || !z) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!x || !z) continue;
+            load_row(X, row_index(rows, r), K, x);
+            row_times_w(x, W, N, K, z);                       /* Z = X W */
+            layernorm_row(z, N, gamma, beta, eps, Y + r * N,  /* norm(Z) */
+                          mean_out ? mean_out + r : NULL,
+                          rstd_out ? rstd_out + r : NULL);
+        }
+        free(x);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}
+
+int nfo_gemm_postnorm_rms(const uint16_t* X, const uint16_t* W,
+                          const uint16_t* gamma, int64_t M, int64_t N,
+                          int64_t K, double eps, const int64_t* rows,
+                          int64_t nrows, double* Y, double* rstd_out) {
+    if (!X || !W || !Y || M < 0 || N <= 0 || K <= 0 || !(eps >= 0.0)) return -1;
+    if (check_rows(rows, nrows, M)) return -1;
+    const int64_t R = row_count(rows, nrows, M);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* x = (double*)malloc(sizeof(double) * (size_t)K);
+        double* z = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!x || !z) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!x || !z) continue;
+            load_row(X, row_index(rows, r), K, x);
+            row_times_w(x, W, N, K, z);
+            rmsnorm_row(z, N, gamma, eps, Y + r * N,
+                        rstd_out ? rstd_out + r : NULL);
+        }
+        free(x);
+        free(z);
+    }
+    return bad ? -1 : 0;
+}
+
+int nfo_norm_rows(const uint16_t* in, const uint16_t* gamma,
+                  const uint16_t* beta, int64_t R, int64_t C, int kind,
+                  double eps, const int64_t* rows, int64_t nrows, double* out,
+                  double* mean_out, double* rstd_out) {
+    if (!in || !out || R < 0 || C <= 0 || !(eps >= 0.0)) return -1;
+    if (kind != NFO_NORM_LN && kind != NFO_NORM_RMS) return -1;
+    if (check_rows(rows, nrows, R)) return -1;
+    const int64_t n = row_count(rows, nrows, R);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* v = (double*)malloc(sizeof(double) * (size_t)C);
+        if (!v) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < n; ++r) {
+            if (!v) continue;
+            load_row(in, row_index(rows, r), C, v);
+            if (kind == NFO_NORM_LN)
+                layernorm_row(v, C, gamma, beta, eps, out + r * C,
+                              mean_out ? mean_out + r : NULL,
+                              rstd_out ? rstd_out + r : NULL);
+            else
+                rmsnorm_row(v, C, gamma, eps, out + r * C,
+                            rstd_out ? rstd_out + r : NULL);
+        }
+        free(v);
+    }
+    return bad ? -1 : 0;
+}
+
+int nfo_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void nfo_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

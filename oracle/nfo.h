@@ -1,0 +1,76 @@
+/*
+ * nfo.h -- fp64 CPU oracle for the normalization-fused bf16 GEMM.
+ *
+ * TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library. The CUDA library never
+ * calls it and the two share no source, header, table or helper.
+ *
+ * Conventions shared by every function:
+ *   - X is M x K, W is K x N, gamma and beta have N entries; all are row-major
+ *     bfloat16 given as raw uint16 bit patterns and widened to double exactly.
+ *   - `rows` lists the output rows to compute (nrows of them, each in [0, M));
+ *     rows == NULL means all rows 0..M-1 (nrows is then ignored).  Results are
+ *     written densely: output row r of Y (N doubles) belongs to X row rows[r].
+ *   - gamma / beta may be NULL (no gain / no bias).  mean / rstd outputs may
+ *     be NULL.
+ *   - eps is added inside the square root, to the mean (of squares or of
+ *     squared deviations).
+ *   - Return value: 0 on success, -1 on an invalid argument.
+ *
+ * Source: "Towards Free Normalization: Fusing Normalization into GEMM and
+ * Attention Kernels" (PyTorch blog), §2 Lazy Pre-Norm and §3 Multi-CTA Norm;
+ * LayerNorm as torch.nn.LayerNorm, which that blog's Introduction links.
+ */
+#ifndef NFO_H
+#define NFO_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NFO_NORM_LN 0
+#define NFO_NORM_RMS 1
+
+/* Y = X W (fp64 sums of exact products). */
+int nfo_gemm_plain(const uint16_t* X, const uint16_t* W, int64_t M, int64_t N,
+                   int64_t K, const int64_t* rows, int64_t nrows, double* Y);
+
+/* Y = rmsnorm(X) W with rmsnorm(X)[i,k] = X[i,k] * r_i and
+ * r_i = 1 / sqrt(sum_k X[i,k]^2 / K + eps): normalize first, then multiply
+ * (blog §2, definition of C = rmsnorm(A) @ B). rstd_out[r] = r_i. */
+int nfo_gemm_prenorm_rms(const uint16_t* X, const uint16_t* W, int64_t M,
+                         int64_t N, int64_t K, double eps, const int64_t* rows,
+                         int64_t nrows, double* Y, double* rstd_out);
+
+/* Z = X W; Y = (Z - mu_i) / sqrt(var_i + eps) * gamma_j + beta_j with
+ * mu_i = mean_j Z[i,j] and var_i = mean_j (Z[i,j] - mu_i)^2 (blog §3,
+ * C = norm(A @ B), LayerNorm over N). */
+int nfo_gemm_postnorm_ln(const uint16_t* X, const uint16_t* W,
+                         const uint16_t* gamma, const uint16_t* beta,
+                         int64_t M, int64_t N, int64_t K, double eps,
+                         const int64_t* rows, int64_t nrows, double* Y,
+                         double* mean_out, double* rstd_out);
+
+/* Z = X W; Y = Z / sqrt(mean_j Z[i,j]^2 + eps) * gamma_j (blog §3 with RMSNorm). */
+int nfo_gemm_postnorm_rms(const uint16_t* X, const uint16_t* W,
+                          const uint16_t* gamma, int64_t M, int64_t N,
+                          int64_t K, double eps, const int64_t* rows,
+                          int64_t nrows, double* Y, double* rstd_out);
+
+/* LayerNorm (kind 0) or RMSNorm (kind 1) of each row of `in` (R x C), the
+ * unfused normalization kernel of the blog's §1 baseline. beta is ignored for
+ * RMSNorm; mean_out is left untouched for RMSNorm. */
+int nfo_norm_rows(const uint16_t* in, const uint16_t* gamma,
+                  const uint16_t* beta, int64_t R, int64_t C, int kind,
+                  double eps, const int64_t* rows, int64_t nrows, double* out,
+                  double* mean_out, double* rstd_out);
+
+/* Threads used by the loops over rows (OpenMP). */
+int nfo_max_threads(void);
+void nfo_set_threads(int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

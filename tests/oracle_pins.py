@@ -1,0 +1,424 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each pin takes an ``oracle.Oracle`` and raises ``AssertionError`` on a
+mismatch.  They are chosen so that a plausible slip anywhere in the oracle (a
+dropped term, a wrong sign, divisor or index, a transposed operand, eps in the
+wrong place) fails at least one of them; ``test_oracle_mutants.py`` plants such
+slips in copies of the oracle and checks exactly that.
+
+What each pin compares against:
+  * brute force   -- exact rational arithmetic (``fractions``) for sums and
+                     products and 60-digit ``decimal`` square roots, on tiny
+                     shapes;
+  * torch float64 -- ``torch.nn.functional.layer_norm`` / ``rms_norm`` and
+                     ``@`` on the CPU, the library special cases;
+  * identity      -- (A * rstd[:, None]) @ B == (A @ B) * rstd[:, None], the
+                     blog's §2 "Proof";
+  * invariants    -- normalized rows have mean 0 / variance (or mean square)
+                     var/(var+eps) = 1 - eps*rstd^2;
+  * closed forms  -- hand-derived results under ``tests/golden/``;
+  * reductions    -- W = I and permutation W, unit gain and zero bias,
+                     power-of-two row scales, row-subset consistency.
+
+Run as a script (``python tests/oracle_pins.py LIB.so``) it loads the given
+library, runs every pin and prints a JSON list of results.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import sys
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+
+_ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+import nf_inputs  # noqa: E402
+from nf_inputs import bf16_round, bf16_to_f64  # noqa: E402
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+getcontext().prec = 60
+
+
+# ---------------------------------------------------------------- helpers
+def _frac_matrix(bits: np.ndarray):
+    """bf16 bits -> nested lists of exact Fractions."""
+    vals = bf16_to_f64(bits)
+    return [[Fraction(float(v)) for v in row] for row in np.atleast_2d(vals)]
+
+
+def _dec(f: Fraction) -> Decimal:
+    return Decimal(f.numerator) / Decimal(f.denominator)
+
+
+def _rsqrt(f: Fraction) -> Decimal:
+    return Decimal(1) / _dec(f).sqrt()
+
+
+def _tiny_cases():
+    """Tiny problems with awkward rows: zero, constant, mixed sign, large."""
+    cases = []
+    for seed, (M, K, N) in enumerate([(3, 5, 4), (4, 8, 6), (2, 1, 3), (5, 7, 8)]):
+        inp = nf_inputs.make_inputs(M, K, N, seed=100 + seed, gamma=True, beta=True,
+                                    w_var=0.5)
+        X = inp["X"].copy()
+        if M >= 3:
+            X[1, :] = 0                                   # zero row
+            X[2, :] = bf16_round(np.full(K, 1.5))         # constant row
+        cases.append((X, inp["W"], inp["gamma"], inp["beta"]))
+    return cases
+
+
+def _close(got, exact, bound, what):
+    got = float(got)
+    err = abs(Decimal(repr(got)) - exact)
+    assert err <= Decimal(repr(float(bound))), f"{what}: got {got!r}, exact {exact}, err {err}"
+
+
+# ---------------------------------------------------------------- brute force
+def pin_bruteforce_plain(o):
+    for X, W, _, _ in _tiny_cases():
+        M, K = X.shape
+        N = W.shape[1]
+        Y = o.gemm_plain(X, W)
+        xf, wf = _frac_matrix(X), _frac_matrix(W)
+        for i in range(M):
+            for j in range(N):
+                exact = sum((xf[i][k] * wf[k][j] for k in range(K)), Fraction(0))
+                mag = sum(abs(xf[i][k] * wf[k][j]) for k in range(K))
+                _close(Y[i, j], _dec(exact), 1e-15 * float(mag) + 1e-300, f"plain[{i},{j}]")
+
+
+def pin_bruteforce_prenorm(o):
+    for eps in (1e-6, 0.5):
+        for X, W, _, _ in _tiny_cases():
+            M, K = X.shape
+            N = W.shape[1]
+            Y, rstd = o.gemm_prenorm_rms(X, W, eps)
+            xf, wf = _frac_matrix(X), _frac_matrix(W)
+            e = Fraction(eps)
+            for i in range(M):
+                ms = sum((x * x for x in xf[i]), Fraction(0)) / K
+                r = _rsqrt(ms + e)
+                _close(rstd[i], r, 1e-14 * float(r), f"pre rstd[{i}]")
+                for j in range(N):
+                    dot = sum((xf[i][k] * wf[k][j] for k in range(K)), Fraction(0))
+                    mag = sum(abs(xf[i][k] * wf[k][j]) for k in range(K))
+                    _close(Y[i, j], _dec(dot) * r, 1e-14 * float(mag) * float(r) + 1e-300,
+                           f"pre[{i},{j}] eps={eps}")
+
+
+def _ln_exact(z, eps, g=None, b=None):
+    n = len(z)
+    mu = sum(z, Fraction(0)) / n
+    var = sum(((v - mu) ** 2 for v in z), Fraction(0)) / n
+    r = _rsqrt(var + Fraction(eps))
+    y = []
+    for j, v in enumerate(z):
+        t = _dec(v - mu) * r
+        if g is not None:
+            t *= _dec(g[j])
+        if b is not None:
+            t += _dec(b[j])
+        y.append(t)
+    return y, _dec(mu), r
+
+
+def _rms_exact(z, eps, g=None):
+    n = len(z)
+    ms = sum((v * v for v in z), Fraction(0)) / n
+    r = _rsqrt(ms + Fraction(eps))
+    y = []
+    for j, v in enumerate(z):
+        t = _dec(v) * r
+        if g is not None:
+            t *= _dec(g[j])
+        y.append(t)
+    return y, r
+
+
+def pin_bruteforce_postnorm(o):
+    for eps in (1e-5, 0.5):
+        for X, W, G, B in _tiny_cases():
+            M, K = X.shape
+            N = W.shape[1]
+            xf, wf = _frac_matrix(X), _frac_matrix(W)
+            gf, bf = _frac_matrix(G)[0], _frac_matrix(B)[0]
+            for affine in (False, True):
+                g = G if affine else None
+                b = B if affine else None
+                Yl, mean, rstd = o.gemm_postnorm_ln(X, W, eps, g, b)
+                Yr, rstd_r = o.gemm_postnorm_rms(X, W, eps, g)
+                for i in range(M):
+                    z = [sum((xf[i][k] * wf[k][j] for k in range(K)), Fraction(0))
+                         for j in range(N)]
+                    mag = max(float(sum(abs(xf[i][k] * wf[k][j]) for k in range(K)))
+                              for j in range(N))
+                    y, mu, r = _ln_exact(z, eps, gf if affine else None, bf if affine else None)
+                    _close(mean[i], mu, 1e-14 * mag + 1e-300, f"ln mean[{i}]")
+                    _close(rstd[i], r, 1e-12 * float(r), f"ln rstd[{i}]")
+                    for j in range(N):
+                        _close(Yl[i, j], y[j], 1e-13 * (1 + mag * float(r)) * 2,
+                               f"post-ln[{i},{j}] eps={eps} affine={affine}")
+                    y2, r2 = _rms_exact(z, eps, gf if affine else None)
+                    _close(rstd_r[i], r2, 1e-13 * float(r2), f"rms rstd[{i}]")
+                    for j in range(N):
+                        _close(Yr[i, j], y2[j], 1e-13 * (1 + mag * float(r2)) * 2,
+                               f"post-rms[{i},{j}] eps={eps} affine={affine}")
+
+
+def pin_bruteforce_norm_rows(o):
+    for eps in (1e-5, 0.5):
+        for X, _, _, _ in _tiny_cases():
+            R, C = X.shape
+            G = bf16_round(np.linspace(0.5, 1.5, C))
+            B = bf16_round(np.linspace(-0.25, 0.25, C))
+            xf = _frac_matrix(X)
+            gf, bf = _frac_matrix(G)[0], _frac_matrix(B)[0]
+            yl, mean, rstd = o.norm_rows(X, 0, eps, G, B)
+            yr, _, rstd_r = o.norm_rows(X, 1, eps, G, None)
+            for i in range(R):
+                mag = float(max(abs(v) for v in xf[i])) + 1e-300
+                y, mu, r = _ln_exact(xf[i], eps, gf, bf)
+                _close(mean[i], mu, 1e-15 * mag, "norm_rows mean")
+                _close(rstd[i], r, 1e-13 * float(r), "norm_rows ln rstd")
+                for j in range(C):
+                    _close(yl[i, j], y[j], 1e-13 * (1 + mag * float(r)), f"norm_rows ln[{i},{j}]")
+                y2, r2 = _rms_exact(xf[i], eps, gf)
+                _close(rstd_r[i], r2, 1e-13 * float(r2), "norm_rows rms rstd")
+                for j in range(C):
+                    _close(yr[i, j], y2[j], 1e-13 * (1 + mag * float(r2)), f"norm_rows rms[{i},{j}]")
+
+
+# ---------------------------------------------------------------- torch fp64
+def pin_torch_f64(o):
+    import torch
+    import torch.nn.functional as F
+    for (M, K, N, eps) in [(37, 72, 40, 1e-5), (19, 136, 24, 1e-6), (8, 8, 264, 1e-5)]:
+        inp = nf_inputs.make_inputs(M, K, N, seed=M + K + N, gamma=True, beta=True)
+        X, W, G, B = inp["X"], inp["W"], inp["gamma"], inp["beta"]
+        x = torch.from_numpy(bf16_to_f64(X))
+        w = torch.from_numpy(bf16_to_f64(W))
+        g = torch.from_numpy(bf16_to_f64(G))
+        b = torch.from_numpy(bf16_to_f64(B))
+        z = x @ w
+        scale = (x.abs() @ w.abs()).max().item()
+
+        def cmp(got, want, tol, what):
+            err = np.max(np.abs(np.asarray(got) - want.numpy()))
+            assert err <= tol, f"{what}: max err {err} > {tol}"
+
+        cmp(o.gemm_plain(X, W), z, 1e-13 * scale, "plain vs torch")
+        Yp, rp = o.gemm_prenorm_rms(X, W, eps)
+        cmp(Yp, F.rms_norm(x, (K,), eps=eps) @ w, 1e-13 * scale, "prenorm vs torch")
+        cmp(rp, torch.rsqrt((x * x).mean(-1) + eps), 1e-13, "prenorm rstd vs torch")
+        for gg, bb in ((None, None), (g, b)):
+            Yl, mean, rstd = o.gemm_postnorm_ln(X, W, eps, G if gg is not None else None,
+                                                B if bb is not None else None)
+            cmp(Yl, F.layer_norm(z, (N,), gg, bb, eps), 1e-11, "post-ln vs torch")
+            cmp(mean, z.mean(-1), 1e-13 * scale, "post-ln mean vs torch")
+            cmp(rstd, torch.rsqrt(z.var(-1, unbiased=False) + eps), 1e-10, "post-ln rstd")
+            Yr, rr = o.gemm_postnorm_rms(X, W, eps, G if gg is not None else None)
+            cmp(Yr, F.rms_norm(z, (N,), gg, eps), 1e-11, "post-rms vs torch")
+        yl, mean, rstd = o.norm_rows(X, 0, eps, None, None)
+        cmp(yl, F.layer_norm(x, (K,), None, None, eps), 1e-11, "norm_rows ln vs torch")
+        Gk = bf16_round(np.linspace(0.5, 1.5, K))
+        Bk = bf16_round(np.linspace(-1.0, 1.0, K))
+        gk = torch.from_numpy(bf16_to_f64(Gk))
+        bk = torch.from_numpy(bf16_to_f64(Bk))
+        yl, mean, rstd = o.norm_rows(X, 0, eps, Gk, Bk)
+        cmp(yl, F.layer_norm(x, (K,), gk, bk, eps), 1e-11, "norm_rows ln affine vs torch")
+        cmp(mean, x.mean(-1), 1e-14, "norm_rows mean vs torch")
+        yr, _, _ = o.norm_rows(X, 1, eps, Gk, None)
+        cmp(yr, F.rms_norm(x, (K,), gk, eps), 1e-11, "norm_rows rms vs torch")
+
+
+# ---------------------------------------------------------------- identity
+def pin_lazy_identity(o):
+    """Blog §2 "Proof": (A*rstd) @ B == (A @ B) * rstd for a row-wise scale."""
+    inp = nf_inputs.make_inputs(64, 192, 96, seed=7, x_dist="row_scaled")
+    X, W = inp["X"], inp["W"]
+    Yp, rstd = o.gemm_prenorm_rms(X, W, 1e-6)
+    Z = o.gemm_plain(X, W)
+    x = bf16_to_f64(X)
+    scale = (np.abs(x) @ np.abs(bf16_to_f64(W))) * rstd[:, None]
+    err = np.abs(Yp - Z * rstd[:, None])
+    assert np.all(err <= 1e-13 * scale + 1e-300), f"lazy identity: max err {err.max()}"
+    # rstd follows the rstd formula of §2 over the full row of X (length K).
+    want = 1.0 / np.sqrt((x * x).sum(-1) / x.shape[1] + 1e-6)
+    assert np.allclose(rstd, want, rtol=1e-13, atol=0), "rstd formula"
+
+
+# ---------------------------------------------------------------- invariants
+def pin_invariants(o):
+    M, K, N = 48, 128, 136
+    for eps in (1e-5, 1e-2):
+        inp = nf_inputs.make_inputs(M, K, N, seed=11)
+        X, W = inp["X"], inp["W"]
+        Yl, mean, rstd = o.gemm_postnorm_ln(X, W, eps)
+        assert np.all(np.abs(Yl.mean(-1)) <= 1e-13), "LN rows must have mean 0"
+        var_out = (Yl * Yl).mean(-1)
+        assert np.allclose(var_out, 1.0 - eps * rstd ** 2, rtol=1e-12, atol=0), \
+            "LN rows must have variance var/(var+eps)"
+        Z = o.gemm_plain(X, W)
+        assert np.allclose(mean, Z.mean(-1), rtol=0, atol=1e-13), "LN mean_out"
+        Yr, rr = o.gemm_postnorm_rms(X, W, eps)
+        assert np.allclose((Yr * Yr).mean(-1), 1.0 - eps * rr ** 2, rtol=1e-12, atol=0), \
+            "RMS rows must have mean square ms/(ms+eps)"
+        # Pre-norm with W = I reproduces RMSNorm(X): mean square ms/(ms+eps) over K.
+        I = bf16_round(np.eye(K))
+        Yp, rp = o.gemm_prenorm_rms(X, I, eps)
+        assert np.allclose((Yp * Yp).mean(-1), 1.0 - eps * rp ** 2, rtol=1e-12, atol=0), \
+            "pre-RMS with W=I must give unit mean square"
+
+
+# ---------------------------------------------------------------- reductions
+def pin_reductions(o):
+    M, K = 24, 96
+    eps = 1e-5
+    inp = nf_inputs.make_inputs(M, K, K, seed=5, gamma=True, beta=True)
+    X, G, B = inp["X"], inp["gamma"], inp["beta"]
+    I = bf16_round(np.eye(K))
+    a, ma, ra = o.gemm_postnorm_ln(X, I, eps, G, B)
+    b, mb, rb = o.norm_rows(X, 0, eps, G, B)
+    assert np.array_equal(a, b) and np.array_equal(ma, mb) and np.array_equal(ra, rb), \
+        "post-LN with W=I must equal LayerNorm(X)"
+    a, ra = o.gemm_postnorm_rms(X, I, eps, G)
+    b, _, rb = o.norm_rows(X, 1, eps, G)
+    assert np.array_equal(a, b) and np.array_equal(ra, rb), "post-RMS with W=I"
+    a, ra = o.gemm_prenorm_rms(X, I, eps)
+    b, _, rb = o.norm_rows(X, 1, eps)
+    assert np.allclose(a, b, rtol=0, atol=1e-15) and np.allclose(ra, rb, rtol=1e-15), \
+        "pre-RMS with W=I must equal RMSNorm(X)"
+    # unit gain and zero bias are the no-affine result
+    one = bf16_round(np.ones(K))
+    zero = bf16_round(np.zeros(K))
+    a, _, _ = o.gemm_postnorm_ln(X, I, eps, one, zero)
+    b, _, _ = o.gemm_postnorm_ln(X, I, eps)
+    assert np.array_equal(a, b), "gamma=1, beta=0 must equal no affine"
+    # a (non-symmetric) permutation W permutes columns: pins the W index order
+    perm = np.roll(np.arange(K), 1)
+    P = np.zeros((K, K))
+    P[np.arange(K), perm] = 1.0
+    Yp = o.gemm_plain(X, bf16_round(P))
+    x = bf16_to_f64(X)
+    want = np.zeros_like(x)
+    want[:, perm] = x
+    assert np.array_equal(Yp, want), "X @ P must move column k to perm[k]"
+    # a non-square W with a distinct value per (k, j) pins the W index order
+    Kp, Np = 6, 4
+    Wr = bf16_round(np.arange(Kp * Np, dtype=np.float64).reshape(Kp, Np))
+    Xr = bf16_round(np.eye(Kp)[:3])                 # rows e_0, e_1, e_2
+    assert np.array_equal(o.gemm_plain(Xr, Wr), bf16_to_f64(Wr)[:3]), "e_k @ W = W[k,:]"
+
+
+def pin_power_of_two_scale(o):
+    """Scaling a row by 2^p is exact in bf16; the normalized result changes only
+    through eps, by the closed-form factor sqrt(q + eps) / sqrt(q + eps / s^2)."""
+    M, K, N = 16, 64, 80
+    eps = 1e-3
+    inp = nf_inputs.make_inputs(M, K, N, seed=9)
+    X, W = inp["X"], inp["W"]
+    x = bf16_to_f64(X)
+    s = 2.0 ** np.arange(-4, 4).repeat(2)[:M]
+    Xs = bf16_round(x * s[:, None])
+    assert np.array_equal(bf16_to_f64(Xs), x * s[:, None])
+    Y0, r0 = o.gemm_prenorm_rms(X, W, eps)
+    Y1, r1 = o.gemm_prenorm_rms(Xs, W, eps)
+    ms = (x * x).mean(-1)
+    f = np.sqrt(ms + eps) / np.sqrt(ms + eps / s ** 2)
+    assert np.allclose(Y1, Y0 * f[:, None], rtol=1e-12, atol=1e-14), "pre-RMS scale law"
+    L0, _, _ = o.gemm_postnorm_ln(X, W, eps)
+    L1, _, _ = o.gemm_postnorm_ln(Xs, W, eps)
+    z = o.gemm_plain(X, W)
+    var = z.var(-1)
+    f = np.sqrt(var + eps) / np.sqrt(var + eps / s ** 2)
+    assert np.allclose(L1, L0 * f[:, None], rtol=1e-11, atol=1e-13), "post-LN scale law"
+
+
+def pin_row_subset(o):
+    M, K, N = 40, 64, 72
+    inp = nf_inputs.make_inputs(M, K, N, seed=3, gamma=True, beta=True)
+    X, W, G, B = inp["X"], inp["W"], inp["gamma"], inp["beta"]
+    rows = np.array([39, 0, 17, 17, 5])
+    full = o.gemm_postnorm_ln(X, W, 1e-5, G, B)
+    part = o.gemm_postnorm_ln(X, W, 1e-5, G, B, rows=rows)
+    for f, p in zip(full, part):
+        assert np.array_equal(f[rows], p), "row subset must equal the full result's rows"
+    full = o.gemm_prenorm_rms(X, W, 1e-6)
+    part = o.gemm_prenorm_rms(X, W, 1e-6, rows=rows)
+    for f, p in zip(full, part):
+        assert np.array_equal(f[rows], p), "prenorm row subset"
+    full = o.gemm_plain(X, W)
+    assert np.array_equal(full[rows], o.gemm_plain(X, W, rows=rows)), "plain row subset"
+    full = o.gemm_postnorm_rms(X, W, 1e-5, G)
+    part = o.gemm_postnorm_rms(X, W, 1e-5, G, rows=rows)
+    for f, p in zip(full, part):
+        assert np.array_equal(f[rows], p), "post-rms row subset"
+    full = o.norm_rows(X, 0, 1e-5, G[:K].copy(), B[:K].copy())
+    part = o.norm_rows(X, 0, 1e-5, G[:K].copy(), B[:K].copy(), rows=rows)
+    for f, p in zip(full, part):
+        assert np.array_equal(f[rows], p), "norm_rows row subset"
+
+
+# ---------------------------------------------------------------- closed forms
+def _golden_cases():
+    with open(os.path.join(GOLDEN, "closed_forms.json")) as fh:
+        return json.load(fh)["cases"]
+
+
+def pin_closed_forms(o):
+    env = {"sqrt": math.sqrt}
+    for case in _golden_cases():
+        X = bf16_round(np.array(case["X"], dtype=np.float64))
+        assert np.array_equal(bf16_to_f64(X), np.array(case["X"], dtype=np.float64)), \
+            f"{case['name']}: fixture X must be exact in bf16"
+        eps = float(case["eps"])
+        want = np.array([[eval(e, env) for e in row] for row in case["Y"]])  # noqa: S307
+        op = case["op"]
+        if op == "norm_rows_ln":
+            got, _, _ = o.norm_rows(X, 0, eps)
+        elif op == "norm_rows_rms":
+            got, _, _ = o.norm_rows(X, 1, eps)
+        else:
+            W = bf16_round(np.array(case["W"], dtype=np.float64))
+            if op == "pre_rms":
+                got, _ = o.gemm_prenorm_rms(X, W, eps)
+            elif op == "post_ln":
+                got, _, _ = o.gemm_postnorm_ln(X, W, eps)
+            elif op == "post_rms":
+                got, _ = o.gemm_postnorm_rms(X, W, eps)
+            elif op == "plain":
+                got = o.gemm_plain(X, W)
+            else:
+                raise AssertionError(f"unknown op {op}")
+        assert np.allclose(got, want, rtol=1e-14, atol=1e-14), \
+            f"closed form {case['name']}: got {got.tolist()} want {want.tolist()}"
+
+
+PINS = [pin_bruteforce_plain, pin_bruteforce_prenorm, pin_bruteforce_postnorm,
+        pin_bruteforce_norm_rows, pin_torch_f64, pin_lazy_identity, pin_invariants,
+        pin_reductions, pin_power_of_two_scale, pin_row_subset, pin_closed_forms]
+
+
+def run_all(o):
+    """Run every pin; return a list of (name, passed, message)."""
+    out = []
+    for pin in PINS:
+        try:
+            pin(o)
+            out.append((pin.__name__, True, ""))
+        except Exception as e:  # a mutant may also raise or return garbage
+            out.append((pin.__name__, False, f"{type(e).__name__}: {e}"[:300]))
+    return out
+
+
+if __name__ == "__main__":
+    import oracle
+    res = run_all(oracle.Oracle(sys.argv[1]))
+    print(json.dumps(res))

@@ -1,0 +1,86 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins
+catch every one.  Each mutant is compiled from a patched copy of
+``oracle/nfo.c`` in a temporary directory (the committed oracle is never
+touched) and judged in a subprocess, so a mutant that crashes counts as caught.
+CPU only."""
+import concurrent.futures as cf
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+# (name, text in nfo.c, replacement).  Each text must occur exactly once.
+MUTANTS = [
+    ("prenorm_divides_by_K_minus_1", "ss / (double)K + eps", "ss / (double)(K - 1) + eps"),
+    ("prenorm_eps_outside_root", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / sqrt(ss / (double)K) + eps"),
+    ("prenorm_drops_normalization", "for (int64_t k = 0; k < K; ++k) x[k] *= rstd;", ""),
+    ("prenorm_rstd_squared", "for (int64_t k = 0; k < K; ++k) x[k] *= rstd;",
+     "for (int64_t k = 0; k < K; ++k) x[k] *= rstd * rstd;"),
+    ("matmul_transposed_W", "z[j] += xk * bf16_to_double(wk[j]);",
+     "z[j] += xk * bf16_to_double(W[j * N + k]);"),
+    ("matmul_skips_last_k", "for (int64_t k = 0; k < K; ++k) {\n        const double xk",
+     "for (int64_t k = 0; k < K - 1; ++k) {\n        const double xk"),
+    ("ln_unbiased_variance", "const double var = ss / (double)n;",
+     "const double var = ss / (double)(n - 1);"),
+    ("ln_mean_divisor", "const double mu = s / (double)n;", "const double mu = s / (double)(n + 1);"),
+    ("ln_no_mean_subtraction", "double t = (v[j] - mu) * rstd;", "double t = v[j] * rstd;"),
+    ("ln_beta_sign", "if (beta) t += bf16_to_double(beta[j]);", "if (beta) t -= bf16_to_double(beta[j]);"),
+    ("ln_gamma_added", "if (gamma) t *= bf16_to_double(gamma[j]);\n        if (beta)",
+     "if (gamma) t += bf16_to_double(gamma[j]);\n        if (beta)"),
+    ("ln_eps_outside_root", "const double rstd = 1.0 / sqrt(var + eps);",
+     "const double rstd = 1.0 / sqrt(var) + eps;"),
+    ("rms_sum_not_squares", "for (int64_t j = 0; j < n; ++j) ss += v[j] * v[j];",
+     "for (int64_t j = 0; j < n; ++j) ss += v[j] * (v[j] < 0 ? -v[j] : v[j]);"),
+    ("rms_eps_scaled", "const double rstd = 1.0 / sqrt(ss / (double)n + eps);",
+     "const double rstd = 1.0 / sqrt((ss + eps) / (double)n);"),
+    ("rms_gamma_dropped", "if (gamma) t *= bf16_to_double(gamma[j]);\n        y[j] = t;\n    }\n    if (rstd_out) *rstd_out = rstd;\n}\n\nint",
+     "y[j] = t;\n    }\n    if (rstd_out) *rstd_out = rstd;\n}\n\nint"),
+    ("bf16_decode_shift", "((uint32_t)b) << 16", "((uint32_t)b) << 15"),
+    ("plain_ignores_row_list", "load_row(X, row_index(rows, r), K, x);\n            row_times_w(x, W, N, K, Y + r * N);",
+     "load_row(X, r, K, x);\n            row_times_w(x, W, N, K, Y + r * N);"),
+    ("postln_wrong_rstd_slot", "rstd_out ? rstd_out + r : NULL);\n        }\n        free(x);\n        free(z);\n    }\n    return bad ? -1 : 0;\n}\n\nint nfo_gemm_postnorm_rms",
+     "rstd_out ? rstd_out : NULL);\n        }\n        free(x);\n        free(z);\n    }\n    return bad ? -1 : 0;\n}\n\nint nfo_gemm_postnorm_rms"),
+]
+
+
+def _judge(name, old, new, workdir):
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, f"mutant {name}: anchor text must occur exactly once"
+    d = os.path.join(workdir, name)
+    os.makedirs(d, exist_ok=True)
+    path = os.path.join(d, "nfo.c")
+    with open(path, "w") as fh:
+        fh.write(src.replace(old, new))
+    lib = os.path.join(d, "libnfo_mutant.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-I", os.path.dirname(oracle._SRC), path, "-o", lib,
+                    "-lm"], check=True, capture_output=True, text=True)
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    p = subprocess.run([sys.executable, os.path.join(HERE, "oracle_pins.py"), lib],
+                       capture_output=True, text=True, timeout=600, env=env)
+    if p.returncode != 0:
+        return name, True, f"crashed (rc={p.returncode})"
+    res = json.loads(p.stdout.strip().splitlines()[-1])
+    failed = [r[0] for r in res if not r[1]]
+    return name, bool(failed), ",".join(failed)
+
+
+@pytest.mark.slow
+def test_every_mutant_is_caught(tmp_path):
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        results = list(ex.map(lambda m: _judge(*m, str(tmp_path)), MUTANTS))
+    missed = [n for n, caught, _ in results if not caught]
+    assert not missed, f"pins missed mutants: {missed}; results: {results}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    """Control: the same harness passes on an unmodified copy."""
+    name, caught, detail = _judge("control", "((uint32_t)b) << 16", "((uint32_t)b) << 16",
+                                  str(tmp_path))
+    assert not caught, f"unmodified oracle failed pins: {detail}"
