@@ -1,0 +1,519 @@
+"""Benchmark of the fused norm-GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {nf,reference}]
+
+Workload: the ads-shaped post-LayerNorm GEMM, Y = LayerNorm(X @ W) over N with
+X 65536 x 128, W 128 x 128 (bf16, fp32 accumulation, eps 1e-5, no affine).
+One step = one call of the fused kernel (nf_gemm_postnorm_ln) on one batch.
+
+Prints ONE JSON line (rank 0):
+  value        fused TFLOP/s (2*M*N*K per step), inputs resident in HBM,
+               timed with CUDA events over exactly K steps.  Successive steps
+               rotate over buffer sets whose footprint exceeds 3x L2, so no
+               step reads its inputs from L2.  The K launches run from CUDA
+               graphs (one graph launch per 1000 steps).
+  roofline     the fused kernel against the HBM roofline (algorithmic bytes
+               X + W + Y per launch over its mean duration), peak from
+               MEASURED_PEAKS.json.
+  norm_hidden_pct  100 * (T_plain + T_norm - T_fused) / T_norm, against this
+               library's own unfused pair (nf_gemm_plain + nf_norm_rows).
+  e2e          the same metric through the Python API with host buffers: each
+               step copies X and W from pinned host memory, runs the fused call
+               and reads Y back.
+  cpu_baseline the fp64 oracle on the host cores (a bounded sample).
+  configs      per-workload figures for the other four workloads (not the
+               headline).
+--impl reference times the fp64 oracle itself as the reference arm.
+Under torchrun (N > 1) every rank runs its own independent batch of the same
+size (rows shard across GPUs, no collective on the data path; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import nf_inputs  # noqa: E402
+
+WORKLOAD = "post_ln_65536x128x128"
+GRAPH_CHUNK = 1000
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------- helpers
+def algorithmic_bytes(M, N, K, gamma=False, beta=False, stats=0):
+    """Each tensor moved once: X and W read, Y written (+ gamma/beta, + stats)."""
+    return 2 * M * K + 2 * K * N + 2 * M * N + 2 * N * (int(gamma) + int(beta)) + 4 * M * stats
+
+
+def norm_bytes(rows, cols, affine=0):
+    return 4 * rows * cols + 2 * cols * affine
+
+
+def shard_rows(total_rows: int, world: int, rank: int):
+    """Contiguous row range [lo, hi) of `rank` when rows split over `world` GPUs."""
+    base, extra = divmod(total_rows, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def max_over_ranks(x: float, dist) -> float:
+    """Max of a per-rank float over the process group (identity without one)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    from normalization_gemm_gb300 import _build
+    return _build._stamp(())[:16]
+
+
+def profiled_traffic(workload: str):
+    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary,
+    or None when the summary is missing or the kernel source changed since."""
+    path = os.path.join(ROOT, "profiles", f"nf_gemm_postnorm_ln_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_hash")):
+            k, v = line.strip().split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while a region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t_start = time.time()
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.t_stop = time.time()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, window: str):
+        rows = []
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for name, flag in zip(names, flags[1:5]):
+                if flag.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "window": window}
+
+
+# ---------------------------------------------------------------- device timing
+def _to_dev(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _l2_bytes(dev):
+    import torch
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20))
+
+
+def make_sets(tensors, set_bytes, dev, min_sets=2):
+    """Copies of the input/output tensors so that cycling through them touches
+    more than 3x L2 between two uses of the same set."""
+    n = max(min_sets, -(-3 * _l2_bytes(dev) // max(1, set_bytes)))
+    return [[t.clone() for t in tensors] for _ in range(n)], n
+
+
+def graph_of(fn, count, stream):
+    """Capture `count` calls fn(i) (i = 0..count-1) into one CUDA graph."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(count):
+            fn(i)
+    return g
+
+
+def time_steps(fn, steps, warmup, stream, dist=None, chunk=GRAPH_CHUNK, sampler=None):
+    """Run `warmup` untimed steps, then time exactly `steps` calls of fn(i) from
+    CUDA graphs with events on `stream`; returns seconds (max over ranks)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            fn(i)
+    torch.cuda.synchronize()
+    full = min(chunk, steps)
+    g_full = graph_of(fn, full, stream) if full > 0 else None
+    rem = steps - (steps // full) * full if full else 0
+    g_rem = graph_of(fn, rem, stream) if rem else None
+    torch.cuda.synchronize()
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps // full if full else 0):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.stop()
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    sec = t0.elapsed_time(t1) / 1e3
+    return max_over_ranks(sec, dist)
+
+
+# ---------------------------------------------------------------- workloads
+def run_op(nf, op, X, W, Y, G, B, eps, stream):
+    if op == "pre_rms":
+        nf.gemm_prenorm_rms(X, W, eps, out=Y, stream=stream)
+    elif op == "post_ln":
+        nf.gemm_postnorm_ln(X, W, eps, G, B, out=Y, stream=stream)
+    elif op == "post_rms":
+        nf.gemm_postnorm_rms(X, W, eps, G, out=Y, stream=stream)
+    else:
+        nf.gemm_plain(X, W, out=Y, stream=stream)
+
+
+def measure_workload(nf, w, op, dev, stream, steps, warmup, seed=0, dist=None, sampler=None):
+    """Fused, plain-GEMM and norm-kernel time per launch for one workload/op."""
+    import torch
+    inp = nf_inputs.workload_inputs(w, seed=seed)
+    X0, W0 = _to_dev(inp["X"], dev), _to_dev(inp["W"], dev)
+    G = _to_dev(inp["gamma"], dev) if w.gamma else None
+    B = _to_dev(inp["beta"], dev) if (w.beta and op == "post_ln") else None
+    Y0 = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    set_bytes = X0.numel() * 2 + Y0.numel() * 2
+    sets, nsets = make_sets([X0, Y0], set_bytes, dev)
+    fused = lambda i: run_op(nf, op, sets[i % nsets][0], W0, sets[i % nsets][1], G, B, w.eps, stream)  # noqa: E731
+    t_fused = time_steps(fused, steps, warmup, stream, dist, sampler=sampler)
+    out = {"t_fused": t_fused / steps, "sets": nsets, "set_bytes": set_bytes}
+    # unfused pair of the blog's §1 baseline
+    plain = lambda i: nf.gemm_plain(sets[i % nsets][0], W0, out=sets[i % nsets][1], stream=stream)  # noqa: E731
+    ksteps = max(1, min(steps, 2000))
+    out["t_plain"] = time_steps(plain, ksteps, min(warmup, 10), stream, dist) / ksteps
+    if op == "pre_rms":
+        rows, cols, src = w.M, w.K, 0   # norm on X (M x K) into a scratch copy
+        scratch = [torch.empty_like(s[0]) for s in sets]
+        norm = lambda i: nf.norm_rows(sets[i % nsets][0], nf.NORM_RMS, w.eps, out=scratch[i % nsets],  # noqa: E731
+                                      stream=stream)
+    else:
+        rows, cols = w.M, w.N
+        scratch = [torch.empty_like(s[1]) for s in sets]
+        kind = nf.NORM_LN if op == "post_ln" else nf.NORM_RMS
+        norm = lambda i: nf.norm_rows(sets[i % nsets][1], kind, w.eps, G, B, out=scratch[i % nsets],  # noqa: E731
+                                      stream=stream)
+    out["t_norm"] = time_steps(norm, ksteps, min(warmup, 10), stream, dist) / ksteps
+    out["norm_cols"] = cols
+    out["norm_rows"] = rows
+    del sets, scratch
+    torch.cuda.empty_cache()
+    return out
+
+
+def roofline_time(w, op, hbm_gbs, tflops):
+    nbytes = algorithmic_bytes(w.M, w.N, w.K, gamma=w.gamma and op != "pre_rms",
+                               beta=w.beta and op == "post_ln")
+    return max(w.flops / (tflops * 1e12), nbytes / (hbm_gbs * 1e9)), nbytes
+
+
+def e2e_measure(nf, w, dev, stream, steps):
+    """Public API with host buffers: H2D X and W (pinned), fused call, D2H Y."""
+    import torch
+    inp = nf_inputs.workload_inputs(w)
+    Xh = torch.from_numpy(inp["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    Wh = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    Yh = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty_like(Xh, device=dev)
+    Wd = torch.empty_like(Wh, device=dev)
+    Yd = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        with torch.cuda.stream(stream):
+            Xd.copy_(Xh, non_blocking=True)
+            Wd.copy_(Wh, non_blocking=True)
+            nf.gemm_postnorm_ln(Xd, Wd, w.eps, out=Yd, stream=stream)
+            Yh.copy_(Yd, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sec = t0.elapsed_time(t1) / 1e3
+    return sec, Xh.numel() * 2 + Wh.numel() * 2, Yh.numel() * 2
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(w, op, budget_s, rows_cap=None, seed=0):
+    """Time the fp64 oracle on whole-row samples of the workload for about
+    budget_s seconds; returns (flops_done, seconds, rows_per_pass, threads)."""
+    import oracle
+    orc = oracle.get()
+    inp = nf_inputs.workload_inputs(w, seed=seed)
+    rows_per_pass = w.M if rows_cap is None else max(1, min(w.M, rows_cap))
+    rows = np.arange(rows_per_pass, dtype=np.int64)
+
+    def once():
+        if op == "post_ln":
+            orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, inp.get("gamma"), inp.get("beta"), rows=rows)
+        elif op == "post_rms":
+            orc.gemm_postnorm_rms(inp["X"], inp["W"], w.eps, inp.get("gamma"), rows=rows)
+        else:
+            orc.gemm_prenorm_rms(inp["X"], inp["W"], w.eps, rows=rows)
+
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        once()
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    sec = time.perf_counter() - t0
+    return done * 2 * rows_per_pass * w.N * w.K, sec, rows_per_pass, orc.max_threads()
+
+
+def reference_arm(args):
+    """--impl reference: the fp64 CPU oracle, timed as the reference arm."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    w = nf_inputs.WORKLOADS[WORKLOAD]
+    orc = oracle.get()
+    inp = nf_inputs.workload_inputs(w)
+    # calibrate rows per second, then size each step so the run stays ~60 s
+    cal_rows = np.arange(min(w.M, 2048), dtype=np.int64)
+    t0 = time.perf_counter()
+    orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, rows=cal_rows)
+    per_row = (time.perf_counter() - t0) / len(cal_rows)
+    total = args.steps + args.warmup
+    rows_per_step = int(max(1, min(w.M, 60.0 / max(1, total) / max(per_row, 1e-9))))
+    rows = np.arange(rows_per_step, dtype=np.int64)
+    for _ in range(args.warmup):
+        orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, rows=rows)
+    sec = time.perf_counter() - t0
+    flops = args.steps * 2 * rows_per_step * w.N * w.K
+    value = flops / sec / 1e12
+    line = {
+        "impl": "reference", "metric": "fused norm-GEMM TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
+                   "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.max_threads(), "kind": "oracle",
+                         "sample": f"{rows_per_step} of {w.M} rows per step (whole rows, fp64 oracle)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- main
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["nf", "reference"], default="nf")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist_mod
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    import normalization_gemm_gb300 as nf
+    from normalization_gemm_gb300 import _build
+    _build.build()
+    nf.clear_device_status()
+    stream = torch.cuda.Stream(device=dev)
+    hbm_gbs, bf16_tf, bf16_sus, peak_src = measured_peaks()
+
+    w = nf_inputs.WORKLOADS[WORKLOAD]
+    sampler = ClockSampler(local_rank)
+    # each rank its own independent batch (seed = rank): weak scaling
+    m = measure_workload(nf, w, "post_ln", dev, stream, args.steps, args.warmup, seed=rank, dist=dist,
+                         sampler=sampler)
+    t_step = m["t_fused"]
+    value = world * w.flops / t_step / 1e12
+    clocks = sampler.summary("timed")
+    if clocks["samples"] < 3:
+        # too short to sample: replay the same graph for ~1.5 s and sample that
+        soak = ClockSampler(local_rank)
+        reps = max(args.steps, int(1.5 / max(t_step, 1e-7)))
+        inp = None  # noqa: F841
+        measure_soak = measure_workload(nf, w, "post_ln", dev, stream, reps, 3, seed=rank, sampler=soak)
+        del measure_soak
+        clocks = soak.summary("soak after the timed region (timed region shorter than the sampling period)")
+
+    nbytes = algorithmic_bytes(w.M, w.N, w.K)
+    achieved = nbytes / t_step / 1e9
+    t_roof, _ = roofline_time(w, "post_ln", hbm_gbs, bf16_tf)
+    hidden = 100.0 * (m["t_plain"] + m["t_norm"] - m["t_fused"]) / m["t_norm"]
+    status, detail = nf.device_status()
+
+    line = {
+        "metric": "fused norm-GEMM TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps, "affine": False,
+                   "per_gpu_rows": w.M, "parallelism": f"rows x{world}, no collective",
+                   "l2": f"rotating {m['sets']} input/output sets of {m['set_bytes'] / 2**20:.0f} MiB "
+                         f"(> 3x L2 between reuses)",
+                   "launch": f"CUDA graphs of {min(GRAPH_CHUNK, args.steps)} launches"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": profiled_traffic(WORKLOAD),
+                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": nbytes},
+        "roofline_frac_of_config_bound": t_roof / t_step,
+        "norm_hidden_pct": hidden,
+        "unfused": {"t_plain_us": m["t_plain"] * 1e6, "t_norm_us": m["t_norm"] * 1e6,
+                    "t_fused_us": t_step * 1e6},
+        "clocks": clocks,
+        "device_status": int(status),
+    }
+    if status != 0:
+        line["device_status_detail"] = detail
+
+    if rank == 0:
+        e2e_steps = max(1, min(args.e2e_steps, args.steps))
+        sec, hb, db = e2e_measure(nf, w, dev, stream, e2e_steps)
+        line["e2e"] = {"value": world * w.flops * e2e_steps / sec / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": e2e_steps}
+        if not args.no_configs:
+            table = []
+            for name in nf_inputs.WORKLOAD_ORDER:
+                cw = nf_inputs.WORKLOADS[name]
+                for op in cw.ops:
+                    steps = 200 if cw.flops > 5e10 else 1000
+                    r = measure_workload(nf, cw, op, dev, stream, steps, 10)
+                    tr, nb = roofline_time(cw, op, hbm_gbs, bf16_tf)
+                    table.append({
+                        "workload": name, "op": op, "t_fused_us": r["t_fused"] * 1e6,
+                        "tflops": cw.flops / r["t_fused"] / 1e12,
+                        "roofline_frac": tr / r["t_fused"],
+                        "bound": "tensor" if cw.flops / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
+                        "hbm_gbs": nb / r["t_fused"] / 1e9,
+                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
+                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
+                    })
+            line["configs"] = table
+        if not args.no_cpu and world == 1:
+            flops, sec, rpp, thr = oracle_sample(w, "post_ln", budget_s=10.0)
+            line["cpu_baseline"] = {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": thr,
+                                    "kind": "oracle",
+                                    "sample": f"full {w.M} x {w.K} x {w.N} workload, repeated for "
+                                              f"{sec:.1f} s (fp64, OpenMP over rows)"}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,185 @@
+/*
+ * nf.h -- C ABI of the normalization-fused bf16 GEMM library (libnf.so).
+ *
+ * The library computes Y = X * W (X: M x K, W: K x N, bf16 in, fp32
+ * accumulation, bf16 out) with a row-wise normalization fused into the GEMM,
+ * as described in "Towards Free Normalization: Fusing Normalization into GEMM
+ * and Attention Kernels" (PyTorch blog):
+ *   - §2 "Lazy Pre-Norm":  Y = RMSNorm(X) * W, no affine;
+ *   - §3 "Multi-CTA Norm": Y = LayerNorm(X * W) or RMSNorm(X * W), optional
+ *     gamma / beta, the row spread over a thread-block cluster;
+ * plus the unfused pair of the blog's §1 baseline (a plain GEMM and a
+ * standalone row-norm kernel).
+ *
+ * Common rules for every compute entry point:
+ *   Layout     All matrices are dense row-major bf16 (IEEE bfloat16 bit
+ *              patterns), rows contiguous: X[i*K + k], W[k*N + j], Y[i*N + j].
+ *              gamma / beta hold N bf16 values; mean / rstd outputs hold one
+ *              fp32 per row.
+ *   Memory     Every pointer is DEVICE memory of the current CUDA device,
+ *              owned by the caller.  The library allocates nothing per call
+ *              and keeps no reference after the call returns.  Y must not
+ *              overlap any input.
+ *   Alignment  X, W, Y (and in/out of nf_norm_rows) start on a 16-byte
+ *              boundary; gamma / beta on 2 bytes; fp32 outputs on 4 bytes.
+ *              K and N (cols for nf_norm_rows) are multiples of 8, so that
+ *              every row starts on a 16-byte boundary.  Violations return
+ *              NF_ERR_ALIGNMENT.
+ *   Shapes     M == 0 is a no-op returning NF_OK (X and Y may then be NULL,
+ *              as the base of an empty tensor can be).  N and K must be >= 1.
+ *              M, N, K < 2^31.  Any M, N, K meeting these rules is handled,
+ *              including ragged tails on every dimension.
+ *   Streams    Work is enqueued on `stream` (NULL = the legacy default
+ *              stream) and runs asynchronously; nothing synchronizes.  The
+ *              first call on a device sets up per-device state (kernel
+ *              attributes, the device status word); make it before any
+ *              stream capture.  Later calls are capture-safe.
+ *   Errors     A status code is returned; nothing is thrown across the ABI.
+ *              Arguments are validated before anything is enqueued.  Launch
+ *              failures return NF_ERR_CUDA (detail in nf_last_error()).
+ *              Faults detected on the device (a pipeline wait that ran past
+ *              its time limit) are recorded in the device status word, read
+ *              with nf_get_device_status().
+ *   Threads    Entry points are thread-safe.
+ */
+#ifndef NF_H
+#define NF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nf_status {
+    NF_OK = 0,
+    NF_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad kind or eps */
+    NF_ERR_ALIGNMENT = 2,         /* pointer or row pitch not aligned as required */
+    NF_ERR_UNSUPPORTED_SHAPE = 3, /* a size beyond what the kernels support */
+    NF_ERR_CUDA = 4,              /* a CUDA runtime / driver call failed */
+    NF_ERR_TIMEOUT = 5,           /* a device-side wait exceeded its time limit */
+    NF_ERR_NO_DEVICE = 6          /* no usable sm_103 device is current */
+} nf_status;
+
+/* Same type as cudaStream_t; declared here so that callers need no CUDA header. */
+typedef struct CUstream_st* nf_stream;
+
+#define NF_NORM_LN 0  /* LayerNorm: (x - mean) / sqrt(var + eps) * gamma + beta */
+#define NF_NORM_RMS 1 /* RMSNorm:   x / sqrt(mean(x^2) + eps) * gamma          */
+
+/* Post-norm N limit: one 256-column tile per CTA times a 16-CTA cluster. */
+#define NF_POSTNORM_MAX_N 4096
+
+/*
+ * nf_gemm_plain -- Y = X * W.
+ * The GEMM of the unfused baseline (blog §1: a GEMM kernel followed by a
+ * separate normalization kernel).  fp32 accumulation, Y rounded to bf16
+ * (round to nearest even).
+ */
+nf_status nf_gemm_plain(const void* X, const void* W, void* Y,
+                        int64_t M, int64_t N, int64_t K, nf_stream stream);
+
+/*
+ * nf_gemm_prenorm_rms -- Y = RMSNorm(X) * W, Lazy Pre-Norm (blog §2).
+ * rstd_i = 1 / sqrt(sum_k X[i,k]^2 / K + eps) is accumulated from the same
+ * shared-memory tiles of X the tensor cores consume, and applied to the fp32
+ * accumulator in the epilogue: Y[i,:] = rstd_i * (X[i,:] * W), which equals
+ * (rstd_i * X[i,:]) * W (the blog's §2 "Proof").  No gamma and no LayerNorm:
+ * the blog's §2 limitations exclude both.
+ * rstd_out: optional (may be NULL), M fp32 values.
+ * eps: finite and >= 0, else NF_ERR_INVALID_ARG.
+ */
+nf_status nf_gemm_prenorm_rms(const void* X, const void* W, void* Y,
+                              int64_t M, int64_t N, int64_t K, float eps,
+                              float* rstd_out, nf_stream stream);
+
+/*
+ * nf_gemm_postnorm_ln -- Y = LayerNorm(X * W) over each row of N, Multi-CTA
+ * post-norm (blog §3): each CTA of a cluster spanning the row reduces the
+ * partial statistics of its tile, the partials are exchanged through
+ * distributed shared memory, and every CTA normalizes before its single store.
+ * LayerNorm as torch.nn.LayerNorm: biased variance, eps inside the root.
+ * gamma, beta: optional (NULL = 1 and 0), N bf16 values each.
+ * mean_out, rstd_out: optional, M fp32 values (row mean, 1/sqrt(var + eps)).
+ * N <= NF_POSTNORM_MAX_N, else NF_ERR_UNSUPPORTED_SHAPE.
+ */
+nf_status nf_gemm_postnorm_ln(const void* X, const void* W, const void* gamma,
+                              const void* beta, void* Y, int64_t M, int64_t N,
+                              int64_t K, float eps, float* mean_out,
+                              float* rstd_out, nf_stream stream);
+
+/*
+ * nf_gemm_postnorm_rms -- Y = RMSNorm(X * W) * gamma over each row of N
+ * (blog §3 with RMSNorm).  gamma optional (NULL = 1); rstd_out optional.
+ * N <= NF_POSTNORM_MAX_N, else NF_ERR_UNSUPPORTED_SHAPE.
+ */
+nf_status nf_gemm_postnorm_rms(const void* X, const void* W, const void* gamma,
+                               void* Y, int64_t M, int64_t N, int64_t K,
+                               float eps, float* rstd_out, nf_stream stream);
+
+/*
+ * nf_norm_rows -- standalone LayerNorm / RMSNorm of each row of `in`
+ * (rows x cols) into `out`: the normalization kernel of the unfused baseline
+ * (blog §1).  kind is NF_NORM_LN or NF_NORM_RMS; beta is ignored for RMSNorm;
+ * mean_out is not written for RMSNorm.  cols <= 16384, else
+ * NF_ERR_UNSUPPORTED_SHAPE.  `in` and `out` must not overlap.
+ */
+nf_status nf_norm_rows(const void* in, void* out, const void* gamma,
+                       const void* beta, int64_t rows, int64_t cols, int kind,
+                       float eps, float* mean_out, float* rstd_out,
+                       nf_stream stream);
+
+/* ---------------------------------------------------------------------
+ * Diagnostics and configuration (no counterpart in the blog).
+ * ------------------------------------------------------------------- */
+
+/* Synchronizes the current device, then returns the status recorded by the
+ * kernels since the last clear: NF_OK, or NF_ERR_TIMEOUT when a pipeline wait
+ * gave up.  `detail` (may be NULL) receives 4 words: code, wait site, block
+ * index, tile index of the first failure. */
+nf_status nf_get_device_status(uint32_t* detail);
+
+/* Synchronizes the current device and resets its status word to NF_OK. */
+nf_status nf_clear_device_status(void);
+
+/* Time limit for every device-side pipeline wait, in nanoseconds (default
+ * 2e9).  After it a kernel records NF_ERR_TIMEOUT, stops its work, releases
+ * its tensor memory and returns; the CUDA context stays usable. */
+nf_status nf_set_wait_timeout_ns(uint64_t ns);
+
+/* Self-test of the time limit: launches one CTA that waits on a barrier no
+ * thread ever arrives on, with limit `timeout_ns` (1e3..1e10).  After the
+ * stream completes, nf_get_device_status() reports NF_ERR_TIMEOUT. */
+nf_status nf_selftest_wait_timeout(uint64_t timeout_ns, nf_stream stream);
+
+/* English text for a status code (static storage). */
+const char* nf_status_string(nf_status status);
+
+/* Detail of the last failing call on this thread ("" if none). */
+const char* nf_last_error(void);
+
+/* Launch plan the library would use; pure host function, no GPU needed.
+ * op: 0 plain, 1 pre-norm RMS, 2 post-norm LN, 3 post-norm RMS.
+ * sm_count: SMs of the device; the grid assumes every SM can hold one CTA
+ * (for clusters, the library asks the driver for the real co-residency). */
+typedef struct nf_plan {
+    int32_t tile_m, tile_n, tile_k; /* CTA tile                            */
+    int32_t stages;                 /* shared-memory ring depth            */
+    int32_t cluster;                /* CTAs per cluster along N            */
+    int32_t grid;                   /* persistent CTAs                      */
+    int32_t threads;                /* threads per CTA                     */
+    int32_t smem_bytes;             /* dynamic shared memory per CTA       */
+    int32_t tmem_cols;              /* tensor-memory columns per CTA       */
+    int32_t tiles;                  /* output tiles (M/tile_m x N/tile_n)  */
+} nf_plan;
+nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count,
+                       nf_plan* out);
+
+/* ABI version of this header (bumped on any incompatible change). */
+#define NF_ABI_VERSION 1
+int nf_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NF_H */

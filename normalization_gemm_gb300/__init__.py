@@ -1,0 +1,250 @@
+"""Python binding of libnf.so, the normalization-fused bf16 GEMM for GB300.
+
+Argument marshalling only: every step of every operation runs in the CUDA
+kernels behind the C ABI of ``include/nf.h``.  Tensors are PyTorch CUDA
+tensors (device memory and streams); nothing here computes on them.  There is
+no fallback: if the library is missing or the device is not sm_103 the calls
+raise.
+
+Operations (blog "Towards Free Normalization: Fusing Normalization into GEMM
+and Attention Kernels"):
+  gemm_plain          Y = X @ W                                  (§1 baseline)
+  gemm_prenorm_rms    Y = RMSNorm(X) @ W, Lazy Pre-Norm          (§2)
+  gemm_postnorm_ln    Y = LayerNorm(X @ W) * gamma + beta        (§3)
+  gemm_postnorm_rms   Y = RMSNorm(X @ W) * gamma                 (§3)
+  norm_rows           standalone LayerNorm / RMSNorm of rows     (§1 baseline)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+LIB_PATH = os.path.join(PKG, "libnf.so")
+HEADER = os.path.join(ROOT, "include", "nf.h")
+
+NF_OK = 0
+NORM_LN = 0
+NORM_RMS = 1
+POSTNORM_MAX_N = 4096
+
+STATUS_NAMES = {0: "NF_OK", 1: "NF_ERR_INVALID_ARG", 2: "NF_ERR_ALIGNMENT",
+                3: "NF_ERR_UNSUPPORTED_SHAPE", 4: "NF_ERR_CUDA", 5: "NF_ERR_TIMEOUT",
+                6: "NF_ERR_NO_DEVICE"}
+
+
+class NFError(RuntimeError):
+    """A non-zero nf_status from the library."""
+
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}"
+                         + (f" ({detail})" if detail else ""))
+
+
+class NFPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "tile_m", "tile_n", "tile_k", "stages", "cluster", "grid", "threads", "smem_bytes",
+        "tmem_cols", "tiles")]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SIGS = {
+    "nf_gemm_plain": [_VP, _VP, _VP, _I64, _I64, _I64, _VP],
+    "nf_gemm_prenorm_rms": [_VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
+    "nf_gemm_postnorm_ln": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
+    "nf_gemm_postnorm_rms": [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
+    "nf_norm_rows": [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
+    "nf_get_device_status": [_VP],
+    "nf_clear_device_status": [],
+    "nf_set_wait_timeout_ns": [ctypes.c_uint64],
+    "nf_selftest_wait_timeout": [ctypes.c_uint64, _VP],
+    "nf_plan_gemm": [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(NFPlan)],
+    "nf_abi_version": [],
+}
+
+
+def header_symbols() -> list:
+    """Names of the functions include/nf.h declares."""
+    with open(HEADER) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nf_[a-z_0-9]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, argtypes in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = argtypes
+            f.restype = ctypes.c_int
+        L.nf_status_string.argtypes = [ctypes.c_int]
+        L.nf_status_string.restype = ctypes.c_char_p
+        L.nf_last_error.argtypes = []
+        L.nf_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != NF_OK:
+        raise NFError(status, where, lib().nf_last_error().decode(errors="replace"))
+
+
+# ------------------------------------------------------------- tensor helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _mat(t, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+    return t.data_ptr()
+
+
+def _vec(t, name, n, dtype):
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dtype:
+        raise TypeError(f"{name} must be a CUDA {dtype} tensor")
+    if t.dim() != 1 or t.numel() != n or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous vector of {n}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _out(out, M, N, like):
+    torch = _torch()
+    if out is None:
+        return torch.empty((M, N), dtype=torch.bfloat16, device=like.device)
+    if tuple(out.shape) != (M, N):
+        raise ValueError(f"out must have shape {(M, N)}")
+    return out
+
+
+def _shapes(x, w):
+    M, K = x.shape
+    K2, N = w.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: X is {tuple(x.shape)}, W is {tuple(w.shape)}")
+    return M, N, K
+
+
+# ------------------------------------------------------------- operations
+def gemm_plain(x, w, out=None, stream=None):
+    """Y = X @ W (bf16 in and out, fp32 accumulation)."""
+    M, N, K = _shapes(x, w)
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_plain(_mat(x, "x"), _mat(w, "w"), _mat(y, "out"), M, N, K,
+                               _stream(stream)), "nf_gemm_plain")
+    return y
+
+
+def gemm_prenorm_rms(x, w, eps, out=None, rstd_out=None, stream=None):
+    """Y = RMSNorm(X) @ W, no affine (Lazy Pre-Norm).  rstd_out: optional fp32 [M]."""
+    torch = _torch()
+    M, N, K = _shapes(x, w)
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_prenorm_rms(_mat(x, "x"), _mat(w, "w"), _mat(y, "out"), M, N, K,
+                                     float(eps), _vec(rstd_out, "rstd_out", M, torch.float32),
+                                     _stream(stream)), "nf_gemm_prenorm_rms")
+    return y
+
+
+def gemm_postnorm_ln(x, w, eps, gamma=None, beta=None, out=None, mean_out=None, rstd_out=None,
+                     stream=None):
+    """Y = LayerNorm(X @ W) over N, optional gamma / beta (bf16 [N])."""
+    torch = _torch()
+    M, N, K = _shapes(x, w)
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_postnorm_ln(_mat(x, "x"), _mat(w, "w"),
+                                     _vec(gamma, "gamma", N, torch.bfloat16),
+                                     _vec(beta, "beta", N, torch.bfloat16), _mat(y, "out"),
+                                     M, N, K, float(eps),
+                                     _vec(mean_out, "mean_out", M, torch.float32),
+                                     _vec(rstd_out, "rstd_out", M, torch.float32),
+                                     _stream(stream)), "nf_gemm_postnorm_ln")
+    return y
+
+
+def gemm_postnorm_rms(x, w, eps, gamma=None, out=None, rstd_out=None, stream=None):
+    """Y = RMSNorm(X @ W) * gamma over N."""
+    torch = _torch()
+    M, N, K = _shapes(x, w)
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_postnorm_rms(_mat(x, "x"), _mat(w, "w"),
+                                      _vec(gamma, "gamma", N, torch.bfloat16), _mat(y, "out"),
+                                      M, N, K, float(eps),
+                                      _vec(rstd_out, "rstd_out", M, torch.float32),
+                                      _stream(stream)), "nf_gemm_postnorm_rms")
+    return y
+
+
+def norm_rows(x, kind, eps, gamma=None, beta=None, out=None, mean_out=None, rstd_out=None,
+              stream=None):
+    """LayerNorm (kind 0) or RMSNorm (kind 1) of each row of x (the unfused norm kernel)."""
+    torch = _torch()
+    R = x.shape[0] if x.dim() == 2 else -1
+    C = x.shape[1] if x.dim() == 2 else -1
+    y = _out(out, R, C, x)
+    _check(lib().nf_norm_rows(_mat(x, "x"), _mat(y, "out"), _vec(gamma, "gamma", C, torch.bfloat16),
+                              _vec(beta, "beta", C, torch.bfloat16), R, C, int(kind), float(eps),
+                              _vec(mean_out, "mean_out", R, torch.float32),
+                              _vec(rstd_out, "rstd_out", R, torch.float32), _stream(stream)),
+           "nf_norm_rows")
+    return y
+
+
+# ------------------------------------------------------------- diagnostics
+def device_status():
+    """(status, [code, site, block, tile]) after synchronizing the device."""
+    buf = (ctypes.c_uint32 * 4)()
+    s = lib().nf_get_device_status(ctypes.cast(buf, ctypes.c_void_p))
+    return s, list(buf)
+
+
+def clear_device_status() -> None:
+    _check(lib().nf_clear_device_status(), "nf_clear_device_status")
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().nf_set_wait_timeout_ns(int(ns)), "nf_set_wait_timeout_ns")
+
+
+def selftest_wait_timeout(ns: int, stream=None) -> None:
+    _check(lib().nf_selftest_wait_timeout(int(ns), _stream(stream)), "nf_selftest_wait_timeout")
+
+
+def plan_gemm(op: int, M: int, N: int, K: int, sm_count: int) -> dict:
+    """Launch plan for op 0 plain / 1 pre-RMS / 2 post-LN / 3 post-RMS (host only)."""
+    p = NFPlan()
+    _check(lib().nf_plan_gemm(op, M, N, K, sm_count, ctypes.byref(p)), "nf_plan_gemm")
+    return {f: getattr(p, f) for f, _ in NFPlan._fields_}

@@ -1,0 +1,488 @@
+// nf_api.cu -- the C ABI declared in include/nf.h: argument validation, tensor
+// maps, launch plans, launches, and the device status word.
+//
+// Blog: "Towards Free Normalization: Fusing Normalization into GEMM and
+// Attention Kernels" -- §1 (unfused GEMM + norm baseline), §2 (Lazy Pre-Norm),
+// §3 (Multi-CTA post-norm over a thread-block cluster).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "nf.h"
+#include "nf_internal.h"
+#include "nf_ptx.cuh"
+
+namespace nf {
+namespace {
+
+// ---------------------------------------------------------------- errors
+thread_local std::string g_last_error;
+
+nf_status fail(nf_status s, const char* what) {
+    g_last_error = what;
+    return s;
+}
+
+nf_status fail_cuda(cudaError_t e, const char* what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return NF_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- device status
+// Four words per the WaitGuard layout: code, wait site, block, tile.
+__device__ uint32_t g_status_word[4];
+
+__global__ void nf_selftest_wait_kernel(uint32_t* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on `bar`: the wait must give up after timeout_ns.
+        const WaitGuard g{status, &abort_flag, timeout_ns};
+        (void)mbar_wait(g, b, 0, SITE_SELFTEST, 0);
+    }
+    __syncthreads();
+}
+
+uint64_t g_timeout_ns = 2000000000ull;
+std::mutex g_mu;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    uint32_t* status = nullptr;
+    // max co-resident clusters, per variant function and cluster size
+    const void* occ_func[16] = {};
+    int occ_cluster[16] = {};
+    int occ_value[16] = {};
+    int occ_n = 0;
+    // kernels whose attributes were set on this device
+    const void* attr_done[32] = {};
+    int attr_n = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+nf_status device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(NF_ERR_NO_DEVICE, "device index out of range");
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!d.ready) {
+            int major = 0, minor = 0, sms = 0;
+            if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+                return fail_cuda(e, "cudaDeviceGetAttribute");
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (major != 10 || minor != 3)
+                return fail(NF_ERR_NO_DEVICE, "the kernels are built for sm_103a only");
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess)
+                return fail_cuda(e, "cudaGetSymbolAddress(status)");
+            d.status = static_cast<uint32_t*>(p);
+            d.sm_count = sms;
+            d.ready = true;
+        }
+    }
+    *out = &d;
+    return NF_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix of `rows` x `cols` (row pitch cols * 2 bytes), read or
+// written in boxes of box_rows x box_cols with 128-byte swizzle; out-of-bounds
+// elements read as zero and are dropped on store.
+nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(NF_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2u};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[128];
+        snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+        return fail(NF_ERR_CUDA, msg);
+    }
+    return NF_OK;
+}
+
+// ---------------------------------------------------------------- plans
+enum Op { OP_PLAIN = 0, OP_PRE = 1, OP_POST_LN = 2, OP_POST_RMS = 3 };
+
+struct Plan {
+    int tile_n = 0;
+    bool clustered = false;
+    int cluster = 1;
+    int m_tiles = 0, n_tiles = 0, k_tiles = 0;
+    const GemmVariant* v = nullptr;
+};
+
+const GemmVariant* find_variant(int op, int tile_n, bool clustered) {
+    int n = 0;
+    const GemmVariant* t = nullptr;
+    switch (op) {
+        case OP_PLAIN: t = gemm_variants_plain(&n); break;
+        case OP_PRE: t = gemm_variants_pre(&n); break;
+        case OP_POST_LN: t = gemm_variants_post_ln(&n); break;
+        case OP_POST_RMS: t = gemm_variants_post_rms(&n); break;
+        default: return nullptr;
+    }
+    for (int i = 0; i < n; ++i)
+        if (t[i].tile_n == tile_n && t[i].clustered == clustered) return &t[i];
+    return nullptr;
+}
+
+// Tile choice.  Plain and pre-norm: the smallest of 64 / 128 / 256 columns
+// that covers N, else 256.  Post-norm (blog §3): one CTA covers the row while
+// N <= 256; beyond that a cluster of ceil(N / 256) CTAs of 256 columns each
+// spans the row (N <= 4096: 16 CTAs).
+nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, Plan* p) {
+    const bool post = op == OP_POST_LN || op == OP_POST_RMS;
+    p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+    p->clustered = post && N > 256;
+    p->cluster = p->clustered ? static_cast<int>((N + 255) / 256) : 1;
+    p->m_tiles = static_cast<int>((M + TILE_M - 1) / TILE_M);
+    p->n_tiles = post ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
+    p->k_tiles = static_cast<int>((K + TILE_K - 1) / TILE_K);
+    p->v = find_variant(op, p->tile_n, p->clustered);
+    if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
+    return NF_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+nf_status check_gemm_args(int op, const void* X, const void* W, const void* Y, const void* gamma, const void* beta,
+                          const float* mean_out, const float* rstd_out, int64_t M, int64_t N, int64_t K, float eps) {
+    if (M < 0 || N < 1 || K < 1) return fail(NF_ERR_INVALID_ARG, "need M >= 0, N >= 1, K >= 1");
+    // An empty X / Y (M == 0) may have a null base: nothing is ever accessed.
+    if (M == 0) {
+        X = X ? X : reinterpret_cast<const void*>(256);
+        Y = Y ? Y : reinterpret_cast<const void*>(256);
+    }
+    if (!X || !W || !Y) return fail(NF_ERR_INVALID_ARG, "X, W and Y must be non-null");
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return fail(NF_ERR_UNSUPPORTED_SHAPE, "M, N and K must be below 2^31");
+    if (op != OP_PLAIN && !(std::isfinite(eps) && eps >= 0.0f))
+        return fail(NF_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (!aligned(X, 16) || !aligned(W, 16) || !aligned(Y, 16))
+        return fail(NF_ERR_ALIGNMENT, "X, W and Y must be 16-byte aligned");
+    if (K % 8 != 0 || N % 8 != 0)
+        return fail(NF_ERR_ALIGNMENT, "K and N must be multiples of 8 (16-byte row pitch)");
+    if ((gamma && !aligned(gamma, 2)) || (beta && !aligned(beta, 2)))
+        return fail(NF_ERR_ALIGNMENT, "gamma and beta must be 2-byte aligned");
+    if ((mean_out && !aligned(mean_out, 4)) || (rstd_out && !aligned(rstd_out, 4)))
+        return fail(NF_ERR_ALIGNMENT, "mean_out and rstd_out must be 4-byte aligned");
+    if ((op == OP_POST_LN || op == OP_POST_RMS) && N > NF_POSTNORM_MAX_N)
+        return fail(NF_ERR_UNSUPPORTED_SHAPE, "post-norm needs N <= 4096 (256 columns x 16-CTA cluster)");
+    // Tile coordinates are int32: M rows plus one tile of slack.
+    if (M > static_cast<int64_t>(INT32_MAX) - TILE_M) return fail(NF_ERR_UNSUPPORTED_SHAPE, "M too large");
+    return NF_OK;
+}
+
+// Sets per-kernel attributes once per device.
+nf_status prepare_kernel(DeviceState* d, const GemmVariant* v) {
+    for (int i = 0; i < d->attr_n; ++i)
+        if (d->attr_done[i] == v->func) return NF_OK;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < d->attr_n; ++i)
+        if (d->attr_done[i] == v->func) return NF_OK;
+    cudaError_t e = cudaFuncSetAttribute(v->func, cudaFuncAttributeMaxDynamicSharedMemorySize, v->smem_bytes);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(max dynamic smem)");
+    if (v->clustered) {
+        e = cudaFuncSetAttribute(v->func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(non-portable cluster)");
+    }
+    if (d->attr_n < 32) d->attr_done[d->attr_n++] = v->func;
+    return NF_OK;
+}
+
+nf_status max_clusters(DeviceState* d, const GemmVariant* v, int cluster, int* out) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int i = 0; i < d->occ_n; ++i)
+            if (d->occ_func[i] == v->func && d->occ_cluster[i] == cluster) {
+                *out = d->occ_value[i];
+                return NF_OK;
+            }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster * 64));
+    cfg.blockDim = dim3(static_cast<unsigned>(v->threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(v->smem_bytes);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, v->func, &cfg);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveClusters");
+    if (n < 1) return fail(NF_ERR_UNSUPPORTED_SHAPE, "this cluster size cannot be co-resident on the device");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d->occ_n < 16) {
+        d->occ_func[d->occ_n] = v->func;
+        d->occ_cluster[d->occ_n] = cluster;
+        d->occ_value[d->occ_n] = n;
+        ++d->occ_n;
+    }
+    *out = n;
+    return NF_OK;
+}
+
+nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
+                   int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream) {
+    nf_status st = check_gemm_args(op, X, W, Y, gamma, beta, mean_out, rstd_out, M, N, K, eps);
+    if (st != NF_OK) return st;
+    if (M == 0) return NF_OK;
+    DeviceState* d = nullptr;
+    if ((st = device_state(&d)) != NF_OK) return st;
+    Plan p;
+    if ((st = plan_tiles(op, M, N, K, &p)) != NF_OK) return st;
+    if ((st = prepare_kernel(d, p.v)) != NF_OK) return st;
+
+    CUtensorMap tmX, tmW, tmY;
+    if ((st = make_map(&tmX, X, M, K, TILE_K, TILE_M)) != NF_OK) return st;
+    if ((st = make_map(&tmW, W, K, N, B_BOX_N, TILE_K)) != NF_OK) return st;
+    if ((st = make_map(&tmY, Y, M, N, STORE_COLS, STORE_ROWS)) != NF_OK) return st;
+
+    GemmArgs a;
+    a.M = static_cast<int32_t>(M);
+    a.N = static_cast<int32_t>(N);
+    a.K = static_cast<int32_t>(K);
+    a.m_tiles = p.m_tiles;
+    a.n_tiles = p.n_tiles;
+    a.k_tiles = p.k_tiles;
+    a.cluster = p.cluster;
+    a.eps = eps;
+    a.inv_len = op == OP_PRE ? 1.0f / static_cast<float>(K) : 1.0f / static_cast<float>(N);
+    a.gamma = static_cast<const uint16_t*>(gamma);
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.mean_out = mean_out;
+    a.rstd_out = rstd_out;
+    a.status = d->status;
+    a.timeout_ns = g_timeout_ns;
+
+    int grid = 0;
+    if (p.clustered) {
+        int mc = 0;
+        if ((st = max_clusters(d, p.v, p.cluster, &mc)) != NF_OK) return st;
+        grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;
+    } else {
+        const int tiles = p.m_tiles * p.n_tiles;
+        grid = tiles < d->sm_count ? tiles : d->sm_count;
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(p.v->threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.v->smem_bytes);
+    cfg.stream = stream;
+    if (p.clustered) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void* kargs[4] = {&tmX, &tmW, &tmY, &a};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
+    if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    return NF_OK;
+}
+
+}  // namespace
+}  // namespace nf
+
+using namespace nf;
+
+extern "C" {
+
+nf_status nf_gemm_plain(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K, nf_stream stream) {
+    return run_gemm(OP_PLAIN, X, W, nullptr, nullptr, Y, M, N, K, 0.0f, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_gemm_prenorm_rms(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K, float eps,
+                              float* rstd_out, nf_stream stream) {
+    return run_gemm(OP_PRE, X, W, nullptr, nullptr, Y, M, N, K, eps, nullptr, rstd_out,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_gemm_postnorm_ln(const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
+                              int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, nf_stream stream) {
+    return run_gemm(OP_POST_LN, X, W, gamma, beta, Y, M, N, K, eps, mean_out, rstd_out,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_gemm_postnorm_rms(const void* X, const void* W, const void* gamma, void* Y, int64_t M, int64_t N,
+                               int64_t K, float eps, float* rstd_out, nf_stream stream) {
+    return run_gemm(OP_POST_RMS, X, W, gamma, nullptr, Y, M, N, K, eps, nullptr, rstd_out,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_norm_rows(const void* in, void* out, const void* gamma, const void* beta, int64_t rows, int64_t cols,
+                       int kind, float eps, float* mean_out, float* rstd_out, nf_stream stream) {
+    if (kind != NF_NORM_LN && kind != NF_NORM_RMS) return fail(NF_ERR_INVALID_ARG, "kind must be LN or RMS");
+    if (rows < 0 || cols < 1) return fail(NF_ERR_INVALID_ARG, "need rows >= 0 and cols >= 1");
+    if (rows == 0) {  // empty tensors may have a null base: nothing is accessed
+        in = in ? in : reinterpret_cast<const void*>(256);
+        out = out ? out : reinterpret_cast<void*>(256);
+    }
+    if (!in || !out) return fail(NF_ERR_INVALID_ARG, "in and out must be non-null");
+    if (!(std::isfinite(eps) && eps >= 0.0f)) return fail(NF_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (cols > NORM_MAX_COLS) return fail(NF_ERR_UNSUPPORTED_SHAPE, "cols must be <= 16384");
+    if (cols % 8 != 0) return fail(NF_ERR_ALIGNMENT, "cols must be a multiple of 8 (16-byte rows)");
+    if (!aligned(in, 16) || !aligned(out, 16)) return fail(NF_ERR_ALIGNMENT, "in and out must be 16-byte aligned");
+    // gamma / beta are read as 16-byte vectors as well
+    if ((gamma && !aligned(gamma, 16)) || (beta && !aligned(beta, 16)))
+        return fail(NF_ERR_ALIGNMENT, "gamma and beta must be 16-byte aligned for nf_norm_rows");
+    if ((mean_out && !aligned(mean_out, 4)) || (rstd_out && !aligned(rstd_out, 4)))
+        return fail(NF_ERR_ALIGNMENT, "mean_out and rstd_out must be 4-byte aligned");
+    if (rows == 0) return NF_OK;
+    DeviceState* d = nullptr;
+    nf_status st = device_state(&d);
+    if (st != NF_OK) return st;
+    NormArgs a;
+    a.in = in;
+    a.out = out;
+    a.gamma = static_cast<const uint16_t*>(gamma);
+    a.beta = static_cast<const uint16_t*>(beta);
+    a.rows = rows;
+    a.cols = static_cast<int32_t>(cols);
+    a.eps = eps;
+    a.inv_cols = 1.0f / static_cast<float>(cols);
+    a.mean_out = mean_out;
+    a.rstd_out = rstd_out;
+    cudaError_t e = launch_norm_rows(a, kind, d->sm_count, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "norm_rows launch");
+    return NF_OK;
+}
+
+nf_status nf_get_device_status(uint32_t* detail) {
+    DeviceState* d = nullptr;
+    nf_status st = device_state(&d);
+    if (st != NF_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    uint32_t w[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(w, d->status, sizeof w, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e, "read status word");
+    if (detail) memcpy(detail, w, sizeof w);
+    return static_cast<nf_status>(w[0]);
+}
+
+nf_status nf_clear_device_status(void) {
+    DeviceState* d = nullptr;
+    nf_status st = device_state(&d);
+    if (st != NF_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    const uint32_t z[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(d->status, z, sizeof z, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e, "clear status word");
+    return NF_OK;
+}
+
+nf_status nf_set_wait_timeout_ns(uint64_t ns) {
+    if (ns < 1000ull || ns > 100000000000ull) return fail(NF_ERR_INVALID_ARG, "timeout must be in [1e3, 1e11] ns");
+    g_timeout_ns = ns;
+    return NF_OK;
+}
+
+nf_status nf_selftest_wait_timeout(uint64_t timeout_ns, nf_stream stream) {
+    if (timeout_ns < 1000ull || timeout_ns > 10000000000ull)
+        return fail(NF_ERR_INVALID_ARG, "timeout must be in [1e3, 1e10] ns");
+    DeviceState* d = nullptr;
+    nf_status st = device_state(&d);
+    if (st != NF_OK) return st;
+    nf_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(d->status, timeout_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "self-test launch");
+    return NF_OK;
+}
+
+const char* nf_status_string(nf_status s) {
+    switch (s) {
+        case NF_OK: return "ok";
+        case NF_ERR_INVALID_ARG: return "invalid argument";
+        case NF_ERR_ALIGNMENT: return "misaligned pointer or row pitch";
+        case NF_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case NF_ERR_CUDA: return "CUDA error";
+        case NF_ERR_TIMEOUT: return "device wait timed out";
+        case NF_ERR_NO_DEVICE: return "no usable sm_103 device";
+    }
+    return "unknown status";
+}
+
+const char* nf_last_error(void) { return g_last_error.c_str(); }
+
+nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf_plan* out) {
+    if (!out || op < 0 || op > 3 || sm_count < 1) return fail(NF_ERR_INVALID_ARG, "bad plan query");
+    nf_status st = check_gemm_args(op, reinterpret_cast<const void*>(256), reinterpret_cast<const void*>(256),
+                                   reinterpret_cast<const void*>(256), nullptr, nullptr, nullptr, nullptr, M, N, K,
+                                   1e-5f);
+    if (st != NF_OK) return st;
+    Plan p;
+    if ((st = plan_tiles(op, M > 0 ? M : 1, N, K, &p)) != NF_OK) return st;
+    out->tile_m = TILE_M;
+    out->tile_n = p.tile_n;
+    out->tile_k = TILE_K;
+    out->stages = p.v->stages;
+    out->cluster = p.cluster;
+    out->threads = p.v->threads;
+    out->smem_bytes = p.v->smem_bytes;
+    out->tmem_cols = p.v->tmem_cols;
+    out->tiles = M > 0 ? p.m_tiles * p.n_tiles : 0;
+    if (p.clustered) {
+        const int mc = sm_count / p.cluster;
+        out->grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;
+    } else {
+        out->grid = out->tiles < sm_count ? out->tiles : sm_count;
+    }
+    return NF_OK;
+}
+
+int nf_abi_version(void) { return NF_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,526 @@
+// nf_gemm_kernel.cuh -- persistent, warp-specialized bf16 GEMM for sm_103a with
+// the row normalization fused in.  One template covers the four epilogues:
+//
+//   EPI_PLAIN     Y = X W                         (blog §1 baseline GEMM)
+//   EPI_PRE_RMS   Y = rstd(X) * (X W)              (blog §2 Lazy Pre-Norm)
+//   EPI_POST_LN   Y = LayerNorm(X W) * g + b       (blog §3 Multi-CTA Norm)
+//   EPI_POST_RMS  Y = RMSNorm(X W) * g             (blog §3 with RMSNorm)
+//
+// Blog: "Towards Free Normalization: Fusing Normalization into GEMM and
+// Attention Kernels".
+//
+// CTA roles (one CTA per SM, persistent over output tiles):
+//   warps 0-3  epilogue: warp w reads TMEM lanes 32w..32w+31, i.e. tile rows
+//              32w..32w+31, one row per thread; normalizes; stores through a
+//              128B-swizzled staging buffer with TMA, once per element.
+//   warp 4     TMA producer (one elected lane): X and W K-tiles into a ring of
+//              STAGES shared-memory stages.
+//   warp 5     MMA issuer (one elected lane): tcgen05.mma 128 x TILE_N x 16
+//              into one of two TMEM accumulators (double buffered so that the
+//              epilogue of tile t overlaps the main loop of tile t+1).
+//   warps 6-9  (pre-norm only) sum of squares of each X row, read from the
+//              same shared-memory stage the tensor cores consume, on CUDA
+//              cores, in parallel with the MMA (blog §2 pseudocode:
+//              square_sum += (tile_A * tile_A).sum(-1)).
+//
+// Shared-memory operands (128-byte swizzle, 1 KB aligned):
+//   A stage  128 rows x 64 K, K-major: row r at r*128 bytes.
+//   B stage  TILE_N/64 boxes of 64 K-rows x 64 N (MN-major, W is row-major
+//            K x N), box i at i*8 KB, K-row k of a box at k*128 bytes.
+//
+// Pipeline barriers: full[s] (TMA bytes landed), empty[s] (MMA done with the
+// stage; pre-norm: also all 128 sum-of-squares threads), acc_full[b] (MMA
+// chain of a tile complete), acc_empty[b] (epilogue drained TMEM buffer b),
+// ss_full[b] (row sums of squares of the tile ready), xch[b] (all partial row
+// statistics of the cluster arrived).  Every wait is bounded in time; on
+// expiry the kernel records NF_ERR_TIMEOUT, drains what it issued, frees TMEM
+// and returns.
+#pragma once
+
+#include "nf_internal.h"
+#include "nf_ptx.cuh"
+
+namespace nf {
+
+// Bounded wait used only while draining: ignores the abort flag and records
+// nothing.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) return;
+    }
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t num_clusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Keeps the compiler from using r[] before an earlier asm statement.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]));
+}
+
+// Tile schedule: CTA-local tile index lt -> (m_tile, n_tile).
+struct TileSched {
+    int first, step, count;  // m (clustered) or linear tile (unclustered) sequence
+    int n_fixed;             // clustered: this CTA's n tile (its cluster rank)
+    int n_tiles;
+    bool clustered;
+    __device__ __forceinline__ void tile(int lt, int& m, int& n) const {
+        const int t = first + lt * step;
+        if (clustered) {
+            m = t;
+            n = n_fixed;
+        } else {
+            m = t / n_tiles;
+            n = t - m * n_tiles;
+        }
+    }
+};
+
+template <int EPI, int TILE_N, bool CLUSTERED>
+__global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
+    nf_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
+    using Cfg = GemmCfg<EPI, TILE_N, CLUSTERED>;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int NBOX = TILE_N / B_BOX_N;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base + Cfg::OFF_A;
+    const uint32_t sB = base + Cfg::OFF_B;
+    const uint32_t sStg = base + Cfg::OFF_STG;
+    const uint32_t sRecv = base + Cfg::OFF_RECV;
+    const uint32_t sBar = base + Cfg::OFF_BAR;
+    const uint32_t bar_full0 = sBar;             // [8]
+    const uint32_t bar_empty0 = sBar + 8u * 8;   // [8]
+    const uint32_t bar_accf0 = sBar + 8u * 16;   // [2]
+    const uint32_t bar_acce0 = sBar + 8u * 18;   // [2]
+    const uint32_t bar_ssf0 = sBar + 8u * 20;    // [2]
+    const uint32_t bar_xch0 = sBar + 8u * 22;    // [2]
+    const uint32_t bar_mma_done = sBar + 8u * 24;
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS);
+    volatile int* const abort_flag =
+        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS + 4);
+    float* const ss_buf = reinterpret_cast<float*>(base_ptr + Cfg::OFF_SS);
+    uint16_t* const aff = reinterpret_cast<uint16_t*>(base_ptr + Cfg::OFF_AFF);
+
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const WaitGuard guard{args.status, abort_flag, args.timeout_ns};
+
+    // ---- tile schedule
+    TileSched sched;
+    sched.clustered = CLUSTERED;
+    sched.n_tiles = args.n_tiles;
+    int my_rank = 0;
+    if (CLUSTERED) {
+        my_rank = static_cast<int>(cluster_ctarank());
+        const int cid = static_cast<int>(cluster_id_x());
+        const int ncl = static_cast<int>(num_clusters_x());
+        sched.first = cid;
+        sched.step = ncl;
+        sched.count = cid < args.m_tiles ? (args.m_tiles - cid + ncl - 1) / ncl : 0;
+        sched.n_fixed = my_rank;
+    } else {
+        const int total = args.m_tiles * args.n_tiles;
+        const int b = static_cast<int>(blockIdx.x);
+        const int g = static_cast<int>(gridDim.x);
+        sched.first = b;
+        sched.step = g;
+        sched.count = b < total ? (total - b + g - 1) / g : 0;
+        sched.n_fixed = 0;
+    }
+    const int count = sched.count;
+    const int k_tiles = args.k_tiles;
+    const uint32_t xch_bytes = static_cast<uint32_t>(args.cluster) * TILE_M * 8u;
+
+    // ---- set-up: barriers, TMEM, affine parameters
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full0 + 8u * s, 1);
+            mbar_init(bar_empty0 + 8u * s, 1 + (Cfg::kPre ? 128 : 0));
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_accf0 + 8u * b, 1);
+            mbar_init(bar_acce0 + 8u * b, 128);
+            mbar_init(bar_ssf0 + 8u * b, 128);
+            mbar_init(bar_xch0 + 8u * b, 1);
+        }
+        mbar_init(bar_mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        if (CLUSTERED) {
+            // Arm the exchange barriers for local tiles 0 and 1 before any peer
+            // can send (peers send only after the cluster barrier below).
+            for (int b = 0; b < 2 && b < count; ++b) mbar_arrive_expect_tx(bar_xch0 + 8u * b, xch_bytes);
+        }
+    }
+    if (warp == Cfg::PRODUCER_WARP) {
+        tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (Cfg::kPost && threadIdx.x < 128) {
+        // This CTA's columns never change: clustered CTAs keep their rank's
+        // tile, unclustered post-norm has a single column tile.
+        const int n0 = sched.n_fixed * TILE_N;
+        for (int i = static_cast<int>(threadIdx.x); i < TILE_N; i += 128) {
+            const int col = n0 + i;
+            const bool in = col < args.N;
+            aff[i] = (args.gamma && in) ? args.gamma[col] : static_cast<uint16_t>(0x3F80);  // 1.0
+            aff[TILE_N + i] = (args.beta && in) ? args.beta[col] : static_cast<uint16_t>(0);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (CLUSTERED) {
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    }
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == Cfg::PRODUCER_WARP) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmX);
+            prefetch_tmap(&tmW);
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int lt = 0; lt < count && ok; ++lt) {
+                int m, n;
+                sched.tile(lt, m, n);
+                for (int kt = 0; kt < k_tiles; ++kt) {
+                    if (!mbar_wait(guard, bar_empty0 + 8u * s, ph ^ 1u, SITE_PROD_EMPTY, lt)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full0 + 8u * s;
+                    mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                    tma_load_2d(sA + s * A_STAGE_BYTES, &tmX, fb, kt * TILE_K, m * TILE_M);
+#pragma unroll
+                    for (int i = 0; i < NBOX; ++i)
+                        tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb,
+                                    n * TILE_N + i * B_BOX_N, kt * TILE_K);
+                    ++issued;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // Drain: every load issued has landed before the CTA may exit.
+            for (int j = 0; j < STAGES; ++j) {
+                const uint32_t uj = static_cast<uint32_t>(j);
+                if (issued > uj) {
+                    const uint32_t fills = (issued - 1u - uj) / STAGES + 1u;
+                    mbar_drain(bar_full0 + 8u * j, (fills - 1u) & 1u, args.timeout_ns);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == Cfg::MMA_WARP) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, TILE_N, true);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int lt = 0; lt < count && ok; ++lt) {
+                const int b = lt & 1;
+                const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+                if (!mbar_wait(guard, bar_acce0 + 8u * b, aph ^ 1u, SITE_MMA_ACC_EMPTY, lt)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(b * TILE_N);
+                for (int kt = 0; kt < k_tiles; ++kt) {
+                    if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_MMA_FULL, lt)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + s * A_STAGE_BYTES;
+                    const uint32_t b0 = sB + s * Cfg::B_STAGE_BYTES;
+#pragma unroll
+                    for (int j = 0; j < TILE_K / UMMA_K; ++j) {
+                        // A: K-major, advance 16 elements = 32 bytes inside the
+                        //    swizzled 128-byte row; 8-row groups 1 KB apart.
+                        // B: MN-major, advance 16 K-rows = 2 KB; 8-row groups
+                        //    1 KB apart, 64-column boxes 8 KB apart.
+                        const uint64_t adesc = smem_desc_sw128(a0 + j * 32, 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b0 + j * 2048, B_BOX_BYTES, 1024);
+                        mma_bf16(d, adesc, bdesc, IDESC, (kt | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar_accf0 + 8u * b);  // accumulator b complete
+            }
+            // Everything issued has completed before TMEM can be released.
+            mma_commit(bar_mma_done);
+            mbar_drain(bar_mma_done, 0, args.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp < EPI_WARPS) {
+        // ================================================================ epilogue
+        const int row = warp * 32 + lane;  // tile row == TMEM lane
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        uint32_t store_count = 0;
+        for (int lt = 0; lt < count; ++lt) {
+            int m, n;
+            sched.tile(lt, m, n);
+            const int b = lt & 1;
+            const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+            bool ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
+            const int nv = min(TILE_N, args.N - n * TILE_N);  // valid columns of this tile
+            const int grow = m * TILE_M + row;                 // global row
+            float mul = 1.0f, sub = 0.0f;                      // y = (acc - sub) * mul
+
+            if (Cfg::kPre) {
+                ok = mbar_wait(guard, bar_ssf0 + 8u * b, aph, SITE_EPI_SS_FULL, lt);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                // blog §2: rstd = rsqrt(square_sum / K + eps); acc *= rstd[:, None]
+                const float ss = ss_buf[b * TILE_M + row];
+                mul = rsqrtf(fmaf(ss, args.inv_len, args.eps));
+                if (n == 0 && args.rstd_out && grow < args.M) args.rstd_out[grow] = mul;
+            }
+
+            if (Cfg::kPost) {
+                // -- local statistics of this CTA's nv columns (blog §3: each
+                //    CTA reduces the partial row statistics of its tile)
+                float s1 = 0.0f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < TILE_N; c0 += 32) {
+                    if (c0 >= nv) break;
+                    uint32_t v[32];
+                    tmem_ld32(tacc + c0, v);
+                    tmem_ld_wait(v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float x = __uint_as_float(v[j]);
+                        const float t = Cfg::kLN ? x : x * x;
+                        s1 += (c0 + j < nv) ? t : 0.0f;
+                    }
+                }
+                float pa, pb;  // partial: LN (mean_c, M2_c); RMS (sum of squares, 0)
+                if (Cfg::kLN) {
+                    const float mean_c = s1 / static_cast<float>(nv);
+                    float m2 = 0.0f;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TILE_N; c0 += 32) {
+                        if (c0 >= nv) break;
+                        uint32_t v[32];
+                        tmem_ld32(tacc + c0, v);
+                        tmem_ld_wait(v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float dlt = __uint_as_float(v[j]) - mean_c;
+                            m2 += (c0 + j < nv) ? dlt * dlt : 0.0f;
+                        }
+                    }
+                    pa = mean_c;
+                    pb = m2;
+                } else {
+                    pa = s1;
+                    pb = 0.0f;
+                }
+
+                float mean = 0.0f, sq;  // sq: M2 (LN) or sum of squares (RMS) over all N
+                if (CLUSTERED) {
+                    // -- exchange through distributed shared memory: push this
+                    //    CTA's partial into slot [my_rank] of every CTA of the
+                    //    cluster (itself included), then wait for all slots.
+                    const uint32_t slot =
+                        sRecv + static_cast<uint32_t>(((b * MAX_CLUSTER + my_rank) * TILE_M + row) * 8);
+                    const uint32_t xbar = bar_xch0 + 8u * b;
+                    for (int p = 0; p < args.cluster; ++p)
+                        st_async_f32x2(mapa_shared(slot, p), pa, pb, mapa_shared(xbar, p));
+                    ok = mbar_wait<true>(guard, xbar, aph, SITE_EPI_XCH, lt);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    // Re-arm for local tile lt + 2.  Its data can arrive only after
+                    // every CTA of the cluster got this CTA's tile lt+1 partials,
+                    // which are sent after this point.
+                    if (threadIdx.x == 0 && lt + 2 < count) mbar_arrive_expect_tx(xbar, xch_bytes);
+                    const float* recv = reinterpret_cast<const float*>(
+                        base_ptr + Cfg::OFF_RECV + (b * MAX_CLUSTER * TILE_M + row) * 8);
+                    if (Cfg::kLN) {
+                        // Chan et al. pairwise merge of (count, mean, M2).
+                        float msum = 0.0f;
+                        for (int p = 0; p < args.cluster; ++p) {
+                            const int np = min(TILE_N, args.N - p * TILE_N);
+                            msum += static_cast<float>(np) * recv[p * TILE_M * 2];
+                        }
+                        mean = msum * args.inv_len;
+                        sq = 0.0f;
+                        for (int p = 0; p < args.cluster; ++p) {
+                            const int np = min(TILE_N, args.N - p * TILE_N);
+                            const float dm = recv[p * TILE_M * 2] - mean;
+                            sq += recv[p * TILE_M * 2 + 1] + static_cast<float>(np) * dm * dm;
+                        }
+                    } else {
+                        sq = 0.0f;
+                        for (int p = 0; p < args.cluster; ++p) sq += recv[p * TILE_M * 2];
+                    }
+                } else {
+                    mean = pa;
+                    sq = Cfg::kLN ? pb : pa;
+                }
+                // LayerNorm: (acc - mean) * rsqrt(M2/N + eps); RMSNorm: acc * rsqrt(ss/N + eps)
+                mul = rsqrtf(fmaf(sq, args.inv_len, args.eps));
+                sub = Cfg::kLN ? mean : 0.0f;
+                if (n == 0 && grow < args.M) {
+                    if (Cfg::kLN && args.mean_out) args.mean_out[grow] = mean;
+                    if (args.rstd_out) args.rstd_out[grow] = mul;
+                }
+            }
+
+            // -- normalize, convert, stage (128B swizzle) and store 64 columns at a time.
+            //    A warp whose 32 rows all lie past M has nothing to store.
+            const int nstore = (m * TILE_M + warp * 32 < args.M) ? nv : 0;
+#pragma unroll 1
+            for (int c0 = 0; c0 < TILE_N; c0 += STORE_COLS) {
+                if (c0 >= nstore) break;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tacc + c0, v0);
+                tmem_ld32(tacc + c0 + 32, v1);
+                tmem_ld_wait(v0);
+                reg_fence(v1);
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const uint32_t* src = (j < 16) ? v0 : v1;
+                    const int jj = (j & 15) * 2;
+                    float y0 = (__uint_as_float(src[jj]) - sub) * mul;
+                    float y1 = (__uint_as_float(src[jj + 1]) - sub) * mul;
+                    if (Cfg::kPost) {
+                        const int c = c0 + 2 * j;
+                        const uint32_t g2 = *reinterpret_cast<const uint32_t*>(aff + c);
+                        const uint32_t b2 = *reinterpret_cast<const uint32_t*>(aff + TILE_N + c);
+                        y0 = fmaf(y0, bf16lo(g2), bf16lo(b2));
+                        y1 = fmaf(y1, bf16hi(g2), bf16hi(b2));
+                    }
+                    pk[j] = pack_bf16x2(y0, y1);
+                }
+                const uint32_t sb = sStg + static_cast<uint32_t>((warp * 2 + (store_count & 1u)) * STORE_BUF_BYTES);
+                ++store_count;
+                if (lane == 0) bulk_wait_read<1>();  // the store that used sb last has read it
+                __syncwarp();
+                const uint32_t rowp = sb + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(rowp + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                                 pk[4 * q + 2], pk[4 * q + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmY, sb, n * TILE_N + c0, m * TILE_M + warp * 32);
+                    bulk_commit();
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_acce0 + 8u * b);  // TMEM buffer b may be overwritten
+        }
+        if (lane == 0) bulk_wait_all<0>();
+        __syncwarp();
+    } else if (Cfg::kPre && warp >= Cfg::SUMSQ_WARP0) {
+        // ================================================================ row sums of squares
+        const int row = static_cast<int>(threadIdx.x) - Cfg::SUMSQ_WARP0 * 32;  // 0..127
+        int s = 0;
+        uint32_t ph = 0;
+        for (int lt = 0; lt < count; ++lt) {
+            const int b = lt & 1;
+            const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+            float acc0 = 0.0f, acc1 = 0.0f;
+            bool ok = true;
+            for (int kt = 0; kt < k_tiles; ++kt) {
+                if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)) {
+                    ok = false;
+                    break;
+                }
+                // The row's 128 bytes are contiguous whatever the swizzle (it
+                // only permutes 16-byte chunks within the row); start each
+                // thread at a different chunk so the 8 threads of a quarter
+                // warp hit 8 different bank groups.
+                const uint32_t rbase = sA + s * A_STAGE_BYTES + static_cast<uint32_t>(row * 128);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 w = ld_shared_v4(rbase + (static_cast<uint32_t>((q + row) & 7) << 4));
+                    float x;
+                    x = bf16lo(w.x); acc0 = fmaf(x, x, acc0);
+                    x = bf16hi(w.x); acc1 = fmaf(x, x, acc1);
+                    x = bf16lo(w.y); acc0 = fmaf(x, x, acc0);
+                    x = bf16hi(w.y); acc1 = fmaf(x, x, acc1);
+                    x = bf16lo(w.z); acc0 = fmaf(x, x, acc0);
+                    x = bf16hi(w.z); acc1 = fmaf(x, x, acc1);
+                    x = bf16lo(w.w); acc0 = fmaf(x, x, acc0);
+                    x = bf16hi(w.w); acc1 = fmaf(x, x, acc1);
+                }
+                mbar_arrive(bar_empty0 + 8u * s);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            // ss_buf[b] is free once the epilogue released accumulator b of tile lt-2.
+            if (!mbar_wait(guard, bar_acce0 + 8u * b, aph ^ 1u, SITE_SS_ACC_EMPTY, lt)) break;
+            ss_buf[b * TILE_M + row] = acc0 + acc1;
+            mbar_arrive(bar_ssf0 + 8u * b);
+        }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (CLUSTERED) {
+        // No CTA leaves while a peer may still write into its shared memory.
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    }
+    if (warp == Cfg::PRODUCER_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int EPI, int TILE_N, bool CLUSTERED>
+GemmVariant make_variant() {
+    using Cfg = GemmCfg<EPI, TILE_N, CLUSTERED>;
+    return GemmVariant{EPI,
+                       TILE_N,
+                       CLUSTERED,
+                       reinterpret_cast<const void*>(&nf_gemm_kernel<EPI, TILE_N, CLUSTERED>),
+                       Cfg::THREADS,
+                       Cfg::SMEM_BYTES,
+                       Cfg::STAGES,
+                       Cfg::TMEM_COLS};
+}
+
+}  // namespace nf

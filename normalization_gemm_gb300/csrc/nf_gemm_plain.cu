@@ -1,0 +1,15 @@
+// nf_gemm_plain.cu -- instantiations of the plain GEMM (unfused baseline) kernel
+// (one translation unit per epilogue so the variants compile in parallel).
+#include "nf_gemm_kernel.cuh"
+
+namespace nf {
+
+const GemmVariant* gemm_variants_plain(int* count) {
+    static const GemmVariant v[] = {
+        make_variant<EPI_PLAIN, 64, false>(), make_variant<EPI_PLAIN, 128, false>(),
+        make_variant<EPI_PLAIN, 256, false>()};
+    *count = 3;
+    return v;
+}
+
+}  // namespace nf

@@ -1,0 +1,15 @@
+// nf_gemm_post_rms.cu -- instantiations of the post-norm RMSNorm GEMM kernel
+// (one translation unit per epilogue so the variants compile in parallel).
+#include "nf_gemm_kernel.cuh"
+
+namespace nf {
+
+const GemmVariant* gemm_variants_post_rms(int* count) {
+    static const GemmVariant v[] = {
+        make_variant<EPI_POST_RMS, 64, false>(), make_variant<EPI_POST_RMS, 128, false>(),
+        make_variant<EPI_POST_RMS, 256, false>(), make_variant<EPI_POST_RMS, 256, true>()};
+    *count = 4;
+    return v;
+}
+
+}  // namespace nf

@@ -1,0 +1,15 @@
+// nf_gemm_pre.cu -- instantiations of the Lazy Pre-Norm RMS GEMM kernel
+// (one translation unit per epilogue so the variants compile in parallel).
+#include "nf_gemm_kernel.cuh"
+
+namespace nf {
+
+const GemmVariant* gemm_variants_pre(int* count) {
+    static const GemmVariant v[] = {
+        make_variant<EPI_PRE_RMS, 64, false>(), make_variant<EPI_PRE_RMS, 128, false>(),
+        make_variant<EPI_PRE_RMS, 256, false>()};
+    *count = 3;
+    return v;
+}
+
+}  // namespace nf

@@ -1,0 +1,131 @@
+// nf_internal.h -- definitions shared by the kernel translation units and the
+// host library: tile shapes, the shared-memory layout of each GEMM variant,
+// the kernel argument block and the table of compiled variants.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nf {
+
+// ---------------------------------------------------------------- GEMM tiling
+constexpr int TILE_M = 128;               // rows per CTA tile = TMEM lanes
+constexpr int TILE_K = 64;                // bf16 K elements per stage = one 128-byte swizzle row
+constexpr int UMMA_K = 16;                // K per tcgen05.mma of kind::f16
+constexpr int B_BOX_N = 64;               // W is loaded as 64-column boxes (128 bytes per K row)
+constexpr int A_STAGE_BYTES = TILE_M * TILE_K * 2;   // 16 KB
+constexpr int B_BOX_BYTES = TILE_K * B_BOX_N * 2;    // 8 KB
+constexpr int EPI_WARPS = 4;              // epilogue warps 0-3 own TMEM lane quarters 0-3
+constexpr int STORE_COLS = 64;            // Y store box: 64 columns x 32 rows (one warp)
+constexpr int STORE_ROWS = 32;
+constexpr int STORE_BUF_BYTES = STORE_COLS * STORE_ROWS * 2;              // 4 KB
+constexpr int STAGING_BYTES = EPI_WARPS * 2 * STORE_BUF_BYTES;             // double buffered
+constexpr int MAX_CLUSTER = 16;           // post-norm: N <= 256 x 16
+constexpr int SMEM_OPTIN_LIMIT = 232448;  // 227 KB of dynamic shared memory per block
+constexpr int MAX_STAGES = 8;
+constexpr int NUM_BARRIER_SLOTS = 25;     // full[8] empty[8] acc_full[2] acc_empty[2] ss_full[2] xch[2] mma_done
+
+enum Epilogue : int { EPI_PLAIN = 0, EPI_PRE_RMS = 1, EPI_POST_LN = 2, EPI_POST_RMS = 3 };
+
+template <int EPI, int TILE_N, bool CLUSTERED>
+struct GemmCfg {
+    static constexpr bool kPre = EPI == EPI_PRE_RMS;
+    static constexpr bool kPost = EPI == EPI_POST_LN || EPI == EPI_POST_RMS;
+    static constexpr bool kLN = EPI == EPI_POST_LN;
+    static_assert(TILE_N == 64 || TILE_N == 128 || TILE_N == 256, "tile_n");
+    static_assert(!CLUSTERED || (kPost && TILE_N == 256), "clusters only for post-norm");
+
+    static constexpr int B_STAGE_BYTES = TILE_K * TILE_N * 2;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    // per-row partial statistics received from every CTA of the cluster,
+    // double buffered by tile parity: [2][MAX_CLUSTER][TILE_M] x float2
+    static constexpr int RECV_BYTES = CLUSTERED ? 2 * MAX_CLUSTER * TILE_M * 8 : 0;
+    static constexpr int AFFINE_BYTES = kPost ? 2 * TILE_N * 2 : 0;   // gamma, beta (bf16)
+    static constexpr int SS_BYTES = kPre ? 2 * TILE_M * 4 : 0;        // sum of squares [2][128]
+    static constexpr int BAR_BYTES = 256;                             // barriers + 2 words
+    static constexpr int FIXED_BYTES =
+        1024 /* alignment slack */ + STAGING_BYTES + RECV_BYTES + AFFINE_BYTES + SS_BYTES + BAR_BYTES;
+    static constexpr int STAGES_FIT = (SMEM_OPTIN_LIMIT - FIXED_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
+    static_assert(STAGES >= 2, "pipeline needs two stages");
+    static constexpr int SMEM_BYTES = FIXED_BYTES + STAGES * STAGE_BYTES;
+
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
+    static constexpr int OFF_STG = OFF_B + STAGES * B_STAGE_BYTES;
+    static constexpr int OFF_RECV = OFF_STG + STAGING_BYTES;
+    static constexpr int OFF_AFF = OFF_RECV + RECV_BYTES;
+    static constexpr int OFF_SS = OFF_AFF + AFFINE_BYTES;
+    static constexpr int OFF_BAR = OFF_SS + SS_BYTES;
+    static_assert(OFF_B % 1024 == 0 && OFF_STG % 1024 == 0, "swizzled buffers need 1 KB alignment");
+    static_assert(NUM_BARRIER_SLOTS * 8 + 8 <= BAR_BYTES, "barrier area");
+
+    static constexpr int PRODUCER_WARP = 4;
+    static constexpr int MMA_WARP = 5;
+    static constexpr int SUMSQ_WARP0 = 6;                 // pre-norm only: warps 6-9
+    static constexpr int THREADS = kPre ? 320 : 192;
+    static constexpr int TMEM_COLS = 2 * TILE_N;           // two accumulator buffers
+};
+
+// Kernel argument block (passed by value).
+struct GemmArgs {
+    int32_t M, N, K;
+    int32_t m_tiles, n_tiles, k_tiles;
+    int32_t cluster;        // CTAs per cluster along N (1 = no cluster)
+    float eps;
+    float inv_len;          // 1/K (pre-norm) or 1/N (post-norm)
+    const uint16_t* gamma;  // bf16, N entries, or null
+    const uint16_t* beta;   // bf16, N entries, or null
+    float* mean_out;        // M entries or null
+    float* rstd_out;        // M entries or null
+    uint32_t* status;       // device status word (4 x u32)
+    uint64_t timeout_ns;
+};
+
+// Wait sites recorded in the status word on a time-out.
+enum WaitSite : uint32_t {
+    SITE_PROD_EMPTY = 1,
+    SITE_MMA_ACC_EMPTY = 2,
+    SITE_MMA_FULL = 3,
+    SITE_EPI_ACC_FULL = 4,
+    SITE_EPI_SS_FULL = 5,
+    SITE_EPI_XCH = 6,
+    SITE_SS_FULL = 7,
+    SITE_SS_ACC_EMPTY = 8,
+    SITE_SELFTEST = 9,
+};
+
+// One compiled GEMM variant.
+struct GemmVariant {
+    int epi, tile_n;
+    bool clustered;
+    const void* func;
+    int threads, smem_bytes, stages, tmem_cols;
+};
+
+// Tables exported by the kernel translation units.
+const GemmVariant* gemm_variants_plain(int* count);
+const GemmVariant* gemm_variants_pre(int* count);
+const GemmVariant* gemm_variants_post_ln(int* count);
+const GemmVariant* gemm_variants_post_rms(int* count);
+
+// ---------------------------------------------------------------- row norm
+struct NormArgs {
+    const void* in;
+    void* out;
+    const uint16_t* gamma;
+    const uint16_t* beta;
+    int64_t rows;
+    int32_t cols;
+    float eps;
+    float inv_cols;
+    float* mean_out;
+    float* rstd_out;
+};
+
+// Picks the variant for `cols` and launches it; returns the CUDA status.
+cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, cudaStream_t stream);
+// Largest supported cols.
+constexpr int NORM_MAX_COLS = 16384;
+
+}  // namespace nf

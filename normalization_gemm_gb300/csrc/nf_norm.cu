@@ -1,0 +1,187 @@
+// nf_norm.cu -- standalone LayerNorm / RMSNorm over rows: the separate,
+// memory-bound normalization kernel of the unfused baseline (blog "Towards
+// Free Normalization: Fusing Normalization into GEMM and Attention Kernels",
+// §1: a GEMM followed by its own norm kernel, each row read and written once).
+//
+// Design: the kernel is HBM-bound, so it is built around 16-byte vector
+// accesses and enough bytes in flight, not around tensor cores or TMA.
+//   * A row of `cols` bf16 is 16-byte chunks; TPR threads (a power of two)
+//     share a row, each holding CPT chunks (CPT * 8 values) in registers, so
+//     the row is read from HBM exactly once and written once.
+//   * Reductions: xor-shuffles inside a warp; for TPR > 32 a second step
+//     through shared memory across the row's warps.
+//   * LayerNorm takes two passes over the registers (mean, then squared
+//     deviations), with biased variance and eps inside the root, as
+//     torch.nn.LayerNorm; RMSNorm takes one.
+//   * The grid is persistent (a multiple of the SM count); every CTA walks
+//     blocks of rows so all its threads take the same trip count.
+#include "nf_internal.h"
+#include "nf_ptx.cuh"
+
+namespace nf {
+
+namespace {
+
+constexpr int NORM_THREADS = 256;
+
+__device__ __forceinline__ void unpack8(const uint4 q, float (&v)[8]) {
+    v[0] = bf16lo(q.x); v[1] = bf16hi(q.x);
+    v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+    v[4] = bf16lo(q.z); v[5] = bf16hi(q.z);
+    v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+}
+
+// Sum over the TPR threads of a row group (groups are aligned, TPR a power of 2).
+template <int TPR>
+__device__ __forceinline__ float group_sum(float x, float* red, int warp, int lane) {
+    constexpr int W = TPR < 32 ? TPR : 32;
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if constexpr (TPR > 32) {
+        constexpr int WPR = TPR / 32;  // warps per row
+        if (lane == 0) red[warp] = x;
+        __syncthreads();
+        const int w0 = (warp / WPR) * WPR;
+        float t = 0.0f;
+#pragma unroll
+        for (int i = 0; i < WPR; ++i) t += red[w0 + i];
+        __syncthreads();
+        x = t;
+    }
+    return x;
+}
+
+template <int TPR, int CPT, int KIND>
+__global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormArgs a) {
+    constexpr int RPB = NORM_THREADS / TPR;  // rows per block-step
+    __shared__ float red[NORM_THREADS / 32];
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int t = static_cast<int>(threadIdx.x) % TPR;
+    const int rg = static_cast<int>(threadIdx.x) / TPR;
+    const int chunks = a.cols >> 3;
+    const uint4* in = reinterpret_cast<const uint4*>(a.in);
+    uint4* out = reinterpret_cast<uint4*>(a.out);
+
+    // This thread always owns chunks t, t+TPR, ...: load its gamma / beta once.
+    float g[CPT][8], bb[CPT][8];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int c = t + i * TPR;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            g[i][e] = 1.0f;
+            bb[i][e] = 0.0f;
+        }
+        if (c < chunks) {
+            if (a.gamma) unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma) + c), g[i]);
+            if (KIND == 0 && a.beta) unpack8(__ldg(reinterpret_cast<const uint4*>(a.beta) + c), bb[i]);
+        }
+    }
+
+    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * RPB; r0 < a.rows;
+         r0 += static_cast<int64_t>(gridDim.x) * RPB) {
+        const int64_t row = r0 + rg;
+        const bool live = row < a.rows;
+        float v[CPT][8];
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = t + i * TPR;
+            if (live && c < chunks) {
+                unpack8(__ldcs(in + row * chunks + c), v[i]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] = 0.0f;
+            }
+        }
+        float mean = 0.0f, rstd;
+        if (KIND == 0) {
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < CPT; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s += v[i][e];
+            mean = group_sum<TPR>(s, red, warp, lane) * a.inv_cols;
+            float d2 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const bool in_row = (t + i * TPR) < chunks;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float d = v[i][e] - mean;
+                    d2 += in_row ? d * d : 0.0f;
+                }
+            }
+            rstd = rsqrtf(fmaf(group_sum<TPR>(d2, red, warp, lane), a.inv_cols, a.eps));
+        } else {
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < CPT; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s = fmaf(v[i][e], v[i][e], s);
+            rstd = rsqrtf(fmaf(group_sum<TPR>(s, red, warp, lane), a.inv_cols, a.eps));
+        }
+        if (!live) continue;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = t + i * TPR;
+            if (c < chunks) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = fmaf((v[i][e] - mean) * rstd, g[i][e], bb[i][e]);
+                uint4 q;
+                q.x = pack_bf16x2(y[0], y[1]);
+                q.y = pack_bf16x2(y[2], y[3]);
+                q.z = pack_bf16x2(y[4], y[5]);
+                q.w = pack_bf16x2(y[6], y[7]);
+                __stcs(out + row * chunks + c, q);
+            }
+        }
+        if (t == 0) {
+            if (KIND == 0 && a.mean_out) a.mean_out[row] = mean;
+            if (a.rstd_out) a.rstd_out[row] = rstd;
+        }
+    }
+}
+
+template <int TPR, int CPT, int KIND>
+cudaError_t launch_one(const NormArgs& a, int sm_count, cudaStream_t stream) {
+    auto kern = nf_norm_rows_kernel<TPR, CPT, KIND>;
+    constexpr int RPB = NORM_THREADS / TPR;
+    static int per_sm = 0;  // occupancy of this variant, queried once
+    if (per_sm == 0) {
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NORM_THREADS, 0);
+        if (e != cudaSuccess) return e;
+        per_sm = n < 1 ? 1 : n;
+    }
+    const int64_t steps = (a.rows + RPB - 1) / RPB;
+    const int64_t cap = static_cast<int64_t>(sm_count) * per_sm;
+    const int grid = static_cast<int>(steps < cap ? steps : cap);
+    kern<<<grid, NORM_THREADS, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t dispatch(const NormArgs& a, int sm_count, cudaStream_t stream) {
+    const int chunks = a.cols >> 3;
+    // TPR: the smallest power of two with TPR * 4 >= chunks (at most 256).
+    if (chunks <= 4) return launch_one<1, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 8) return launch_one<2, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 16) return launch_one<4, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 32) return launch_one<8, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 64) return launch_one<16, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 128) return launch_one<32, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 256) return launch_one<64, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 512) return launch_one<128, 4, KIND>(a, sm_count, stream);
+    if (chunks <= 1024) return launch_one<256, 4, KIND>(a, sm_count, stream);
+    return launch_one<256, 8, KIND>(a, sm_count, stream);  // cols <= 16384
+}
+
+}  // namespace
+
+cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, cudaStream_t stream) {
+    return kind == 0 ? dispatch<0>(a, sm_count, stream) : dispatch<1>(a, sm_count, stream);
+}
+
+}  // namespace nf

@@ -1,0 +1,116 @@
+"""The C ABI on the CPU: the library loads, exports every symbol include/nf.h
+declares, rejects bad arguments before touching a device, and plans tiles as
+documented.  No compute call is made."""
+import ctypes
+
+import pytest
+
+import normalization_gemm_gb300 as nf
+from normalization_gemm_gb300 import _build
+
+OK, INVALID, ALIGN, SHAPE = 0, 1, 2, 3
+P = 1 << 20          # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return nf.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = nf.header_symbols()
+    assert "nf_gemm_prenorm_rms" in names and "nf_norm_rows" in names
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in nf.h but not exported"
+    assert L.nf_abi_version() == 1
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.nf_status_string(code)
+    assert L.nf_status_string(5) == b"device wait timed out"
+
+
+def test_null_and_negative_arguments(L):
+    assert L.nf_gemm_plain(None, P, P, 128, 64, 64, None) == INVALID
+    assert L.nf_gemm_plain(P, P, P, -1, 64, 64, None) == INVALID
+    assert L.nf_gemm_plain(P, P, P, 128, 0, 64, None) == INVALID
+    assert L.nf_gemm_plain(P, P, P, 128, 64, 0, None) == INVALID
+    assert b"non-null" in L.nf_last_error() or b"M >= 0" in L.nf_last_error()
+    assert L.nf_norm_rows(P, P, None, None, 4, 64, 7, 1e-5, None, None, None) == INVALID
+
+
+def test_eps_must_be_finite_and_nonnegative(L):
+    for eps in (float("nan"), float("inf"), -1e-6):
+        assert L.nf_gemm_prenorm_rms(P, P, P, 128, 64, 64, eps, None, None) == INVALID
+        assert L.nf_gemm_postnorm_ln(P, P, None, None, P, 128, 64, 64, eps, None, None, None) == INVALID
+        assert L.nf_norm_rows(P, P, None, None, 4, 64, 0, eps, None, None, None) == INVALID
+
+
+def test_alignment_rules(L):
+    assert L.nf_gemm_plain(P + 8, P, P, 128, 64, 64, None) == ALIGN
+    assert L.nf_gemm_plain(P, P, P + 2, 128, 64, 64, None) == ALIGN
+    assert L.nf_gemm_plain(P, P, P, 128, 64, 60, None) == ALIGN      # K % 8
+    assert L.nf_gemm_plain(P, P, P, 128, 36, 64, None) == ALIGN      # N % 8
+    assert L.nf_gemm_postnorm_ln(P, P, P + 1, None, P, 128, 64, 64, 1e-5, None, None, None) == ALIGN
+    assert L.nf_gemm_prenorm_rms(P, P, P, 128, 64, 64, 1e-5, P + 2, None) == ALIGN
+    assert L.nf_norm_rows(P, P, None, None, 4, 12, 0, 1e-5, None, None, None) == ALIGN
+    assert L.nf_norm_rows(P, P, P + 2, None, 4, 64, 0, 1e-5, None, None, None) == ALIGN
+
+
+def test_unsupported_shapes(L):
+    assert L.nf_gemm_postnorm_ln(P, P, None, None, P, 128, 4104, 64, 1e-5, None, None, None) == SHAPE
+    assert L.nf_gemm_postnorm_rms(P, P, None, P, 128, 8192, 64, 1e-5, None, None) == SHAPE
+    assert L.nf_gemm_plain(P, P, P, 1 << 31, 64, 64, None) == SHAPE
+    assert L.nf_norm_rows(P, P, None, None, 4, 16392, 0, 1e-5, None, None, None) == SHAPE
+
+
+def test_empty_m_is_a_noop(L):
+    # M == 0 returns before any device call, so this is safe without a GPU.
+    assert L.nf_gemm_plain(P, P, P, 0, 64, 64, None) == OK
+    assert L.nf_gemm_postnorm_ln(P, P, None, None, P, 0, 4096, 64, 1e-5, None, None, None) == OK
+    assert L.nf_norm_rows(P, P, None, None, 0, 64, 1, 1e-5, None, None, None) == OK
+
+
+def test_timeout_setting_range(L):
+    assert L.nf_set_wait_timeout_ns(10) == INVALID
+    assert L.nf_set_wait_timeout_ns(2_000_000_000) == OK
+
+
+@pytest.mark.parametrize("op,M,N,K,tile_n,cluster", [
+    (0, 256, 64, 64, 64, 1), (1, 256, 64, 64, 64, 1), (1, 32768, 512, 512, 256, 1),
+    (2, 65536, 128, 128, 128, 1), (2, 16384, 2048, 1024, 256, 8), (3, 16384, 2048, 1024, 256, 8),
+    (2, 8192, 4096, 4096, 256, 16), (2, 300, 264, 72, 256, 2), (2, 5, 8, 8, 64, 1),
+    (0, 100, 200, 8, 256, 1), (1, 100, 120, 8, 128, 1),
+])
+def test_plans(L, op, M, N, K, tile_n, cluster):
+    p = nf.plan_gemm(op, M, N, K, 148)
+    assert (p["tile_m"], p["tile_k"]) == (128, 64)
+    assert p["tile_n"] == tile_n and p["cluster"] == cluster
+    assert cluster * tile_n >= N or op in (0, 1)
+    assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
+    assert p["tmem_cols"] == 2 * tile_n
+    assert p["threads"] == (320 if op == 1 else 192)
+    m_tiles = -(-M // 128)
+    n_tiles = 1 if op >= 2 else -(-N // tile_n)
+    assert p["tiles"] == m_tiles * n_tiles
+    assert p["grid"] % cluster == 0 and 0 < p["grid"] <= 148
+    # 1 CTA per SM whenever the kernel takes all 512 TMEM columns
+    if p["tmem_cols"] == 512:
+        assert p["smem_bytes"] > 232448 // 2
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        nf.gemm_plain(x, x.t().contiguous())
+
+
+def test_empty_m_accepts_null_bases(L):
+    # empty torch tensors report a null data pointer
+    assert L.nf_gemm_plain(None, P, None, 0, 64, 64, None) == OK
+    assert L.nf_gemm_prenorm_rms(None, P, None, 0, 64, 64, 1e-6, None, None) == OK
+    assert L.nf_norm_rows(None, None, None, None, 0, 64, 0, 1e-5, None, None, None) == OK
+    assert L.nf_gemm_plain(None, P, None, 1, 64, 64, None) == INVALID

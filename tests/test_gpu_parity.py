@@ -1,0 +1,307 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small shapes span several tiles and ragged tails on every dimension and are
+compared element by element over the whole output; the five full-size
+workloads run in the benchmark's launch configuration and are compared on
+sampled rows (the oracle computes rows independently), with whole-output
+properties (finite values, per-row moments) checked on every row.
+"""
+import numpy as np
+import pytest
+
+import nf_inputs
+import normalization_gemm_gb300 as nf
+from gpu_util import ATOL, RTOL, assert_close, require_gpu, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = require_gpu()
+    from normalization_gemm_gb300 import _build
+    _build.build()
+    nf.clear_device_status()
+    # Every kernel here finishes in milliseconds: a pipeline wait that needs
+    # more than 250 ms is a bug, reported as NF_ERR_TIMEOUT instead of a stall.
+    nf.set_wait_timeout_ns(250_000_000)
+    yield d
+    import torch
+    torch.cuda.synchronize()
+    status, detail = nf.device_status()
+    assert status == nf.NF_OK, f"device status word set: {detail}"
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    return oracle.get()
+
+
+def _inputs(M, K, N, seed, **kw):
+    return nf_inputs.make_inputs(M, K, N, seed=seed, **kw)
+
+
+# Shapes: (M, K, N).  Ragged M (not a multiple of 128), K (not of 64) and N
+# (not of the tile), single rows, the smallest legal K and N, several tiles.
+GEMM_SHAPES = [(256, 64, 64), (300, 200, 320), (1, 8, 8), (129, 72, 136), (513, 520, 264),
+               (130, 1032, 8), (384, 128, 128), (257, 64, 456)]
+
+
+@pytest.mark.parametrize("M,K,N", GEMM_SHAPES)
+def test_plain(dev, orc, M, K, N):
+    inp = _inputs(M, K, N, seed=M + K + N)
+    y = nf.gemm_plain(to_dev(inp["X"], dev), to_dev(inp["W"], dev))
+    assert_close(to_f64(y), orc.gemm_plain(inp["X"], inp["W"]), f"plain {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M,K,N", GEMM_SHAPES)
+@pytest.mark.parametrize("x_dist", ["normal", "row_scaled"])
+def test_prenorm_rms(dev, orc, M, K, N, x_dist):
+    import torch
+    inp = _inputs(M, K, N, seed=2 * M + K + N, x_dist=x_dist)
+    rstd = torch.full((M,), -1.0, dtype=torch.float32, device=dev)
+    y = nf.gemm_prenorm_rms(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-6, rstd_out=rstd)
+    ref, rref = orc.gemm_prenorm_rms(inp["X"], inp["W"], 1e-6)
+    assert_close(to_f64(y), ref, f"pre {M}x{K}x{N} {x_dist}")
+    np.testing.assert_allclose(rstd.cpu().numpy(), rref, rtol=1e-4)
+
+
+# Post-norm shapes: N covers one CTA (64/128/256 tiles, ragged) and clusters
+# of 2, 3, 4, 8 and 16 CTAs (the last with a ragged CTA).
+POST_SHAPES = [(300, 64, 8), (300, 136, 64), (257, 64, 120), (384, 128, 128), (129, 72, 200),
+               (300, 64, 256), (300, 64, 264), (200, 136, 576), (256, 128, 1024),
+               (130, 64, 2048), (129, 64, 4096), (64, 64, 4088)]
+
+
+@pytest.mark.parametrize("M,K,N", POST_SHAPES)
+@pytest.mark.parametrize("affine", [False, True])
+def test_postnorm_ln(dev, orc, M, K, N, affine):
+    import torch
+    inp = _inputs(M, K, N, seed=3 * M + K + N, gamma=True, beta=True)
+    g = inp["gamma"] if affine else None
+    b = inp["beta"] if affine else None
+    mean = torch.zeros(M, dtype=torch.float32, device=dev)
+    rstd = torch.zeros(M, dtype=torch.float32, device=dev)
+    y = nf.gemm_postnorm_ln(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-5,
+                            None if g is None else to_dev(g, dev), None if b is None else to_dev(b, dev),
+                            mean_out=mean, rstd_out=rstd)
+    ref, mref, rref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, g, b)
+    assert_close(to_f64(y), ref, f"post-ln {M}x{K}x{N} affine={affine}")
+    np.testing.assert_allclose(rstd.cpu().numpy(), rref, rtol=1e-3)
+    np.testing.assert_allclose(mean.cpu().numpy(), mref, atol=1e-3 / rref.min(), rtol=1e-3)
+
+
+@pytest.mark.parametrize("M,K,N", POST_SHAPES)
+@pytest.mark.parametrize("affine", [False, True])
+def test_postnorm_rms(dev, orc, M, K, N, affine):
+    import torch
+    inp = _inputs(M, K, N, seed=5 * M + K + N, gamma=True)
+    g = inp["gamma"] if affine else None
+    rstd = torch.zeros(M, dtype=torch.float32, device=dev)
+    y = nf.gemm_postnorm_rms(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-5,
+                             None if g is None else to_dev(g, dev), rstd_out=rstd)
+    ref, rref = orc.gemm_postnorm_rms(inp["X"], inp["W"], 1e-5, g)
+    assert_close(to_f64(y), ref, f"post-rms {M}x{K}x{N} affine={affine}")
+    np.testing.assert_allclose(rstd.cpu().numpy(), rref, rtol=1e-3)
+
+
+@pytest.mark.parametrize("rows,cols", [(300, 8), (1000, 64), (65, 128), (257, 136), (129, 512),
+                                       (33, 2048), (17, 4096), (5, 16384), (3, 1032)])
+@pytest.mark.parametrize("kind", [0, 1])
+def test_norm_rows(dev, orc, rows, cols, kind):
+    import torch
+    inp = _inputs(rows, cols, cols, seed=rows + cols + kind, gamma=True, beta=True, w_var=1.0)
+    X = inp["X"]
+    G = inp["gamma"]
+    B = inp["beta"] if kind == 0 else None
+    mean = torch.zeros(rows, dtype=torch.float32, device=dev)
+    rstd = torch.zeros(rows, dtype=torch.float32, device=dev)
+    y = nf.norm_rows(to_dev(X, dev), kind, 1e-5, to_dev(G, dev), None if B is None else to_dev(B, dev),
+                     mean_out=mean, rstd_out=rstd)
+    ref, mref, rref = orc.norm_rows(X, kind, 1e-5, G, B)
+    assert_close(to_f64(y), ref, f"norm_rows {rows}x{cols} kind={kind}")
+    np.testing.assert_allclose(rstd.cpu().numpy(), rref, rtol=1e-4)
+    if kind == 0:
+        np.testing.assert_allclose(mean.cpu().numpy(), mref, atol=1e-5, rtol=1e-4)
+
+
+# ------------------------------------------------------------ persistence
+def test_many_tiles_per_cta(dev, orc):
+    """Several tiles per persistent CTA: both TMEM buffers and every ring stage
+    are reused many times (M = 3 waves of 128-row tiles per SM plus a tail)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    M = 128 * sms * 3 + 77
+    inp = _inputs(M, 192, 64, seed=17)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    rows = nf_inputs.sample_rows(M, 400, seed=3)
+    y = to_f64(nf.gemm_prenorm_rms(X, W, 1e-6))[rows]
+    assert_close(y, orc.gemm_prenorm_rms(inp["X"], inp["W"], 1e-6, rows=rows)[0], "pre persistent")
+    y = to_f64(nf.gemm_postnorm_ln(X, W, 1e-5))[rows]
+    assert_close(y, orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, rows=rows)[0], "post-ln persistent")
+    y = to_f64(nf.gemm_plain(X, W))[rows]
+    assert_close(y, orc.gemm_plain(inp["X"], inp["W"], rows=rows), "plain persistent")
+
+
+def test_cluster_many_tiles_per_cluster(dev, orc):
+    """16-CTA clusters walking many m tiles: the exchange barriers and both
+    receive buffers cycle through many phases."""
+    M = 128 * 64 + 5
+    inp = _inputs(M, 64, 4096, seed=19, gamma=True, beta=True)
+    rows = nf_inputs.sample_rows(M, 160, seed=4)
+    y = nf.gemm_postnorm_ln(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-6,
+                            to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev))
+    ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-6, inp["gamma"], inp["beta"], rows=rows)[0]
+    assert_close(to_f64(y)[rows], ref, "post-ln cluster 16, many tiles")
+
+
+# ------------------------------------------------------------ full-size workloads
+def _row_moments(y):
+    import torch
+    yf = y.float()
+    return yf.mean(-1), (yf * yf).mean(-1)
+
+
+@pytest.mark.parametrize("name", nf_inputs.WORKLOAD_ORDER)
+def test_full_size_workloads(dev, orc, name):
+    import torch
+    w = nf_inputs.WORKLOADS[name]
+    inp = nf_inputs.workload_inputs(w)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    G = to_dev(inp["gamma"], dev) if w.gamma else None
+    B = to_dev(inp["beta"], dev) if w.beta else None
+    rows = nf_inputs.sample_rows(w.M, 128 if w.K * w.N >= 4096 * 4096 else 512)
+    for op in w.ops:
+        if op == "pre_rms":
+            y = nf.gemm_prenorm_rms(X, W, w.eps)
+            ref = orc.gemm_prenorm_rms(inp["X"], inp["W"], w.eps, rows=rows)[0]
+        elif op == "post_ln":
+            y = nf.gemm_postnorm_ln(X, W, w.eps, G, B)
+            ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, inp.get("gamma"), inp.get("beta"),
+                                       rows=rows)[0]
+        else:
+            y = nf.gemm_postnorm_rms(X, W, w.eps, G)
+            ref = orc.gemm_postnorm_rms(inp["X"], inp["W"], w.eps, inp.get("gamma"), rows=rows)[0]
+        assert bool(torch.isfinite(y.float()).all()), f"{name} {op}: non-finite output"
+        assert_close(to_f64(y[torch.from_numpy(rows).to(dev)]), ref, f"{name} {op}")
+        if op in ("post_ln", "post_rms") and G is None:
+            # every row of a no-affine post-norm: mean 0 (LN) and mean square
+            # var/(var+eps) ~ 1 up to bf16 rounding
+            mu, ms = _row_moments(y)
+            if op == "post_ln":
+                assert float(mu.abs().max()) < 2e-2, f"{name}: LN row mean"
+            assert float((ms - 1).abs().max()) < 2e-2, f"{name}: row mean square"
+
+
+def test_unfused_pair_matches_fused(dev, orc):
+    """Blog §1 baseline pair (GEMM + separate norm kernel) against the fused
+    kernels, both against the oracle, on the same inputs."""
+    import torch
+    M, K, N = 1000, 512, 512
+    inp = _inputs(M, K, N, seed=23, x_dist="row_scaled", gamma=True, beta=True)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    G, B = to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev)
+    # pre-norm: RMSNorm(X) materialised in bf16, then the GEMM
+    xn = nf.norm_rows(X, nf.NORM_RMS, 1e-6)
+    unf = to_f64(nf.gemm_plain(xn, W))
+    fused = to_f64(nf.gemm_prenorm_rms(X, W, 1e-6))
+    ref = orc.gemm_prenorm_rms(inp["X"], inp["W"], 1e-6)[0]
+    assert_close(unf, ref, "unfused pre")
+    assert_close(fused, ref, "fused pre")
+    # post-norm: GEMM materialised in bf16, then LayerNorm
+    z = nf.gemm_plain(X, W)
+    unf = to_f64(nf.norm_rows(z, nf.NORM_LN, 1e-5, G, B))
+    fused = to_f64(nf.gemm_postnorm_ln(X, W, 1e-5, G, B))
+    ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, inp["gamma"], inp["beta"])[0]
+    assert_close(unf, ref, "unfused post")
+    assert_close(fused, ref, "fused post")
+
+
+# ------------------------------------------------------------ edge cases
+def test_degenerate_rows(dev, orc):
+    """Zero rows (RMS: output 0, rstd = 1/sqrt(eps)) and constant-output rows
+    (LN: output beta)."""
+    import torch
+    M, K, N = 200, 64, 576
+    inp = _inputs(M, K, N, seed=29, gamma=True, beta=True)
+    X = inp["X"].copy()
+    X[3] = 0
+    X[130] = 0
+    W = inp["W"].copy()
+    Wc = W.copy()
+    Wc[:] = nf_inputs.bf16_round(np.ones((K, N)) * 0.25)   # every column equal: Z rows constant
+    for Wm in (W, Wc):
+        for fn in ("ln", "rms"):
+            if fn == "ln":
+                y = nf.gemm_postnorm_ln(to_dev(X, dev), to_dev(Wm, dev), 1e-5,
+                                        to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev))
+                ref = orc.gemm_postnorm_ln(X, Wm, 1e-5, inp["gamma"], inp["beta"])[0]
+            else:
+                y = nf.gemm_postnorm_rms(to_dev(X, dev), to_dev(Wm, dev), 1e-5, to_dev(inp["gamma"], dev))
+                ref = orc.gemm_postnorm_rms(X, Wm, 1e-5, inp["gamma"])[0]
+            assert_close(to_f64(y), ref, f"degenerate post-{fn}")
+    rstd = torch.zeros(M, dtype=torch.float32, device=dev)
+    y = nf.gemm_prenorm_rms(to_dev(X, dev), to_dev(W, dev), 1e-6, rstd_out=rstd)
+    assert float(y[3].float().abs().max()) == 0.0
+    assert abs(float(rstd[3]) - 1e3) < 1.0
+
+
+def test_empty_m_leaves_output_untouched(dev):
+    import torch
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device=dev)
+    w = torch.zeros((64, 64), dtype=torch.bfloat16, device=dev)
+    y = torch.full((0, 64), 1.0, dtype=torch.bfloat16, device=dev)
+    nf.gemm_postnorm_ln(x, w, 1e-5, out=y)
+    nf.gemm_prenorm_rms(x, w, 1e-5, out=y)
+    nf.norm_rows(x, 0, 1e-5, out=torch.empty((0, 64), dtype=torch.bfloat16, device=dev))
+
+
+@pytest.mark.parametrize("op", ["plain", "pre", "post_ln"])
+def test_guard_band_around_output(dev, op):
+    """Stores are clipped to M x N: canary rows before and after Y survive."""
+    import torch
+    M, K, N = 201, 64, 264
+    inp = _inputs(M, K, N, seed=31)
+    buf = torch.full(((M + 4) * N,), 7.0, dtype=torch.bfloat16, device=dev)
+    y = buf[2 * N:(M + 2) * N].view(M, N)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    if op == "plain":
+        nf.gemm_plain(X, W, out=y)
+    elif op == "pre":
+        nf.gemm_prenorm_rms(X, W, 1e-6, out=y)
+    else:
+        nf.gemm_postnorm_ln(X, W, 1e-5, out=y)
+    torch.cuda.synchronize()
+    assert bool((buf[:2 * N] == 7.0).all()) and bool((buf[(M + 2) * N:] == 7.0).all())
+
+
+def test_repeated_calls_are_deterministic(dev):
+    import torch
+    inp = _inputs(1000, 256, 2048, seed=37, gamma=True, beta=True)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    G, B = to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev)
+    a = nf.gemm_postnorm_ln(X, W, 1e-5, G, B)
+    b = nf.gemm_postnorm_ln(X, W, 1e-5, G, B)
+    assert torch.equal(a, b)
+    a = nf.gemm_prenorm_rms(X, W, 1e-6)
+    b = nf.gemm_prenorm_rms(X, W, 1e-6)
+    assert torch.equal(a, b)
+
+
+def test_wait_timeout_is_reported_not_hung(dev):
+    """A barrier nobody arrives on: the bounded wait gives up after 5 ms and
+    records NF_ERR_TIMEOUT; the context stays usable."""
+    import torch
+    torch.cuda.synchronize()
+    nf.clear_device_status()
+    nf.selftest_wait_timeout(5_000_000)
+    status, detail = nf.device_status()
+    assert status == 5 and detail[1] == 9, (status, detail)
+    nf.clear_device_status()
+    assert nf.device_status()[0] == nf.NF_OK
+    # the device still computes correctly afterwards
+    inp = _inputs(128, 64, 64, seed=41)
+    y = nf.gemm_plain(to_dev(inp["X"], dev), to_dev(inp["W"], dev))
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y.float()).all())
