@@ -206,14 +206,27 @@ def graph_of(fn, count, stream):
     return g
 
 
-def time_steps(fn, steps, warmup, stream, dist=None, chunk=GRAPH_CHUNK, sampler=None):
+def time_steps(fn, steps, warmup, stream, dist=None, chunk=GRAPH_CHUNK, sampler=None, eager=False):
     """Run `warmup` untimed steps, then time exactly `steps` calls of fn(i) from
-    CUDA graphs with events on `stream`; returns seconds (max over ranks)."""
+    CUDA graphs (or eagerly) with events on `stream`; returns seconds (max over
+    ranks)."""
     import torch
     with torch.cuda.stream(stream):
         for i in range(warmup):
             fn(i)
     torch.cuda.synchronize()
+    if eager:
+        if dist is not None and dist.is_initialized():
+            dist.barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for i in range(steps):
+                fn(i)
+            t1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(t0.elapsed_time(t1) / 1e3, dist)
     full = min(chunk, steps)
     g_full = graph_of(fn, full, stream) if full > 0 else None
     rem = steps - (steps // full) * full if full else 0
@@ -254,7 +267,8 @@ def run_op(nf, op, X, W, Y, G, B, eps, stream):
         nf.gemm_plain(X, W, out=Y, stream=stream)
 
 
-def measure_workload(nf, w, op, dev, stream, steps, warmup, seed=0, dist=None, sampler=None):
+def measure_workload(nf, w, op, dev, stream, steps, warmup, seed=0, dist=None, sampler=None,
+                     unfused=True, eager=False):
     """Fused, plain-GEMM and norm-kernel time per launch for one workload/op."""
     import torch
     inp = nf_inputs.workload_inputs(w, seed=seed)
@@ -265,12 +279,14 @@ def measure_workload(nf, w, op, dev, stream, steps, warmup, seed=0, dist=None, s
     set_bytes = X0.numel() * 2 + Y0.numel() * 2
     sets, nsets = make_sets([X0, Y0], set_bytes, dev)
     fused = lambda i: run_op(nf, op, sets[i % nsets][0], W0, sets[i % nsets][1], G, B, w.eps, stream)  # noqa: E731
-    t_fused = time_steps(fused, steps, warmup, stream, dist, sampler=sampler)
-    out = {"t_fused": t_fused / steps, "sets": nsets, "set_bytes": set_bytes}
+    t_fused = time_steps(fused, steps, warmup, stream, dist, sampler=sampler, eager=eager)
+    out = {"t_fused": t_fused / steps, "sets": nsets, "set_bytes": set_bytes, "fused_fn": fused}
+    if not unfused:
+        return out
     # unfused pair of the blog's §1 baseline
     plain = lambda i: nf.gemm_plain(sets[i % nsets][0], W0, out=sets[i % nsets][1], stream=stream)  # noqa: E731
     ksteps = max(1, min(steps, 2000))
-    out["t_plain"] = time_steps(plain, ksteps, min(warmup, 10), stream, dist) / ksteps
+    out["t_plain"] = time_steps(plain, ksteps, min(warmup, 10), stream, dist, eager=eager) / ksteps
     if op == "pre_rms":
         rows, cols, src = w.M, w.K, 0   # norm on X (M x K) into a scratch copy
         scratch = [torch.empty_like(s[0]) for s in sets]
@@ -282,10 +298,10 @@ def measure_workload(nf, w, op, dev, stream, steps, warmup, seed=0, dist=None, s
         kind = nf.NORM_LN if op == "post_ln" else nf.NORM_RMS
         norm = lambda i: nf.norm_rows(sets[i % nsets][1], kind, w.eps, G, B, out=scratch[i % nsets],  # noqa: E731
                                       stream=stream)
-    out["t_norm"] = time_steps(norm, ksteps, min(warmup, 10), stream, dist) / ksteps
+    out["t_norm"] = time_steps(norm, ksteps, min(warmup, 10), stream, dist, eager=eager) / ksteps
     out["norm_cols"] = cols
     out["norm_rows"] = rows
-    del sets, scratch
+    del scratch
     torch.cuda.empty_cache()
     return out
 
@@ -404,8 +420,15 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["nf", "reference"], default="nf")
+    ap.add_argument("--workload", default=WORKLOAD, choices=list(nf_inputs.WORKLOAD_ORDER),
+                    help="workload of the headline line (default: the ads-shaped post-LN GEMM)")
+    ap.add_argument("--op", default=None, help="pre_rms | post_ln | post_rms (default: the workload's first)")
+    ap.add_argument("--eager", action="store_true", help="launch every step from Python (no CUDA graphs)")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end figure")
+    ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused pair")
+    ap.add_argument("--no-soak", action="store_true", help="never add a clock-sampling soak")
     ap.add_argument("--e2e-steps", type=int, default=100)
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -432,27 +455,38 @@ def main(argv=None):
     stream = torch.cuda.Stream(device=dev)
     hbm_gbs, bf16_tf, bf16_sus, peak_src = measured_peaks()
 
-    w = nf_inputs.WORKLOADS[WORKLOAD]
+    w = nf_inputs.WORKLOADS[args.workload]
+    op = args.op or w.ops[0]
+    if op not in w.ops:
+        ap.error(f"--op {op} is not run on {w.name} (ops: {w.ops})")
     sampler = ClockSampler(local_rank)
     # each rank its own independent batch (seed = rank): weak scaling
-    m = measure_workload(nf, w, "post_ln", dev, stream, args.steps, args.warmup, seed=rank, dist=dist,
-                         sampler=sampler)
+    m = measure_workload(nf, w, op, dev, stream, args.steps, args.warmup, seed=rank, dist=dist,
+                         sampler=sampler, unfused=not args.no_unfused, eager=args.eager)
     t_step = m["t_fused"]
     value = world * w.flops / t_step / 1e12
     clocks = sampler.summary("timed")
-    if clocks["samples"] < 3:
-        # too short to sample: replay the same graph for ~1.5 s and sample that
+    if clocks["samples"] < 3 and not args.no_soak:
+        # The timed region was shorter than the sampling period: replay the same
+        # fused step for ~1.5 s right after it and sample that instead.
         soak = ClockSampler(local_rank)
         reps = max(args.steps, int(1.5 / max(t_step, 1e-7)))
-        inp = None  # noqa: F841
-        measure_soak = measure_workload(nf, w, "post_ln", dev, stream, reps, 3, seed=rank, sampler=soak)
-        del measure_soak
-        clocks = soak.summary("soak after the timed region (timed region shorter than the sampling period)")
+        time_steps(m["fused_fn"], reps, 3, stream, None, sampler=soak)
+        clocks = soak.summary("soak after the timed region (the timed region was shorter than "
+                              "the 50 ms sampling period)")
 
-    nbytes = algorithmic_bytes(w.M, w.N, w.K)
-    achieved = nbytes / t_step / 1e9
-    t_roof, _ = roofline_time(w, "post_ln", hbm_gbs, bf16_tf)
-    hidden = 100.0 * (m["t_plain"] + m["t_norm"] - m["t_fused"]) / m["t_norm"]
+    t_roof, nbytes = roofline_time(w, op, hbm_gbs, bf16_tf)
+    tensor_bound = w.flops / (bf16_tf * 1e12) > nbytes / (hbm_gbs * 1e9)
+    if tensor_bound:
+        achieved = w.flops / t_step / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
+                "frac": achieved / bf16_tf, "traffic": profiled_traffic(w.name),
+                "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic_flops_per_launch": w.flops}
+    else:
+        achieved = nbytes / t_step / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "traffic": profiled_traffic(w.name),
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": nbytes}
     status, detail = nf.device_status()
 
     line = {
@@ -460,53 +494,58 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps, "affine": False,
+        "config": {"workload": w.name, "op": op, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
+                   "gamma": bool(w.gamma and op != "pre_rms"), "beta": bool(w.beta and op == "post_ln"),
                    "per_gpu_rows": w.M, "parallelism": f"rows x{world}, no collective",
                    "l2": f"rotating {m['sets']} input/output sets of {m['set_bytes'] / 2**20:.0f} MiB "
                          f"(> 3x L2 between reuses)",
-                   "launch": f"CUDA graphs of {min(GRAPH_CHUNK, args.steps)} launches"},
+                   "launch": "eager" if args.eager else f"CUDA graphs of {min(GRAPH_CHUNK, args.steps)} launches"},
         "gpu_launches": args.steps,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": profiled_traffic(WORKLOAD),
-                     "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": nbytes},
+        "roofline": roof,
         "roofline_frac_of_config_bound": t_roof / t_step,
-        "norm_hidden_pct": hidden,
-        "unfused": {"t_plain_us": m["t_plain"] * 1e6, "t_norm_us": m["t_norm"] * 1e6,
-                    "t_fused_us": t_step * 1e6},
         "clocks": clocks,
         "device_status": int(status),
     }
+    if "t_norm" in m:
+        line["norm_hidden_pct"] = 100.0 * (m["t_plain"] + m["t_norm"] - m["t_fused"]) / m["t_norm"]
+        line["unfused"] = {"t_plain_us": m["t_plain"] * 1e6, "t_norm_us": m["t_norm"] * 1e6,
+                           "t_fused_us": t_step * 1e6}
     if status != 0:
         line["device_status_detail"] = detail
 
     if rank == 0:
-        e2e_steps = max(1, min(args.e2e_steps, args.steps))
-        sec, hb, db = e2e_measure(nf, w, dev, stream, e2e_steps)
-        line["e2e"] = {"value": world * w.flops * e2e_steps / sec / 1e12, "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": e2e_steps}
+        if not args.no_e2e and op == "post_ln":
+            e2e_steps = max(1, min(args.e2e_steps, args.steps))
+            sec, hb, db = e2e_measure(nf, w, dev, stream, e2e_steps)
+            line["e2e"] = {"value": world * w.flops * e2e_steps / sec / 1e12, "unit": "TFLOP/s",
+                           "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": e2e_steps}
         if not args.no_configs:
             table = []
             for name in nf_inputs.WORKLOAD_ORDER:
                 cw = nf_inputs.WORKLOADS[name]
-                for op in cw.ops:
+                for cop in cw.ops:
                     steps = 200 if cw.flops > 5e10 else 1000
-                    r = measure_workload(nf, cw, op, dev, stream, steps, 10)
-                    tr, nb = roofline_time(cw, op, hbm_gbs, bf16_tf)
+                    r = measure_workload(nf, cw, cop, dev, stream, steps, 10)
+                    tr, nb = roofline_time(cw, cop, hbm_gbs, bf16_tf)
                     table.append({
-                        "workload": name, "op": op, "t_fused_us": r["t_fused"] * 1e6,
+                        "workload": name, "op": cop, "t_fused_us": r["t_fused"] * 1e6,
                         "tflops": cw.flops / r["t_fused"] / 1e12,
                         "roofline_frac": tr / r["t_fused"],
                         "bound": "tensor" if cw.flops / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
                         "hbm_gbs": nb / r["t_fused"] / 1e9,
                         "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
+                        "norm_gbs": norm_bytes(r["norm_rows"], r["norm_cols"]) / r["t_norm"] / 1e9,
                         "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
                     })
+                    del r
+                    torch.cuda.empty_cache()
             line["configs"] = table
         if not args.no_cpu and world == 1:
-            flops, sec, rpp, thr = oracle_sample(w, "post_ln", budget_s=10.0)
+            cap = max(1, int(2e10 // (2 * w.N * w.K)))   # about 20 GFLOP per pass
+            flops, sec, rpp, thr = oracle_sample(w, op, budget_s=10.0, rows_cap=cap)
             line["cpu_baseline"] = {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": thr,
                                     "kind": "oracle",
-                                    "sample": f"full {w.M} x {w.K} x {w.N} workload, repeated for "
+                                    "sample": f"{rpp} of {w.M} rows of {w.M} x {w.K} x {w.N}, repeated for "
                                               f"{sec:.1f} s (fp64, OpenMP over rows)"}
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -75,6 +75,47 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                    "+r"(r[30]), "+r"(r[31]));
 }
 
+// Loads NC 32-column chunks of this thread's TMEM lane starting at `taddr`,
+// then waits once for all of them.
+template <int NC>
+__device__ __forceinline__ void tmem_load_seg(uint32_t taddr, uint32_t (&v)[NC][32]) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) tmem_ld32(taddr + static_cast<uint32_t>(c * 32), v[c]);
+    tmem_ld_wait(v[0]);
+#pragma unroll
+    for (int c = 1; c < NC; ++c) reg_fence(v[c]);
+}
+
+// 64 fp32 columns (two 32-column chunks) -> 32 packed bf16 pairs:
+// y = x * scale + bias, then y * gamma + beta when AFF (gamma / beta read as
+// bf16 from shared memory at saff_g / saff_b, 8 columns per 16-byte load).
+template <bool AFF>
+__device__ __forceinline__ void convert64(const uint32_t (&va)[32], const uint32_t (&vb)[32], float scale,
+                                          float bias, uint32_t saff_g, uint32_t saff_b, uint32_t (&pk)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t* src = q < 4 ? va : vb;
+        const int o = (q & 3) * 8;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(src[o + e]), scale, bias);
+        if (AFF) {
+            const uint4 g = ld_shared_v4(saff_g + static_cast<uint32_t>(q * 16));
+            const uint4 t = ld_shared_v4(saff_b + static_cast<uint32_t>(q * 16));
+            y[0] = fmaf(y[0], bf16lo(g.x), bf16lo(t.x));
+            y[1] = fmaf(y[1], bf16hi(g.x), bf16hi(t.x));
+            y[2] = fmaf(y[2], bf16lo(g.y), bf16lo(t.y));
+            y[3] = fmaf(y[3], bf16hi(g.y), bf16hi(t.y));
+            y[4] = fmaf(y[4], bf16lo(g.z), bf16lo(t.z));
+            y[5] = fmaf(y[5], bf16hi(g.z), bf16hi(t.z));
+            y[6] = fmaf(y[6], bf16lo(g.w), bf16lo(t.w));
+            y[7] = fmaf(y[7], bf16hi(g.w), bf16hi(t.w));
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[4 * q + e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
+    }
+}
+
 // Tile schedule: CTA-local tile index lt -> (m_tile, n_tile).
 struct TileSched {
     int first, step, count;  // m (clustered) or linear tile (unclustered) sequence
@@ -287,8 +328,16 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
         __syncwarp();
     } else if (warp < EPI_WARPS) {
         // ================================================================ epilogue
+        // The row is read from TMEM in segments of up to 128 columns (NC
+        // tcgen05.ld of 32 columns, one wait).  Post-norm keeps the last
+        // segment in registers across the statistics exchange, so each column
+        // leaves TMEM once when TILE_N <= 128 and 1.5 times when TILE_N = 256.
+        constexpr int SEG = TILE_N < 128 ? TILE_N : 128;
+        constexpr int NC = SEG / 32;
         const int row = warp * 32 + lane;  // tile row == TMEM lane
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        const bool affine = Cfg::kPost && (args.gamma != nullptr || args.beta != nullptr);
+        const uint32_t saff = smem_u32(aff);
         uint32_t store_count = 0;
         for (int lt = 0; lt < count; ++lt) {
             int m, n;
@@ -299,56 +348,64 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
-            const int nv = min(TILE_N, args.N - n * TILE_N);  // valid columns of this tile
-            const int grow = m * TILE_M + row;                 // global row
-            float mul = 1.0f, sub = 0.0f;                      // y = (acc - sub) * mul
+            const int nv = min(TILE_N, args.N - n * TILE_N);        // valid columns of this tile
+            const int nseg = (nv + SEG - 1) / SEG;                   // segments holding them
+            const int nstore = (m * TILE_M + warp * 32 < args.M) ? nv : 0;  // nothing past M
+            const int grow = m * TILE_M + row;                       // global row
+            float scale = 1.0f, bias = 0.0f;                         // y = acc * scale + bias
+            bool released = false;
+            uint32_t v[NC][32];
 
             if (Cfg::kPre) {
                 ok = mbar_wait(guard, bar_ssf0 + 8u * b, aph, SITE_EPI_SS_FULL, lt);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 // blog §2: rstd = rsqrt(square_sum / K + eps); acc *= rstd[:, None]
                 const float ss = ss_buf[b * TILE_M + row];
-                mul = rsqrtf(fmaf(ss, args.inv_len, args.eps));
-                if (n == 0 && args.rstd_out && grow < args.M) args.rstd_out[grow] = mul;
+                scale = rsqrtf(fmaf(ss, args.inv_len, args.eps));
+                if (n == 0 && args.rstd_out && grow < args.M) args.rstd_out[grow] = scale;
             }
 
             if (Cfg::kPost) {
-                // -- local statistics of this CTA's nv columns (blog §3: each
-                //    CTA reduces the partial row statistics of its tile)
-                float s1 = 0.0f;
-#pragma unroll 1
-                for (int c0 = 0; c0 < TILE_N; c0 += 32) {
-                    if (c0 >= nv) break;
-                    uint32_t v[32];
-                    tmem_ld32(tacc + c0, v);
-                    tmem_ld_wait(v);
+                // -- partial statistics of this CTA's nv columns (blog §3: each CTA
+                //    reduces the partial row statistics of its tile).  LayerNorm
+                //    uses sums shifted by the row's first value, sh, which keeps the
+                //    one-pass variance accurate; four accumulators break the chains.
+                float sh = 0.0f;
+                float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int sg = 0; sg < nseg; ++sg) {
+                    tmem_load_seg<NC>(tacc + sg * SEG, v);
+                    if (Cfg::kLN && sg == 0) sh = __uint_as_float(v[0][0]);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float x = __uint_as_float(v[j]);
-                        const float t = Cfg::kLN ? x : x * x;
-                        s1 += (c0 + j < nv) ? t : 0.0f;
-                    }
+                    for (int c = 0; c < NC; ++c)
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float x = __uint_as_float(v[c][j]);
+                            if (Cfg::kLN) {
+                                const float d = x - sh;
+                                a1[j & 3] += d;
+                                a2[j & 3] = fmaf(d, d, a2[j & 3]);
+                            } else {
+                                a2[j & 3] = fmaf(x, x, a2[j & 3]);
+                            }
+                        }
+                }
+                if (nseg == 1) {  // the row is in registers: TMEM buffer b is free
+                    tc_fence_before();
+                    mbar_arrive(bar_acce0 + 8u * b);
+                    released = true;
                 }
                 float pa, pb;  // partial: LN (mean_c, M2_c); RMS (sum of squares, 0)
                 if (Cfg::kLN) {
-                    const float mean_c = s1 / static_cast<float>(nv);
-                    float m2 = 0.0f;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < TILE_N; c0 += 32) {
-                        if (c0 >= nv) break;
-                        uint32_t v[32];
-                        tmem_ld32(tacc + c0, v);
-                        tmem_ld_wait(v);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float dlt = __uint_as_float(v[j]) - mean_c;
-                            m2 += (c0 + j < nv) ? dlt * dlt : 0.0f;
-                        }
-                    }
-                    pa = mean_c;
-                    pb = m2;
+                    // Columns past N inside the loaded segments hold exact zeros (W
+                    // is zero-filled there); each added -sh to a1 and sh^2 to a2.
+                    const float npad = static_cast<float>(nseg * SEG - nv);
+                    const float fnv = static_cast<float>(nv);
+                    const float s1 = (a1[0] + a1[1]) + (a1[2] + a1[3]) + npad * sh;
+                    const float s2 = (a2[0] + a2[1]) + (a2[2] + a2[3]) - npad * sh * sh;
+                    pa = sh + s1 / fnv;
+                    pb = fmaxf(s2 - s1 * (s1 / fnv), 0.0f);
                 } else {
-                    pa = s1;
+                    pa = (a2[0] + a2[1]) + (a2[2] + a2[3]);
                     pb = 0.0f;
                 }
 
@@ -393,59 +450,59 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                     sq = Cfg::kLN ? pb : pa;
                 }
                 // LayerNorm: (acc - mean) * rsqrt(M2/N + eps); RMSNorm: acc * rsqrt(ss/N + eps)
-                mul = rsqrtf(fmaf(sq, args.inv_len, args.eps));
-                sub = Cfg::kLN ? mean : 0.0f;
+                const float rstd = rsqrtf(fmaf(sq, args.inv_len, args.eps));
+                scale = rstd;
+                bias = Cfg::kLN ? -mean * rstd : 0.0f;
                 if (n == 0 && grow < args.M) {
                     if (Cfg::kLN && args.mean_out) args.mean_out[grow] = mean;
-                    if (args.rstd_out) args.rstd_out[grow] = mul;
+                    if (args.rstd_out) args.rstd_out[grow] = rstd;
                 }
             }
 
-            // -- normalize, convert, stage (128B swizzle) and store 64 columns at a time.
-            //    A warp whose 32 rows all lie past M has nothing to store.
-            const int nstore = (m * TILE_M + warp * 32 < args.M) ? nv : 0;
-#pragma unroll 1
-            for (int c0 = 0; c0 < TILE_N; c0 += STORE_COLS) {
-                if (c0 >= nstore) break;
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tacc + c0, v0);
-                tmem_ld32(tacc + c0 + 32, v1);
-                tmem_ld_wait(v0);
-                reg_fence(v1);
-                uint32_t pk[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const uint32_t* src = (j < 16) ? v0 : v1;
-                    const int jj = (j & 15) * 2;
-                    float y0 = (__uint_as_float(src[jj]) - sub) * mul;
-                    float y1 = (__uint_as_float(src[jj + 1]) - sub) * mul;
-                    if (Cfg::kPost) {
-                        const int c = c0 + 2 * j;
-                        const uint32_t g2 = *reinterpret_cast<const uint32_t*>(aff + c);
-                        const uint32_t b2 = *reinterpret_cast<const uint32_t*>(aff + TILE_N + c);
-                        y0 = fmaf(y0, bf16lo(g2), bf16lo(b2));
-                        y1 = fmaf(y1, bf16hi(g2), bf16hi(b2));
+            // -- normalize, convert, stage (128B swizzle) and store 64 columns at
+            //    a time.  Post-norm starts with the segment still in registers.
+            for (int k = 0; k < nseg; ++k) {
+                const int sg = Cfg::kPost ? nseg - 1 - k : k;
+                if (!(Cfg::kPost && k == 0)) {
+                    tmem_load_seg<NC>(tacc + sg * SEG, v);
+                    if (k == nseg - 1) {  // last TMEM read of this tile
+                        tc_fence_before();
+                        mbar_arrive(bar_acce0 + 8u * b);
+                        released = true;
                     }
-                    pk[j] = pack_bf16x2(y0, y1);
                 }
-                const uint32_t sb = sStg + static_cast<uint32_t>((warp * 2 + (store_count & 1u)) * STORE_BUF_BYTES);
-                ++store_count;
-                if (lane == 0) bulk_wait_read<1>();  // the store that used sb last has read it
-                __syncwarp();
-                const uint32_t rowp = sb + static_cast<uint32_t>(lane * 128);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    st_shared_v4(rowp + (static_cast<uint32_t>(q ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
-                                 pk[4 * q + 2], pk[4 * q + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmY, sb, n * TILE_N + c0, m * TILE_M + warp * 32);
-                    bulk_commit();
+                for (int q = 0; q < SEG / STORE_COLS; ++q) {
+                    const int c0 = sg * SEG + q * STORE_COLS;
+                    if (c0 >= nstore) break;
+                    uint32_t pk[32];
+                    if (affine)
+                        convert64<true>(v[2 * q], v[2 * q + 1], scale, bias, saff + c0 * 2,
+                                        saff + (TILE_N + c0) * 2, pk);
+                    else
+                        convert64<false>(v[2 * q], v[2 * q + 1], scale, bias, 0, 0, pk);
+                    const uint32_t sb =
+                        sStg + static_cast<uint32_t>((warp * 2 + (store_count & 1u)) * STORE_BUF_BYTES);
+                    ++store_count;
+                    if (lane == 0) bulk_wait_read<1>();  // the store that used sb last has read it
+                    __syncwarp();
+                    const uint32_t rowp = sb + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        st_shared_v4(rowp + (static_cast<uint32_t>(e ^ (lane & 7)) << 4), pk[4 * e],
+                                     pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, sb, n * TILE_N + c0, m * TILE_M + warp * 32);
+                        bulk_commit();
+                    }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar_acce0 + 8u * b);  // TMEM buffer b may be overwritten
+            if (!released) {
+                tc_fence_before();
+                mbar_arrive(bar_acce0 + 8u * b);  // TMEM buffer b may be overwritten
+            }
         }
         if (lane == 0) bulk_wait_all<0>();
         __syncwarp();
