@@ -147,6 +147,12 @@ nf_status nf_clear_device_status(void);
  * its tensor memory and returns; the CUDA context stays usable. */
 nf_status nf_set_wait_timeout_ns(uint64_t ns);
 
+/* Programmatic dependent launch (default on): each kernel may be scheduled
+ * while the kernel before it on the stream finishes; it performs its set-up
+ * (barriers, tensor memory) and then waits for that kernel to complete before
+ * touching global memory, so results are unchanged.  0 turns it off. */
+nf_status nf_set_launch_overlap(int enable);
+
 /* Self-test of the time limit: launches one CTA that waits on a barrier no
  * thread ever arrives on, with limit `timeout_ns` (1e3..1e10).  After the
  * stream completes, nf_get_device_status() reports NF_ERR_TIMEOUT. */

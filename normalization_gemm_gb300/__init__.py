@@ -65,6 +65,7 @@ _SIGS = {
     "nf_get_device_status": [_VP],
     "nf_clear_device_status": [],
     "nf_set_wait_timeout_ns": [ctypes.c_uint64],
+    "nf_set_launch_overlap": [ctypes.c_int],
     "nf_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "nf_plan_gemm": [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(NFPlan)],
     "nf_abi_version": [],
@@ -237,6 +238,11 @@ def clear_device_status() -> None:
 
 def set_wait_timeout_ns(ns: int) -> None:
     _check(lib().nf_set_wait_timeout_ns(int(ns)), "nf_set_wait_timeout_ns")
+
+
+def set_launch_overlap(enable: bool) -> None:
+    """Programmatic dependent launch on (default) or off."""
+    _check(lib().nf_set_launch_overlap(1 if enable else 0), "nf_set_launch_overlap")
 
 
 def selftest_wait_timeout(ns: int, stream=None) -> None:

@@ -56,6 +56,10 @@ __global__ void nf_selftest_wait_kernel(uint32_t* status, uint64_t timeout_ns) {
 }
 
 uint64_t g_timeout_ns = 2000000000ull;
+// Programmatic dependent launch: a kernel's prologue may overlap the tail of
+// the kernel before it on the stream (it waits in griddepcontrol.wait before
+// touching global memory).
+bool g_overlap = true;
 std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
@@ -312,19 +316,26 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     }
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(p.v->threads));
     cfg.dynamicSmemBytes = static_cast<size_t>(p.v->smem_bytes);
     cfg.stream = stream;
     if (p.clustered) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
     }
+    if (g_overlap) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = nattr ? attr : nullptr;
+    cfg.numAttrs = static_cast<unsigned>(nattr);
     void* kargs[4] = {&tmX, &tmW, &tmY, &a};
     cudaError_t e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
@@ -394,7 +405,7 @@ nf_status nf_norm_rows(const void* in, void* out, const void* gamma, const void*
     a.inv_cols = 1.0f / static_cast<float>(cols);
     a.mean_out = mean_out;
     a.rstd_out = rstd_out;
-    cudaError_t e = launch_norm_rows(a, kind, d->sm_count, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_norm_rows(a, kind, d->sm_count, g_overlap, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "norm_rows launch");
     return NF_OK;
 }
@@ -427,6 +438,11 @@ nf_status nf_clear_device_status(void) {
 nf_status nf_set_wait_timeout_ns(uint64_t ns) {
     if (ns < 1000ull || ns > 100000000000ull) return fail(NF_ERR_INVALID_ARG, "timeout must be in [1e3, 1e11] ns");
     g_timeout_ns = ns;
+    return NF_OK;
+}
+
+nf_status nf_set_launch_overlap(int enable) {
+    g_overlap = enable != 0;
     return NF_OK;
 }
 

@@ -220,6 +220,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
         tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
         tmem_relinquish();
     }
+    // Everything above may overlap the tail of a preceding grid launched with
+    // programmatic serialization; global memory is touched only after this.
+    griddep_wait();
+    griddep_launch_dependents();
     if (Cfg::kPost && threadIdx.x < 128) {
         // This CTA's columns never change: clustered CTAs keep their rank's
         // tile, unclustered post-norm has a single column tile.

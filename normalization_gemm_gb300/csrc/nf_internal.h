@@ -124,7 +124,7 @@ struct NormArgs {
 };
 
 // Picks the variant for `cols` and launches it; returns the CUDA status.
-cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, cudaStream_t stream);
+cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, bool overlap, cudaStream_t stream);
 // Largest supported cols.
 constexpr int NORM_MAX_COLS = 16384;
 

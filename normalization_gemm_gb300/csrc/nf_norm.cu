@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
     const int chunks = a.cols >> 3;
     const uint4* in = reinterpret_cast<const uint4*>(a.in);
     uint4* out = reinterpret_cast<uint4*>(a.out);
+    griddep_wait();  // inputs may come from the kernel launched just before
+    griddep_launch_dependents();
 
     // This thread always owns chunks t, t+TPR, ...: load its gamma / beta once.
     float g[CPT][8], bb[CPT][8];
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
 }
 
 template <int TPR, int CPT, int KIND>
-cudaError_t launch_one(const NormArgs& a, int sm_count, cudaStream_t stream) {
+cudaError_t launch_one(const NormArgs& a, int sm_count, bool overlap, cudaStream_t stream) {
     auto kern = nf_norm_rows_kernel<TPR, CPT, KIND>;
     constexpr int RPB = NORM_THREADS / TPR;
     static int per_sm = 0;  // occupancy of this variant, queried once
@@ -158,30 +160,40 @@ cudaError_t launch_one(const NormArgs& a, int sm_count, cudaStream_t stream) {
     const int64_t steps = (a.rows + RPB - 1) / RPB;
     const int64_t cap = static_cast<int64_t>(sm_count) * per_sm;
     const int grid = static_cast<int>(steps < cap ? steps : cap);
-    kern<<<grid, NORM_THREADS, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NORM_THREADS);
+    cfg.stream = stream;
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <int KIND>
-cudaError_t dispatch(const NormArgs& a, int sm_count, cudaStream_t stream) {
+cudaError_t dispatch(const NormArgs& a, int sm_count, bool overlap, cudaStream_t stream) {
     const int chunks = a.cols >> 3;
     // TPR: the smallest power of two with TPR * 4 >= chunks (at most 256).
-    if (chunks <= 4) return launch_one<1, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 8) return launch_one<2, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 16) return launch_one<4, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 32) return launch_one<8, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 64) return launch_one<16, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 128) return launch_one<32, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 256) return launch_one<64, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 512) return launch_one<128, 4, KIND>(a, sm_count, stream);
-    if (chunks <= 1024) return launch_one<256, 4, KIND>(a, sm_count, stream);
-    return launch_one<256, 8, KIND>(a, sm_count, stream);  // cols <= 16384
+    if (chunks <= 4) return launch_one<1, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 8) return launch_one<2, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 16) return launch_one<4, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 32) return launch_one<8, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 64) return launch_one<16, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 128) return launch_one<32, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 256) return launch_one<64, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 512) return launch_one<128, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 1024) return launch_one<256, 4, KIND>(a, sm_count, overlap, stream);
+    return launch_one<256, 8, KIND>(a, sm_count, overlap, stream);  // cols <= 16384
 }
 
 }  // namespace
 
-cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, cudaStream_t stream) {
-    return kind == 0 ? dispatch<0>(a, sm_count, stream) : dispatch<1>(a, sm_count, stream);
+cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, bool overlap, cudaStream_t stream) {
+    return kind == 0 ? dispatch<0>(a, sm_count, overlap, stream) : dispatch<1>(a, sm_count, overlap, stream);
 }
 
 }  // namespace nf

@@ -48,11 +48,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
         : "memory");
 }
 
+// The waiting thread sleeps until the phase completes (or about 1 ms passes,
+// after which the caller re-checks its time limit).  Without the hint the
+// hardware wakes the thread at short intervals, which measurably slows the
+// single-thread producer / MMA loops.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -61,7 +65,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Same, with cluster-scope acquire: for phases completed by other CTAs'
-// st.async writes into this CTA's shared memory.
+// st.async writes into this CTA's shared memory (no suspend hint: measured
+// faster for the cross-CTA exchange).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -108,6 +113,17 @@ __device__ __forceinline__ bool mbar_wait(const WaitGuard& g, uint32_t bar, uint
             return false;
         }
     }
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// Blocks until every grid this one depends on has completed and its memory is
+// visible (a no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets a grid launched after this one with programmatic serialization start
+// its prologue; it still waits in griddep_wait() for this grid to finish.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ TMA

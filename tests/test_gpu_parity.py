@@ -305,3 +305,34 @@ def test_wait_timeout_is_reported_not_hung(dev):
     y = nf.gemm_plain(to_dev(inp["X"], dev), to_dev(inp["W"], dev))
     torch.cuda.synchronize()
     assert bool(torch.isfinite(y.float()).all())
+
+
+def test_launch_overlap_keeps_dependent_chains_exact(dev):
+    """Programmatic dependent launch: each kernel below reads the previous one's
+    output.  With the overlap on, every result must be bit-identical to the
+    serialized run (griddepcontrol.wait precedes every global access)."""
+    import torch
+    inp = _inputs(4096, 256, 256, seed=43, gamma=True, beta=True)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    G, B = to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev)
+
+    def chain():
+        outs = []
+        y = X
+        for i in range(6):
+            y = nf.gemm_postnorm_ln(y, W, 1e-5, G, B) if i % 3 == 0 else (
+                nf.gemm_prenorm_rms(y, W, 1e-6) if i % 3 == 1 else nf.norm_rows(nf.gemm_plain(y, W), 0, 1e-5))
+            outs.append(y)
+        torch.cuda.synchronize()
+        return outs
+
+    try:
+        nf.set_launch_overlap(False)
+        ref = chain()
+        nf.set_launch_overlap(True)
+        for _ in range(3):
+            got = chain()
+            for a, b in zip(ref, got):
+                assert torch.equal(a, b)
+    finally:
+        nf.set_launch_overlap(True)
