@@ -93,7 +93,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     from normalization_gemm_gb300 import _build
-    return _build._stamp(())[:16]
+    return _build.source_hash()
 
 
 def profiled_traffic(workload: str):

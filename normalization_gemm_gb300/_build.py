@@ -40,8 +40,15 @@ def _stamp(extra_flags) -> str:
             if name.endswith((".cu", ".cuh", ".h")):
                 with open(os.path.join(d, name), "rb") as fh:
                     h.update(name.encode() + fh.read())
-    h.update(" ".join(NVCC_FLAGS + list(extra_flags)).encode())
+    # flags without the machine-specific include paths
+    flags = [f for f in NVCC_FLAGS + list(extra_flags) if not os.path.isabs(f)]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
+
+
+def source_hash() -> str:
+    """Short hash of the CUDA sources, headers and flags (path independent)."""
+    return _stamp(())[:16]
 
 
 def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
