@@ -10,15 +10,16 @@
 // Attention Kernels".
 //
 // CTA roles (one CTA per SM, persistent over output tiles):
-//   warps 0-3  epilogue: warp w reads TMEM lanes 32w..32w+31, i.e. tile rows
-//              32w..32w+31, one row per thread; normalizes; stores through a
+//   warps 0-7  epilogue, two warpgroups that alternate tiles: warp w of group
+//              g = w / 4 reads TMEM lanes 32(w%4)..+31 of accumulator g, i.e.
+//              one tile row per thread; normalizes; stores through a
 //              128B-swizzled staging buffer with TMA, once per element.
-//   warp 4     TMA producer (one elected lane): X and W K-tiles into a ring of
+//   warp 8     TMA producer (one elected lane): X and W K-tiles into a ring of
 //              STAGES shared-memory stages.
-//   warp 5     MMA issuer (one elected lane): tcgen05.mma 128 x TILE_N x 16
+//   warp 9     MMA issuer (one elected lane): tcgen05.mma 128 x TILE_N x 16
 //              into one of two TMEM accumulators (double buffered so that the
 //              epilogue of tile t overlaps the main loop of tile t+1).
-//   warps 6-9  (pre-norm only) sum of squares of each X row, read from the
+//   warps 10-13 (pre-norm only) sum of squares of each X row, read from the
 //              same shared-memory stage the tensor cores consume, on CUDA
 //              cores, in parallel with the MMA (blog §2 pseudocode:
 //              square_sum += (tile_A * tile_A).sum(-1)).
@@ -89,30 +90,31 @@ __device__ __forceinline__ void tmem_load_seg(uint32_t taddr, uint32_t (&v)[NC][
 // 64 fp32 columns (two 32-column chunks) -> 32 packed bf16 pairs:
 // y = x * scale + bias, then y * gamma + beta when AFF (gamma / beta read as
 // bf16 from shared memory at saff_g / saff_b, 8 columns per 16-byte load).
+// Works on fp32 pairs: one f32x2 FMA per two columns.
 template <bool AFF>
-__device__ __forceinline__ void convert64(const uint32_t (&va)[32], const uint32_t (&vb)[32], float scale,
-                                          float bias, uint32_t saff_g, uint32_t saff_b, uint32_t (&pk)[32]) {
+__device__ __forceinline__ void convert64(const uint32_t (&va)[32], const uint32_t (&vb)[32], uint64_t scale2,
+                                          uint64_t bias2, uint32_t saff_g, uint32_t saff_b, uint32_t (&pk)[32]) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const uint32_t* src = q < 4 ? va : vb;
         const int o = (q & 3) * 8;
-        float y[8];
+        uint64_t y[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = fmaf(__uint_as_float(src[o + e]), scale, bias);
+        for (int e = 0; e < 4; ++e) y[e] = f2_fma(f2_pack(src[o + 2 * e], src[o + 2 * e + 1]), scale2, bias2);
         if (AFF) {
             const uint4 g = ld_shared_v4(saff_g + static_cast<uint32_t>(q * 16));
             const uint4 t = ld_shared_v4(saff_b + static_cast<uint32_t>(q * 16));
-            y[0] = fmaf(y[0], bf16lo(g.x), bf16lo(t.x));
-            y[1] = fmaf(y[1], bf16hi(g.x), bf16hi(t.x));
-            y[2] = fmaf(y[2], bf16lo(g.y), bf16lo(t.y));
-            y[3] = fmaf(y[3], bf16hi(g.y), bf16hi(t.y));
-            y[4] = fmaf(y[4], bf16lo(g.z), bf16lo(t.z));
-            y[5] = fmaf(y[5], bf16hi(g.z), bf16hi(t.z));
-            y[6] = fmaf(y[6], bf16lo(g.w), bf16lo(t.w));
-            y[7] = fmaf(y[7], bf16hi(g.w), bf16hi(t.w));
+            y[0] = f2_fma(y[0], bf16x2_to_f2(g.x), bf16x2_to_f2(t.x));
+            y[1] = f2_fma(y[1], bf16x2_to_f2(g.y), bf16x2_to_f2(t.y));
+            y[2] = f2_fma(y[2], bf16x2_to_f2(g.z), bf16x2_to_f2(t.z));
+            y[3] = f2_fma(y[3], bf16x2_to_f2(g.w), bf16x2_to_f2(t.w));
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) pk[4 * q + e] = pack_bf16x2(y[2 * e], y[2 * e + 1]);
+        for (int e = 0; e < 4; ++e) {
+            float lo, hi;
+            f2_unpack(y[e], lo, hi);
+            pk[4 * q + e] = pack_bf16x2(lo, hi);
+        }
     }
 }
 
@@ -332,18 +334,21 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
         __syncwarp();
     } else if (warp < EPI_WARPS) {
         // ================================================================ epilogue
-        // The row is read from TMEM in segments of up to 128 columns (NC
-        // tcgen05.ld of 32 columns, one wait).  Post-norm keeps the last
-        // segment in registers across the statistics exchange, so each column
-        // leaves TMEM once when TILE_N <= 128 and 1.5 times when TILE_N = 256.
-        constexpr int SEG = TILE_N < 128 ? TILE_N : 128;
+        // Two warpgroups alternate tiles: group g drains TMEM accumulator g, so
+        // each group has two tiles' time for its chain of TMEM reads,
+        // statistics, conversion and stores.  Warp (g, qtr) owns TMEM lane
+        // quarter qtr (tile rows 32 qtr .. +31, one row per thread).  The row is
+        // read in segments of 64 columns (two tcgen05.ld, one wait); post-norm
+        // keeps the last segment in registers across the statistics exchange.
+        constexpr int SEG = TILE_N < 64 ? TILE_N : 64;
         constexpr int NC = SEG / 32;
-        const int row = warp * 32 + lane;  // tile row == TMEM lane
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        const int grp = warp >> 2;
+        const int qtr = warp & 3;
+        const int row = qtr * 32 + lane;  // tile row == TMEM lane
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qtr * 32) << 16);
         const bool affine = Cfg::kPost && (args.gamma != nullptr || args.beta != nullptr);
         const uint32_t saff = smem_u32(aff);
-        uint32_t store_count = 0;
-        for (int lt = 0; lt < count; ++lt) {
+        for (int lt = grp; lt < count; lt += 2) {
             int m, n;
             sched.tile(lt, m, n);
             const int b = lt & 1;
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
             const int nv = min(TILE_N, args.N - n * TILE_N);        // valid columns of this tile
             const int nseg = (nv + SEG - 1) / SEG;                   // segments holding them
-            const int nstore = (m * TILE_M + warp * 32 < args.M) ? nv : 0;  // nothing past M
+            const int nstore = (m * TILE_M + qtr * 32 < args.M) ? nv : 0;  // nothing past M
             const int grow = m * TILE_M + row;                       // global row
             float scale = 1.0f, bias = 0.0f;                         // y = acc * scale + bias
             bool released = false;
@@ -374,22 +379,24 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                 //    reduces the partial row statistics of its tile).  LayerNorm
                 //    uses sums shifted by the row's first value, sh, which keeps the
                 //    one-pass variance accurate; four accumulators break the chains.
+                // Column pairs go through f32x2 instructions; four pair accumulators.
                 float sh = 0.0f;
-                float a1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, a2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                uint64_t a1[4] = {0, 0, 0, 0}, a2[4] = {0, 0, 0, 0};
                 for (int sg = 0; sg < nseg; ++sg) {
                     tmem_load_seg<NC>(tacc + sg * SEG, v);
                     if (Cfg::kLN && sg == 0) sh = __uint_as_float(v[0][0]);
+                    const uint64_t sh2 = f2_splat(sh);
 #pragma unroll
                     for (int c = 0; c < NC; ++c)
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float x = __uint_as_float(v[c][j]);
+                        for (int i = 0; i < 16; ++i) {
+                            const uint64_t x2 = f2_pack(v[c][2 * i], v[c][2 * i + 1]);
                             if (Cfg::kLN) {
-                                const float d = x - sh;
-                                a1[j & 3] += d;
-                                a2[j & 3] = fmaf(d, d, a2[j & 3]);
+                                const uint64_t d2 = f2_sub(x2, sh2);
+                                a1[i & 3] = f2_add(a1[i & 3], d2);
+                                a2[i & 3] = f2_fma(d2, d2, a2[i & 3]);
                             } else {
-                                a2[j & 3] = fmaf(x, x, a2[j & 3]);
+                                a2[i & 3] = f2_fma(x2, x2, a2[i & 3]);
                             }
                         }
                 }
@@ -403,13 +410,14 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                     // Columns past N inside the loaded segments hold exact zeros (W
                     // is zero-filled there); each added -sh to a1 and sh^2 to a2.
                     const float npad = static_cast<float>(nseg * SEG - nv);
-                    const float fnv = static_cast<float>(nv);
-                    const float s1 = (a1[0] + a1[1]) + (a1[2] + a1[3]) + npad * sh;
-                    const float s2 = (a2[0] + a2[1]) + (a2[2] + a2[3]) - npad * sh * sh;
-                    pa = sh + s1 / fnv;
-                    pb = fmaxf(s2 - s1 * (s1 / fnv), 0.0f);
+                    const float inv_nv = 1.0f / static_cast<float>(nv);
+                    const float s1 = f2_hsum(f2_add(f2_add(a1[0], a1[1]), f2_add(a1[2], a1[3]))) + npad * sh;
+                    const float s2 = f2_hsum(f2_add(f2_add(a2[0], a2[1]), f2_add(a2[2], a2[3]))) - npad * sh * sh;
+                    const float d1 = s1 * inv_nv;
+                    pa = sh + d1;
+                    pb = fmaxf(fmaf(-s1, d1, s2), 0.0f);
                 } else {
-                    pa = (a2[0] + a2[1]) + (a2[2] + a2[3]);
+                    pa = f2_hsum(f2_add(f2_add(a2[0], a2[1]), f2_add(a2[2], a2[3])));
                     pb = 0.0f;
                 }
 
@@ -428,7 +436,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                     // Re-arm for local tile lt + 2.  Its data can arrive only after
                     // every CTA of the cluster got this CTA's tile lt+1 partials,
                     // which are sent after this point.
-                    if (threadIdx.x == 0 && lt + 2 < count) mbar_arrive_expect_tx(xbar, xch_bytes);
+                    if (qtr == 0 && lane == 0 && lt + 2 < count) mbar_arrive_expect_tx(xbar, xch_bytes);
                     const float* recv = reinterpret_cast<const float*>(
                         base_ptr + Cfg::OFF_RECV + (b * MAX_CLUSTER * TILE_M + row) * 8);
                     if (Cfg::kLN) {
@@ -475,30 +483,40 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                         released = true;
                     }
                 }
-#pragma unroll
-                for (int q = 0; q < SEG / STORE_COLS; ++q) {
-                    const int c0 = sg * SEG + q * STORE_COLS;
-                    if (c0 >= nstore) break;
-                    uint32_t pk[32];
-                    if (affine)
-                        convert64<true>(v[2 * q], v[2 * q + 1], scale, bias, saff + c0 * 2,
-                                        saff + (TILE_N + c0) * 2, pk);
-                    else
-                        convert64<false>(v[2 * q], v[2 * q + 1], scale, bias, 0, 0, pk);
-                    const uint32_t sb =
-                        sStg + static_cast<uint32_t>((warp * 2 + (store_count & 1u)) * STORE_BUF_BYTES);
-                    ++store_count;
-                    if (lane == 0) bulk_wait_read<1>();  // the store that used sb last has read it
+                // The segment's 64-column box goes through this warp's staging
+                // buffer (128B swizzle) and one TMA store.
+                constexpr int NQ = SEG / STORE_COLS;
+                const int cs = sg * SEG;
+                if (cs < nstore) {
+                    const uint64_t scale2 = f2_splat(scale), bias2 = f2_splat(bias);
+                    if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
                     __syncwarp();
-                    const uint32_t rowp = sb + static_cast<uint32_t>(lane * 128);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        st_shared_v4(rowp + (static_cast<uint32_t>(e ^ (lane & 7)) << 4), pk[4 * e],
-                                     pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    for (int q = 0; q < NQ; ++q) {
+                        const int c0 = cs + q * STORE_COLS;
+                        if (c0 < nstore) {
+                            uint32_t pk[32];
+                            if (affine)
+                                convert64<true>(v[2 * q], v[2 * q + 1], scale2, bias2, saff + c0 * 2,
+                                                saff + (TILE_N + c0) * 2, pk);
+                            else
+                                convert64<false>(v[2 * q], v[2 * q + 1], scale2, bias2, 0, 0, pk);
+                            const uint32_t rowp = sStg + static_cast<uint32_t>((warp + q) * STORE_BUF_BYTES) +
+                                                  static_cast<uint32_t>(lane * 128);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                st_shared_v4(rowp + (static_cast<uint32_t>(e ^ (lane & 7)) << 4), pk[4 * e],
+                                             pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        }
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmY, sb, n * TILE_N + c0, m * TILE_M + warp * 32);
+#pragma unroll
+                        for (int q = 0; q < NQ; ++q)
+                            if (cs + q * STORE_COLS < nstore)
+                                tma_store_2d(&tmY, sStg + static_cast<uint32_t>((warp + q) * STORE_BUF_BYTES),
+                                             n * TILE_N + cs + q * STORE_COLS, m * TILE_M + qtr * 32);
                         bulk_commit();
                     }
                 }

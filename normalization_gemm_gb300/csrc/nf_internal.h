@@ -15,11 +15,11 @@ constexpr int UMMA_K = 16;                // K per tcgen05.mma of kind::f16
 constexpr int B_BOX_N = 64;               // W is loaded as 64-column boxes (128 bytes per K row)
 constexpr int A_STAGE_BYTES = TILE_M * TILE_K * 2;   // 16 KB
 constexpr int B_BOX_BYTES = TILE_K * B_BOX_N * 2;    // 8 KB
-constexpr int EPI_WARPS = 4;              // epilogue warps 0-3 own TMEM lane quarters 0-3
+constexpr int EPI_WARPS = 8;              // two warpgroups of 4: group g drains accumulator g
 constexpr int STORE_COLS = 64;            // Y store box: 64 columns x 32 rows (one warp)
 constexpr int STORE_ROWS = 32;
 constexpr int STORE_BUF_BYTES = STORE_COLS * STORE_ROWS * 2;              // 4 KB
-constexpr int STAGING_BYTES = EPI_WARPS * 2 * STORE_BUF_BYTES;             // double buffered
+constexpr int STAGING_BYTES = EPI_WARPS * STORE_BUF_BYTES;                 // one box per warp
 constexpr int MAX_CLUSTER = 16;           // post-norm: N <= 256 x 16
 constexpr int SMEM_OPTIN_LIMIT = 232448;  // 227 KB of dynamic shared memory per block
 constexpr int MAX_STAGES = 8;
@@ -60,10 +60,10 @@ struct GemmCfg {
     static_assert(OFF_B % 1024 == 0 && OFF_STG % 1024 == 0, "swizzled buffers need 1 KB alignment");
     static_assert(NUM_BARRIER_SLOTS * 8 + 8 <= BAR_BYTES, "barrier area");
 
-    static constexpr int PRODUCER_WARP = 4;
-    static constexpr int MMA_WARP = 5;
-    static constexpr int SUMSQ_WARP0 = 6;                 // pre-norm only: warps 6-9
-    static constexpr int THREADS = kPre ? 320 : 192;
+    static constexpr int PRODUCER_WARP = EPI_WARPS;       // 8
+    static constexpr int MMA_WARP = EPI_WARPS + 1;        // 9
+    static constexpr int SUMSQ_WARP0 = EPI_WARPS + 2;     // pre-norm only: warps 10-13
+    static constexpr int THREADS = (kPre ? EPI_WARPS + 6 : EPI_WARPS + 2) * 32;
     static constexpr int TMEM_COLS = 2 * TILE_N;           // two accumulator buffers
 };
 

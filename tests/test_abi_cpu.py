@@ -91,7 +91,7 @@ def test_plans(L, op, M, N, K, tile_n, cluster):
     assert cluster * tile_n >= N or op in (0, 1)
     assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
     assert p["tmem_cols"] == 2 * tile_n
-    assert p["threads"] == (320 if op == 1 else 192)
+    assert p["threads"] == (448 if op == 1 else 320)
     m_tiles = -(-M // 128)
     n_tiles = 1 if op >= 2 else -(-N // tile_n)
     assert p["tiles"] == m_tiles * n_tiles
