@@ -190,6 +190,22 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, Plan* p) {
     return NF_OK;
 }
 
+// Memory-bound shapes (short K) whose last, partial wave holds at most half
+// a wave of tiles: cut each of those tiles into two 64-row units so that the
+// wave spreads over twice as many SMs.  (A half still runs the full MMA, so
+// tensor-bound shapes gain nothing and keep whole tiles.)
+void split_last_wave(int tiles, int grid, int k_tiles, int32_t* units, int32_t* split_base) {
+    *units = tiles;
+    *split_base = tiles;
+    if (k_tiles > 4 || tiles <= grid) return;
+    const int full = (tiles / grid) * grid;
+    const int rest = tiles - full;
+    if (rest > 0 && 2 * rest <= grid) {
+        *split_base = full;
+        *units = full + 2 * rest;
+    }
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 nf_status check_gemm_args(int op, const void* X, const void* W, const void* Y, const void* gamma, const void* beta,
@@ -306,6 +322,8 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.timeout_ns = g_timeout_ns;
 
     int grid = 0;
+    a.units = p.m_tiles * p.n_tiles;
+    a.split_base = a.units;
     if (p.clustered) {
         int mc = 0;
         if ((st = max_clusters(d, p.v, p.cluster, &mc)) != NF_OK) return st;
@@ -313,6 +331,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     } else {
         const int tiles = p.m_tiles * p.n_tiles;
         grid = tiles < d->sm_count ? tiles : d->sm_count;
+        split_last_wave(tiles, grid, p.k_tiles, &a.units, &a.split_base);
     }
 
     cudaLaunchConfig_t cfg = {};

@@ -118,21 +118,36 @@ __device__ __forceinline__ void convert64(const uint32_t (&va)[32], const uint32
     }
 }
 
-// Tile schedule: CTA-local tile index lt -> (m_tile, n_tile).
+// Tile schedule: CTA-local work unit lt -> (m_tile, n_tile, first row, rows).
+// Unclustered launches walk linear units; units from split_base on are the
+// tiles of the last, partial wave cut into two 64-row halves, so that wave
+// spreads over twice as many SMs.  A half still runs the 128-row MMA (the X
+// box simply starts 64 rows further for the second half); only its own 64
+// rows are stored.
 struct TileSched {
-    int first, step, count;  // m (clustered) or linear tile (unclustered) sequence
+    int first, step, count;  // m (clustered) or linear unit (unclustered) sequence
     int n_fixed;             // clustered: this CTA's n tile (its cluster rank)
     int n_tiles;
+    int split_base;          // first half-tile unit (unclustered)
     bool clustered;
-    __device__ __forceinline__ void tile(int lt, int& m, int& n) const {
-        const int t = first + lt * step;
+    __device__ __forceinline__ void tile(int lt, int& m, int& n, int& row0, int& rows) const {
+        const int u = first + lt * step;
         if (clustered) {
-            m = t;
+            m = u;
             n = n_fixed;
-        } else {
-            m = t / n_tiles;
-            n = t - m * n_tiles;
+            row0 = m * TILE_M;
+            rows = TILE_M;
+            return;
         }
+        int t = u, half = -1;
+        if (u >= split_base) {
+            t = split_base + ((u - split_base) >> 1);
+            half = (u - split_base) & 1;
+        }
+        m = t / n_tiles;
+        n = t - m * n_tiles;
+        row0 = m * TILE_M + (half == 1 ? TILE_M / 2 : 0);
+        rows = half < 0 ? TILE_M : TILE_M / 2;
     }
 };
 
@@ -185,13 +200,14 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
         sched.count = cid < args.m_tiles ? (args.m_tiles - cid + ncl - 1) / ncl : 0;
         sched.n_fixed = my_rank;
     } else {
-        const int total = args.m_tiles * args.n_tiles;
+        const int total = args.units;
         const int b = static_cast<int>(blockIdx.x);
         const int g = static_cast<int>(gridDim.x);
         sched.first = b;
         sched.step = g;
         sched.count = b < total ? (total - b + g - 1) / g : 0;
         sched.n_fixed = 0;
+        sched.split_base = args.split_base;
     }
     const int count = sched.count;
     const int k_tiles = args.k_tiles;
@@ -256,8 +272,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             uint32_t issued = 0;
             bool ok = true;
             for (int lt = 0; lt < count && ok; ++lt) {
-                int m, n;
-                sched.tile(lt, m, n);
+                int m, n, row0, rows;
+                sched.tile(lt, m, n, row0, rows);
                 for (int kt = 0; kt < k_tiles; ++kt) {
                     if (!mbar_wait(guard, bar_empty0 + 8u * s, ph ^ 1u, SITE_PROD_EMPTY, lt)) {
                         ok = false;
@@ -265,7 +281,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                     }
                     const uint32_t fb = bar_full0 + 8u * s;
                     mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                    tma_load_2d(sA + s * A_STAGE_BYTES, &tmX, fb, kt * TILE_K, m * TILE_M);
+                    tma_load_2d(sA + s * A_STAGE_BYTES, &tmX, fb, kt * TILE_K, row0);
 #pragma unroll
                     for (int i = 0; i < NBOX; ++i)
                         tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb,
@@ -349,8 +365,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
         const bool affine = Cfg::kPost && (args.gamma != nullptr || args.beta != nullptr);
         const uint32_t saff = smem_u32(aff);
         for (int lt = grp; lt < count; lt += 2) {
-            int m, n;
-            sched.tile(lt, m, n);
+            int m, n, row0, rows;
+            sched.tile(lt, m, n, row0, rows);
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
             bool ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
@@ -359,8 +375,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
             const int nv = min(TILE_N, args.N - n * TILE_N);        // valid columns of this tile
             const int nseg = (nv + SEG - 1) / SEG;                   // segments holding them
-            const int nstore = (m * TILE_M + qtr * 32 < args.M) ? nv : 0;  // nothing past M
-            const int grow = m * TILE_M + row;                       // global row
+            // Store only this unit's rows, and nothing past M.
+            const int nstore = (qtr * 32 < rows && row0 + qtr * 32 < args.M) ? nv : 0;
+            const int grow = row0 + row;                             // global row
+            const bool own_row = row < rows && grow < args.M;
             float scale = 1.0f, bias = 0.0f;                         // y = acc * scale + bias
             bool released = false;
             uint32_t v[NC][32];
@@ -371,7 +389,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                 // blog §2: rstd = rsqrt(square_sum / K + eps); acc *= rstd[:, None]
                 const float ss = ss_buf[b * TILE_M + row];
                 scale = rsqrtf(fmaf(ss, args.inv_len, args.eps));
-                if (n == 0 && args.rstd_out && grow < args.M) args.rstd_out[grow] = scale;
+                if (n == 0 && args.rstd_out && own_row) args.rstd_out[grow] = scale;
             }
 
             if (Cfg::kPost) {
@@ -465,7 +483,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                 const float rstd = rsqrtf(fmaf(sq, args.inv_len, args.eps));
                 scale = rstd;
                 bias = Cfg::kLN ? -mean * rstd : 0.0f;
-                if (n == 0 && grow < args.M) {
+                if (n == 0 && own_row) {
                     if (Cfg::kLN && args.mean_out) args.mean_out[grow] = mean;
                     if (args.rstd_out) args.rstd_out[grow] = rstd;
                 }
@@ -516,7 +534,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                         for (int q = 0; q < NQ; ++q)
                             if (cs + q * STORE_COLS < nstore)
                                 tma_store_2d(&tmY, sStg + static_cast<uint32_t>((warp + q) * STORE_BUF_BYTES),
-                                             n * TILE_N + cs + q * STORE_COLS, m * TILE_M + qtr * 32);
+                                             n * TILE_N + cs + q * STORE_COLS, row0 + qtr * 32);
                         bulk_commit();
                     }
                 }

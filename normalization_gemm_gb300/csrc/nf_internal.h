@@ -72,6 +72,8 @@ struct GemmArgs {
     int32_t M, N, K;
     int32_t m_tiles, n_tiles, k_tiles;
     int32_t cluster;        // CTAs per cluster along N (1 = no cluster)
+    int32_t units;          // unclustered: work units (tiles, with the last wave's tiles halved)
+    int32_t split_base;     // unclustered: first half-tile unit (== units when nothing is split)
     float eps;
     float inv_len;          // 1/K (pre-norm) or 1/N (post-norm)
     const uint16_t* gamma;  // bf16, N entries, or null

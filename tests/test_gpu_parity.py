@@ -336,3 +336,30 @@ def test_launch_overlap_keeps_dependent_chains_exact(dev):
                 assert torch.equal(a, b)
     finally:
         nf.set_launch_overlap(True)
+
+
+@pytest.mark.parametrize("op", ["plain", "pre", "post_ln", "post_rms"])
+def test_split_last_wave_whole_output(dev, orc, op):
+    """Short-K shapes whose last wave holds few tiles run them as 64-row halves:
+    two extra tiles here, the last with 72 rows (its second half has 8)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    M, K, N = 128 * sms * 2 + 128 + 72, 64, 128
+    inp = _inputs(M, K, N, seed=47, gamma=True, beta=True)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    stats = torch.full((M,), -7.0, dtype=torch.float32, device=dev)
+    if op == "plain":
+        got, want = nf.gemm_plain(X, W), orc.gemm_plain(inp["X"], inp["W"])
+    elif op == "pre":
+        got = nf.gemm_prenorm_rms(X, W, 1e-6, rstd_out=stats)
+        want, wstat = orc.gemm_prenorm_rms(inp["X"], inp["W"], 1e-6)
+    elif op == "post_ln":
+        got = nf.gemm_postnorm_ln(X, W, 1e-5, to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev),
+                                  rstd_out=stats)
+        want, _, wstat = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, inp["gamma"], inp["beta"])
+    else:
+        got = nf.gemm_postnorm_rms(X, W, 1e-5, to_dev(inp["gamma"], dev), rstd_out=stats)
+        want, wstat = orc.gemm_postnorm_rms(inp["X"], inp["W"], 1e-5, inp["gamma"])
+    assert_close(to_f64(got), want, f"split last wave {op}")
+    if op != "plain":
+        np.testing.assert_allclose(stats.cpu().numpy(), wstat, rtol=1e-3)
