@@ -153,6 +153,12 @@ nf_status nf_set_wait_timeout_ns(uint64_t ns);
  * touching global memory, so results are unchanged.  0 turns it off. */
 nf_status nf_set_launch_overlap(int enable);
 
+/* Post-norm column tile per CTA: 0 (default) chooses automatically (512
+ * columns and a cluster of ceil(N/512) <= 8 CTAs when N > 256); 256 forces
+ * 256-column tiles and clusters of up to 16 CTAs; 512 forces 512-column
+ * tiles.  Applies to later calls of nf_gemm_postnorm_ln / _rms. */
+nf_status nf_set_postnorm_tile_n(int tile_n);
+
 /* Self-test of the time limit: launches one CTA that waits on a barrier no
  * thread ever arrives on, with limit `timeout_ns` (1e3..1e10).  After the
  * stream completes, nf_get_device_status() reports NF_ERR_TIMEOUT. */

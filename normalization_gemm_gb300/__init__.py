@@ -66,6 +66,7 @@ _SIGS = {
     "nf_clear_device_status": [],
     "nf_set_wait_timeout_ns": [ctypes.c_uint64],
     "nf_set_launch_overlap": [ctypes.c_int],
+    "nf_set_postnorm_tile_n": [ctypes.c_int],
     "nf_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "nf_plan_gemm": [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(NFPlan)],
     "nf_abi_version": [],
@@ -243,6 +244,11 @@ def set_wait_timeout_ns(ns: int) -> None:
 def set_launch_overlap(enable: bool) -> None:
     """Programmatic dependent launch on (default) or off."""
     _check(lib().nf_set_launch_overlap(1 if enable else 0), "nf_set_launch_overlap")
+
+
+def set_postnorm_tile_n(tile_n: int) -> None:
+    """Post-norm column tile per CTA: 0 automatic, 256 or 512 forced."""
+    _check(lib().nf_set_postnorm_tile_n(int(tile_n)), "nf_set_postnorm_tile_n")
 
 
 def selftest_wait_timeout(ns: int, stream=None) -> None:

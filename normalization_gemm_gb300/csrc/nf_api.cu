@@ -60,6 +60,8 @@ uint64_t g_timeout_ns = 2000000000ull;
 // the kernel before it on the stream (it waits in griddepcontrol.wait before
 // touching global memory).
 bool g_overlap = true;
+// Post-norm column tile per CTA: 0 = automatic, 256 or 512 forced.
+int g_post_tile = 0;
 std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
@@ -129,7 +131,8 @@ EncodeTiledFn encode_fn() {
 // Row-major bf16 matrix of `rows` x `cols` (row pitch cols * 2 bytes), read or
 // written in boxes of box_rows x box_cols with 128-byte swizzle; out-of-bounds
 // elements read as zero and are dropped on store.
-nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(NF_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -137,7 +140,7 @@ nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t col
     cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char msg[128];
@@ -180,13 +183,20 @@ const GemmVariant* find_variant(int op, int tile_n, bool clustered) {
 nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, Plan* p) {
     const bool post = op == OP_POST_LN || op == OP_POST_RMS;
     p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
-    p->clustered = post && N > 256;
-    p->cluster = p->clustered ? static_cast<int>((N + 255) / 256) : 1;
+    if (post && N > 256) {
+        // Wider rows: 512 columns per CTA (two N = 256 MMAs per K step) and a
+        // cluster of ceil(N / 512) <= 8 CTAs, or 256 columns and up to 16 CTAs.
+        const int wide = g_post_tile == 256 ? 0 : 1;
+        if (g_post_tile == 512 || (wide && g_post_tile == 0)) p->tile_n = 512;
+        if (g_post_tile == 256 && N > 16 * 256) return fail(NF_ERR_UNSUPPORTED_SHAPE, "N too large");
+    }
+    p->clustered = post && N > p->tile_n;
+    p->cluster = p->clustered ? static_cast<int>((N + p->tile_n - 1) / p->tile_n) : 1;
     p->m_tiles = static_cast<int>((M + TILE_M - 1) / TILE_M);
     p->n_tiles = post ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
-    p->k_tiles = static_cast<int>((K + TILE_K - 1) / TILE_K);
     p->v = find_variant(op, p->tile_n, p->clustered);
     if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
+    p->k_tiles = static_cast<int>((K + p->v->tile_k - 1) / p->v->tile_k);
     return NF_OK;
 }
 
@@ -300,8 +310,11 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     if ((st = prepare_kernel(d, p.v)) != NF_OK) return st;
 
     CUtensorMap tmX, tmW, tmY;
-    if ((st = make_map(&tmX, X, M, K, TILE_K, TILE_M)) != NF_OK) return st;
-    if ((st = make_map(&tmW, W, K, N, B_BOX_N, TILE_K)) != NF_OK) return st;
+    const int tk = p.v->tile_k;  // 64: 128-byte rows of X; 32: 64-byte rows
+    if ((st = make_map(&tmX, X, M, K, tk, TILE_M, tk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        NF_OK)
+        return st;
+    if ((st = make_map(&tmW, W, K, N, B_BOX_N, tk)) != NF_OK) return st;
     if ((st = make_map(&tmY, Y, M, N, STORE_COLS, STORE_ROWS)) != NF_OK) return st;
 
     GemmArgs a;
@@ -460,6 +473,12 @@ nf_status nf_set_wait_timeout_ns(uint64_t ns) {
     return NF_OK;
 }
 
+nf_status nf_set_postnorm_tile_n(int tile_n) {
+    if (tile_n != 0 && tile_n != 256 && tile_n != 512) return fail(NF_ERR_INVALID_ARG, "tile_n must be 0, 256 or 512");
+    g_post_tile = tile_n;
+    return NF_OK;
+}
+
 nf_status nf_set_launch_overlap(int enable) {
     g_overlap = enable != 0;
     return NF_OK;
@@ -502,7 +521,7 @@ nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf
     if ((st = plan_tiles(op, M > 0 ? M : 1, N, K, &p)) != NF_OK) return st;
     out->tile_m = TILE_M;
     out->tile_n = p.tile_n;
-    out->tile_k = TILE_K;
+    out->tile_k = p.v->tile_k;
     out->stages = p.v->stages;
     out->cluster = p.cluster;
     out->threads = p.v->threads;

@@ -617,7 +617,8 @@ GemmVariant make_variant() {
                        Cfg::THREADS,
                        Cfg::SMEM_BYTES,
                        Cfg::STAGES,
-                       Cfg::TMEM_COLS};
+                       Cfg::TMEM_COLS,
+                       TILE_K};
 }
 
 }  // namespace nf

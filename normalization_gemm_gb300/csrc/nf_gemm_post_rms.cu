@@ -1,14 +1,15 @@
 // nf_gemm_post_rms.cu -- instantiations of the post-norm RMSNorm GEMM kernel
 // (one translation unit per epilogue so the variants compile in parallel).
-#include "nf_gemm_kernel.cuh"
+#include "nf_gemm_wide.cuh"
 
 namespace nf {
 
 const GemmVariant* gemm_variants_post_rms(int* count) {
     static const GemmVariant v[] = {
         make_variant<EPI_POST_RMS, 64, false>(), make_variant<EPI_POST_RMS, 128, false>(),
-        make_variant<EPI_POST_RMS, 256, false>(), make_variant<EPI_POST_RMS, 256, true>()};
-    *count = 4;
+        make_variant<EPI_POST_RMS, 256, false>(), make_variant<EPI_POST_RMS, 256, true>(),
+        make_wide_variant<EPI_POST_RMS, false>(), make_wide_variant<EPI_POST_RMS, true>()};
+    *count = 6;
     return v;
 }
 

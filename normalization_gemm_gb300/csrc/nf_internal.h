@@ -95,6 +95,7 @@ enum WaitSite : uint32_t {
     SITE_SS_FULL = 7,
     SITE_SS_ACC_EMPTY = 8,
     SITE_SELFTEST = 9,
+    SITE_EPI_PAIR = 10,
 };
 
 // One compiled GEMM variant.
@@ -103,6 +104,7 @@ struct GemmVariant {
     bool clustered;
     const void* func;
     int threads, smem_bytes, stages, tmem_cols;
+    int tile_k;  // K per ring stage: 64 (X boxes 128-byte swizzled) or 32 (64-byte swizzled)
 };
 
 // Tables exported by the kernel translation units.

@@ -216,18 +216,27 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
-// start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride
-// byte offset >> 4 in 32-45, the fixed value 1 in bits 46-48, base offset 0
-// (buffers are 1024-byte aligned) and layout type 2 (128B swizzle) in 61-63.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor (tcgen05 format): start address >> 4 in
+// bits 0-13, leading byte offset >> 4 in 16-29, stride byte offset >> 4 in
+// 32-45, the fixed value 1 in bits 46-48, base offset 0 (buffers are aligned
+// to their swizzle period) and the layout type in 61-63: 2 = 128-byte swizzle,
+// 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(saddr, lbo, sbo, 2u);
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(saddr, lbo, sbo, 4u);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 D:

@@ -80,17 +80,18 @@ def test_timeout_setting_range(L):
 
 @pytest.mark.parametrize("op,M,N,K,tile_n,cluster", [
     (0, 256, 64, 64, 64, 1), (1, 256, 64, 64, 64, 1), (1, 32768, 512, 512, 256, 1),
-    (2, 65536, 128, 128, 128, 1), (2, 16384, 2048, 1024, 256, 8), (3, 16384, 2048, 1024, 256, 8),
-    (2, 8192, 4096, 4096, 256, 16), (2, 300, 264, 72, 256, 2), (2, 5, 8, 8, 64, 1),
-    (0, 100, 200, 8, 256, 1), (1, 100, 120, 8, 128, 1),
+    (2, 65536, 128, 128, 128, 1), (2, 16384, 2048, 1024, 512, 4), (3, 16384, 2048, 1024, 512, 4),
+    (2, 8192, 4096, 4096, 512, 8), (2, 300, 264, 72, 512, 1), (2, 5, 8, 8, 64, 1),
+    (0, 100, 200, 8, 256, 1), (1, 100, 120, 8, 128, 1), (3, 64, 4088, 64, 512, 8),
 ])
 def test_plans(L, op, M, N, K, tile_n, cluster):
     p = nf.plan_gemm(op, M, N, K, 148)
-    assert (p["tile_m"], p["tile_k"]) == (128, 64)
+    assert p["tile_m"] == 128 and p["tile_k"] == (32 if tile_n == 512 else 64)
     assert p["tile_n"] == tile_n and p["cluster"] == cluster
     assert cluster * tile_n >= N or op in (0, 1)
+    assert cluster <= 8  # the default plans stay within the portable cluster size
     assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
-    assert p["tmem_cols"] == 2 * tile_n
+    assert p["tmem_cols"] == min(2 * tile_n, 512)
     assert p["threads"] == (448 if op == 1 else 320)
     m_tiles = -(-M // 128)
     n_tiles = 1 if op >= 2 else -(-N // tile_n)
@@ -114,3 +115,17 @@ def test_empty_m_accepts_null_bases(L):
     assert L.nf_gemm_prenorm_rms(None, P, None, 0, 64, 64, 1e-6, None, None) == OK
     assert L.nf_norm_rows(None, None, None, None, 0, 64, 0, 1e-5, None, None, None) == OK
     assert L.nf_gemm_plain(None, P, None, 1, 64, 64, None) == INVALID
+
+
+def test_forced_256_column_post_norm_plans(L):
+    try:
+        nf.set_postnorm_tile_n(256)
+        p = nf.plan_gemm(2, 8192, 4096, 4096, 148)
+        assert (p["tile_n"], p["cluster"], p["tile_k"]) == (256, 16, 64)
+        p = nf.plan_gemm(3, 16384, 2048, 1024, 148)
+        assert (p["tile_n"], p["cluster"]) == (256, 8)
+        nf.set_postnorm_tile_n(512)
+        assert nf.plan_gemm(2, 300, 264, 72, 148)["tile_n"] == 512
+    finally:
+        nf.set_postnorm_tile_n(0)
+    assert L.nf_set_postnorm_tile_n(384) == INVALID

@@ -74,9 +74,18 @@ POST_SHAPES = [(300, 64, 8), (300, 136, 64), (257, 64, 120), (384, 128, 128), (1
                (130, 64, 2048), (129, 64, 4096), (64, 64, 4088)]
 
 
+@pytest.fixture(params=[0, 256], ids=["auto_tiles", "tile256"])
+def post_tile(request):
+    """Post-norm tiling: automatic (512-column CTAs in clusters of <= 8 when
+    N > 256) or forced 256-column CTAs in clusters of up to 16."""
+    nf.set_postnorm_tile_n(request.param)
+    yield request.param
+    nf.set_postnorm_tile_n(0)
+
+
 @pytest.mark.parametrize("M,K,N", POST_SHAPES)
 @pytest.mark.parametrize("affine", [False, True])
-def test_postnorm_ln(dev, orc, M, K, N, affine):
+def test_postnorm_ln(dev, orc, post_tile, M, K, N, affine):
     import torch
     inp = _inputs(M, K, N, seed=3 * M + K + N, gamma=True, beta=True)
     g = inp["gamma"] if affine else None
@@ -94,7 +103,7 @@ def test_postnorm_ln(dev, orc, M, K, N, affine):
 
 @pytest.mark.parametrize("M,K,N", POST_SHAPES)
 @pytest.mark.parametrize("affine", [False, True])
-def test_postnorm_rms(dev, orc, M, K, N, affine):
+def test_postnorm_rms(dev, orc, post_tile, M, K, N, affine):
     import torch
     inp = _inputs(M, K, N, seed=5 * M + K + N, gamma=True)
     g = inp["gamma"] if affine else None
@@ -144,9 +153,9 @@ def test_many_tiles_per_cta(dev, orc):
     assert_close(y, orc.gemm_plain(inp["X"], inp["W"], rows=rows), "plain persistent")
 
 
-def test_cluster_many_tiles_per_cluster(dev, orc):
-    """16-CTA clusters walking many m tiles: the exchange barriers and both
-    receive buffers cycle through many phases."""
+def test_cluster_many_tiles_per_cluster(dev, orc, post_tile):
+    """Clusters (16 x 256 or 8 x 512 columns) walking many m tiles: the
+    exchange barriers and both receive buffers cycle through many phases."""
     M = 128 * 64 + 5
     inp = _inputs(M, 64, 4096, seed=19, gamma=True, beta=True)
     rows = nf_inputs.sample_rows(M, 160, seed=4)
