@@ -7,7 +7,8 @@
  * and Attention Kernels" (PyTorch blog):
  *   - §2 "Lazy Pre-Norm":  Y = RMSNorm(X) * W, no affine;
  *   - §3 "Multi-CTA Norm": Y = LayerNorm(X * W) or RMSNorm(X * W), optional
- *     gamma / beta, the row spread over a thread-block cluster;
+ *     gamma / beta, the row spread over several CTAs that exchange partial
+ *     row statistics (through DSMEM in a thread-block cluster, or through L2);
  * plus the unfused pair of the blog's §1 baseline (a plain GEMM and a
  * standalone row-norm kernel).
  *
@@ -17,9 +18,21 @@
  *              gamma / beta hold N bf16 values; mean / rstd outputs hold one
  *              fp32 per row.
  *   Memory     Every pointer is DEVICE memory of the current CUDA device,
- *              owned by the caller.  The library allocates nothing per call
- *              and keeps no reference after the call returns.  Y must not
- *              overlap any input.
+ *              owned by the caller; the library keeps no reference after the
+ *              call returns.  Y must not overlap any input.  The library
+ *              allocates nothing per call, with one exception: post-norm
+ *              rows wider than 256 columns exchanged through L2 (the default,
+ *              see nf_set_postnorm_exchange) use a scratch buffer owned by
+ *              the library, one per (device, stream), of about
+ *              8 * M * ceil(N / 256) bytes.  The first such call on a stream
+ *              (and a call with a larger M * ceil(N / 256) than before)
+ *              allocates or grows it, synchronizing that stream; while the
+ *              stream is being captured that call fails with
+ *              NF_ERR_INVALID_ARG, so make it before capture.  Later calls
+ *              reuse the buffer and are capture-safe; a captured graph keeps
+ *              the buffer of the stream it was captured on, so replays of it
+ *              must not run concurrently with other post-norm work on that
+ *              stream's buffer.
  *   Alignment  X, W, Y (and in/out of nf_norm_rows) start on a 16-byte
  *              boundary; gamma / beta on 2 bytes; fp32 outputs on 4 bytes.
  *              K and N (cols for nf_norm_rows) are multiples of 8, so that
@@ -95,9 +108,13 @@ nf_status nf_gemm_prenorm_rms(const void* X, const void* W, void* Y,
 
 /*
  * nf_gemm_postnorm_ln -- Y = LayerNorm(X * W) over each row of N, Multi-CTA
- * post-norm (blog §3): each CTA of a cluster spanning the row reduces the
- * partial statistics of its tile, the partials are exchanged through
- * distributed shared memory, and every CTA normalizes before its single store.
+ * post-norm (blog §3): each CTA holding a tile of the row reduces the partial
+ * statistics of its tile, the partials are exchanged, and every CTA
+ * normalizes before its single store.  N <= 256: one CTA holds whole rows.
+ * Wider rows: the exchange runs through L2 between the 256-column tiles of a
+ * cooperative grid (default), or, as on the blog, through distributed shared
+ * memory inside a thread-block cluster spanning the row
+ * (nf_set_postnorm_exchange).
  * LayerNorm as torch.nn.LayerNorm: biased variance, eps inside the root.
  * gamma, beta: optional (NULL = 1 and 0), N bf16 values each.
  * mean_out, rstd_out: optional, M fp32 values (row mean, 1/sqrt(var + eps)).
@@ -139,7 +156,8 @@ nf_status nf_norm_rows(const void* in, void* out, const void* gamma,
  * index, tile index of the first failure. */
 nf_status nf_get_device_status(uint32_t* detail);
 
-/* Synchronizes the current device and resets its status word to NF_OK. */
+/* Synchronizes the current device, resets its status word to NF_OK and
+ * zeroes the library's post-norm exchange scratch on it. */
 nf_status nf_clear_device_status(void);
 
 /* Time limit for every device-side pipeline wait, in nanoseconds (default
@@ -153,11 +171,22 @@ nf_status nf_set_wait_timeout_ns(uint64_t ns);
  * touching global memory, so results are unchanged.  0 turns it off. */
 nf_status nf_set_launch_overlap(int enable);
 
-/* Post-norm column tile per CTA: 0 (default) chooses automatically (512
- * columns and a cluster of ceil(N/512) <= 8 CTAs when N > 256); 256 forces
- * 256-column tiles and clusters of up to 16 CTAs; 512 forces 512-column
- * tiles.  Applies to later calls of nf_gemm_postnorm_ln / _rms. */
+/* Column tile per CTA when post-norm rows go to a cluster: 0 (default)
+ * automatic, 512 (a cluster of ceil(N/512) <= 8 CTAs; a row of N <= 512 then
+ * needs no cluster) or 256 (clusters of up to 16 CTAs).  Applies to later
+ * post-norm calls that use the cluster exchange. */
 nf_status nf_set_postnorm_tile_n(int tile_n);
+
+/* How post-norm rows wider than 256 columns exchange partial statistics:
+ * 0 (default) automatic -- one 512-column CTA per row while N <= 512, else
+ * NF_XCH_GLOBAL when K >= 512, else NF_XCH_CLUSTER; NF_XCH_CLUSTER: a
+ * thread-block cluster spans the row and the partials go through
+ * distributed shared memory (blog §3); NF_XCH_GLOBAL: 256-column tiles of a
+ * persistent cooperative grid using every SM, partials through L2 (scratch
+ * memory, see "Memory" above).  Applies to later calls. */
+#define NF_XCH_CLUSTER 1
+#define NF_XCH_GLOBAL 2
+nf_status nf_set_postnorm_exchange(int mode);
 
 /* Self-test of the time limit: launches one CTA that waits on a barrier no
  * thread ever arrives on, with limit `timeout_ns` (1e3..1e10).  After the
@@ -183,12 +212,13 @@ typedef struct nf_plan {
     int32_t smem_bytes;             /* dynamic shared memory per CTA       */
     int32_t tmem_cols;              /* tensor-memory columns per CTA       */
     int32_t tiles;                  /* output tiles (M/tile_m x N/tile_n)  */
+    int32_t exchange;               /* 0 none, NF_XCH_CLUSTER, NF_XCH_GLOBAL */
 } nf_plan;
 nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count,
                        nf_plan* out);
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define NF_ABI_VERSION 1
+#define NF_ABI_VERSION 2
 int nf_abi_version(void);
 
 #ifdef __cplusplus

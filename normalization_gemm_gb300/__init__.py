@@ -30,6 +30,8 @@ NF_OK = 0
 NORM_LN = 0
 NORM_RMS = 1
 POSTNORM_MAX_N = 4096
+XCH_CLUSTER = 1
+XCH_GLOBAL = 2
 
 STATUS_NAMES = {0: "NF_OK", 1: "NF_ERR_INVALID_ARG", 2: "NF_ERR_ALIGNMENT",
                 3: "NF_ERR_UNSUPPORTED_SHAPE", 4: "NF_ERR_CUDA", 5: "NF_ERR_TIMEOUT",
@@ -48,7 +50,7 @@ class NFError(RuntimeError):
 class NFPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "tile_m", "tile_n", "tile_k", "stages", "cluster", "grid", "threads", "smem_bytes",
-        "tmem_cols", "tiles")]
+        "tmem_cols", "tiles", "exchange")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -67,6 +69,7 @@ _SIGS = {
     "nf_set_wait_timeout_ns": [ctypes.c_uint64],
     "nf_set_launch_overlap": [ctypes.c_int],
     "nf_set_postnorm_tile_n": [ctypes.c_int],
+    "nf_set_postnorm_exchange": [ctypes.c_int],
     "nf_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "nf_plan_gemm": [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(NFPlan)],
     "nf_abi_version": [],
@@ -249,6 +252,12 @@ def set_launch_overlap(enable: bool) -> None:
 def set_postnorm_tile_n(tile_n: int) -> None:
     """Post-norm column tile per CTA: 0 automatic, 256 or 512 forced."""
     _check(lib().nf_set_postnorm_tile_n(int(tile_n)), "nf_set_postnorm_tile_n")
+
+
+def set_postnorm_exchange(mode: int) -> None:
+    """Post-norm rows wider than 256 columns: 0 automatic, XCH_CLUSTER (DSMEM in a
+    thread-block cluster) or XCH_GLOBAL (L2 between tiles of a cooperative grid)."""
+    _check(lib().nf_set_postnorm_exchange(int(mode)), "nf_set_postnorm_exchange")
 
 
 def selftest_wait_timeout(ns: int, stream=None) -> None:

@@ -60,8 +60,12 @@ uint64_t g_timeout_ns = 2000000000ull;
 // the kernel before it on the stream (it waits in griddepcontrol.wait before
 // touching global memory).
 bool g_overlap = true;
-// Post-norm column tile per CTA: 0 = automatic, 256 or 512 forced.
+// Post-norm column tile per CTA of a cluster: 0 = automatic, 256 or 512 forced.
 int g_post_tile = 0;
+// Post-norm rows wider than 256 columns: 0 = automatic, else an Exchange mode.
+int g_post_xch = 0;
+// A cooperative launch accepted the programmatic-serialization attribute.
+bool g_coop_overlap_ok = true;
 std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
@@ -78,8 +82,32 @@ struct DeviceState {
     // kernels whose attributes were set on this device
     const void* attr_done[32] = {};
     int attr_n = 0;
+    // resident CTAs per SM, per kernel (for cooperative grids)
+    const void* blk_func[16] = {};
+    int blk_value[16] = {};
+    int blk_n = 0;
 };
 DeviceState g_dev[kMaxDevices];
+
+// Global-exchange scratch, one buffer per (device, stream): launches on one
+// stream run in order, so each buffer is used by one launch at a time.  The
+// buffer holds the header and two counter banks of bank_ints each, then
+// (256-byte aligned) stats_bytes of partial statistics; both capacities only
+// grow.
+struct XScratch {
+    int dev = -1;
+    cudaStream_t stream = nullptr;
+    uint8_t* ptr = nullptr;
+    size_t bytes = 0;
+    int64_t bank_ints = 0;
+    int64_t stats_bytes = 0;
+    int* cnt() const { return reinterpret_cast<int*>(ptr); }
+    float2* stats() const { return reinterpret_cast<float2*>(ptr + stats_offset(bank_ints)); }
+    static int64_t stats_offset(int64_t bank_ints) { return ((XCH_CNT0 + 2 * bank_ints) * 4 + 255) / 256 * 256; }
+};
+constexpr int kMaxScratch = 64;
+XScratch g_xs[kMaxScratch];
+int g_xs_n = 0;
 
 nf_status device_state(DeviceState** out) {
     int dev = 0;
@@ -155,13 +183,14 @@ enum Op { OP_PLAIN = 0, OP_PRE = 1, OP_POST_LN = 2, OP_POST_RMS = 3 };
 
 struct Plan {
     int tile_n = 0;
+    int xch = XCH_NONE;
     bool clustered = false;
     int cluster = 1;
     int m_tiles = 0, n_tiles = 0, k_tiles = 0;
     const GemmVariant* v = nullptr;
 };
 
-const GemmVariant* find_variant(int op, int tile_n, bool clustered) {
+const GemmVariant* find_variant(int op, int tile_n, int xch) {
     int n = 0;
     const GemmVariant* t = nullptr;
     switch (op) {
@@ -172,29 +201,56 @@ const GemmVariant* find_variant(int op, int tile_n, bool clustered) {
         default: return nullptr;
     }
     for (int i = 0; i < n; ++i)
-        if (t[i].tile_n == tile_n && t[i].clustered == clustered) return &t[i];
+        if (t[i].tile_n == tile_n && t[i].xch == xch) return &t[i];
     return nullptr;
 }
 
 // Tile choice.  Plain and pre-norm: the smallest of 64 / 128 / 256 columns
-// that covers N, else 256.  Post-norm (blog §3): one CTA covers the row while
-// N <= 256; beyond that a cluster of ceil(N / 256) CTAs of 256 columns each
-// spans the row (N <= 4096: 16 CTAs).
-nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, Plan* p) {
+// that covers N, else 256.  Post-norm (blog §3): one CTA holds whole rows
+// while N <= 256 (and, with 512 columns per CTA, while N <= 512).  Wider rows
+// are split over CTAs that exchange partial row statistics:
+//   through L2 between 256-column tiles of a cooperative grid that keeps
+//   every SM busy -- the automatic choice when K >= 512, where a tile's
+//   main loop outlasts the exchange and the cluster's co-residency limits
+//   (GB300 holds 15 clusters of 8, i.e. 120 of 152 SMs) cost the most;
+//   or, as on the blog, through DSMEM inside a thread-block cluster, with
+//   256 columns per CTA (automatic for K < 512 up to N = 2048, a cluster of
+//   <= 8) or 512 (two N = 256 MMAs per K step, a cluster of <= 8 for
+//   N <= 4096).
+// `sms`: SMs of the device.  The global exchange runs one CTA per SM and
+// needs at least half as many CTAs as a row has tiles; with fewer the row
+// goes to a cluster instead.
+nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p) {
     const bool post = op == OP_POST_LN || op == OP_POST_RMS;
     p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+    p->xch = XCH_NONE;
     if (post && N > 256) {
-        // Wider rows: 512 columns per CTA (two N = 256 MMAs per K step) and a
-        // cluster of ceil(N / 512) <= 8 CTAs, or 256 columns and up to 16 CTAs.
-        const int wide = g_post_tile == 256 ? 0 : 1;
-        if (g_post_tile == 512 || (wide && g_post_tile == 0)) p->tile_n = 512;
-        if (g_post_tile == 256 && N > 16 * 256) return fail(NF_ERR_UNSUPPORTED_SHAPE, "N too large");
+        int mode = g_post_xch, tile = g_post_tile;
+        if (mode == 0) {
+            if (N <= 512)
+                mode = XCH_CLUSTER, tile = tile ? tile : 512;  // one 512-column CTA: no exchange
+            else if (K >= 512)
+                mode = XCH_GLOBAL;
+            else
+                mode = XCH_CLUSTER, tile = tile ? tile : (N <= 2048 ? 256 : 512);
+        }
+        if (mode == XCH_GLOBAL) {
+            const int64_t nt = (N + 255) / 256, tiles = ((M + TILE_M - 1) / TILE_M) * nt;
+            if (2 * (tiles < sms ? tiles : sms) < nt) mode = XCH_CLUSTER;
+        }
+        p->xch = mode;
+        if (mode == XCH_CLUSTER) {
+            p->tile_n = tile == 256 ? 256 : 512;
+            if (N > static_cast<int64_t>(p->tile_n) * (p->tile_n == 512 ? 8 : 16))
+                return fail(NF_ERR_UNSUPPORTED_SHAPE, "N too large for the cluster");
+            if (N <= p->tile_n) p->xch = XCH_NONE;  // one wide CTA covers the row
+        }
     }
-    p->clustered = post && N > p->tile_n;
+    p->clustered = p->xch == XCH_CLUSTER;
     p->cluster = p->clustered ? static_cast<int>((N + p->tile_n - 1) / p->tile_n) : 1;
     p->m_tiles = static_cast<int>((M + TILE_M - 1) / TILE_M);
-    p->n_tiles = post ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
-    p->v = find_variant(op, p->tile_n, p->clustered);
+    p->n_tiles = (post && p->xch != XCH_GLOBAL) ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
+    p->v = find_variant(op, p->tile_n, p->xch);
     if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
     p->k_tiles = static_cast<int>((K + p->v->tile_k - 1) / p->v->tile_k);
     return NF_OK;
@@ -298,6 +354,90 @@ nf_status max_clusters(DeviceState* d, const GemmVariant* v, int cluster, int* o
     return NF_OK;
 }
 
+// Resident CTAs per SM of a variant (cached per device).
+nf_status blocks_per_sm(DeviceState* d, const GemmVariant* v, int* out) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int i = 0; i < d->blk_n; ++i)
+            if (d->blk_func[i] == v->func) {
+                *out = d->blk_value[i];
+                return NF_OK;
+            }
+    }
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, v->func, v->threads,
+                                                                  static_cast<size_t>(v->smem_bytes));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (n < 1) return fail(NF_ERR_UNSUPPORTED_SHAPE, "the kernel does not fit on an SM");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d->blk_n < 16) {
+        d->blk_func[d->blk_n] = v->func;
+        d->blk_value[d->blk_n] = n;
+        ++d->blk_n;
+    }
+    *out = n;
+    return NF_OK;
+}
+
+// The stream's global-exchange scratch for m_tiles x n_tiles tiles.
+// Allocating (first use on a stream, or a larger shape) synchronizes the
+// stream and is refused while the stream is being captured into a graph.
+nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, int32_t* bank, float2** stats) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    const int64_t need_bank = xch_bank_ints(m_tiles), need_stats = xch_stats_bytes(m_tiles, n_tiles);
+    std::lock_guard<std::mutex> lk(g_mu);
+    XScratch* x = nullptr;
+    for (int i = 0; i < g_xs_n; ++i)
+        if (g_xs[i].dev == dev && g_xs[i].stream == stream) x = &g_xs[i];
+    if (x && x->bank_ints >= need_bank && x->stats_bytes >= need_stats) {
+        *cnt = x->cnt();
+        *bank = static_cast<int32_t>(x->bank_ints);
+        *stats = x->stats();
+        return NF_OK;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(NF_ERR_INVALID_ARG,
+                    "post-norm exchange scratch is set up on the first call per stream (and grown for larger "
+                    "shapes): make that call before capturing the stream");
+    int64_t bank_ints = need_bank, stats_bytes = need_stats;
+    if (!x) {
+        if (g_xs_n == kMaxScratch) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many streams with post-norm scratch");
+        x = &g_xs[g_xs_n++];
+        x->dev = dev;
+        x->stream = stream;
+    } else {
+        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+        cudaFree(x->ptr);
+        bank_ints = bank_ints > x->bank_ints ? bank_ints : x->bank_ints;
+        stats_bytes = stats_bytes > x->stats_bytes ? stats_bytes : x->stats_bytes;
+        x->ptr = nullptr;
+        x->bytes = 0;
+        x->bank_ints = x->stats_bytes = 0;
+    }
+    // Round both regions up so that modest growth reuses the buffer.
+    bank_ints = (bank_ints + 4095) / 4096 * 4096;
+    stats_bytes = (stats_bytes + (1 << 20) - 1) >> 20 << 20;
+    const size_t bytes = static_cast<size_t>(XScratch::stats_offset(bank_ints) + stats_bytes);
+    void* ptr = nullptr;
+    if ((e = cudaMalloc(&ptr, bytes)) != cudaSuccess) return fail_cuda(e, "cudaMalloc(exchange scratch)");
+    if ((e = cudaMemsetAsync(ptr, 0, bytes, stream)) != cudaSuccess) {
+        cudaFree(ptr);
+        return fail_cuda(e, "cudaMemsetAsync(exchange scratch)");
+    }
+    x->ptr = static_cast<uint8_t*>(ptr);
+    x->bytes = bytes;
+    x->bank_ints = bank_ints;
+    x->stats_bytes = stats_bytes;
+    *cnt = x->cnt();
+    *bank = static_cast<int32_t>(x->bank_ints);
+    *stats = x->stats();
+    return NF_OK;
+}
+
 nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
                    int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream) {
     nf_status st = check_gemm_args(op, X, W, Y, gamma, beta, mean_out, rstd_out, M, N, K, eps);
@@ -306,7 +446,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     DeviceState* d = nullptr;
     if ((st = device_state(&d)) != NF_OK) return st;
     Plan p;
-    if ((st = plan_tiles(op, M, N, K, &p)) != NF_OK) return st;
+    if ((st = plan_tiles(op, M, N, K, d->sm_count, &p)) != NF_OK) return st;
     if ((st = prepare_kernel(d, p.v)) != NF_OK) return st;
 
     CUtensorMap tmX, tmW, tmY;
@@ -333,6 +473,9 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.rstd_out = rstd_out;
     a.status = d->status;
     a.timeout_ns = g_timeout_ns;
+    a.xcnt = nullptr;
+    a.xbank = 0;
+    a.xstats = nullptr;
 
     int grid = 0;
     a.units = p.m_tiles * p.n_tiles;
@@ -341,6 +484,17 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         int mc = 0;
         if ((st = max_clusters(d, p.v, p.cluster, &mc)) != NF_OK) return st;
         grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;
+    } else if (p.xch == XCH_GLOBAL) {
+        // Every CTA resident at once (cooperative launch), tiles in order,
+        // no split units.  grid >= n_tiles / 2 keeps the exchange deadlock
+        // free (see the kernel); n_tiles <= 16 and tiles >= n_tiles.
+        int per_sm = 0;
+        if ((st = blocks_per_sm(d, p.v, &per_sm)) != NF_OK) return st;
+        const int tiles = p.m_tiles * p.n_tiles;
+        const int cap = per_sm * d->sm_count;
+        grid = tiles < cap ? tiles : cap;
+        if (2 * grid < p.n_tiles) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too few resident CTAs for the exchange");
+        if ((st = xch_scratch(stream, p.m_tiles, p.n_tiles, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) return st;
     } else {
         const int tiles = p.m_tiles * p.n_tiles;
         grid = tiles < d->sm_count ? tiles : d->sm_count;
@@ -348,7 +502,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     }
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     int nattr = 0;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(p.v->threads));
@@ -361,7 +515,13 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         attr[nattr].val.clusterDim.z = 1;
         ++nattr;
     }
-    if (g_overlap) {
+    if (p.xch == XCH_GLOBAL) {
+        attr[nattr].id = cudaLaunchAttributeCooperative;
+        attr[nattr].val.cooperative = 1;
+        ++nattr;
+    }
+    const bool overlap = g_overlap && (p.xch != XCH_GLOBAL || g_coop_overlap_ok);
+    if (overlap) {
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[nattr].val.programmaticStreamSerializationAllowed = 1;
         ++nattr;
@@ -370,6 +530,14 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     cfg.numAttrs = static_cast<unsigned>(nattr);
     void* kargs[4] = {&tmX, &tmW, &tmY, &a};
     cudaError_t e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
+    if (e != cudaSuccess && overlap && p.xch == XCH_GLOBAL) {
+        // The runtime refused programmatic serialization on a cooperative
+        // launch: drop it for these launches from now on.
+        (void)cudaGetLastError();
+        g_coop_overlap_ok = false;
+        cfg.numAttrs = static_cast<unsigned>(nattr - 1);
+        e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
+    }
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
     return NF_OK;
 }
@@ -464,6 +632,17 @@ nf_status nf_clear_device_status(void) {
     const uint32_t z[4] = {0, 0, 0, 0};
     e = cudaMemcpy(d->status, z, sizeof z, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return fail_cuda(e, "clear status word");
+    // A launch that gave up may have left exchange counters part-way.
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_xs_n; ++i)
+        if (g_xs[i].dev == dev && g_xs[i].ptr) {
+            e = cudaMemset(g_xs[i].ptr, 0, g_xs[i].bytes);
+            if (e != cudaSuccess) return fail_cuda(e, "clear exchange scratch");
+        }
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
     return NF_OK;
 }
 
@@ -476,6 +655,13 @@ nf_status nf_set_wait_timeout_ns(uint64_t ns) {
 nf_status nf_set_postnorm_tile_n(int tile_n) {
     if (tile_n != 0 && tile_n != 256 && tile_n != 512) return fail(NF_ERR_INVALID_ARG, "tile_n must be 0, 256 or 512");
     g_post_tile = tile_n;
+    return NF_OK;
+}
+
+nf_status nf_set_postnorm_exchange(int mode) {
+    if (mode != 0 && mode != NF_XCH_CLUSTER && mode != NF_XCH_GLOBAL)
+        return fail(NF_ERR_INVALID_ARG, "mode must be 0 (automatic), 1 (cluster) or 2 (global)");
+    g_post_xch = mode;
     return NF_OK;
 }
 
@@ -518,7 +704,7 @@ nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf
                                    1e-5f);
     if (st != NF_OK) return st;
     Plan p;
-    if ((st = plan_tiles(op, M > 0 ? M : 1, N, K, &p)) != NF_OK) return st;
+    if ((st = plan_tiles(op, M > 0 ? M : 1, N, K, sm_count, &p)) != NF_OK) return st;
     out->tile_m = TILE_M;
     out->tile_n = p.tile_n;
     out->tile_k = p.v->tile_k;
@@ -528,6 +714,7 @@ nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf
     out->smem_bytes = p.v->smem_bytes;
     out->tmem_cols = p.v->tmem_cols;
     out->tiles = M > 0 ? p.m_tiles * p.n_tiles : 0;
+    out->exchange = p.xch;
     if (p.clustered) {
         const int mc = sm_count / p.cluster;
         out->grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;

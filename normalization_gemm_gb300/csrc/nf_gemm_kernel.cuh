@@ -36,6 +36,21 @@
 // statistics of the cluster arrived).  Every wait is bounded in time; on
 // expiry the kernel records NF_ERR_TIMEOUT, drains what it issued, frees TMEM
 // and returns.
+//
+// Post-norm rows wider than one tile exchange partial row statistics between
+// the CTAs that hold the row (XCH):
+//   XCH_CLUSTER  the row's CTAs form a thread-block cluster along N and push
+//                their partials into every peer's shared memory (DSMEM), as
+//                in blog §3.
+//   XCH_GLOBAL   the row's tiles are ordinary tiles of a persistent grid whose
+//                CTAs are all resident at once (cooperative launch); partials
+//                go through L2 with an arrival counter per (row tile,
+//                32-row quarter).
+//                Tile t runs on CTA t mod G in order, G >= n_tiles / 2, so a
+//                CTA's tiles t_i and t_{i-2} (which share a TMEM buffer) lie in
+//                different row tiles and every wait points at an earlier row
+//                tile: the exchange cannot deadlock.  This uses every SM,
+//                whereas clusters of 8 or 16 co-reside on fewer of them.
 #pragma once
 
 #include "nf_internal.h"
@@ -87,11 +102,14 @@ __device__ __forceinline__ void tmem_load_seg(uint32_t taddr, uint32_t (&v)[NC][
     for (int c = 1; c < NC; ++c) reg_fence(v[c]);
 }
 
+// Where the epilogue finds gamma / beta.
+enum AffSrc : int { AFF_NONE = 0, AFF_SMEM = 1 };
+
 // 64 fp32 columns (two 32-column chunks) -> 32 packed bf16 pairs:
-// y = x * scale + bias, then y * gamma + beta when AFF (gamma / beta read as
-// bf16 from shared memory at saff_g / saff_b, 8 columns per 16-byte load).
-// Works on fp32 pairs: one f32x2 FMA per two columns.
-template <bool AFF>
+// y = x * scale + bias, then y * gamma + beta unless AFF == AFF_NONE (gamma /
+// beta as bf16 in shared memory at saff_g / saff_b, 8 columns per 16-byte
+// load).  Works on fp32 pairs: one f32x2 FMA per two columns.
+template <int AFF>
 __device__ __forceinline__ void convert64(const uint32_t (&va)[32], const uint32_t (&vb)[32], uint64_t scale2,
                                           uint64_t bias2, uint32_t saff_g, uint32_t saff_b, uint32_t (&pk)[32]) {
 #pragma unroll
@@ -101,7 +119,7 @@ __device__ __forceinline__ void convert64(const uint32_t (&va)[32], const uint32
         uint64_t y[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) y[e] = f2_fma(f2_pack(src[o + 2 * e], src[o + 2 * e + 1]), scale2, bias2);
-        if (AFF) {
+        if (AFF != AFF_NONE) {
             const uint4 g = ld_shared_v4(saff_g + static_cast<uint32_t>(q * 16));
             const uint4 t = ld_shared_v4(saff_b + static_cast<uint32_t>(q * 16));
             y[0] = f2_fma(y[0], bf16x2_to_f2(g.x), bf16x2_to_f2(t.x));
@@ -151,16 +169,26 @@ struct TileSched {
     }
 };
 
-template <int EPI, int TILE_N, bool CLUSTERED>
-__global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
+template <int EPI, int TILE_N, int XCH>
+__global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
     nf_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
-    using Cfg = GemmCfg<EPI, TILE_N, CLUSTERED>;
+    using Cfg = GemmCfg<EPI, TILE_N, XCH>;
+    constexpr bool CLUSTERED = XCH == XCH_CLUSTER;
+    constexpr bool GLOBALX = XCH == XCH_GLOBAL;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int NBOX = TILE_N / B_BOX_N;
 
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
+    if (Cfg::ALIGN_SLACK == 0 && (raw & 1023u) != 0) {
+        // No room to realign: report and leave before touching anything.
+        if (threadIdx.x == 0 && atomicCAS(&args.status[0], 0u, 2u /* NF_ERR_ALIGNMENT */) == 0u) {
+            atomicExch(&args.status[1], SITE_SMEM_ALIGN);
+            atomicExch(&args.status[2], blockIdx.x);
+        }
+        return;
+    }
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
 
@@ -176,6 +204,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
     const uint32_t bar_ssf0 = sBar + 8u * 20;    // [2]
     const uint32_t bar_xch0 = sBar + 8u * 22;    // [2]
     const uint32_t bar_mma_done = sBar + 8u * 24;
+    const uint32_t bar_afff0 = sBar + 8u * 25;   // [2] global exchange: a group's affine slot filled
+    const uint32_t bar_affe0 = sBar + 8u * 27;   // [2] global exchange: a group's affine slot free
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS);
     volatile int* const abort_flag =
         reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS + 4);
@@ -226,6 +256,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             mbar_init(bar_xch0 + 8u * b, 1);
         }
         mbar_init(bar_mma_done, 1);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(bar_afff0 + 8u * g, 4);  // one arrival per warp of the group
+            mbar_init(bar_affe0 + 8u * g, 4);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         if (CLUSTERED) {
@@ -242,7 +276,18 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
     // programmatic serialization; global memory is touched only after this.
     griddep_wait();
     griddep_launch_dependents();
-    if (Cfg::kPost && threadIdx.x < 128) {
+    // Global exchange: count in bank E & 1; clear the other bank, which the
+    // previous launch on this scratch used (it has completed).
+    int* xbank = nullptr;
+    if (GLOBALX) {
+        const int e = ld_acquire_gpu(args.xcnt + 2);
+        const int prev_ints = ld_acquire_gpu(args.xcnt + 3) * 4;
+        xbank = args.xcnt + XCH_CNT0 + (e & 1) * args.xbank;
+        int* const other = args.xcnt + XCH_CNT0 + ((e + 1) & 1) * args.xbank;
+        const int stride = static_cast<int>(gridDim.x * blockDim.x);
+        for (int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i < prev_ints; i += stride) other[i] = 0;
+    }
+    if (Cfg::kPost && !GLOBALX && threadIdx.x < 128) {
         // This CTA's columns never change: clustered CTAs keep their rank's
         // tile, unclustered post-norm has a single column tile.
         const int n0 = sched.n_fixed * TILE_N;
@@ -357,13 +402,19 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
         // read in segments of 64 columns (two tcgen05.ld, one wait); post-norm
         // keeps the last segment in registers across the statistics exchange.
         constexpr int SEG = TILE_N < 64 ? TILE_N : 64;
+        // Post-norm keeps the row's last segment in registers across the
+        // statistics exchange, except the global exchange, whose partials of up
+        // to 16 column tiles need those registers: it reads the segment again.
+        constexpr bool KEEP_SEG = Cfg::kPost && !GLOBALX;
         constexpr int NC = SEG / 32;
         const int grp = warp >> 2;
         const int qtr = warp & 3;
         const int row = qtr * 32 + lane;  // tile row == TMEM lane
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qtr * 32) << 16);
         const bool affine = Cfg::kPost && (args.gamma != nullptr || args.beta != nullptr);
-        const uint32_t saff = smem_u32(aff);
+        // gamma at saff, beta at saff + 2 TILE_N; the global exchange keeps one
+        // such slot per group, refilled for each tile's columns.
+        const uint32_t saff = smem_u32(aff) + (GLOBALX ? static_cast<uint32_t>(grp * 4 * TILE_N) : 0u);
         for (int lt = grp; lt < count; lt += 2) {
             int m, n, row0, rows;
             sched.tile(lt, m, n, row0, rows);
@@ -382,6 +433,23 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             float scale = 1.0f, bias = 0.0f;                         // y = acc * scale + bias
             bool released = false;
             uint32_t v[NC][32];
+            const uint32_t jph = static_cast<uint32_t>(lt >> 1) & 1u;  // this group's tile count parity
+
+            if (GLOBALX && affine) {
+                // -- this warp's quarter of the group's affine slot (64 columns),
+                //    once the group's four warps are done with the previous tile.
+                ok = mbar_wait(guard, bar_affe0 + 8u * grp, jph ^ 1u, SITE_EPI_AFF, lt);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                const int c = qtr * 64 + 2 * lane, col = n * TILE_N + c;  // N % 8 == 0: both or neither in
+                const bool in = col < args.N;
+                uint32_t g2 = 0x3F803F80u, b2 = 0u;
+                if (in && args.gamma) g2 = static_cast<uint32_t>(args.gamma[col]) | (static_cast<uint32_t>(args.gamma[col + 1]) << 16);
+                if (in && args.beta) b2 = static_cast<uint32_t>(args.beta[col]) | (static_cast<uint32_t>(args.beta[col + 1]) << 16);
+                st_shared_u32(saff + static_cast<uint32_t>(c * 2), g2);
+                st_shared_u32(saff + static_cast<uint32_t>((TILE_N + c) * 2), b2);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_afff0 + 8u * grp);
+            }
 
             if (Cfg::kPre) {
                 ok = mbar_wait(guard, bar_ssf0 + 8u * b, aph, SITE_EPI_SS_FULL, lt);
@@ -418,7 +486,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                             }
                         }
                 }
-                if (nseg == 1) {  // the row is in registers: TMEM buffer b is free
+                if (KEEP_SEG && nseg == 1) {  // the row is in registers: TMEM buffer b is free
                     tc_fence_before();
                     mbar_arrive(bar_acce0 + 8u * b);
                     released = true;
@@ -475,9 +543,49 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                         sq = 0.0f;
                         for (int p = 0; p < args.cluster; ++p) sq += recv[p * TILE_M * 2];
                     }
+                } else if (GLOBALX) {
+                    // -- exchange through L2: publish this quarter's partials
+                    //    for column tile n, count the publication, wait until
+                    //    all n_tiles column tiles of row tile m have counted,
+                    //    read their partials.
+                    const int nt = args.n_tiles;
+                    float2* const xst = args.xstats + static_cast<size_t>(m) * nt * TILE_M + row;
+                    int* const cnt = xbank + m * 4 + qtr;
+                    __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
+                    __syncwarp();  // the warp's stores precede lane 0's release
+                    if (lane == 0) red_release_gpu_add(cnt, 1);
+                    if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
+                    float2 pp[MAX_CLUSTER];
+#pragma unroll
+                    for (int p = 0; p < MAX_CLUSTER; ++p)
+                        pp[p] = p < nt ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
+                    if (Cfg::kLN) {
+                        // Chan et al. pairwise merge of (count, mean, M2).
+                        float msum = 0.0f;
+#pragma unroll
+                        for (int p = 0; p < MAX_CLUSTER; ++p)
+                            if (p < nt) msum += static_cast<float>(min(TILE_N, args.N - p * TILE_N)) * pp[p].x;
+                        mean = msum * args.inv_len;
+                        sq = 0.0f;
+#pragma unroll
+                        for (int p = 0; p < MAX_CLUSTER; ++p)
+                            if (p < nt) {
+                                const float dm = pp[p].x - mean;
+                                sq += pp[p].y + static_cast<float>(min(TILE_N, args.N - p * TILE_N)) * dm * dm;
+                            }
+                    } else {
+                        sq = 0.0f;
+#pragma unroll
+                        for (int p = 0; p < MAX_CLUSTER; ++p)
+                            if (p < nt) sq += pp[p].x;
+                    }
                 } else {
                     mean = pa;
                     sq = Cfg::kLN ? pb : pa;
+                }
+                if (GLOBALX && affine) {  // the whole slot is written before the first conversion
+                    ok = mbar_wait(guard, bar_afff0 + 8u * grp, jph, SITE_EPI_AFF, lt);
+                    if (!__all_sync(0xffffffffu, ok)) break;
                 }
                 // LayerNorm: (acc - mean) * rsqrt(M2/N + eps); RMSNorm: acc * rsqrt(ss/N + eps)
                 const float rstd = rsqrtf(fmaf(sq, args.inv_len, args.eps));
@@ -490,10 +598,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             }
 
             // -- normalize, convert, stage (128B swizzle) and store 64 columns at
-            //    a time.  Post-norm starts with the segment still in registers.
+            //    a time.  Post-norm starts with the segment it kept in registers.
             for (int k = 0; k < nseg; ++k) {
                 const int sg = Cfg::kPost ? nseg - 1 - k : k;
-                if (!(Cfg::kPost && k == 0)) {
+                if (!(KEEP_SEG && k == 0)) {
                     tmem_load_seg<NC>(tacc + sg * SEG, v);
                     if (k == nseg - 1) {  // last TMEM read of this tile
                         tc_fence_before();
@@ -515,10 +623,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
                         if (c0 < nstore) {
                             uint32_t pk[32];
                             if (affine)
-                                convert64<true>(v[2 * q], v[2 * q + 1], scale2, bias2, saff + c0 * 2,
-                                                saff + (TILE_N + c0) * 2, pk);
+                                convert64<AFF_SMEM>(v[2 * q], v[2 * q + 1], scale2, bias2, saff + c0 * 2,
+                                                    saff + (TILE_N + c0) * 2, pk);
                             else
-                                convert64<false>(v[2 * q], v[2 * q + 1], scale2, bias2, 0, 0, pk);
+                                convert64<AFF_NONE>(v[2 * q], v[2 * q + 1], scale2, bias2, 0, 0, pk);
                             const uint32_t rowp = sStg + static_cast<uint32_t>((warp + q) * STORE_BUF_BYTES) +
                                                   static_cast<uint32_t>(lane * 128);
 #pragma unroll
@@ -542,6 +650,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
             if (!released) {
                 tc_fence_before();
                 mbar_arrive(bar_acce0 + 8u * b);  // TMEM buffer b may be overwritten
+            }
+            if (GLOBALX && affine) {  // this warp is done with the group's affine slot
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_affe0 + 8u * grp);
             }
         }
         if (lane == 0) bulk_wait_all<0>();
@@ -596,6 +708,18 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
     // ---- teardown
     tc_fence_before();
     __syncthreads();
+    if (GLOBALX && threadIdx.x == 0) {
+        // Every CTA counts itself out; the last one resets the count, records
+        // how many counters this launch used (the next launch clears them)
+        // and advances the epoch.
+        int* const hdr = args.xcnt;
+        const int e = ld_acquire_gpu(hdr + 2);
+        if (atom_acq_rel_gpu_add(hdr, 1) == static_cast<int>(gridDim.x) - 1) {
+            hdr[0] = 0;
+            hdr[3] = args.m_tiles;
+            st_release_gpu(hdr + 2, e + 1);
+        }
+    }
     if (CLUSTERED) {
         // No CTA leaves while a peer may still write into its shared memory.
         cluster_arrive_release();
@@ -607,13 +731,14 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, CLUSTERED>::THREADS, 1)
     }
 }
 
-template <int EPI, int TILE_N, bool CLUSTERED>
+template <int EPI, int TILE_N, int XCH>
 GemmVariant make_variant() {
-    using Cfg = GemmCfg<EPI, TILE_N, CLUSTERED>;
+    using Cfg = GemmCfg<EPI, TILE_N, XCH>;
     return GemmVariant{EPI,
                        TILE_N,
-                       CLUSTERED,
-                       reinterpret_cast<const void*>(&nf_gemm_kernel<EPI, TILE_N, CLUSTERED>),
+                       XCH == XCH_CLUSTER,
+                       XCH,
+                       reinterpret_cast<const void*>(&nf_gemm_kernel<EPI, TILE_N, XCH>),
                        Cfg::THREADS,
                        Cfg::SMEM_BYTES,
                        Cfg::STAGES,

@@ -6,8 +6,8 @@ namespace nf {
 
 const GemmVariant* gemm_variants_plain(int* count) {
     static const GemmVariant v[] = {
-        make_variant<EPI_PLAIN, 64, false>(), make_variant<EPI_PLAIN, 128, false>(),
-        make_variant<EPI_PLAIN, 256, false>()};
+        make_variant<EPI_PLAIN, 64, XCH_NONE>(), make_variant<EPI_PLAIN, 128, XCH_NONE>(),
+        make_variant<EPI_PLAIN, 256, XCH_NONE>()};
     *count = 3;
     return v;
 }

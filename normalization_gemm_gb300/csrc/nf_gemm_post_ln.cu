@@ -6,10 +6,11 @@ namespace nf {
 
 const GemmVariant* gemm_variants_post_ln(int* count) {
     static const GemmVariant v[] = {
-        make_variant<EPI_POST_LN, 64, false>(), make_variant<EPI_POST_LN, 128, false>(),
-        make_variant<EPI_POST_LN, 256, false>(), make_variant<EPI_POST_LN, 256, true>(),
-        make_wide_variant<EPI_POST_LN, false>(), make_wide_variant<EPI_POST_LN, true>()};
-    *count = 6;
+        make_variant<EPI_POST_LN, 64, XCH_NONE>(), make_variant<EPI_POST_LN, 128, XCH_NONE>(),
+        make_variant<EPI_POST_LN, 256, XCH_NONE>(), make_variant<EPI_POST_LN, 256, XCH_CLUSTER>(),
+        make_wide_variant<EPI_POST_LN, false>(), make_wide_variant<EPI_POST_LN, true>(),
+        make_variant<EPI_POST_LN, 256, XCH_GLOBAL>()};
+    *count = 7;
     return v;
 }
 

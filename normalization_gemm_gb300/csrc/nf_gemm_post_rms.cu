@@ -6,10 +6,11 @@ namespace nf {
 
 const GemmVariant* gemm_variants_post_rms(int* count) {
     static const GemmVariant v[] = {
-        make_variant<EPI_POST_RMS, 64, false>(), make_variant<EPI_POST_RMS, 128, false>(),
-        make_variant<EPI_POST_RMS, 256, false>(), make_variant<EPI_POST_RMS, 256, true>(),
-        make_wide_variant<EPI_POST_RMS, false>(), make_wide_variant<EPI_POST_RMS, true>()};
-    *count = 6;
+        make_variant<EPI_POST_RMS, 64, XCH_NONE>(), make_variant<EPI_POST_RMS, 128, XCH_NONE>(),
+        make_variant<EPI_POST_RMS, 256, XCH_NONE>(), make_variant<EPI_POST_RMS, 256, XCH_CLUSTER>(),
+        make_wide_variant<EPI_POST_RMS, false>(), make_wide_variant<EPI_POST_RMS, true>(),
+        make_variant<EPI_POST_RMS, 256, XCH_GLOBAL>()};
+    *count = 7;
     return v;
 }
 

@@ -387,10 +387,10 @@ __global__ void __launch_bounds__(WideCfg<EPI, CLUSTERED>::THREADS, 1)
                 if (c0 < nstore) {
                     uint32_t pk[32];
                     if (affine)
-                        convert64<true>(v[0], v[1], scale2, bias2, saff + (col0 + c0) * 2,
-                                        saff + (Cfg::TILE_N + col0 + c0) * 2, pk);
+                        convert64<AFF_SMEM>(v[0], v[1], scale2, bias2, saff + (col0 + c0) * 2,
+                                            saff + (Cfg::TILE_N + col0 + c0) * 2, pk);
                     else
-                        convert64<false>(v[0], v[1], scale2, bias2, 0, 0, pk);
+                        convert64<AFF_NONE>(v[0], v[1], scale2, bias2, 0, 0, pk);
                     const uint32_t sb = sStg + static_cast<uint32_t>(warp * STORE_BUF_BYTES);
                     if (lane == 0) bulk_wait_read<0>();  // the previous store has read the box
                     __syncwarp();
@@ -435,6 +435,7 @@ GemmVariant make_wide_variant() {
     return GemmVariant{EPI,
                        Cfg::TILE_N,
                        CLUSTERED,
+                       CLUSTERED ? XCH_CLUSTER : XCH_NONE,
                        reinterpret_cast<const void*>(&nf_gemm_wide_kernel<EPI, CLUSTERED>),
                        Cfg::THREADS,
                        Cfg::SMEM_BYTES,

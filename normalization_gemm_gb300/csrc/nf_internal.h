@@ -23,28 +23,63 @@ constexpr int STAGING_BYTES = EPI_WARPS * STORE_BUF_BYTES;                 // on
 constexpr int MAX_CLUSTER = 16;           // post-norm: N <= 256 x 16
 constexpr int SMEM_OPTIN_LIMIT = 232448;  // 227 KB of dynamic shared memory per block
 constexpr int MAX_STAGES = 8;
-constexpr int NUM_BARRIER_SLOTS = 25;     // full[8] empty[8] acc_full[2] acc_empty[2] ss_full[2] xch[2] mma_done
+constexpr int NUM_BARRIER_SLOTS = 29;     // full[8] empty[8] acc_full[2] acc_empty[2] ss_full[2] xch[2] mma_done
+                                          // aff_full[2] aff_empty[2]
 
 enum Epilogue : int { EPI_PLAIN = 0, EPI_PRE_RMS = 1, EPI_POST_LN = 2, EPI_POST_RMS = 3 };
 
-template <int EPI, int TILE_N, bool CLUSTERED>
+// How the CTAs that share an output row exchange partial row statistics
+// (post-norm with the row split over several CTAs).
+enum Exchange : int {
+    XCH_NONE = 0,     // one CTA owns whole rows
+    XCH_CLUSTER = 1,  // the row's CTAs form a thread-block cluster; DSMEM
+    XCH_GLOBAL = 2,   // the row's CTAs are any CTAs of a co-resident grid; L2
+};
+
+// Global-exchange scratch (device memory, zero when first set up), two
+// regions whose sizes are fixed when the buffer is set up:
+//   xcnt   int: [0] exit count, [2] launch epoch E (the last CTA to leave a
+//          launch advances it), [3] row tiles of that launch; from XCH_CNT0
+//          two banks of xbank ints, one arrival counter per (row tile,
+//          32-row quarter).  Launch E counts in bank E & 1, which the launch
+//          before it cleared, and clears the other bank, which that launch
+//          used: no counter is ever reset while it may be read, and a launch
+//          that gave up part-way leaves nothing behind.
+//   xstats float2 partial (mean, M2) or (sum of squares, 0) per
+//          (row tile, column tile, tile row)
+constexpr int XCH_CNT0 = 64;  // banks start 256 bytes in
+__host__ __device__ inline int64_t xch_bank_ints(int m_tiles) { return static_cast<int64_t>(m_tiles) * 4; }
+__host__ __device__ inline int64_t xch_stats_bytes(int m_tiles, int n_tiles) {
+    return static_cast<int64_t>(m_tiles) * n_tiles * 128 * 8;
+}
+
+template <int EPI, int TILE_N, int XCH>
 struct GemmCfg {
     static constexpr bool kPre = EPI == EPI_PRE_RMS;
     static constexpr bool kPost = EPI == EPI_POST_LN || EPI == EPI_POST_RMS;
     static constexpr bool kLN = EPI == EPI_POST_LN;
+    static constexpr bool CLUSTERED = XCH == XCH_CLUSTER;
     static_assert(TILE_N == 64 || TILE_N == 128 || TILE_N == 256, "tile_n");
-    static_assert(!CLUSTERED || (kPost && TILE_N == 256), "clusters only for post-norm");
+    static_assert(XCH == XCH_NONE || (kPost && TILE_N == 256), "row exchange only for post-norm");
 
     static constexpr int B_STAGE_BYTES = TILE_K * TILE_N * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     // per-row partial statistics received from every CTA of the cluster,
     // double buffered by tile parity: [2][MAX_CLUSTER][TILE_M] x float2
     static constexpr int RECV_BYTES = CLUSTERED ? 2 * MAX_CLUSTER * TILE_M * 8 : 0;
-    static constexpr int AFFINE_BYTES = kPost ? 2 * TILE_N * 2 : 0;   // gamma, beta (bf16)
+    // gamma, beta (bf16) of the CTA's fixed column tile; the global exchange
+    // moves across column tiles and keeps one slot per epilogue warpgroup,
+    // refilled for each tile.
+    static constexpr int AFFINE_BYTES = !kPost ? 0 : (XCH == XCH_GLOBAL ? 2 * (2 * TILE_N * 2) : 2 * TILE_N * 2);
     static constexpr int SS_BYTES = kPre ? 2 * TILE_M * 4 : 0;        // sum of squares [2][128]
     static constexpr int BAR_BYTES = 256;                             // barriers + 2 words
+    // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
+    // starts 1 KB aligned in practice; the global-exchange variant, whose
+    // fourth pipeline stage needs the room, relies on that (and checks it at
+    // run time), the others keep 1 KB of slack to realign.
+    static constexpr int ALIGN_SLACK = XCH == XCH_GLOBAL ? 0 : 1024;
     static constexpr int FIXED_BYTES =
-        1024 /* alignment slack */ + STAGING_BYTES + RECV_BYTES + AFFINE_BYTES + SS_BYTES + BAR_BYTES;
+        ALIGN_SLACK + STAGING_BYTES + RECV_BYTES + AFFINE_BYTES + SS_BYTES + BAR_BYTES;
     static constexpr int STAGES_FIT = (SMEM_OPTIN_LIMIT - FIXED_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
     static_assert(STAGES >= 2, "pipeline needs two stages");
@@ -58,7 +93,7 @@ struct GemmCfg {
     static constexpr int OFF_SS = OFF_AFF + AFFINE_BYTES;
     static constexpr int OFF_BAR = OFF_SS + SS_BYTES;
     static_assert(OFF_B % 1024 == 0 && OFF_STG % 1024 == 0, "swizzled buffers need 1 KB alignment");
-    static_assert(NUM_BARRIER_SLOTS * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(NUM_BARRIER_SLOTS * 8 + 8 <= BAR_BYTES, "barrier area + 2 words");
 
     static constexpr int PRODUCER_WARP = EPI_WARPS;       // 8
     static constexpr int MMA_WARP = EPI_WARPS + 1;        // 9
@@ -82,6 +117,9 @@ struct GemmArgs {
     float* rstd_out;        // M entries or null
     uint32_t* status;       // device status word (4 x u32)
     uint64_t timeout_ns;
+    int* xcnt;              // global exchange only: XCH_CNT0 + 2 * xbank ints
+    int32_t xbank;          // ints per counter bank, >= xch_bank_ints(m_tiles)
+    float2* xstats;         // global exchange only: >= xch_stats_bytes(m_tiles, n_tiles)
 };
 
 // Wait sites recorded in the status word on a time-out.
@@ -96,12 +134,16 @@ enum WaitSite : uint32_t {
     SITE_SS_ACC_EMPTY = 8,
     SITE_SELFTEST = 9,
     SITE_EPI_PAIR = 10,
+    SITE_EPI_GXCH = 11,
+    SITE_EPI_AFF = 12,
+    SITE_SMEM_ALIGN = 13,  // code NF_ERR_ALIGNMENT: dynamic shared memory not 1 KB aligned
 };
 
 // One compiled GEMM variant.
 struct GemmVariant {
     int epi, tile_n;
-    bool clustered;
+    bool clustered;  // xch == XCH_CLUSTER
+    int xch;
     const void* func;
     int threads, smem_bytes, stages, tmem_cols;
     int tile_k;  // K per ring stage: 64 (X boxes 128-byte swizzled) or 32 (64-byte swizzled)

@@ -115,6 +115,82 @@ __device__ __forceinline__ bool mbar_wait(const WaitGuard& g, uint32_t bar, uint
     }
 }
 
+// ------------------------------------------------------------------ global-memory counters
+// GPU-scope acquire load of a counter written by other CTAs.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// GPU-scope relaxed load: coherent at GPU scope without the acquire's cache
+// invalidation (polling with acquire loads measurably slows the shared-memory
+// traffic of the other warps on the SM).
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// GPU-scope acquire-release fence: after a relaxed load that observed a
+// release, makes the releasing side's earlier writes visible (acquire pattern).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// GPU-scope release store.
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// GPU-scope acquire-release add; returns the previous value.
+__device__ __forceinline__ int atom_acq_rel_gpu_add(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// GPU-scope release add (no return value).
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded warp-wide wait until *p >= target.  Lane 0 polls with relaxed
+// loads (backing off with nanosleep); once the target is seen, one fence
+// turns the observation into an acquire for the whole warp.  Gives up like
+// mbar_wait when the CTA aborts or the time limit passes.
+__device__ __forceinline__ bool gwait_geq(const WaitGuard& g, const int* p, int target, uint32_t site,
+                                          uint32_t tile) {
+    const bool l0 = (threadIdx.x & 31u) == 0;
+    int state = 0;  // lane 0: 1 reached, 2 aborted, 3 timed out
+    if (l0) {
+        if (ld_relaxed_gpu(p) >= target) {
+            state = 1;
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            uint32_t ns = 64;
+            while (true) {
+                __nanosleep(ns);
+                if (ns < 512) ns <<= 1;
+                if (ld_relaxed_gpu(p) >= target) {
+                    state = 1;
+                    break;
+                }
+                if (*g.abort_flag) {
+                    state = 2;
+                    break;
+                }
+                if (globaltimer_ns() - t0 > g.timeout_ns) {
+                    record_failure(g, 5u /* NF_ERR_TIMEOUT */, site, tile);
+                    state = 3;
+                    break;
+                }
+            }
+        }
+        if (state == 1) fence_acq_rel_gpu();
+    }
+    state = __shfl_sync(0xffffffffu, state, 0);  // orders the other lanes after lane 0's fence
+    return state == 1;
+}
+
 // ------------------------------------------------------------------ programmatic dependent launch
 // Blocks until every grid this one depends on has completed and its memory is
 // visible (a no-op when the launch has no programmatic dependency).
@@ -361,6 +437,10 @@ __device__ __forceinline__ float f2_hsum(uint64_t v) {
 
 // Two bf16 in one 32-bit word -> a packed fp32 pair (exact).
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) { return f2_pack(w << 16, w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t a) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

@@ -23,7 +23,7 @@ def test_exports_every_declared_symbol(L):
     assert "nf_gemm_prenorm_rms" in names and "nf_norm_rows" in names
     for name in names:
         assert hasattr(L, name), f"{name} declared in nf.h but not exported"
-    assert L.nf_abi_version() == 1
+    assert L.nf_abi_version() == 2
 
 
 def test_status_strings(L):
@@ -78,28 +78,82 @@ def test_timeout_setting_range(L):
     assert L.nf_set_wait_timeout_ns(2_000_000_000) == OK
 
 
-@pytest.mark.parametrize("op,M,N,K,tile_n,cluster", [
-    (0, 256, 64, 64, 64, 1), (1, 256, 64, 64, 64, 1), (1, 32768, 512, 512, 256, 1),
-    (2, 65536, 128, 128, 128, 1), (2, 16384, 2048, 1024, 512, 4), (3, 16384, 2048, 1024, 512, 4),
-    (2, 8192, 4096, 4096, 512, 8), (2, 300, 264, 72, 512, 1), (2, 5, 8, 8, 64, 1),
-    (0, 100, 200, 8, 256, 1), (1, 100, 120, 8, 128, 1), (3, 64, 4088, 64, 512, 8),
+@pytest.mark.parametrize("op,M,N,K,tile_n,cluster,xch", [
+    (0, 256, 64, 64, 64, 1, 0), (1, 256, 64, 64, 64, 1, 0), (1, 32768, 512, 512, 256, 1, 0),
+    (2, 65536, 128, 128, 128, 1, 0), (2, 16384, 2048, 1024, 256, 1, 2), (3, 16384, 2048, 1024, 256, 1, 2),
+    (2, 8192, 4096, 4096, 256, 1, 2), (2, 300, 264, 72, 512, 1, 0), (2, 5, 8, 8, 64, 1, 0),
+    (0, 100, 200, 8, 256, 1, 0), (1, 100, 120, 8, 128, 1, 0), (3, 64, 4088, 64, 512, 8, 1),
+    (2, 1000, 256, 64, 256, 1, 0), (2, 16384, 2048, 256, 256, 8, 1), (2, 16384, 512, 1024, 512, 1, 0),
+    (3, 16384, 1024, 512, 256, 1, 2), (2, 16384, 1024, 448, 256, 4, 1),
 ])
-def test_plans(L, op, M, N, K, tile_n, cluster):
+def test_plans(L, op, M, N, K, tile_n, cluster, xch):
     p = nf.plan_gemm(op, M, N, K, 148)
     assert p["tile_m"] == 128 and p["tile_k"] == (32 if tile_n == 512 else 64)
-    assert p["tile_n"] == tile_n and p["cluster"] == cluster
-    assert cluster * tile_n >= N or op in (0, 1)
-    assert cluster <= 8  # the default plans stay within the portable cluster size
+    assert p["tile_n"] == tile_n and p["cluster"] == cluster and p["exchange"] == xch
     assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
     assert p["tmem_cols"] == min(2 * tile_n, 512)
     assert p["threads"] == (448 if op == 1 else 320)
     m_tiles = -(-M // 128)
-    n_tiles = 1 if op >= 2 else -(-N // tile_n)
+    n_tiles = 1 if (op >= 2 and xch != 2) else -(-N // tile_n)
     assert p["tiles"] == m_tiles * n_tiles
-    assert p["grid"] % cluster == 0 and 0 < p["grid"] <= 148
+    assert 0 < p["grid"] <= 148 and p["grid"] % cluster == 0
+    assert cluster <= 8  # automatic plans stay within the portable cluster size
     # 1 CTA per SM whenever the kernel takes all 512 TMEM columns
     if p["tmem_cols"] == 512:
         assert p["smem_bytes"] > 232448 // 2
+
+
+@pytest.mark.parametrize("M,N,K,sms", [
+    (8192, 4096, 4096, 148), (16384, 2048, 1024, 148), (300, 264, 72, 148), (64, 4088, 64, 148),
+    (128 * 9, 4096, 64, 8), (128 * 3, 2048, 64, 152), (65536, 4096, 64, 152), (1, 264, 8, 1),
+])
+def test_global_exchange_schedule_is_deadlock_free(L, M, N, K, sms):
+    """Tile t runs on CTA t mod G, in order; tiles i and i+2 of a CTA share a
+    TMEM buffer, so the later one waits for the earlier one's row exchange.
+    That wait must always point at an earlier row tile."""
+    try:
+        nf.set_postnorm_exchange(nf.XCH_GLOBAL)
+        p = nf.plan_gemm(2, M, N, K, sms)
+    finally:
+        nf.set_postnorm_exchange(0)
+    assert p["exchange"] == 2
+    n_tiles, G = -(-N // 256), p["grid"]
+    assert p["tiles"] == -(-M // 128) * n_tiles and G == min(p["tiles"], sms)
+    for c in range(G):
+        mine = list(range(c, p["tiles"], G))
+        for a, b in zip(mine, mine[2:]):
+            assert a // n_tiles < b // n_tiles
+
+
+def test_too_few_sms_for_the_global_exchange_use_a_cluster(L):
+    try:
+        nf.set_postnorm_exchange(nf.XCH_GLOBAL)
+        p = nf.plan_gemm(2, 128 * 9, 4096, 64, 7)
+    finally:
+        nf.set_postnorm_exchange(0)
+    assert p["exchange"] == 1 and p["cluster"] == 8
+
+
+def test_cluster_exchange_plans(L):
+    try:
+        nf.set_postnorm_exchange(nf.XCH_CLUSTER)
+        p = nf.plan_gemm(2, 8192, 4096, 4096, 148)
+        assert (p["tile_n"], p["cluster"], p["tile_k"], p["exchange"]) == (512, 8, 32, 1)
+        assert p["grid"] % 8 == 0
+        p = nf.plan_gemm(3, 16384, 2048, 1024, 148)
+        assert (p["tile_n"], p["cluster"], p["exchange"]) == (512, 4, 1)
+        p = nf.plan_gemm(2, 300, 264, 72, 148)  # one 512-column CTA covers the row
+        assert (p["tile_n"], p["cluster"], p["exchange"]) == (512, 1, 0)
+        nf.set_postnorm_tile_n(256)
+        p = nf.plan_gemm(2, 8192, 4096, 4096, 148)
+        assert (p["tile_n"], p["cluster"], p["tile_k"], p["exchange"]) == (256, 16, 64, 1)
+        p = nf.plan_gemm(3, 16384, 2048, 1024, 148)
+        assert (p["tile_n"], p["cluster"]) == (256, 8)
+    finally:
+        nf.set_postnorm_tile_n(0)
+        nf.set_postnorm_exchange(0)
+    assert L.nf_set_postnorm_tile_n(384) == INVALID
+    assert L.nf_set_postnorm_exchange(3) == INVALID
 
 
 def test_python_binding_rejects_cpu_tensors():
@@ -115,17 +169,3 @@ def test_empty_m_accepts_null_bases(L):
     assert L.nf_gemm_prenorm_rms(None, P, None, 0, 64, 64, 1e-6, None, None) == OK
     assert L.nf_norm_rows(None, None, None, None, 0, 64, 0, 1e-5, None, None, None) == OK
     assert L.nf_gemm_plain(None, P, None, 1, 64, 64, None) == INVALID
-
-
-def test_forced_256_column_post_norm_plans(L):
-    try:
-        nf.set_postnorm_tile_n(256)
-        p = nf.plan_gemm(2, 8192, 4096, 4096, 148)
-        assert (p["tile_n"], p["cluster"], p["tile_k"]) == (256, 16, 64)
-        p = nf.plan_gemm(3, 16384, 2048, 1024, 148)
-        assert (p["tile_n"], p["cluster"]) == (256, 8)
-        nf.set_postnorm_tile_n(512)
-        assert nf.plan_gemm(2, 300, 264, 72, 148)["tile_n"] == 512
-    finally:
-        nf.set_postnorm_tile_n(0)
-    assert L.nf_set_postnorm_tile_n(384) == INVALID

@@ -74,18 +74,23 @@ POST_SHAPES = [(300, 64, 8), (300, 136, 64), (257, 64, 120), (384, 128, 128), (1
                (130, 64, 2048), (129, 64, 4096), (64, 64, 4088)]
 
 
-@pytest.fixture(params=[0, 256], ids=["auto_tiles", "tile256"])
-def post_tile(request):
-    """Post-norm tiling: automatic (512-column CTAs in clusters of <= 8 when
-    N > 256) or forced 256-column CTAs in clusters of up to 16."""
-    nf.set_postnorm_tile_n(request.param)
+@pytest.fixture(params=[(0, 0), (nf.XCH_GLOBAL, 0), (nf.XCH_CLUSTER, 512), (nf.XCH_CLUSTER, 256)],
+                ids=["auto", "global", "cluster512", "cluster256"])
+def post_mode(request):
+    """How rows wider than 256 columns exchange statistics: the automatic
+    choice, through L2 between 256-column tiles, or inside a thread-block
+    cluster of 512-column CTAs (<= 8) or of 256-column CTAs (<= 16)."""
+    xch, tile = request.param
+    nf.set_postnorm_exchange(xch)
+    nf.set_postnorm_tile_n(tile)
     yield request.param
+    nf.set_postnorm_exchange(0)
     nf.set_postnorm_tile_n(0)
 
 
 @pytest.mark.parametrize("M,K,N", POST_SHAPES)
 @pytest.mark.parametrize("affine", [False, True])
-def test_postnorm_ln(dev, orc, post_tile, M, K, N, affine):
+def test_postnorm_ln(dev, orc, post_mode, M, K, N, affine):
     import torch
     inp = _inputs(M, K, N, seed=3 * M + K + N, gamma=True, beta=True)
     g = inp["gamma"] if affine else None
@@ -103,7 +108,7 @@ def test_postnorm_ln(dev, orc, post_tile, M, K, N, affine):
 
 @pytest.mark.parametrize("M,K,N", POST_SHAPES)
 @pytest.mark.parametrize("affine", [False, True])
-def test_postnorm_rms(dev, orc, post_tile, M, K, N, affine):
+def test_postnorm_rms(dev, orc, post_mode, M, K, N, affine):
     import torch
     inp = _inputs(M, K, N, seed=5 * M + K + N, gamma=True)
     g = inp["gamma"] if affine else None
@@ -153,16 +158,17 @@ def test_many_tiles_per_cta(dev, orc):
     assert_close(y, orc.gemm_plain(inp["X"], inp["W"], rows=rows), "plain persistent")
 
 
-def test_cluster_many_tiles_per_cluster(dev, orc, post_tile):
-    """Clusters (16 x 256 or 8 x 512 columns) walking many m tiles: the
-    exchange barriers and both receive buffers cycle through many phases."""
+def test_cluster_many_tiles_per_cluster(dev, orc, post_mode):
+    """Row tiles many times the resident CTAs: cluster exchange barriers and
+    both receive buffers cycle through many phases; global-exchange counters
+    go up and back to zero many times within one launch."""
     M = 128 * 64 + 5
     inp = _inputs(M, 64, 4096, seed=19, gamma=True, beta=True)
     rows = nf_inputs.sample_rows(M, 160, seed=4)
     y = nf.gemm_postnorm_ln(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-6,
                             to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev))
     ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-6, inp["gamma"], inp["beta"], rows=rows)[0]
-    assert_close(to_f64(y)[rows], ref, "post-ln cluster 16, many tiles")
+    assert_close(to_f64(y)[rows], ref, f"post-ln {post_mode}, many row tiles")
 
 
 # ------------------------------------------------------------ full-size workloads
@@ -372,3 +378,109 @@ def test_split_last_wave_whole_output(dev, orc, op):
     assert_close(to_f64(got), want, f"split last wave {op}")
     if op != "plain":
         np.testing.assert_allclose(stats.cpu().numpy(), wstat, rtol=1e-3)
+
+
+# ------------------------------------------------------------ global exchange
+@pytest.fixture
+def force_global():
+    nf.set_postnorm_exchange(nf.XCH_GLOBAL)
+    yield
+    nf.set_postnorm_exchange(0)
+
+
+def test_global_exchange_across_launches_and_graph_replays(dev, orc, force_global):
+    """The exchange counters live in scratch memory that each launch must
+    leave at zero: back-to-back launches and replays of a captured graph all
+    give the first launch's bits."""
+    import torch
+    M, K, N = 128 * 40 + 3, 64, 4096
+    inp = _inputs(M, K, N, seed=53, gamma=True, beta=True)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    G, B = to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev)
+    assert nf.plan_gemm(2, M, N, K, 148)["exchange"] == nf.XCH_GLOBAL
+    ys = [nf.gemm_postnorm_ln(X, W, 1e-5, G, B) for _ in range(5)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+    rows = nf_inputs.sample_rows(M, 200, seed=6)
+    ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, inp["gamma"], inp["beta"], rows=rows)[0]
+    assert_close(to_f64(ys[0])[rows], ref, "global exchange, first launch")
+
+    s = torch.cuda.Stream()
+    out = torch.empty_like(ys[0])
+    with torch.cuda.stream(s):  # sets up the stream's scratch before capture
+        nf.gemm_postnorm_ln(X, W, 1e-5, G, B, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nf.gemm_postnorm_ln(X, W, 1e-5, G, B, out=out)
+        nf.gemm_postnorm_ln(X, W, 1e-5, G, B, out=out)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ys[0])
+    assert nf.device_status()[0] == nf.NF_OK
+
+
+def test_global_exchange_unaligned_affine(dev, orc, force_global):
+    """gamma / beta only 2-byte aligned: the epilogue falls back to scalar
+    loads of the affine parameters (ragged N: the last tile holds 8 columns)."""
+    import torch
+    M, K, N = 300, 64, 1032
+    inp = _inputs(M, K, N, seed=59, gamma=True, beta=True)
+    gbuf = torch.zeros(N + 1, dtype=torch.bfloat16, device=dev)
+    bbuf = torch.zeros(N + 1, dtype=torch.bfloat16, device=dev)
+    gbuf[1:] = to_dev(inp["gamma"], dev)
+    bbuf[1:] = to_dev(inp["beta"], dev)
+    g, b = gbuf[1:], bbuf[1:]
+    assert g.data_ptr() % 16 != 0
+    y = nf.gemm_postnorm_ln(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-5, g, b)
+    ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, inp["gamma"], inp["beta"])[0]
+    assert_close(to_f64(y), ref, "global exchange, unaligned gamma/beta")
+    y = nf.gemm_postnorm_rms(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-5, g)
+    ref = orc.gemm_postnorm_rms(inp["X"], inp["W"], 1e-5, inp["gamma"])[0]
+    assert_close(to_f64(y), ref, "global exchange rms, unaligned gamma")
+
+
+def test_global_exchange_on_two_streams(dev, force_global):
+    """Each stream has its own scratch: launches on two streams may overlap and
+    still give the single-stream bits."""
+    import torch
+    a = _inputs(1024, 256, 2048, seed=61, gamma=True, beta=True)
+    b = _inputs(777, 128, 4096, seed=67, gamma=True)
+    XA, WA = to_dev(a["X"], dev), to_dev(a["W"], dev)
+    GA, BA = to_dev(a["gamma"], dev), to_dev(a["beta"], dev)
+    XB, WB, GB = to_dev(b["X"], dev), to_dev(b["W"], dev), to_dev(b["gamma"], dev)
+    ref_a = nf.gemm_postnorm_ln(XA, WA, 1e-5, GA, BA)
+    ref_b = nf.gemm_postnorm_rms(XB, WB, 1e-6, GB)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            ya = [nf.gemm_postnorm_ln(XA, WA, 1e-5, GA, BA) for _ in range(4)]
+        with torch.cuda.stream(s2):
+            yb = [nf.gemm_postnorm_rms(XB, WB, 1e-6, GB) for _ in range(4)]
+        torch.cuda.synchronize()
+        for y in ya:
+            assert torch.equal(y, ref_a)
+        for y in yb:
+            assert torch.equal(y, ref_b)
+
+
+def test_global_exchange_shape_sequence_on_one_stream(dev, orc, force_global):
+    """Shapes with different row-tile counts share one stream's scratch: a
+    launch with more row tiles must find zero counters where an earlier launch
+    with fewer row tiles (and more column tiles) wrote statistics; the last
+    shape grows the buffer."""
+    import torch
+    for i, (M, K, N) in enumerate([(128 * 65 + 5, 64, 4096), (128 * 300, 64, 512), (128 * 65 + 5, 64, 4096),
+                                   (128 * 1100, 64, 1024)]):
+        inp = _inputs(M, K, N, seed=71 + i, gamma=True, beta=True)
+        y = nf.gemm_postnorm_ln(to_dev(inp["X"], dev), to_dev(inp["W"], dev), 1e-5, to_dev(inp["gamma"], dev),
+                                to_dev(inp["beta"], dev))
+        rows = nf_inputs.sample_rows(M, 256, seed=i)
+        ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, inp["gamma"], inp["beta"], rows=rows)[0]
+        assert_close(to_f64(y)[rows], ref, f"global exchange sequence {M}x{K}x{N}")
+        torch.cuda.synchronize()
+        assert nf.device_status()[0] == nf.NF_OK
