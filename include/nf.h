@@ -126,6 +126,28 @@ nf_status nf_gemm_postnorm_ln(const void* X, const void* W, const void* gamma,
                               float* rstd_out, nf_stream stream);
 
 /*
+ * nf_gemm_postnorm_ln_noalloc -- nf_gemm_postnorm_ln that allocates no
+ * memory at any time, on any call.  The blog has no counterpart: this is a
+ * deployment variant.  Same arguments, plan, kernels and results as
+ * nf_gemm_postnorm_ln.  Where that plan exchanges row statistics through L2,
+ * the scratch is a fixed device array inside the library (about 4.1 MiB per
+ * device, cleared on the first call on each device) instead of the
+ * per-stream buffer.  Limits of that array: ceil(M / 128) * ceil(N / 256)
+ * <= 4096 and M <= 2^21, else NF_ERR_UNSUPPORTED_SHAPE (only for shapes that
+ * use the L2 exchange).
+ * Races: the array is one per device, shared by every stream and every
+ * thread.  Two calls that may run on the device at the same time (on
+ * different streams, or from graphs replayed concurrently) corrupt each
+ * other's exchange; the caller serializes them (one stream, or events).
+ * Calls ordered on one stream are safe.
+ */
+nf_status nf_gemm_postnorm_ln_noalloc(const void* X, const void* W,
+                                      const void* gamma, const void* beta,
+                                      void* Y, int64_t M, int64_t N, int64_t K,
+                                      float eps, float* mean_out,
+                                      float* rstd_out, nf_stream stream);
+
+/*
  * nf_gemm_postnorm_rms -- Y = RMSNorm(X * W) * gamma over each row of N
  * (blog §3 with RMSNorm).  gamma optional (NULL = 1); rstd_out optional.
  * N <= NF_POSTNORM_MAX_N, else NF_ERR_UNSUPPORTED_SHAPE.

@@ -62,6 +62,7 @@ _SIGS = {
     "nf_gemm_plain": [_VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_gemm_prenorm_rms": [_VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
     "nf_gemm_postnorm_ln": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
+    "nf_gemm_postnorm_ln_noalloc": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
     "nf_gemm_postnorm_rms": [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
     "nf_norm_rows": [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
     "nf_get_device_status": [_VP],
@@ -197,6 +198,23 @@ def gemm_postnorm_ln(x, w, eps, gamma=None, beta=None, out=None, mean_out=None, 
                                      _vec(mean_out, "mean_out", M, torch.float32),
                                      _vec(rstd_out, "rstd_out", M, torch.float32),
                                      _stream(stream)), "nf_gemm_postnorm_ln")
+    return y
+
+
+def gemm_postnorm_ln_noalloc(x, w, eps, gamma=None, beta=None, out=None, mean_out=None, rstd_out=None,
+                             stream=None):
+    """gemm_postnorm_ln whose L2 exchange uses the library's fixed per-device
+    scratch array (no allocation; calls that may overlap must be serialized)."""
+    torch = _torch()
+    M, N, K = _shapes(x, w)
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_postnorm_ln_noalloc(_mat(x, "x"), _mat(w, "w"),
+                                             _vec(gamma, "gamma", N, torch.bfloat16),
+                                             _vec(beta, "beta", N, torch.bfloat16), _mat(y, "out"),
+                                             M, N, K, float(eps),
+                                             _vec(mean_out, "mean_out", M, torch.float32),
+                                             _vec(rstd_out, "rstd_out", M, torch.float32),
+                                             _stream(stream)), "nf_gemm_postnorm_ln_noalloc")
     return y
 
 

@@ -106,6 +106,17 @@ struct XScratch {
     static int64_t stats_offset(int64_t bank_ints) { return ((XCH_CNT0 + 2 * bank_ints) * 4 + 255) / 256 * 256; }
 };
 constexpr int kMaxScratch = 64;
+
+// Fixed exchange scratch of nf_gemm_postnorm_ln_noalloc: a file-scope device
+// array (header, two counter banks, partial statistics), so that entry point
+// allocates nothing at any time.  Zero when set up on a device.
+constexpr int64_t kNoAllocBankInts = 16384;      // row tiles (M <= 2^21)
+constexpr int64_t kNoAllocStatsBytes = 4 << 20;  // m_tiles * n_tiles <= 4096
+constexpr int64_t kNoAllocStatsOffset = (XCH_CNT0 + 2 * kNoAllocBankInts) * 4;
+constexpr int64_t kNoAllocBytes = kNoAllocStatsOffset + kNoAllocStatsBytes;
+static_assert(kNoAllocStatsOffset % 256 == 0, "statistics region alignment");
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+uint8_t* g_noalloc_ptr[64] = {};
 XScratch g_xs[kMaxScratch];
 int g_xs_n = 0;
 
@@ -438,8 +449,32 @@ nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, 
     return NF_OK;
 }
 
+// The current device's fixed no-alloc scratch: address looked up and the
+// array cleared on first use per device.
+nf_status noalloc_scratch(uint8_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(NF_ERR_NO_DEVICE, "device index out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess)
+            return fail_cuda(e, "cudaGetSymbolAddress(no-alloc scratch)");
+        if ((e = cudaMemset(p, 0, static_cast<size_t>(kNoAllocBytes))) != cudaSuccess)
+            return fail_cuda(e, "clear no-alloc scratch");
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return NF_OK;
+}
+
+// fixed_scratch: the global exchange uses the no-alloc array instead of the
+// stream's scratch buffer.
 nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
-                   int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream) {
+                   int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream,
+                   bool fixed_scratch = false) {
     nf_status st = check_gemm_args(op, X, W, Y, gamma, beta, mean_out, rstd_out, M, N, K, eps);
     if (st != NF_OK) return st;
     if (M == 0) return NF_OK;
@@ -494,7 +529,18 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         const int cap = per_sm * d->sm_count;
         grid = tiles < cap ? tiles : cap;
         if (2 * grid < p.n_tiles) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too few resident CTAs for the exchange");
-        if ((st = xch_scratch(stream, p.m_tiles, p.n_tiles, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) return st;
+        if (fixed_scratch) {
+            if (xch_bank_ints(p.m_tiles) > kNoAllocBankInts || xch_stats_bytes(p.m_tiles, p.n_tiles) > kNoAllocStatsBytes)
+                return fail(NF_ERR_UNSUPPORTED_SHAPE,
+                            "no-alloc post-norm: ceil(M/128) * ceil(N/256) must be <= 4096 and M <= 2^21");
+            uint8_t* base = nullptr;
+            if ((st = noalloc_scratch(&base)) != NF_OK) return st;
+            a.xcnt = reinterpret_cast<int*>(base);
+            a.xbank = static_cast<int32_t>(kNoAllocBankInts);
+            a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
+        } else if ((st = xch_scratch(stream, p.m_tiles, p.n_tiles, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
+            return st;
+        }
     } else {
         const int tiles = p.m_tiles * p.n_tiles;
         grid = tiles < d->sm_count ? tiles : d->sm_count;
@@ -564,6 +610,13 @@ nf_status nf_gemm_postnorm_ln(const void* X, const void* W, const void* gamma, c
                               int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, nf_stream stream) {
     return run_gemm(OP_POST_LN, X, W, gamma, beta, Y, M, N, K, eps, mean_out, rstd_out,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+nf_status nf_gemm_postnorm_ln_noalloc(const void* X, const void* W, const void* gamma, const void* beta, void* Y,
+                                      int64_t M, int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out,
+                                      nf_stream stream) {
+    return run_gemm(OP_POST_LN, X, W, gamma, beta, Y, M, N, K, eps, mean_out, rstd_out,
+                    reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 nf_status nf_gemm_postnorm_rms(const void* X, const void* W, const void* gamma, void* Y, int64_t M, int64_t N,
