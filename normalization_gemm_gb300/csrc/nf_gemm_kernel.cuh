@@ -406,6 +406,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         // statistics exchange, except the global exchange, whose partials of up
         // to 16 column tiles need those registers: it reads the segment again.
         constexpr bool KEEP_SEG = Cfg::kPost && !GLOBALX;
+        // The global exchange's release fence (lane 0) should not wait for
+        // this warp's bulk stores: another lane issues them.
+        constexpr int STORE_LANE = GLOBALX ? 31 : 0;
         constexpr int NC = SEG / 32;
         const int grp = warp >> 2;
         const int qtr = warp & 3;
@@ -615,7 +618,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                 const int cs = sg * SEG;
                 if (cs < nstore) {
                     const uint64_t scale2 = f2_splat(scale), bias2 = f2_splat(bias);
-                    if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
+                    if (lane == STORE_LANE) bulk_wait_read<0>();  // the previous store has read the buffer
                     __syncwarp();
 #pragma unroll
                     for (int q = 0; q < NQ; ++q) {
@@ -637,7 +640,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
+                    if (lane == STORE_LANE) {
 #pragma unroll
                         for (int q = 0; q < NQ; ++q)
                             if (cs + q * STORE_COLS < nstore)
@@ -656,7 +659,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                 if (lane == 0) mbar_arrive(bar_affe0 + 8u * grp);
             }
         }
-        if (lane == 0) bulk_wait_all<0>();
+        if (lane == STORE_LANE) bulk_wait_all<0>();
         __syncwarp();
     } else if (Cfg::kPre && warp >= Cfg::SUMSQ_WARP0) {
         // ================================================================ row sums of squares

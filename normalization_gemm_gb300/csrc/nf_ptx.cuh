@@ -166,10 +166,9 @@ __device__ __forceinline__ bool gwait_geq(const WaitGuard& g, const int* p, int 
             state = 1;
         } else {
             const uint64_t t0 = globaltimer_ns();
-            uint32_t ns = 64;
+            const uint32_t ns = 32;
             while (true) {
                 __nanosleep(ns);
-                if (ns < 512) ns <<= 1;
                 if (ld_relaxed_gpu(p) >= target) {
                     state = 1;
                     break;
