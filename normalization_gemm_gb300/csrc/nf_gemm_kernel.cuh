@@ -245,6 +245,11 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
 
     // ---- set-up: barriers, TMEM, affine parameters
     if (threadIdx.x == 0) {
+        // The tensor maps are kernel parameters, independent of any earlier
+        // grid: fetch them while a preceding kernel may still be running.
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmY);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full0 + 8u * s, 1);
             mbar_init(bar_empty0 + 8u * s, 1 + (Cfg::kPre ? 128 : 0));
@@ -272,8 +277,24 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
         tmem_relinquish();
     }
+    // Warm L2 with this CTA's first ring-full of X K-tiles while a preceding
+    // grid may still be running.  A prefetch only fills L2 lines, and L2 is
+    // where that grid's writes land, so the loads below never see stale data.
+    if (warp == Cfg::PRODUCER_WARP && lane == 0) {
+        int lt = 0, kt = 0;
+        for (int i = 0; i < STAGES && lt < count; ++i) {
+            int m, n, row0, rows;
+            sched.tile(lt, m, n, row0, rows);
+            tma_prefetch_l2_2d(&tmX, kt * TILE_K, row0);
+            if (++kt == k_tiles) {
+                kt = 0;
+                ++lt;
+            }
+        }
+    }
     // Everything above may overlap the tail of a preceding grid launched with
-    // programmatic serialization; global memory is touched only after this.
+    // programmatic serialization; global memory is read or written only after
+    // this (the prefetches above only warm L2).
     griddep_wait();
     griddep_launch_dependents();
     // Global exchange: count in bank E & 1; clear the other bank, which the
@@ -310,8 +331,6 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
     if (warp == Cfg::PRODUCER_WARP) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tmX);
-            prefetch_tmap(&tmW);
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;
@@ -659,7 +678,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                 if (lane == 0) mbar_arrive(bar_affe0 + 8u * grp);
             }
         }
-        if (lane == STORE_LANE) bulk_wait_all<0>();
+        // Shared memory must outlive the stores' reads of it; their writes
+        // complete with the grid.
+        if (lane == STORE_LANE) bulk_wait_read<0>();
         __syncwarp();
     } else if (Cfg::kPre && warp >= Cfg::SUMSQ_WARP0) {
         // ================================================================ row sums of squares

@@ -131,6 +131,11 @@ __global__ void __launch_bounds__(WideCfg<EPI, CLUSTERED>::THREADS, 1)
 
     // ---- set-up
     if (threadIdx.x == 0) {
+        // The tensor maps are kernel parameters, independent of any earlier
+        // grid: fetch them while a preceding kernel may still be running.
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmY);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(WideBars::FULL + s), 1);
             mbar_init(bar(WideBars::EMPTY + s), 1);
@@ -149,6 +154,19 @@ __global__ void __launch_bounds__(WideCfg<EPI, CLUSTERED>::THREADS, 1)
     if (warp == Cfg::PRODUCER_WARP) {
         tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
         tmem_relinquish();
+        // Warm L2 with this CTA's first ring-full of X K-tiles while a preceding
+        // grid may still be running (a prefetch only fills L2, where that
+        // grid's writes land, so the loads after the wait never see stale data).
+        if (lane == 0) {
+            int lt = 0, kt = 0;
+            for (int i = 0; i < STAGES && lt < count; ++i) {
+                tma_prefetch_l2_2d(&tmX, kt * Cfg::TK, (first + lt * step) * TILE_M);
+                if (++kt == k_tiles) {
+                    kt = 0;
+                    ++lt;
+                }
+            }
+        }
     }
     griddep_wait();
     griddep_launch_dependents();
@@ -170,8 +188,6 @@ __global__ void __launch_bounds__(WideCfg<EPI, CLUSTERED>::THREADS, 1)
     if (warp == Cfg::PRODUCER_WARP) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tmX);
-            prefetch_tmap(&tmW);
             int s = 0;
             uint32_t ph = 0, issued = 0;
             bool ok = true;
@@ -412,7 +428,9 @@ __global__ void __launch_bounds__(WideCfg<EPI, CLUSTERED>::THREADS, 1)
                 mbar_arrive(bar(WideBars::ACC_EMPTY));
             }
         }
-        if (lane == 0) bulk_wait_all<0>();
+        // Shared memory must outlive the stores' reads of it; their writes
+        // complete with the grid.
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
     }
 

@@ -62,6 +62,18 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
     const int chunks = a.cols >> 3;
     const uint4* in = reinterpret_cast<const uint4*>(a.in);
     uint4* out = reinterpret_cast<uint4*>(a.out);
+    // Warm L2 with this CTA's first two row blocks while a preceding grid may
+    // still be running (a prefetch only fills L2, where that grid's writes
+    // land, so the loads after the wait below never see stale data).
+    if (threadIdx.x == 0) {
+        for (int it = 0; it < 2; ++it) {
+            const int64_t r = (static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x) * RPB;
+            if (r < a.rows) {
+                const int64_t nr = a.rows - r < RPB ? a.rows - r : RPB;
+                bulk_prefetch_l2(in + r * chunks, static_cast<uint32_t>(nr * chunks * 16));
+            }
+        }
+    }
     griddep_wait();  // inputs may come from the kernel launched just before
     griddep_launch_dependents();
 

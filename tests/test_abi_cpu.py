@@ -103,14 +103,21 @@ def test_plans(L, op, M, N, K, tile_n, cluster, xch):
         assert p["smem_bytes"] > 232448 // 2
 
 
+def global_exchange_schedule(tiles, G):
+    """Tiles of each CTA, in order, as the L2-exchange kernel walks them: tile t
+    on CTA t mod G (host plan and kernel tile schedule)."""
+    return [list(range(b, tiles, G)) for b in range(G)]
+
+
 @pytest.mark.parametrize("M,N,K,sms", [
     (8192, 4096, 4096, 148), (16384, 2048, 1024, 148), (300, 264, 72, 148), (64, 4088, 64, 148),
     (128 * 9, 4096, 64, 8), (128 * 3, 2048, 64, 152), (65536, 4096, 64, 152), (1, 264, 8, 1),
+    (8192, 3072, 4096, 152), (12345, 1800, 512, 152), (8192, 4096, 4096, 20),
 ])
 def test_global_exchange_schedule_is_deadlock_free(L, M, N, K, sms):
-    """Tile t runs on CTA t mod G, in order; tiles i and i+2 of a CTA share a
-    TMEM buffer, so the later one waits for the earlier one's row exchange.
-    That wait must always point at an earlier row tile."""
+    """Tiles i and i+2 of a CTA share a TMEM buffer, so the later one waits for
+    the earlier one's row exchange: that wait must always point at an earlier
+    row tile, and every tile must run exactly once."""
     try:
         nf.set_postnorm_exchange(nf.XCH_GLOBAL)
         p = nf.plan_gemm(2, M, N, K, sms)
@@ -119,8 +126,10 @@ def test_global_exchange_schedule_is_deadlock_free(L, M, N, K, sms):
     assert p["exchange"] == 2
     n_tiles, G = -(-N // 256), p["grid"]
     assert p["tiles"] == -(-M // 128) * n_tiles and G == min(p["tiles"], sms)
-    for c in range(G):
-        mine = list(range(c, p["tiles"], G))
+    sched = global_exchange_schedule(p["tiles"], G)
+    assert sorted(t for mine in sched for t in mine) == list(range(p["tiles"]))
+    for mine in sched:
+        assert mine == sorted(mine)
         for a, b in zip(mine, mine[2:]):
             assert a // n_tiles < b // n_tiles
 
