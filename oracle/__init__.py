@@ -77,8 +77,13 @@ class Oracle:
                                               ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64]
         lib.nfo_norm_rows.argtypes = [_P_U16, _P_U16, _P_U16, _I64, _I64, ctypes.c_int,
                                       ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64, _P_F64]
+        lib.nfo_gemm_postnorm_bwd.argtypes = [_P_U16, _P_U16, _P_U16, _P_U16, _P_F64, _P_F64, _I64,
+                                              _I64, _I64, ctypes.c_int, _P_I64, _I64, _P_F64]
+        lib.nfo_norm_rows_bwd.argtypes = [_P_U16, _P_U16, _P_U16, _P_F64, _P_F64, _I64, _I64,
+                                          ctypes.c_int, _P_I64, _I64, _P_F64]
         for f in ("nfo_gemm_plain", "nfo_gemm_prenorm_rms", "nfo_gemm_postnorm_ln",
-                  "nfo_gemm_postnorm_rms", "nfo_norm_rows", "nfo_max_threads"):
+                  "nfo_gemm_postnorm_rms", "nfo_norm_rows", "nfo_gemm_postnorm_bwd",
+                  "nfo_norm_rows_bwd", "nfo_max_threads"):
             getattr(lib, f).restype = ctypes.c_int
         lib.nfo_set_threads.argtypes = [ctypes.c_int]
         lib.nfo_set_threads.restype = None
@@ -156,6 +161,40 @@ class Oracle:
                                            eps, rp, R, _f64(out), _f64(mean), _f64(rstd)),
                     "norm_rows")
         return out, (mean if kind == NORM_LN else None), rstd
+
+    @staticmethod
+    def _stats(a, M):
+        if a is None:
+            return None, None
+        v = np.ascontiguousarray(a, dtype=np.float64)
+        assert v.shape == (M,)
+        return v, v.ctypes.data_as(_P_F64)
+
+    def gemm_postnorm_bwd(self, A, B, Z, kind, mean, rstd, gamma=None, rows=None):
+        """dZ = norm_bwd(A @ B; Z, mean, rstd, gamma) (mean: None for RMS)."""
+        M, K = A.shape
+        N = B.shape[1]
+        assert Z.shape == (M, N)
+        r, R, rp = self._rows(rows, M)
+        m, mp = self._stats(mean, M)
+        s, sp = self._stats(rstd, M)
+        dZ = np.empty((R, N), np.float64)
+        self._check(self.lib.nfo_gemm_postnorm_bwd(_u16(A), _u16(B), _u16(Z), _u16(gamma), mp, sp,
+                                                   M, N, K, int(kind), rp, R, _f64(dZ)),
+                    "gemm_postnorm_bwd")
+        return dZ
+
+    def norm_rows_bwd(self, dY, Z, kind, mean, rstd, gamma=None, rows=None):
+        """dZ = norm_bwd(dY; Z, mean, rstd, gamma) row by row (mean: None for RMS)."""
+        Rr, C = dY.shape
+        assert Z.shape == (Rr, C)
+        r, R, rp = self._rows(rows, Rr)
+        m, mp = self._stats(mean, Rr)
+        s, sp = self._stats(rstd, Rr)
+        dZ = np.empty((R, C), np.float64)
+        self._check(self.lib.nfo_norm_rows_bwd(_u16(dY), _u16(Z), _u16(gamma), mp, sp, Rr, C,
+                                               int(kind), rp, R, _f64(dZ)), "norm_rows_bwd")
+        return dZ
 
 
 _DEFAULT: Optional[Oracle] = None

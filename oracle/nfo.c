@@ -258,6 +258,91 @@ int nfo_norm_rows(const uint16_t* in, const uint16_t* gamma,
     return bad ? -1 : 0;
 }
 
+/* Backward of one normalized row of length n, given that row's forward
+ * statistics: g = dy * gamma, xhat = (z - mean) * rstd (LN) or z * rstd
+ * (RMS); dz = rstd * (g - mean(g) - xhat * mean(g * xhat)), the mean(g)
+ * term for LN only.  g and xh are scratch rows of length n. */
+static void norm_bwd_row(const double* dy, const double* z, int64_t n,
+                         const uint16_t* gamma, int kind, double mean, double rstd,
+                         double* g, double* xh, double* dz) {
+    double sg = 0.0, sgx = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        g[j] = gamma ? dy[j] * bf16_to_double(gamma[j]) : dy[j];
+        xh[j] = (kind == NFO_NORM_LN ? z[j] - mean : z[j]) * rstd;
+        sg += g[j];
+        sgx += g[j] * xh[j];
+    }
+    const double mg = kind == NFO_NORM_LN ? sg / (double)n : 0.0;
+    const double mgx = sgx / (double)n;
+    for (int64_t j = 0; j < n; ++j) dz[j] = rstd * (g[j] - mg - xh[j] * mgx);
+}
+
+int nfo_gemm_postnorm_bwd(const uint16_t* A, const uint16_t* B, const uint16_t* Z,
+                          const uint16_t* gamma, const double* mean,
+                          const double* rstd, int64_t M, int64_t N, int64_t K,
+                          int kind, const int64_t* rows, int64_t nrows, double* dZ) {
+    if (!A || !B || !Z || !rstd || !dZ || M < 0 || N <= 0 || K <= 0) return -1;
+    if (kind != NFO_NORM_LN && kind != NFO_NORM_RMS) return -1;
+    if (kind == NFO_NORM_LN && !mean) return -1;
+    if (check_rows(rows, nrows, M)) return -1;
+    const int64_t R = row_count(rows, nrows, M);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* a = (double*)malloc(sizeof(double) * (size_t)K);
+        double* buf = (double*)malloc(sizeof(double) * (size_t)N * 4);
+        if (!a || !buf) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!a || !buf) continue;
+            const int64_t i = row_index(rows, r);
+            double* dy = buf;
+            double* z = buf + N;
+            load_row(A, i, K, a);
+            row_times_w(a, B, N, K, dy);
+            load_row(Z, i, N, z);
+            norm_bwd_row(dy, z, N, gamma, kind, kind == NFO_NORM_LN ? mean[i] : 0.0, rstd[i],
+                         buf + 2 * N, buf + 3 * N, dZ + r * N);
+        }
+        free(a);
+        free(buf);
+    }
+    return bad ? -1 : 0;
+}
+
+int nfo_norm_rows_bwd(const uint16_t* dY, const uint16_t* Z, const uint16_t* gamma,
+                      const double* mean, const double* rstd, int64_t R, int64_t C,
+                      int kind, const int64_t* rows, int64_t nrows, double* dZ) {
+    if (!dY || !Z || !rstd || !dZ || R < 0 || C <= 0) return -1;
+    if (kind != NFO_NORM_LN && kind != NFO_NORM_RMS) return -1;
+    if (kind == NFO_NORM_LN && !mean) return -1;
+    if (check_rows(rows, nrows, R)) return -1;
+    const int64_t n = row_count(rows, nrows, R);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* buf = (double*)malloc(sizeof(double) * (size_t)C * 4);
+        if (!buf) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < n; ++r) {
+            if (!buf) continue;
+            const int64_t i = row_index(rows, r);
+            load_row(dY, i, C, buf);
+            load_row(Z, i, C, buf + C);
+            norm_bwd_row(buf, buf + C, C, gamma, kind, kind == NFO_NORM_LN ? mean[i] : 0.0, rstd[i],
+                         buf + 2 * C, buf + 3 * C, dZ + r * C);
+        }
+        free(buf);
+    }
+    return bad ? -1 : 0;
+}
+
 int nfo_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -66,6 +66,29 @@ int nfo_norm_rows(const uint16_t* in, const uint16_t* gamma,
                   double eps, const int64_t* rows, int64_t nrows, double* out,
                   double* mean_out, double* rstd_out);
 
+/* Backward of the row normalization, from the row statistics the forward
+ * pass saved (blog §3 "What about backward? Fusion regrouping"):
+ *   g = dY * gamma;  xhat = (Z - mean_i) * rstd_i (LN) or Z * rstd_i (RMS);
+ *   LN:  dZ = rstd_i * (g - mean_j g - xhat * mean_j(g * xhat))
+ *   RMS: dZ = rstd_i * (g - xhat * mean_j(g * xhat))
+ * With Z's own statistics this is the gradient of sum(dY * norm(Z)) with
+ * respect to Z.  mean and rstd hold one value per row of Z, indexed by the
+ * row itself (mean is unused, and may be NULL, for RMS); gamma may be NULL.
+ *
+ * nfo_gemm_postnorm_bwd: dY = A B (A is M x K, B is K x N; fp64, never
+ * rounded), then dZ as above, Z being M x N: the norm's backward fused into
+ * the epilogue of the GEMM that produces its incoming gradient. */
+int nfo_gemm_postnorm_bwd(const uint16_t* A, const uint16_t* B, const uint16_t* Z,
+                          const uint16_t* gamma, const double* mean,
+                          const double* rstd, int64_t M, int64_t N, int64_t K,
+                          int kind, const int64_t* rows, int64_t nrows, double* dZ);
+
+/* nfo_norm_rows_bwd: dZ as above for each row of dY (R x C, bf16), the
+ * unfused normalization-backward kernel. */
+int nfo_norm_rows_bwd(const uint16_t* dY, const uint16_t* Z, const uint16_t* gamma,
+                      const double* mean, const double* rstd, int64_t R, int64_t C,
+                      int kind, const int64_t* rows, int64_t nrows, double* dZ);
+
 /* Threads used by the loops over rows (OpenMP). */
 int nfo_max_threads(void);
 void nfo_set_threads(int n);

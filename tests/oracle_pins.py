@@ -18,7 +18,11 @@ What each pin compares against:
                      var/(var+eps) = 1 - eps*rstd^2;
   * closed forms  -- hand-derived results under ``tests/golden/``;
   * reductions    -- W = I and permutation W, unit gain and zero bias,
-                     power-of-two row scales, row-subset consistency.
+                     power-of-two row scales, row-subset consistency;
+  * backward      -- exact rationals, torch float64 autograd through
+                     layer_norm / rms_norm, and the closed-form invariants of a
+                     normalization's gradient (LN rows sum to 0, the
+                     xhat-weighted sum is N rstd^3 eps mean(g xhat)).
 
 Run as a script (``python tests/oracle_pins.py LIB.so``) it loads the given
 library, runs every pin and prints a JSON list of results.
@@ -401,9 +405,154 @@ def pin_closed_forms(o):
             f"closed form {case['name']}: got {got.tolist()} want {want.tolist()}"
 
 
+# ---------------------------------------------------------------- backward
+# The norm's backward fused into the epilogue of the GEMM that produces its
+# incoming gradient (blog §3 "What about backward? Fusion regrouping"), and
+# the unfused row kernel, both from the forward's saved row statistics.
+def _bwd_cases():
+    """Tiny problems: A (M x K), B (K x N), Z (M x N), gamma, and dyadic row
+    statistics (exact in binary; the formula takes any statistics)."""
+    cases = []
+    for seed, (M, K, N) in enumerate([(3, 5, 4), (4, 8, 6), (2, 1, 3)]):
+        inp = nf_inputs.make_inputs(M, K, N, seed=200 + seed, gamma=True, w_var=0.5)
+        rng = np.random.default_rng(300 + seed)
+        Z = bf16_round(rng.normal(0.5, 1.5, size=(M, N)))
+        mean = np.array([0.125 * (i - 1) for i in range(M)])
+        rstd = np.array([0.75 + 0.25 * i for i in range(M)])
+        cases.append((inp["X"], inp["W"], Z, inp["gamma"], mean, rstd))
+    return cases
+
+
+def _bwd_exact(dy, z, g, kind, mean, rstd):
+    """dz of one row in exact rationals, written from the chain rule through
+    y = xhat * g with xhat = (z - mean) * rstd (LN) or z * rstd (RMS)."""
+    n = len(dy)
+    gg = [dy[j] * (g[j] if g is not None else 1) for j in range(n)]
+    xh = [((z[j] - mean) if kind == 0 else z[j]) * rstd for j in range(n)]
+    mg = sum(gg, Fraction(0)) / n if kind == 0 else Fraction(0)
+    mgx = sum((gg[j] * xh[j] for j in range(n)), Fraction(0)) / n
+    return [rstd * (gg[j] - mg - xh[j] * mgx) for j in range(n)]
+
+
+def pin_bruteforce_norm_bwd(o):
+    for A, B, Z, gamma, mean, rstd in _bwd_cases():
+        M, K = A.shape
+        N = B.shape[1]
+        af, bf, zf = _frac_matrix(A), _frac_matrix(B), _frac_matrix(Z)
+        gf = _frac_matrix(gamma)[0]
+        dyf = [[sum((af[i][k] * bf[k][j] for k in range(K)), Fraction(0)) for j in range(N)]
+               for i in range(M)]
+        dY16 = bf16_round(np.array([[float(v) for v in row] for row in dyf]))
+        d16 = _frac_matrix(dY16)
+        for kind in (0, 1):
+            for use_g in (False, True):
+                m = mean if kind == 0 else None
+                g = gamma if use_g else None
+                fused = o.gemm_postnorm_bwd(A, B, Z, kind, m, rstd, g)
+                unfused = o.norm_rows_bwd(dY16, Z, kind, m, rstd, g)
+                for i in range(M):
+                    mu, r = Fraction(float(mean[i])), Fraction(float(rstd[i]))
+                    want_f = _bwd_exact(dyf[i], zf[i], gf if use_g else None, kind, mu, r)
+                    want_u = _bwd_exact(d16[i], zf[i], gf if use_g else None, kind, mu, r)
+                    scale = 1e-13 * (1 + max(float(abs(v)) for v in want_f + want_u))
+                    for j in range(N):
+                        _close(fused[i, j], _dec(want_f[j]), scale, f"bwd fused kind={kind}[{i},{j}]")
+                        _close(unfused[i, j], _dec(want_u[j]), scale, f"bwd rows kind={kind}[{i},{j}]")
+
+
+def pin_torch_autograd_bwd(o):
+    """torch float64 autograd through F.layer_norm / F.rms_norm, with the
+    statistics of Z itself."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(41)
+    M, K, N = 7, 33, 40
+    A = bf16_round(rng.normal(size=(M, K)))
+    B = bf16_round(rng.normal(0, 0.3, size=(K, N)))
+    Z = bf16_round(rng.normal(0.3, 2.0, size=(M, N)))
+    G = bf16_round(rng.normal(1.0, 0.3, size=N))
+    eps = 1e-3
+    dY = torch.from_numpy(bf16_to_f64(A)) @ torch.from_numpy(bf16_to_f64(B))
+    for kind in (0, 1):
+        for use_g in (False, True):
+            z = torch.from_numpy(bf16_to_f64(Z)).requires_grad_(True)
+            w = torch.from_numpy(bf16_to_f64(G)) if use_g else None
+            if kind == 0:
+                y = F.layer_norm(z, (N,), w, None, eps)
+                mu = z.detach().mean(-1)
+                rs = 1.0 / torch.sqrt(z.detach().var(-1, unbiased=False) + eps)
+            else:
+                y = F.rms_norm(z, (N,), w, eps)
+                mu = None
+                rs = 1.0 / torch.sqrt((z.detach() ** 2).mean(-1) + eps)
+            (y * dY).sum().backward()
+            want = z.grad.numpy()
+            got = o.gemm_postnorm_bwd(A, B, Z, kind, None if mu is None else mu.numpy(), rs.numpy(),
+                                      G if use_g else None)
+            assert np.allclose(got, want, rtol=1e-10, atol=1e-11 * np.abs(want).max()), \
+                f"autograd kind={kind} gamma={use_g}: max err {np.abs(got - want).max()}"
+
+
+def pin_norm_bwd_invariants(o):
+    """With Z's own statistics: LN gradient rows sum to 0; for both norms
+    sum_j dz_j * xhat_j = N * rstd^3 * eps * mean_j(g_j * xhat_j)."""
+    rng = np.random.default_rng(43)
+    R, C = 6, 48
+    Z = bf16_round(rng.normal(-0.7, 1.3, size=(R, C)))
+    dY = bf16_round(rng.normal(size=(R, C)))
+    G = bf16_round(rng.normal(1.0, 0.2, size=C))
+    z, dy, g = bf16_to_f64(Z), bf16_to_f64(dY), bf16_to_f64(G)
+    for eps in (1e-5, 0.25):
+        for kind in (0, 1):
+            _, mean, rstd = o.norm_rows(Z, kind, eps)
+            dz = o.norm_rows_bwd(dY, Z, kind, mean, rstd, G)
+            xh = ((z - mean[:, None]) if kind == 0 else z) * rstd[:, None]
+            gx = (dy * g * xh).mean(-1)
+            scale = np.abs(dz).max()
+            if kind == 0:
+                assert np.abs(dz.sum(-1)).max() <= 1e-12 * C * scale, f"LN bwd row sums eps={eps}"
+            want = C * rstd ** 3 * eps * gx
+            got = (dz * xh).sum(-1)
+            assert np.allclose(got, want, rtol=1e-9, atol=1e-12 * C * scale), \
+                f"bwd orthogonality kind={kind} eps={eps}: {got} vs {want}"
+
+
+def pin_norm_bwd_reductions(o):
+    """B = I and B = a column permutation reduce the fused backward to the row
+    kernel on A; gamma = 1 equals no gamma; a row list gives the same rows."""
+    rng = np.random.default_rng(47)
+    M, N = 5, 12
+    A = bf16_round(rng.normal(size=(M, N)))
+    Z = bf16_round(rng.normal(0.2, 1.0, size=(M, N)))
+    mean = rng.normal(size=M)
+    rstd = rng.uniform(0.5, 2.0, size=M)
+    I = bf16_round(np.eye(N))
+    perm = np.roll(np.arange(N), 5)
+    P = np.ascontiguousarray(bf16_round(np.eye(N)[:, perm]))  # (A @ P)[:, j] = A[:, perm[j]]
+    ones = bf16_round(np.ones(N))
+    G = bf16_round(rng.normal(1.0, 0.5, size=N))
+    for kind in (0, 1):
+        m = mean if kind == 0 else None
+        rows = o.norm_rows_bwd(A, Z, kind, m, rstd, G)
+        assert np.array_equal(o.gemm_postnorm_bwd(A, I, Z, kind, m, rstd, G), rows), f"B=I kind={kind}"
+        Ap = np.ascontiguousarray(A[:, perm])
+        assert np.array_equal(o.gemm_postnorm_bwd(A, P, Z, kind, m, rstd, G),
+                              o.norm_rows_bwd(Ap, Z, kind, m, rstd, G)), f"B=P kind={kind}"
+        assert np.array_equal(o.gemm_postnorm_bwd(A, I, Z, kind, m, rstd, ones),
+                              o.gemm_postnorm_bwd(A, I, Z, kind, m, rstd, None)), f"gamma=1 kind={kind}"
+        sub = np.array([4, 0, 2])
+        full = o.gemm_postnorm_bwd(A, P, Z, kind, m, rstd, G)
+        assert np.array_equal(o.gemm_postnorm_bwd(A, P, Z, kind, m, rstd, G, rows=sub), full[sub]), \
+            f"row list kind={kind}"
+        assert np.array_equal(o.norm_rows_bwd(A, Z, kind, m, rstd, G, rows=sub), rows[sub]), \
+            f"row list (rows kernel) kind={kind}"
+
+
 PINS = [pin_bruteforce_plain, pin_bruteforce_prenorm, pin_bruteforce_postnorm,
         pin_bruteforce_norm_rows, pin_torch_f64, pin_lazy_identity, pin_invariants,
-        pin_reductions, pin_power_of_two_scale, pin_row_subset, pin_closed_forms]
+        pin_reductions, pin_power_of_two_scale, pin_row_subset, pin_closed_forms,
+        pin_bruteforce_norm_bwd, pin_torch_autograd_bwd, pin_norm_bwd_invariants,
+        pin_norm_bwd_reductions]
 
 
 def run_all(o):

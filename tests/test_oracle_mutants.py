@@ -46,6 +46,17 @@ MUTANTS = [
      "load_row(X, r, K, x);\n            row_times_w(x, W, N, K, Y + r * N);"),
     ("postln_wrong_rstd_slot", "rstd_out ? rstd_out + r : NULL);\n        }\n        free(x);\n        free(z);\n    }\n    return bad ? -1 : 0;\n}\n\nint nfo_gemm_postnorm_rms",
      "rstd_out ? rstd_out : NULL);\n        }\n        free(x);\n        free(z);\n    }\n    return bad ? -1 : 0;\n}\n\nint nfo_gemm_postnorm_rms"),
+    ("bwd_drops_mean_g", "const double mg = kind == NFO_NORM_LN ? sg / (double)n : 0.0;", "const double mg = 0.0;"),
+    ("bwd_mean_g_for_rms", "const double mg = kind == NFO_NORM_LN ? sg / (double)n : 0.0;",
+     "const double mg = sg / (double)n;"),
+    ("bwd_drops_xhat_term", "dz[j] = rstd * (g[j] - mg - xh[j] * mgx);", "dz[j] = rstd * (g[j] - mg);"),
+    ("bwd_xhat_term_sign", "dz[j] = rstd * (g[j] - mg - xh[j] * mgx);", "dz[j] = rstd * (g[j] - mg + xh[j] * mgx);"),
+    ("bwd_no_rstd", "dz[j] = rstd * (g[j] - mg - xh[j] * mgx);", "dz[j] = (g[j] - mg - xh[j] * mgx);"),
+    ("bwd_ignores_gamma", "g[j] = gamma ? dy[j] * bf16_to_double(gamma[j]) : dy[j];", "g[j] = dy[j];"),
+    ("bwd_xhat_not_centred", "xh[j] = (kind == NFO_NORM_LN ? z[j] - mean : z[j]) * rstd;", "xh[j] = z[j] * rstd;"),
+    ("bwd_divisor", "const double mgx = sgx / (double)n;", "const double mgx = sgx / (double)(n - 1);"),
+    ("bwd_z_ignores_row_list", "load_row(Z, i, N, z);", "load_row(Z, r, N, z);"),
+    ("bwd_stats_dense_index", "mean[i] : 0.0, rstd[i],\n                         buf + 2 * N", "mean[r] : 0.0, rstd[r],\n                         buf + 2 * N"),
 ]
 
 
