@@ -168,6 +168,57 @@ nf_status nf_norm_rows(const void* in, void* out, const void* gamma,
                        float eps, float* mean_out, float* rstd_out,
                        nf_stream stream);
 
+/*
+ * nf_gemm_postnorm_ln_bwd -- dZ = LayerNorm backward of dY = A * B, the
+ * norm's backward fused into the epilogue of the GEMM that produces its
+ * incoming gradient (blog §3 "What about backward? Fusion regrouping": the
+ * norm sits between two linears; the forward fuses it into the first one's
+ * epilogue, the backward into the epilogue of the second one's input-gradient
+ * GEMM dY = dOut * W2^T, so both directions are epilogue fusions with the
+ * same multi-CTA structure).  With g = dY * gamma and xhat = (Z - mean_i) *
+ * rstd_i:  dZ = rstd_i * (g - mean_j g - xhat * mean_j(g * xhat)); dY is
+ * never rounded or stored.
+ * A: M x K, B: K x N (row-major, e.g. W2^T), Z: M x N bf16 (the forward's
+ * norm input, 16-byte aligned), gamma: optional N bf16, mean / rstd: the
+ * forward's saved row statistics (M fp32 each, required), dZ: M x N bf16.
+ * Same shape, alignment and N <= NF_POSTNORM_MAX_N rules as the forward;
+ * rows wider than 256 columns exchange their two partial sums like the
+ * forward (L2 for K >= 512, else a cluster).  dgamma / dbeta (column sums
+ * over M) are not computed.
+ */
+nf_status nf_gemm_postnorm_ln_bwd(const void* A, const void* B, const void* Z,
+                                  const void* gamma, const float* mean,
+                                  const float* rstd, void* dZ, int64_t M,
+                                  int64_t N, int64_t K, nf_stream stream);
+
+/*
+ * nf_gemm_postnorm_rms_bwd -- the same for RMSNorm: xhat = Z * rstd_i,
+ * dZ = rstd_i * (g - xhat * mean_j(g * xhat)).
+ */
+nf_status nf_gemm_postnorm_rms_bwd(const void* A, const void* B, const void* Z,
+                                   const void* gamma, const float* rstd,
+                                   void* dZ, int64_t M, int64_t N, int64_t K,
+                                   nf_stream stream);
+
+/*
+ * nf_norm_rows_bwd -- backward of LayerNorm / RMSNorm over each row, from
+ * the statistics the forward pass saved (blog §3 "What about backward?"):
+ *   g = dY * gamma;  xhat = (Z - mean_i) * rstd_i (LN) or Z * rstd_i (RMS);
+ *   LN:  dZ = rstd_i * (g - mean_j g - xhat * mean_j(g * xhat))
+ *   RMS: dZ = rstd_i * (g - xhat * mean_j(g * xhat)).
+ * With Z's own statistics this is the gradient of sum(dY * norm(Z)) with
+ * respect to Z (dgamma / dbeta are not computed).  The unfused kernel the
+ * fused backward (nf_gemm_postnorm_ln_bwd / _rms_bwd) is compared with.
+ * dY, Z, dZ: rows x cols bf16, 16-byte aligned, cols a multiple of 8 and
+ * <= 16384; gamma: optional, cols bf16, 16-byte aligned; mean (LN only,
+ * required) and rstd (required): rows fp32, device memory.  dZ must not
+ * overlap dY or Z.  rows == 0 is a no-op.
+ */
+nf_status nf_norm_rows_bwd(const void* dY, const void* Z, const void* gamma,
+                           const float* mean, const float* rstd, void* dZ,
+                           int64_t rows, int64_t cols, int kind,
+                           nf_stream stream);
+
 /* ---------------------------------------------------------------------
  * Diagnostics and configuration (no counterpart in the blog).
  * ------------------------------------------------------------------- */
@@ -222,7 +273,8 @@ const char* nf_status_string(nf_status status);
 const char* nf_last_error(void);
 
 /* Launch plan the library would use; pure host function, no GPU needed.
- * op: 0 plain, 1 pre-norm RMS, 2 post-norm LN, 3 post-norm RMS.
+ * op: 0 plain, 1 pre-norm RMS, 2 post-norm LN, 3 post-norm RMS,
+ * 4 LN backward, 5 RMS backward.
  * sm_count: SMs of the device; the grid assumes every SM can hold one CTA
  * (for clusters, the library asks the driver for the real co-residency). */
 typedef struct nf_plan {

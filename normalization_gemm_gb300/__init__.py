@@ -13,6 +13,10 @@ and Attention Kernels"):
   gemm_postnorm_ln    Y = LayerNorm(X @ W) * gamma + beta        (§3)
   gemm_postnorm_rms   Y = RMSNorm(X @ W) * gamma                 (§3)
   norm_rows           standalone LayerNorm / RMSNorm of rows     (§1 baseline)
+  gemm_postnorm_ln_bwd / gemm_postnorm_rms_bwd
+                      dZ = norm backward of (A @ B) from saved   (§3 backward,
+                      row statistics, fused in the GEMM epilogue   fusion regrouping)
+  norm_rows_bwd       their backward from saved row statistics   (§3 backward baseline)
 """
 from __future__ import annotations
 
@@ -65,6 +69,9 @@ _SIGS = {
     "nf_gemm_postnorm_ln_noalloc": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
     "nf_gemm_postnorm_rms": [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
     "nf_norm_rows": [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
+    "nf_norm_rows_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP],
+    "nf_gemm_postnorm_ln_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
+    "nf_gemm_postnorm_rms_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_get_device_status": [_VP],
     "nf_clear_device_status": [],
     "nf_set_wait_timeout_ns": [ctypes.c_uint64],
@@ -246,6 +253,49 @@ def norm_rows(x, kind, eps, gamma=None, beta=None, out=None, mean_out=None, rstd
     return y
 
 
+def gemm_postnorm_ln_bwd(a, b, z, mean, rstd, gamma=None, out=None, stream=None):
+    """dZ = LayerNorm backward of dY = a @ b (fused), from the saved row mean / rstd (fp32 [M])."""
+    torch = _torch()
+    M, N, K = _shapes(a, b)
+    if tuple(z.shape) != (M, N):
+        raise ValueError(f"z must have shape {(M, N)}")
+    y = _out(out, M, N, a)
+    _check(lib().nf_gemm_postnorm_ln_bwd(_mat(a, "a"), _mat(b, "b"), _mat(z, "z"),
+                                         _vec(gamma, "gamma", N, torch.bfloat16),
+                                         _vec(mean, "mean", M, torch.float32), _vec(rstd, "rstd", M, torch.float32),
+                                         _mat(y, "out"), M, N, K, _stream(stream)), "nf_gemm_postnorm_ln_bwd")
+    return y
+
+
+def gemm_postnorm_rms_bwd(a, b, z, rstd, gamma=None, out=None, stream=None):
+    """dZ = RMSNorm backward of dY = a @ b (fused), from the saved row rstd (fp32 [M])."""
+    torch = _torch()
+    M, N, K = _shapes(a, b)
+    if tuple(z.shape) != (M, N):
+        raise ValueError(f"z must have shape {(M, N)}")
+    y = _out(out, M, N, a)
+    _check(lib().nf_gemm_postnorm_rms_bwd(_mat(a, "a"), _mat(b, "b"), _mat(z, "z"),
+                                          _vec(gamma, "gamma", N, torch.bfloat16),
+                                          _vec(rstd, "rstd", M, torch.float32), _mat(y, "out"), M, N, K,
+                                          _stream(stream)), "nf_gemm_postnorm_rms_bwd")
+    return y
+
+
+def norm_rows_bwd(dy, z, kind, mean, rstd, gamma=None, out=None, stream=None):
+    """Backward of LayerNorm (kind 0) / RMSNorm (kind 1) of each row from the saved
+    statistics (mean: fp32 [rows], None for RMS; rstd: fp32 [rows]); returns dZ."""
+    torch = _torch()
+    R = dy.shape[0] if dy.dim() == 2 else -1
+    C = dy.shape[1] if dy.dim() == 2 else -1
+    if tuple(z.shape) != (R, C):
+        raise ValueError(f"z must have shape {(R, C)}")
+    y = _out(out, R, C, dy)
+    _check(lib().nf_norm_rows_bwd(_mat(dy, "dy"), _mat(z, "z"), _vec(gamma, "gamma", C, torch.bfloat16),
+                                  _vec(mean, "mean", R, torch.float32), _vec(rstd, "rstd", R, torch.float32),
+                                  _mat(y, "out"), R, C, int(kind), _stream(stream)), "nf_norm_rows_bwd")
+    return y
+
+
 # ------------------------------------------------------------- diagnostics
 def device_status():
     """(status, [code, site, block, tile]) after synchronizing the device."""
@@ -283,7 +333,7 @@ def selftest_wait_timeout(ns: int, stream=None) -> None:
 
 
 def plan_gemm(op: int, M: int, N: int, K: int, sm_count: int) -> dict:
-    """Launch plan for op 0 plain / 1 pre-RMS / 2 post-LN / 3 post-RMS (host only)."""
+    """Launch plan for op 0 plain / 1 pre-RMS / 2 post-LN / 3 post-RMS / 4 LN bwd / 5 RMS bwd (host only)."""
     p = NFPlan()
     _check(lib().nf_plan_gemm(op, M, N, K, sm_count, ctypes.byref(p)), "nf_plan_gemm")
     return {f: getattr(p, f) for f, _ in NFPlan._fields_}

@@ -190,7 +190,7 @@ nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 }
 
 // ---------------------------------------------------------------- plans
-enum Op { OP_PLAIN = 0, OP_PRE = 1, OP_POST_LN = 2, OP_POST_RMS = 3 };
+enum Op { OP_PLAIN = 0, OP_PRE = 1, OP_POST_LN = 2, OP_POST_RMS = 3, OP_BWD_LN = 4, OP_BWD_RMS = 5 };
 
 struct Plan {
     int tile_n = 0;
@@ -209,6 +209,8 @@ const GemmVariant* find_variant(int op, int tile_n, int xch) {
         case OP_PRE: t = gemm_variants_pre(&n); break;
         case OP_POST_LN: t = gemm_variants_post_ln(&n); break;
         case OP_POST_RMS: t = gemm_variants_post_rms(&n); break;
+        case OP_BWD_LN: t = gemm_variants_bwd_ln(&n); break;
+        case OP_BWD_RMS: t = gemm_variants_bwd_rms(&n); break;
         default: return nullptr;
     }
     for (int i = 0; i < n; ++i)
@@ -231,10 +233,23 @@ const GemmVariant* find_variant(int op, int tile_n, int xch) {
 // `sms`: SMs of the device.  The global exchange runs one CTA per SM and
 // needs at least half as many CTAs as a row has tiles; with fewer the row
 // goes to a cluster instead.
+// The normalization backward (ops 4, 5) follows the same choice with
+// 256-column CTAs only (no 512-column variant): L2 exchange for K >= 512,
+// else a cluster of <= 16.
 nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p) {
     const bool post = op == OP_POST_LN || op == OP_POST_RMS;
+    const bool bwd = op == OP_BWD_LN || op == OP_BWD_RMS;
     p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
     p->xch = XCH_NONE;
+    if (bwd && N > 256) {
+        int mode = g_post_xch ? g_post_xch : (K >= 512 ? XCH_GLOBAL : XCH_CLUSTER);
+        if (mode == XCH_GLOBAL) {
+            const int64_t nt = (N + 255) / 256, tiles = ((M + TILE_M - 1) / TILE_M) * nt;
+            if (2 * (tiles < sms ? tiles : sms) < nt) mode = XCH_CLUSTER;
+        }
+        p->xch = mode;
+        if (N > 16 * 256) return fail(NF_ERR_UNSUPPORTED_SHAPE, "N too large for the cluster");
+    }
     if (post && N > 256) {
         int mode = g_post_xch, tile = g_post_tile;
         if (mode == 0) {
@@ -260,7 +275,7 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p) 
     p->clustered = p->xch == XCH_CLUSTER;
     p->cluster = p->clustered ? static_cast<int>((N + p->tile_n - 1) / p->tile_n) : 1;
     p->m_tiles = static_cast<int>((M + TILE_M - 1) / TILE_M);
-    p->n_tiles = (post && p->xch != XCH_GLOBAL) ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
+    p->n_tiles = ((post || bwd) && p->xch != XCH_GLOBAL) ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
     p->v = find_variant(op, p->tile_n, p->xch);
     if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
     p->k_tiles = static_cast<int>((K + p->v->tile_k - 1) / p->v->tile_k);
@@ -306,7 +321,7 @@ nf_status check_gemm_args(int op, const void* X, const void* W, const void* Y, c
         return fail(NF_ERR_ALIGNMENT, "gamma and beta must be 2-byte aligned");
     if ((mean_out && !aligned(mean_out, 4)) || (rstd_out && !aligned(rstd_out, 4)))
         return fail(NF_ERR_ALIGNMENT, "mean_out and rstd_out must be 4-byte aligned");
-    if ((op == OP_POST_LN || op == OP_POST_RMS) && N > NF_POSTNORM_MAX_N)
+    if (op >= OP_POST_LN && N > NF_POSTNORM_MAX_N)
         return fail(NF_ERR_UNSUPPORTED_SHAPE, "post-norm needs N <= 4096 (256 columns x 16-CTA cluster)");
     // Tile coordinates are int32: M rows plus one tile of slack.
     if (M > static_cast<int64_t>(INT32_MAX) - TILE_M) return fail(NF_ERR_UNSUPPORTED_SHAPE, "M too large");
@@ -474,10 +489,18 @@ nf_status noalloc_scratch(uint8_t** out) {
 // stream's scratch buffer.
 nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
                    int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream,
-                   bool fixed_scratch = false) {
+                   bool fixed_scratch = false, const void* zin = nullptr, const float* mean_in = nullptr,
+                   const float* rstd_in = nullptr) {
     nf_status st = check_gemm_args(op, X, W, Y, gamma, beta, mean_out, rstd_out, M, N, K, eps);
     if (st != NF_OK) return st;
     if (M == 0) return NF_OK;
+    if (op == OP_BWD_LN || op == OP_BWD_RMS) {
+        if (!zin || !rstd_in || (op == OP_BWD_LN && !mean_in))
+            return fail(NF_ERR_INVALID_ARG, "Z, rstd (and mean for LN) must be non-null");
+        if (!aligned(zin, 16)) return fail(NF_ERR_ALIGNMENT, "Z must be 16-byte aligned");
+        if ((mean_in && !aligned(mean_in, 4)) || !aligned(rstd_in, 4))
+            return fail(NF_ERR_ALIGNMENT, "mean and rstd must be 4-byte aligned");
+    }
     DeviceState* d = nullptr;
     if ((st = device_state(&d)) != NF_OK) return st;
     Plan p;
@@ -508,6 +531,9 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.rstd_out = rstd_out;
     a.status = d->status;
     a.timeout_ns = g_timeout_ns;
+    a.zin = static_cast<const uint16_t*>(zin);
+    a.mean_in = mean_in;
+    a.rstd_in = rstd_in;
     a.xcnt = nullptr;
     a.xbank = 0;
     a.xstats = nullptr;
@@ -619,6 +645,18 @@ nf_status nf_gemm_postnorm_ln_noalloc(const void* X, const void* W, const void* 
                     reinterpret_cast<cudaStream_t>(stream), true);
 }
 
+nf_status nf_gemm_postnorm_ln_bwd(const void* A, const void* B, const void* Z, const void* gamma, const float* mean,
+                                  const float* rstd, void* dZ, int64_t M, int64_t N, int64_t K, nf_stream stream) {
+    return run_gemm(OP_BWD_LN, A, B, gamma, nullptr, dZ, M, N, K, 0.0f, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), false, Z, mean, rstd);
+}
+
+nf_status nf_gemm_postnorm_rms_bwd(const void* A, const void* B, const void* Z, const void* gamma, const float* rstd,
+                                   void* dZ, int64_t M, int64_t N, int64_t K, nf_stream stream) {
+    return run_gemm(OP_BWD_RMS, A, B, gamma, nullptr, dZ, M, N, K, 0.0f, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), false, Z, nullptr, rstd);
+}
+
 nf_status nf_gemm_postnorm_rms(const void* X, const void* W, const void* gamma, void* Y, int64_t M, int64_t N,
                                int64_t K, float eps, float* rstd_out, nf_stream stream) {
     return run_gemm(OP_POST_RMS, X, W, gamma, nullptr, Y, M, N, K, eps, nullptr, rstd_out,
@@ -660,6 +698,38 @@ nf_status nf_norm_rows(const void* in, void* out, const void* gamma, const void*
     a.rstd_out = rstd_out;
     cudaError_t e = launch_norm_rows(a, kind, d->sm_count, g_overlap, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "norm_rows launch");
+    return NF_OK;
+}
+
+nf_status nf_norm_rows_bwd(const void* dY, const void* Z, const void* gamma, const float* mean, const float* rstd,
+                           void* dZ, int64_t rows, int64_t cols, int kind, nf_stream stream) {
+    if (kind != NF_NORM_LN && kind != NF_NORM_RMS) return fail(NF_ERR_INVALID_ARG, "kind must be LN or RMS");
+    if (rows < 0 || cols < 1) return fail(NF_ERR_INVALID_ARG, "need rows >= 0 and cols >= 1");
+    if (rows == 0) return NF_OK;  // nothing is accessed
+    if (!dY || !Z || !dZ || !rstd || (kind == NF_NORM_LN && !mean))
+        return fail(NF_ERR_INVALID_ARG, "dY, Z, dZ, rstd (and mean for LN) must be non-null");
+    if (cols > NORM_MAX_COLS) return fail(NF_ERR_UNSUPPORTED_SHAPE, "cols must be <= 16384");
+    if (cols % 8 != 0) return fail(NF_ERR_ALIGNMENT, "cols must be a multiple of 8 (16-byte rows)");
+    if (!aligned(dY, 16) || !aligned(Z, 16) || !aligned(dZ, 16))
+        return fail(NF_ERR_ALIGNMENT, "dY, Z and dZ must be 16-byte aligned");
+    if (gamma && !aligned(gamma, 16)) return fail(NF_ERR_ALIGNMENT, "gamma must be 16-byte aligned for nf_norm_rows_bwd");
+    if ((mean && !aligned(mean, 4)) || !aligned(rstd, 4))
+        return fail(NF_ERR_ALIGNMENT, "mean and rstd must be 4-byte aligned");
+    DeviceState* d = nullptr;
+    nf_status st = device_state(&d);
+    if (st != NF_OK) return st;
+    NormBwdArgs a;
+    a.dy = dY;
+    a.z = Z;
+    a.gamma = static_cast<const uint16_t*>(gamma);
+    a.mean = mean;
+    a.rstd = rstd;
+    a.dz = dZ;
+    a.rows = rows;
+    a.cols = static_cast<int32_t>(cols);
+    a.inv_cols = 1.0f / static_cast<float>(cols);
+    cudaError_t e = launch_norm_rows_bwd(a, kind, d->sm_count, g_overlap, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "norm_rows_bwd launch");
     return NF_OK;
 }
 
@@ -751,7 +821,7 @@ const char* nf_status_string(nf_status s) {
 const char* nf_last_error(void) { return g_last_error.c_str(); }
 
 nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf_plan* out) {
-    if (!out || op < 0 || op > 3 || sm_count < 1) return fail(NF_ERR_INVALID_ARG, "bad plan query");
+    if (!out || op < 0 || op > 5 || sm_count < 1) return fail(NF_ERR_INVALID_ARG, "bad plan query");
     nf_status st = check_gemm_args(op, reinterpret_cast<const void*>(256), reinterpret_cast<const void*>(256),
                                    reinterpret_cast<const void*>(256), nullptr, nullptr, nullptr, nullptr, M, N, K,
                                    1e-5f);

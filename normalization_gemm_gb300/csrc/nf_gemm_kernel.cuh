@@ -5,6 +5,10 @@
 //   EPI_PRE_RMS   Y = rstd(X) * (X W)              (blog §2 Lazy Pre-Norm)
 //   EPI_POST_LN   Y = LayerNorm(X W) * g + b       (blog §3 Multi-CTA Norm)
 //   EPI_POST_RMS  Y = RMSNorm(X W) * g             (blog §3 with RMSNorm)
+//   EPI_BWD_LN    dZ = LayerNorm backward of dY = X W, from saved row
+//   EPI_BWD_RMS   statistics (blog §3 "What about backward? Fusion
+//                 regrouping": the norm's backward in the epilogue of the
+//                 GEMM that produces its incoming gradient)
 //
 // Blog: "Towards Free Normalization: Fusing Normalization into GEMM and
 // Attention Kernels".
@@ -134,6 +138,43 @@ __device__ __forceinline__ void convert64(const uint32_t (&va)[32], const uint32
             pk[4 * q + e] = pack_bf16x2(lo, hi);
         }
     }
+}
+
+// Backward of 64 columns (two 32-column chunks of dY = X W) -> 32 packed
+// bf16 pairs: dz = g * rstd + z * c1 + c0 with g = dY * gamma (AFF; gamma as
+// bf16 in shared memory at saff_g) and z the saved forward input (zq, 64 bf16).
+template <bool AFF>
+__device__ __forceinline__ void convert64_bwd(const uint32_t (&va)[32], const uint32_t (&vb)[32],
+                                              const uint4 (&zq)[8], uint32_t saff_g, uint64_t rs2, uint64_t c12,
+                                              uint64_t c02, uint32_t (&pk)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t* src = q < 4 ? va : vb;
+        const int o = (q & 3) * 8;
+        const uint32_t zw[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+        uint32_t gw[4] = {0u, 0u, 0u, 0u};
+        if (AFF) {
+            const uint4 g = ld_shared_v4(saff_g + static_cast<uint32_t>(q * 16));
+            gw[0] = g.x, gw[1] = g.y, gw[2] = g.z, gw[3] = g.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            uint64_t x2 = f2_pack(src[o + 2 * e], src[o + 2 * e + 1]);
+            if (AFF) x2 = f2_fma(x2, bf16x2_to_f2(gw[e]), 0ull);
+            const uint64_t y = f2_fma(x2, rs2, f2_fma(bf16x2_to_f2(zw[e]), c12, c02));
+            float lo, hi;
+            f2_unpack(y, lo, hi);
+            pk[4 * q + e] = pack_bf16x2(lo, hi);
+        }
+    }
+}
+
+// 64 bf16 of a row of Z starting at p (16-byte aligned); 8-column groups at or
+// past `valid` read as zero (N is a multiple of 8).
+__device__ __forceinline__ void load_z64(const uint16_t* p, bool own, int valid, uint4 (&zq)[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        zq[q] = (own && q * 8 < valid) ? __ldg(reinterpret_cast<const uint4*>(p + q * 8)) : make_uint4(0, 0, 0, 0);
 }
 
 // Tile schedule: CTA-local work unit lt -> (m_tile, n_tile, first row, rows).
@@ -308,7 +349,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         const int stride = static_cast<int>(gridDim.x * blockDim.x);
         for (int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i < prev_ints; i += stride) other[i] = 0;
     }
-    if (Cfg::kPost && !GLOBALX && threadIdx.x < 128) {
+    if (Cfg::kRow && !GLOBALX && threadIdx.x < 128) {
         // This CTA's columns never change: clustered CTAs keep their rank's
         // tile, unclustered post-norm has a single column tile.
         const int n0 = sched.n_fixed * TILE_N;
@@ -424,7 +465,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         // Post-norm keeps the row's last segment in registers across the
         // statistics exchange, except the global exchange, whose partials of up
         // to 16 column tiles need those registers: it reads the segment again.
-        constexpr bool KEEP_SEG = Cfg::kPost && !GLOBALX;
+        constexpr bool KEEP_SEG = Cfg::kPost && !GLOBALX;  // (the backward needs them for Z)
         // The global exchange's release fence (lane 0) should not wait for
         // this warp's bulk stores: another lane issues them.
         constexpr int STORE_LANE = GLOBALX ? 31 : 0;
@@ -433,7 +474,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         const int qtr = warp & 3;
         const int row = qtr * 32 + lane;  // tile row == TMEM lane
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qtr * 32) << 16);
-        const bool affine = Cfg::kPost && (args.gamma != nullptr || args.beta != nullptr);
+        const bool affine = Cfg::kRow && (args.gamma != nullptr || args.beta != nullptr);
         // gamma at saff, beta at saff + 2 TILE_N; the global exchange keeps one
         // such slot per group, refilled for each tile's columns.
         const uint32_t saff = smem_u32(aff) + (GLOBALX ? static_cast<uint32_t>(grp * 4 * TILE_N) : 0u);
@@ -480,6 +521,92 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                 const float ss = ss_buf[b * TILE_M + row];
                 scale = rsqrtf(fmaf(ss, args.inv_len, args.eps));
                 if (n == 0 && args.rstd_out && own_row) args.rstd_out[grow] = scale;
+            }
+
+            // Backward: the row's saved statistics and its Z values.
+            const float bmu = (Cfg::kBwdLN && own_row) ? args.mean_in[grow] : 0.0f;
+            const float brs = (Cfg::kBwd && own_row) ? args.rstd_in[grow] : 0.0f;
+            const uint16_t* const zrow =
+                Cfg::kBwd ? args.zin + static_cast<size_t>(own_row ? grow : 0) * args.N + n * TILE_N : nullptr;
+            float bc1 = 0.0f, bc0 = 0.0f;  // backward: dz = g * brs + z * bc1 + bc0
+
+            if (Cfg::kBwd) {
+                // -- backward partials of this CTA's nv columns: sum of g and of
+                //    g * (z - mean), g = dY * gamma (xhat = (z - mean) * rstd).
+                if (GLOBALX && affine) {  // gamma of this tile is in the group's slot
+                    ok = mbar_wait(guard, bar_afff0 + 8u * grp, jph, SITE_EPI_AFF, lt);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                }
+                const uint64_t mu2 = f2_splat(bmu);
+                uint64_t a1[4] = {0, 0, 0, 0}, a2[4] = {0, 0, 0, 0};
+                for (int sg = 0; sg < nseg; ++sg) {
+                    uint4 zq[8];
+                    load_z64(zrow + sg * SEG, own_row, nv - sg * SEG, zq);
+                    tmem_load_seg<NC>(tacc + sg * SEG, v);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t* src = v[q >> 2];
+                        const int o = (q & 3) * 8;
+                        const uint32_t zw[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+                        uint32_t gw[4] = {0u, 0u, 0u, 0u};
+                        if (affine && args.gamma) {
+                            const uint4 gq = ld_shared_v4(saff + static_cast<uint32_t>((sg * SEG + q * 8) * 2));
+                            gw[0] = gq.x, gw[1] = gq.y, gw[2] = gq.z, gw[3] = gq.w;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint64_t g2 = f2_pack(src[o + 2 * e], src[o + 2 * e + 1]);
+                            if (affine && args.gamma) g2 = f2_fma(g2, bf16x2_to_f2(gw[e]), 0ull);
+                            const uint64_t d2 = f2_sub(bf16x2_to_f2(zw[e]), mu2);
+                            a1[e] = f2_add(a1[e], g2);
+                            a2[e] = f2_fma(g2, d2, a2[e]);
+                        }
+                    }
+                }
+                const float pa = f2_hsum(f2_add(f2_add(a1[0], a1[1]), f2_add(a1[2], a1[3])));
+                const float pb = f2_hsum(f2_add(f2_add(a2[0], a2[1]), f2_add(a2[2], a2[3])));
+                float s1 = pa, s2 = pb;  // sums over the whole row
+                if (CLUSTERED) {
+                    const uint32_t slot =
+                        sRecv + static_cast<uint32_t>(((b * MAX_CLUSTER + my_rank) * TILE_M + row) * 8);
+                    const uint32_t xbar = bar_xch0 + 8u * b;
+                    for (int p = 0; p < args.cluster; ++p)
+                        st_async_f32x2(mapa_shared(slot, p), pa, pb, mapa_shared(xbar, p));
+                    ok = mbar_wait<true>(guard, xbar, aph, SITE_EPI_XCH, lt);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    if (qtr == 0 && lane == 0 && lt + 2 < count) mbar_arrive_expect_tx(xbar, xch_bytes);
+                    const float* recv = reinterpret_cast<const float*>(
+                        base_ptr + Cfg::OFF_RECV + (b * MAX_CLUSTER * TILE_M + row) * 8);
+                    s1 = s2 = 0.0f;
+                    for (int p = 0; p < args.cluster; ++p) {
+                        s1 += recv[p * TILE_M * 2];
+                        s2 += recv[p * TILE_M * 2 + 1];
+                    }
+                } else if (GLOBALX) {
+                    const int nt = args.n_tiles;
+                    float2* const xst = args.xstats + static_cast<size_t>(m) * nt * TILE_M + row;
+                    int* const cnt = xbank + m * 4 + qtr;
+                    __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
+                    __syncwarp();  // the warp's stores precede lane 0's release
+                    if (lane == 0) red_release_gpu_add(cnt, 1);
+                    if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
+                    float2 pp[MAX_CLUSTER];
+#pragma unroll
+                    for (int p = 0; p < MAX_CLUSTER; ++p)
+                        pp[p] = p < nt ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
+                    s1 = s2 = 0.0f;
+#pragma unroll
+                    for (int p = 0; p < MAX_CLUSTER; ++p) {
+                        s1 += pp[p].x;
+                        s2 += pp[p].y;
+                    }
+                }
+                // dz = rstd (g - mean(g) - xhat mean(g xhat)), mean(g) for LN only:
+                //    = g * rstd + z * bc1 + bc0.
+                const float mg = Cfg::kBwdLN ? s1 * args.inv_len : 0.0f;
+                const float mgx = brs * s2 * args.inv_len;
+                bc1 = -brs * brs * mgx;
+                bc0 = -brs * mg - bc1 * bmu;
             }
 
             if (Cfg::kPost) {
@@ -644,11 +771,21 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                         const int c0 = cs + q * STORE_COLS;
                         if (c0 < nstore) {
                             uint32_t pk[32];
-                            if (affine)
+                            if (Cfg::kBwd) {
+                                uint4 zq[8];
+                                load_z64(zrow + c0, own_row, nv - c0, zq);
+                                if (affine && args.gamma)
+                                    convert64_bwd<true>(v[2 * q], v[2 * q + 1], zq, saff + c0 * 2, f2_splat(brs),
+                                                        f2_splat(bc1), f2_splat(bc0), pk);
+                                else
+                                    convert64_bwd<false>(v[2 * q], v[2 * q + 1], zq, 0, f2_splat(brs),
+                                                         f2_splat(bc1), f2_splat(bc0), pk);
+                            } else if (affine) {
                                 convert64<AFF_SMEM>(v[2 * q], v[2 * q + 1], scale2, bias2, saff + c0 * 2,
                                                     saff + (TILE_N + c0) * 2, pk);
-                            else
+                            } else {
                                 convert64<AFF_NONE>(v[2 * q], v[2 * q + 1], scale2, bias2, 0, 0, pk);
+                            }
                             const uint32_t rowp = sStg + static_cast<uint32_t>((warp + q) * STORE_BUF_BYTES) +
                                                   static_cast<uint32_t>(lane * 128);
 #pragma unroll

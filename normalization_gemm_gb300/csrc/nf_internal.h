@@ -26,7 +26,14 @@ constexpr int MAX_STAGES = 8;
 constexpr int NUM_BARRIER_SLOTS = 29;     // full[8] empty[8] acc_full[2] acc_empty[2] ss_full[2] xch[2] mma_done
                                           // aff_full[2] aff_empty[2]
 
-enum Epilogue : int { EPI_PLAIN = 0, EPI_PRE_RMS = 1, EPI_POST_LN = 2, EPI_POST_RMS = 3 };
+enum Epilogue : int {
+    EPI_PLAIN = 0,
+    EPI_PRE_RMS = 1,
+    EPI_POST_LN = 2,
+    EPI_POST_RMS = 3,
+    EPI_BWD_LN = 4,   // dZ = LayerNorm backward of (X W) from saved statistics
+    EPI_BWD_RMS = 5,  // dZ = RMSNorm backward of (X W) from saved statistics
+};
 
 // How the CTAs that share an output row exchange partial row statistics
 // (post-norm with the row split over several CTAs).
@@ -58,9 +65,12 @@ struct GemmCfg {
     static constexpr bool kPre = EPI == EPI_PRE_RMS;
     static constexpr bool kPost = EPI == EPI_POST_LN || EPI == EPI_POST_RMS;
     static constexpr bool kLN = EPI == EPI_POST_LN;
+    static constexpr bool kBwd = EPI == EPI_BWD_LN || EPI == EPI_BWD_RMS;
+    static constexpr bool kBwdLN = EPI == EPI_BWD_LN;
+    static constexpr bool kRow = kPost || kBwd;  // reduces over the output row (N)
     static constexpr bool CLUSTERED = XCH == XCH_CLUSTER;
     static_assert(TILE_N == 64 || TILE_N == 128 || TILE_N == 256, "tile_n");
-    static_assert(XCH == XCH_NONE || (kPost && TILE_N == 256), "row exchange only for post-norm");
+    static_assert(XCH == XCH_NONE || (kRow && TILE_N == 256), "row exchange only for post-norm");
 
     static constexpr int B_STAGE_BYTES = TILE_K * TILE_N * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
@@ -70,7 +80,7 @@ struct GemmCfg {
     // gamma, beta (bf16) of the CTA's fixed column tile; the global exchange
     // moves across column tiles and keeps one slot per epilogue warpgroup,
     // refilled for each tile.
-    static constexpr int AFFINE_BYTES = !kPost ? 0 : (XCH == XCH_GLOBAL ? 2 * (2 * TILE_N * 2) : 2 * TILE_N * 2);
+    static constexpr int AFFINE_BYTES = !kRow ? 0 : (XCH == XCH_GLOBAL ? 2 * (2 * TILE_N * 2) : 2 * TILE_N * 2);
     static constexpr int SS_BYTES = kPre ? 2 * TILE_M * 4 : 0;        // sum of squares [2][128]
     static constexpr int BAR_BYTES = 256;                             // barriers + 2 words
     // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
@@ -117,6 +127,9 @@ struct GemmArgs {
     float* rstd_out;        // M entries or null
     uint32_t* status;       // device status word (4 x u32)
     uint64_t timeout_ns;
+    const uint16_t* zin;    // backward: Z, M x N bf16 (the forward's norm input)
+    const float* mean_in;   // backward LN: saved row means (M)
+    const float* rstd_in;   // backward: saved row rstd (M)
     int* xcnt;              // global exchange only: XCH_CNT0 + 2 * xbank ints
     int32_t xbank;          // ints per counter bank, >= xch_bank_ints(m_tiles)
     float2* xstats;         // global exchange only: >= xch_stats_bytes(m_tiles, n_tiles)
@@ -154,6 +167,8 @@ const GemmVariant* gemm_variants_plain(int* count);
 const GemmVariant* gemm_variants_pre(int* count);
 const GemmVariant* gemm_variants_post_ln(int* count);
 const GemmVariant* gemm_variants_post_rms(int* count);
+const GemmVariant* gemm_variants_bwd_ln(int* count);
+const GemmVariant* gemm_variants_bwd_rms(int* count);
 
 // ---------------------------------------------------------------- row norm
 struct NormArgs {
@@ -171,6 +186,20 @@ struct NormArgs {
 
 // Picks the variant for `cols` and launches it; returns the CUDA status.
 cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, bool overlap, cudaStream_t stream);
+
+// Backward of the row normalization from saved statistics.
+struct NormBwdArgs {
+    const void* dy;        // rows x cols bf16
+    const void* z;         // rows x cols bf16, the forward's norm input
+    const uint16_t* gamma;  // bf16, cols entries, or null
+    const float* mean;     // rows entries (LN), may be null for RMS
+    const float* rstd;     // rows entries
+    void* dz;              // rows x cols bf16
+    int64_t rows;
+    int32_t cols;
+    float inv_cols;
+};
+cudaError_t launch_norm_rows_bwd(const NormBwdArgs& a, int kind, int sm_count, bool overlap, cudaStream_t stream);
 // Largest supported cols.
 constexpr int NORM_MAX_COLS = 16384;
 

@@ -158,6 +158,93 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
     }
 }
 
+// Backward of the row normalization from the forward's saved statistics
+// (blog "Towards Free Normalization: ...", §3 "What about backward?"; the
+// unfused kernel the fused backward is compared with):
+//   g = dY * gamma; xhat = (Z - mean) * rstd (LN) or Z * rstd (RMS);
+//   dZ = rstd * (g - mean(g) - xhat * mean(g * xhat)), mean(g) for LN only.
+// Same layout as the forward kernel: TPR threads per row, CPT 16-byte chunks
+// of dY and of Z per thread in registers, each row read and written once.
+template <int TPR, int CPT, int KIND>
+__global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_bwd_kernel(const NormBwdArgs a) {
+    constexpr int RPB = NORM_THREADS / TPR;
+    __shared__ float red[NORM_THREADS / 32];
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int t = static_cast<int>(threadIdx.x) % TPR;
+    const int rg = static_cast<int>(threadIdx.x) / TPR;
+    const int chunks = a.cols >> 3;
+    const uint4* dyp = reinterpret_cast<const uint4*>(a.dy);
+    const uint4* zp = reinterpret_cast<const uint4*>(a.z);
+    uint4* out = reinterpret_cast<uint4*>(a.dz);
+    // Warm L2 with the first row block of dY and Z (see the forward kernel).
+    if (threadIdx.x == 0) {
+        const int64_t r = static_cast<int64_t>(blockIdx.x) * RPB;
+        if (r < a.rows) {
+            const int64_t nr = a.rows - r < RPB ? a.rows - r : RPB;
+            bulk_prefetch_l2(dyp + r * chunks, static_cast<uint32_t>(nr * chunks * 16));
+            bulk_prefetch_l2(zp + r * chunks, static_cast<uint32_t>(nr * chunks * 16));
+        }
+    }
+    griddep_wait();  // inputs may come from the kernel launched just before
+    griddep_launch_dependents();
+
+    float g[CPT][8];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int c = t + i * TPR;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) g[i][e] = 1.0f;
+        if (c < chunks && a.gamma) unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma) + c), g[i]);
+    }
+
+    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * RPB; r0 < a.rows;
+         r0 += static_cast<int64_t>(gridDim.x) * RPB) {
+        const int64_t row = r0 + rg;
+        const bool live = row < a.rows;
+        float gy[CPT][8], xh[CPT][8];
+        const float mu = (KIND == 0 && live) ? a.mean[row] : 0.0f;
+        const float rs = live ? a.rstd[row] : 0.0f;
+        float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = t + i * TPR;
+            if (live && c < chunks) {
+                unpack8(__ldcs(dyp + row * chunks + c), gy[i]);
+                unpack8(__ldcs(zp + row * chunks + c), xh[i]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gy[i][e] = xh[i][e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                gy[i][e] *= g[i][e];                                   // g = dY * gamma
+                xh[i][e] = (KIND == 0 ? xh[i][e] - mu : xh[i][e]) * rs;  // xhat
+                s1 += gy[i][e];
+                s2 = fmaf(gy[i][e], xh[i][e], s2);
+            }
+        }
+        const float mg = KIND == 0 ? group_sum<TPR>(s1, red, warp, lane) * a.inv_cols : 0.0f;
+        const float mgx = group_sum<TPR>(s2, red, warp, lane) * a.inv_cols;
+        if (!live) continue;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            const int c = t + i * TPR;
+            if (c < chunks) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = rs * (gy[i][e] - mg - xh[i][e] * mgx);
+                uint4 q;
+                q.x = pack_bf16x2(y[0], y[1]);
+                q.y = pack_bf16x2(y[2], y[3]);
+                q.z = pack_bf16x2(y[4], y[5]);
+                q.w = pack_bf16x2(y[6], y[7]);
+                __stcs(out + row * chunks + c, q);
+            }
+        }
+    }
+}
+
 template <int TPR, int CPT, int KIND>
 cudaError_t launch_one(const NormArgs& a, int sm_count, bool overlap, cudaStream_t stream) {
     auto kern = nf_norm_rows_kernel<TPR, CPT, KIND>;
@@ -202,10 +289,59 @@ cudaError_t dispatch(const NormArgs& a, int sm_count, bool overlap, cudaStream_t
     return launch_one<256, 8, KIND>(a, sm_count, overlap, stream);  // cols <= 16384
 }
 
+template <int TPR, int CPT, int KIND>
+cudaError_t launch_one_bwd(const NormBwdArgs& a, int sm_count, bool overlap, cudaStream_t stream) {
+    auto kern = nf_norm_rows_bwd_kernel<TPR, CPT, KIND>;
+    constexpr int RPB = NORM_THREADS / TPR;
+    static int per_sm = 0;  // occupancy of this variant, queried once
+    if (per_sm == 0) {
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NORM_THREADS, 0);
+        if (e != cudaSuccess) return e;
+        per_sm = n < 1 ? 1 : n;
+    }
+    const int64_t steps = (a.rows + RPB - 1) / RPB;
+    const int64_t cap = static_cast<int64_t>(sm_count) * per_sm;
+    const int grid = static_cast<int>(steps < cap ? steps : cap);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NORM_THREADS);
+    cfg.stream = stream;
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int KIND>
+cudaError_t dispatch_bwd(const NormBwdArgs& a, int sm_count, bool overlap, cudaStream_t stream) {
+    const int chunks = a.cols >> 3;
+    if (chunks <= 4) return launch_one_bwd<1, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 8) return launch_one_bwd<2, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 16) return launch_one_bwd<4, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 32) return launch_one_bwd<8, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 64) return launch_one_bwd<16, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 128) return launch_one_bwd<32, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 256) return launch_one_bwd<64, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 512) return launch_one_bwd<128, 4, KIND>(a, sm_count, overlap, stream);
+    if (chunks <= 1024) return launch_one_bwd<256, 4, KIND>(a, sm_count, overlap, stream);
+    return launch_one_bwd<256, 8, KIND>(a, sm_count, overlap, stream);  // cols <= 16384
+}
+
 }  // namespace
 
 cudaError_t launch_norm_rows(const NormArgs& a, int kind, int sm_count, bool overlap, cudaStream_t stream) {
     return kind == 0 ? dispatch<0>(a, sm_count, overlap, stream) : dispatch<1>(a, sm_count, overlap, stream);
+}
+
+cudaError_t launch_norm_rows_bwd(const NormBwdArgs& a, int kind, int sm_count, bool overlap,
+                                 cudaStream_t stream) {
+    return kind == 0 ? dispatch_bwd<0>(a, sm_count, overlap, stream)
+                     : dispatch_bwd<1>(a, sm_count, overlap, stream);
 }
 
 }  // namespace nf

@@ -178,3 +178,27 @@ def test_empty_m_accepts_null_bases(L):
     assert L.nf_gemm_prenorm_rms(None, P, None, 0, 64, 64, 1e-6, None, None) == OK
     assert L.nf_norm_rows(None, None, None, None, 0, 64, 0, 1e-5, None, None, None) == OK
     assert L.nf_gemm_plain(None, P, None, 1, 64, 64, None) == INVALID
+
+
+@pytest.mark.parametrize("op,M,N,K,tile_n,cluster,xch", [
+    (4, 16384, 2048, 1024, 256, 1, 2), (5, 8192, 4096, 4096, 256, 1, 2), (4, 130, 2048, 64, 256, 8, 1),
+    (5, 64, 4088, 64, 256, 16, 1), (4, 300, 200, 64, 256, 1, 0), (5, 300, 120, 512, 128, 1, 0),
+    (4, 65536, 128, 128, 128, 1, 0),
+])
+def test_backward_plans(L, op, M, N, K, tile_n, cluster, xch):
+    """The norm backward (ops 4, 5) takes 256-column CTAs past 256 columns: the
+    L2 exchange for K >= 512, else a cluster of ceil(N / 256) (<= 16)."""
+    p = nf.plan_gemm(op, M, N, K, 148)
+    assert (p["tile_n"], p["cluster"], p["exchange"], p["tile_k"]) == (tile_n, cluster, xch, 64)
+    assert p["threads"] == 320 and p["tmem_cols"] == 2 * tile_n
+
+
+def test_backward_argument_checks(L):
+    # null Z / stats, misaligned Z, N beyond the post-norm limit
+    assert L.nf_gemm_postnorm_ln_bwd(P, P, None, None, P, P, P, 128, 64, 64, None) == INVALID
+    assert L.nf_gemm_postnorm_ln_bwd(P, P, P, None, None, P, P, 128, 64, 64, None) == INVALID
+    assert L.nf_gemm_postnorm_rms_bwd(P, P, P, None, None, P, 128, 64, 64, None) == INVALID
+    assert L.nf_gemm_postnorm_rms_bwd(P, P, P + 8, None, P, P, 128, 64, 64, None) in (2, 6)
+    assert L.nf_gemm_postnorm_ln_bwd(P, P, P, None, P, P, P, 128, 4104, 64, None) == 3
+    assert L.nf_norm_rows_bwd(P, P, None, None, P, P, 4, 64, 0, None) == INVALID
+    assert L.nf_norm_rows_bwd(P, P, None, None, P, P, 0, 64, 0, None) == OK
