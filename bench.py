@@ -22,7 +22,9 @@ Prints ONE JSON line (rank 0):
                and reads Y back.
   cpu_baseline the fp64 oracle on the host cores (a bounded sample).
   configs      per-workload figures for the other four workloads (not the
-               headline).
+               headline), and for the normalization backward fused into the
+               epilogue of the GEMM producing its incoming gradient (post-norm
+               shapes; unfused pair: plain GEMM + row backward kernel).
 --impl reference times the fp64 oracle itself as the reference arm.
 Under torchrun (N > 1) every rank runs its own independent batch of the same
 size (rows shard across GPUs, no collective on the data path; weak scaling).
@@ -306,6 +308,62 @@ def measure_workload(nf, w, op, dev, stream, steps, warmup, seed=0, dist=None, s
     return out
 
 
+def backward_inputs(w, seed=0):
+    """Inputs of the normalization backward on workload w's shapes: A = X
+    (M x K, the incoming gradient dOut), B = W (K x N, standing in for the next
+    linear's transposed weight), Z (M x N, the forward's norm input: mean 0.3,
+    std 1.5) and Z's own row statistics (fp32), as the forward would save them."""
+    inp = nf_inputs.workload_inputs(w, seed=seed)
+    z = nf_inputs.make_inputs(w.M, w.N, 8, seed=seed + 7)["X"]
+    Z = nf_inputs.bf16_round(nf_inputs.bf16_to_f64(z) * 1.5 + 0.3)
+    zf = nf_inputs.bf16_to_f64(Z)
+    mean = zf.mean(-1)
+    var = ((zf - mean[:, None]) ** 2).mean(-1)
+    ms = (zf * zf).mean(-1)
+    return inp, Z, mean.astype(np.float32), var, ms
+
+
+def measure_backward(nf, w, kind, dev, stream, steps, warmup, seed=0):
+    """Fused GEMM + norm-backward epilogue, and the unfused pair (plain GEMM
+    writing dY, then the row backward kernel), time per launch."""
+    import torch
+    inp, Z, mean, var, ms = backward_inputs(w, seed)
+    rstd = (1.0 / np.sqrt((var if kind == 0 else ms) + w.eps)).astype(np.float32)
+    A0, B0, Z0 = _to_dev(inp["X"], dev), _to_dev(inp["W"], dev), _to_dev(Z, dev)
+    G = _to_dev(inp["gamma"], dev) if w.gamma else None
+    mean_d = torch.from_numpy(mean).to(dev) if kind == 0 else None
+    rstd_d = torch.from_numpy(rstd).to(dev)
+    D0 = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    set_bytes = A0.numel() * 2 + Z0.numel() * 2 + D0.numel() * 2
+    sets, nsets = make_sets([A0, Z0, D0], set_bytes, dev)
+
+    def fused(i):
+        a, z, d = sets[i % nsets]
+        if kind == 0:
+            nf.gemm_postnorm_ln_bwd(a, B0, z, mean_d, rstd_d, G, out=d, stream=stream)
+        else:
+            nf.gemm_postnorm_rms_bwd(a, B0, z, rstd_d, G, out=d, stream=stream)
+
+    out = {"t_fused": time_steps(fused, steps, warmup, stream) / steps}
+    dys = [torch.empty_like(D0) for _ in range(nsets)]
+    plain = lambda i: nf.gemm_plain(sets[i % nsets][0], B0, out=dys[i % nsets], stream=stream)  # noqa: E731
+    norm = lambda i: nf.norm_rows_bwd(dys[i % nsets], sets[i % nsets][1], kind, mean_d, rstd_d, G,  # noqa: E731
+                                      out=sets[i % nsets][2], stream=stream)
+    ksteps = max(1, min(steps, 2000))
+    out["t_plain"] = time_steps(plain, ksteps, min(warmup, 10), stream) / ksteps
+    out["t_norm"] = time_steps(norm, ksteps, min(warmup, 10), stream) / ksteps
+    del sets, dys
+    torch.cuda.empty_cache()
+    return out
+
+
+def backward_bytes(w, kind):
+    """Each tensor moved once: A, B and Z read, dZ written, the saved
+    statistics (and gamma) read."""
+    return (2 * w.M * w.K + 2 * w.K * w.N + 4 * w.M * w.N + 4 * w.M * (2 if kind == 0 else 1)
+            + (2 * w.N if w.gamma else 0))
+
+
 def roofline_time(w, op, hbm_gbs, tflops):
     nbytes = algorithmic_bytes(w.M, w.N, w.K, gamma=w.gamma and op != "pre_rms",
                                beta=w.beta and op == "post_ln")
@@ -535,6 +593,28 @@ def main(argv=None):
                         "hbm_gbs": nb / r["t_fused"] / 1e9,
                         "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
                         "norm_gbs": norm_bytes(r["norm_rows"], r["norm_cols"]) / r["t_norm"] / 1e9,
+                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
+                    })
+                    del r
+                    torch.cuda.empty_cache()
+                # the norm's backward fused into the epilogue of the GEMM that
+                # produces its incoming gradient (same shapes as the forward)
+                for cop in cw.ops:
+                    if cop not in ("post_ln", "post_rms"):
+                        continue
+                    kind = 0 if cop == "post_ln" else 1
+                    steps = 200 if cw.flops > 5e10 else 1000
+                    r = measure_backward(nf, cw, kind, dev, stream, steps, 10)
+                    nb = backward_bytes(cw, kind)
+                    tr = max(cw.flops / (bf16_tf * 1e12), nb / (hbm_gbs * 1e9))
+                    table.append({
+                        "workload": name, "op": cop + "_bwd", "t_fused_us": r["t_fused"] * 1e6,
+                        "tflops": cw.flops / r["t_fused"] / 1e12,
+                        "roofline_frac": tr / r["t_fused"],
+                        "bound": "tensor" if cw.flops / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
+                        "hbm_gbs": nb / r["t_fused"] / 1e9,
+                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
+                        "norm_gbs": 6 * cw.M * cw.N / r["t_norm"] / 1e9,
                         "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
                     })
                     del r

@@ -250,6 +250,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS);
     volatile int* const abort_flag =
         reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS + 4);
+    volatile int* const epoch_sm =  // global exchange: launch epoch and the last launch's row counters
+        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS + 8);
     float* const ss_buf = reinterpret_cast<float*>(base_ptr + Cfg::OFF_SS);
     uint16_t* const aff = reinterpret_cast<uint16_t*>(base_ptr + Cfg::OFF_AFF);
 
@@ -341,13 +343,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
     // Global exchange: count in bank E & 1; clear the other bank, which the
     // previous launch on this scratch used (it has completed).
     int* xbank = nullptr;
-    if (GLOBALX) {
-        const int e = ld_acquire_gpu(args.xcnt + 2);
-        const int prev_ints = ld_acquire_gpu(args.xcnt + 3) * 4;
-        xbank = args.xcnt + XCH_CNT0 + (e & 1) * args.xbank;
-        int* const other = args.xcnt + XCH_CNT0 + ((e + 1) & 1) * args.xbank;
-        const int stride = static_cast<int>(gridDim.x * blockDim.x);
-        for (int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i < prev_ints; i += stride) other[i] = 0;
+    if (GLOBALX && threadIdx.x == 0) {  // shared with the CTA by the barrier below
+        epoch_sm[0] = ld_acquire_gpu(args.xcnt + 2);
+        epoch_sm[1] = ld_acquire_gpu(args.xcnt + 3) * 4;
     }
     if (Cfg::kRow && !GLOBALX && threadIdx.x < 128) {
         // This CTA's columns never change: clustered CTAs keep their rank's
@@ -368,6 +366,13 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         cluster_wait_acquire();
     }
     const uint32_t tmem_base = *tmem_holder;
+    if (GLOBALX) {
+        const int e = epoch_sm[0], prev_ints = epoch_sm[1];
+        xbank = args.xcnt + XCH_CNT0 + (e & 1) * args.xbank;
+        int* const other = args.xcnt + XCH_CNT0 + ((e + 1) & 1) * args.xbank;
+        const int stride = static_cast<int>(gridDim.x * blockDim.x);
+        for (int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i < prev_ints; i += stride) other[i] = 0;
+    }
 
     if (warp == Cfg::PRODUCER_WARP) {
         // ================================================================ TMA producer

@@ -82,7 +82,7 @@ struct GemmCfg {
     // refilled for each tile.
     static constexpr int AFFINE_BYTES = !kRow ? 0 : (XCH == XCH_GLOBAL ? 2 * (2 * TILE_N * 2) : 2 * TILE_N * 2);
     static constexpr int SS_BYTES = kPre ? 2 * TILE_M * 4 : 0;        // sum of squares [2][128]
-    static constexpr int BAR_BYTES = 256;                             // barriers + 2 words
+    static constexpr int BAR_BYTES = 256;                             // barriers + 4 words
     // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
     // starts 1 KB aligned in practice; the global-exchange variant, whose
     // fourth pipeline stage needs the room, relies on that (and checks it at
@@ -103,7 +103,7 @@ struct GemmCfg {
     static constexpr int OFF_SS = OFF_AFF + AFFINE_BYTES;
     static constexpr int OFF_BAR = OFF_SS + SS_BYTES;
     static_assert(OFF_B % 1024 == 0 && OFF_STG % 1024 == 0, "swizzled buffers need 1 KB alignment");
-    static_assert(NUM_BARRIER_SLOTS * 8 + 8 <= BAR_BYTES, "barrier area + 2 words");
+    static_assert(NUM_BARRIER_SLOTS * 8 + 16 <= BAR_BYTES, "barrier area + 4 words");
 
     static constexpr int PRODUCER_WARP = EPI_WARPS;       // 8
     static constexpr int MMA_WARP = EPI_WARPS + 1;        // 9
