@@ -483,12 +483,37 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         // gamma at saff, beta at saff + 2 TILE_N; the global exchange keeps one
         // such slot per group, refilled for each tile's columns.
         const uint32_t saff = smem_u32(aff) + (GLOBALX ? static_cast<uint32_t>(grp * 4 * TILE_N) : 0u);
+        int aff_n = -1;  // global exchange: the column tile whose gamma / beta are in the slot
         for (int lt = grp; lt < count; lt += 2) {
             int m, n, row0, rows;
             sched.tile(lt, m, n, row0, rows);
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-            bool ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
+            const uint32_t jph = static_cast<uint32_t>(lt >> 1) & 1u;  // this group's tile count parity
+            bool ok = true;
+            if (GLOBALX && affine) {
+                // -- this warp's quarter of the group's affine slot (64 columns),
+                //    refilled only when the column tile changes, once the group's
+                //    four warps are done with the previous tile; done before the
+                //    accumulator is ready so the loads overlap the main loop.
+                if (n != aff_n) {
+                    ok = mbar_wait(guard, bar_affe0 + 8u * grp, jph ^ 1u, SITE_EPI_AFF, lt);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    const int c = qtr * 64 + 2 * lane, col = n * TILE_N + c;  // N % 8 == 0: both or neither in
+                    const bool in = col < args.N;
+                    uint32_t g2 = 0x3F803F80u, b2 = 0u;
+                    if (in && args.gamma)
+                        g2 = static_cast<uint32_t>(args.gamma[col]) | (static_cast<uint32_t>(args.gamma[col + 1]) << 16);
+                    if (in && args.beta)
+                        b2 = static_cast<uint32_t>(args.beta[col]) | (static_cast<uint32_t>(args.beta[col + 1]) << 16);
+                    st_shared_u32(saff + static_cast<uint32_t>(c * 2), g2);
+                    st_shared_u32(saff + static_cast<uint32_t>((TILE_N + c) * 2), b2);
+                    aff_n = n;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_afff0 + 8u * grp);
+            }
+            ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
@@ -501,23 +526,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
             float scale = 1.0f, bias = 0.0f;                         // y = acc * scale + bias
             bool released = false;
             uint32_t v[NC][32];
-            const uint32_t jph = static_cast<uint32_t>(lt >> 1) & 1u;  // this group's tile count parity
 
-            if (GLOBALX && affine) {
-                // -- this warp's quarter of the group's affine slot (64 columns),
-                //    once the group's four warps are done with the previous tile.
-                ok = mbar_wait(guard, bar_affe0 + 8u * grp, jph ^ 1u, SITE_EPI_AFF, lt);
-                if (!__all_sync(0xffffffffu, ok)) break;
-                const int c = qtr * 64 + 2 * lane, col = n * TILE_N + c;  // N % 8 == 0: both or neither in
-                const bool in = col < args.N;
-                uint32_t g2 = 0x3F803F80u, b2 = 0u;
-                if (in && args.gamma) g2 = static_cast<uint32_t>(args.gamma[col]) | (static_cast<uint32_t>(args.gamma[col + 1]) << 16);
-                if (in && args.beta) b2 = static_cast<uint32_t>(args.beta[col]) | (static_cast<uint32_t>(args.beta[col + 1]) << 16);
-                st_shared_u32(saff + static_cast<uint32_t>(c * 2), g2);
-                st_shared_u32(saff + static_cast<uint32_t>((TILE_N + c) * 2), b2);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_afff0 + 8u * grp);
-            }
 
             if (Cfg::kPre) {
                 ok = mbar_wait(guard, bar_ssf0 + 8u * b, aph, SITE_EPI_SS_FULL, lt);
