@@ -513,16 +513,22 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_afff0 + 8u * grp);
             }
-            ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
             const int nv = min(TILE_N, args.N - n * TILE_N);        // valid columns of this tile
             const int nseg = (nv + SEG - 1) / SEG;                   // segments holding them
             // Store only this unit's rows, and nothing past M.
             const int nstore = (qtr * 32 < rows && row0 + qtr * 32 < args.M) ? nv : 0;
             const int grow = row0 + row;                             // global row
             const bool own_row = row < rows && grow < args.M;
+            // Backward: the row's saved statistics, requested before the
+            // accumulator wait (they do not depend on it).
+            const float bmu = (Cfg::kBwdLN && own_row) ? args.mean_in[grow] : 0.0f;
+            const float brs = (Cfg::kBwd && own_row) ? args.rstd_in[grow] : 0.0f;
+            const uint16_t* const zrow =
+                Cfg::kBwd ? args.zin + static_cast<size_t>(own_row ? grow : 0) * args.N + n * TILE_N : nullptr;
+            ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
             float scale = 1.0f, bias = 0.0f;                         // y = acc * scale + bias
             bool released = false;
             uint32_t v[NC][32];
@@ -537,11 +543,6 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                 if (n == 0 && args.rstd_out && own_row) args.rstd_out[grow] = scale;
             }
 
-            // Backward: the row's saved statistics and its Z values.
-            const float bmu = (Cfg::kBwdLN && own_row) ? args.mean_in[grow] : 0.0f;
-            const float brs = (Cfg::kBwd && own_row) ? args.rstd_in[grow] : 0.0f;
-            const uint16_t* const zrow =
-                Cfg::kBwd ? args.zin + static_cast<size_t>(own_row ? grow : 0) * args.N + n * TILE_N : nullptr;
             float bc1 = 0.0f, bc0 = 0.0f;  // backward: dz = g * brs + z * bc1 + bc0
 
             if (Cfg::kBwd) {
