@@ -81,9 +81,14 @@ class Oracle:
                                               _I64, _I64, ctypes.c_int, _P_I64, _I64, _P_F64]
         lib.nfo_norm_rows_bwd.argtypes = [_P_U16, _P_U16, _P_U16, _P_F64, _P_F64, _I64, _I64,
                                           ctypes.c_int, _P_I64, _I64, _P_F64]
+        lib.nfo_prenorm_rms_bwd_da.argtypes = [_P_U16, _P_U16, _P_F64, _P_U16, _I64, _I64, _I64,
+                                               _P_I64, _I64, _P_F64]
+        lib.nfo_prenorm_rms_bwd_db.argtypes = [_P_U16, _P_F64, _P_U16, _I64, _I64, _I64, _P_I64, _I64,
+                                               _P_F64]
         for f in ("nfo_gemm_plain", "nfo_gemm_prenorm_rms", "nfo_gemm_postnorm_ln",
                   "nfo_gemm_postnorm_rms", "nfo_norm_rows", "nfo_gemm_postnorm_bwd",
-                  "nfo_norm_rows_bwd", "nfo_max_threads"):
+                  "nfo_norm_rows_bwd", "nfo_prenorm_rms_bwd_da", "nfo_prenorm_rms_bwd_db",
+                  "nfo_max_threads"):
             getattr(lib, f).restype = ctypes.c_int
         lib.nfo_set_threads.argtypes = [ctypes.c_int]
         lib.nfo_set_threads.restype = None
@@ -195,6 +200,29 @@ class Oracle:
         self._check(self.lib.nfo_norm_rows_bwd(_u16(dY), _u16(Z), _u16(gamma), mp, sp, Rr, C,
                                                int(kind), rp, R, _f64(dZ)), "norm_rows_bwd")
         return dZ
+
+    def prenorm_rms_bwd_da(self, A, B, rstd, dC, rows=None):
+        """dA of C = rmsnorm(A) @ B from dC and the saved rstd (rows of dA)."""
+        M, K = A.shape
+        N = B.shape[1]
+        assert dC.shape == (M, N)
+        r, R, rp = self._rows(rows, M)
+        s, sp = self._stats(rstd, M)
+        dA = np.empty((R, K), np.float64)
+        self._check(self.lib.nfo_prenorm_rms_bwd_da(_u16(A), _u16(B), sp, _u16(dC), M, N, K, rp, R,
+                                                    _f64(dA)), "prenorm_rms_bwd_da")
+        return dA
+
+    def prenorm_rms_bwd_db(self, A, rstd, dC, krows=None):
+        """dB of C = rmsnorm(A) @ B from dC and the saved rstd (rows of dB, over K)."""
+        M, K = A.shape
+        N = dC.shape[1]
+        r, R, rp = self._rows(krows, K)
+        s, sp = self._stats(rstd, M)
+        dB = np.empty((R, N), np.float64)
+        self._check(self.lib.nfo_prenorm_rms_bwd_db(_u16(A), sp, _u16(dC), M, N, K, rp, R, _f64(dB)),
+                    "prenorm_rms_bwd_db")
+        return dB
 
 
 _DEFAULT: Optional[Oracle] = None

@@ -343,6 +343,65 @@ int nfo_norm_rows_bwd(const uint16_t* dY, const uint16_t* Z, const uint16_t* gam
     return bad ? -1 : 0;
 }
 
+int nfo_prenorm_rms_bwd_da(const uint16_t* A, const uint16_t* B, const double* rstd,
+                           const uint16_t* dC, int64_t M, int64_t N, int64_t K,
+                           const int64_t* rows, int64_t nrows, double* dA) {
+    if (!A || !B || !rstd || !dC || !dA || M < 0 || N <= 0 || K <= 0) return -1;
+    if (check_rows(rows, nrows, M)) return -1;
+    const int64_t R = row_count(rows, nrows, M);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* buf = (double*)malloc(sizeof(double) * (size_t)(N + 4 * K));
+        if (!buf) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!buf) continue;
+            const int64_t i = row_index(rows, r);
+            double* dc = buf;
+            double* dxh = buf + N;
+            double* a = buf + N + K;
+            load_row(dC, i, N, dc);
+            /* dXhat[i,k] = sum_n dC[i,n] * B[k,n] */
+            for (int64_t k = 0; k < K; ++k) {
+                const uint16_t* bk = B + k * N;
+                double t = 0.0;
+                for (int64_t n = 0; n < N; ++n) t += dc[n] * bf16_to_double(bk[n]);
+                dxh[k] = t;
+            }
+            load_row(A, i, K, a);
+            norm_bwd_row(dxh, a, K, NULL, NFO_NORM_RMS, 0.0, rstd[i], buf + N + 2 * K, buf + N + 3 * K,
+                         dA + r * K);
+        }
+        free(buf);
+    }
+    return bad ? -1 : 0;
+}
+
+int nfo_prenorm_rms_bwd_db(const uint16_t* A, const double* rstd, const uint16_t* dC,
+                           int64_t M, int64_t N, int64_t K, const int64_t* krows,
+                           int64_t nkrows, double* dB) {
+    if (!A || !rstd || !dC || !dB || M < 0 || N <= 0 || K <= 0) return -1;
+    if (check_rows(krows, nkrows, K)) return -1;
+    const int64_t R = row_count(krows, nkrows, K);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        const int64_t k = row_index(krows, r);
+        double* out = dB + r * N;
+        for (int64_t n = 0; n < N; ++n) out[n] = 0.0;
+        /* dB[k,n] = sum_i (A[i,k] * rstd_i) * dC[i,n] */
+        for (int64_t i = 0; i < M; ++i) {
+            const double xh = bf16_to_double(A[i * K + k]) * rstd[i];
+            const uint16_t* dci = dC + i * N;
+            for (int64_t n = 0; n < N; ++n) out[n] += xh * bf16_to_double(dci[n]);
+        }
+    }
+    return 0;
+}
+
 int nfo_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -89,6 +89,21 @@ int nfo_norm_rows_bwd(const uint16_t* dY, const uint16_t* Z, const uint16_t* gam
                       const double* mean, const double* rstd, int64_t R, int64_t C,
                       int kind, const int64_t* rows, int64_t nrows, double* dZ);
 
+/* Lazy Pre-Norm backward (blog §2, limitation 3: the backward rebuilds
+ * rmsnorm(A) from A and the saved rstd).  Forward: C = xhat B with
+ * xhat[i,k] = A[i,k] * rstd_i.  Given dC (M x N):
+ *   dXhat = dC B^T;  dA[i,k] = rstd_i * (dXhat[i,k] - xhat[i,k] * mean_k(dXhat * xhat))
+ *   dB[k,n] = sum_i xhat[i,k] * dC[i,n].
+ * A is M x K, B is K x N, dC is M x N (bf16), rstd has M entries.
+ * nfo_prenorm_rms_bwd_da writes the listed rows of dA (`rows` over M);
+ * nfo_prenorm_rms_bwd_db writes the listed rows of dB (`krows` over K). */
+int nfo_prenorm_rms_bwd_da(const uint16_t* A, const uint16_t* B, const double* rstd,
+                           const uint16_t* dC, int64_t M, int64_t N, int64_t K,
+                           const int64_t* rows, int64_t nrows, double* dA);
+int nfo_prenorm_rms_bwd_db(const uint16_t* A, const double* rstd, const uint16_t* dC,
+                           int64_t M, int64_t N, int64_t K, const int64_t* krows,
+                           int64_t nkrows, double* dB);
+
 /* Threads used by the loops over rows (OpenMP). */
 int nfo_max_threads(void);
 void nfo_set_threads(int n);

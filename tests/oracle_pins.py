@@ -548,11 +548,84 @@ def pin_norm_bwd_reductions(o):
             f"row list (rows kernel) kind={kind}"
 
 
+def pin_prenorm_bwd_bruteforce(o):
+    """Lazy Pre-Norm backward in exact rationals on tiny problems."""
+    for seed, (M, K, N) in enumerate([(3, 5, 4), (4, 6, 3), (2, 1, 2)]):
+        inp = nf_inputs.make_inputs(M, K, N, seed=400 + seed, w_var=0.5)
+        A, B = inp["X"], inp["W"]
+        dC = bf16_round(np.random.default_rng(500 + seed).normal(size=(M, N)))
+        rstd = np.array([0.5 + 0.25 * i for i in range(M)])
+        af, bf, cf = _frac_matrix(A), _frac_matrix(B), _frac_matrix(dC)
+        rf = [Fraction(float(v)) for v in rstd]
+        dA = o.prenorm_rms_bwd_da(A, B, rstd, dC)
+        dB = o.prenorm_rms_bwd_db(A, rstd, dC)
+        for i in range(M):
+            dxh = [sum((cf[i][n] * bf[k][n] for n in range(N)), Fraction(0)) for k in range(K)]
+            want = _bwd_exact(dxh, af[i], None, 1, Fraction(0), rf[i])
+            scale = 1e-13 * (1 + max(float(abs(v)) for v in want))
+            for k in range(K):
+                _close(dA[i, k], _dec(want[k]), scale, f"pre bwd dA[{i},{k}]")
+        for k in range(K):
+            for n in range(N):
+                want = sum((af[i][k] * rf[i] * cf[i][n] for i in range(M)), Fraction(0))
+                mag = sum(abs(af[i][k] * rf[i] * cf[i][n]) for i in range(M))
+                _close(dB[k, n], _dec(want), 1e-14 * float(mag) + 1e-300, f"pre bwd dB[{k},{n}]")
+
+
+def pin_prenorm_bwd_autograd(o):
+    """torch float64 autograd through C = rms_norm(A) @ B, with A's own rstd."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(53)
+    M, K, N = 9, 40, 24
+    A = bf16_round(rng.normal(0.2, 1.3, size=(M, K)))
+    B = bf16_round(rng.normal(0, 0.2, size=(K, N)))
+    dC = bf16_round(rng.normal(size=(M, N)))
+    eps = 1e-2
+    a = torch.from_numpy(bf16_to_f64(A)).requires_grad_(True)
+    b = torch.from_numpy(bf16_to_f64(B)).requires_grad_(True)
+    c = F.rms_norm(a, (K,), None, eps) @ b
+    (c * torch.from_numpy(bf16_to_f64(dC))).sum().backward()
+    rstd = (1.0 / torch.sqrt((a.detach() ** 2).mean(-1) + eps)).numpy()
+    got_a = o.prenorm_rms_bwd_da(A, B, rstd, dC)
+    got_b = o.prenorm_rms_bwd_db(A, rstd, dC)
+    assert np.allclose(got_a, a.grad.numpy(), rtol=1e-10, atol=1e-12), "pre-norm bwd dA vs autograd"
+    assert np.allclose(got_b, b.grad.numpy(), rtol=1e-10, atol=1e-12), "pre-norm bwd dB vs autograd"
+
+
+def pin_prenorm_bwd_reductions(o):
+    """dC = 1: dB rows are the column sums of xhat; the dA rows' xhat-weighted
+    sums follow the normalization-gradient closed form; row lists agree."""
+    rng = np.random.default_rng(59)
+    M, K, N = 6, 16, 5
+    A = bf16_round(rng.normal(size=(M, K)))
+    B = bf16_round(rng.normal(0, 0.3, size=(K, N)))
+    eps = 0.1
+    a = bf16_to_f64(A)
+    ms = (a * a).mean(-1)
+    rstd = 1.0 / np.sqrt(ms + eps)
+    ones = bf16_round(np.ones((M, N)))
+    xh = a * rstd[:, None]
+    dB = o.prenorm_rms_bwd_db(A, rstd, ones)
+    assert np.allclose(dB, np.repeat(xh.sum(0)[:, None], N, axis=1), rtol=1e-13, atol=1e-13), "dB with dC = 1"
+    dC = bf16_round(rng.normal(size=(M, N)))
+    dA = o.prenorm_rms_bwd_da(A, B, rstd, dC)
+    dxh = bf16_to_f64(dC) @ bf16_to_f64(B).T
+    want = K * rstd ** 3 * eps * (dxh * xh).mean(-1)
+    assert np.allclose((dA * xh).sum(-1), want, rtol=1e-9, atol=1e-12), "dA orthogonality"
+    sub = np.array([5, 1])
+    assert np.array_equal(o.prenorm_rms_bwd_da(A, B, rstd, dC, rows=sub), dA[sub]), "dA row list"
+    ksub = np.array([3, 0, 15])
+    full_b = o.prenorm_rms_bwd_db(A, rstd, dC)
+    assert np.array_equal(o.prenorm_rms_bwd_db(A, rstd, dC, krows=ksub), full_b[ksub]), "dB row list"
+
+
 PINS = [pin_bruteforce_plain, pin_bruteforce_prenorm, pin_bruteforce_postnorm,
         pin_bruteforce_norm_rows, pin_torch_f64, pin_lazy_identity, pin_invariants,
         pin_reductions, pin_power_of_two_scale, pin_row_subset, pin_closed_forms,
         pin_bruteforce_norm_bwd, pin_torch_autograd_bwd, pin_norm_bwd_invariants,
-        pin_norm_bwd_reductions]
+        pin_norm_bwd_reductions, pin_prenorm_bwd_bruteforce, pin_prenorm_bwd_autograd,
+        pin_prenorm_bwd_reductions]
 
 
 def run_all(o):

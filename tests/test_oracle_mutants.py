@@ -57,6 +57,14 @@ MUTANTS = [
     ("bwd_divisor", "const double mgx = sgx / (double)n;", "const double mgx = sgx / (double)(n - 1);"),
     ("bwd_z_ignores_row_list", "load_row(Z, i, N, z);", "load_row(Z, r, N, z);"),
     ("bwd_stats_dense_index", "mean[i] : 0.0, rstd[i],\n                         buf + 2 * N", "mean[r] : 0.0, rstd[r],\n                         buf + 2 * N"),
+    ("prebwd_db_no_rstd", "const double xh = bf16_to_double(A[i * K + k]) * rstd[i];",
+     "const double xh = bf16_to_double(A[i * K + k]);"),
+    ("prebwd_db_transposed_dC", "for (int64_t n = 0; n < N; ++n) out[n] += xh * bf16_to_double(dci[n]);",
+     "for (int64_t n = 0; n < N; ++n) out[n] += xh * bf16_to_double(dC[n * N + i % N]);"),
+    ("prebwd_da_B_not_transposed", "for (int64_t n = 0; n < N; ++n) t += dc[n] * bf16_to_double(bk[n]);",
+     "for (int64_t n = 0; n < N; ++n) t += dc[n] * bf16_to_double(B[(n % K) * N + k % N]);"),
+    ("prebwd_da_wrong_rstd_row", "norm_bwd_row(dxh, a, K, NULL, NFO_NORM_RMS, 0.0, rstd[i],",
+     "norm_bwd_row(dxh, a, K, NULL, NFO_NORM_RMS, 0.0, rstd[r],"),
 ]
 
 
