@@ -93,6 +93,18 @@ nf_status nf_gemm_plain(const void* X, const void* W, void* Y,
                         int64_t M, int64_t N, int64_t K, nf_stream stream);
 
 /*
+ * nf_gemm_plain_t -- Y = op(X) op(W) with one operand read transposed:
+ * flags NF_TRANS_X: X is stored K x M row-major (Y = X^T W; needs M a
+ * multiple of 8); NF_TRANS_W: W is stored N x K row-major (Y = X W^T).  Not
+ * both.  Otherwise as nf_gemm_plain (Y is M x N row-major).  The unfused
+ * baseline of the Lazy Pre-Norm backward uses both forms.
+ */
+#define NF_TRANS_X 1
+#define NF_TRANS_W 4
+nf_status nf_gemm_plain_t(const void* X, const void* W, void* Y, int64_t M,
+                          int64_t N, int64_t K, int flags, nf_stream stream);
+
+/*
  * nf_gemm_prenorm_rms -- Y = RMSNorm(X) * W, Lazy Pre-Norm (blog §2).
  * rstd_i = 1 / sqrt(sum_k X[i,k]^2 / K + eps) is accumulated from the same
  * shared-memory tiles of X the tensor cores consume, and applied to the fp32
@@ -105,6 +117,24 @@ nf_status nf_gemm_plain(const void* X, const void* W, void* Y,
 nf_status nf_gemm_prenorm_rms(const void* X, const void* W, void* Y,
                               int64_t M, int64_t N, int64_t K, float eps,
                               float* rstd_out, nf_stream stream);
+
+/*
+ * nf_gemm_prenorm_rms_bwd -- backward of C = RMSNorm(A) * B (Lazy Pre-Norm,
+ * no affine), from the rstd the forward saved (blog §2, limitation 3: the
+ * backward rebuilds rmsnorm(A) from A and rstd).  With xhat = A * rstd_i:
+ *   dA = rstd_i * (dXhat - xhat * mean_k(dXhat * xhat)),  dXhat = dC B^T
+ *        (the RMS-backward epilogue on a GEMM that reads B transposed);
+ *   dB = xhat^T dC (a GEMM over M whose A operand is read transposed and
+ *        scaled row by row by rstd in shared memory before the MMA).
+ * A: M x K, B: K x N, dC: M x N, dA: M x K, dB: K x N, all bf16 row-major
+ * device memory; rstd: M fp32.  dA or dB may be NULL (not computed).  Same
+ * alignment rules as the forward; dB needs M a multiple of 8 and dA
+ * K <= NF_POSTNORM_MAX_N.  Two kernels are enqueued on `stream`.
+ */
+nf_status nf_gemm_prenorm_rms_bwd(const void* A, const void* B,
+                                  const float* rstd, const void* dC, void* dA,
+                                  void* dB, int64_t M, int64_t N, int64_t K,
+                                  nf_stream stream);
 
 /*
  * nf_gemm_postnorm_ln -- Y = LayerNorm(X * W) over each row of N, Multi-CTA

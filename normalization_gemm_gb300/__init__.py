@@ -70,6 +70,8 @@ _SIGS = {
     "nf_gemm_postnorm_rms": [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
     "nf_norm_rows": [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
     "nf_norm_rows_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP],
+    "nf_gemm_plain_t": [_VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int, _VP],
+    "nf_gemm_prenorm_rms_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_gemm_postnorm_ln_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_gemm_postnorm_rms_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_get_device_status": [_VP],
@@ -179,6 +181,43 @@ def gemm_plain(x, w, out=None, stream=None):
     _check(lib().nf_gemm_plain(_mat(x, "x"), _mat(w, "w"), _mat(y, "out"), M, N, K,
                                _stream(stream)), "nf_gemm_plain")
     return y
+
+
+TRANS_X = 1
+TRANS_W = 4
+
+
+def gemm_plain_t(x, w, flags, out=None, stream=None):
+    """Y = op(x) op(w): TRANS_X -- x holds X^T (K x M); TRANS_W -- w holds W^T (N x K)."""
+    if flags & TRANS_X:
+        K, M = x.shape
+    else:
+        M, K = x.shape
+    if flags & TRANS_W:
+        N, K2 = w.shape
+    else:
+        K2, N = w.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {tuple(x.shape)} and {tuple(w.shape)} with flags {flags}")
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_plain_t(_mat(x, "x"), _mat(w, "w"), _mat(y, "out"), M, N, K, int(flags), _stream(stream)),
+           "nf_gemm_plain_t")
+    return y
+
+
+def gemm_prenorm_rms_bwd(a, b, rstd, dc, da=None, db=None, want_da=True, want_db=True, stream=None):
+    """Backward of C = rmsnorm(a) @ b from the saved rstd (fp32 [M]): returns (dA, dB)."""
+    torch = _torch()
+    M, N, K = _shapes(a, b)
+    if tuple(dc.shape) != (M, N):
+        raise ValueError(f"dc must have shape {(M, N)}")
+    da = (_out(da, M, K, a) if want_da else None)
+    db = (_out(db, K, N, a) if want_db else None)
+    _check(lib().nf_gemm_prenorm_rms_bwd(_mat(a, "a"), _mat(b, "b"), _vec(rstd, "rstd", M, torch.float32),
+                                         _mat(dc, "dc"), None if da is None else _mat(da, "da"),
+                                         None if db is None else _mat(db, "db"), M, N, K, _stream(stream)),
+           "nf_gemm_prenorm_rms_bwd")
+    return da, db
 
 
 def gemm_prenorm_rms(x, w, eps, out=None, rstd_out=None, stream=None):

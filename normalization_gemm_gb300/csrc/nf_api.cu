@@ -201,10 +201,14 @@ struct Plan {
     const GemmVariant* v = nullptr;
 };
 
-const GemmVariant* find_variant(int op, int tile_n, int xch) {
+const GemmVariant* find_variant(int op, int tile_n, int xch, int ops = 0) {
     int n = 0;
     const GemmVariant* t = nullptr;
-    switch (op) {
+    if (ops != 0) {
+        if (op == OP_PLAIN) t = gemm_variants_trans_plain(&n);
+        else if (op == OP_BWD_RMS) t = gemm_variants_trans_bwd(&n);
+        else return nullptr;
+    } else switch (op) {
         case OP_PLAIN: t = gemm_variants_plain(&n); break;
         case OP_PRE: t = gemm_variants_pre(&n); break;
         case OP_POST_LN: t = gemm_variants_post_ln(&n); break;
@@ -214,7 +218,7 @@ const GemmVariant* find_variant(int op, int tile_n, int xch) {
         default: return nullptr;
     }
     for (int i = 0; i < n; ++i)
-        if (t[i].tile_n == tile_n && t[i].xch == xch) return &t[i];
+        if (t[i].tile_n == tile_n && t[i].xch == xch && t[i].ops == ops) return &t[i];
     return nullptr;
 }
 
@@ -236,7 +240,7 @@ const GemmVariant* find_variant(int op, int tile_n, int xch) {
 // The normalization backward (ops 4, 5) follows the same choice with
 // 256-column CTAs only (no 512-column variant): L2 exchange for K >= 512,
 // else a cluster of <= 16.
-nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p) {
+nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, int ops = 0) {
     const bool post = op == OP_POST_LN || op == OP_POST_RMS;
     const bool bwd = op == OP_BWD_LN || op == OP_BWD_RMS;
     p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
@@ -276,7 +280,7 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p) 
     p->cluster = p->clustered ? static_cast<int>((N + p->tile_n - 1) / p->tile_n) : 1;
     p->m_tiles = static_cast<int>((M + TILE_M - 1) / TILE_M);
     p->n_tiles = ((post || bwd) && p->xch != XCH_GLOBAL) ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
-    p->v = find_variant(op, p->tile_n, p->xch);
+    p->v = find_variant(op, p->tile_n, p->xch, ops);
     if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
     p->k_tiles = static_cast<int>((K + p->v->tile_k - 1) / p->v->tile_k);
     return NF_OK;
@@ -487,13 +491,19 @@ nf_status noalloc_scratch(uint8_t** out) {
 
 // fixed_scratch: the global exchange uses the no-alloc array instead of the
 // stream's scratch buffer.
+// ops (OperandFlags): OPS_A_MN -- X is stored K x M; OPS_A_SCALE -- and its
+// row k is scaled by rstd_in[k] on the fly; OPS_B_K -- W is stored N x K.
 nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
                    int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream,
                    bool fixed_scratch = false, const void* zin = nullptr, const float* mean_in = nullptr,
-                   const float* rstd_in = nullptr) {
+                   const float* rstd_in = nullptr, int ops = 0) {
     nf_status st = check_gemm_args(op, X, W, Y, gamma, beta, mean_out, rstd_out, M, N, K, eps);
     if (st != NF_OK) return st;
     if (M == 0) return NF_OK;
+    if ((ops & OPS_A_MN) && M % 8 != 0)
+        return fail(NF_ERR_ALIGNMENT, "a transposed X (K x M) needs M a multiple of 8 (16-byte rows)");
+    if ((ops & OPS_A_SCALE) && (!rstd_in || !aligned(rstd_in, 4)))
+        return fail(NF_ERR_INVALID_ARG, "row scaling needs a 4-byte aligned rstd");
     if (op == OP_BWD_LN || op == OP_BWD_RMS) {
         if (!zin || !rstd_in || (op == OP_BWD_LN && !mean_in))
             return fail(NF_ERR_INVALID_ARG, "Z, rstd (and mean for LN) must be non-null");
@@ -504,15 +514,22 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     DeviceState* d = nullptr;
     if ((st = device_state(&d)) != NF_OK) return st;
     Plan p;
-    if ((st = plan_tiles(op, M, N, K, d->sm_count, &p)) != NF_OK) return st;
+    if ((st = plan_tiles(op, M, N, K, d->sm_count, &p, ops)) != NF_OK) return st;
     if ((st = prepare_kernel(d, p.v)) != NF_OK) return st;
 
     CUtensorMap tmX, tmW, tmY;
     const int tk = p.v->tile_k;  // 64: 128-byte rows of X; 32: 64-byte rows
-    if ((st = make_map(&tmX, X, M, K, tk, TILE_M, tk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) !=
-        NF_OK)
+    if (ops & OPS_A_MN) {  // X stored K x M: boxes of 64 K-rows x 64 output rows
+        if ((st = make_map(&tmX, X, K, M, 64, 64)) != NF_OK) return st;
+    } else if ((st = make_map(&tmX, X, M, K, tk, TILE_M,
+                              tk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) != NF_OK) {
         return st;
-    if ((st = make_map(&tmW, W, K, N, B_BOX_N, tk)) != NF_OK) return st;
+    }
+    if (ops & OPS_B_K) {  // W stored N x K: boxes of tile_n output columns x 64 K
+        if ((st = make_map(&tmW, W, N, K, tk, p.tile_n)) != NF_OK) return st;
+    } else if ((st = make_map(&tmW, W, K, N, B_BOX_N, tk)) != NF_OK) {
+        return st;
+    }
     if ((st = make_map(&tmY, Y, M, N, STORE_COLS, STORE_ROWS)) != NF_OK) return st;
 
     GemmArgs a;
@@ -655,6 +672,40 @@ nf_status nf_gemm_postnorm_rms_bwd(const void* A, const void* B, const void* Z, 
                                    void* dZ, int64_t M, int64_t N, int64_t K, nf_stream stream) {
     return run_gemm(OP_BWD_RMS, A, B, gamma, nullptr, dZ, M, N, K, 0.0f, nullptr, nullptr,
                     reinterpret_cast<cudaStream_t>(stream), false, Z, nullptr, rstd);
+}
+
+nf_status nf_gemm_plain_t(const void* X, const void* W, void* Y, int64_t M, int64_t N, int64_t K, int flags,
+                          nf_stream stream) {
+    if (flags & ~(NF_TRANS_X | NF_TRANS_W)) return fail(NF_ERR_INVALID_ARG, "flags: NF_TRANS_X | NF_TRANS_W");
+    if ((flags & NF_TRANS_X) && (flags & NF_TRANS_W))
+        return fail(NF_ERR_UNSUPPORTED_SHAPE, "only one operand may be transposed");
+    const int ops = ((flags & NF_TRANS_X) ? OPS_A_MN : 0) | ((flags & NF_TRANS_W) ? OPS_B_K : 0);
+    return run_gemm(OP_PLAIN, X, W, nullptr, nullptr, Y, M, N, K, 0.0f, nullptr, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), false, nullptr, nullptr, nullptr, ops);
+}
+
+nf_status nf_gemm_prenorm_rms_bwd(const void* A, const void* B, const float* rstd, const void* dC, void* dA, void* dB,
+                                  int64_t M, int64_t N, int64_t K, nf_stream stream) {
+    if (M < 0 || N < 1 || K < 1) return fail(NF_ERR_INVALID_ARG, "need M >= 0, N >= 1, K >= 1");
+    if (M == 0) return NF_OK;
+    if (!A || !B || !rstd || !dC) return fail(NF_ERR_INVALID_ARG, "A, B, rstd and dC must be non-null");
+    if (!dA && !dB) return NF_OK;
+    if (M % 8 != 0 && dB) return fail(NF_ERR_ALIGNMENT, "dB needs M a multiple of 8 (A is read transposed)");
+    if (K > NF_POSTNORM_MAX_N && dA)
+        return fail(NF_ERR_UNSUPPORTED_SHAPE, "dA needs K <= 4096 (the RMS backward reduces over K)");
+    nf_status st = NF_OK;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // dA = rmsnorm_bwd(dC B^T; A, rstd): a GEMM of M x K over N whose W (= B,
+    // stored K x N) is read transposed, RMS-backward epilogue with Z = A.
+    if (dA && (st = run_gemm(OP_BWD_RMS, dC, B, nullptr, nullptr, dA, M, K, N, 0.0f, nullptr, nullptr, s, false, A,
+                             nullptr, rstd, OPS_B_K)) != NF_OK)
+        return st;
+    // dB = rmsnorm(A)^T dC: a GEMM of K x N over M whose X (= A, stored M x K)
+    // is read transposed with row m scaled by rstd[m] on the fly.
+    if (dB && (st = run_gemm(OP_PLAIN, A, dC, nullptr, nullptr, dB, K, N, M, 0.0f, nullptr, nullptr, s, false,
+                             nullptr, nullptr, rstd, OPS_A_MN | OPS_A_SCALE)) != NF_OK)
+        return st;
+    return NF_OK;
 }
 
 nf_status nf_gemm_postnorm_rms(const void* X, const void* W, const void* gamma, void* Y, int64_t M, int64_t N,

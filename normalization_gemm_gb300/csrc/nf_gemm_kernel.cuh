@@ -210,11 +210,11 @@ struct TileSched {
     }
 };
 
-template <int EPI, int TILE_N, int XCH>
-__global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
+template <int EPI, int TILE_N, int XCH, int OPS = 0>
+__global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     nf_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const __grid_constant__ CUtensorMap tmY, const GemmArgs args) {
-    using Cfg = GemmCfg<EPI, TILE_N, XCH>;
+    using Cfg = GemmCfg<EPI, TILE_N, XCH, OPS>;
     constexpr bool CLUSTERED = XCH == XCH_CLUSTER;
     constexpr bool GLOBALX = XCH == XCH_GLOBAL;
     constexpr int STAGES = Cfg::STAGES;
@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
     const uint32_t bar_ssf0 = sBar + 8u * 20;    // [2]
     const uint32_t bar_xch0 = sBar + 8u * 22;    // [2]
     const uint32_t bar_mma_done = sBar + 8u * 24;
+    const uint32_t bar_xf0 = sBar + 256u;        // [8] A row scaling: stage s transformed
     const uint32_t bar_afff0 = sBar + 8u * 25;   // [2] global exchange: a group's affine slot filled
     const uint32_t bar_affe0 = sBar + 8u * 27;   // [2] global exchange: a group's affine slot free
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS);
@@ -304,6 +305,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
             mbar_init(bar_xch0 + 8u * b, 1);
         }
         mbar_init(bar_mma_done, 1);
+        if (Cfg::kScaleA)
+            for (int st = 0; st < STAGES; ++st) mbar_init(bar_xf0 + 8u * st, 128);  // the transform threads
         for (int g = 0; g < 2; ++g) {
             mbar_init(bar_afff0 + 8u * g, 4);  // one arrival per warp of the group
             mbar_init(bar_affe0 + 8u * g, 4);
@@ -328,7 +331,12 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         for (int i = 0; i < STAGES && lt < count; ++i) {
             int m, n, row0, rows;
             sched.tile(lt, m, n, row0, rows);
-            tma_prefetch_l2_2d(&tmX, kt * TILE_K, row0);
+            if (Cfg::kAMN) {
+                tma_prefetch_l2_2d(&tmX, row0, kt * TILE_K);
+                tma_prefetch_l2_2d(&tmX, row0 + 64, kt * TILE_K);
+            } else {
+                tma_prefetch_l2_2d(&tmX, kt * TILE_K, row0);
+            }
             if (++kt == k_tiles) {
                 kt = 0;
                 ++lt;
@@ -391,11 +399,24 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                     }
                     const uint32_t fb = bar_full0 + 8u * s;
                     mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                    tma_load_2d(sA + s * A_STAGE_BYTES, &tmX, fb, kt * TILE_K, row0);
+                    if (Cfg::kAMN) {
+                        // X stored K x M: two boxes of 64 output rows x 64 K-rows
+                        // (MN-major A: 128-byte rows along the output rows).
+                        tma_load_2d(sA + s * A_STAGE_BYTES, &tmX, fb, row0, kt * TILE_K);
+                        tma_load_2d(sA + s * A_STAGE_BYTES + B_BOX_BYTES, &tmX, fb, row0 + 64, kt * TILE_K);
+                    } else {
+                        tma_load_2d(sA + s * A_STAGE_BYTES, &tmX, fb, kt * TILE_K, row0);
+                    }
+                    if (Cfg::kBK) {
+                        // W stored N x K: one box of TILE_N output columns x 64 K
+                        // (K-major B: 128-byte rows along K, like A).
+                        tma_load_2d(sB + s * Cfg::B_STAGE_BYTES, &tmW, fb, kt * TILE_K, n * TILE_N);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < NBOX; ++i)
-                        tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb,
-                                    n * TILE_N + i * B_BOX_N, kt * TILE_K);
+                        for (int i = 0; i < NBOX; ++i)
+                            tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb,
+                                        n * TILE_N + i * B_BOX_N, kt * TILE_K);
+                    }
                     ++issued;
                     if (++s == STAGES) {
                         s = 0;
@@ -416,7 +437,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
     } else if (warp == Cfg::MMA_WARP) {
         // ================================================================ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, TILE_N, true);
+            constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, TILE_N, !Cfg::kBK, Cfg::kAMN);
+            // A transformed in shared memory is consumed after the transform
+            // warps released the stage, not when its bytes landed.
+            const uint32_t bar_ready0 = Cfg::kScaleA ? bar_xf0 : bar_full0;
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(b * TILE_N);
                 for (int kt = 0; kt < k_tiles; ++kt) {
-                    if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_MMA_FULL, lt)) {
+                    if (!mbar_wait(guard, bar_ready0 + 8u * s, ph, SITE_MMA_FULL, lt)) {
                         ok = false;
                         break;
                     }
@@ -440,8 +464,13 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
                         //    swizzled 128-byte row; 8-row groups 1 KB apart.
                         // B: MN-major, advance 16 K-rows = 2 KB; 8-row groups
                         //    1 KB apart, 64-column boxes 8 KB apart.
-                        const uint64_t adesc = smem_desc_sw128(a0 + j * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + j * 2048, B_BOX_BYTES, 1024);
+                        // (Transposed operands: MN-major A advances 2 KB per 16
+                        //  K-rows with its two 64-row boxes 8 KB apart; K-major B
+                        //  advances 32 bytes like A.)
+                        const uint64_t adesc = Cfg::kAMN ? smem_desc_sw128(a0 + j * 2048, B_BOX_BYTES, 1024)
+                                                         : smem_desc_sw128(a0 + j * 32, 16, 1024);
+                        const uint64_t bdesc = Cfg::kBK ? smem_desc_sw128(b0 + j * 32, 16, 1024)
+                                                        : smem_desc_sw128(b0 + j * 2048, B_BOX_BYTES, 1024);
                         mma_bf16(d, adesc, bdesc, IDESC, (kt | j) != 0 ? 1u : 0u);
                     }
                     mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
@@ -834,6 +863,44 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
         // complete with the grid.
         if (lane == STORE_LANE) bulk_wait_read<0>();
         __syncwarp();
+    } else if (Cfg::kScaleA && warp >= Cfg::SUMSQ_WARP0) {
+        // ================================================================ A row scaling
+        // The stored matrix's rmsnorm rebuilt on the fly: contraction row m of
+        // the transposed A (a 128-byte row of 64 output rows in one of the
+        // stage's two boxes; the swizzle only permutes its 16-byte chunks) is
+        // multiplied by rstd[m] and rounded back to bf16 before the MMA reads it.
+        const int t = static_cast<int>(threadIdx.x) - Cfg::SUMSQ_WARP0 * 32;  // 0..127
+        const int box = t >> 6, r = t & 63;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int lt = 0; lt < count && ok; ++lt) {
+            for (int kt = 0; kt < k_tiles; ++kt) {
+                const int mrow = kt * TILE_K + r;
+                const float sc = mrow < args.K ? args.rstd_in[mrow] : 0.0f;
+                if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t rbase = sA + s * A_STAGE_BYTES + static_cast<uint32_t>(box * B_BOX_BYTES + r * 128);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t a = rbase + static_cast<uint32_t>(q * 16);
+                    const uint4 w = ld_shared_v4(a);
+                    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = pack_bf16x2(bf16lo(in[e]) * sc, bf16hi(in[e]) * sc);
+                    st_shared_v4(a, o[0], o[1], o[2], o[3]);
+                }
+                fence_proxy_async_smem();  // the tensor cores read these writes
+                mbar_arrive(bar_xf0 + 8u * s);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
     } else if (Cfg::kPre && warp >= Cfg::SUMSQ_WARP0) {
         // ================================================================ row sums of squares
         const int row = static_cast<int>(threadIdx.x) - Cfg::SUMSQ_WARP0 * 32;  // 0..127
@@ -907,14 +974,15 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH>::THREADS, 1)
     }
 }
 
-template <int EPI, int TILE_N, int XCH>
+template <int EPI, int TILE_N, int XCH, int OPS = 0>
 GemmVariant make_variant() {
-    using Cfg = GemmCfg<EPI, TILE_N, XCH>;
+    using Cfg = GemmCfg<EPI, TILE_N, XCH, OPS>;
     return GemmVariant{EPI,
                        TILE_N,
                        XCH == XCH_CLUSTER,
                        XCH,
-                       reinterpret_cast<const void*>(&nf_gemm_kernel<EPI, TILE_N, XCH>),
+                       OPS,
+                       reinterpret_cast<const void*>(&nf_gemm_kernel<EPI, TILE_N, XCH, OPS>),
                        Cfg::THREADS,
                        Cfg::SMEM_BYTES,
                        Cfg::STAGES,

@@ -60,7 +60,16 @@ __host__ __device__ inline int64_t xch_stats_bytes(int m_tiles, int n_tiles) {
     return static_cast<int64_t>(m_tiles) * n_tiles * 128 * 8;
 }
 
-template <int EPI, int TILE_N, int XCH>
+// Operand layouts (GemmCfg OPS bits).  Default: A K-major (X is M x K
+// row-major), B MN-major (W is K x N row-major).
+enum OperandFlags : int {
+    OPS_A_MN = 1,     // A given as its transpose: X stored K x M row-major (Y = X^T W)
+    OPS_A_SCALE = 2,  // with OPS_A_MN: each contraction row m of A scaled by rstd[m] in shared
+                      // memory before the MMA (rmsnorm of the stored matrix rebuilt on the fly)
+    OPS_B_K = 4,      // B given as its transpose: W stored N x K row-major (Y = X W^T)
+};
+
+template <int EPI, int TILE_N, int XCH, int OPS = 0>
 struct GemmCfg {
     static constexpr bool kPre = EPI == EPI_PRE_RMS;
     static constexpr bool kPost = EPI == EPI_POST_LN || EPI == EPI_POST_RMS;
@@ -69,6 +78,10 @@ struct GemmCfg {
     static constexpr bool kBwdLN = EPI == EPI_BWD_LN;
     static constexpr bool kRow = kPost || kBwd;  // reduces over the output row (N)
     static constexpr bool CLUSTERED = XCH == XCH_CLUSTER;
+    static constexpr bool kAMN = (OPS & OPS_A_MN) != 0;
+    static constexpr bool kScaleA = (OPS & OPS_A_SCALE) != 0;
+    static constexpr bool kBK = (OPS & OPS_B_K) != 0;
+    static_assert(!kScaleA || (kAMN && EPI == EPI_PLAIN), "row scaling applies to a transposed A, plain epilogue");
     static_assert(TILE_N == 64 || TILE_N == 128 || TILE_N == 256, "tile_n");
     static_assert(XCH == XCH_NONE || (kRow && TILE_N == 256), "row exchange only for post-norm");
 
@@ -82,7 +95,7 @@ struct GemmCfg {
     // refilled for each tile.
     static constexpr int AFFINE_BYTES = !kRow ? 0 : (XCH == XCH_GLOBAL ? 2 * (2 * TILE_N * 2) : 2 * TILE_N * 2);
     static constexpr int SS_BYTES = kPre ? 2 * TILE_M * 4 : 0;        // sum of squares [2][128]
-    static constexpr int BAR_BYTES = 256;                             // barriers + 4 words
+    static constexpr int BAR_BYTES = kScaleA ? 320 : 256;             // barriers (+ xformed[8]) + 4 words
     // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
     // starts 1 KB aligned in practice; the global-exchange variant, whose
     // fourth pipeline stage needs the room, relies on that (and checks it at
@@ -103,12 +116,14 @@ struct GemmCfg {
     static constexpr int OFF_SS = OFF_AFF + AFFINE_BYTES;
     static constexpr int OFF_BAR = OFF_SS + SS_BYTES;
     static_assert(OFF_B % 1024 == 0 && OFF_STG % 1024 == 0, "swizzled buffers need 1 KB alignment");
-    static_assert(NUM_BARRIER_SLOTS * 8 + 16 <= BAR_BYTES, "barrier area + 4 words");
+    static_assert(NUM_BARRIER_SLOTS * 8 + 16 <= 256, "barrier area + 4 words");
+    static_assert(!kScaleA || (NUM_BARRIER_SLOTS + 8) * 8 + 16 <= BAR_BYTES, "barrier area with xformed[8]");
 
     static constexpr int PRODUCER_WARP = EPI_WARPS;       // 8
     static constexpr int MMA_WARP = EPI_WARPS + 1;        // 9
-    static constexpr int SUMSQ_WARP0 = EPI_WARPS + 2;     // pre-norm only: warps 10-13
-    static constexpr int THREADS = (kPre ? EPI_WARPS + 6 : EPI_WARPS + 2) * 32;
+    static constexpr int SUMSQ_WARP0 = EPI_WARPS + 2;     // pre-norm: sum-of-squares warps 10-13;
+                                                          // A row scaling: transform warps 10-13
+    static constexpr int THREADS = (kPre || kScaleA ? EPI_WARPS + 6 : EPI_WARPS + 2) * 32;
     static constexpr int TMEM_COLS = 2 * TILE_N;           // two accumulator buffers
 };
 
@@ -129,7 +144,7 @@ struct GemmArgs {
     uint64_t timeout_ns;
     const uint16_t* zin;    // backward: Z, M x N bf16 (the forward's norm input)
     const float* mean_in;   // backward LN: saved row means (M)
-    const float* rstd_in;   // backward: saved row rstd (M)
+    const float* rstd_in;   // backward: saved row rstd (M); OPS_A_SCALE: rstd per contraction row (K)
     int* xcnt;              // global exchange only: XCH_CNT0 + 2 * xbank ints
     int32_t xbank;          // ints per counter bank, >= xch_bank_ints(m_tiles)
     float2* xstats;         // global exchange only: >= xch_stats_bytes(m_tiles, n_tiles)
@@ -157,6 +172,7 @@ struct GemmVariant {
     int epi, tile_n;
     bool clustered;  // xch == XCH_CLUSTER
     int xch;
+    int ops;         // OperandFlags
     const void* func;
     int threads, smem_bytes, stages, tmem_cols;
     int tile_k;  // K per ring stage: 64 (X boxes 128-byte swizzled) or 32 (64-byte swizzled)
@@ -169,6 +185,8 @@ const GemmVariant* gemm_variants_post_ln(int* count);
 const GemmVariant* gemm_variants_post_rms(int* count);
 const GemmVariant* gemm_variants_bwd_ln(int* count);
 const GemmVariant* gemm_variants_bwd_rms(int* count);
+const GemmVariant* gemm_variants_trans_plain(int* count);  // plain GEMMs with OperandFlags
+const GemmVariant* gemm_variants_trans_bwd(int* count);    // RMS-backward epilogue over X W^T
 
 // ---------------------------------------------------------------- row norm
 struct NormArgs {

@@ -333,8 +333,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo,
 // D format in bits 4-5 (1 = f32), A format 7-9 and B format 10-12 (1 = bf16),
 // A major bit 15 (0 = K-major), B major bit 16 (1 = MN-major), N >> 3 in bits
 // 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major, bool a_mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
            (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 

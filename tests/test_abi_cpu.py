@@ -202,3 +202,16 @@ def test_backward_argument_checks(L):
     assert L.nf_gemm_postnorm_ln_bwd(P, P, P, None, P, P, P, 128, 4104, 64, None) == 3
     assert L.nf_norm_rows_bwd(P, P, None, None, P, P, 4, 64, 0, None) == INVALID
     assert L.nf_norm_rows_bwd(P, P, None, None, P, P, 0, 64, 0, None) == OK
+
+
+def test_transposed_and_prenorm_backward_checks(L):
+    # both operands transposed; an unknown flag; a transposed X needs M % 8 == 0
+    assert L.nf_gemm_plain_t(P, P, P, 64, 64, 64, 5, None) == SHAPE
+    assert L.nf_gemm_plain_t(P, P, P, 64, 64, 64, 2, None) == INVALID
+    assert L.nf_gemm_plain_t(P, P, P, 60, 64, 64, 1, None) == ALIGN
+    assert L.nf_gemm_plain_t(P, P, P, 0, 64, 64, 1, None) == OK
+    # pre-norm backward: null inputs; dB needs M % 8 == 0; dA needs K <= 4096; nothing asked
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, None, P, P, P, 64, 64, 64, None) == INVALID
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, None, P, 60, 64, 64, None) == ALIGN
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, P, None, 64, 64, 4104, None) == SHAPE
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, None, None, 64, 64, 64, None) == OK
