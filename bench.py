@@ -22,9 +22,11 @@ Prints ONE JSON line (rank 0):
                and reads Y back.
   cpu_baseline the fp64 oracle on the host cores (a bounded sample).
   configs      per-workload figures for the other four workloads (not the
-               headline), and for the normalization backward fused into the
+               headline), for the normalization backward fused into the
                epilogue of the GEMM producing its incoming gradient (post-norm
-               shapes; unfused pair: plain GEMM + row backward kernel).
+               shapes; unfused pair: plain GEMM + row backward kernel), and for
+               the Lazy Pre-Norm backward (pre-norm shapes; unfused: rmsnorm
+               materialized, transposed plain GEMMs, row backward kernel).
 --impl reference times the fp64 oracle itself as the reference arm.
 Under torchrun (N > 1) every rank runs its own independent batch of the same
 size (rows shard across GPUs, no collective on the data path; weak scaling).
@@ -357,6 +359,49 @@ def measure_backward(nf, w, kind, dev, stream, steps, warmup, seed=0):
     return out
 
 
+def measure_prenorm_backward(nf, w, dev, stream, steps, warmup, seed=0):
+    """Lazy Pre-Norm backward: the fused pair of kernels (dA with the RMS-backward
+    epilogue, dB with rmsnorm(A) rebuilt in shared memory) against the unfused
+    sequence: rmsnorm(A) materialized, dB = xhat^T dC and dXhat = dC B^T by the
+    transposed plain GEMMs, dA by the row backward kernel."""
+    import torch
+    inp = nf_inputs.workload_inputs(w, seed=seed)
+    dC = nf_inputs.make_inputs(w.M, w.N, 8, seed=seed + 3)["X"]
+    a = nf_inputs.bf16_to_f64(inp["X"])
+    rstd = (1.0 / np.sqrt((a * a).mean(-1) + w.eps)).astype(np.float32)
+    A0, B0, C0 = _to_dev(inp["X"], dev), _to_dev(inp["W"], dev), _to_dev(dC, dev)
+    r = torch.from_numpy(rstd).to(dev)
+    dA0 = torch.empty_like(A0)
+    dB0 = torch.empty((w.K, w.N), dtype=torch.bfloat16, device=dev)
+    set_bytes = 2 * (2 * A0.numel() + C0.numel()) + dB0.numel() * 2
+    sets, nsets = make_sets([A0, C0, dA0, dB0], set_bytes, dev)
+
+    def fused(i):
+        x, c, da, db = sets[i % nsets]
+        nf.gemm_prenorm_rms_bwd(x, B0, r, c, da=da, db=db, stream=stream)
+
+    out = {"t_fused": time_steps(fused, steps, warmup, stream) / steps}
+    xh = [torch.empty_like(A0) for _ in range(nsets)]
+    dxh = [torch.empty_like(A0) for _ in range(nsets)]
+
+    def gemms(i):
+        x, c, da, db = sets[i % nsets]
+        nf.gemm_plain_t(xh[i % nsets], c, nf.TRANS_X, out=db, stream=stream)
+        nf.gemm_plain_t(c, B0, nf.TRANS_W, out=dxh[i % nsets], stream=stream)
+
+    def norms(i):
+        x, c, da, db = sets[i % nsets]
+        nf.norm_rows(x, nf.NORM_RMS, w.eps, out=xh[i % nsets], stream=stream)
+        nf.norm_rows_bwd(dxh[i % nsets], x, nf.NORM_RMS, None, r, out=da, stream=stream)
+
+    ksteps = max(1, min(steps, 2000))
+    out["t_plain"] = time_steps(gemms, ksteps, min(warmup, 10), stream) / ksteps
+    out["t_norm"] = time_steps(norms, ksteps, min(warmup, 10), stream) / ksteps
+    del sets, xh, dxh
+    torch.cuda.empty_cache()
+    return out
+
+
 def backward_bytes(w, kind):
     """Each tensor moved once: A, B and Z read, dZ written, the saved
     statistics (and gamma) read."""
@@ -593,6 +638,25 @@ def main(argv=None):
                         "hbm_gbs": nb / r["t_fused"] / 1e9,
                         "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
                         "norm_gbs": norm_bytes(r["norm_rows"], r["norm_cols"]) / r["t_norm"] / 1e9,
+                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
+                    })
+                    del r
+                    torch.cuda.empty_cache()
+                if "pre_rms" in cw.ops:
+                    # Lazy Pre-Norm backward: two GEMMs (4MNK flops); bytes: A read
+                    # twice, dC twice, B, dA, dB, rstd twice
+                    steps = 100 if cw.flops > 5e10 else 500
+                    r = measure_prenorm_backward(nf, cw, dev, stream, steps, 10)
+                    nb = (6 * cw.M * cw.K + 4 * cw.M * cw.N + 4 * cw.K * cw.N + 8 * cw.M)
+                    fl = 2 * cw.flops
+                    tr = max(fl / (bf16_tf * 1e12), nb / (hbm_gbs * 1e9))
+                    table.append({
+                        "workload": name, "op": "pre_rms_bwd", "t_fused_us": r["t_fused"] * 1e6,
+                        "tflops": fl / r["t_fused"] / 1e12, "roofline_frac": tr / r["t_fused"],
+                        "bound": "tensor" if fl / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
+                        "hbm_gbs": nb / r["t_fused"] / 1e9,
+                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
+                        "norm_gbs": (4 * cw.M * cw.K + 6 * cw.M * cw.K) / r["t_norm"] / 1e9,
                         "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
                     })
                     del r

@@ -127,7 +127,8 @@ nf_status nf_gemm_prenorm_rms(const void* X, const void* W, void* Y,
  *   dB = xhat^T dC (a GEMM over M whose A operand is read transposed and
  *        scaled row by row by rstd in shared memory before the MMA).
  * A: M x K, B: K x N, dC: M x N, dA: M x K, dB: K x N, all bf16 row-major
- * device memory; rstd: M fp32.  dA or dB may be NULL (not computed).  Same
+ * device memory; rstd: M fp32 (16-byte aligned for dB).  dA or dB may be
+ * NULL (not computed).  Same
  * alignment rules as the forward; dB needs M a multiple of 8 and dA
  * K <= NF_POSTNORM_MAX_N.  Two kernels are enqueued on `stream`.
  */

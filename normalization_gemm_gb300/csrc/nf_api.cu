@@ -502,8 +502,9 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     if (M == 0) return NF_OK;
     if ((ops & OPS_A_MN) && M % 8 != 0)
         return fail(NF_ERR_ALIGNMENT, "a transposed X (K x M) needs M a multiple of 8 (16-byte rows)");
-    if ((ops & OPS_A_SCALE) && (!rstd_in || !aligned(rstd_in, 4)))
-        return fail(NF_ERR_INVALID_ARG, "row scaling needs a 4-byte aligned rstd");
+    if ((ops & OPS_A_SCALE) && !rstd_in) return fail(NF_ERR_INVALID_ARG, "row scaling needs rstd");
+    if ((ops & OPS_A_SCALE) && !aligned(rstd_in, 16))  // copied 64 values at a time with the ring stages
+        return fail(NF_ERR_ALIGNMENT, "row scaling needs a 16-byte aligned rstd");
     if (op == OP_BWD_LN || op == OP_BWD_RMS) {
         if (!zin || !rstd_in || (op == OP_BWD_LN && !mean_in))
             return fail(NF_ERR_INVALID_ARG, "Z, rstd (and mean for LN) must be non-null");

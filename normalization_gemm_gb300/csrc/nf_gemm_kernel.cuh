@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     const uint32_t sStg = base + Cfg::OFF_STG;
     const uint32_t sRecv = base + Cfg::OFF_RECV;
     const uint32_t sBar = base + Cfg::OFF_BAR;
+    const uint32_t sRS = base + Cfg::OFF_RS;  // A row scaling: rstd of each stage's 64 K-rows
     const uint32_t bar_full0 = sBar;             // [8]
     const uint32_t bar_empty0 = sBar + 8u * 8;   // [8]
     const uint32_t bar_accf0 = sBar + 8u * 16;   // [2]
@@ -398,7 +399,16 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                         break;
                     }
                     const uint32_t fb = bar_full0 + 8u * s;
-                    mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                    if (Cfg::kScaleA) {
+                        // The stage's 64 rstd values (fewer at the end of K) come
+                        // with it: K % 8 == 0 keeps the byte count a multiple of 32.
+                        const int nr = min(TILE_K, args.K - kt * TILE_K);
+                        mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES + static_cast<uint32_t>(nr * 4));
+                        bulk_load_g2s(sRS + static_cast<uint32_t>(s * TILE_K * 4), args.rstd_in + kt * TILE_K,
+                                      static_cast<uint32_t>(nr * 4), fb);
+                    } else {
+                        mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                    }
                     if (Cfg::kAMN) {
                         // X stored K x M: two boxes of 64 output rows x 64 K-rows
                         // (MN-major A: 128-byte rows along the output rows).
@@ -876,16 +886,18 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         bool ok = true;
         for (int lt = 0; lt < count && ok; ++lt) {
             for (int kt = 0; kt < k_tiles; ++kt) {
-                const int mrow = kt * TILE_K + r;
-                const float sc = mrow < args.K ? args.rstd_in[mrow] : 0.0f;
                 if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)) {
                     ok = false;
                     break;
                 }
+                const int mrow = kt * TILE_K + r;
+                const float sc = mrow < args.K ? ld_shared_f32(sRS + static_cast<uint32_t>((s * TILE_K + r) * 4)) : 0.0f;
                 const uint32_t rbase = sA + s * A_STAGE_BYTES + static_cast<uint32_t>(box * B_BOX_BYTES + r * 128);
+                // Rows are 128 bytes apart: each thread starts at a different
+                // 16-byte chunk so a quarter-warp covers 8 bank groups.
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const uint32_t a = rbase + static_cast<uint32_t>(q * 16);
+                    const uint32_t a = rbase + (static_cast<uint32_t>((q + r) & 7) << 4);
                     const uint4 w = ld_shared_v4(a);
                     const uint32_t in[4] = {w.x, w.y, w.z, w.w};
                     uint32_t o[4];

@@ -95,6 +95,9 @@ struct GemmCfg {
     // refilled for each tile.
     static constexpr int AFFINE_BYTES = !kRow ? 0 : (XCH == XCH_GLOBAL ? 2 * (2 * TILE_N * 2) : 2 * TILE_N * 2);
     static constexpr int SS_BYTES = kPre ? 2 * TILE_M * 4 : 0;        // sum of squares [2][128]
+    // A row scaling: each ring stage's 64 rstd values, copied with the stage.
+    // (256-column tiles fit four stages at most, narrower ones up to eight.)
+    static constexpr int RS_BYTES = kScaleA ? (TILE_N == 256 ? 4 : MAX_STAGES) * TILE_K * 4 : 0;
     static constexpr int BAR_BYTES = kScaleA ? 320 : 256;             // barriers (+ xformed[8]) + 4 words
     // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
     // starts 1 KB aligned in practice; the global-exchange variant, whose
@@ -102,10 +105,11 @@ struct GemmCfg {
     // run time), the others keep 1 KB of slack to realign.
     static constexpr int ALIGN_SLACK = XCH == XCH_GLOBAL ? 0 : 1024;
     static constexpr int FIXED_BYTES =
-        ALIGN_SLACK + STAGING_BYTES + RECV_BYTES + AFFINE_BYTES + SS_BYTES + BAR_BYTES;
+        ALIGN_SLACK + STAGING_BYTES + RECV_BYTES + AFFINE_BYTES + SS_BYTES + RS_BYTES + BAR_BYTES;
     static constexpr int STAGES_FIT = (SMEM_OPTIN_LIMIT - FIXED_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
     static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert(!kScaleA || RS_BYTES >= STAGES * TILE_K * 4, "one rstd slot per stage");
     static constexpr int SMEM_BYTES = FIXED_BYTES + STAGES * STAGE_BYTES;
 
     static constexpr int OFF_A = 0;
@@ -114,7 +118,8 @@ struct GemmCfg {
     static constexpr int OFF_RECV = OFF_STG + STAGING_BYTES;
     static constexpr int OFF_AFF = OFF_RECV + RECV_BYTES;
     static constexpr int OFF_SS = OFF_AFF + AFFINE_BYTES;
-    static constexpr int OFF_BAR = OFF_SS + SS_BYTES;
+    static constexpr int OFF_RS = OFF_SS + SS_BYTES;
+    static constexpr int OFF_BAR = OFF_RS + RS_BYTES;
     static_assert(OFF_B % 1024 == 0 && OFF_STG % 1024 == 0, "swizzled buffers need 1 KB alignment");
     static_assert(NUM_BARRIER_SLOTS * 8 + 16 <= 256, "barrier area + 4 words");
     static_assert(!kScaleA || (NUM_BARRIER_SLOTS + 8) * 8 + 16 <= BAR_BYTES, "barrier area with xformed[8]");
