@@ -325,7 +325,7 @@ def backward_inputs(w, seed=0):
     return inp, Z, mean.astype(np.float32), var, ms
 
 
-def measure_backward(nf, w, kind, dev, stream, steps, warmup, seed=0):
+def measure_backward(nf, w, kind, dev, stream, steps, warmup, seed=0, eager=False, unfused=True):
     """Fused GEMM + norm-backward epilogue, and the unfused pair (plain GEMM
     writing dY, then the row backward kernel), time per launch."""
     import torch
@@ -346,7 +346,11 @@ def measure_backward(nf, w, kind, dev, stream, steps, warmup, seed=0):
         else:
             nf.gemm_postnorm_rms_bwd(a, B0, z, rstd_d, G, out=d, stream=stream)
 
-    out = {"t_fused": time_steps(fused, steps, warmup, stream) / steps}
+    out = {"t_fused": time_steps(fused, steps, warmup, stream, eager=eager) / steps}
+    if not unfused:
+        del sets
+        torch.cuda.empty_cache()
+        return out
     dys = [torch.empty_like(D0) for _ in range(nsets)]
     plain = lambda i: nf.gemm_plain(sets[i % nsets][0], B0, out=dys[i % nsets], stream=stream)  # noqa: E731
     norm = lambda i: nf.norm_rows_bwd(dys[i % nsets], sets[i % nsets][1], kind, mean_d, rstd_d, G,  # noqa: E731
@@ -359,7 +363,7 @@ def measure_backward(nf, w, kind, dev, stream, steps, warmup, seed=0):
     return out
 
 
-def measure_prenorm_backward(nf, w, dev, stream, steps, warmup, seed=0):
+def measure_prenorm_backward(nf, w, dev, stream, steps, warmup, seed=0, eager=False, unfused=True):
     """Lazy Pre-Norm backward: the fused pair of kernels (dA with the RMS-backward
     epilogue, dB with rmsnorm(A) rebuilt in shared memory) against the unfused
     sequence: rmsnorm(A) materialized, dB = xhat^T dC and dXhat = dC B^T by the
@@ -380,7 +384,11 @@ def measure_prenorm_backward(nf, w, dev, stream, steps, warmup, seed=0):
         x, c, da, db = sets[i % nsets]
         nf.gemm_prenorm_rms_bwd(x, B0, r, c, da=da, db=db, stream=stream)
 
-    out = {"t_fused": time_steps(fused, steps, warmup, stream) / steps}
+    out = {"t_fused": time_steps(fused, steps, warmup, stream, eager=eager) / steps}
+    if not unfused:
+        del sets
+        torch.cuda.empty_cache()
+        return out
     xh = [torch.empty_like(A0) for _ in range(nsets)]
     dxh = [torch.empty_like(A0) for _ in range(nsets)]
 
@@ -533,6 +541,9 @@ def main(argv=None):
     ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused pair")
     ap.add_argument("--no-soak", action="store_true", help="never add a clock-sampling soak")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--backward", choices=["post_ln", "post_rms", "pre_rms"], default=None,
+                    help="time only this op's backward on the workload's shapes and print its figures "
+                         "(a profiling aid; not the benchmark line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -557,6 +568,17 @@ def main(argv=None):
     nf.clear_device_status()
     stream = torch.cuda.Stream(device=dev)
     hbm_gbs, bf16_tf, bf16_sus, peak_src = measured_peaks()
+    if args.backward:
+        w = nf_inputs.WORKLOADS[args.workload]
+        if args.backward == "pre_rms":
+            r = measure_prenorm_backward(nf, w, dev, stream, args.steps, args.warmup, eager=args.eager,
+                                         unfused=not args.no_unfused)
+        else:
+            r = measure_backward(nf, w, 0 if args.backward == "post_ln" else 1, dev, stream, args.steps,
+                                 args.warmup, eager=args.eager, unfused=not args.no_unfused)
+        print(json.dumps({"backward": args.backward, "workload": w.name,
+                          **{k: v * 1e6 for k, v in r.items() if k.startswith("t_")}}), flush=True)
+        return 0
 
     w = nf_inputs.WORKLOADS[args.workload]
     op = args.op or w.ops[0]
