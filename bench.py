@@ -365,9 +365,9 @@ def measure_backward(nf, w, kind, dev, stream, steps, warmup, seed=0, eager=Fals
 
 def measure_prenorm_backward(nf, w, dev, stream, steps, warmup, seed=0, eager=False, unfused=True):
     """Lazy Pre-Norm backward: the fused pair of kernels (dA with the RMS-backward
-    epilogue, dB with rmsnorm(A) rebuilt in shared memory) against the unfused
-    sequence: rmsnorm(A) materialized, dB = xhat^T dC and dXhat = dC B^T by the
-    transposed plain GEMMs, dA by the row backward kernel."""
+    epilogue, which also writes rmsnorm(A) as a side output; dB a GEMM over it)
+    against the unfused sequence: rmsnorm(A) materialized, dB = xhat^T dC and
+    dXhat = dC B^T by the transposed plain GEMMs, dA by the row backward kernel."""
     import torch
     inp = nf_inputs.workload_inputs(w, seed=seed)
     dC = nf_inputs.make_inputs(w.M, w.N, 8, seed=seed + 3)["X"]
@@ -377,12 +377,13 @@ def measure_prenorm_backward(nf, w, dev, stream, steps, warmup, seed=0, eager=Fa
     r = torch.from_numpy(rstd).to(dev)
     dA0 = torch.empty_like(A0)
     dB0 = torch.empty((w.K, w.N), dtype=torch.bfloat16, device=dev)
-    set_bytes = 2 * (2 * A0.numel() + C0.numel()) + dB0.numel() * 2
-    sets, nsets = make_sets([A0, C0, dA0, dB0], set_bytes, dev)
+    XH0 = torch.empty_like(A0)
+    set_bytes = 2 * (3 * A0.numel() + C0.numel()) + dB0.numel() * 2
+    sets, nsets = make_sets([A0, C0, dA0, dB0, XH0], set_bytes, dev)
 
     def fused(i):
-        x, c, da, db = sets[i % nsets]
-        nf.gemm_prenorm_rms_bwd(x, B0, r, c, da=da, db=db, stream=stream)
+        x, c, da, db, xhat = sets[i % nsets]
+        nf.gemm_prenorm_rms_bwd(x, B0, r, c, da=da, db=db, xhat=xhat, stream=stream)
 
     out = {"t_fused": time_steps(fused, steps, warmup, stream, eager=eager) / steps}
     if not unfused:
@@ -393,12 +394,12 @@ def measure_prenorm_backward(nf, w, dev, stream, steps, warmup, seed=0, eager=Fa
     dxh = [torch.empty_like(A0) for _ in range(nsets)]
 
     def gemms(i):
-        x, c, da, db = sets[i % nsets]
+        x, c, da, db, _ = sets[i % nsets]
         nf.gemm_plain_t(xh[i % nsets], c, nf.TRANS_X, out=db, stream=stream)
         nf.gemm_plain_t(c, B0, nf.TRANS_W, out=dxh[i % nsets], stream=stream)
 
     def norms(i):
-        x, c, da, db = sets[i % nsets]
+        x, c, da, db, _ = sets[i % nsets]
         nf.norm_rows(x, nf.NORM_RMS, w.eps, out=xh[i % nsets], stream=stream)
         nf.norm_rows_bwd(dxh[i % nsets], x, nf.NORM_RMS, None, r, out=da, stream=stream)
 

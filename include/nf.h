@@ -124,18 +124,25 @@ nf_status nf_gemm_prenorm_rms(const void* X, const void* W, void* Y,
  * backward rebuilds rmsnorm(A) from A and rstd).  With xhat = A * rstd_i:
  *   dA = rstd_i * (dXhat - xhat * mean_k(dXhat * xhat)),  dXhat = dC B^T
  *        (the RMS-backward epilogue on a GEMM that reads B transposed);
- *   dB = xhat^T dC (a GEMM over M whose A operand is read transposed and
- *        scaled row by row by rstd in shared memory before the MMA).
+ *   dB = xhat^T dC (a GEMM over M whose A operand is read transposed).
+ * xhat: optional M x K bf16 buffer (16-byte aligned), owned by the caller.
+ *   Given together with dA, the dA kernel's epilogue, which reads A and rstd
+ *   anyway, also writes xhat = bf16(A * rstd_i) into it, and dB is a plain
+ *   GEMM over that buffer.  NULL (or dA NULL): dB rebuilds xhat from A in
+ *   shared memory, scaling each contraction row by rstd before the MMA -- no
+ *   extra memory, but the rescaling competes with the tensor cores for
+ *   shared-memory bandwidth.  Both forms round xhat to bf16 the same way.
  * A: M x K, B: K x N, dC: M x N, dA: M x K, dB: K x N, all bf16 row-major
  * device memory; rstd: M fp32 (16-byte aligned for dB).  dA or dB may be
- * NULL (not computed).  Same
- * alignment rules as the forward; dB needs M a multiple of 8 and dA
- * K <= NF_POSTNORM_MAX_N.  Two kernels are enqueued on `stream`.
+ * NULL (not computed).  Same alignment rules as the forward; dB needs M a
+ * multiple of 8 and dA K <= NF_POSTNORM_MAX_N.  Two to three kernels are
+ * enqueued on `stream` (dB with few output tiles is split over the
+ * contraction, see nf_set_gemm_splitk).
  */
 nf_status nf_gemm_prenorm_rms_bwd(const void* A, const void* B,
                                   const float* rstd, const void* dC, void* dA,
-                                  void* dB, int64_t M, int64_t N, int64_t K,
-                                  nf_stream stream);
+                                  void* dB, void* xhat, int64_t M, int64_t N,
+                                  int64_t K, nf_stream stream);
 
 /*
  * nf_gemm_postnorm_ln -- Y = LayerNorm(X * W) over each row of N, Multi-CTA
@@ -292,6 +299,17 @@ nf_status nf_set_postnorm_tile_n(int tile_n);
 #define NF_XCH_GLOBAL 2
 nf_status nf_set_postnorm_exchange(int mode);
 
+/* Split-K of plain GEMMs (nf_gemm_plain, nf_gemm_plain_t and the weight
+ * gradient of nf_gemm_prenorm_rms_bwd).  mode 0 (default): when the output
+ * has at most half as many 128-row tiles as the device has SMs, the
+ * contraction is cut into slices of >= 8 K-tiles, one (tile, slice) per SM;
+ * each writes an fp32 partial product into a per-stream workspace (SMs x
+ * 128 KB, allocated by the first such call on a stream, which must not be
+ * inside a graph capture), and a second kernel adds the slices in a fixed
+ * order and rounds to bf16, so results are reproducible.  mode 1: never
+ * split.  Applies to later calls. */
+nf_status nf_set_gemm_splitk(int mode);
+
 /* Self-test of the time limit: launches one CTA that waits on a barrier no
  * thread ever arrives on, with limit `timeout_ns` (1e3..1e10).  After the
  * stream completes, nf_get_device_status() reports NF_ERR_TIMEOUT. */
@@ -318,12 +336,13 @@ typedef struct nf_plan {
     int32_t tmem_cols;              /* tensor-memory columns per CTA       */
     int32_t tiles;                  /* output tiles (M/tile_m x N/tile_n)  */
     int32_t exchange;               /* 0 none, NF_XCH_CLUSTER, NF_XCH_GLOBAL */
+    int32_t splitk;                 /* contraction slices (plain GEMM; 1 = none) */
 } nf_plan;
 nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count,
                        nf_plan* out);
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define NF_ABI_VERSION 2
+#define NF_ABI_VERSION 3
 int nf_abi_version(void);
 
 #ifdef __cplusplus

@@ -54,7 +54,7 @@ class NFError(RuntimeError):
 class NFPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "tile_m", "tile_n", "tile_k", "stages", "cluster", "grid", "threads", "smem_bytes",
-        "tmem_cols", "tiles", "exchange")]
+        "tmem_cols", "tiles", "exchange", "splitk")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -71,7 +71,7 @@ _SIGS = {
     "nf_norm_rows": [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
     "nf_norm_rows_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP],
     "nf_gemm_plain_t": [_VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int, _VP],
-    "nf_gemm_prenorm_rms_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
+    "nf_gemm_prenorm_rms_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_gemm_postnorm_ln_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_gemm_postnorm_rms_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP],
     "nf_get_device_status": [_VP],
@@ -80,6 +80,7 @@ _SIGS = {
     "nf_set_launch_overlap": [ctypes.c_int],
     "nf_set_postnorm_tile_n": [ctypes.c_int],
     "nf_set_postnorm_exchange": [ctypes.c_int],
+    "nf_set_gemm_splitk": [ctypes.c_int],
     "nf_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "nf_plan_gemm": [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(NFPlan)],
     "nf_abi_version": [],
@@ -205,17 +206,29 @@ def gemm_plain_t(x, w, flags, out=None, stream=None):
     return y
 
 
-def gemm_prenorm_rms_bwd(a, b, rstd, dc, da=None, db=None, want_da=True, want_db=True, stream=None):
-    """Backward of C = rmsnorm(a) @ b from the saved rstd (fp32 [M]): returns (dA, dB)."""
+def gemm_prenorm_rms_bwd(a, b, rstd, dc, da=None, db=None, want_da=True, want_db=True, xhat=None,
+                         use_xhat=True, stream=None):
+    """Backward of C = rmsnorm(a) @ b from the saved rstd (fp32 [M]): returns (dA, dB).
+
+    With both gradients wanted and ``use_xhat`` (default), the dA kernel also
+    writes rmsnorm(a) (bf16 [M, K], into ``xhat`` if given, else a temporary)
+    and dB is a plain GEMM over it; ``use_xhat=False`` rebuilds it in shared
+    memory inside the dB GEMM instead (no extra memory)."""
     torch = _torch()
     M, N, K = _shapes(a, b)
     if tuple(dc.shape) != (M, N):
         raise ValueError(f"dc must have shape {(M, N)}")
     da = (_out(da, M, K, a) if want_da else None)
     db = (_out(db, K, N, a) if want_db else None)
+    if want_da and want_db and use_xhat:
+        xhat = _out(xhat, M, K, a)
+    else:
+        xhat = None
     _check(lib().nf_gemm_prenorm_rms_bwd(_mat(a, "a"), _mat(b, "b"), _vec(rstd, "rstd", M, torch.float32),
                                          _mat(dc, "dc"), None if da is None else _mat(da, "da"),
-                                         None if db is None else _mat(db, "db"), M, N, K, _stream(stream)),
+                                         None if db is None else _mat(db, "db"),
+                                         None if xhat is None else _mat(xhat, "xhat"), M, N, K,
+                                         _stream(stream)),
            "nf_gemm_prenorm_rms_bwd")
     return da, db
 
@@ -359,6 +372,11 @@ def set_launch_overlap(enable: bool) -> None:
 def set_postnorm_tile_n(tile_n: int) -> None:
     """Post-norm column tile per CTA: 0 automatic, 256 or 512 forced."""
     _check(lib().nf_set_postnorm_tile_n(int(tile_n)), "nf_set_postnorm_tile_n")
+
+
+def set_gemm_splitk(mode: int) -> None:
+    """Split-K of plain GEMMs with few output tiles: 0 automatic (default), 1 never."""
+    _check(lib().nf_set_gemm_splitk(int(mode)), "nf_set_gemm_splitk")
 
 
 def set_postnorm_exchange(mode: int) -> None:

@@ -66,6 +66,8 @@ int g_post_tile = 0;
 int g_post_xch = 0;
 // A cooperative launch accepted the programmatic-serialization attribute.
 bool g_coop_overlap_ok = true;
+// Split-K of plain GEMMs: 0 = automatic, 1 = never.
+int g_splitk_mode = 0;
 std::mutex g_mu;
 
 constexpr int kMaxDevices = 64;
@@ -193,6 +195,7 @@ nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 enum Op { OP_PLAIN = 0, OP_PRE = 1, OP_POST_LN = 2, OP_POST_RMS = 3, OP_BWD_LN = 4, OP_BWD_RMS = 5 };
 
 struct Plan {
+    int splitk = 1;  // contraction slices (plain GEMM)
     int tile_n = 0;
     int xch = XCH_NONE;
     bool clustered = false;
@@ -283,6 +286,19 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
     p->v = find_variant(op, p->tile_n, p->xch, ops);
     if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
     p->k_tiles = static_cast<int>((K + p->v->tile_k - 1) / p->v->tile_k);
+    // Split-K (plain GEMM): when the output has at most half as many tiles as
+    // there are SMs, cut the contraction into slices of >= 8 K-tiles so that
+    // tiles x slices fills the SMs once; fp32 partials, added by a second kernel.
+    p->splitk = 1;
+    if (op == OP_PLAIN && g_splitk_mode != 1) {
+        const int tiles = p->m_tiles * p->n_tiles;
+        if (2 * tiles <= sms) {
+            int s = sms / tiles;
+            const int kmax = p->k_tiles / 8;
+            if (s > kmax) s = kmax;
+            if (s > 1) p->splitk = s;
+        }
+    }
     return NF_OK;
 }
 
@@ -468,6 +484,46 @@ nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, 
     return NF_OK;
 }
 
+// Split-K workspace, one per (device, stream), sized once for a full wave of
+// 128 x 256 fp32 partial tiles (splitk x M x N <= SMs x 128 x 256).  Every
+// value the reduction reads was written by the GEMM before it, so it needs no
+// clearing.  The first call per stream allocates (refused during capture).
+struct SKScratch {
+    int dev = -1;
+    cudaStream_t stream = nullptr;
+    float* ptr = nullptr;
+};
+SKScratch g_sk[kMaxScratch];
+int g_sk_n = 0;
+
+nf_status splitk_scratch(cudaStream_t stream, int sm_count, float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_sk_n; ++i)
+        if (g_sk[i].dev == dev && g_sk[i].stream == stream) {
+            *out = g_sk[i].ptr;
+            return NF_OK;
+        }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(NF_ERR_INVALID_ARG,
+                    "the split-K workspace is set up on the first split GEMM per stream: make that call before "
+                    "capturing the stream");
+    if (g_sk_n == kMaxScratch) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many streams with split-K workspaces");
+    void* ptr = nullptr;
+    const size_t bytes = static_cast<size_t>(sm_count) * TILE_M * 256 * sizeof(float);
+    if ((e = cudaMalloc(&ptr, bytes)) != cudaSuccess) return fail_cuda(e, "cudaMalloc(split-K workspace)");
+    g_sk[g_sk_n].dev = dev;
+    g_sk[g_sk_n].stream = stream;
+    g_sk[g_sk_n].ptr = static_cast<float*>(ptr);
+    ++g_sk_n;
+    *out = static_cast<float*>(ptr);
+    return NF_OK;
+}
+
 // The current device's fixed no-alloc scratch: address looked up and the
 // array cleared on first use per device.
 nf_status noalloc_scratch(uint8_t** out) {
@@ -496,7 +552,7 @@ nf_status noalloc_scratch(uint8_t** out) {
 nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
                    int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream,
                    bool fixed_scratch = false, const void* zin = nullptr, const float* mean_in = nullptr,
-                   const float* rstd_in = nullptr, int ops = 0) {
+                   const float* rstd_in = nullptr, int ops = 0, void* xhat_out = nullptr) {
     nf_status st = check_gemm_args(op, X, W, Y, gamma, beta, mean_out, rstd_out, M, N, K, eps);
     if (st != NF_OK) return st;
     if (M == 0) return NF_OK;
@@ -511,6 +567,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         if (!aligned(zin, 16)) return fail(NF_ERR_ALIGNMENT, "Z must be 16-byte aligned");
         if ((mean_in && !aligned(mean_in, 4)) || !aligned(rstd_in, 4))
             return fail(NF_ERR_ALIGNMENT, "mean and rstd must be 4-byte aligned");
+        if (xhat_out && !aligned(xhat_out, 16)) return fail(NF_ERR_ALIGNMENT, "xhat must be 16-byte aligned");
     }
     DeviceState* d = nullptr;
     if ((st = device_state(&d)) != NF_OK) return st;
@@ -555,6 +612,9 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.xcnt = nullptr;
     a.xbank = 0;
     a.xstats = nullptr;
+    a.splitk = p.splitk;
+    a.ws = nullptr;
+    a.xhat_out = (op == OP_BWD_LN || op == OP_BWD_RMS) ? static_cast<uint16_t*>(xhat_out) : nullptr;
 
     int grid = 0;
     a.units = p.m_tiles * p.n_tiles;
@@ -585,6 +645,12 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         } else if ((st = xch_scratch(stream, p.m_tiles, p.n_tiles, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
             return st;
         }
+    } else if (p.splitk > 1) {
+        // One (tile, slice) unit per CTA: tiles x splitk <= SMs.
+        if ((st = splitk_scratch(stream, d->sm_count, &a.ws)) != NF_OK) return st;
+        a.units = p.m_tiles * p.n_tiles * p.splitk;
+        a.split_base = a.units;
+        grid = a.units;
     } else {
         const int tiles = p.m_tiles * p.n_tiles;
         grid = tiles < d->sm_count ? tiles : d->sm_count;
@@ -629,6 +695,10 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
     }
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+    if (p.splitk > 1 &&
+        (e = launch_splitk_reduce(a.ws, p.splitk, M * N, static_cast<uint16_t*>(Y), d->sm_count, g_overlap, stream)) !=
+            cudaSuccess)
+        return fail_cuda(e, "split-K reduction launch");
     return NF_OK;
 }
 
@@ -686,7 +756,7 @@ nf_status nf_gemm_plain_t(const void* X, const void* W, void* Y, int64_t M, int6
 }
 
 nf_status nf_gemm_prenorm_rms_bwd(const void* A, const void* B, const float* rstd, const void* dC, void* dA, void* dB,
-                                  int64_t M, int64_t N, int64_t K, nf_stream stream) {
+                                  void* xhat, int64_t M, int64_t N, int64_t K, nf_stream stream) {
     if (M < 0 || N < 1 || K < 1) return fail(NF_ERR_INVALID_ARG, "need M >= 0, N >= 1, K >= 1");
     if (M == 0) return NF_OK;
     if (!A || !B || !rstd || !dC) return fail(NF_ERR_INVALID_ARG, "A, B, rstd and dC must be non-null");
@@ -696,15 +766,24 @@ nf_status nf_gemm_prenorm_rms_bwd(const void* A, const void* B, const float* rst
         return fail(NF_ERR_UNSUPPORTED_SHAPE, "dA needs K <= 4096 (the RMS backward reduces over K)");
     nf_status st = NF_OK;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (xhat && !aligned(xhat, 16)) return fail(NF_ERR_ALIGNMENT, "xhat must be 16-byte aligned");
+    const bool side = xhat && dA;  // the dA kernel writes xhat, dB reads it
     // dA = rmsnorm_bwd(dC B^T; A, rstd): a GEMM of M x K over N whose W (= B,
-    // stored K x N) is read transposed, RMS-backward epilogue with Z = A.
+    // stored K x N) is read transposed, RMS-backward epilogue with Z = A
+    // (and, with xhat, the side output xhat = bf16(A * rstd)).
     if (dA && (st = run_gemm(OP_BWD_RMS, dC, B, nullptr, nullptr, dA, M, K, N, 0.0f, nullptr, nullptr, s, false, A,
-                             nullptr, rstd, OPS_B_K)) != NF_OK)
+                             nullptr, rstd, OPS_B_K, side ? xhat : nullptr)) != NF_OK)
         return st;
-    // dB = rmsnorm(A)^T dC: a GEMM of K x N over M whose X (= A, stored M x K)
-    // is read transposed with row m scaled by rstd[m] on the fly.
-    if (dB && (st = run_gemm(OP_PLAIN, A, dC, nullptr, nullptr, dB, K, N, M, 0.0f, nullptr, nullptr, s, false,
-                             nullptr, nullptr, rstd, OPS_A_MN | OPS_A_SCALE)) != NF_OK)
+    // dB = rmsnorm(A)^T dC: a GEMM of K x N over M whose X is read
+    // transposed -- xhat as written above, or A with row m scaled by rstd[m]
+    // in shared memory on the fly.
+    if (dB && side &&
+        (st = run_gemm(OP_PLAIN, xhat, dC, nullptr, nullptr, dB, K, N, M, 0.0f, nullptr, nullptr, s, false, nullptr,
+                       nullptr, nullptr, OPS_A_MN)) != NF_OK)
+        return st;
+    if (dB && !side &&
+        (st = run_gemm(OP_PLAIN, A, dC, nullptr, nullptr, dB, K, N, M, 0.0f, nullptr, nullptr, s, false, nullptr,
+                       nullptr, rstd, OPS_A_MN | OPS_A_SCALE)) != NF_OK)
         return st;
     return NF_OK;
 }
@@ -840,6 +919,12 @@ nf_status nf_set_postnorm_exchange(int mode) {
     return NF_OK;
 }
 
+nf_status nf_set_gemm_splitk(int mode) {
+    if (mode != 0 && mode != 1) return fail(NF_ERR_INVALID_ARG, "split-K mode: 0 automatic, 1 never");
+    g_splitk_mode = mode;
+    return NF_OK;
+}
+
 nf_status nf_set_launch_overlap(int enable) {
     g_overlap = enable != 0;
     return NF_OK;
@@ -890,9 +975,12 @@ nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf
     out->tmem_cols = p.v->tmem_cols;
     out->tiles = M > 0 ? p.m_tiles * p.n_tiles : 0;
     out->exchange = p.xch;
+    out->splitk = p.splitk;
     if (p.clustered) {
         const int mc = sm_count / p.cluster;
         out->grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;
+    } else if (p.splitk > 1) {
+        out->grid = out->tiles * p.splitk;
     } else {
         out->grid = out->tiles < sm_count ? out->tiles : sm_count;
     }

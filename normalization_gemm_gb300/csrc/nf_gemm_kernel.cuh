@@ -182,15 +182,33 @@ __device__ __forceinline__ void load_z64(const uint16_t* p, bool own, int valid,
 // tiles of the last, partial wave cut into two 64-row halves, so that wave
 // spreads over twice as many SMs.  A half still runs the 128-row MMA (the X
 // box simply starts 64 rows further for the second half); only its own 64
-// rows are stored.
+// rows are stored.  A split-K launch (splitk > 1, plain GEMM) has
+// tiles x splitk units, slice-major: unit u is tile u mod tiles over the
+// contraction slice u / tiles, K-tiles [s k_tiles / splitk, (s+1) k_tiles / splitk).
 struct TileSched {
     int first, step, count;  // m (clustered) or linear unit (unclustered) sequence
     int n_fixed;             // clustered: this CTA's n tile (its cluster rank)
     int n_tiles;
     int split_base;          // first half-tile unit (unclustered)
+    int tiles;               // m_tiles x n_tiles
+    int splitk;              // contraction slices
+    int k_tiles;
     bool clustered;
+    // K-tiles of unit lt and its slice.
+    __device__ __forceinline__ void krange(int lt, int& kt0, int& kt1, int& slice) const {
+        if (splitk <= 1) {
+            kt0 = 0;
+            kt1 = k_tiles;
+            slice = 0;
+            return;
+        }
+        slice = (first + lt * step) / tiles;
+        kt0 = static_cast<int>(static_cast<int64_t>(slice) * k_tiles / splitk);
+        kt1 = static_cast<int>(static_cast<int64_t>(slice + 1) * k_tiles / splitk);
+    }
     __device__ __forceinline__ void tile(int lt, int& m, int& n, int& row0, int& rows) const {
-        const int u = first + lt * step;
+        int u = first + lt * step;
+        if (splitk > 1) u -= (u / tiles) * tiles;
         if (clustered) {
             m = u;
             n = n_fixed;
@@ -284,6 +302,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         sched.n_fixed = 0;
         sched.split_base = args.split_base;
     }
+    sched.tiles = args.m_tiles * args.n_tiles;
+    sched.splitk = args.splitk;
+    sched.k_tiles = args.k_tiles;
     const int count = sched.count;
     const int k_tiles = args.k_tiles;
     const uint32_t xch_bytes = static_cast<uint32_t>(args.cluster) * TILE_M * 8u;
@@ -327,8 +348,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     // Warm L2 with this CTA's first ring-full of X K-tiles while a preceding
     // grid may still be running.  A prefetch only fills L2 lines, and L2 is
     // where that grid's writes land, so the loads below never see stale data.
-    if (warp == Cfg::PRODUCER_WARP && lane == 0) {
-        int lt = 0, kt = 0;
+    if (warp == Cfg::PRODUCER_WARP && lane == 0 && count > 0) {
+        int lt = 0, kt0, kt1, slice;
+        sched.krange(0, kt0, kt1, slice);
+        int kt = kt0;
         for (int i = 0; i < STAGES && lt < count; ++i) {
             int m, n, row0, rows;
             sched.tile(lt, m, n, row0, rows);
@@ -338,9 +361,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             } else {
                 tma_prefetch_l2_2d(&tmX, kt * TILE_K, row0);
             }
-            if (++kt == k_tiles) {
-                kt = 0;
-                ++lt;
+            if (++kt == kt1) {
+                if (++lt < count) sched.krange(lt, kt0, kt1, slice);
+                kt = kt0;
             }
         }
     }
@@ -391,9 +414,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             uint32_t issued = 0;
             bool ok = true;
             for (int lt = 0; lt < count && ok; ++lt) {
-                int m, n, row0, rows;
+                int m, n, row0, rows, kt0, kt1, slice;
                 sched.tile(lt, m, n, row0, rows);
-                for (int kt = 0; kt < k_tiles; ++kt) {
+                sched.krange(lt, kt0, kt1, slice);
+                for (int kt = kt0; kt < kt1; ++kt) {
                     if (!mbar_wait(guard, bar_empty0 + 8u * s, ph ^ 1u, SITE_PROD_EMPTY, lt)) {
                         ok = false;
                         break;
@@ -460,7 +484,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 if (!mbar_wait(guard, bar_acce0 + 8u * b, aph ^ 1u, SITE_MMA_ACC_EMPTY, lt)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(b * TILE_N);
-                for (int kt = 0; kt < k_tiles; ++kt) {
+                int kt0, kt1, slice;
+                sched.krange(lt, kt0, kt1, slice);
+                for (int kt = kt0; kt < kt1; ++kt) {
                     if (!mbar_wait(guard, bar_ready0 + 8u * s, ph, SITE_MMA_FULL, lt)) {
                         ok = false;
                         break;
@@ -481,7 +507,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                                                          : smem_desc_sw128(a0 + j * 32, 16, 1024);
                         const uint64_t bdesc = Cfg::kBK ? smem_desc_sw128(b0 + j * 32, 16, 1024)
                                                         : smem_desc_sw128(b0 + j * 2048, B_BOX_BYTES, 1024);
-                        mma_bf16(d, adesc, bdesc, IDESC, (kt | j) != 0 ? 1u : 0u);
+                        mma_bf16(d, adesc, bdesc, IDESC, (kt != kt0 || j != 0) ? 1u : 0u);
                     }
                     mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
                     if (++s == STAGES) {
@@ -524,8 +550,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         const uint32_t saff = smem_u32(aff) + (GLOBALX ? static_cast<uint32_t>(grp * 4 * TILE_N) : 0u);
         int aff_n = -1;  // global exchange: the column tile whose gamma / beta are in the slot
         for (int lt = grp; lt < count; lt += 2) {
-            int m, n, row0, rows;
+            int m, n, row0, rows, kt0, kt1, slice;
             sched.tile(lt, m, n, row0, rows);
+            sched.krange(lt, kt0, kt1, slice);
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
             const uint32_t jph = static_cast<uint32_t>(lt >> 1) & 1u;  // this group's tile count parity
@@ -812,6 +839,25 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                         released = true;
                     }
                 }
+                if (EPI == EPI_PLAIN && args.splitk > 1) {
+                    // Split-K: the row's fp32 partial over this unit's slice of
+                    // the contraction goes to the slice's plane of the
+                    // workspace; a second kernel adds the planes in order.
+                    const int cw = sg * SEG;
+                    if (own_row && cw < nv) {
+                        float* const dst =
+                            args.ws + (static_cast<size_t>(slice) * args.M + grow) * args.N + n * TILE_N + cw;
+#pragma unroll
+                        for (int q = 0; q < SEG / 4; ++q)
+                            if (q * 4 < nv - cw) {
+                                const uint32_t* src = &v[q >> 3][(q & 7) * 4];
+                                __stcg(reinterpret_cast<float4*>(dst + q * 4),
+                                       make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
+                                                   __uint_as_float(src[2]), __uint_as_float(src[3])));
+                            }
+                    }
+                    continue;
+                }
                 // The segment's 64-column box goes through this warp's staging
                 // buffer (128B swizzle) and one TMA store.
                 constexpr int NQ = SEG / STORE_COLS;
@@ -828,6 +874,22 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                             if (Cfg::kBwd) {
                                 uint4 zq[8];
                                 load_z64(zrow + c0, own_row, nv - c0, zq);
+                                if (args.xhat_out != nullptr && own_row) {
+                                    // Side output: the normalized forward input
+                                    // xhat = (z - mean) * rstd, rounded to bf16.
+                                    uint16_t* const xp =
+                                        args.xhat_out + static_cast<size_t>(grow) * args.N + n * TILE_N + c0;
+#pragma unroll
+                                    for (int q = 0; q < 8; ++q)
+                                        if (q * 8 < nv - c0) {
+                                            const uint32_t zw[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+                                            uint32_t o[4];
+#pragma unroll
+                                            for (int e = 0; e < 4; ++e)
+                                                o[e] = pack_bf16x2((bf16lo(zw[e]) - bmu) * brs, (bf16hi(zw[e]) - bmu) * brs);
+                                            *reinterpret_cast<uint4*>(xp + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                                        }
+                                }
                                 if (affine && args.gamma)
                                     convert64_bwd<true>(v[2 * q], v[2 * q + 1], zq, saff + c0 * 2, f2_splat(brs),
                                                         f2_splat(bc1), f2_splat(bc0), pk);
@@ -885,7 +947,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         uint32_t ph = 0;
         bool ok = true;
         for (int lt = 0; lt < count && ok; ++lt) {
-            for (int kt = 0; kt < k_tiles; ++kt) {
+            int kt0, kt1, slice;
+            sched.krange(lt, kt0, kt1, slice);
+            for (int kt = kt0; kt < kt1; ++kt) {
                 if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)) {
                     ok = false;
                     break;

@@ -153,6 +153,9 @@ struct GemmArgs {
     int* xcnt;              // global exchange only: XCH_CNT0 + 2 * xbank ints
     int32_t xbank;          // ints per counter bank, >= xch_bank_ints(m_tiles)
     float2* xstats;         // global exchange only: >= xch_stats_bytes(m_tiles, n_tiles)
+    int32_t splitk;         // plain GEMM: contraction slices (1 = none); units are tiles x slices
+    float* ws;              // splitk > 1: fp32 partial products, [splitk][M][N]
+    uint16_t* xhat_out;     // RMS backward (optional): bf16(Z * rstd), M x N, the rebuilt rmsnorm input
 };
 
 // Wait sites recorded in the status word on a time-out.
@@ -225,5 +228,10 @@ struct NormBwdArgs {
 cudaError_t launch_norm_rows_bwd(const NormBwdArgs& a, int kind, int sm_count, bool overlap, cudaStream_t stream);
 // Largest supported cols.
 constexpr int NORM_MAX_COLS = 16384;
+
+// Split-K: Y (bf16, `elems` values) = sum over `slices` of the fp32 partial
+// products ws[s][.], added in slice order.  elems % 8 == 0.
+cudaError_t launch_splitk_reduce(const float* ws, int slices, int64_t elems, uint16_t* y, int sm_count, bool overlap,
+                                 cudaStream_t stream);
 
 }  // namespace nf

@@ -23,7 +23,7 @@ def test_exports_every_declared_symbol(L):
     assert "nf_gemm_prenorm_rms" in names and "nf_norm_rows" in names
     for name in names:
         assert hasattr(L, name), f"{name} declared in nf.h but not exported"
-    assert L.nf_abi_version() == 2
+    assert L.nf_abi_version() == 3
 
 
 def test_status_strings(L):
@@ -211,7 +211,55 @@ def test_transposed_and_prenorm_backward_checks(L):
     assert L.nf_gemm_plain_t(P, P, P, 60, 64, 64, 1, None) == ALIGN
     assert L.nf_gemm_plain_t(P, P, P, 0, 64, 64, 1, None) == OK
     # pre-norm backward: null inputs; dB needs M % 8 == 0; dA needs K <= 4096; nothing asked
-    assert L.nf_gemm_prenorm_rms_bwd(P, P, None, P, P, P, 64, 64, 64, None) == INVALID
-    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, None, P, 60, 64, 64, None) == ALIGN
-    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, P, None, 64, 64, 4104, None) == SHAPE
-    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, None, None, 64, 64, 64, None) == OK
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, None, P, P, P, None, 64, 64, 64, None) == INVALID
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, None, P, None, 60, 64, 64, None) == ALIGN
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, P, None, None, 64, 64, 4104, None) == SHAPE
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, None, None, None, 64, 64, 64, None) == OK
+    # the xhat side buffer is written with 16-byte stores
+    assert L.nf_gemm_prenorm_rms_bwd(P, P, P, P, P, P, P + 2, 64, 64, 64, None) == ALIGN
+
+
+def splitk_slices(k_tiles, splitk):
+    """K-tile range of each contraction slice, as the kernel's tile schedule
+    assigns them: slice s covers [s k_tiles / splitk, (s+1) k_tiles / splitk)."""
+    return [(s * k_tiles // splitk, (s + 1) * k_tiles // splitk) for s in range(splitk)]
+
+
+@pytest.mark.parametrize("M,N,K,sms,splitk", [
+    (512, 512, 32768, 152, 19),    # the weight gradient of the Lazy Pre-Norm backward, 32768 x 512 x 512
+    (512, 512, 32768, 148, 18),
+    (128, 64, 4096, 152, 8),       # one tile: slices of 8 K-tiles
+    (4096, 4096, 8192, 152, 1),    # 512 tiles: no split
+    (512, 512, 512, 152, 1),       # 8 K-tiles: no split
+    (9728, 256, 4096, 152, 2),     # 76 tiles = half the SMs, 64 K-tiles: 2 slices
+    (100, 200, 2048, 152, 4),      # one tile, 32 K-tiles: slices of 8
+])
+def test_splitk_plans(L, M, N, K, sms, splitk):
+    p = nf.plan_gemm(0, M, N, K, sms)
+    tiles = p["tiles"]
+    assert p["splitk"] == splitk
+    assert p["grid"] == (tiles * splitk if splitk > 1 else min(tiles, sms))
+    assert p["grid"] <= sms
+    k_tiles = -(-K // 64)
+    if splitk > 1:
+        assert 2 * tiles <= sms
+        sl = splitk_slices(k_tiles, splitk)
+        assert sl[0][0] == 0 and sl[-1][1] == k_tiles
+        assert all(a[1] == b[0] for a, b in zip(sl, sl[1:]))
+        assert all(hi - lo >= 8 for lo, hi in sl)
+        # a split workspace of splitk x M x N fp32 fits the per-stream buffer (SMs x 128 x 256)
+        assert splitk * M * N <= sms * 128 * 256
+    # the normalizing epilogues never split the contraction
+    for op in (1, 2, 3):
+        if N <= 4096:
+            assert nf.plan_gemm(op, M, N, K, sms)["splitk"] == 1
+
+
+def test_splitk_can_be_switched_off(L):
+    try:
+        nf.set_gemm_splitk(1)
+        assert nf.plan_gemm(0, 512, 512, 32768, 152)["splitk"] == 1
+    finally:
+        nf.set_gemm_splitk(0)
+    assert nf.plan_gemm(0, 512, 512, 32768, 152)["splitk"] == 19
+    assert L.nf_set_gemm_splitk(2) == INVALID

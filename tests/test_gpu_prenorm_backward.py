@@ -68,19 +68,35 @@ def _f32(a, dev):
 
 # (M, K, N): ragged K and N, M a multiple of 8 (A is read transposed for dB),
 # several tiles in every direction, K over 1-16 column tiles of dA.
+# The last two have a long contraction for dB over few output tiles, which
+# the library splits over the contraction (16 and 8 slices on 152 SMs).
 SHAPES = [(256, 64, 64), (264, 200, 136), (128, 520, 72), (1000, 136, 264), (512, 1024, 512), (136, 4096, 64),
-          (64, 2056, 8)]
+          (64, 2056, 8), (8192, 64, 64), (4096, 200, 136)]
+
+
+def _assert_xhat(got, A, rstd, what):
+    """The side output xhat = bf16(A * rstd): the fp32 product rounded to
+    bf16 is within 2^-8 of the exact product, relative."""
+    want = nf_inputs.bf16_to_f64(A) * rstd.astype(np.float64)[:, None]
+    err = np.abs(got - want)
+    bad = err > 2.0 ** -8 * np.abs(want)
+    assert not bad.any(), f"{what}: {int(bad.sum())}/{bad.size} off; max err {err.max():.3e}"
 
 
 @pytest.mark.parametrize("M,K,N", SHAPES)
-def test_prenorm_bwd(dev, orc, M, K, N):
+@pytest.mark.parametrize("use_xhat", [True, False], ids=["xhat", "rowscale"])
+def test_prenorm_bwd(dev, orc, M, K, N, use_xhat):
     import torch
     A, B, dC, rstd = _problem(M, K, N, seed=M + K + N)
-    da, db = nf.gemm_prenorm_rms_bwd(to_dev(A, dev), to_dev(B, dev), _f32(rstd, dev), to_dev(dC, dev))
+    xh = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device=dev) if use_xhat else None
+    da, db = nf.gemm_prenorm_rms_bwd(to_dev(A, dev), to_dev(B, dev), _f32(rstd, dev), to_dev(dC, dev), xhat=xh,
+                                     use_xhat=use_xhat)
     torch.cuda.synchronize()
     r64 = rstd.astype(np.float64)
     assert_close(to_f64(da), orc.prenorm_rms_bwd_da(A, B, r64, dC), f"pre-norm bwd dA {M}x{K}x{N}")
     _assert_db(orc, to_f64(db), A, r64, dC, f"pre-norm bwd dB {M}x{K}x{N}")
+    if use_xhat:
+        _assert_xhat(to_f64(xh), A, rstd, f"xhat {M}x{K}x{N}")
 
 
 def test_prenorm_bwd_one_output_only(dev, orc):
@@ -128,10 +144,12 @@ def test_unfused_prenorm_bwd_pair(dev, orc):
 
 @pytest.mark.parametrize("M,K,N", [(32768, 512, 512), (8192, 4096, 4096)],
                          ids=["rowscale_32768x512x512", "llm_8192x4096x4096"])
-def test_prenorm_bwd_full_size(dev, orc, M, K, N):
+@pytest.mark.parametrize("use_xhat", [True, False], ids=["xhat", "rowscale"])
+def test_prenorm_bwd_full_size(dev, orc, M, K, N, use_xhat):
     import torch
     A, B, dC, rstd = _problem(M, K, N, seed=M + N)
-    da, db = nf.gemm_prenorm_rms_bwd(to_dev(A, dev), to_dev(B, dev), _f32(rstd, dev), to_dev(dC, dev))
+    da, db = nf.gemm_prenorm_rms_bwd(to_dev(A, dev), to_dev(B, dev), _f32(rstd, dev), to_dev(dC, dev),
+                                     use_xhat=use_xhat)
     torch.cuda.synchronize()
     assert bool(torch.isfinite(da.float()).all()) and bool(torch.isfinite(db.float()).all())
     r64 = rstd.astype(np.float64)
@@ -139,3 +157,59 @@ def test_prenorm_bwd_full_size(dev, orc, M, K, N):
     assert_close(to_f64(da)[rows], orc.prenorm_rms_bwd_da(A, B, r64, dC, rows=rows), f"dA full {M}x{K}x{N}")
     krows = nf_inputs.sample_rows(K, 24, seed=6)
     _assert_db(orc, to_f64(db)[krows], A, r64, dC, f"dB full {M}x{K}x{N}", krows=krows)
+
+
+# Plain GEMMs with few output tiles over a long contraction: split over the
+# contraction (fp32 partials, a second kernel adds them in a fixed order).
+SPLIT_SHAPES = [(128, 4096, 64), (200, 2056, 136), (512, 32768, 512), (8, 1024, 8)]
+
+
+@pytest.mark.parametrize("M,K,N", SPLIT_SHAPES)
+@pytest.mark.parametrize("flags", [0, nf.TRANS_X, nf.TRANS_W], ids=["plain", "trans_x", "trans_w"])
+def test_plain_splitk(dev, orc, M, K, N, flags):
+    import torch
+    p = nf.plan_gemm(0, M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
+    assert p["splitk"] > 1, "shape chosen to be split"
+    inp = nf_inputs.make_inputs(M, K, N, seed=M + 7 * K + N)
+    X, W = inp["X"], inp["W"]
+    xs = np.ascontiguousarray(X.T) if flags & nf.TRANS_X else X
+    ws = np.ascontiguousarray(W.T) if flags & nf.TRANS_W else W
+    x, w = to_dev(xs, dev), to_dev(ws, dev)
+    y = nf.gemm_plain_t(x, w, flags) if flags else nf.gemm_plain(x, w)
+    y2 = nf.gemm_plain_t(x, w, flags) if flags else nf.gemm_plain(x, w)
+    torch.cuda.synchronize()
+    # the slices are added in a fixed order: the result does not depend on timing
+    assert torch.equal(y, y2)
+    assert_close(to_f64(y), orc.gemm_plain(X, W), f"split-K flags={flags} {M}x{K}x{N}")
+    try:
+        nf.set_gemm_splitk(1)
+        y1 = nf.gemm_plain_t(x, w, flags) if flags else nf.gemm_plain(x, w)
+    finally:
+        nf.set_gemm_splitk(0)
+    torch.cuda.synchronize()
+    assert_close(to_f64(y1), orc.gemm_plain(X, W), f"unsplit flags={flags} {M}x{K}x{N}")
+
+
+def test_splitk_graph_replay(dev, orc):
+    """A split GEMM captured into a CUDA graph (after its first call on the
+    stream set up the workspace) and replayed on new inputs."""
+    import torch
+    M, K, N = 256, 8192, 256
+    s = torch.cuda.Stream()
+    xs, ws, ys = [], [], []
+    with torch.cuda.stream(s):
+        for seed in (1, 2):
+            inp = nf_inputs.make_inputs(M, K, N, seed=seed)
+            xs.append(inp)
+        x = to_dev(xs[0]["X"], dev)
+        w = to_dev(xs[0]["W"], dev)
+        y = nf.gemm_plain(x, w, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            nf.gemm_plain(x, w, out=y, stream=s)
+        x.copy_(to_dev(xs[1]["X"], dev))
+        w.copy_(to_dev(xs[1]["W"], dev))
+        g.replay()
+    s.synchronize()
+    assert_close(to_f64(y), orc.gemm_plain(xs[1]["X"], xs[1]["W"]), "split-K graph replay")
