@@ -241,15 +241,16 @@ const GemmVariant* find_variant(int op, int tile_n, int xch, int ops = 0) {
 // needs at least half as many CTAs as a row has tiles; with fewer the row
 // goes to a cluster instead.
 // The normalization backward (ops 4, 5) follows the same choice with
-// 256-column CTAs only (no 512-column variant): L2 exchange for K >= 512,
-// else a cluster of <= 16.
+// 256-column CTAs only (no 512-column variant): L2 exchange for K >= 512 and
+// N > 512, else a cluster of <= 16 (of 2 for N <= 512, which fits every SM).
 nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, int ops = 0) {
     const bool post = op == OP_POST_LN || op == OP_POST_RMS;
     const bool bwd = op == OP_BWD_LN || op == OP_BWD_RMS;
     p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
     p->xch = XCH_NONE;
     if (bwd && N > 256) {
-        int mode = g_post_xch ? g_post_xch : (K >= 512 ? XCH_GLOBAL : XCH_CLUSTER);
+        // Rows of two tiles: a cluster of 2, which co-resides on every SM.
+        int mode = g_post_xch ? g_post_xch : ((K >= 512 && N > 512) ? XCH_GLOBAL : XCH_CLUSTER);
         if (mode == XCH_GLOBAL) {
             const int64_t nt = (N + 255) / 256, tiles = ((M + TILE_M - 1) / TILE_M) * nt;
             if (2 * (tiles < sms ? tiles : sms) < nt) mode = XCH_CLUSTER;

@@ -60,6 +60,7 @@
 #include "nf_internal.h"
 #include "nf_ptx.cuh"
 
+
 namespace nf {
 
 // Bounded wait used only while draining: ignores the abort flag and records
@@ -557,6 +558,11 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
             const uint32_t jph = static_cast<uint32_t>(lt >> 1) & 1u;  // this group's tile count parity
             bool ok = true;
+            const int nv = min(TILE_N, args.N - n * TILE_N);        // valid columns of this tile
+            const int grow = row0 + row;                             // global row
+            const bool own_row = row < rows && grow < args.M;
+            const uint16_t* const zrow =
+                Cfg::kBwd ? args.zin + static_cast<size_t>(own_row ? grow : 0) * args.N + n * TILE_N : nullptr;
             if (GLOBALX && affine) {
                 // -- this warp's quarter of the group's affine slot (64 columns),
                 //    refilled only when the column tile changes, once the group's
@@ -579,18 +585,13 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_afff0 + 8u * grp);
             }
-            const int nv = min(TILE_N, args.N - n * TILE_N);        // valid columns of this tile
             const int nseg = (nv + SEG - 1) / SEG;                   // segments holding them
             // Store only this unit's rows, and nothing past M.
             const int nstore = (qtr * 32 < rows && row0 + qtr * 32 < args.M) ? nv : 0;
-            const int grow = row0 + row;                             // global row
-            const bool own_row = row < rows && grow < args.M;
             // Backward: the row's saved statistics, requested before the
             // accumulator wait (they do not depend on it).
             const float bmu = (Cfg::kBwdLN && own_row) ? args.mean_in[grow] : 0.0f;
             const float brs = (Cfg::kBwd && own_row) ? args.rstd_in[grow] : 0.0f;
-            const uint16_t* const zrow =
-                Cfg::kBwd ? args.zin + static_cast<size_t>(own_row ? grow : 0) * args.N + n * TILE_N : nullptr;
             ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();

@@ -184,10 +184,12 @@ def test_empty_m_accepts_null_bases(L):
     (4, 16384, 2048, 1024, 256, 1, 2), (5, 8192, 4096, 4096, 256, 1, 2), (4, 130, 2048, 64, 256, 8, 1),
     (5, 64, 4088, 64, 256, 16, 1), (4, 300, 200, 64, 256, 1, 0), (5, 300, 120, 512, 128, 1, 0),
     (4, 65536, 128, 128, 128, 1, 0),
+    # rows of two tiles: a cluster of 2 (co-resident on every SM) whatever K
+    (5, 32768, 512, 512, 256, 2, 1), (4, 1000, 512, 1024, 256, 2, 1), (5, 1000, 520, 4096, 256, 1, 2),
 ])
 def test_backward_plans(L, op, M, N, K, tile_n, cluster, xch):
     """The norm backward (ops 4, 5) takes 256-column CTAs past 256 columns: the
-    L2 exchange for K >= 512, else a cluster of ceil(N / 256) (<= 16)."""
+    L2 exchange for K >= 512 and N > 512, else a cluster of ceil(N / 256) (<= 16)."""
     p = nf.plan_gemm(op, M, N, K, 148)
     assert (p["tile_n"], p["cluster"], p["exchange"], p["tile_k"]) == (tile_n, cluster, xch, 64)
     assert p["threads"] == 320 and p["tmem_cols"] == 2 * tile_n

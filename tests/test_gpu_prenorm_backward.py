@@ -213,3 +213,21 @@ def test_splitk_graph_replay(dev, orc):
         g.replay()
     s.synchronize()
     assert_close(to_f64(y), orc.gemm_plain(xs[1]["X"], xs[1]["W"]), "split-K graph replay")
+
+
+@pytest.mark.parametrize("M,K,N", [(4096, 2688, 8192), (1000, 2688, 8200)])
+def test_every_tile_computed_once(dev, M, K, N):
+    """A GEMM of hundreds of tiles over several waves (ragged in M and N).
+    With one-hot rows of X (row i picks row i mod K of W) every output row is a
+    row of W, exactly: a tile computed twice, never, or at the wrong place
+    shows up bit for bit."""
+    import torch
+    idx = torch.arange(M, device=dev) % K
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device=dev)
+    x[torch.arange(M, device=dev), idx] = 1.0
+    g = torch.Generator(device="cpu").manual_seed(M + N)
+    w = (torch.randn((K, N), generator=g) * 4).to(torch.bfloat16).to(dev)
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    nf.gemm_plain(x, w, out=y)
+    torch.cuda.synchronize()
+    assert torch.equal(y, w[idx])
