@@ -75,6 +75,9 @@ class Oracle:
                                              ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64, _P_F64]
         lib.nfo_gemm_postnorm_rms.argtypes = [_P_U16, _P_U16, _P_U16, _I64, _I64, _I64,
                                               ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64]
+        lib.nfo_gemm_postnorm_res.argtypes = [_P_U16, _P_U16, _P_U16, _P_U16, _P_U16, _I64, _I64, _I64,
+                                              ctypes.c_int, ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64,
+                                              _P_F64, _P_F64]
         lib.nfo_norm_rows.argtypes = [_P_U16, _P_U16, _P_U16, _I64, _I64, ctypes.c_int,
                                       ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64, _P_F64]
         lib.nfo_gemm_postnorm_bwd.argtypes = [_P_U16, _P_U16, _P_U16, _P_U16, _P_F64, _P_F64, _I64,
@@ -88,6 +91,7 @@ class Oracle:
         for f in ("nfo_gemm_plain", "nfo_gemm_prenorm_rms", "nfo_gemm_postnorm_ln",
                   "nfo_gemm_postnorm_rms", "nfo_norm_rows", "nfo_gemm_postnorm_bwd",
                   "nfo_norm_rows_bwd", "nfo_prenorm_rms_bwd_da", "nfo_prenorm_rms_bwd_db",
+                  "nfo_gemm_postnorm_res",
                   "nfo_max_threads"):
             getattr(lib, f).restype = ctypes.c_int
         lib.nfo_set_threads.argtypes = [ctypes.c_int]
@@ -155,6 +159,22 @@ class Oracle:
                                                    rp, R, _f64(Y), _f64(rstd)),
                     "gemm_postnorm_rms")
         return Y, rstd
+
+    def gemm_postnorm_res(self, X, W, Rs, kind, eps, gamma=None, beta=None, rows=None):
+        """H = X @ W + Rs; Y = norm(H) (LN: kind 0, RMS: kind 1).  Returns
+        (Y, H, mean or None, rstd)."""
+        M, K = X.shape
+        N = W.shape[1]
+        assert Rs.shape == (M, N)
+        r, R, rp = self._rows(rows, M)
+        Y = np.empty((R, N), np.float64)
+        H = np.empty((R, N), np.float64)
+        mean = np.full(R, np.nan, np.float64)
+        rstd = np.empty(R, np.float64)
+        self._check(self.lib.nfo_gemm_postnorm_res(_u16(X), _u16(W), _u16(Rs), _u16(gamma), _u16(beta), M, N,
+                                                   K, int(kind), eps, rp, R, _f64(Y), _f64(H), _f64(mean),
+                                                   _f64(rstd)), "gemm_postnorm_res")
+        return Y, H, (mean if kind == NORM_LN else None), rstd
 
     def norm_rows(self, A, kind, eps, gamma=None, beta=None, rows=None):
         Rr, C = A.shape

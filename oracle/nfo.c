@@ -225,6 +225,46 @@ int nfo_gemm_postnorm_rms(const uint16_t* X, const uint16_t* W,
     return bad ? -1 : 0;
 }
 
+int nfo_gemm_postnorm_res(const uint16_t* X, const uint16_t* W,
+                          const uint16_t* Rs, const uint16_t* gamma,
+                          const uint16_t* beta, int64_t M, int64_t N,
+                          int64_t K, int kind, double eps,
+                          const int64_t* rows, int64_t nrows, double* Y,
+                          double* H_out, double* mean_out, double* rstd_out) {
+    if (!X || !W || !Rs || !Y || M < 0 || N <= 0 || K <= 0 || !(eps >= 0.0)) return -1;
+    if (kind != NFO_NORM_LN && kind != NFO_NORM_RMS) return -1;
+    if (check_rows(rows, nrows, M)) return -1;
+    const int64_t R = row_count(rows, nrows, M);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* x = (double*)malloc(sizeof(double) * (size_t)K);
+        double* h = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!x || !h) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            if (!x || !h) continue;
+            const int64_t i = row_index(rows, r);
+            load_row(X, i, K, x);
+            row_times_w(x, W, N, K, h);                        /* X W */
+            const uint16_t* ri = Rs + i * N;
+            for (int64_t j = 0; j < N; ++j) h[j] += bf16_to_double(ri[j]);  /* + residual */
+            if (H_out) memcpy(H_out + r * N, h, sizeof(double) * (size_t)N);
+            if (kind == NFO_NORM_LN)
+                layernorm_row(h, N, gamma, beta, eps, Y + r * N, mean_out ? mean_out + r : NULL,
+                              rstd_out ? rstd_out + r : NULL);
+            else
+                rmsnorm_row(h, N, gamma, eps, Y + r * N, rstd_out ? rstd_out + r : NULL);
+        }
+        free(x);
+        free(h);
+    }
+    return bad ? -1 : 0;
+}
+
 int nfo_norm_rows(const uint16_t* in, const uint16_t* gamma,
                   const uint16_t* beta, int64_t R, int64_t C, int kind,
                   double eps, const int64_t* rows, int64_t nrows, double* out,

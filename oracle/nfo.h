@@ -58,6 +58,20 @@ int nfo_gemm_postnorm_rms(const uint16_t* X, const uint16_t* W,
                           int64_t K, double eps, const int64_t* rows,
                           int64_t nrows, double* Y, double* rstd_out);
 
+/* Residual add before the norm: H = X W + Rs (Rs: M x N, bf16), then
+ * Y = LayerNorm(H) * gamma + beta (kind 0) or RMSNorm(H) * gamma (kind 1),
+ * over N.  H_out (may be NULL) receives H itself, the updated residual stream
+ * that the next layer reads.  Sources: chapter 8 "Element-wise 与算子融合"
+ * of the CUDA book, §8.4 (residual add followed by RMSNorm, the updated
+ * residual written back) and §8.5.1 (the residual add taken into a GEMM's
+ * epilogue); the norm over the GEMM output as blog §3. */
+int nfo_gemm_postnorm_res(const uint16_t* X, const uint16_t* W,
+                          const uint16_t* Rs, const uint16_t* gamma,
+                          const uint16_t* beta, int64_t M, int64_t N,
+                          int64_t K, int kind, double eps,
+                          const int64_t* rows, int64_t nrows, double* Y,
+                          double* H_out, double* mean_out, double* rstd_out);
+
 /* LayerNorm (kind 0) or RMSNorm (kind 1) of each row of `in` (R x C), the
  * unfused normalization kernel of the blog's §1 baseline. beta is ignored for
  * RMSNorm; mean_out is left untouched for RMSNorm. */

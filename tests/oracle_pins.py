@@ -620,12 +620,92 @@ def pin_prenorm_bwd_reductions(o):
     assert np.array_equal(o.prenorm_rms_bwd_db(A, rstd, dC, krows=ksub), full_b[ksub]), "dB row list"
 
 
+# ---------------------------------------------------------------- residual add
+def _res_cases():
+    """(M, K, N, eps, X, W, Rs, gamma, beta): non-square shapes so that a
+    transposed residual cannot pass."""
+    out = []
+    for (M, K, N, eps) in [(37, 72, 40, 1e-5), (19, 24, 136, 1e-6), (8, 8, 264, 1e-5)]:
+        inp = nf_inputs.make_inputs(M, K, N, seed=3 * M + N, gamma=True, beta=True)
+        Rs = nf_inputs.make_inputs(M, N, 8, seed=M + 5 * N)["X"]
+        out.append((M, K, N, eps, inp["X"], inp["W"], Rs, inp["gamma"], inp["beta"]))
+    return out
+
+
+def pin_residual_torch(o):
+    """H = X W + R and its LayerNorm / RMSNorm against torch CPU float64."""
+    import torch
+    import torch.nn.functional as F
+    for (M, K, N, eps, X, W, Rs, G, B) in _res_cases():
+        x, w, r = (torch.from_numpy(bf16_to_f64(a)) for a in (X, W, Rs))
+        g, b = torch.from_numpy(bf16_to_f64(G)), torch.from_numpy(bf16_to_f64(B))
+        h = x @ w + r
+        scale = (x.abs() @ w.abs() + r.abs()).max().item()
+        for gg, bb in ((None, None), (G, B)):
+            tg = g if gg is not None else None
+            tb = b if bb is not None else None
+            Y, H, mean, rstd = o.gemm_postnorm_res(X, W, Rs, 0, eps, gg, bb)
+            assert np.max(np.abs(H - h.numpy())) <= 1e-13 * scale, "residual H vs torch"
+            assert np.max(np.abs(Y - F.layer_norm(h, (N,), tg, tb, eps).numpy())) <= 1e-11, "res LN vs torch"
+            assert np.max(np.abs(mean - h.mean(-1).numpy())) <= 1e-13 * scale, "res LN mean"
+            want_r = torch.rsqrt(h.var(-1, unbiased=False) + eps).numpy()
+            assert np.max(np.abs(rstd - want_r) / want_r) <= 1e-10, "res LN rstd"
+            Y, H, mean, rstd = o.gemm_postnorm_res(X, W, Rs, 1, eps, gg, None)
+            assert mean is None
+            assert np.max(np.abs(Y - F.rms_norm(h, (N,), tg, eps).numpy())) <= 1e-11, "res RMS vs torch"
+            want_r = torch.rsqrt((h * h).mean(-1) + eps).numpy()
+            assert np.max(np.abs(rstd - want_r) / want_r) <= 1e-12, "res RMS rstd"
+
+
+def pin_residual_reductions(o):
+    """W = 0: the result is the row norm of R alone (and H = R); R = 0: the
+    post-norm GEMM; a row list selects rows of X and of R alike; LayerNorm is
+    blind to a constant added to a row of R, which moves H by that constant."""
+    for (M, K, N, eps, X, W, Rs, G, B) in _res_cases():
+        Z0 = bf16_round(np.zeros((K, N)))
+        Y, H, mean, rstd = o.gemm_postnorm_res(X, Z0, Rs, 0, eps, G, B)
+        y2, m2, r2 = o.norm_rows(Rs, 0, eps, G, B)
+        assert np.array_equal(Y, y2) and np.array_equal(mean, m2) and np.array_equal(rstd, r2), \
+            "W = 0: LayerNorm(R)"
+        assert np.array_equal(H, bf16_to_f64(Rs)), "W = 0: H = R"
+        Y, H, _, rstd = o.gemm_postnorm_res(X, Z0, Rs, 1, eps, G)
+        y2, _, r2 = o.norm_rows(Rs, 1, eps, G)
+        assert np.array_equal(Y, y2) and np.array_equal(rstd, r2), "W = 0: RMSNorm(R)"
+        R0 = bf16_round(np.zeros((M, N)))
+        Y, H, mean, rstd = o.gemm_postnorm_res(X, W, R0, 0, eps, G, B)
+        y2, m2, r2 = o.gemm_postnorm_ln(X, W, eps, G, B)
+        assert np.array_equal(Y, y2) and np.array_equal(mean, m2) and np.array_equal(rstd, r2), \
+            "R = 0: post-LN"
+        assert np.array_equal(H, o.gemm_plain(X, W)), "R = 0: H = X W"
+        Y, H, _, rstd = o.gemm_postnorm_res(X, W, R0, 1, eps, G)
+        y2, r2 = o.gemm_postnorm_rms(X, W, eps, G)
+        assert np.array_equal(Y, y2) and np.array_equal(rstd, r2), "R = 0: post-RMS"
+        rows = np.array([M - 1, 0, M // 2, 1], np.int64)
+        for kind in (0, 1):
+            Yf, Hf, _, rf = o.gemm_postnorm_res(X, W, Rs, kind, eps, G, B)
+            Ys, Hs, _, rs = o.gemm_postnorm_res(X, W, Rs, kind, eps, G, B, rows=rows)
+            assert np.array_equal(Ys, Yf[rows]) and np.array_equal(Hs, Hf[rows]) and \
+                np.array_equal(rs, rf[rows]), "row list"
+        # R on a 1/64 grid in [-2, 2] and a small integer c_i added to row i:
+        # both exact in bf16 (at most 9 significant bits).  H moves by c_i and
+        # LayerNorm, blind to a constant shift of its row, does not move.
+        rng = np.random.default_rng(M + N)
+        Rq = bf16_round(rng.integers(-128, 129, size=(M, N)) / 64.0)
+        c = np.arange(M, dtype=np.float64) % 5 - 2.0
+        Rc = bf16_round(bf16_to_f64(Rq) + c[:, None])
+        assert np.array_equal(bf16_to_f64(Rc), bf16_to_f64(Rq) + c[:, None])
+        Y1, H1, _, _ = o.gemm_postnorm_res(X, W, Rq, 0, eps)
+        Y2, H2, _, _ = o.gemm_postnorm_res(X, W, Rc, 0, eps)
+        assert np.allclose(H2 - H1, c[:, None], rtol=0, atol=1e-12), "H moves with R"
+        assert np.max(np.abs(Y2 - Y1)) <= 1e-10, "LN is shift invariant in R"
+
+
 PINS = [pin_bruteforce_plain, pin_bruteforce_prenorm, pin_bruteforce_postnorm,
         pin_bruteforce_norm_rows, pin_torch_f64, pin_lazy_identity, pin_invariants,
         pin_reductions, pin_power_of_two_scale, pin_row_subset, pin_closed_forms,
         pin_bruteforce_norm_bwd, pin_torch_autograd_bwd, pin_norm_bwd_invariants,
         pin_norm_bwd_reductions, pin_prenorm_bwd_bruteforce, pin_prenorm_bwd_autograd,
-        pin_prenorm_bwd_reductions]
+        pin_prenorm_bwd_reductions, pin_residual_torch, pin_residual_reductions]
 
 
 def run_all(o):

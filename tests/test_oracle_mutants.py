@@ -65,6 +65,15 @@ MUTANTS = [
      "for (int64_t n = 0; n < N; ++n) t += dc[n] * bf16_to_double(B[(n % K) * N + k % N]);"),
     ("prebwd_da_wrong_rstd_row", "norm_bwd_row(dxh, a, K, NULL, NFO_NORM_RMS, 0.0, rstd[i],",
      "norm_bwd_row(dxh, a, K, NULL, NFO_NORM_RMS, 0.0, rstd[r],"),
+    ("res_not_added", "for (int64_t j = 0; j < N; ++j) h[j] += bf16_to_double(ri[j]);", ""),
+    ("res_subtracted", "h[j] += bf16_to_double(ri[j]);", "h[j] -= bf16_to_double(ri[j]);"),
+    ("res_dense_row_index", "const uint16_t* ri = Rs + i * N;", "const uint16_t* ri = Rs + r * N;"),
+    ("res_transposed", "h[j] += bf16_to_double(ri[j]);", "h[j] += bf16_to_double(Rs[(j % M) * N + i % N]);"),
+    ("res_h_before_add",
+     "for (int64_t j = 0; j < N; ++j) h[j] += bf16_to_double(ri[j]);  /* + residual */\n            if (H_out) memcpy(H_out + r * N, h, sizeof(double) * (size_t)N);",
+     "if (H_out) memcpy(H_out + r * N, h, sizeof(double) * (size_t)N);\n            for (int64_t j = 0; j < N; ++j) h[j] += bf16_to_double(ri[j]);"),
+    ("res_rms_uses_ln", "rmsnorm_row(h, N, gamma, eps, Y + r * N, rstd_out ? rstd_out + r : NULL);",
+     "layernorm_row(h, N, gamma, NULL, eps, Y + r * N, NULL, rstd_out ? rstd_out + r : NULL);"),
 ]
 
 
