@@ -310,6 +310,55 @@ def measure_workload(nf, w, op, dev, stream, steps, warmup, seed=0, dist=None, s
     return out
 
 
+def measure_residual(nf, w, kind, dev, stream, steps, warmup, seed=0, eager=False, unfused=True):
+    """Residual-add post-norm (H = X W + R, Y = norm(H), H written back) and
+    its unfused pair: the plain GEMM, then the residual-add row norm."""
+    import torch
+    inp = nf_inputs.workload_inputs(w, seed=seed)
+    R0 = _to_dev(nf_inputs.make_inputs(w.M, w.N, 8, seed=seed + 11)["X"], dev)
+    X0, W0 = _to_dev(inp["X"], dev), _to_dev(inp["W"], dev)
+    G = _to_dev(inp["gamma"], dev) if w.gamma else None
+    B = _to_dev(inp["beta"], dev) if (w.beta and kind == 0) else None
+    Y0 = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    H0 = torch.empty_like(Y0)
+    set_bytes = 2 * (X0.numel() + 3 * Y0.numel())
+    sets, nsets = make_sets([X0, R0, Y0, H0], set_bytes, dev)
+
+    def fused(i):
+        x, r, y, h = sets[i % nsets]
+        if kind == 0:
+            nf.gemm_postnorm_ln_res(x, W0, r, w.eps, G, B, out=y, h_out=h, stream=stream)
+        else:
+            nf.gemm_postnorm_rms_res(x, W0, r, w.eps, G, out=y, h_out=h, stream=stream)
+
+    out = {"t_fused": time_steps(fused, steps, warmup, stream, eager=eager) / steps}
+    if not unfused:
+        del sets
+        torch.cuda.empty_cache()
+        return out
+    zs = [torch.empty_like(Y0) for _ in range(nsets)]
+
+    def plain(i):
+        nf.gemm_plain(sets[i % nsets][0], W0, out=zs[i % nsets], stream=stream)
+
+    def norm(i):
+        x, r, y, h = sets[i % nsets]
+        nf.norm_rows_res(zs[i % nsets], r, kind, w.eps, G, B, out=y, h_out=h, stream=stream)
+
+    ksteps = max(1, min(steps, 2000))
+    out["t_plain"] = time_steps(plain, ksteps, min(warmup, 10), stream) / ksteps
+    out["t_norm"] = time_steps(norm, ksteps, min(warmup, 10), stream) / ksteps
+    del sets, zs
+    torch.cuda.empty_cache()
+    return out
+
+
+def residual_bytes(w, kind):
+    """Each tensor moved once: X, W and R read, Y and H written (+ gamma, beta)."""
+    return (2 * w.M * w.K + 2 * w.K * w.N + 6 * w.M * w.N + (2 * w.N if w.gamma else 0)
+            + (2 * w.N if (w.beta and kind == 0) else 0))
+
+
 def backward_inputs(w, seed=0):
     """Inputs of the normalization backward on workload w's shapes: A = X
     (M x K, the incoming gradient dOut), B = W (K x N, standing in for the next
@@ -545,6 +594,9 @@ def main(argv=None):
     ap.add_argument("--backward", choices=["post_ln", "post_rms", "pre_rms"], default=None,
                     help="time only this op's backward on the workload's shapes and print its figures "
                          "(a profiling aid; not the benchmark line)")
+    ap.add_argument("--residual", choices=["post_ln", "post_rms"], default=None,
+                    help="time only this op with a residual add on the workload's shapes and print its "
+                         "figures (a profiling aid; not the benchmark line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -578,6 +630,13 @@ def main(argv=None):
             r = measure_backward(nf, w, 0 if args.backward == "post_ln" else 1, dev, stream, args.steps,
                                  args.warmup, eager=args.eager, unfused=not args.no_unfused)
         print(json.dumps({"backward": args.backward, "workload": w.name,
+                          **{k: v * 1e6 for k, v in r.items() if k.startswith("t_")}}), flush=True)
+        return 0
+    if args.residual:
+        w = nf_inputs.WORKLOADS[args.workload]
+        r = measure_residual(nf, w, 0 if args.residual == "post_ln" else 1, dev, stream, args.steps,
+                             args.warmup, eager=args.eager, unfused=not args.no_unfused)
+        print(json.dumps({"residual": args.residual, "workload": w.name,
                           **{k: v * 1e6 for k, v in r.items() if k.startswith("t_")}}), flush=True)
         return 0
 
@@ -702,6 +761,28 @@ def main(argv=None):
                         "hbm_gbs": nb / r["t_fused"] / 1e9,
                         "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
                         "norm_gbs": 6 * cw.M * cw.N / r["t_norm"] / 1e9,
+                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
+                    })
+                    del r
+                    torch.cuda.empty_cache()
+                # the residual add before the post-norm (H = X W + R, Y = norm(H),
+                # H written back); unfused: plain GEMM + residual-add row norm
+                for cop in cw.ops:
+                    if cop not in ("post_ln", "post_rms"):
+                        continue
+                    kind = 0 if cop == "post_ln" else 1
+                    steps = 200 if cw.flops > 5e10 else 1000
+                    r = measure_residual(nf, cw, kind, dev, stream, steps, 10)
+                    nb = residual_bytes(cw, kind)
+                    tr = max(cw.flops / (bf16_tf * 1e12), nb / (hbm_gbs * 1e9))
+                    table.append({
+                        "workload": name, "op": cop + "_res", "t_fused_us": r["t_fused"] * 1e6,
+                        "tflops": cw.flops / r["t_fused"] / 1e12,
+                        "roofline_frac": tr / r["t_fused"],
+                        "bound": "tensor" if cw.flops / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
+                        "hbm_gbs": nb / r["t_fused"] / 1e9,
+                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
+                        "norm_gbs": 8 * cw.M * cw.N / r["t_norm"] / 1e9,
                         "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
                     })
                     del r

@@ -119,6 +119,35 @@ nf_status nf_gemm_prenorm_rms(const void* X, const void* W, void* Y,
                               float* rstd_out, nf_stream stream);
 
 /*
+ * nf_gemm_postnorm_ln_res / nf_gemm_postnorm_rms_res -- residual add before
+ * the post-norm, in the same epilogue:
+ *   H = X W + R                       (fp32 accumulator plus R)
+ *   Y = LayerNorm(H) * gamma + beta   (RMS: RMSNorm(H) * gamma)
+ * The pattern of a transformer block's residual stream: the CUDA book chapter
+ * "Element-wise 与算子融合", §8.4 (residual add followed by RMSNorm in one
+ * kernel, the updated residual written back for the next layer) and §8.5.1
+ * (the residual add taken into a GEMM's epilogue); the norm over the GEMM
+ * output as blog §3.
+ * R: M x N bf16 row-major device memory, 16-byte aligned, read once by the
+ * kernel that owns each row segment.  H: optional (NULL) M x N bf16, 16-byte
+ * aligned: bf16(H), the updated residual; H may be R itself (each element of
+ * R is read before the same thread overwrites it).  Y must not overlap X, W,
+ * R or H.  The statistics (mean_out, rstd_out) are those of H.  Same shapes,
+ * alignment rules, exchanges and errors as nf_gemm_postnorm_ln, except that
+ * the 512-column cluster kernel is not used (rows of 257..512 columns take a
+ * cluster of two 256-column CTAs).
+ */
+nf_status nf_gemm_postnorm_ln_res(const void* X, const void* W, const void* R,
+                                  const void* gamma, const void* beta, void* Y,
+                                  void* H, int64_t M, int64_t N, int64_t K,
+                                  float eps, float* mean_out, float* rstd_out,
+                                  nf_stream stream);
+nf_status nf_gemm_postnorm_rms_res(const void* X, const void* W, const void* R,
+                                   const void* gamma, void* Y, void* H,
+                                   int64_t M, int64_t N, int64_t K, float eps,
+                                   float* rstd_out, nf_stream stream);
+
+/*
  * nf_gemm_prenorm_rms_bwd -- backward of C = RMSNorm(A) * B (Lazy Pre-Norm,
  * no affine), from the rstd the forward saved (blog §2, limitation 3: the
  * backward rebuilds rmsnorm(A) from A and rstd).  With xhat = A * rstd_i:
@@ -205,6 +234,15 @@ nf_status nf_norm_rows(const void* in, void* out, const void* gamma,
                        const void* beta, int64_t rows, int64_t cols, int kind,
                        float eps, float* mean_out, float* rstd_out,
                        nf_stream stream);
+
+/* nf_norm_rows_res -- the unfused residual-add norm (CUDA book chapter
+ * "Element-wise 与算子融合" §8.4): H = in + R, out = norm(H) as nf_norm_rows,
+ * H (optional, may be R itself) = bf16(H).  R and H: rows x cols bf16,
+ * 16-byte aligned; R non-null when rows > 0. */
+nf_status nf_norm_rows_res(const void* in, const void* R, void* out, void* H,
+                           const void* gamma, const void* beta, int64_t rows,
+                           int64_t cols, int kind, float eps, float* mean_out,
+                           float* rstd_out, nf_stream stream);
 
 /*
  * nf_gemm_postnorm_ln_bwd -- dZ = LayerNorm backward of dY = A * B, the

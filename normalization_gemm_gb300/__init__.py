@@ -68,6 +68,9 @@ _SIGS = {
     "nf_gemm_postnorm_ln": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
     "nf_gemm_postnorm_ln_noalloc": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
     "nf_gemm_postnorm_rms": [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
+    "nf_gemm_postnorm_ln_res": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
+    "nf_gemm_postnorm_rms_res": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
+    "nf_norm_rows_res": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
     "nf_norm_rows": [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
     "nf_norm_rows_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP],
     "nf_gemm_plain_t": [_VP, _VP, _VP, _I64, _I64, _I64, ctypes.c_int, _VP],
@@ -287,6 +290,59 @@ def gemm_postnorm_rms(x, w, eps, gamma=None, out=None, rstd_out=None, stream=Non
                                       M, N, K, float(eps),
                                       _vec(rstd_out, "rstd_out", M, torch.float32),
                                       _stream(stream)), "nf_gemm_postnorm_rms")
+    return y
+
+
+def _res(r, M, N, name="r"):
+    if tuple(r.shape) != (M, N):
+        raise ValueError(f"{name} must have shape {(M, N)}")
+    return _mat(r, name)
+
+
+def gemm_postnorm_ln_res(x, w, r, eps, gamma=None, beta=None, out=None, h_out=None, mean_out=None,
+                         rstd_out=None, stream=None):
+    """H = X @ W + R; Y = LayerNorm(H) * gamma + beta over N.  h_out (optional,
+    may be r itself): bf16(H), the updated residual.  Returns Y."""
+    torch = _torch()
+    M, N, K = _shapes(x, w)
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_postnorm_ln_res(_mat(x, "x"), _mat(w, "w"), _res(r, M, N),
+                                         _vec(gamma, "gamma", N, torch.bfloat16),
+                                         _vec(beta, "beta", N, torch.bfloat16), _mat(y, "out"),
+                                         None if h_out is None else _res(h_out, M, N, "h_out"), M, N, K,
+                                         float(eps), _vec(mean_out, "mean_out", M, torch.float32),
+                                         _vec(rstd_out, "rstd_out", M, torch.float32), _stream(stream)),
+           "nf_gemm_postnorm_ln_res")
+    return y
+
+
+def gemm_postnorm_rms_res(x, w, r, eps, gamma=None, out=None, h_out=None, rstd_out=None, stream=None):
+    """H = X @ W + R; Y = RMSNorm(H) * gamma over N.  h_out as gemm_postnorm_ln_res."""
+    torch = _torch()
+    M, N, K = _shapes(x, w)
+    y = _out(out, M, N, x)
+    _check(lib().nf_gemm_postnorm_rms_res(_mat(x, "x"), _mat(w, "w"), _res(r, M, N),
+                                          _vec(gamma, "gamma", N, torch.bfloat16), _mat(y, "out"),
+                                          None if h_out is None else _res(h_out, M, N, "h_out"), M, N, K,
+                                          float(eps), _vec(rstd_out, "rstd_out", M, torch.float32),
+                                          _stream(stream)), "nf_gemm_postnorm_rms_res")
+    return y
+
+
+def norm_rows_res(x, r, kind, eps, gamma=None, beta=None, out=None, h_out=None, mean_out=None,
+                  rstd_out=None, stream=None):
+    """The unfused residual-add norm: H = x + r, out = norm(H) (kind 0 LN, 1 RMS);
+    h_out (optional, may be r): bf16(H)."""
+    torch = _torch()
+    R = x.shape[0] if x.dim() == 2 else -1
+    C = x.shape[1] if x.dim() == 2 else -1
+    y = _out(out, R, C, x)
+    _check(lib().nf_norm_rows_res(_mat(x, "x"), _res(r, R, C), _mat(y, "out"),
+                                  None if h_out is None else _res(h_out, R, C, "h_out"),
+                                  _vec(gamma, "gamma", C, torch.bfloat16), _vec(beta, "beta", C, torch.bfloat16),
+                                  R, C, int(kind), float(eps), _vec(mean_out, "mean_out", R, torch.float32),
+                                  _vec(rstd_out, "rstd_out", R, torch.float32), _stream(stream)),
+           "nf_norm_rows_res")
     return y
 
 

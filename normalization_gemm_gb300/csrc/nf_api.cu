@@ -210,6 +210,8 @@ const GemmVariant* find_variant(int op, int tile_n, int xch, int ops = 0) {
     if (ops != 0) {
         if (op == OP_PLAIN) t = gemm_variants_trans_plain(&n);
         else if (op == OP_BWD_RMS) t = gemm_variants_trans_bwd(&n);
+        else if (op == OP_POST_LN && ops == OPS_RESID) t = gemm_variants_res_ln(&n);
+        else if (op == OP_POST_RMS && ops == OPS_RESID) t = gemm_variants_res_rms(&n);
         else return nullptr;
     } else switch (op) {
         case OP_PLAIN: t = gemm_variants_plain(&n); break;
@@ -240,10 +242,12 @@ const GemmVariant* find_variant(int op, int tile_n, int xch, int ops = 0) {
 // `sms`: SMs of the device.  The global exchange runs one CTA per SM and
 // needs at least half as many CTAs as a row has tiles; with fewer the row
 // goes to a cluster instead.
+// A residual add (post-norm) takes the 256-column kernels only.
 // The normalization backward (ops 4, 5) follows the same choice with
 // 256-column CTAs only (no 512-column variant): L2 exchange for K >= 512 and
 // N > 512, else a cluster of <= 16 (of 2 for N <= 512, which fits every SM).
 nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, int ops = 0) {
+    const bool resid = (ops & OPS_RESID) != 0;
     const bool post = op == OP_POST_LN || op == OP_POST_RMS;
     const bool bwd = op == OP_BWD_LN || op == OP_BWD_RMS;
     p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
@@ -274,7 +278,7 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
         }
         p->xch = mode;
         if (mode == XCH_CLUSTER) {
-            p->tile_n = tile == 256 ? 256 : 512;
+            p->tile_n = (tile == 256 || resid) ? 256 : 512;  // the 512-column kernel adds no residual
             if (N > static_cast<int64_t>(p->tile_n) * (p->tile_n == 512 ? 8 : 16))
                 return fail(NF_ERR_UNSUPPORTED_SHAPE, "N too large for the cluster");
             if (N <= p->tile_n) p->xch = XCH_NONE;  // one wide CTA covers the row
@@ -553,10 +557,16 @@ nf_status noalloc_scratch(uint8_t** out) {
 nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, const void* beta, void* Y, int64_t M,
                    int64_t N, int64_t K, float eps, float* mean_out, float* rstd_out, cudaStream_t stream,
                    bool fixed_scratch = false, const void* zin = nullptr, const float* mean_in = nullptr,
-                   const float* rstd_in = nullptr, int ops = 0, void* xhat_out = nullptr) {
+                   const float* rstd_in = nullptr, int ops = 0, void* xhat_out = nullptr,
+                   const void* resid = nullptr, void* h_out = nullptr) {
     nf_status st = check_gemm_args(op, X, W, Y, gamma, beta, mean_out, rstd_out, M, N, K, eps);
     if (st != NF_OK) return st;
+    if (h_out && !resid) return fail(NF_ERR_INVALID_ARG, "the residual output needs a residual");
+    if (resid && op != OP_POST_LN && op != OP_POST_RMS)
+        return fail(NF_ERR_INVALID_ARG, "a residual is added by the post-norm epilogues only");
     if (M == 0) return NF_OK;
+    if ((resid && !aligned(resid, 16)) || (h_out && !aligned(h_out, 16)))
+        return fail(NF_ERR_ALIGNMENT, "R and H must be 16-byte aligned");
     if ((ops & OPS_A_MN) && M % 8 != 0)
         return fail(NF_ERR_ALIGNMENT, "a transposed X (K x M) needs M a multiple of 8 (16-byte rows)");
     if ((ops & OPS_A_SCALE) && !rstd_in) return fail(NF_ERR_INVALID_ARG, "row scaling needs rstd");
@@ -573,6 +583,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     DeviceState* d = nullptr;
     if ((st = device_state(&d)) != NF_OK) return st;
     Plan p;
+    if (resid) ops |= OPS_RESID;
     if ((st = plan_tiles(op, M, N, K, d->sm_count, &p, ops)) != NF_OK) return st;
     if ((st = prepare_kernel(d, p.v)) != NF_OK) return st;
 
@@ -616,6 +627,8 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.splitk = p.splitk;
     a.ws = nullptr;
     a.xhat_out = (op == OP_BWD_LN || op == OP_BWD_RMS) ? static_cast<uint16_t*>(xhat_out) : nullptr;
+    a.resid = static_cast<const uint16_t*>(resid);
+    a.h_out = static_cast<uint16_t*>(h_out);
 
     int grid = 0;
     a.units = p.m_tiles * p.n_tiles;
@@ -789,14 +802,34 @@ nf_status nf_gemm_prenorm_rms_bwd(const void* A, const void* B, const float* rst
     return NF_OK;
 }
 
+nf_status nf_gemm_postnorm_ln_res(const void* X, const void* W, const void* R, const void* gamma, const void* beta,
+                                  void* Y, void* H, int64_t M, int64_t N, int64_t K, float eps, float* mean_out,
+                                  float* rstd_out, nf_stream stream) {
+    if (M > 0 && !R) return fail(NF_ERR_INVALID_ARG, "R must be non-null");
+    return run_gemm(OP_POST_LN, X, W, gamma, beta, Y, M, N, K, eps, mean_out, rstd_out,
+                    reinterpret_cast<cudaStream_t>(stream), false, nullptr, nullptr, nullptr, 0, nullptr, R, H);
+}
+
+nf_status nf_gemm_postnorm_rms_res(const void* X, const void* W, const void* R, const void* gamma, void* Y, void* H,
+                                   int64_t M, int64_t N, int64_t K, float eps, float* rstd_out, nf_stream stream) {
+    if (M > 0 && !R) return fail(NF_ERR_INVALID_ARG, "R must be non-null");
+    return run_gemm(OP_POST_RMS, X, W, gamma, nullptr, Y, M, N, K, eps, nullptr, rstd_out,
+                    reinterpret_cast<cudaStream_t>(stream), false, nullptr, nullptr, nullptr, 0, nullptr, R, H);
+}
+
 nf_status nf_gemm_postnorm_rms(const void* X, const void* W, const void* gamma, void* Y, int64_t M, int64_t N,
                                int64_t K, float eps, float* rstd_out, nf_stream stream) {
     return run_gemm(OP_POST_RMS, X, W, gamma, nullptr, Y, M, N, K, eps, nullptr, rstd_out,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
-nf_status nf_norm_rows(const void* in, void* out, const void* gamma, const void* beta, int64_t rows, int64_t cols,
-                       int kind, float eps, float* mean_out, float* rstd_out, nf_stream stream) {
+}  // extern "C"
+
+namespace nf {
+namespace {
+nf_status norm_rows_impl(const void* in, const void* res, void* out, void* h_out, const void* gamma,
+                         const void* beta, int64_t rows, int64_t cols, int kind, float eps, float* mean_out,
+                         float* rstd_out, nf_stream stream) {
     if (kind != NF_NORM_LN && kind != NF_NORM_RMS) return fail(NF_ERR_INVALID_ARG, "kind must be LN or RMS");
     if (rows < 0 || cols < 1) return fail(NF_ERR_INVALID_ARG, "need rows >= 0 and cols >= 1");
     if (rows == 0) {  // empty tensors may have a null base: nothing is accessed
@@ -813,11 +846,16 @@ nf_status nf_norm_rows(const void* in, void* out, const void* gamma, const void*
         return fail(NF_ERR_ALIGNMENT, "gamma and beta must be 16-byte aligned for nf_norm_rows");
     if ((mean_out && !aligned(mean_out, 4)) || (rstd_out && !aligned(rstd_out, 4)))
         return fail(NF_ERR_ALIGNMENT, "mean_out and rstd_out must be 4-byte aligned");
+    if (h_out && !res) return fail(NF_ERR_INVALID_ARG, "the residual output needs a residual");
+    if (rows > 0 && ((res && !aligned(res, 16)) || (h_out && !aligned(h_out, 16))))
+        return fail(NF_ERR_ALIGNMENT, "the residual and its output must be 16-byte aligned");
     if (rows == 0) return NF_OK;
     DeviceState* d = nullptr;
     nf_status st = device_state(&d);
     if (st != NF_OK) return st;
     NormArgs a;
+    a.res = res;
+    a.h_out = h_out;
     a.in = in;
     a.out = out;
     a.gamma = static_cast<const uint16_t*>(gamma);
@@ -831,6 +869,22 @@ nf_status nf_norm_rows(const void* in, void* out, const void* gamma, const void*
     cudaError_t e = launch_norm_rows(a, kind, d->sm_count, g_overlap, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "norm_rows launch");
     return NF_OK;
+}
+}  // namespace
+}  // namespace nf
+
+extern "C" {
+
+nf_status nf_norm_rows(const void* in, void* out, const void* gamma, const void* beta, int64_t rows, int64_t cols,
+                       int kind, float eps, float* mean_out, float* rstd_out, nf_stream stream) {
+    return norm_rows_impl(in, nullptr, out, nullptr, gamma, beta, rows, cols, kind, eps, mean_out, rstd_out, stream);
+}
+
+nf_status nf_norm_rows_res(const void* in, const void* R, void* out, void* H, const void* gamma, const void* beta,
+                           int64_t rows, int64_t cols, int kind, float eps, float* mean_out, float* rstd_out,
+                           nf_stream stream) {
+    if (rows > 0 && !R) return fail(NF_ERR_INVALID_ARG, "R must be non-null");
+    return norm_rows_impl(in, R, out, H, gamma, beta, rows, cols, kind, eps, mean_out, rstd_out, stream);
 }
 
 nf_status nf_norm_rows_bwd(const void* dY, const void* Z, const void* gamma, const float* mean, const float* rstd,

@@ -171,11 +171,77 @@ __device__ __forceinline__ void convert64_bwd(const uint32_t (&va)[32], const ui
 }
 
 // 64 bf16 of a row of Z starting at p (16-byte aligned); 8-column groups at or
-// past `valid` read as zero (N is a multiple of 8).
+// past `valid` read as zero (N is a multiple of 8).  One thread per row: the
+// loads of a segment can be issued ahead of the TMEM reads they pair with.
 __device__ __forceinline__ void load_z64(const uint16_t* p, bool own, int valid, uint4 (&zq)[8]) {
 #pragma unroll
     for (int q = 0; q < 8; ++q)
         zq[q] = (own && q * 8 < valid) ? __ldg(reinterpret_cast<const uint4*>(p + q * 8)) : make_uint4(0, 0, 0, 0);
+}
+
+// A warp's 32 x 64 bf16 block through its 4 KB staging buffer (128-byte
+// rows, 16-byte chunk e of row r at r * 128 + ((e ^ (r & 7)) << 4), the
+// layout of the output staging).  Global memory is touched coalesced: lane l
+// moves chunk l & 7 of rows (l >> 3) + 4 i, i.e. 4 full 128-byte lines per
+// instruction, instead of one thread per row (32 lines per instruction).
+// Rows at or past `nrows` and 8-column groups at or past `valid` read as
+// zero and are not written.  Loads go through L2 (not the read-only path):
+// the residual output may overwrite the residual in place, each block after
+// it was read here.
+__device__ __forceinline__ void stage_in64(uint32_t buf, const uint16_t* p, int64_t ld, int nrows, int valid,
+                                           int lane) {
+    const int c = lane & 7;
+    uint4 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (lane >> 3) + 4 * i;
+        q[i] = (r < nrows && c * 8 < valid) ? __ldcg(reinterpret_cast<const uint4*>(p + r * ld + c * 8))
+                                            : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (lane >> 3) + 4 * i;
+        st_shared_v4(buf + static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)), q[i].x, q[i].y, q[i].z, q[i].w);
+    }
+}
+
+__device__ __forceinline__ void stage_out64(uint32_t buf, uint16_t* p, int64_t ld, int nrows, int valid, int lane) {
+    const int c = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (lane >> 3) + 4 * i;
+        const uint4 q = ld_shared_v4(buf + static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)));
+        if (r < nrows && c * 8 < valid) *reinterpret_cast<uint4*>(p + r * ld + c * 8) = q;
+    }
+}
+
+// v (64 fp32 columns of this lane's row, two 32-column chunks) += the row's 64
+// bf16 in the staging buffer.
+__device__ __forceinline__ void add_staged_row(uint32_t buf, int lane, uint32_t (&v)[2][32]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint4 rq = ld_shared_v4(buf + static_cast<uint32_t>(lane * 128 + ((e ^ (lane & 7)) << 4)));
+        const uint32_t rw[4] = {rq.x, rq.y, rq.z, rq.w};
+        uint32_t* d = &v[e >> 2][(e & 3) * 8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            d[2 * k] = __float_as_uint(__uint_as_float(d[2 * k]) + bf16lo(rw[k]));
+            d[2 * k + 1] = __float_as_uint(__uint_as_float(d[2 * k + 1]) + bf16hi(rw[k]));
+        }
+    }
+}
+
+// The row's 64 fp32 columns -> bf16 into the staging buffer (same layout).
+__device__ __forceinline__ void put_staged_row(uint32_t buf, int lane, const uint32_t (&v)[2][32]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t* s = &v[e >> 2][(e & 3) * 8];
+        st_shared_v4(buf + static_cast<uint32_t>(lane * 128 + ((e ^ (lane & 7)) << 4)),
+                     pack_bf16x2(__uint_as_float(s[0]), __uint_as_float(s[1])),
+                     pack_bf16x2(__uint_as_float(s[2]), __uint_as_float(s[3])),
+                     pack_bf16x2(__uint_as_float(s[4]), __uint_as_float(s[5])),
+                     pack_bf16x2(__uint_as_float(s[6]), __uint_as_float(s[7])));
+    }
 }
 
 // Tile schedule: CTA-local work unit lt -> (m_tile, n_tile, first row, rows).
@@ -535,8 +601,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         constexpr int SEG = TILE_N < 64 ? TILE_N : 64;
         // Post-norm keeps the row's last segment in registers across the
         // statistics exchange, except the global exchange, whose partials of up
-        // to 16 column tiles need those registers: it reads the segment again.
-        constexpr bool KEEP_SEG = Cfg::kPost && !GLOBALX;  // (the backward needs them for Z)
+        // to 16 column tiles need those registers, and the residual add, whose
+        // staging of R does: those read the segment (X W + R) again from TMEM.
+        constexpr bool KEEP_SEG = Cfg::kPost && !GLOBALX && !Cfg::kRes;  // (the backward needs them for Z)
         // The global exchange's release fence (lane 0) should not wait for
         // this warp's bulk stores: another lane issues them.
         constexpr int STORE_LANE = GLOBALX ? 31 : 0;
@@ -563,6 +630,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             const bool own_row = row < rows && grow < args.M;
             const uint16_t* const zrow =
                 Cfg::kBwd ? args.zin + static_cast<size_t>(own_row ? grow : 0) * args.N + n * TILE_N : nullptr;
+            // This warp's 32-row block of the tile (wrows valid rows from wr0):
+            // the residual R is read, and the residual output written, block by
+            // block through the warp's staging buffer (coalesced 128-byte lines).
+            const int wr0 = row0 + qtr * 32;
+            const int wrows = max(0, min(32, min(rows - qtr * 32, args.M - wr0)));
+            const size_t woff = static_cast<size_t>(wrows > 0 ? wr0 : 0) * args.N + n * TILE_N;
+            const uint32_t wbuf = sStg + static_cast<uint32_t>(warp * STORE_BUF_BYTES);
+            // Post-norm residual add: R's row in this tile is asked of L2 before
+            // the accumulator wait; it is read once, in the statistics loop,
+            // which writes X W + R back into TMEM.
+            constexpr bool res = Cfg::kRes;
+            if (res && own_row)  // nv * 2 bytes: N % 8 == 0 keeps it a multiple of 16
+                bulk_prefetch_l2(args.resid + woff + static_cast<size_t>(row - qtr * 32) * args.N,
+                                 static_cast<uint32_t>(nv * 2));
             if (GLOBALX && affine) {
                 // -- this warp's quarter of the group's affine slot (64 columns),
                 //    refilled only when the column tile changes, once the group's
@@ -701,6 +782,25 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 uint64_t a1[4] = {0, 0, 0, 0}, a2[4] = {0, 0, 0, 0};
                 for (int sg = 0; sg < nseg; ++sg) {
                     tmem_load_seg<NC>(tacc + sg * SEG, v);
+                    if (res) {
+                        // R's block through the staging buffer (free once the last
+                        // output store read it), added to the row; X W + R back
+                        // into TMEM; H out the same way.
+                        if (lane == STORE_LANE) bulk_wait_read<0>();
+                        __syncwarp();
+                        stage_in64(wbuf, args.resid + woff + sg * SEG, args.N, wrows, nv - sg * SEG, lane);
+                        __syncwarp();
+                        add_staged_row(wbuf, lane, v);
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) tmem_st32(tacc + sg * SEG + c * 32, v[c]);
+                        if (args.h_out != nullptr) {
+                            __syncwarp();  // every lane has read its row of R
+                            put_staged_row(wbuf, lane, v);
+                            __syncwarp();
+                            stage_out64(wbuf, args.h_out + woff + sg * SEG, args.N, wrows, nv - sg * SEG, lane);
+                        }
+                        __syncwarp();  // the buffer is read out before it is reused
+                    }
                     if (Cfg::kLN && sg == 0) sh = __uint_as_float(v[0][0]);
                     const uint64_t sh2 = f2_splat(sh);
 #pragma unroll
@@ -717,6 +817,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                             }
                         }
                 }
+                if (res) tmem_st_wait();  // the finish loop reads X W + R back
                 if (KEEP_SEG && nseg == 1) {  // the row is in registers: TMEM buffer b is free
                     tc_fence_before();
                     mbar_arrive(bar_acce0 + 8u * b);
@@ -878,17 +979,16 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                                 if (args.xhat_out != nullptr && own_row) {
                                     // Side output: the normalized forward input
                                     // xhat = (z - mean) * rstd, rounded to bf16.
-                                    uint16_t* const xp =
-                                        args.xhat_out + static_cast<size_t>(grow) * args.N + n * TILE_N + c0;
+                                    uint16_t* const xp = args.xhat_out + static_cast<size_t>(grow) * args.N + n * TILE_N + c0;
 #pragma unroll
-                                    for (int q = 0; q < 8; ++q)
-                                        if (q * 8 < nv - c0) {
-                                            const uint32_t zw[4] = {zq[q].x, zq[q].y, zq[q].z, zq[q].w};
+                                    for (int e = 0; e < 8; ++e)
+                                        if (e * 8 < nv - c0) {
+                                            const uint32_t zw[4] = {zq[e].x, zq[e].y, zq[e].z, zq[e].w};
                                             uint32_t o[4];
 #pragma unroll
-                                            for (int e = 0; e < 4; ++e)
-                                                o[e] = pack_bf16x2((bf16lo(zw[e]) - bmu) * brs, (bf16hi(zw[e]) - bmu) * brs);
-                                            *reinterpret_cast<uint4*>(xp + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+                                            for (int k = 0; k < 4; ++k)
+                                                o[k] = pack_bf16x2((bf16lo(zw[k]) - bmu) * brs, (bf16hi(zw[k]) - bmu) * brs);
+                                            *reinterpret_cast<uint4*>(xp + e * 8) = make_uint4(o[0], o[1], o[2], o[3]);
                                         }
                                 }
                                 if (affine && args.gamma)

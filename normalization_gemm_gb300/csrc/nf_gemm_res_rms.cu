@@ -1,0 +1,16 @@
+// nf_gemm_res_rms.cu -- instantiations of the post-norm RMSNorm GEMM kernel
+// with the residual add (H = X W + R before the statistics).
+#include "nf_gemm_kernel.cuh"
+
+namespace nf {
+
+const GemmVariant* gemm_variants_res_rms(int* count) {
+    static const GemmVariant v[] = {
+        make_variant<EPI_POST_RMS, 64, XCH_NONE, OPS_RESID>(), make_variant<EPI_POST_RMS, 128, XCH_NONE, OPS_RESID>(),
+        make_variant<EPI_POST_RMS, 256, XCH_NONE, OPS_RESID>(), make_variant<EPI_POST_RMS, 256, XCH_CLUSTER, OPS_RESID>(),
+        make_variant<EPI_POST_RMS, 256, XCH_GLOBAL, OPS_RESID>()};
+    *count = 5;
+    return v;
+}
+
+}  // namespace nf

@@ -67,6 +67,7 @@ enum OperandFlags : int {
     OPS_A_SCALE = 2,  // with OPS_A_MN: each contraction row m of A scaled by rstd[m] in shared
                       // memory before the MMA (rmsnorm of the stored matrix rebuilt on the fly)
     OPS_B_K = 4,      // B given as its transpose: W stored N x K row-major (Y = X W^T)
+    OPS_RESID = 8,    // post-norm: a residual R (M x N) added to X W before the statistics
 };
 
 template <int EPI, int TILE_N, int XCH, int OPS = 0>
@@ -81,6 +82,8 @@ struct GemmCfg {
     static constexpr bool kAMN = (OPS & OPS_A_MN) != 0;
     static constexpr bool kScaleA = (OPS & OPS_A_SCALE) != 0;
     static constexpr bool kBK = (OPS & OPS_B_K) != 0;
+    static constexpr bool kRes = (OPS & OPS_RESID) != 0;
+    static_assert(!kRes || kPost, "the residual add belongs to the post-norm epilogues");
     static_assert(!kScaleA || (kAMN && EPI == EPI_PLAIN), "row scaling applies to a transposed A, plain epilogue");
     static_assert(TILE_N == 64 || TILE_N == 128 || TILE_N == 256, "tile_n");
     static_assert(XCH == XCH_NONE || (kRow && TILE_N == 256), "row exchange only for post-norm");
@@ -156,6 +159,8 @@ struct GemmArgs {
     int32_t splitk;         // plain GEMM: contraction slices (1 = none); units are tiles x slices
     float* ws;              // splitk > 1: fp32 partial products, [splitk][M][N]
     uint16_t* xhat_out;     // RMS backward (optional): bf16(Z * rstd), M x N, the rebuilt rmsnorm input
+    const uint16_t* resid;  // post-norm (optional): R, M x N bf16, added to X W before the statistics
+    uint16_t* h_out;        // with resid (optional): bf16(X W + R), M x N, the updated residual stream
 };
 
 // Wait sites recorded in the status word on a time-out.
@@ -195,6 +200,8 @@ const GemmVariant* gemm_variants_bwd_ln(int* count);
 const GemmVariant* gemm_variants_bwd_rms(int* count);
 const GemmVariant* gemm_variants_trans_plain(int* count);  // plain GEMMs with OperandFlags
 const GemmVariant* gemm_variants_trans_bwd(int* count);    // RMS-backward epilogue over X W^T
+const GemmVariant* gemm_variants_res_ln(int* count);       // post-norm LayerNorm with a residual add
+const GemmVariant* gemm_variants_res_rms(int* count);      // post-norm RMSNorm with a residual add
 
 // ---------------------------------------------------------------- row norm
 struct NormArgs {
@@ -208,6 +215,8 @@ struct NormArgs {
     float inv_cols;
     float* mean_out;
     float* rstd_out;
+    const void* res;        // optional residual (rows x cols bf16) added to `in` before the norm
+    void* h_out;            // with res (optional): bf16(in + res), rows x cols
 };
 
 // Picks the variant for `cols` and launches it; returns the CUDA status.

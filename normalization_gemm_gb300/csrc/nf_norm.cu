@@ -108,6 +108,27 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
                 for (int e = 0; e < 8; ++e) v[i][e] = 0.0f;
             }
         }
+        if (a.res != nullptr) {
+            // Residual add before the norm; the sum (rounded to bf16) is the
+            // updated residual stream.  The row's chunks of res are read before
+            // this thread writes the same chunks of h_out, so h_out may be res.
+            const uint4* res = reinterpret_cast<const uint4*>(a.res);
+            uint4* hout = reinterpret_cast<uint4*>(a.h_out);
+#pragma unroll
+            for (int i = 0; i < CPT; ++i) {
+                const int c = t + i * TPR;
+                if (live && c < chunks) {
+                    float r[8];
+                    unpack8(__ldcg(res + row * chunks + c), r);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[i][e] += r[e];
+                    if (hout != nullptr)
+                        __stcs(hout + row * chunks + c,
+                               make_uint4(pack_bf16x2(v[i][0], v[i][1]), pack_bf16x2(v[i][2], v[i][3]),
+                                          pack_bf16x2(v[i][4], v[i][5]), pack_bf16x2(v[i][6], v[i][7])));
+                }
+            }
+        }
         float mean = 0.0f, rstd;
         if (KIND == 0) {
             float s = 0.0f;

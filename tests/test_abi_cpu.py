@@ -41,6 +41,20 @@ def test_null_and_negative_arguments(L):
     assert L.nf_norm_rows(P, P, None, None, 4, 64, 7, 1e-5, None, None, None) == INVALID
 
 
+def test_residual_argument_checks(L):
+    # R is required; an H without R; misaligned R / H; empty M is a no-op
+    assert L.nf_gemm_postnorm_ln_res(P, P, None, None, None, P, None, 128, 64, 64, 1e-5, None, None, None) == INVALID
+    assert L.nf_gemm_postnorm_rms_res(P, P, None, None, P, P, 128, 64, 64, 1e-5, None, None) == INVALID
+    assert L.nf_gemm_postnorm_ln_res(P, P, P + 8, None, None, P, None, 128, 64, 64, 1e-5, None, None, None) == ALIGN
+    assert L.nf_gemm_postnorm_ln_res(P, P, P, None, None, P, P + 2, 128, 64, 64, 1e-5, None, None, None) == ALIGN
+    assert L.nf_gemm_postnorm_rms_res(P, P, P, None, P, None, 0, 64, 64, 1e-5, None, None) == OK
+    assert L.nf_gemm_postnorm_ln_res(P, P, P, None, None, P, None, 128, 4104, 64, 1e-5, None, None, None) == SHAPE
+    assert L.nf_norm_rows_res(P, None, P, None, None, None, 4, 64, 0, 1e-5, None, None, None) == INVALID
+    assert L.nf_norm_rows_res(P, P + 8, P, None, None, None, 4, 64, 0, 1e-5, None, None, None) == ALIGN
+    assert L.nf_norm_rows_res(P, P, P, P + 8, None, None, 4, 64, 1, 1e-5, None, None, None) == ALIGN
+    assert L.nf_norm_rows_res(P, None, P, None, None, None, 0, 64, 0, 1e-5, None, None, None) == OK
+
+
 def test_eps_must_be_finite_and_nonnegative(L):
     for eps in (float("nan"), float("inf"), -1e-6):
         assert L.nf_gemm_prenorm_rms(P, P, P, 128, 64, 64, eps, None, None) == INVALID
