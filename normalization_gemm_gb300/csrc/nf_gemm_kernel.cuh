@@ -61,6 +61,12 @@
 #include "nf_ptx.cuh"
 
 
+// The producer loads W's tiles, which every wave of tiles reads again, with an
+// evict-last L2 policy.
+#ifndef NF_W_EVICT_LAST
+#define NF_W_EVICT_LAST 1
+#endif
+
 namespace nf {
 
 // Bounded wait used only while draining: ignores the abort flag and records
@@ -480,6 +486,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;
             bool ok = true;
+            const uint64_t wpol = NF_W_EVICT_LAST ? l2_policy_evict_last() : 0;
             for (int lt = 0; lt < count && ok; ++lt) {
                 int m, n, row0, rows, kt0, kt1, slice;
                 sched.tile(lt, m, n, row0, rows);
@@ -511,12 +518,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                     if (Cfg::kBK) {
                         // W stored N x K: one box of TILE_N output columns x 64 K
                         // (K-major B: 128-byte rows along K, like A).
-                        tma_load_2d(sB + s * Cfg::B_STAGE_BYTES, &tmW, fb, kt * TILE_K, n * TILE_N);
+                        if (NF_W_EVICT_LAST)
+                            tma_load_2d_hint(sB + s * Cfg::B_STAGE_BYTES, &tmW, fb, kt * TILE_K, n * TILE_N, wpol);
+                        else
+                            tma_load_2d(sB + s * Cfg::B_STAGE_BYTES, &tmW, fb, kt * TILE_K, n * TILE_N);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < NBOX; ++i)
-                            tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb,
-                                        n * TILE_N + i * B_BOX_N, kt * TILE_K);
+                        for (int i = 0; i < NBOX; ++i) {
+                            if (NF_W_EVICT_LAST)
+                                tma_load_2d_hint(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb,
+                                                 n * TILE_N + i * B_BOX_N, kt * TILE_K, wpol);
+                            else
+                                tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb,
+                                            n * TILE_N + i * B_BOX_N, kt * TILE_K);
+                        }
                     }
                     ++issued;
                     if (++s == STAGES) {
