@@ -21,8 +21,9 @@
 //   warp 8     TMA producer (one elected lane): X and W K-tiles into a ring of
 //              STAGES shared-memory stages.
 //   warp 9     MMA issuer (one elected lane): tcgen05.mma 128 x TILE_N x 16
-//              into one of two TMEM accumulators (double buffered so that the
-//              epilogue of tile t overlaps the main loop of tile t+1).
+//              into one of NACC TMEM accumulators (two, or four for tiles of
+//              <= 128 columns without a row exchange) so that the epilogue of
+//              tile t overlaps the main loops of the tiles after it.
 //   warps 10-13 (pre-norm only) sum of squares of each X row, read from the
 //              same shared-memory stage the tensor cores consume, on CUDA
 //              cores, in parallel with the MMA (blog §2 pseudocode:
@@ -332,19 +333,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     const uint32_t sRS = base + Cfg::OFF_RS;  // A row scaling: rstd of each stage's 64 K-rows
     const uint32_t bar_full0 = sBar;             // [8]
     const uint32_t bar_empty0 = sBar + 8u * 8;   // [8]
-    const uint32_t bar_accf0 = sBar + 8u * 16;   // [2]
-    const uint32_t bar_acce0 = sBar + 8u * 18;   // [2]
-    const uint32_t bar_ssf0 = sBar + 8u * 20;    // [2]
-    const uint32_t bar_xch0 = sBar + 8u * 22;    // [2]
-    const uint32_t bar_mma_done = sBar + 8u * 24;
+    constexpr int NACC = Cfg::NACC;
+    const uint32_t bar_accf0 = sBar + 8u * 16;               // [NACC]
+    const uint32_t bar_acce0 = bar_accf0 + 8u * NACC;        // [NACC]
+    const uint32_t bar_ssf0 = bar_acce0 + 8u * NACC;         // [NACC]
+    const uint32_t bar_xch0 = bar_ssf0 + 8u * NACC;          // [NACC]
+    const uint32_t bar_mma_done = bar_xch0 + 8u * NACC;
     const uint32_t bar_xf0 = sBar + 256u;        // [8] A row scaling: stage s transformed
-    const uint32_t bar_afff0 = sBar + 8u * 25;   // [2] global exchange: a group's affine slot filled
-    const uint32_t bar_affe0 = sBar + 8u * 27;   // [2] global exchange: a group's affine slot free
-    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS);
+    const uint32_t bar_afff0 = bar_mma_done + 8u;  // [2] global exchange: a group's affine slot filled
+    const uint32_t bar_affe0 = bar_afff0 + 16u;    // [2] global exchange: a group's affine slot free
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS);
     volatile int* const abort_flag =
-        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS + 4);
+        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 4);
     volatile int* const epoch_sm =  // global exchange: launch epoch and the last launch's row counters
-        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * NUM_BARRIER_SLOTS + 8);
+        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 8);
     float* const ss_buf = reinterpret_cast<float*>(base_ptr + Cfg::OFF_SS);
     uint16_t* const aff = reinterpret_cast<uint16_t*>(base_ptr + Cfg::OFF_AFF);
 
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             mbar_init(bar_full0 + 8u * s, 1);
             mbar_init(bar_empty0 + 8u * s, 1 + (Cfg::kPre ? 128 : 0));
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NACC; ++b) {
             mbar_init(bar_accf0 + 8u * b, 1);
             mbar_init(bar_acce0 + 8u * b, 128);
             mbar_init(bar_ssf0 + 8u * b, 128);
@@ -561,8 +563,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int lt = 0; lt < count && ok; ++lt) {
-                const int b = lt & 1;
-                const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+                const int b = lt % NACC;
+                const uint32_t aph = static_cast<uint32_t>(lt / NACC) & 1u;
                 if (!mbar_wait(guard, bar_acce0 + 8u * b, aph ^ 1u, SITE_MMA_ACC_EMPTY, lt)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(b * TILE_N);
@@ -636,8 +638,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             int m, n, row0, rows, kt0, kt1, slice;
             sched.tile(lt, m, n, row0, rows);
             sched.krange(lt, kt0, kt1, slice);
-            const int b = lt & 1;
-            const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+            const int b = lt % NACC;
+            const uint32_t aph = static_cast<uint32_t>(lt / NACC) & 1u;
             const uint32_t jph = static_cast<uint32_t>(lt >> 1) & 1u;  // this group's tile count parity
             bool ok = true;
             const int nv = min(TILE_N, args.N - n * TILE_N);        // valid columns of this tile
@@ -1099,8 +1101,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         int s = 0;
         uint32_t ph = 0;
         for (int lt = 0; lt < count; ++lt) {
-            const int b = lt & 1;
-            const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+            const int b = lt % NACC;
+            const uint32_t aph = static_cast<uint32_t>(lt / NACC) & 1u;
             float acc0 = 0.0f, acc1 = 0.0f;
             bool ok = true;
             for (int kt = 0; kt < k_tiles; ++kt) {

@@ -23,8 +23,6 @@ constexpr int STAGING_BYTES = EPI_WARPS * STORE_BUF_BYTES;                 // on
 constexpr int MAX_CLUSTER = 16;           // post-norm: N <= 256 x 16
 constexpr int SMEM_OPTIN_LIMIT = 232448;  // 227 KB of dynamic shared memory per block
 constexpr int MAX_STAGES = 8;
-constexpr int NUM_BARRIER_SLOTS = 29;     // full[8] empty[8] acc_full[2] acc_empty[2] ss_full[2] xch[2] mma_done
-                                          // aff_full[2] aff_empty[2]
 
 enum Epilogue : int {
     EPI_PLAIN = 0,
@@ -97,11 +95,18 @@ struct GemmCfg {
     // moves across column tiles and keeps one slot per epilogue warpgroup,
     // refilled for each tile.
     static constexpr int AFFINE_BYTES = !kRow ? 0 : (XCH == XCH_GLOBAL ? 2 * (2 * TILE_N * 2) : 2 * TILE_N * 2);
-    static constexpr int SS_BYTES = kPre ? 2 * TILE_M * 4 : 0;        // sum of squares [2][128]
+    // TMEM accumulators: four when a tile has <= 128 columns and no row exchange
+    // (4 x 128 columns fill TMEM), so the MMA can run up to three tiles ahead of
+    // the epilogue, whose two warpgroups each alternate between two of them;
+    // two otherwise.
+    static constexpr int NACC = (TILE_N <= 128 && XCH == XCH_NONE && OPS == 0) ? 4 : 2;
+    // full[8] empty[8] acc_full, acc_empty, ss_full, xch [NACC] mma_done aff_full[2] aff_empty[2]
+    static constexpr int NSLOTS = 16 + 4 * NACC + 1 + 4;
+    static constexpr int SS_BYTES = kPre ? NACC * TILE_M * 4 : 0;     // sum of squares [NACC][128]
     // A row scaling: each ring stage's 64 rstd values, copied with the stage.
     // (256-column tiles fit four stages at most, narrower ones up to eight.)
     static constexpr int RS_BYTES = kScaleA ? (TILE_N == 256 ? 4 : MAX_STAGES) * TILE_K * 4 : 0;
-    static constexpr int BAR_BYTES = kScaleA ? 320 : 256;             // barriers (+ xformed[8]) + 4 words
+    static constexpr int BAR_BYTES = (kScaleA || NACC == 4) ? 320 : 256;  // barriers (+ xformed[8]) + 4 words
     // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
     // starts 1 KB aligned in practice; the global-exchange variant, whose
     // fourth pipeline stage needs the room, relies on that (and checks it at
@@ -124,15 +129,15 @@ struct GemmCfg {
     static constexpr int OFF_RS = OFF_SS + SS_BYTES;
     static constexpr int OFF_BAR = OFF_RS + RS_BYTES;
     static_assert(OFF_B % 1024 == 0 && OFF_STG % 1024 == 0, "swizzled buffers need 1 KB alignment");
-    static_assert(NUM_BARRIER_SLOTS * 8 + 16 <= 256, "barrier area + 4 words");
-    static_assert(!kScaleA || (NUM_BARRIER_SLOTS + 8) * 8 + 16 <= BAR_BYTES, "barrier area with xformed[8]");
+    static_assert(NSLOTS * 8 + 16 <= (kScaleA ? 256 : BAR_BYTES), "barrier area + 4 words");
+    static_assert(!kScaleA || 256 + 8 * 8 <= BAR_BYTES, "xformed[8] after the barrier area");
 
     static constexpr int PRODUCER_WARP = EPI_WARPS;       // 8
     static constexpr int MMA_WARP = EPI_WARPS + 1;        // 9
     static constexpr int SUMSQ_WARP0 = EPI_WARPS + 2;     // pre-norm: sum-of-squares warps 10-13;
                                                           // A row scaling: transform warps 10-13
     static constexpr int THREADS = (kPre || kScaleA ? EPI_WARPS + 6 : EPI_WARPS + 2) * 32;
-    static constexpr int TMEM_COLS = 2 * TILE_N;           // two accumulator buffers
+    static constexpr int TMEM_COLS = NACC * TILE_N;        // the accumulator buffers
 };
 
 // Kernel argument block (passed by value).

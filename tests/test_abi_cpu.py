@@ -105,7 +105,8 @@ def test_plans(L, op, M, N, K, tile_n, cluster, xch):
     assert p["tile_m"] == 128 and p["tile_k"] == (32 if tile_n == 512 else 64)
     assert p["tile_n"] == tile_n and p["cluster"] == cluster and p["exchange"] == xch
     assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
-    assert p["tmem_cols"] == min(2 * tile_n, 512)
+    # four accumulators for tiles of <= 128 columns without a row exchange, else two
+    assert p["tmem_cols"] == min((4 if (tile_n <= 128 and xch == 0) else 2) * tile_n, 512)
     assert p["threads"] == (448 if op == 1 else 320)
     m_tiles = -(-M // 128)
     n_tiles = 1 if (op >= 2 and xch != 2) else -(-N // tile_n)
@@ -206,7 +207,7 @@ def test_backward_plans(L, op, M, N, K, tile_n, cluster, xch):
     L2 exchange for K >= 512 and N > 512, else a cluster of ceil(N / 256) (<= 16)."""
     p = nf.plan_gemm(op, M, N, K, 148)
     assert (p["tile_n"], p["cluster"], p["exchange"], p["tile_k"]) == (tile_n, cluster, xch, 64)
-    assert p["threads"] == 320 and p["tmem_cols"] == 2 * tile_n
+    assert p["threads"] == 320 and p["tmem_cols"] == (4 if (tile_n <= 128 and xch == 0) else 2) * tile_n
 
 
 def test_backward_argument_checks(L):
