@@ -307,14 +307,25 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
     return NF_OK;
 }
 
-// Memory-bound shapes (short K) whose last, partial wave holds at most half
-// a wave of tiles: cut each of those tiles into two 64-row units so that the
-// wave spreads over twice as many SMs.  (A half still runs the full MMA, so
-// tensor-bound shapes gain nothing and keep whole tiles.)
-void split_last_wave(int tiles, int grid, int k_tiles, int32_t* units, int32_t* split_base) {
+// Whether a tile's share of HBM traffic takes longer than its MMA: its X rows
+// (128 x K, read once per row tile and shared by the row's n_tiles CTAs) and
+// its Y (128 x tile_n) against 2 * 128 * tile_n * K flops, at GB300's ratio of
+// tensor throughput to HBM bandwidth (about 290 flop per byte).
+bool tile_memory_bound(int64_t K, int tile_n, int n_tiles) {
+    const double bytes = static_cast<double>(TILE_M) * K * 2 / n_tiles + static_cast<double>(TILE_M) * tile_n * 2;
+    const double flops = 2.0 * TILE_M * tile_n * static_cast<double>(K);
+    return flops < 290.0 * bytes;
+}
+
+// Memory-bound tiles whose last, partial wave holds at most half a wave of
+// tiles: cut each of those tiles into two 64-row units so that the wave
+// spreads over twice as many SMs.  (A half still runs the full MMA, so it
+// gains only where the tile waits on memory; tensor-bound shapes keep whole
+// tiles.)
+void split_last_wave(int tiles, int grid, bool memory_bound, int32_t* units, int32_t* split_base) {
     *units = tiles;
     *split_base = tiles;
-    if (k_tiles > 4 || tiles <= grid) return;
+    if (!memory_bound || tiles <= grid) return;
     const int full = (tiles / grid) * grid;
     const int rest = tiles - full;
     if (rest > 0 && 2 * rest <= grid) {
@@ -668,7 +679,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     } else {
         const int tiles = p.m_tiles * p.n_tiles;
         grid = tiles < d->sm_count ? tiles : d->sm_count;
-        split_last_wave(tiles, grid, p.k_tiles, &a.units, &a.split_base);
+        split_last_wave(tiles, grid, tile_memory_bound(K, p.tile_n, p.n_tiles), &a.units, &a.split_base);
     }
 
     cudaLaunchConfig_t cfg = {};

@@ -484,3 +484,33 @@ def test_global_exchange_shape_sequence_on_one_stream(dev, orc, force_global):
         assert_close(to_f64(y)[rows], ref, f"global exchange sequence {M}x{K}x{N}")
         torch.cuda.synchronize()
         assert nf.device_status()[0] == nf.NF_OK
+
+
+@pytest.mark.parametrize("op,M,K,N", [("pre_rms", 24320, 512, 512), ("plain", 24320, 512, 512),
+                                      ("post_ln", 27136, 320, 256), ("post_rms", 27136 + 40, 1024, 200)])
+def test_split_last_wave_long_k(dev, orc, op, M, K, N):
+    """Memory-bound tiles with K > 256 whose last partial wave holds at most
+    half a wave: those tiles run as two 64-row units (each still a 128-row MMA,
+    storing its own half).  Rows of the split tail and of full tiles against
+    the oracle."""
+    import torch
+    inp = _inputs(M, K, N, seed=M + K, gamma=True, beta=True)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([rng.integers(0, M, 64), rng.integers(max(0, M - 9000), M, 128),
+                                     np.arange(M - 70, M)])).astype(np.int64)
+    if op == "pre_rms":
+        y = nf.gemm_prenorm_rms(X, W, 1e-6)
+        ref = orc.gemm_prenorm_rms(inp["X"], inp["W"], 1e-6, rows=rows)[0]
+    elif op == "plain":
+        y = nf.gemm_plain(X, W)
+        ref = orc.gemm_plain(inp["X"], inp["W"], rows=rows)
+    elif op == "post_ln":
+        y = nf.gemm_postnorm_ln(X, W, 1e-5, to_dev(inp["gamma"], dev), to_dev(inp["beta"], dev))
+        ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, inp["gamma"], inp["beta"], rows=rows)[0]
+    else:
+        y = nf.gemm_postnorm_rms(X, W, 1e-5, to_dev(inp["gamma"], dev))
+        ref = orc.gemm_postnorm_rms(inp["X"], inp["W"], 1e-5, inp["gamma"], rows=rows)[0]
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y.float()).all())
+    assert_close(to_f64(y[torch.from_numpy(rows).to(dev)]), ref, f"split tail {op} {M}x{K}x{N}")
