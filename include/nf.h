@@ -340,8 +340,10 @@ nf_status nf_set_postnorm_exchange(int mode);
 /* Split-K of plain GEMMs (nf_gemm_plain, nf_gemm_plain_t and the weight
  * gradient of nf_gemm_prenorm_rms_bwd).  mode 0 (default): when the output
  * has at most half as many 128-row tiles as the device has SMs, the
- * contraction is cut into slices of >= 8 K-tiles, one (tile, slice) per SM;
- * each writes an fp32 partial product into a per-stream workspace (SMs x
+ * contraction of every tile is cut into slices of >= 8 K-tiles, one
+ * (tile, slice) per SM; when a tensor-bound GEMM's last, partial wave holds
+ * at most half as many tiles as SMs, only that wave's tiles are split.  Each
+ * split unit writes an fp32 partial tile into a per-stream workspace (SMs x
  * 128 KB, allocated by the first such call on a stream, which must not be
  * inside a graph capture), and a second kernel adds the slices in a fixed
  * order and rounds to bf16, so results are reproducible.  mode 1: never
@@ -375,6 +377,7 @@ typedef struct nf_plan {
     int32_t tiles;                  /* output tiles (M/tile_m x N/tile_n)  */
     int32_t exchange;               /* 0 none, NF_XCH_CLUSTER, NF_XCH_GLOBAL */
     int32_t splitk;                 /* contraction slices (plain GEMM; 1 = none) */
+    int32_t split_tiles;            /* tiles split over the contraction (the last ones) */
 } nf_plan;
 nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count,
                        nf_plan* out);

@@ -54,7 +54,7 @@ class NFError(RuntimeError):
 class NFPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "tile_m", "tile_n", "tile_k", "stages", "cluster", "grid", "threads", "smem_bytes",
-        "tmem_cols", "tiles", "exchange", "splitk")]
+        "tmem_cols", "tiles", "exchange", "splitk", "split_tiles")]
 
 
 _lib: Optional[ctypes.CDLL] = None

@@ -195,7 +195,8 @@ nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 enum Op { OP_PLAIN = 0, OP_PRE = 1, OP_POST_LN = 2, OP_POST_RMS = 3, OP_BWD_LN = 4, OP_BWD_RMS = 5 };
 
 struct Plan {
-    int splitk = 1;  // contraction slices (plain GEMM)
+    int splitk = 1;  // contraction slices of the split tiles (plain GEMM)
+    int sk_base = 0, sk_tiles = 0;  // split-K: first split tile, split tiles
     int tile_n = 0;
     int xch = XCH_NONE;
     bool clustered = false;
@@ -225,6 +226,16 @@ const GemmVariant* find_variant(int op, int tile_n, int xch, int ops = 0) {
     for (int i = 0; i < n; ++i)
         if (t[i].tile_n == tile_n && t[i].xch == xch && t[i].ops == ops) return &t[i];
     return nullptr;
+}
+
+// Whether a tile's share of HBM traffic takes longer than its MMA: its X rows
+// (128 x K, read once per row tile and shared by the row's n_tiles CTAs) and
+// its Y (128 x tile_n) against 2 * 128 * tile_n * K flops, at GB300's ratio of
+// tensor throughput to HBM bandwidth (about 290 flop per byte).
+bool tile_memory_bound(int64_t K, int tile_n, int n_tiles) {
+    const double bytes = static_cast<double>(TILE_M) * K * 2 / n_tiles + static_cast<double>(TILE_M) * tile_n * 2;
+    const double flops = 2.0 * TILE_M * tile_n * static_cast<double>(K);
+    return flops < 290.0 * bytes;
 }
 
 // Tile choice.  Plain and pre-norm: the smallest of 64 / 128 / 256 columns
@@ -291,30 +302,29 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
     p->v = find_variant(op, p->tile_n, p->xch, ops);
     if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
     p->k_tiles = static_cast<int>((K + p->v->tile_k - 1) / p->v->tile_k);
-    // Split-K (plain GEMM): when the output has at most half as many tiles as
-    // there are SMs, cut the contraction into slices of >= 8 K-tiles so that
-    // tiles x slices fills the SMs once; fp32 partials, added by a second kernel.
+    // Split-K (plain GEMM), slices of >= 8 K-tiles, fp32 partials added by a
+    // second kernel:
+    //   * at most half as many output tiles as SMs: every tile is split, so
+    //     that tiles x slices fills the SMs once;
+    //   * tensor-bound tiles whose last, partial wave holds at most half the
+    //     SMs: only that wave's tiles are split, so it takes a fraction of a
+    //     tile's time instead of a whole one while most SMs idle.  (Memory-bound
+    //     tiles cut that wave into 64-row halves instead, split_last_wave.)
     p->splitk = 1;
+    p->sk_base = p->sk_tiles = 0;
     if (op == OP_PLAIN && g_splitk_mode != 1) {
         const int tiles = p->m_tiles * p->n_tiles;
+        const int kmax = p->k_tiles / 8;
         if (2 * tiles <= sms) {
-            int s = sms / tiles;
-            const int kmax = p->k_tiles / 8;
-            if (s > kmax) s = kmax;
-            if (s > 1) p->splitk = s;
+            const int s = sms / tiles < kmax ? sms / tiles : kmax;
+            if (s > 1) p->splitk = s, p->sk_tiles = tiles;
+        } else if (!tile_memory_bound(K, p->tile_n, p->n_tiles)) {
+            const int full = (tiles / sms) * sms, rest = tiles - full;
+            const int s = rest > 0 ? (sms / rest < kmax ? sms / rest : kmax) : 0;
+            if (rest > 0 && 2 * rest <= sms && s > 1) p->splitk = s, p->sk_base = full, p->sk_tiles = rest;
         }
     }
     return NF_OK;
-}
-
-// Whether a tile's share of HBM traffic takes longer than its MMA: its X rows
-// (128 x K, read once per row tile and shared by the row's n_tiles CTAs) and
-// its Y (128 x tile_n) against 2 * 128 * tile_n * K flops, at GB300's ratio of
-// tensor throughput to HBM bandwidth (about 290 flop per byte).
-bool tile_memory_bound(int64_t K, int tile_n, int n_tiles) {
-    const double bytes = static_cast<double>(TILE_M) * K * 2 / n_tiles + static_cast<double>(TILE_M) * tile_n * 2;
-    const double flops = 2.0 * TILE_M * tile_n * static_cast<double>(K);
-    return flops < 290.0 * bytes;
 }
 
 // Memory-bound tiles whose last, partial wave holds at most half a wave of
@@ -636,6 +646,8 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.xbank = 0;
     a.xstats = nullptr;
     a.splitk = p.splitk;
+    a.sk_base = p.sk_base;
+    a.sk_tiles = p.sk_tiles;
     a.ws = nullptr;
     a.xhat_out = (op == OP_BWD_LN || op == OP_BWD_RMS) ? static_cast<uint16_t*>(xhat_out) : nullptr;
     a.resid = static_cast<const uint16_t*>(resid);
@@ -671,11 +683,12 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
             return st;
         }
     } else if (p.splitk > 1) {
-        // One (tile, slice) unit per CTA: tiles x splitk <= SMs.
+        // Whole tiles first (whole waves), then the split tiles' units, at most
+        // one per CTA: sk_tiles x splitk <= SMs.
         if ((st = splitk_scratch(stream, d->sm_count, &a.ws)) != NF_OK) return st;
-        a.units = p.m_tiles * p.n_tiles * p.splitk;
+        a.units = p.sk_base + p.sk_tiles * p.splitk;
         a.split_base = a.units;
-        grid = a.units;
+        grid = a.units < d->sm_count ? a.units : d->sm_count;
     } else {
         const int tiles = p.m_tiles * p.n_tiles;
         grid = tiles < d->sm_count ? tiles : d->sm_count;
@@ -720,10 +733,20 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
     }
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
-    if (p.splitk > 1 &&
-        (e = launch_splitk_reduce(a.ws, p.splitk, M * N, static_cast<uint16_t*>(Y), d->sm_count, g_overlap, stream)) !=
-            cudaSuccess)
-        return fail_cuda(e, "split-K reduction launch");
+    if (p.splitk > 1) {
+        SplitkReduceArgs r;
+        r.ws = a.ws;
+        r.y = static_cast<uint16_t*>(Y);
+        r.slices = p.splitk;
+        r.sk_base = p.sk_base;
+        r.sk_tiles = p.sk_tiles;
+        r.n_tiles = p.n_tiles;
+        r.tile_n = p.tile_n;
+        r.M = a.M;
+        r.N = a.N;
+        if ((e = launch_splitk_reduce(r, d->sm_count, g_overlap, stream)) != cudaSuccess)
+            return fail_cuda(e, "split-K reduction launch");
+    }
     return NF_OK;
 }
 
@@ -1042,11 +1065,13 @@ nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf
     out->tiles = M > 0 ? p.m_tiles * p.n_tiles : 0;
     out->exchange = p.xch;
     out->splitk = p.splitk;
+    out->split_tiles = p.splitk > 1 ? p.sk_tiles : 0;
     if (p.clustered) {
         const int mc = sm_count / p.cluster;
         out->grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;
     } else if (p.splitk > 1) {
-        out->grid = out->tiles * p.splitk;
+        const int units = p.sk_base + p.sk_tiles * p.splitk;
+        out->grid = units < sm_count ? units : sm_count;
     } else {
         out->grid = out->tiles < sm_count ? out->tiles : sm_count;
     }

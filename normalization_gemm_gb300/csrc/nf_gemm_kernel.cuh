@@ -256,33 +256,37 @@ __device__ __forceinline__ void put_staged_row(uint32_t buf, int lane, const uin
 // tiles of the last, partial wave cut into two 64-row halves, so that wave
 // spreads over twice as many SMs.  A half still runs the 128-row MMA (the X
 // box simply starts 64 rows further for the second half); only its own 64
-// rows are stored.  A split-K launch (splitk > 1, plain GEMM) has
-// tiles x splitk units, slice-major: unit u is tile u mod tiles over the
-// contraction slice u / tiles, K-tiles [s k_tiles / splitk, (s+1) k_tiles / splitk).
+// rows are stored.  A split-K launch (splitk > 1, plain GEMM) runs units
+// [0, sk_base) as whole tiles and splits the sk_tiles tiles from sk_base on
+// over the contraction, slice-major: unit sk_base + j is tile
+// sk_base + j mod sk_tiles over slice s = j / sk_tiles, K-tiles
+// [s k_tiles / splitk, (s+1) k_tiles / splitk).  (sk_base = 0 splits every
+// tile; sk_base > 0 only the last, partial wave.)
 struct TileSched {
     int first, step, count;  // m (clustered) or linear unit (unclustered) sequence
     int n_fixed;             // clustered: this CTA's n tile (its cluster rank)
     int n_tiles;
     int split_base;          // first half-tile unit (unclustered)
-    int tiles;               // m_tiles x n_tiles
-    int splitk;              // contraction slices
+    int sk_base, sk_tiles;   // split-K: first split unit / tile, split tiles
+    int splitk;              // contraction slices of the split tiles
     int k_tiles;
     bool clustered;
-    // K-tiles of unit lt and its slice.
+    // K-tiles of unit lt and its slice (-1 for a whole tile).
     __device__ __forceinline__ void krange(int lt, int& kt0, int& kt1, int& slice) const {
-        if (splitk <= 1) {
+        const int u = first + lt * step;
+        if (splitk <= 1 || u < sk_base) {
             kt0 = 0;
             kt1 = k_tiles;
-            slice = 0;
+            slice = -1;
             return;
         }
-        slice = (first + lt * step) / tiles;
+        slice = (u - sk_base) / sk_tiles;
         kt0 = static_cast<int>(static_cast<int64_t>(slice) * k_tiles / splitk);
         kt1 = static_cast<int>(static_cast<int64_t>(slice + 1) * k_tiles / splitk);
     }
     __device__ __forceinline__ void tile(int lt, int& m, int& n, int& row0, int& rows) const {
         int u = first + lt * step;
-        if (splitk > 1) u -= (u / tiles) * tiles;
+        if (splitk > 1 && u >= sk_base) u = sk_base + (u - sk_base) % sk_tiles;
         if (clustered) {
             m = u;
             n = n_fixed;
@@ -377,7 +381,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         sched.n_fixed = 0;
         sched.split_base = args.split_base;
     }
-    sched.tiles = args.m_tiles * args.n_tiles;
+    sched.sk_base = args.sk_base;
+    sched.sk_tiles = args.sk_tiles;
     sched.splitk = args.splitk;
     sched.k_tiles = args.k_tiles;
     const int count = sched.count;
@@ -966,14 +971,16 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                         released = true;
                     }
                 }
-                if (EPI == EPI_PLAIN && args.splitk > 1) {
+                if (EPI == EPI_PLAIN && args.splitk > 1 && slice >= 0) {
                     // Split-K: the row's fp32 partial over this unit's slice of
-                    // the contraction goes to the slice's plane of the
-                    // workspace; a second kernel adds the planes in order.
+                    // the contraction goes to the tile's slot in the slice's
+                    // plane of the workspace; a second kernel adds the planes in
+                    // order.
                     const int cw = sg * SEG;
                     if (own_row && cw < nv) {
+                        const int tl = m * args.n_tiles + n - args.sk_base;  // split tile index
                         float* const dst =
-                            args.ws + (static_cast<size_t>(slice) * args.M + grow) * args.N + n * TILE_N + cw;
+                            args.ws + ((static_cast<size_t>(slice) * args.sk_tiles + tl) * TILE_M + row) * TILE_N + cw;
 #pragma unroll
                         for (int q = 0; q < SEG / 4; ++q)
                             if (q * 4 < nv - cw) {

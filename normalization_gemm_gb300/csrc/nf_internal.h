@@ -161,8 +161,10 @@ struct GemmArgs {
     int* xcnt;              // global exchange only: XCH_CNT0 + 2 * xbank ints
     int32_t xbank;          // ints per counter bank, >= xch_bank_ints(m_tiles)
     float2* xstats;         // global exchange only: >= xch_stats_bytes(m_tiles, n_tiles)
-    int32_t splitk;         // plain GEMM: contraction slices (1 = none); units are tiles x slices
-    float* ws;              // splitk > 1: fp32 partial products, [splitk][M][N]
+    int32_t splitk;         // plain GEMM: contraction slices of the split tiles (1 = none)
+    int32_t sk_base;        // splitk > 1: first split unit (= first split tile); units before it are whole tiles
+    int32_t sk_tiles;       // splitk > 1: split tiles (sk_base .. sk_base + sk_tiles - 1), each in splitk units
+    float* ws;              // splitk > 1: fp32 partial tiles, [splitk][sk_tiles][TILE_M][TILE_N]
     uint16_t* xhat_out;     // RMS backward (optional): bf16(Z * rstd), M x N, the rebuilt rmsnorm input
     const uint16_t* resid;  // post-norm (optional): R, M x N bf16, added to X W before the statistics
     uint16_t* h_out;        // with resid (optional): bf16(X W + R), M x N, the updated residual stream
@@ -243,9 +245,16 @@ cudaError_t launch_norm_rows_bwd(const NormBwdArgs& a, int kind, int sm_count, b
 // Largest supported cols.
 constexpr int NORM_MAX_COLS = 16384;
 
-// Split-K: Y (bf16, `elems` values) = sum over `slices` of the fp32 partial
-// products ws[s][.], added in slice order.  elems % 8 == 0.
-cudaError_t launch_splitk_reduce(const float* ws, int slices, int64_t elems, uint16_t* y, int sm_count, bool overlap,
-                                 cudaStream_t stream);
+// Split-K: for each split tile t = sk_base + i (i < sk_tiles), Y's tile
+// (TILE_M x tile_n at row tile t / n_tiles, column tile t % n_tiles) in bf16 =
+// the sum over `slices` of the fp32 partial tiles ws[s][i], added in slice
+// order; only elements inside M x N are written.  N % 8 == 0.
+struct SplitkReduceArgs {
+    const float* ws;
+    uint16_t* y;
+    int32_t slices, sk_base, sk_tiles, n_tiles, tile_n;
+    int32_t M, N;
+};
+cudaError_t launch_splitk_reduce(const SplitkReduceArgs& a, int sm_count, bool overlap, cudaStream_t stream);
 
 }  // namespace nf

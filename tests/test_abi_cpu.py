@@ -246,8 +246,10 @@ def splitk_slices(k_tiles, splitk):
     (512, 512, 32768, 152, 19),    # the weight gradient of the Lazy Pre-Norm backward, 32768 x 512 x 512
     (512, 512, 32768, 148, 18),
     (128, 64, 4096, 152, 8),       # one tile: slices of 8 K-tiles
-    (4096, 4096, 8192, 152, 1),    # 512 tiles: no split
+    (4096, 4096, 8192, 152, 2),    # 512 tiles, tensor-bound: the last wave's 56 tiles in 2 slices
     (512, 512, 512, 152, 1),       # 8 K-tiles: no split
+    (8192, 4096, 4096, 152, 1),    # 1024 tiles: last wave of 112 tiles, more than half the SMs
+    (4096, 4096, 256, 152, 1),     # last wave of 56 tiles but 4 K-tiles: too short to split
     (9728, 256, 4096, 152, 2),     # 76 tiles = half the SMs, 64 K-tiles: 2 slices
     (100, 200, 2048, 152, 4),      # one tile, 32 K-tiles: slices of 8
 ])
@@ -255,10 +257,17 @@ def test_splitk_plans(L, M, N, K, sms, splitk):
     p = nf.plan_gemm(0, M, N, K, sms)
     tiles = p["tiles"]
     assert p["splitk"] == splitk
-    assert p["grid"] == (tiles * splitk if splitk > 1 else min(tiles, sms))
     assert p["grid"] <= sms
     k_tiles = -(-K // 64)
+    if splitk > 1 and 2 * tiles > sms:
+        # only the last, partial wave is split: whole waves, then <= one split unit per SM
+        rest = tiles % sms
+        assert p["split_tiles"] == rest and 0 < 2 * rest <= sms and rest * splitk <= sms
+        assert p["grid"] == sms
+        return
+    assert p["grid"] == (tiles * splitk if splitk > 1 else min(tiles, sms))
     if splitk > 1:
+        assert p["split_tiles"] == tiles
         assert 2 * tiles <= sms
         sl = splitk_slices(k_tiles, splitk)
         assert sl[0][0] == 0 and sl[-1][1] == k_tiles

@@ -231,3 +231,33 @@ def test_every_tile_computed_once(dev, M, K, N):
     nf.gemm_plain(x, w, out=y)
     torch.cuda.synchronize()
     assert torch.equal(y, w[idx])
+
+
+@pytest.mark.parametrize("flags", [0, nf.TRANS_X, nf.TRANS_W], ids=["plain", "trans_x", "trans_w"])
+def test_plain_tail_splitk(dev, orc, flags):
+    """A tensor-bound GEMM whose last wave is at most half full: its tiles are
+    split over the contraction (whole tiles before them).  Rows of the split
+    tiles and of whole tiles against the oracle; repeated calls give the same
+    bits."""
+    import torch
+    M, K, N = 3840, 1024, 4096
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    p = nf.plan_gemm(0, M, N, K, sms)
+    tiles = p["tiles"]
+    if tiles % sms == 0 or 2 * (tiles % sms) > sms:
+        pytest.skip("shape does not leave a half-empty last wave on this device")
+    assert p["splitk"] > 1 and p["split_tiles"] == tiles % sms
+    inp = nf_inputs.make_inputs(M, K, N, seed=41)
+    X, W = inp["X"], inp["W"]
+    xs = np.ascontiguousarray(X.T) if flags & nf.TRANS_X else X
+    ws = np.ascontiguousarray(W.T) if flags & nf.TRANS_W else W
+    x, w = to_dev(xs, dev), to_dev(ws, dev)
+    run = (lambda: nf.gemm_plain_t(x, w, flags)) if flags else (lambda: nf.gemm_plain(x, w))
+    y, y2 = run(), run()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    first_split_row = (tiles - p["split_tiles"]) // (N // 256) * 128
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([rng.integers(0, M, 24), rng.integers(first_split_row, M, 40),
+                                     np.array([M - 1, first_split_row])])).astype(np.int64)
+    assert_close(to_f64(y)[rows], orc.gemm_plain(X, W, rows=rows), f"tail split-K flags={flags}")
