@@ -25,6 +25,7 @@ _HDR = os.path.join(_HERE, "nfo.h")
 LIB_PATH = os.path.join(_HERE, "libnfo.so")
 
 NORM_LN = 0
+ACT_IDENTITY, ACT_GELU_TANH, ACT_SILU = 0, 1, 2
 NORM_RMS = 1
 
 # -ffp-contract=off keeps every multiply and add separately rounded, so the
@@ -78,6 +79,9 @@ class Oracle:
         lib.nfo_gemm_postnorm_res.argtypes = [_P_U16, _P_U16, _P_U16, _P_U16, _P_U16, _I64, _I64, _I64,
                                               ctypes.c_int, ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64,
                                               _P_F64, _P_F64]
+        lib.nfo_flashnorm_attn_fwd.argtypes = [_P_U16, _P_U16, _P_U16, ctypes.POINTER(ctypes.c_int32), _I64, _I64,
+                                               _I64, _I64, _I64, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                               _P_F64]
         lib.nfo_norm_rows.argtypes = [_P_U16, _P_U16, _P_U16, _I64, _I64, ctypes.c_int,
                                       ctypes.c_double, _P_I64, _I64, _P_F64, _P_F64, _P_F64]
         lib.nfo_gemm_postnorm_bwd.argtypes = [_P_U16, _P_U16, _P_U16, _P_U16, _P_F64, _P_F64, _I64,
@@ -91,7 +95,7 @@ class Oracle:
         for f in ("nfo_gemm_plain", "nfo_gemm_prenorm_rms", "nfo_gemm_postnorm_ln",
                   "nfo_gemm_postnorm_rms", "nfo_norm_rows", "nfo_gemm_postnorm_bwd",
                   "nfo_norm_rows_bwd", "nfo_prenorm_rms_bwd_da", "nfo_prenorm_rms_bwd_db",
-                  "nfo_gemm_postnorm_res",
+                  "nfo_gemm_postnorm_res", "nfo_flashnorm_attn_fwd",
                   "nfo_max_threads"):
             getattr(lib, f).restype = ctypes.c_int
         lib.nfo_set_threads.argtypes = [ctypes.c_int]
@@ -175,6 +179,23 @@ class Oracle:
                                                    K, int(kind), eps, rp, R, _f64(Y), _f64(H), _f64(mean),
                                                    _f64(rstd)), "gemm_postnorm_res")
         return Y, H, (mean if kind == NORM_LN else None), rstd
+
+    def flashnorm_attn_fwd(self, Q, K, V, act, eps1, eps2, q_len=None):
+        """FlashNormAttention forward.  Q: [B, Lq, H, D], K / V: [B, Lkv, H, D]
+        (bf16 bit patterns); q_len: B ints or None.  Returns Out [B, Lq, H, D]
+        fp64 with rows t >= q_len[b] left NaN."""
+        Bn, Lq, H, D = Q.shape
+        Lkv = K.shape[1]
+        assert K.shape == (Bn, Lkv, H, D) and V.shape == K.shape
+        out = np.full((Bn, Lq, H, D), np.nan, np.float64)
+        ql = None
+        if q_len is not None:
+            ql = np.ascontiguousarray(q_len, dtype=np.int32)
+            assert ql.shape == (Bn,)
+        self._check(self.lib.nfo_flashnorm_attn_fwd(
+            _u16(Q), _u16(K), _u16(V), None if ql is None else ql.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            Bn, Lq, Lkv, H, D, int(act), float(eps1), float(eps2), _f64(out)), "flashnorm_attn_fwd")
+        return out
 
     def norm_rows(self, A, kind, eps, gamma=None, beta=None, rows=None):
         Rr, C = A.shape

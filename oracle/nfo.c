@@ -442,6 +442,80 @@ int nfo_prenorm_rms_bwd_db(const uint16_t* A, const double* rstd, const uint16_t
     return 0;
 }
 
+/* x rounded to the nearest bfloat16 (ties to even), from the definition:
+ * 8 significant bits; below 2^-126 the spacing stays 2^-133. */
+static double round_bf16(double x) {
+    if (x == 0.0 || isnan(x) || isinf(x)) return x;
+    int e;
+    (void)frexp(x, &e);                 /* |x| in [2^(e-1), 2^e) */
+    if (e < -125) e = -125;             /* subnormal range: fixed spacing */
+    const double q = ldexp(1.0, e - 8); /* spacing of the 8 significant bits */
+    return rint(x / q) * q;             /* rint: nearest, ties to even */
+}
+
+static double activation(double x, int act) {
+    if (act == NFO_ACT_GELU_TANH)
+        return 0.5 * x * (1.0 + tanh(sqrt(2.0 / 3.14159265358979323846) * (x + 0.044715 * x * x * x)));
+    if (act == NFO_ACT_SILU) return x / (1.0 + exp(-x));
+    return x;
+}
+
+int nfo_flashnorm_attn_fwd(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                           const int32_t* q_len, int64_t B, int64_t Lq, int64_t Lkv,
+                           int64_t H, int64_t D, int act, double eps1, double eps2,
+                           double* Out) {
+    if (!Q || !K || !V || !Out || B < 0 || Lq < 0 || Lkv <= 0 || H <= 0 || D <= 0) return -1;
+    if (act != NFO_ACT_IDENTITY && act != NFO_ACT_GELU_TANH && act != NFO_ACT_SILU) return -1;
+    if (!(eps1 >= 0.0) || !(eps2 >= 0.0)) return -1;
+    if (q_len)
+        for (int64_t b = 0; b < B; ++b)
+            if (q_len[b] < 0 || q_len[b] > Lq) return -1;
+    const int64_t HD = H * D;
+    const int64_t tokens = B * Lq;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* q = (double*)malloc(sizeof(double) * (size_t)HD);
+        double* ln = (double*)malloc(sizeof(double) * (size_t)HD);
+        double* o = (double*)malloc(sizeof(double) * (size_t)HD);
+        double* s = (double*)malloc(sizeof(double) * (size_t)Lkv);
+        if (!q || !ln || !o || !s) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t i = 0; i < tokens; ++i) {
+            if (!q || !ln || !o || !s) continue;
+            const int64_t b = i / Lq, t = i - b * Lq;
+            if (t >= (q_len ? q_len[b] : Lq)) continue;
+            load_row(Q, i, HD, q);
+            layernorm_row(q, HD, NULL, NULL, eps1, ln, NULL, NULL);      /* ln_q over all heads */
+            for (int64_t h = 0; h < H; ++h) {
+                const double* lh = ln + h * D;
+                for (int64_t j = 0; j < Lkv; ++j) {                      /* s = act(bf16(ln_q_h) . k_j) */
+                    const uint16_t* kj = K + ((b * Lkv + j) * H + h) * D;
+                    double acc = 0.0;
+                    for (int64_t d = 0; d < D; ++d) acc += round_bf16(lh[d]) * bf16_to_double(kj[d]);
+                    s[j] = round_bf16(activation(acc, act));
+                }
+                for (int64_t d = 0; d < D; ++d) o[h * D + d] = lh[d];    /* residual 1 */
+                for (int64_t j = 0; j < Lkv; ++j) {                      /* + bf16(s) . V */
+                    const uint16_t* vj = V + ((b * Lkv + j) * H + h) * D;
+                    for (int64_t d = 0; d < D; ++d) o[h * D + d] += s[j] * bf16_to_double(vj[d]);
+                }
+            }
+            double* out = Out + i * HD;
+            rmsnorm_row(o, HD, NULL, eps2, out, NULL);                   /* RMSNorm over all heads */
+            for (int64_t k = 0; k < HD; ++k) out[k] += q[k];             /* residual 2 */
+        }
+        free(q);
+        free(ln);
+        free(o);
+        free(s);
+    }
+    return bad ? -1 : 0;
+}
+
 int nfo_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

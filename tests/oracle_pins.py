@@ -700,12 +700,110 @@ def pin_residual_reductions(o):
         assert np.max(np.abs(Y2 - Y1)) <= 1e-10, "LN is shift invariant in R"
 
 
+# ---------------------------------------------------------------- FlashNormAttention forward
+def _fna_case(B, Lq, Lkv, H, D, seed, scale_kv=0.15):
+    g = np.random.default_rng(seed)
+    Q = bf16_round(g.standard_normal((B, Lq, H, D)) * 1.3 + 0.2)
+    K = bf16_round(g.standard_normal((B, Lkv, H, D)) * scale_kv)
+    V = bf16_round(g.standard_normal((B, Lkv, H, D)) * scale_kv)
+    return Q, K, V
+
+
+def _fna_torch(Q, K, V, act, eps1, eps2):
+    """The blog §4 pseudocode as torch float64 ops, the two matmuls' left
+    operands rounded to bf16 (bf16_round of the input generator, not the
+    oracle's rounding)."""
+    import torch
+    import torch.nn.functional as F
+    B, Lq, H, D = Q.shape
+    q = torch.from_numpy(bf16_to_f64(Q)).reshape(B, Lq, H * D)
+    k = torch.from_numpy(bf16_to_f64(K))
+    v = torch.from_numpy(bf16_to_f64(V))
+    ln = F.layer_norm(q, (H * D,), eps=eps1).reshape(B, Lq, H, D)
+    lnr = torch.from_numpy(bf16_to_f64(bf16_round(ln.numpy())))
+    s = torch.einsum("bthd,bjhd->bhtj", lnr, k)
+    a = {0: s, 1: F.gelu(s, approximate="tanh"), 2: F.silu(s)}[act]
+    p = torch.from_numpy(bf16_to_f64(bf16_round(a.numpy())))
+    o = torch.einsum("bhtj,bjhd->bthd", p, v) + ln
+    out = F.rms_norm(o.reshape(B, Lq, H * D), (H * D,), eps=eps2) + q
+    return out.reshape(B, Lq, H, D).numpy()
+
+
+def pin_fna_torch(o):
+    for (B, Lq, Lkv, H, D, act) in [(2, 5, 8, 3, 16, 1), (1, 4, 128, 2, 32, 2), (3, 2, 16, 1, 8, 0)]:
+        Q, K, V = _fna_case(B, Lq, Lkv, H, D, seed=B * 7 + H)
+        got = o.flashnorm_attn_fwd(Q, K, V, act, 1e-5, 1e-6)
+        want = _fna_torch(Q, K, V, act, 1e-5, 1e-6)
+        err = np.max(np.abs(got - want))
+        assert err <= 1e-9, f"FlashNormAttention vs torch (act {act}): max err {err}"
+
+
+def pin_fna_bruteforce(o):
+    """Plain Python loops over a tiny case (math.tanh / math.exp)."""
+    import math
+    B, Lq, Lkv, H, D = 1, 2, 3, 2, 4
+    Q, K, V = _fna_case(B, Lq, Lkv, H, D, seed=3, scale_kv=0.8)
+    q, k, v = bf16_to_f64(Q), bf16_to_f64(K), bf16_to_f64(V)
+    rb = lambda x: float(bf16_to_f64(bf16_round(np.array([x])))[0])  # noqa: E731
+    for act in (0, 1, 2):
+        got = o.flashnorm_attn_fwd(Q, K, V, act, 1e-3, 1e-2)
+        for t in range(Lq):
+            x = [q[0, t, h, d] for h in range(H) for d in range(D)]
+            n = len(x)
+            mu = sum(x) / n
+            var = sum((xi - mu) ** 2 for xi in x) / n
+            ln = [(xi - mu) / math.sqrt(var + 1e-3) for xi in x]
+            out_o = []
+            for h in range(H):
+                ps = []
+                for j in range(Lkv):
+                    sj = sum(rb(ln[h * D + d]) * k[0, j, h, d] for d in range(D))
+                    if act == 1:
+                        sj = 0.5 * sj * (1 + math.tanh(math.sqrt(2 / math.pi) * (sj + 0.044715 * sj ** 3)))
+                    elif act == 2:
+                        sj = sj / (1 + math.exp(-sj))
+                    ps.append(rb(sj))
+                for d in range(D):
+                    out_o.append(ln[h * D + d] + sum(ps[j] * v[0, j, h, d] for j in range(Lkv)))
+            r = 1 / math.sqrt(sum(z * z for z in out_o) / n + 1e-2)
+            want = [out_o[i] * r + x[i] for i in range(n)]
+            err = max(abs(got[0, t].reshape(-1)[i] - want[i]) for i in range(n))
+            assert err <= 1e-12, f"FlashNormAttention brute force (act {act}): {err}"
+
+
+def pin_fna_reductions(o):
+    """V = 0 leaves the two norms and residuals: out = RMSNorm(LayerNorm(q)) + q,
+    with both norms over all heads; permuting the heads of Q, K and V permutes
+    the output's heads; a jagged batch leaves rows past its length unwritten
+    and gives the dense result on the others."""
+    B, Lq, Lkv, H, D = 2, 6, 16, 4, 8
+    Q, K, V = _fna_case(B, Lq, Lkv, H, D, seed=11)
+    Z = bf16_round(np.zeros_like(bf16_to_f64(V)))
+    got = o.flashnorm_attn_fwd(Q, K, Z, 1, 1e-5, 1e-6)
+    rows = Q.reshape(B * Lq, H * D)
+    ln = o.norm_rows(rows, 0, 1e-5)[0]                     # LayerNorm over H*D (pinned above)
+    rms = ln / np.sqrt((ln * ln).mean(-1, keepdims=True) + 1e-6)
+    want = (rms + bf16_to_f64(rows)).reshape(B, Lq, H, D)
+    assert np.max(np.abs(got - want)) <= 1e-12, "V = 0"
+    perm = np.array([2, 0, 3, 1])
+    base = o.flashnorm_attn_fwd(Q, K, V, 2, 1e-5, 1e-6)
+    pq = np.ascontiguousarray(Q[:, :, perm, :])
+    pk = np.ascontiguousarray(K[:, :, perm, :])
+    pv = np.ascontiguousarray(V[:, :, perm, :])
+    assert np.max(np.abs(o.flashnorm_attn_fwd(pq, pk, pv, 2, 1e-5, 1e-6) - base[:, :, perm, :])) <= 1e-12, \
+        "head permutation"
+    jag = o.flashnorm_attn_fwd(Q, K, V, 2, 1e-5, 1e-6, q_len=[6, 2])
+    assert np.array_equal(jag[0], base[0]) and np.array_equal(jag[1, :2], base[1, :2])
+    assert np.isnan(jag[1, 2:]).all(), "rows past q_len are not written"
+
+
 PINS = [pin_bruteforce_plain, pin_bruteforce_prenorm, pin_bruteforce_postnorm,
         pin_bruteforce_norm_rows, pin_torch_f64, pin_lazy_identity, pin_invariants,
         pin_reductions, pin_power_of_two_scale, pin_row_subset, pin_closed_forms,
         pin_bruteforce_norm_bwd, pin_torch_autograd_bwd, pin_norm_bwd_invariants,
         pin_norm_bwd_reductions, pin_prenorm_bwd_bruteforce, pin_prenorm_bwd_autograd,
-        pin_prenorm_bwd_reductions, pin_residual_torch, pin_residual_reductions]
+        pin_prenorm_bwd_reductions, pin_residual_torch, pin_residual_reductions, pin_fna_torch,
+        pin_fna_bruteforce, pin_fna_reductions]
 
 
 def run_all(o):

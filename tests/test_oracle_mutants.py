@@ -74,6 +74,21 @@ MUTANTS = [
      "if (H_out) memcpy(H_out + r * N, h, sizeof(double) * (size_t)N);\n            for (int64_t j = 0; j < N; ++j) h[j] += bf16_to_double(ri[j]);"),
     ("res_rms_uses_ln", "rmsnorm_row(h, N, gamma, eps, Y + r * N, rstd_out ? rstd_out + r : NULL);",
      "layernorm_row(h, N, gamma, NULL, eps, Y + r * N, NULL, rstd_out ? rstd_out + r : NULL);"),
+    ("fna_no_residual1", "for (int64_t d = 0; d < D; ++d) o[h * D + d] = lh[d];    /* residual 1 */",
+     "for (int64_t d = 0; d < D; ++d) o[h * D + d] = 0.0;"),
+    ("fna_no_residual2", "for (int64_t k = 0; k < HD; ++k) out[k] += q[k];             /* residual 2 */", ""),
+    ("fna_ln_per_head", "layernorm_row(q, HD, NULL, NULL, eps1, ln, NULL, NULL);",
+     "for (int64_t h2 = 0; h2 < H; ++h2) layernorm_row(q + h2 * D, D, NULL, NULL, eps1, ln + h2 * D, NULL, NULL);"),
+    ("fna_rms_per_head", "rmsnorm_row(o, HD, NULL, eps2, out, NULL);",
+     "for (int64_t h2 = 0; h2 < H; ++h2) rmsnorm_row(o + h2 * D, D, NULL, eps2, out + h2 * D, NULL);"),
+    ("fna_wrong_k_head", "const uint16_t* kj = K + ((b * Lkv + j) * H + h) * D;",
+     "const uint16_t* kj = K + ((b * Lkv + j) * H + (h + 1) % H) * D;"),
+    ("fna_p_unrounded", "s[j] = round_bf16(activation(acc, act));", "s[j] = activation(acc, act);"),
+    ("fna_lnq_unrounded", "acc += round_bf16(lh[d]) * bf16_to_double(kj[d]);", "acc += lh[d] * bf16_to_double(kj[d]);"),
+    ("fna_gelu_coefficient", "(x + 0.044715 * x * x * x)", "(x + 0.04715 * x * x * x)"),
+    ("fna_silu_sign", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
+    ("fna_v_transposed", "const uint16_t* vj = V + ((b * Lkv + j) * H + h) * D;",
+     "const uint16_t* vj = V + ((b * Lkv + (j + 1) % Lkv) * H + h) * D;"),
 ]
 
 
