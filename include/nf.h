@@ -148,6 +148,37 @@ nf_status nf_gemm_postnorm_rms_res(const void* X, const void* W, const void* R,
                                    float* rstd_out, nf_stream stream);
 
 /*
+ * nf_flashnorm_attn_fwd -- FlashNormAttention forward (blog §4, the fused
+ * GDPA pseudocode over a short K/V sequence): for each batch b and query
+ * token t < q_len[b], with q = Q[b, t, :, :] (H heads x D):
+ *   ln_q = LayerNorm(q) over all H*D values (eps1, biased variance, no affine)
+ *   per head h:  p = act(ln_q[h] . K[b, :, h, :]^T)            (Lkv keys)
+ *                o[h] = p . V[b, :, h, :] + ln_q[h]            (residual 1)
+ *   Out[b, t] = RMSNorm(o) over all H*D values (eps2, no affine) + q
+ *                                                              (residual 2)
+ * The two matmuls run on tensor cores with bf16 operands: ln_q and p enter
+ * them rounded to bf16 (fp32 accumulation); the residuals and norms are fp32.
+ * act: NF_ACT_IDENTITY, NF_ACT_GELU_TANH (x/2 (1 + tanh(sqrt(2/pi)(x + 0.044715
+ * x^3)))) or NF_ACT_SILU (x / (1 + e^-x)); the pages name the activation
+ * elementwise without fixing it.
+ * Q, Out: [B, Lq, H, D]; K, V: [B, Lkv, H, D]; bf16 row-major device memory,
+ * 16-byte aligned.  q_len: device int32[B] (4-byte aligned) or NULL (Lq for
+ * every batch); rows t >= q_len[b] of Out are left as they were, except those
+ * inside the last 32-row group holding a valid row, which are written as 0.
+ * Supported: D = Lkv = 128, 1 <= H <= 8 (one thread-block cluster of H CTAs
+ * per batch exchanges the row statistics of both norms through distributed
+ * shared memory), Lq a multiple of 128; else NF_ERR_UNSUPPORTED_SHAPE.
+ */
+#define NF_ACT_IDENTITY 0
+#define NF_ACT_GELU_TANH 1
+#define NF_ACT_SILU 2
+nf_status nf_flashnorm_attn_fwd(const void* Q, const void* K, const void* V,
+                                const int32_t* q_len, void* Out, int64_t B,
+                                int64_t Lq, int64_t Lkv, int64_t H, int64_t D,
+                                int act, float eps1, float eps2,
+                                nf_stream stream);
+
+/*
  * nf_gemm_prenorm_rms_bwd -- backward of C = RMSNorm(A) * B (Lazy Pre-Norm,
  * no affine), from the rstd the forward saved (blog §2, limitation 3: the
  * backward rebuilds rmsnorm(A) from A and rstd).  With xhat = A * rstd_i:

@@ -159,3 +159,25 @@ def sample_rows(M: int, count: int, seed: int = 1, tile_m: int = 128) -> np.ndar
     extra = rng.integers(0, M, size=max(0, count - len(edges)))
     rows = np.unique(np.clip(np.array(edges + list(extra), dtype=np.int64), 0, M - 1))
     return rows
+
+
+# ---------------------------------------------------------------- attention inputs
+# FlashNormAttention (blog §4): Q [B, Lq, H, D] with jagged lengths, dense K / V
+# [B, Lkv, H, D].  The pages give the structure (K/V length exactly 128, head
+# dimension 128, batch 768, Q of average sparsity 0.5 and varied maximum
+# length) but no value distributions: Q ~ N(0, 1); K with variance 1/D and V
+# with variance 1/Lkv, so that scores and the attention output stay of order
+# one; q_len[b] uniform on [0, Lq] (half the positions empty on average).
+def fna_inputs(B: int, Lq: int, Lkv: int, H: int, D: int, seed: int = 0, jagged: bool = True):
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xF7A])))
+    Q = bf16_round(_normal(g, (B, Lq, H, D), 0.0, 1.0))
+    K = bf16_round(_normal(g, (B, Lkv, H, D), 0.0, 1.0 / D))
+    V = bf16_round(_normal(g, (B, Lkv, H, D), 0.0, 1.0 / Lkv))
+    q_len = (g.integers(0, Lq + 1, size=B) if jagged else np.full(B, Lq)).astype(np.int32)
+    return {"Q": Q, "K": K, "V": V, "q_len": q_len}
+
+
+# The attention workload of the blog's §4 benchmark shapes: batch 768, K/V
+# length 128, head dimension 128, 4 heads (H*D = 512), maximum query length 1024.
+FNA_WORKLOAD = {"name": "fna_768x1024x4x128", "B": 768, "Lq": 1024, "Lkv": 128, "H": 4, "D": 128,
+                "act": 1, "eps1": 1e-5, "eps2": 1e-6}

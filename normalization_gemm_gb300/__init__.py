@@ -70,6 +70,7 @@ _SIGS = {
     "nf_gemm_postnorm_rms": [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
     "nf_gemm_postnorm_ln_res": [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP, _VP],
     "nf_gemm_postnorm_rms_res": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _F, _VP, _VP],
+    "nf_flashnorm_attn_fwd": [_VP, _VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, ctypes.c_int, _F, _F, _VP],
     "nf_norm_rows_res": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
     "nf_norm_rows": [_VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _F, _VP, _VP, _VP],
     "nf_norm_rows_bwd": [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int, _VP],
@@ -327,6 +328,38 @@ def gemm_postnorm_rms_res(x, w, r, eps, gamma=None, out=None, h_out=None, rstd_o
                                           float(eps), _vec(rstd_out, "rstd_out", M, torch.float32),
                                           _stream(stream)), "nf_gemm_postnorm_rms_res")
     return y
+
+
+ACT_IDENTITY, ACT_GELU_TANH, ACT_SILU = 0, 1, 2
+
+
+def flashnorm_attn_fwd(q, k, v, act=ACT_GELU_TANH, eps1=1e-5, eps2=1e-6, q_len=None, out=None, stream=None):
+    """FlashNormAttention forward: q [B, Lq, H, D], k / v [B, Lkv, H, D] (bf16
+    CUDA tensors, D = Lkv = 128, H <= 8, Lq % 128 == 0); q_len: int32 CUDA
+    tensor [B] or None.  Returns out [B, Lq, H, D]."""
+    torch = _torch()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k and v must be 4-D [B, L, H, D]")
+    B, Lq, H, D = q.shape
+    Lkv = k.shape[1]
+    if tuple(k.shape) != (B, Lkv, H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, Lkv, H, D] with q's B, H, D")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if out is None:
+        out = torch.empty_like(q)
+    elif tuple(out.shape) != tuple(q.shape) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    ql = None
+    if q_len is not None:
+        if not q_len.is_cuda or q_len.dtype != torch.int32 or q_len.numel() != B or not q_len.is_contiguous():
+            raise TypeError("q_len must be a contiguous int32 CUDA tensor of B entries")
+        ql = q_len.data_ptr()
+    _check(lib().nf_flashnorm_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ql, out.data_ptr(), B, Lq,
+                                       Lkv, H, D, int(act), float(eps1), float(eps2), _stream(stream)),
+           "nf_flashnorm_attn_fwd")
+    return out
 
 
 def norm_rows_res(x, r, kind, eps, gamma=None, beta=None, out=None, h_out=None, mean_out=None,

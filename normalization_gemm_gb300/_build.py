@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libnf.so")
 SOURCES = ["nf_api.cu", "nf_norm.cu", "nf_gemm_plain.cu", "nf_gemm_pre.cu",
            "nf_gemm_post_ln.cu", "nf_gemm_post_rms.cu", "nf_gemm_bwd_ln.cu", "nf_gemm_bwd_rms.cu",
            "nf_gemm_trans_plain.cu", "nf_gemm_trans_bwd.cu", "nf_splitk.cu",
-           "nf_gemm_res_ln.cu", "nf_gemm_res_rms.cu"]
+           "nf_gemm_res_ln.cu", "nf_gemm_res_rms.cu", "nf_flashnorm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-ffp-contract=off", "-I", INCLUDE, "-I", CSRC]

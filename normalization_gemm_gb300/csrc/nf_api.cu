@@ -851,6 +851,45 @@ nf_status nf_gemm_postnorm_rms_res(const void* X, const void* W, const void* R, 
                     reinterpret_cast<cudaStream_t>(stream), false, nullptr, nullptr, nullptr, 0, nullptr, R, H);
 }
 
+nf_status nf_flashnorm_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* q_len, void* Out,
+                                int64_t B, int64_t Lq, int64_t Lkv, int64_t H, int64_t D, int act, float eps1,
+                                float eps2, nf_stream stream) {
+    if (B < 0 || Lq < 0 || H < 1) return fail(NF_ERR_INVALID_ARG, "need B >= 0, Lq >= 0, H >= 1");
+    if (act < NF_ACT_IDENTITY || act > NF_ACT_SILU) return fail(NF_ERR_INVALID_ARG, "act: identity, GELU or SiLU");
+    if (!(std::isfinite(eps1) && eps1 >= 0.0f && std::isfinite(eps2) && eps2 >= 0.0f))
+        return fail(NF_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (D != 128 || Lkv != 128) return fail(NF_ERR_UNSUPPORTED_SHAPE, "head dimension and K/V length must be 128");
+    if (H > 8) return fail(NF_ERR_UNSUPPORTED_SHAPE, "at most 8 heads (one cluster of H CTAs)");
+    if (Lq % 128 != 0) return fail(NF_ERR_UNSUPPORTED_SHAPE, "Lq must be a multiple of 128");
+    if (B * Lq > INT32_MAX || B * Lkv > INT32_MAX) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many rows");
+    if (B == 0 || Lq == 0) return NF_OK;
+    if (!Q || !K || !V || !Out) return fail(NF_ERR_INVALID_ARG, "Q, K, V and Out must be non-null");
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(Out, 16) || (q_len && !aligned(q_len, 4)))
+        return fail(NF_ERR_ALIGNMENT, "Q, K, V, Out must be 16-byte aligned, q_len 4-byte");
+    DeviceState* d = nullptr;
+    nf_status st = device_state(&d);
+    if (st != NF_OK) return st;
+    CUtensorMap maps[4];
+    const int64_t hd = H * 128;
+    if ((st = make_map(&maps[0], Q, B * Lq, hd, 64, 128)) != NF_OK) return st;
+    if ((st = make_map(&maps[1], K, B * Lkv, hd, 64, 128)) != NF_OK) return st;
+    if ((st = make_map(&maps[2], V, B * Lkv, hd, 64, 64)) != NF_OK) return st;
+    if ((st = make_map(&maps[3], Out, B * Lq, hd, 64, 32)) != NF_OK) return st;
+    FlashNormLaunch a;
+    a.q_len = q_len;
+    a.B = static_cast<int32_t>(B);
+    a.Lq = static_cast<int32_t>(Lq);
+    a.H = static_cast<int32_t>(H);
+    a.act = act;
+    a.eps1 = eps1;
+    a.eps2 = eps2;
+    a.status = d->status;
+    a.timeout_ns = g_timeout_ns;
+    cudaError_t e = launch_flashnorm_fwd(maps, a, g_overlap, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "FlashNormAttention launch");
+    return NF_OK;
+}
+
 nf_status nf_gemm_postnorm_rms(const void* X, const void* W, const void* gamma, void* Y, int64_t M, int64_t N,
                                int64_t K, float eps, float* rstd_out, nf_stream stream) {
     return run_gemm(OP_POST_RMS, X, W, gamma, nullptr, Y, M, N, K, eps, nullptr, rstd_out,

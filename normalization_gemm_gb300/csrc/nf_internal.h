@@ -245,6 +245,19 @@ cudaError_t launch_norm_rows_bwd(const NormBwdArgs& a, int kind, int sm_count, b
 // Largest supported cols.
 constexpr int NORM_MAX_COLS = 16384;
 
+// FlashNormAttention forward (nf_flashnorm.cu): head dimension and key /
+// value length 128, up to 8 heads (one cluster of H CTAs per batch).
+struct FlashNormLaunch {
+    const int32_t* q_len;  // B entries or null
+    int32_t B, Lq, H, act;
+    float eps1, eps2;
+    uint32_t* status;
+    uint64_t timeout_ns;
+};
+// tmaps: four CUtensorMap, Q / K / V / Out viewed as [rows, H * 128] bf16 with
+// the 128-byte swizzle and boxes {64, 128}, {64, 128}, {64, 64}, {64, 32}.
+cudaError_t launch_flashnorm_fwd(const void* tmaps, const FlashNormLaunch& a, bool overlap, cudaStream_t stream);
+
 // Split-K: for each split tile t = sk_base + i (i < sk_tiles), Y's tile
 // (TILE_M x tile_n at row tile t / n_tiles, column tile t % n_tiles) in bf16 =
 // the sum over `slices` of the fp32 partial tiles ws[s][i], added in slice

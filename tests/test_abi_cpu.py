@@ -55,6 +55,22 @@ def test_residual_argument_checks(L):
     assert L.nf_norm_rows_res(P, None, P, None, None, None, 0, 64, 0, 1e-5, None, None, None) == OK
 
 
+def test_flashnorm_argument_checks(L):
+    fn = L.nf_flashnorm_attn_fwd
+    # shapes outside the kernel: D, Lkv, H, Lq; activation and eps; empty batch; alignment
+    assert fn(P, P, P, None, P, 2, 256, 128, 4, 64, 1, 1e-5, 1e-6, None) == SHAPE
+    assert fn(P, P, P, None, P, 2, 256, 64, 4, 128, 1, 1e-5, 1e-6, None) == SHAPE
+    assert fn(P, P, P, None, P, 2, 256, 128, 9, 128, 1, 1e-5, 1e-6, None) == SHAPE
+    assert fn(P, P, P, None, P, 2, 200, 128, 4, 128, 1, 1e-5, 1e-6, None) == SHAPE
+    assert fn(P, P, P, None, P, 2, 256, 128, 4, 128, 3, 1e-5, 1e-6, None) == INVALID
+    assert fn(P, P, P, None, P, 2, 256, 128, 4, 128, 1, -1.0, 1e-6, None) == INVALID
+    assert fn(P, P, P, None, P, 2, 256, 128, 0, 128, 1, 1e-5, 1e-6, None) == INVALID
+    assert fn(P, P, P, None, P, 0, 256, 128, 4, 128, 1, 1e-5, 1e-6, None) == OK
+    assert fn(P + 8, P, P, None, P, 2, 256, 128, 4, 128, 1, 1e-5, 1e-6, None) == ALIGN
+    assert fn(P, P, P, P + 2, P, 2, 256, 128, 4, 128, 1, 1e-5, 1e-6, None) == ALIGN
+    assert fn(None, P, P, None, P, 2, 256, 128, 4, 128, 1, 1e-5, 1e-6, None) == INVALID
+
+
 def test_eps_must_be_finite_and_nonnegative(L):
     for eps in (float("nan"), float("inf"), -1e-6):
         assert L.nf_gemm_prenorm_rms(P, P, P, 128, 64, 64, eps, None, None) == INVALID

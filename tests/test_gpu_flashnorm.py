@@ -1,0 +1,106 @@
+"""Parity of the FlashNormAttention forward (blog "Towards Free Normalization",
+§4: LayerNorm over all heads, per-head act(ln_q K^T) V with two residuals,
+RMSNorm over all heads) through the C ABI with the fp64 oracle."""
+import numpy as np
+import pytest
+
+import nf_inputs
+import normalization_gemm_gb300 as nf
+from gpu_util import assert_close, require_gpu, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = require_gpu()
+    from normalization_gemm_gb300 import _build
+    _build.build()
+    nf.clear_device_status()
+    nf.set_wait_timeout_ns(250_000_000)
+    yield d
+    import torch
+    torch.cuda.synchronize()
+    status, detail = nf.device_status()
+    assert status == nf.NF_OK, f"device status word set: {detail}"
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    return oracle.get()
+
+
+def _dev4(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _run(dev, inp, act, jagged, sentinel=None):
+    import torch
+    q, k, v = _dev4(inp["Q"], dev), _dev4(inp["K"], dev), _dev4(inp["V"], dev)
+    ql = torch.from_numpy(inp["q_len"]).to(dev) if jagged else None
+    out = torch.full_like(q, float("nan") if sentinel is None else sentinel)
+    nf.flashnorm_attn_fwd(q, k, v, act=act, eps1=1e-5, eps2=1e-6, q_len=ql, out=out)
+    torch.cuda.synchronize()
+    return out
+
+
+def _valid_rows(got, want, q_len):
+    B, Lq, H, D = want.shape
+    rows = [(b, t) for b in range(B) for t in range(int(q_len[b]))]
+    if not rows:
+        return np.zeros((0, H * D)), np.zeros((0, H * D))
+    bi, ti = np.array(rows).T
+    return got[bi, ti].reshape(len(rows), H * D), want[bi, ti].reshape(len(rows), H * D)
+
+
+@pytest.mark.parametrize("B,Lq,H", [(1, 128, 1), (2, 256, 2), (3, 128, 4), (2, 384, 8), (4, 256, 3)])
+@pytest.mark.parametrize("act", [nf.ACT_GELU_TANH, nf.ACT_SILU, nf.ACT_IDENTITY], ids=["gelu", "silu", "identity"])
+@pytest.mark.parametrize("jagged", [False, True], ids=["dense", "jagged"])
+def test_flashnorm_fwd(dev, orc, B, Lq, H, act, jagged):
+    inp = nf_inputs.fna_inputs(B, Lq, 128, H, 128, seed=B * 100 + Lq + H, jagged=jagged)
+    out = _run(dev, inp, act, jagged)
+    want = orc.flashnorm_attn_fwd(inp["Q"], inp["K"], inp["V"], act, 1e-5, 1e-6,
+                                  q_len=inp["q_len"] if jagged else None)
+    got = to_f64(out.reshape(B * Lq, H * 128)).reshape(B, Lq, H, 128)
+    ql = inp["q_len"] if jagged else np.full(B, Lq)
+    g, w = _valid_rows(got, want, ql)
+    assert_close(g, w, f"FlashNormAttention B={B} Lq={Lq} H={H} act={act} jagged={jagged}")
+
+
+def test_flashnorm_padding_rows(dev, orc):
+    """Rows past q_len: those in the last 32-row group that holds a valid row
+    are written as zero, later ones keep the caller's content."""
+    import torch
+    B, Lq, H = 4, 256, 2
+    inp = nf_inputs.fna_inputs(B, Lq, 128, H, 128, seed=7)
+    inp["q_len"] = np.array([0, 1, 40, 256], np.int32)
+    out = _run(dev, inp, nf.ACT_GELU_TANH, True, sentinel=3.0)
+    o = out.float().cpu().numpy()
+    for b, n in enumerate(inp["q_len"]):
+        end = min(Lq, -(-int(n) // 32) * 32)
+        assert np.all(o[b, n:end] == 0.0), f"batch {b}: padded rows of the last group"
+        assert np.all(o[b, end:] == 3.0), f"batch {b}: rows past the last group untouched"
+    want = orc.flashnorm_attn_fwd(inp["Q"], inp["K"], inp["V"], 1, 1e-5, 1e-6, q_len=inp["q_len"])
+    got = to_f64(out.reshape(B * Lq, H * 128)).reshape(B, Lq, H, 128)
+    g, w = _valid_rows(got, want, inp["q_len"])
+    assert_close(g, w, "FlashNormAttention padding case")
+    assert torch.isfinite(out).all()
+
+
+def test_flashnorm_many_clusters(dev, orc):
+    """More clusters than fit at once (a batch per cluster of 4 CTAs), jagged,
+    on sampled batches against the oracle; repeated calls give the same bits."""
+    import torch
+    B, Lq, H = 160, 512, 4
+    inp = nf_inputs.fna_inputs(B, Lq, 128, H, 128, seed=3)
+    a = _run(dev, inp, nf.ACT_GELU_TANH, True)
+    b2 = _run(dev, inp, nf.ACT_GELU_TANH, True)
+    assert torch.equal(torch.nan_to_num(a, nan=7.0), torch.nan_to_num(b2, nan=7.0))
+    pick = np.array([0, 1, 57, 100, 159])
+    sub = {k: np.ascontiguousarray(inp[k][pick]) for k in ("Q", "K", "V", "q_len")}
+    want = orc.flashnorm_attn_fwd(sub["Q"], sub["K"], sub["V"], 1, 1e-5, 1e-6, q_len=sub["q_len"])
+    got = to_f64(a[torch.from_numpy(pick).to(dev)].reshape(len(pick) * Lq, H * 128)).reshape(len(pick), Lq, H, 128)
+    g, w = _valid_rows(got, want, sub["q_len"])
+    assert_close(g, w, "FlashNormAttention many clusters")
