@@ -353,6 +353,52 @@ def measure_residual(nf, w, kind, dev, stream, steps, warmup, seed=0, eager=Fals
     return out
 
 
+def measure_flashnorm(nf, dev, stream, steps, warmup, seed=0, eager=False, unfused=True, batch=None):
+    """FlashNormAttention forward on the blog §4 benchmark shapes (batch 768, K/V
+    length 128, head dimension 128, 4 heads, query length up to 1024 with
+    jagged lengths of average sparsity 0.5).  Returns times and the algorithmic
+    figures: each valid query row read once and written once, K and V read
+    once; flops of the two matmuls over the valid rows.  The comparison is the
+    same computation as torch eager ops (layer_norm, two bf16 einsums, the
+    activation, adds, rms_norm), dense over the padded rows."""
+    import torch
+    import torch.nn.functional as F
+    fw = nf_inputs.FNA_WORKLOAD
+    B, Lq, Lkv, H, D = fw["B"], fw["Lq"], fw["Lkv"], fw["H"], fw["D"]
+    B = batch or B
+    inp = nf_inputs.fna_inputs(B, Lq, Lkv, H, D, seed=seed)
+    dev4 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    q0, k, v = dev4(inp["Q"]), dev4(inp["K"]), dev4(inp["V"])
+    ql = torch.from_numpy(inp["q_len"]).to(dev)
+    rows = int(inp["q_len"].sum())
+    out0 = torch.empty_like(q0)
+    sets, nsets = make_sets([q0, out0], 4 * q0.numel(), dev)
+
+    def fused(i):
+        q, o = sets[i % nsets]
+        nf.flashnorm_attn_fwd(q, k, v, act=fw["act"], eps1=fw["eps1"], eps2=fw["eps2"], q_len=ql, out=o,
+                              stream=stream)
+
+    res = {"t_fused": time_steps(fused, steps, warmup, stream, eager=eager) / steps,
+           "bytes": 2 * rows * H * D * 2 + 2 * B * Lkv * H * D * 2,
+           "flops": 4 * rows * Lkv * D * H, "rows": rows}
+    if unfused:
+        def torch_step(i):
+            q, o = sets[i % nsets]
+            x = q.view(B, Lq, H * D)
+            ln = F.layer_norm(x.float(), (H * D,), eps=fw["eps1"]).to(torch.bfloat16).view(B, Lq, H, D)
+            s = torch.einsum("bthd,bjhd->bhtj", ln, k)
+            p = F.gelu(s.float(), approximate="tanh").to(torch.bfloat16)
+            h = torch.einsum("bhtj,bjhd->bthd", p, v).float() + ln.float()
+            y = F.rms_norm(h.reshape(B, Lq, H * D), (H * D,), eps=fw["eps2"]) + x.float()
+            o.copy_(y.view(B, Lq, H, D))
+        n = max(3, min(steps, 20))
+        res["t_torch"] = time_steps(torch_step, n, 3, stream, eager=True) / n
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
 def residual_bytes(w, kind):
     """Each tensor moved once: X, W and R read, Y and H written (+ gamma, beta)."""
     return (2 * w.M * w.K + 2 * w.K * w.N + 6 * w.M * w.N + (2 * w.N if w.gamma else 0)
@@ -620,6 +666,11 @@ def main(argv=None):
     ap.add_argument("--backward", choices=["post_ln", "post_rms", "pre_rms"], default=None,
                     help="time only this op's backward on the workload's shapes and print its figures "
                          "(a profiling aid; not the benchmark line)")
+    ap.add_argument("--flashnorm", action="store_true",
+                    help="time only the FlashNormAttention forward on its benchmark shapes and print its figures "
+                         "(a profiling aid; not the benchmark line)")
+    ap.add_argument("--fna-batch", type=int, default=None,
+                    help="with --flashnorm: batch size in place of the benchmark's 768 (small profiling cases)")
     ap.add_argument("--residual", choices=["post_ln", "post_rms"], default=None,
                     help="time only this op with a residual add on the workload's shapes and print its "
                          "figures (a profiling aid; not the benchmark line)")
@@ -657,6 +708,12 @@ def main(argv=None):
                                  args.warmup, eager=args.eager, unfused=not args.no_unfused)
         print(json.dumps({"backward": args.backward, "workload": w.name,
                           **{k: v * 1e6 for k, v in r.items() if k.startswith("t_")}}), flush=True)
+        return 0
+    if args.flashnorm:
+        r = measure_flashnorm(nf, dev, stream, args.steps, args.warmup, eager=args.eager,
+                              unfused=not args.no_unfused, batch=args.fna_batch)
+        print(json.dumps({"flashnorm": nf_inputs.FNA_WORKLOAD["name"],
+                          **{k: (v * 1e6 if k.startswith("t_") else v) for k, v in r.items()}}), flush=True)
         return 0
     if args.residual:
         w = nf_inputs.WORKLOADS[args.workload]
@@ -813,6 +870,19 @@ def main(argv=None):
                     })
                     del r
                     torch.cuda.empty_cache()
+            # FlashNormAttention forward on the blog §4 benchmark shapes
+            r = measure_flashnorm(nf, dev, stream, 50, 5)
+            tr = max(r["flops"] / (bf16_tf * 1e12), r["bytes"] / (hbm_gbs * 1e9))
+            table.append({
+                "workload": nf_inputs.FNA_WORKLOAD["name"], "op": "flashnorm_attn_fwd",
+                "t_fused_us": r["t_fused"] * 1e6, "tflops": r["flops"] / r["t_fused"] / 1e12,
+                "roofline_frac": tr / r["t_fused"],
+                "bound": "tensor" if r["flops"] / (bf16_tf * 1e12) > r["bytes"] / (hbm_gbs * 1e9) else "hbm",
+                "hbm_gbs": r["bytes"] / r["t_fused"] / 1e9, "t_torch_eager_us": r["t_torch"] * 1e6,
+                "valid_rows": r["rows"],
+            })
+            del r
+            torch.cuda.empty_cache()
             line["configs"] = table
         if not args.no_cpu and world == 1:
             cap = max(1, int(2e10 // (2 * w.N * w.K)))   # about 20 GFLOP per pass

@@ -15,17 +15,26 @@
 // one head each); each CTA keeps its head's K and V in shared memory and walks
 // the batch's 128-row query tiles (ceil(q_len[b] / 128) of them).
 //
-// CTA roles (192 threads):
-//   warps 0-3  compute, one query row per thread (TMEM lane = row): the
-//              LayerNorm (partial statistics over the CTA's 128 columns, pushed
-//              to every CTA of the cluster with st.async, merged), writes
-//              bf16(ln_q) as the first MMA's A operand and ln_q in fp32 into
-//              the O accumulator (so residual 1 is the MMA's accumulate), the
-//              activation of S into P (the second MMA's A operand), then the
-//              RMSNorm of O (second exchange) and out = o * rstd + q, staged
-//              over the q tile in shared memory and stored with TMA.
-//   warp 4     TMA producer: K and V once, the q tiles into two buffers.
-//   warp 5     MMA issuer: S = ln_q K^T and O += P V (tcgen05.mma, M = N = 128).
+// CTA roles, NG compute groups (NG = 2 for H <= 4, 1 above: shared memory):
+//   warps 4g..4g+3  compute group g, tiles g, g + NG, ...; one query row per
+//              thread (TMEM lane = row): the LayerNorm (partial statistics over
+//              the CTA's 128 columns, pushed to every CTA of the cluster with
+//              st.async, merged), bf16(ln_q) as the first MMA's A operand and
+//              ln_q in fp32 into the O accumulator (residual 1 through the
+//              MMA's accumulate), the activation of S into P (the second MMA's
+//              A operand), the RMSNorm of O (second exchange) and
+//              out = o * rstd + q, staged over the q tile and stored with TMA.
+//              Two groups overlap one tile's exchanges and MMAs with the other
+//              tile's CUDA-core work.
+//   warp 4NG   TMA producer: K and V once, the q tiles into two buffers (tile
+//              it into buffer it & 1, which with two groups is group it & 1's).
+//   warp 4NG+1+g  MMA issuer of group g: S = ln_q K^T and O += P V
+//              (tcgen05.mma, M = N = 128) into the group's 256 TMEM columns.
+//
+// Exchange slots: tile it uses slot it mod 2NG of each exchange.  A peer sends
+// tile it + 2NG's partials (the same slot) only after it received every CTA's
+// partials of tile it + NG, the same group's next tile, which this CTA sends
+// after it has read slot it: a slot is never overwritten before it is read.
 //
 // Every wait is bounded; on expiry the kernel records NF_ERR_TIMEOUT with the
 // site in the device status word, drains what it issued and returns.
@@ -35,27 +44,44 @@
 namespace nf {
 namespace {
 
-constexpr int FN_D = 128;                  // head dimension
-constexpr int FN_LKV = 128;                // key / value length
-constexpr int FN_ROWS = 128;               // query rows per tile
-constexpr int FN_MAXH = 8;                 // heads per cluster (portable cluster size)
-constexpr int FN_THREADS = 192;
-constexpr int FN_PRODUCER_WARP = 4;
-constexpr int FN_MMA_WARP = 5;
+constexpr int FN_D = 128;                          // head dimension
+constexpr int FN_LKV = 128;                        // key / value length
+constexpr int FN_ROWS = 128;                       // query rows per tile
 constexpr int FN_TILE_BYTES = FN_ROWS * FN_D * 2;  // 32 KB: a 128 x 128 bf16 tile
 constexpr int FN_HALF_BYTES = FN_TILE_BYTES / 2;   // one 64-column box of 128 rows
-constexpr int FN_RECV_BYTES = 2 * FN_MAXH * FN_ROWS * 8;  // [parity][cluster rank][row] float2
 
-// Shared-memory layout (1 KB aligned base).
-constexpr int FN_OFF_K = 0;                                  // K: 2 boxes of 128 keys x 64 d
-constexpr int FN_OFF_V = FN_OFF_K + FN_TILE_BYTES;           // V: 2 K-tiles x 2 boxes of 64 keys x 64 d
-constexpr int FN_OFF_Q = FN_OFF_V + FN_TILE_BYTES;           // q tiles [2], later the output staging
-constexpr int FN_OFF_A = FN_OFF_Q + 2 * FN_TILE_BYTES;       // bf16(ln_q), then P
-constexpr int FN_OFF_R1 = FN_OFF_A + FN_TILE_BYTES;          // LayerNorm partials received
-constexpr int FN_OFF_R2 = FN_OFF_R1 + FN_RECV_BYTES;         // RMSNorm partials received
-constexpr int FN_OFF_BAR = FN_OFF_R2 + FN_RECV_BYTES;
-constexpr int FN_SMEM_BYTES = FN_OFF_BAR + 256 + 1024;       // barriers + words, 1 KB realignment slack
-static_assert(FN_SMEM_BYTES <= SMEM_OPTIN_LIMIT, "shared memory");
+template <int NG>
+struct FnCfg {
+    static constexpr int MAXH = NG == 2 ? 4 : 8;   // heads per cluster
+    static constexpr int NSLOT = 2 * NG;           // exchange slots
+    static constexpr int THREADS = (4 * NG + 1 + NG) * 32;
+    static constexpr int PRODUCER_WARP = 4 * NG;
+    static constexpr int MMA_WARP0 = 4 * NG + 1;
+    static constexpr int RECV_BYTES = NSLOT * MAXH * FN_ROWS * 8;  // [slot][cluster rank][row] float2
+    // Shared-memory layout (1 KB aligned base).
+    static constexpr int OFF_K = 0;                               // K: 2 boxes of 128 keys x 64 d
+    static constexpr int OFF_V = OFF_K + FN_TILE_BYTES;           // V: 2 K-tiles x 2 boxes of 64 keys x 64 d
+    static constexpr int OFF_Q = OFF_V + FN_TILE_BYTES;           // q tiles [2], later the output staging
+    static constexpr int OFF_A = OFF_Q + 2 * FN_TILE_BYTES;       // [NG] bf16(ln_q), then P
+    static constexpr int OFF_R1 = OFF_A + NG * FN_TILE_BYTES;     // LayerNorm partials received
+    static constexpr int OFF_R2 = OFF_R1 + RECV_BYTES;            // RMSNorm partials received
+    static constexpr int OFF_BAR = OFF_R2 + RECV_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;       // barriers + words, 1 KB realignment slack
+    static_assert(SMEM_BYTES <= SMEM_OPTIN_LIMIT, "shared memory");
+    // barriers (8 bytes each): kv, qfull[2], qempty[2], GROUP_BARS per group
+    // (below), x1[NSLOT], x2[NSLOT]
+    static constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_GROUP = 5, GROUP_BARS = 8,
+                         B_X1 = B_GROUP + GROUP_BARS * NG, B_X2 = B_X1 + NSLOT, NBAR = B_X2 + NSLOT;
+    static_assert(NBAR * 8 <= 240, "barrier area");
+    static constexpr int OFF_TMEM_HOLDER = 240, OFF_ABORT = 244;
+    static constexpr int TMEM_COLS = 256 * NG;     // per group: S 128 columns, O 128
+};
+
+// A group's barriers, by offset from its first: the two halves of the
+// contraction of S (ln_q columns 0-63 / 64-127 written), the two 64-key halves
+// of S (computed), the two 64-key halves of P (written), O (computed) and the
+// MMA warp's final drain.
+constexpr int G_AREADY = 0, G_SFULL = 2, G_PREADY = 4, G_OFULL = 6, G_MMA_DONE = 7;
 
 enum FnSite : uint32_t {
     FN_SITE_KV = 20, FN_SITE_QFULL = 21, FN_SITE_QEMPTY = 22, FN_SITE_AREADY = 23, FN_SITE_SFULL = 24,
@@ -72,16 +98,55 @@ struct FnArgs {
     uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ float fn_act(float x, int act) {
-    if (act == 1) return 0.5f * x * (1.0f + tanhf(0.7978845608028654f * fmaf(0.044715f * x, x * x, x)));
-    if (act == 2) return x / (1.0f + expf(-x));
-    return x;
+// Hardware tanh (MUFU, about 2^-11 relative error: below the bf16 rounding
+// that P gets before the second MMA).
+__device__ __forceinline__ float fn_tanh(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// P = bf16(act(s)) for two S values held as 32-bit words, in packed fp32 pairs:
+//   GELU (tanh form)  h + h tanh(u),  h = s / 2,  u = sqrt(2 / pi) (s + 0.044715 s^3)
+//   SiLU              h + h tanh(h),  h = s / 2   (s sigmoid(s), written with tanh)
+//   identity          s
+template <int ACT>
+__device__ __forceinline__ uint32_t fn_act_pack(uint32_t s0, uint32_t s1) {
+    const uint64_t x = f2_pack(s0, s1);
+    if (ACT == 0) return pack_bf16x2(__uint_as_float(s0), __uint_as_float(s1));
+    const uint64_t h = f2_mul(x, f2_splat(0.5f));
+    uint64_t u = h;
+    if (ACT == 1) {
+        constexpr float K0 = 0.7978845608028654f, K1 = 0.7978845608028654f * 0.044715f;
+        u = f2_mul(x, f2_fma(f2_mul(x, x), f2_splat(K1), f2_splat(K0)));
+    }
+    float u0, u1;
+    f2_unpack(u, u0, u1);
+    const uint64_t th = f2_pack(__float_as_uint(fn_tanh(u0)), __float_as_uint(fn_tanh(u1)));
+    return f2_to_bf16x2(f2_fma(h, th, h));
 }
 
 // Address of 16-byte chunk c (0..15, 8 columns each) of row r in a 128-row,
 // 128-column bf16 tile held as two 64-column boxes with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t fn_chunk(uint32_t base, int r, int c) {
     return base + static_cast<uint32_t>((c >> 3) * FN_HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// The activation of one 64-key half of S (TMEM columns ts .. ts + 63 of this
+// thread's row) into the matching 64-column box of the A tile at sA.
+template <int ACT>
+__device__ __forceinline__ void fn_act_half(uint32_t ts, uint32_t sA, int r, int half) {
+    uint32_t v0[32], v1[32];
+    tmem_ld32(ts, v0);
+    tmem_ld32(ts + 32u, v1);
+    tmem_ld_wait(v0);
+    tmem_ld_wait(v1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t* v = k < 4 ? v0 + k * 8 : v1 + (k - 4) * 8;
+        st_shared_v4(fn_chunk(sA, r, half * 8 + k), fn_act_pack<ACT>(v[0], v[1]), fn_act_pack<ACT>(v[2], v[3]),
+                     fn_act_pack<ACT>(v[4], v[5]), fn_act_pack<ACT>(v[6], v[7]));
+    }
 }
 
 __device__ __forceinline__ uint32_t fn_cluster_id() {
@@ -98,28 +163,21 @@ __device__ __forceinline__ void fn_drain(uint32_t bar, uint32_t parity, uint64_t
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
-__global__ void __launch_bounds__(FN_THREADS, 1)
+template <int NG>
+__global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
     nf_flashnorm_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                             const FnArgs args) {
+    using C = FnCfg<NG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
-    const uint32_t sK = base + FN_OFF_K, sV = base + FN_OFF_V, sQ = base + FN_OFF_Q, sA = base + FN_OFF_A;
-    const uint32_t sR1 = base + FN_OFF_R1, sR2 = base + FN_OFF_R2, sBar = base + FN_OFF_BAR;
-    const uint32_t bar_kv = sBar;               // K and V landed
-    const uint32_t bar_qfull0 = sBar + 8;       // [2] q tile landed
-    const uint32_t bar_qempty0 = sBar + 24;     // [2] q buffer free (its output store has read it)
-    const uint32_t bar_aready = sBar + 40;      // bf16(ln_q) in sA and ln_q in O's TMEM columns
-    const uint32_t bar_sfull = sBar + 48;       // S = ln_q K^T in TMEM
-    const uint32_t bar_pready = sBar + 56;      // P in sA
-    const uint32_t bar_ofull = sBar + 64;       // O = ln_q + P V in TMEM
-    const uint32_t bar_x1 = sBar + 72;          // [2] LayerNorm partials of the cluster arrived
-    const uint32_t bar_x2 = sBar + 88;          // [2] RMSNorm partials of the cluster arrived
-    const uint32_t bar_mma_done = sBar + 104;
-    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + FN_OFF_BAR + 128);
-    volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + FN_OFF_BAR + 132);
+    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQ = base + C::OFF_Q, sA0 = base + C::OFF_A;
+    const uint32_t sR1 = base + C::OFF_R1, sR2 = base + C::OFF_R2, sBar = base + C::OFF_BAR;
+    auto bar = [&](int slot) { return sBar + 8u * static_cast<uint32_t>(slot); };
+    uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::OFF_BAR + C::OFF_TMEM_HOLDER);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::OFF_BAR + C::OFF_ABORT);
 
     const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
     const int H = args.H;
@@ -133,23 +191,30 @@ __global__ void __launch_bounds__(FN_THREADS, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmO);
-        mbar_init(bar_kv, 1);
+        mbar_init(bar(C::B_KV), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_qfull0 + 8u * i, 1);
-            mbar_init(bar_qempty0 + 8u * i, 4);  // one arrival per compute warp
-            mbar_init(bar_x1 + 8u * i, 1);
-            mbar_init(bar_x2 + 8u * i, 1);
+            mbar_init(bar(C::B_QFULL + i), 1);
+            mbar_init(bar(C::B_QEMPTY + i), 4);  // one arrival per warp of the group using the buffer
         }
-        mbar_init(bar_aready, 128);
-        mbar_init(bar_sfull, 1);
-        mbar_init(bar_pready, 128);
-        mbar_init(bar_ofull, 1);
-        mbar_init(bar_mma_done, 1);
+        for (int g = 0; g < NG; ++g) {
+            const int b0 = C::B_GROUP + g * C::GROUP_BARS;
+            for (int h = 0; h < 2; ++h) {
+                mbar_init(bar(b0 + G_AREADY + h), 128);  // every thread of the group
+                mbar_init(bar(b0 + G_SFULL + h), 1);     // an MMA commit
+                mbar_init(bar(b0 + G_PREADY + h), 128);
+            }
+            mbar_init(bar(b0 + G_OFULL), 1);
+            mbar_init(bar(b0 + G_MMA_DONE), 1);
+        }
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(bar(C::B_X1 + s), 1);
+            mbar_init(bar(C::B_X2 + s), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == FN_PRODUCER_WARP) {
-        tmem_alloc(smem_u32(tmem_holder), 256);  // S: columns 0-127, O: 128-255
+    if (warp == C::PRODUCER_WARP) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
         tmem_relinquish();
     }
     // Global memory (q_len included) is read only after the preceding grid.
@@ -158,11 +223,11 @@ __global__ void __launch_bounds__(FN_THREADS, 1)
     const int qlen = args.q_len ? min(max(args.q_len[bidx], 0), args.Lq) : args.Lq;
     const int tiles = (qlen + FN_ROWS - 1) / FN_ROWS;  // the same for every CTA of the cluster
     if (threadIdx.x == 0) {
-        // Arm the exchange barriers of tiles 0 and 1 before any peer can send
-        // (peers send only after the cluster barrier below).
-        for (int i = 0; i < 2 && i < tiles; ++i) {
-            mbar_arrive_expect_tx(bar_x1 + 8u * i, xbytes);
-            mbar_arrive_expect_tx(bar_x2 + 8u * i, xbytes);
+        // Arm the exchange barriers of the first NSLOT tiles before any peer
+        // can send (peers send only after the cluster barrier below).
+        for (int s = 0; s < C::NSLOT && s < tiles; ++s) {
+            mbar_arrive_expect_tx(bar(C::B_X1 + s), xbytes);
+            mbar_arrive_expect_tx(bar(C::B_X2 + s), xbytes);
         }
     }
     tc_fence_before();
@@ -174,115 +239,158 @@ __global__ void __launch_bounds__(FN_THREADS, 1)
     const int64_t qrow0 = static_cast<int64_t>(bidx) * args.Lq;  // the batch's first row in Q / Out
     const int col0 = rank * FN_D;                                 // this head's first column
 
-    if (warp == FN_PRODUCER_WARP) {
+    if (warp == C::PRODUCER_WARP) {
         // ======================================================== TMA producer
         if (lane == 0 && tiles > 0) {
-            mbar_arrive_expect_tx(bar_kv, 2 * FN_TILE_BYTES);
+            mbar_arrive_expect_tx(bar(C::B_KV), 2 * FN_TILE_BYTES);
             const int krow = bidx * FN_LKV;
             for (int kt = 0; kt < 2; ++kt) {
                 // K: 128 keys x 64 d (K-major B of S); V: 64 keys x 64 d boxes (MN-major B of O)
-                tma_load_2d(sK + kt * FN_HALF_BYTES, &tmK, bar_kv, col0 + kt * 64, krow);
+                tma_load_2d(sK + kt * FN_HALF_BYTES, &tmK, bar(C::B_KV), col0 + kt * 64, krow);
                 for (int i = 0; i < 2; ++i)
-                    tma_load_2d(sV + kt * FN_HALF_BYTES + i * (FN_HALF_BYTES / 2), &tmV, bar_kv, col0 + i * 64,
-                                krow + kt * 64);
+                    tma_load_2d(sV + kt * FN_HALF_BYTES + i * (FN_HALF_BYTES / 2), &tmV, bar(C::B_KV),
+                                col0 + i * 64, krow + kt * 64);
             }
             for (int it = 0; it < tiles; ++it) {
                 const int qb = it & 1;
                 const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
-                if (!mbar_wait(guard, bar_qempty0 + 8u * qb, ph ^ 1u, FN_SITE_QEMPTY, it)) break;
-                const uint32_t fb = bar_qfull0 + 8u * qb;
+                if (!mbar_wait(guard, bar(C::B_QEMPTY + qb), ph ^ 1u, FN_SITE_QEMPTY, it)) break;
+                const uint32_t fb = bar(C::B_QFULL + qb);
                 mbar_arrive_expect_tx(fb, FN_TILE_BYTES);
                 for (int half = 0; half < 2; ++half)
                     tma_load_2d(sQ + qb * FN_TILE_BYTES + half * FN_HALF_BYTES, &tmQ, fb, col0 + half * 64,
                                 static_cast<int32_t>(qrow0 + it * FN_ROWS));
             }
             // Every load issued has landed before the CTA may exit.
-            fn_drain(bar_kv, 0, args.timeout_ns);
+            fn_drain(bar(C::B_KV), 0, args.timeout_ns);
             for (int j = 0; j < 2 && j < tiles; ++j) {
                 const int last = j + ((tiles - 1 - j) / 2) * 2;  // the last tile that used buffer j
-                fn_drain(bar_qfull0 + 8u * j, static_cast<uint32_t>(last >> 1) & 1u, args.timeout_ns);
+                fn_drain(bar(C::B_QFULL + j), static_cast<uint32_t>(last >> 1) & 1u, args.timeout_ns);
             }
         }
         __syncwarp();
-    } else if (warp == FN_MMA_WARP) {
-        // ======================================================== MMA issuer
-        if (lane == 0 && tiles > 0) {
-            constexpr uint32_t IDESC_S = idesc_bf16_f32(FN_ROWS, FN_LKV, false);  // B = K (K-major)
-            constexpr uint32_t IDESC_O = idesc_bf16_f32(FN_ROWS, FN_D, true);     // B = V (MN-major)
-            const uint32_t tS = tmem_base, tO = tmem_base + 128u;
-            bool ok = mbar_wait(guard, bar_kv, 0, FN_SITE_KV, 0);
-            for (int it = 0; it < tiles && ok; ++it) {
-                const uint32_t ph = static_cast<uint32_t>(it) & 1u;
-                if (!(ok = mbar_wait(guard, bar_aready, ph, FN_SITE_AREADY, it))) break;
+    } else if (warp >= C::MMA_WARP0) {
+        // ======================================================== MMA issuer of group g
+        const int g = warp - C::MMA_WARP0;
+        const int b0 = C::B_GROUP + g * C::GROUP_BARS;
+        if (lane == 0 && g < tiles) {
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(FN_ROWS, FN_LKV / 2, false);  // B = K (K-major), 64 keys
+            constexpr uint32_t IDESC_O = idesc_bf16_f32(FN_ROWS, FN_D, true);         // B = V (MN-major)
+            const uint32_t tS = tmem_base + static_cast<uint32_t>(g * 256), tO = tS + 128u;
+            const uint32_t sA = sA0 + static_cast<uint32_t>(g * FN_TILE_BYTES);
+            // S half n (keys 64n..64n+63) += ln_q[:, 64kt..] K[64n.., 64kt..]^T
+            auto mma_s = [&](int n, int kt) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_bf16(tS + static_cast<uint32_t>(n * 64), smem_desc_sw128(sA + kt * FN_HALF_BYTES + j * 32, 16, 1024),
+                             smem_desc_sw128(sK + kt * FN_HALF_BYTES + n * (FN_HALF_BYTES / 2) + j * 32, 16, 1024),
+                             IDESC_S, (kt | j) != 0 ? 1u : 0u);
+            };
+            bool ok = mbar_wait(guard, bar(C::B_KV), 0, FN_SITE_KV, 0);
+            for (int it = g; it < tiles && ok; it += NG) {
+                const uint32_t ph = static_cast<uint32_t>(it / NG) & 1u;
+                // ln_q columns 0-63 written: the first half of both S halves' contraction
+                if (!(ok = mbar_wait(guard, bar(b0 + G_AREADY), ph, FN_SITE_AREADY, it))) break;
                 tc_fence_after();
-                for (int kt = 0; kt < 2; ++kt)
+                mma_s(0, 0);
+                mma_s(1, 0);
+                if (!(ok = mbar_wait(guard, bar(b0 + G_AREADY + 1), ph, FN_SITE_AREADY, it))) break;
+                tc_fence_after();
+                mma_s(0, 1);
+                mma_commit(bar(b0 + G_SFULL));      // keys 0-63 done (and every read of ln_q's columns 0-63)
+                mma_s(1, 1);
+                mma_commit(bar(b0 + G_SFULL + 1));  // keys 64-127 done
+                // O already holds ln_q: every step accumulates.  P's keys 0-63 first.
+                for (int kt = 0; kt < 2; ++kt) {
+                    if (!(ok = mbar_wait(guard, bar(b0 + G_PREADY + kt), ph, FN_SITE_PREADY, it))) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        mma_bf16(tS, smem_desc_sw128(sA + kt * FN_HALF_BYTES + j * 32, 16, 1024),
-                                 smem_desc_sw128(sK + kt * FN_HALF_BYTES + j * 32, 16, 1024), IDESC_S,
-                                 (kt | j) != 0 ? 1u : 0u);
-                mma_commit(bar_sfull);
-                if (!(ok = mbar_wait(guard, bar_pready, ph, FN_SITE_PREADY, it))) break;
-                tc_fence_after();
-                for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)  // O already holds ln_q: accumulate from the first step
                         mma_bf16(tO, smem_desc_sw128(sA + kt * FN_HALF_BYTES + j * 32, 16, 1024),
                                  smem_desc_sw128(sV + kt * FN_HALF_BYTES + j * 2048, FN_HALF_BYTES / 2, 1024),
                                  IDESC_O, 1u);
-                mma_commit(bar_ofull);
+                }
+                if (!ok) break;
+                mma_commit(bar(b0 + G_OFULL));
             }
-            mma_commit(bar_mma_done);
-            fn_drain(bar_mma_done, 0, args.timeout_ns);
+            mma_commit(bar(b0 + G_MMA_DONE));
+            fn_drain(bar(b0 + G_MMA_DONE), 0, args.timeout_ns);
         }
         __syncwarp();
     } else {
-        // ======================================================== compute warps 0-3
-        const int r = warp * 32 + lane;  // tile row == TMEM lane
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
+        // ======================================================== compute group g (warps 4g..4g+3)
+        const int g = warp >> 2, gw = warp & 3;
+        const int r = gw * 32 + lane;  // tile row == TMEM lane
+        const int b0 = C::B_GROUP + g * C::GROUP_BARS;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(gw * 32) << 16) + static_cast<uint32_t>(g * 256);
         const uint32_t tS = t_lane, tO = t_lane + 128u;
-        for (int it = 0; it < tiles; ++it) {
+        const uint32_t sA = sA0 + static_cast<uint32_t>(g * FN_TILE_BYTES);
+        for (int it = g; it < tiles; it += NG) {
             const int qb = it & 1;
-            const uint32_t ph = static_cast<uint32_t>(it) & 1u, qph = static_cast<uint32_t>(it >> 1) & 1u;
+            const uint32_t qph = static_cast<uint32_t>(it >> 1) & 1u;     // q buffer use count parity
+            const uint32_t gph = static_cast<uint32_t>(it / NG) & 1u;     // this group's tile count parity
+            const int slot = it % C::NSLOT;
+            const uint32_t xph = static_cast<uint32_t>(it / C::NSLOT) & 1u;
             const int m0 = it * FN_ROWS;
-            const bool valid = m0 + r < qlen;
             const uint32_t sq = sQ + static_cast<uint32_t>(qb * FN_TILE_BYTES);
-            bool ok = mbar_wait(guard, bar_qfull0 + 8u * qb, qph, FN_SITE_QFULL, it);
+            if (NG == 2 && it >= NG && lane == 0) {
+                // This group's previous tile used the same q buffer: once its
+                // output stores have read it, the producer may load this tile.
+                bulk_wait_read<0>();
+                mbar_arrive(bar(C::B_QEMPTY + qb));
+            }
+            bool ok = mbar_wait(guard, bar(C::B_QFULL + qb), qph, FN_SITE_QFULL, it);
             if (!__all_sync(0xffffffffu, ok)) break;
-
-            // ---- LayerNorm: partial (mean, M2) over this CTA's 128 columns,
-            //      sums shifted by the row's first value; rows past q_len are zero.
-            float sh, a1 = 0.0f, a2 = 0.0f;
-            {
-                const uint4 w = ld_shared_v4(fn_chunk(sq, r, 0));
-                sh = valid ? bf16lo(w.x) : 0.0f;
-            }
-#pragma unroll 4
-            for (int c = 0; c < 16; ++c) {
-                const uint4 w = ld_shared_v4(fn_chunk(sq, r, c));
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            if (m0 + r >= qlen) {
+                // A row past q_len: zero it once, so that every later step gives
+                // exactly 0 for it, whatever the caller's buffer holds there.
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float d0 = (valid ? bf16lo(ww[e]) : 0.0f) - sh, d1 = (valid ? bf16hi(ww[e]) : 0.0f) - sh;
-                    a1 += d0 + d1;
-                    a2 = fmaf(d0, d0, fmaf(d1, d1, a2));
-                }
+                for (int c = 0; c < 16; ++c) st_shared_v4(fn_chunk(sq, r, c), 0u, 0u, 0u, 0u);
             }
-            const float mean_c = sh + a1 * (1.0f / FN_D);
-            const float m2_c = fmaxf(fmaf(-a1, a1 * (1.0f / FN_D), a2), 0.0f);
-            const int xp = it & 1;
+
+            // ---- LayerNorm: partial (mean, M2) over this CTA's 128 columns, the
+            //      sums shifted by the row's first value, in packed fp32 pairs.
+            float mean_c, m2_c;
             {
-                // push to slot [rank] of every CTA of the cluster, wait for all H slots
-                const uint32_t x1 = bar_x1 + 8u * xp;
-                const uint32_t slot = sR1 + static_cast<uint32_t>(((xp * FN_MAXH + rank) * FN_ROWS + r) * 8);
-                for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(slot, p), mean_c, m2_c, mapa_shared(x1, p));
-                ok = mbar_wait<true>(guard, x1, qph, FN_SITE_X1, it);
-                if (!__all_sync(0xffffffffu, ok)) break;
-                // Re-arm for tile it + 2: its partials can arrive only after every
-                // CTA got this CTA's tile it + 1 partials, sent after this point.
-                if (warp == 0 && lane == 0 && it + 2 < tiles) mbar_arrive_expect_tx(x1, xbytes);
+                const float sh = bf16lo(ld_shared_v4(fn_chunk(sq, r, 0)).x);
+                const uint64_t nsh = f2_splat(-sh);
+                uint64_t s1a = 0, s1b = 0, s2a = 0, s2b = 0;  // (0.0f, 0.0f)
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    const uint4 w0 = ld_shared_v4(fn_chunk(sq, r, c)), w1 = ld_shared_v4(fn_chunk(sq, r, c + 1));
+                    const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const uint64_t d0 = f2_add(bf16x2_to_f2(ww[e]), nsh);
+                        const uint64_t d1 = f2_add(bf16x2_to_f2(ww[e + 1]), nsh);
+                        s1a = f2_add(s1a, d0);
+                        s2a = f2_fma(d0, d0, s2a);
+                        s1b = f2_add(s1b, d1);
+                        s2b = f2_fma(d1, d1, s2b);
+                    }
+                }
+                const float a1 = f2_hsum(f2_add(s1a, s1b)), a2 = f2_hsum(f2_add(s2a, s2b));
+                mean_c = sh + a1 * (1.0f / FN_D);
+                m2_c = fmaxf(fmaf(-a1, a1 * (1.0f / FN_D), a2), 0.0f);
             }
-            const float* rv1 = reinterpret_cast<const float*>(base_ptr + FN_OFF_R1 + (xp * FN_MAXH * FN_ROWS + r) * 8);
+            {
+                // push to slot [rank] of every CTA of the cluster, wait for all H
+                const uint32_t xb = bar(C::B_X1 + slot);
+                const uint32_t dst = sR1 + static_cast<uint32_t>(((slot * C::MAXH + rank) * FN_ROWS + r) * 8);
+                for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(dst, p), mean_c, m2_c, mapa_shared(xb, p));
+                ok = mbar_wait<true>(guard, xb, xph, FN_SITE_X1, it);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                if (gw == 0 && lane == 0 && it + C::NSLOT < tiles) mbar_arrive_expect_tx(xb, xbytes);
+            }
+            if (NG == 1 && it > 0 && lane == 0) {
+                // The previous tile's output stores have read its q buffer by
+                // now: hand it to the producer, which loads tile it + 1 into it
+                // while this tile finishes.
+                bulk_wait_read<0>();
+                mbar_arrive(bar(C::B_QEMPTY + (qb ^ 1)));
+            }
+            const float* rv1 =
+                reinterpret_cast<const float*>(base_ptr + C::OFF_R1 + (slot * C::MAXH * FN_ROWS + r) * 8);
             float msum = 0.0f;
             for (int p = 0; p < H; ++p) msum += rv1[p * FN_ROWS * 2];
             const float mean = msum / static_cast<float>(H);
@@ -293,104 +401,127 @@ __global__ void __launch_bounds__(FN_THREADS, 1)
             }
             const float rstd1 = rsqrtf(fmaf(m2, args.inv_hd, args.eps1));
 
-            // ---- ln_q: bf16 into sA (the first MMA's A operand, K-major) and
-            //      fp32 into O's TMEM columns (residual 1 through the MMA's accumulate).
+            // ---- ln_q = (q - mean) rstd1: bf16 into sA (the first MMA's A operand,
+            //      K-major) and fp32 into O's TMEM columns (residual 1 through the
+            //      MMA's accumulate).  Each 64-column half, once written, releases
+            //      its half of the contraction of S.
+            {
+                const uint64_t rs = f2_splat(rstd1), nmr = f2_splat(-mean * rstd1);
 #pragma unroll 1
-            for (int seg = 0; seg < 4; ++seg) {
-                uint32_t lv[32];
+                for (int seg = 0; seg < 4; ++seg) {
+                    uint4 w[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int c = seg * 4 + k;
-                    const uint4 w = ld_shared_v4(fn_chunk(sq, r, c));
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-                    uint32_t pk[4];
+                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, seg * 4 + k));
+                    uint32_t lv[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float l0 = valid ? (bf16lo(ww[e]) - mean) * rstd1 : 0.0f;
-                        const float l1 = valid ? (bf16hi(ww[e]) - mean) * rstd1 : 0.0f;
-                        lv[k * 8 + 2 * e] = __float_as_uint(l0);
-                        lv[k * 8 + 2 * e + 1] = __float_as_uint(l1);
-                        pk[e] = pack_bf16x2(l0, l1);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint64_t l = f2_fma(bf16x2_to_f2(ww[e]), rs, nmr);
+                            float l0, l1;
+                            f2_unpack(l, l0, l1);
+                            lv[k * 8 + 2 * e] = __float_as_uint(l0);
+                            lv[k * 8 + 2 * e + 1] = __float_as_uint(l1);
+                            pk[e] = pack_bf16x2(l0, l1);
+                        }
+                        st_shared_v4(fn_chunk(sA, r, seg * 4 + k), pk[0], pk[1], pk[2], pk[3]);
                     }
-                    st_shared_v4(fn_chunk(sA, r, c), pk[0], pk[1], pk[2], pk[3]);
+                    tmem_st32(tO + static_cast<uint32_t>(seg * 32), lv);
+                    if (seg & 1) {
+                        fence_proxy_async_smem();  // the tensor cores read sA
+                        tc_fence_before();         // this thread's reads of the last tile's S are done
+                        mbar_arrive(bar(b0 + G_AREADY + (seg >> 1)));
+                    }
                 }
-                tmem_st32(tO + static_cast<uint32_t>(seg * 32), lv);
+                tmem_st_wait();
             }
-            tmem_st_wait();
-            fence_proxy_async_smem();  // the tensor cores read sA
-            tc_fence_before();
-            mbar_arrive(bar_aready);
 
-            // ---- activation: P = bf16(act(S)) into sA (the second MMA's A operand)
-            ok = mbar_wait(guard, bar_sfull, ph, FN_SITE_SFULL, it);
+            // ---- P = bf16(act(S)) into sA (the second MMA's A operand), per 64-key
+            //      half of S as soon as the MMA has it; each half written releases
+            //      its half of the contraction of O.
+            bool good = true;
+            for (int h = 0; h < 2; ++h) {
+                ok = mbar_wait(guard, bar(b0 + G_SFULL + h), gph, FN_SITE_SFULL, it);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    good = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ts = tS + static_cast<uint32_t>(h * 64);
+                if (args.act == 1)
+                    fn_act_half<1>(ts, sA, r, h);
+                else if (args.act == 2)
+                    fn_act_half<2>(ts, sA, r, h);
+                else
+                    fn_act_half<0>(ts, sA, r, h);
+                fence_proxy_async_smem();
+                tc_fence_before();  // orders this thread's TMEM stores of ln_q before the MMA too
+                mbar_arrive(bar(b0 + G_PREADY + h));
+            }
+            if (!good) break;
+
+            // ---- RMSNorm of O over all heads (second exchange), out = o rstd2 + q
+            ok = mbar_wait(guard, bar(b0 + G_OFULL), gph, FN_SITE_OFULL, it);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
+            float ss;
+            {
+                uint64_t q0 = 0, q1 = 0;
 #pragma unroll 1
-            for (int seg = 0; seg < 4; ++seg) {
-                uint32_t v[32];
-                tmem_ld32(tS + static_cast<uint32_t>(seg * 32), v);
-                tmem_ld_wait(v);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tO + static_cast<uint32_t>(hh * 64), v0);
+                    tmem_ld32(tO + static_cast<uint32_t>(hh * 64 + 32), v1);
+                    tmem_ld_wait(v0);
+                    tmem_ld_wait(v1);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        pk[e] = pack_bf16x2(fn_act(__uint_as_float(v[k * 8 + 2 * e]), args.act),
-                                            fn_act(__uint_as_float(v[k * 8 + 2 * e + 1]), args.act));
-                    st_shared_v4(fn_chunk(sA, r, seg * 4 + k), pk[0], pk[1], pk[2], pk[3]);
+                    for (int i = 0; i < 32; i += 4) {
+                        const uint64_t a = f2_pack(v0[i], v0[i + 1]), b = f2_pack(v0[i + 2], v0[i + 3]);
+                        const uint64_t c = f2_pack(v1[i], v1[i + 1]), d = f2_pack(v1[i + 2], v1[i + 3]);
+                        q0 = f2_fma(a, a, q0);
+                        q1 = f2_fma(b, b, q1);
+                        q0 = f2_fma(c, c, q0);
+                        q1 = f2_fma(d, d, q1);
+                    }
                 }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar_pready);
-
-            // ---- RMSNorm of O over all heads (second exchange), out = o * rstd + q
-            ok = mbar_wait(guard, bar_ofull, ph, FN_SITE_OFULL, it);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            float ss0 = 0.0f, ss1 = 0.0f;
-#pragma unroll 1
-            for (int seg = 0; seg < 4; ++seg) {
-                uint32_t v[32];
-                tmem_ld32(tO + static_cast<uint32_t>(seg * 32), v);
-                tmem_ld_wait(v);
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float o0 = __uint_as_float(v[i]), o1 = __uint_as_float(v[i + 1]);
-                    ss0 = fmaf(o0, o0, ss0);
-                    ss1 = fmaf(o1, o1, ss1);
-                }
+                ss = f2_hsum(f2_add(q0, q1));
             }
             {
-                const uint32_t x2 = bar_x2 + 8u * xp;
-                const uint32_t slot = sR2 + static_cast<uint32_t>(((xp * FN_MAXH + rank) * FN_ROWS + r) * 8);
-                for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(slot, p), ss0 + ss1, 0.0f, mapa_shared(x2, p));
-                ok = mbar_wait<true>(guard, x2, qph, FN_SITE_X2, it);
+                const uint32_t xb = bar(C::B_X2 + slot);
+                const uint32_t dst = sR2 + static_cast<uint32_t>(((slot * C::MAXH + rank) * FN_ROWS + r) * 8);
+                for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(dst, p), ss, 0.0f, mapa_shared(xb, p));
+                ok = mbar_wait<true>(guard, xb, xph, FN_SITE_X2, it);
                 if (!__all_sync(0xffffffffu, ok)) break;
-                if (warp == 0 && lane == 0 && it + 2 < tiles) mbar_arrive_expect_tx(x2, xbytes);
+                if (gw == 0 && lane == 0 && it + C::NSLOT < tiles) mbar_arrive_expect_tx(xb, xbytes);
             }
-            const float* rv2 = reinterpret_cast<const float*>(base_ptr + FN_OFF_R2 + (xp * FN_MAXH * FN_ROWS + r) * 8);
+            const float* rv2 =
+                reinterpret_cast<const float*>(base_ptr + C::OFF_R2 + (slot * C::MAXH * FN_ROWS + r) * 8);
             float tot = 0.0f;
             for (int p = 0; p < H; ++p) tot += rv2[p * FN_ROWS * 2];
             const float rstd2 = rsqrtf(fmaf(tot, args.inv_hd, args.eps2));
+            {
+                const uint64_t rr = f2_splat(rstd2);
 #pragma unroll 1
-            for (int seg = 0; seg < 4; ++seg) {
-                uint32_t v[32];
-                tmem_ld32(tO + static_cast<uint32_t>(seg * 32), v);
-                tmem_ld_wait(v);
+                for (int seg = 0; seg < 4; ++seg) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + static_cast<uint32_t>(seg * 32), v);
+                    uint4 w[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t a = fn_chunk(sq, r, seg * 4 + k);  // q, overwritten in place by out
-                    const uint4 w = ld_shared_v4(a);
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-                    uint32_t pk[4];
+                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, seg * 4 + k));
+                    tmem_ld_wait(v);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float y0 = valid ? fmaf(__uint_as_float(v[k * 8 + 2 * e]), rstd2, bf16lo(ww[e])) : 0.0f;
-                        const float y1 = valid ? fmaf(__uint_as_float(v[k * 8 + 2 * e + 1]), rstd2, bf16hi(ww[e])) : 0.0f;
-                        pk[e] = pack_bf16x2(y0, y1);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            pk[e] = f2_to_bf16x2(f2_fma(f2_pack(v[k * 8 + 2 * e], v[k * 8 + 2 * e + 1]), rr,
+                                                        bf16x2_to_f2(ww[e])));
+                        // q is overwritten in place by out
+                        st_shared_v4(fn_chunk(sq, r, seg * 4 + k), pk[0], pk[1], pk[2], pk[3]);
                     }
-                    st_shared_v4(a, pk[0], pk[1], pk[2], pk[3]);
                 }
             }
             fence_proxy_async_smem();  // the TMA store reads the staged rows
@@ -398,17 +529,16 @@ __global__ void __launch_bounds__(FN_THREADS, 1)
             if (lane == 0) {
                 // This warp's 32 rows, two 64-column boxes; none past the batch's
                 // last 32-row group that holds a valid row.
-                if (m0 + warp * 32 < qlen) {
+                if (m0 + gw * 32 < qlen)
                     for (int half = 0; half < 2; ++half)
-                        tma_store_2d(&tmO, sq + static_cast<uint32_t>(half * FN_HALF_BYTES + warp * 32 * 128),
-                                     col0 + half * 64, static_cast<int32_t>(qrow0 + m0 + warp * 32));
-                    bulk_commit();
-                    bulk_wait_read<0>();  // the buffer is read before the next q tile lands in it
-                }
-                mbar_arrive(bar_qempty0 + 8u * qb);
+                        tma_store_2d(&tmO, sq + static_cast<uint32_t>(half * FN_HALF_BYTES + gw * 32 * 128),
+                                     col0 + half * 64, static_cast<int32_t>(qrow0 + m0 + gw * 32));
+                bulk_commit();
             }
             __syncwarp();
         }
+        if (lane == 0) bulk_wait_read<0>();  // shared memory outlives the stores' reads
+        __syncwarp();
     }
 
     // ---- teardown: no CTA leaves while a peer may still write into its shared memory
@@ -416,22 +546,47 @@ __global__ void __launch_bounds__(FN_THREADS, 1)
     __syncthreads();
     cluster_arrive_release();
     cluster_wait_acquire();
-    if (warp == FN_PRODUCER_WARP) {
+    if (warp == C::PRODUCER_WARP) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 256);
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+}
+
+template <int NG>
+cudaError_t launch_fn(const CUtensorMap* m, const FnArgs& args, bool overlap, cudaStream_t stream) {
+    using C = FnCfg<NG>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(nf_flashnorm_fwd_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    cfg.gridDim = dim3(static_cast<unsigned>(args.B * args.H));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(args.H);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+    if (overlap) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(n);
+    return cudaLaunchKernelEx(&cfg, nf_flashnorm_fwd_kernel<NG>, m[0], m[1], m[2], m[3], args);
 }
 
 }  // namespace
 
 cudaError_t launch_flashnorm_fwd(const void* tmaps, const FlashNormLaunch& a, bool overlap, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(nf_flashnorm_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             FN_SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     const CUtensorMap* m = static_cast<const CUtensorMap*>(tmaps);
     FnArgs args;
     args.B = a.B;
@@ -444,26 +599,8 @@ cudaError_t launch_flashnorm_fwd(const void* tmaps, const FlashNormLaunch& a, bo
     args.q_len = a.q_len;
     args.status = a.status;
     args.timeout_ns = a.timeout_ns;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    int n = 0;
-    cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.H));
-    cfg.blockDim = dim3(FN_THREADS);
-    cfg.dynamicSmemBytes = FN_SMEM_BYTES;
-    cfg.stream = stream;
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = static_cast<unsigned>(a.H);
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-    if (overlap) {
-        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[n].val.programmaticStreamSerializationAllowed = 1;
-        ++n;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = static_cast<unsigned>(n);
-    return cudaLaunchKernelEx(&cfg, nf_flashnorm_fwd_kernel, m[0], m[1], m[2], m[3], args);
+    // Two compute groups fit shared memory up to 4 heads per cluster.
+    return a.H <= FnCfg<2>::MAXH ? launch_fn<2>(m, args, overlap, stream) : launch_fn<1>(m, args, overlap, stream);
 }
 
 }  // namespace nf

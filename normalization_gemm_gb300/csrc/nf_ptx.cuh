@@ -480,6 +480,12 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     return d;
 }
 
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -494,6 +500,13 @@ __device__ __forceinline__ float f2_hsum(uint64_t v) {
 
 // Two bf16 in one 32-bit word -> a packed fp32 pair (exact).
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) { return f2_pack(w << 16, w & 0xFFFF0000u); }
+
+// A packed fp32 pair -> two bf16 in one 32-bit word (round to nearest even).
+__device__ __forceinline__ uint32_t f2_to_bf16x2(uint64_t v) {
+    float lo, hi;
+    f2_unpack(v, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
 
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t a) {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
