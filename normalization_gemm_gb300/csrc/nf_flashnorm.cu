@@ -15,21 +15,27 @@
 // one head each); each CTA keeps its head's K and V in shared memory and walks
 // the batch's 128-row query tiles (ceil(q_len[b] / 128) of them).
 //
-// CTA roles, NG compute groups (NG = 2 for H <= 4, 1 above: shared memory):
+// CTA roles, NG compute groups (NG = 2 for H <= 4; 1 above, where the
+// exchange slots of 2 groups x 8 heads would not fit in shared memory):
 //   warps 4g..4g+3  compute group g, tiles g, g + NG, ...; one query row per
 //              thread (TMEM lane = row): the LayerNorm (partial statistics over
 //              the CTA's 128 columns, pushed to every CTA of the cluster with
-//              st.async, merged), bf16(ln_q) as the first MMA's A operand and
-//              ln_q in fp32 into the O accumulator (residual 1 through the
-//              MMA's accumulate), the activation of S into P (the second MMA's
-//              A operand), the RMSNorm of O (second exchange) and
-//              out = o * rstd + q, staged over the q tile and stored with TMA.
-//              Two groups overlap one tile's exchanges and MMAs with the other
-//              tile's CUDA-core work.
-//   warp 4NG   TMA producer: K and V once, the q tiles into two buffers (tile
-//              it into buffer it & 1, which with two groups is group it & 1's).
-//   warp 4NG+1+g  MMA issuer of group g: S = ln_q K^T and O += P V
-//              (tcgen05.mma, M = N = 128) into the group's 256 TMEM columns.
+//              st.async, merged); bf16(ln_q) into TMEM as the first MMA's A
+//              operand; P = bf16(act(S)) into TMEM over S's columns already
+//              read, the second MMA's A operand; o = P V + ln_q (residual 1,
+//              ln_q recomputed from q in fp32), its RMSNorm (second exchange)
+//              and out = o * rstd + q, staged over the q tile and stored with
+//              TMA.  Two groups overlap one tile's exchanges and MMAs with the
+//              other tile's CUDA-core work.
+//   warp 4NG   TMA producer: K and V once, the q tiles into NQ = 4 buffers
+//              (tile it into buffer it mod 4), each refilled once its tile's
+//              output stores have read it, so a group's next tile lands while
+//              it computes the current one.
+//   warp 4NG+1+g  MMA issuer of group g: S = ln_q K^T (two 64-key halves) and
+//              O = P V (tcgen05.mma, A from TMEM, B from shared memory) in the
+//              group's 256 TMEM columns (S / P 128, O / bf16(ln_q) 128); each
+//              contraction runs in two halves, released as the compute group
+//              writes the matching half of its A operand.
 //
 // Exchange slots: tile it uses slot it mod 2NG of each exchange.  A peer sends
 // tile it + 2NG's partials (the same slot) only after it received every CTA's
@@ -57,23 +63,23 @@ struct FnCfg {
     static constexpr int THREADS = (4 * NG + 1 + NG) * 32;
     static constexpr int PRODUCER_WARP = 4 * NG;
     static constexpr int MMA_WARP0 = 4 * NG + 1;
+    static constexpr int NQ = 4;                                  // q tile buffers
     static constexpr int RECV_BYTES = NSLOT * MAXH * FN_ROWS * 8;  // [slot][cluster rank][row] float2
     // Shared-memory layout (1 KB aligned base).
     static constexpr int OFF_K = 0;                               // K: 2 boxes of 128 keys x 64 d
     static constexpr int OFF_V = OFF_K + FN_TILE_BYTES;           // V: 2 K-tiles x 2 boxes of 64 keys x 64 d
-    static constexpr int OFF_Q = OFF_V + FN_TILE_BYTES;           // q tiles [2], later the output staging
-    static constexpr int OFF_A = OFF_Q + 2 * FN_TILE_BYTES;       // [NG] bf16(ln_q), then P
-    static constexpr int OFF_R1 = OFF_A + NG * FN_TILE_BYTES;     // LayerNorm partials received
+    static constexpr int OFF_Q = OFF_V + FN_TILE_BYTES;           // q tiles [NQ], later the output staging
+    static constexpr int OFF_R1 = OFF_Q + NQ * FN_TILE_BYTES;     // LayerNorm partials received
     static constexpr int OFF_R2 = OFF_R1 + RECV_BYTES;            // RMSNorm partials received
     static constexpr int OFF_BAR = OFF_R2 + RECV_BYTES;
-    static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;       // barriers + words, 1 KB realignment slack
+    static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;       // barriers + words, 1 KB realignment slack
     static_assert(SMEM_BYTES <= SMEM_OPTIN_LIMIT, "shared memory");
-    // barriers (8 bytes each): kv, qfull[2], qempty[2], GROUP_BARS per group
+    // barriers (8 bytes each): kv, qfull[NQ], qempty[NQ], GROUP_BARS per group
     // (below), x1[NSLOT], x2[NSLOT]
-    static constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_GROUP = 5, GROUP_BARS = 8,
+    static constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + NQ, B_GROUP = 1 + 2 * NQ, GROUP_BARS = 8,
                          B_X1 = B_GROUP + GROUP_BARS * NG, B_X2 = B_X1 + NSLOT, NBAR = B_X2 + NSLOT;
-    static_assert(NBAR * 8 <= 240, "barrier area");
-    static constexpr int OFF_TMEM_HOLDER = 240, OFF_ABORT = 244;
+    static_assert(NBAR * 8 <= 504, "barrier area");
+    static constexpr int OFF_TMEM_HOLDER = 504, OFF_ABORT = 508;
     static constexpr int TMEM_COLS = 256 * NG;     // per group: S 128 columns, O 128
 };
 
@@ -133,20 +139,20 @@ __device__ __forceinline__ uint32_t fn_chunk(uint32_t base, int r, int c) {
 }
 
 // The activation of one 64-key half of S (TMEM columns ts .. ts + 63 of this
-// thread's row) into the matching 64-column box of the A tile at sA.
+// thread's row), as 32 bf16 pairs into the TMEM columns tp .. tp + 31.
 template <int ACT>
-__device__ __forceinline__ void fn_act_half(uint32_t ts, uint32_t sA, int r, int half) {
-    uint32_t v0[32], v1[32];
+__device__ __forceinline__ void fn_act_half(uint32_t ts, uint32_t tp) {
+    uint32_t v0[32], v1[32], pk[32];
     tmem_ld32(ts, v0);
     tmem_ld32(ts + 32u, v1);
     tmem_ld_wait(v0);
     tmem_ld_wait(v1);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t* v = k < 4 ? v0 + k * 8 : v1 + (k - 4) * 8;
-        st_shared_v4(fn_chunk(sA, r, half * 8 + k), fn_act_pack<ACT>(v[0], v[1]), fn_act_pack<ACT>(v[2], v[3]),
-                     fn_act_pack<ACT>(v[4], v[5]), fn_act_pack<ACT>(v[6], v[7]));
+    for (int i = 0; i < 16; ++i) {
+        pk[i] = fn_act_pack<ACT>(v0[2 * i], v0[2 * i + 1]);
+        pk[16 + i] = fn_act_pack<ACT>(v1[2 * i], v1[2 * i + 1]);
     }
+    tmem_st32(tp, pk);
 }
 
 __device__ __forceinline__ uint32_t fn_cluster_id() {
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
-    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQ = base + C::OFF_Q, sA0 = base + C::OFF_A;
+    const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sQ = base + C::OFF_Q;
     const uint32_t sR1 = base + C::OFF_R1, sR2 = base + C::OFF_R2, sBar = base + C::OFF_BAR;
     auto bar = [&](int slot) { return sBar + 8u * static_cast<uint32_t>(slot); };
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::OFF_BAR + C::OFF_TMEM_HOLDER);
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmO);
         mbar_init(bar(C::B_KV), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NQ; ++i) {
             mbar_init(bar(C::B_QFULL + i), 1);
             mbar_init(bar(C::B_QEMPTY + i), 4);  // one arrival per warp of the group using the buffer
         }
@@ -252,8 +258,8 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                                 col0 + i * 64, krow + kt * 64);
             }
             for (int it = 0; it < tiles; ++it) {
-                const int qb = it & 1;
-                const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+                const int qb = it % C::NQ;
+                const uint32_t ph = static_cast<uint32_t>(it / C::NQ) & 1u;
                 if (!mbar_wait(guard, bar(C::B_QEMPTY + qb), ph ^ 1u, FN_SITE_QEMPTY, it)) break;
                 const uint32_t fb = bar(C::B_QFULL + qb);
                 mbar_arrive_expect_tx(fb, FN_TILE_BYTES);
@@ -263,9 +269,9 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
             }
             // Every load issued has landed before the CTA may exit.
             fn_drain(bar(C::B_KV), 0, args.timeout_ns);
-            for (int j = 0; j < 2 && j < tiles; ++j) {
-                const int last = j + ((tiles - 1 - j) / 2) * 2;  // the last tile that used buffer j
-                fn_drain(bar(C::B_QFULL + j), static_cast<uint32_t>(last >> 1) & 1u, args.timeout_ns);
+            for (int j = 0; j < C::NQ && j < tiles; ++j) {
+                const int last = j + ((tiles - 1 - j) / C::NQ) * C::NQ;  // the last tile that used buffer j
+                fn_drain(bar(C::B_QFULL + j), static_cast<uint32_t>(last / C::NQ) & 1u, args.timeout_ns);
             }
         }
         __syncwarp();
@@ -277,14 +283,14 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
             constexpr uint32_t IDESC_S = idesc_bf16_f32(FN_ROWS, FN_LKV / 2, false);  // B = K (K-major), 64 keys
             constexpr uint32_t IDESC_O = idesc_bf16_f32(FN_ROWS, FN_D, true);         // B = V (MN-major)
             const uint32_t tS = tmem_base + static_cast<uint32_t>(g * 256), tO = tS + 128u;
-            const uint32_t sA = sA0 + static_cast<uint32_t>(g * FN_TILE_BYTES);
-            // S half n (keys 64n..64n+63) += ln_q[:, 64kt..] K[64n.., 64kt..]^T
+            // S half n (keys 64n..64n+63) += ln_q[:, 64kt..] K[64n.., 64kt..]^T, with
+            // bf16(ln_q) in TMEM columns tO .. tO + 63 (8 columns per K step of 16)
             auto mma_s = [&](int n, int kt) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    mma_bf16(tS + static_cast<uint32_t>(n * 64), smem_desc_sw128(sA + kt * FN_HALF_BYTES + j * 32, 16, 1024),
-                             smem_desc_sw128(sK + kt * FN_HALF_BYTES + n * (FN_HALF_BYTES / 2) + j * 32, 16, 1024),
-                             IDESC_S, (kt | j) != 0 ? 1u : 0u);
+                    mma_bf16_ts(tS + static_cast<uint32_t>(n * 64), tO + static_cast<uint32_t>(kt * 32 + j * 8),
+                                smem_desc_sw128(sK + kt * FN_HALF_BYTES + n * (FN_HALF_BYTES / 2) + j * 32, 16, 1024),
+                                IDESC_S, (kt | j) != 0 ? 1u : 0u);
             };
             bool ok = mbar_wait(guard, bar(C::B_KV), 0, FN_SITE_KV, 0);
             for (int it = g; it < tiles && ok; it += NG) {
@@ -297,18 +303,21 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 if (!(ok = mbar_wait(guard, bar(b0 + G_AREADY + 1), ph, FN_SITE_AREADY, it))) break;
                 tc_fence_after();
                 mma_s(0, 1);
-                mma_commit(bar(b0 + G_SFULL));      // keys 0-63 done (and every read of ln_q's columns 0-63)
+                mma_commit(bar(b0 + G_SFULL));      // keys 0-63 done
                 mma_s(1, 1);
                 mma_commit(bar(b0 + G_SFULL + 1));  // keys 64-127 done
-                // O already holds ln_q: every step accumulates.  P's keys 0-63 first.
+                // O = P V overwrites the columns that held bf16(ln_q): every S MMA is
+                // complete first.  P (bf16 pairs in TMEM columns tS .. tS + 63), keys
+                // 0-63 first.
+                if (!(ok = mbar_wait(guard, bar(b0 + G_SFULL + 1), ph, FN_SITE_SFULL, it))) break;
                 for (int kt = 0; kt < 2; ++kt) {
                     if (!(ok = mbar_wait(guard, bar(b0 + G_PREADY + kt), ph, FN_SITE_PREADY, it))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        mma_bf16(tO, smem_desc_sw128(sA + kt * FN_HALF_BYTES + j * 32, 16, 1024),
-                                 smem_desc_sw128(sV + kt * FN_HALF_BYTES + j * 2048, FN_HALF_BYTES / 2, 1024),
-                                 IDESC_O, 1u);
+                        mma_bf16_ts(tO, tS + static_cast<uint32_t>(kt * 32 + j * 8),
+                                    smem_desc_sw128(sV + kt * FN_HALF_BYTES + j * 2048, FN_HALF_BYTES / 2, 1024),
+                                    IDESC_O, (kt | j) != 0 ? 1u : 0u);
                 }
                 if (!ok) break;
                 mma_commit(bar(b0 + G_OFULL));
@@ -324,20 +333,19 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
         const int b0 = C::B_GROUP + g * C::GROUP_BARS;
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(gw * 32) << 16) + static_cast<uint32_t>(g * 256);
         const uint32_t tS = t_lane, tO = t_lane + 128u;
-        const uint32_t sA = sA0 + static_cast<uint32_t>(g * FN_TILE_BYTES);
         for (int it = g; it < tiles; it += NG) {
-            const int qb = it & 1;
-            const uint32_t qph = static_cast<uint32_t>(it >> 1) & 1u;     // q buffer use count parity
+            const int qb = it % C::NQ;
+            const uint32_t qph = static_cast<uint32_t>(it / C::NQ) & 1u;  // q buffer use count parity
             const uint32_t gph = static_cast<uint32_t>(it / NG) & 1u;     // this group's tile count parity
             const int slot = it % C::NSLOT;
             const uint32_t xph = static_cast<uint32_t>(it / C::NSLOT) & 1u;
             const int m0 = it * FN_ROWS;
             const uint32_t sq = sQ + static_cast<uint32_t>(qb * FN_TILE_BYTES);
-            if (NG == 2 && it >= NG && lane == 0) {
-                // This group's previous tile used the same q buffer: once its
-                // output stores have read it, the producer may load this tile.
+            if (it >= NG && lane == 0) {
+                // Once the output stores of this group's previous tile have read
+                // its q buffer, the producer may refill it (with tile it - NG + NQ).
                 bulk_wait_read<0>();
-                mbar_arrive(bar(C::B_QEMPTY + qb));
+                mbar_arrive(bar(C::B_QEMPTY + (it - NG) % C::NQ));
             }
             bool ok = mbar_wait(guard, bar(C::B_QFULL + qb), qph, FN_SITE_QFULL, it);
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -382,13 +390,6 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 if (!__all_sync(0xffffffffu, ok)) break;
                 if (gw == 0 && lane == 0 && it + C::NSLOT < tiles) mbar_arrive_expect_tx(xb, xbytes);
             }
-            if (NG == 1 && it > 0 && lane == 0) {
-                // The previous tile's output stores have read its q buffer by
-                // now: hand it to the producer, which loads tile it + 1 into it
-                // while this tile finishes.
-                bulk_wait_read<0>();
-                mbar_arrive(bar(C::B_QEMPTY + (qb ^ 1)));
-            }
             const float* rv1 =
                 reinterpret_cast<const float*>(base_ptr + C::OFF_R1 + (slot * C::MAXH * FN_ROWS + r) * 8);
             float msum = 0.0f;
@@ -400,47 +401,34 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 m2 += rv1[p * FN_ROWS * 2 + 1] + static_cast<float>(FN_D) * dm * dm;
             }
             const float rstd1 = rsqrtf(fmaf(m2, args.inv_hd, args.eps1));
+            // ln_q = (q - mean) rstd1 = q rstd1 - mean rstd1, in packed pairs
+            const uint64_t rs = f2_splat(rstd1), nmr = f2_splat(-mean * rstd1);
 
-            // ---- ln_q = (q - mean) rstd1: bf16 into sA (the first MMA's A operand,
-            //      K-major) and fp32 into O's TMEM columns (residual 1 through the
-            //      MMA's accumulate).  Each 64-column half, once written, releases
-            //      its half of the contraction of S.
-            {
-                const uint64_t rs = f2_splat(rstd1), nmr = f2_splat(-mean * rstd1);
+            // ---- bf16(ln_q) as bf16 pairs into TMEM columns tO .. tO + 63 (the first
+            //      MMA's A operand); each 64-column half, once written, releases its
+            //      half of the contraction of S.
 #pragma unroll 1
-                for (int seg = 0; seg < 4; ++seg) {
-                    uint4 w[4];
+            for (int hh = 0; hh < 2; ++hh) {
+                uint4 w[8];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, seg * 4 + k));
-                    uint32_t lv[32];
+                for (int k = 0; k < 8; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, hh * 8 + k));
+                uint32_t pk[32];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-                        uint32_t pk[4];
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint64_t l = f2_fma(bf16x2_to_f2(ww[e]), rs, nmr);
-                            float l0, l1;
-                            f2_unpack(l, l0, l1);
-                            lv[k * 8 + 2 * e] = __float_as_uint(l0);
-                            lv[k * 8 + 2 * e + 1] = __float_as_uint(l1);
-                            pk[e] = pack_bf16x2(l0, l1);
-                        }
-                        st_shared_v4(fn_chunk(sA, r, seg * 4 + k), pk[0], pk[1], pk[2], pk[3]);
-                    }
-                    tmem_st32(tO + static_cast<uint32_t>(seg * 32), lv);
-                    if (seg & 1) {
-                        fence_proxy_async_smem();  // the tensor cores read sA
-                        tc_fence_before();         // this thread's reads of the last tile's S are done
-                        mbar_arrive(bar(b0 + G_AREADY + (seg >> 1)));
-                    }
+                    for (int e = 0; e < 4; ++e) pk[k * 4 + e] = f2_to_bf16x2(f2_fma(bf16x2_to_f2(ww[e]), rs, nmr));
                 }
+                tmem_st32(tO + static_cast<uint32_t>(hh * 32), pk);
                 tmem_st_wait();
+                tc_fence_before();  // also orders this thread's reads of the last tile's S and O
+                mbar_arrive(bar(b0 + G_AREADY + hh));
             }
 
-            // ---- P = bf16(act(S)) into sA (the second MMA's A operand), per 64-key
-            //      half of S as soon as the MMA has it; each half written releases
-            //      its half of the contraction of O.
+            // ---- P = bf16(act(S)) as bf16 pairs into TMEM columns tS .. tS + 63 (the
+            //      second MMA's A operand, over S's columns already read), per 64-key
+            //      half of S as soon as the MMA has it; each half written releases its
+            //      half of the contraction of O.
             bool good = true;
             for (int h = 0; h < 2; ++h) {
                 ok = mbar_wait(guard, bar(b0 + G_SFULL + h), gph, FN_SITE_SFULL, it);
@@ -449,20 +437,21 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ts = tS + static_cast<uint32_t>(h * 64);
+                const uint32_t ts = tS + static_cast<uint32_t>(h * 64), tp = tS + static_cast<uint32_t>(h * 32);
                 if (args.act == 1)
-                    fn_act_half<1>(ts, sA, r, h);
+                    fn_act_half<1>(ts, tp);
                 else if (args.act == 2)
-                    fn_act_half<2>(ts, sA, r, h);
+                    fn_act_half<2>(ts, tp);
                 else
-                    fn_act_half<0>(ts, sA, r, h);
-                fence_proxy_async_smem();
-                tc_fence_before();  // orders this thread's TMEM stores of ln_q before the MMA too
+                    fn_act_half<0>(ts, tp);
+                tmem_st_wait();
+                tc_fence_before();
                 mbar_arrive(bar(b0 + G_PREADY + h));
             }
             if (!good) break;
 
-            // ---- RMSNorm of O over all heads (second exchange), out = o rstd2 + q
+            // ---- o = P V + ln_q (residual 1), written back over P V in TMEM, and its
+            //      RMSNorm over all heads (second exchange); out = o rstd2 + q
             ok = mbar_wait(guard, bar(b0 + G_OFULL), gph, FN_SITE_OFULL, it);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
@@ -470,23 +459,34 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
             {
                 uint64_t q0 = 0, q1 = 0;
 #pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tO + static_cast<uint32_t>(hh * 64), v0);
-                    tmem_ld32(tO + static_cast<uint32_t>(hh * 64 + 32), v1);
-                    tmem_ld_wait(v0);
-                    tmem_ld_wait(v1);
+                for (int seg = 0; seg < 4; ++seg) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + static_cast<uint32_t>(seg * 32), v);
+                    uint4 w[4];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const uint64_t a = f2_pack(v0[i], v0[i + 1]), b = f2_pack(v0[i + 2], v0[i + 3]);
-                        const uint64_t c = f2_pack(v1[i], v1[i + 1]), d = f2_pack(v1[i + 2], v1[i + 3]);
-                        q0 = f2_fma(a, a, q0);
-                        q1 = f2_fma(b, b, q1);
-                        q0 = f2_fma(c, c, q0);
-                        q1 = f2_fma(d, d, q1);
+                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, seg * 4 + k));
+                    tmem_ld_wait(v);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = k * 8 + 2 * e;
+                            const uint64_t o = f2_add(f2_pack(v[i], v[i + 1]), f2_fma(bf16x2_to_f2(ww[e]), rs, nmr));
+                            if (e & 1)
+                                q1 = f2_fma(o, o, q1);
+                            else
+                                q0 = f2_fma(o, o, q0);
+                            float o0, o1;
+                            f2_unpack(o, o0, o1);
+                            v[i] = __float_as_uint(o0);
+                            v[i + 1] = __float_as_uint(o1);
+                        }
                     }
+                    tmem_st32(tO + static_cast<uint32_t>(seg * 32), v);
                 }
                 ss = f2_hsum(f2_add(q0, q1));
+                tmem_st_wait();
             }
             {
                 const uint32_t xb = bar(C::B_X2 + slot);
@@ -599,7 +599,7 @@ cudaError_t launch_flashnorm_fwd(const void* tmaps, const FlashNormLaunch& a, bo
     args.q_len = a.q_len;
     args.status = a.status;
     args.timeout_ns = a.timeout_ns;
-    // Two compute groups fit shared memory up to 4 heads per cluster.
+    // Two compute groups' exchange slots fit shared memory up to 4 heads per cluster.
     return a.H <= FnCfg<2>::MAXH ? launch_fn<2>(m, args, overlap, stream) : launch_fn<1>(m, args, overlap, stream);
 }
 
