@@ -15,32 +15,41 @@
 // one head each); each CTA keeps its head's K and V in shared memory and walks
 // the batch's 128-row query tiles (ceil(q_len[b] / 128) of them).
 //
-// CTA roles, NG compute groups (NG = 2 for H <= 4; 1 above, where the
-// exchange slots of 2 groups x 8 heads would not fit in shared memory):
-//   warps 4g..4g+3  compute group g, tiles g, g + NG, ...; one query row per
-//              thread (TMEM lane = row): the LayerNorm (partial statistics over
-//              the CTA's 128 columns, pushed to every CTA of the cluster with
-//              st.async, merged); bf16(ln_q) into TMEM as the first MMA's A
-//              operand; P = bf16(act(S)) into TMEM over S's columns already
-//              read, the second MMA's A operand; o = P V + ln_q (residual 1,
-//              ln_q recomputed from q in fp32), its RMSNorm (second exchange)
-//              and out = o * rstd + q, staged over the q tile and stored with
-//              TMA.  Two groups overlap one tile's exchanges and MMAs with the
-//              other tile's CUDA-core work.
-//   warp 4NG   TMA producer: K and V once, the q tiles into NQ = 4 buffers
+// CTA roles, NG compute groups (NG = 2 for H <= 4; 1 above, where two groups'
+// exchange slots for up to 16 partials per row would crowd out the q buffers):
+//   warps 8g..8g+7  compute group g, tiles g, g + NG, ...; warp 8g + 4hf + q4
+//              takes rows 32q4 .. 32q4 + 31 (its TMEM lane quarter) and the 64
+//              columns of half hf, one half row per thread: the LayerNorm
+//              (partial statistics over the 64 columns, pushed to every CTA of
+//              the cluster with st.async, 2H partials per row merged);
+//              bf16(ln_q) into TMEM as the first MMA's A operand; P =
+//              bf16(act(S)) for keys 64hf .. 64hf + 63 into TMEM over S's
+//              columns already read, the second MMA's A operand; o = P V + ln_q
+//              (residual 1, ln_q recomputed from q in fp32), its RMSNorm
+//              (second exchange) and out = o * rstd + q, staged over the q tile
+//              and stored with TMA.  Two groups overlap one tile's exchanges
+//              and MMAs with the other tile's CUDA-core work.
+//   warp 8NG   TMA producer: K and V once, the q tiles into NQ = 4 buffers
 //              (tile it into buffer it mod 4), each refilled once its tile's
 //              output stores have read it, so a group's next tile lands while
 //              it computes the current one.
-//   warp 4NG+1+g  MMA issuer of group g: S = ln_q K^T (two 64-key halves) and
+//   warp 8NG+1+g  MMA issuer of group g: S = ln_q K^T (two 64-key halves) and
 //              O = P V (tcgen05.mma, A from TMEM, B from shared memory) in the
 //              group's 256 TMEM columns (S / P 128, O / bf16(ln_q) 128); each
 //              contraction runs in two halves, released as the compute group
 //              writes the matching half of its A operand.
 //
-// Exchange slots: tile it uses slot it mod 2NG of each exchange.  A peer sends
-// tile it + 2NG's partials (the same slot) only after it received every CTA's
-// partials of tile it + NG, the same group's next tile, which this CTA sends
-// after it has read slot it: a slot is never overwritten before it is read.
+// Exchange slots: tile it uses slot it mod NG of each exchange, so slot s
+// serves group s alone and a slot is reused by the same group's next tile,
+// it + NG.  A peer sends its partials of tile it + NG to the LayerNorm slot
+// only after its RMSNorm exchange of tile it completed, which needs every
+// thread of this CTA's group to have sent its RMSNorm partial of tile it,
+// which each does after reading its LayerNorm partials of tile it.  Likewise a
+// peer sends to the RMSNorm slot for tile it + NG only after the LayerNorm
+// exchange of tile it + NG, which each thread here joins after reading its
+// RMSNorm partials of tile it.  So no slot is overwritten before it is read,
+// and no slot's barrier completes a second phase before every thread here has
+// waited on the first.
 //
 // Every wait is bounded; on expiry the kernel records NF_ERR_TIMEOUT with the
 // site in the device status word, drains what it issued and returns.
@@ -59,12 +68,13 @@ constexpr int FN_HALF_BYTES = FN_TILE_BYTES / 2;   // one 64-column box of 128 r
 template <int NG>
 struct FnCfg {
     static constexpr int MAXH = NG == 2 ? 4 : 8;   // heads per cluster
-    static constexpr int NSLOT = 2 * NG;           // exchange slots
-    static constexpr int THREADS = (4 * NG + 1 + NG) * 32;
-    static constexpr int PRODUCER_WARP = 4 * NG;
-    static constexpr int MMA_WARP0 = 4 * NG + 1;
+    static constexpr int NSLOT = NG;               // exchange slots
+    static constexpr int THREADS = (8 * NG + 1 + NG) * 32;
+    static constexpr int PRODUCER_WARP = 8 * NG;
+    static constexpr int MMA_WARP0 = 8 * NG + 1;
     static constexpr int NQ = 4;                                  // q tile buffers
-    static constexpr int RECV_BYTES = NSLOT * MAXH * FN_ROWS * 8;  // [slot][cluster rank][row] float2
+    // received partials: [slot][cluster rank x column half][row] float2
+    static constexpr int RECV_BYTES = NSLOT * 2 * MAXH * FN_ROWS * 8;
     // Shared-memory layout (1 KB aligned base).
     static constexpr int OFF_K = 0;                               // K: 2 boxes of 128 keys x 64 d
     static constexpr int OFF_V = OFF_K + FN_TILE_BYTES;           // V: 2 K-tiles x 2 boxes of 64 keys x 64 d
@@ -139,20 +149,19 @@ __device__ __forceinline__ uint32_t fn_chunk(uint32_t base, int r, int c) {
 }
 
 // The activation of one 64-key half of S (TMEM columns ts .. ts + 63 of this
-// thread's row), as 32 bf16 pairs into the TMEM columns tp .. tp + 31.
+// thread's row), as 32 bf16 pairs into the TMEM columns tp .. tp + 31, in two
+// 32-key parts; tp <= ts, so each part's results land on columns already read.
 template <int ACT>
 __device__ __forceinline__ void fn_act_half(uint32_t ts, uint32_t tp) {
-    uint32_t v0[32], v1[32], pk[32];
-    tmem_ld32(ts, v0);
-    tmem_ld32(ts + 32u, v1);
-    tmem_ld_wait(v0);
-    tmem_ld_wait(v1);
+#pragma unroll 1
+    for (int part = 0; part < 2; ++part) {
+        uint32_t v[32], pk[16];
+        tmem_ld32(ts + static_cast<uint32_t>(part * 32), v);
+        tmem_ld_wait(v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        pk[i] = fn_act_pack<ACT>(v0[2 * i], v0[2 * i + 1]);
-        pk[16 + i] = fn_act_pack<ACT>(v1[2 * i], v1[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) pk[i] = fn_act_pack<ACT>(v[2 * i], v[2 * i + 1]);
+        tmem_st16(tp + static_cast<uint32_t>(part * 16), pk);
     }
-    tmem_st32(tp, pk);
 }
 
 __device__ __forceinline__ uint32_t fn_cluster_id() {
@@ -189,7 +198,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
     const int H = args.H;
     const int rank = static_cast<int>(cluster_ctarank());  // this CTA's head
     const int bidx = static_cast<int>(fn_cluster_id());     // this cluster's batch
-    const uint32_t xbytes = static_cast<uint32_t>(H) * FN_ROWS * 8u;
+    const uint32_t xbytes = static_cast<uint32_t>(2 * H) * FN_ROWS * 8u;  // one partial per row and column half
     const WaitGuard guard{args.status, abort_flag, args.timeout_ns};
 
     if (threadIdx.x == 0) {
@@ -200,7 +209,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
         mbar_init(bar(C::B_KV), 1);
         for (int i = 0; i < C::NQ; ++i) {
             mbar_init(bar(C::B_QFULL + i), 1);
-            mbar_init(bar(C::B_QEMPTY + i), 4);  // one arrival per warp of the group using the buffer
+            mbar_init(bar(C::B_QEMPTY + i), 8);  // one arrival per warp of the group using the buffer
         }
         for (int g = 0; g < NG; ++g) {
             const int b0 = C::B_GROUP + g * C::GROUP_BARS;
@@ -307,15 +316,15 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 mma_s(1, 1);
                 mma_commit(bar(b0 + G_SFULL + 1));  // keys 64-127 done
                 // O = P V overwrites the columns that held bf16(ln_q): every S MMA is
-                // complete first.  P (bf16 pairs in TMEM columns tS .. tS + 63), keys
-                // 0-63 first.
+                // complete first.  P's keys 64kt..64kt+63 are bf16 pairs in TMEM
+                // columns tS + 64kt .. tS + 64kt + 31; keys 0-63 first.
                 if (!(ok = mbar_wait(guard, bar(b0 + G_SFULL + 1), ph, FN_SITE_SFULL, it))) break;
                 for (int kt = 0; kt < 2; ++kt) {
                     if (!(ok = mbar_wait(guard, bar(b0 + G_PREADY + kt), ph, FN_SITE_PREADY, it))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        mma_bf16_ts(tO, tS + static_cast<uint32_t>(kt * 32 + j * 8),
+                        mma_bf16_ts(tO, tS + static_cast<uint32_t>(kt * 64 + j * 8),
                                     smem_desc_sw128(sV + kt * FN_HALF_BYTES + j * 2048, FN_HALF_BYTES / 2, 1024),
                                     IDESC_O, (kt | j) != 0 ? 1u : 0u);
                 }
@@ -327,11 +336,14 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ======================================================== compute group g (warps 4g..4g+3)
-        const int g = warp >> 2, gw = warp & 3;
-        const int r = gw * 32 + lane;  // tile row == TMEM lane
+        // ======================================================== compute group g (warps 8g..8g+7)
+        // Warp 8g + 4hf + q4 takes rows 32q4 .. 32q4 + 31 (its TMEM lane quarter)
+        // and the 64 columns of half hf: one half row per thread.
+        const int g = warp >> 3, gw = warp & 7, q4 = gw & 3, hf = gw >> 2;
+        const int r = q4 * 32 + lane;  // tile row == TMEM lane
         const int b0 = C::B_GROUP + g * C::GROUP_BARS;
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(gw * 32) << 16) + static_cast<uint32_t>(g * 256);
+        const int pidx = rank * 2 + hf;  // this thread's partial in the exchanges
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(g * 256);
         const uint32_t tS = t_lane, tO = t_lane + 128u;
         for (int it = g; it < tiles; it += NG) {
             const int qb = it % C::NQ;
@@ -341,31 +353,26 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
             const uint32_t xph = static_cast<uint32_t>(it / C::NSLOT) & 1u;
             const int m0 = it * FN_ROWS;
             const uint32_t sq = sQ + static_cast<uint32_t>(qb * FN_TILE_BYTES);
-            if (it >= NG && lane == 0) {
-                // Once the output stores of this group's previous tile have read
-                // its q buffer, the producer may refill it (with tile it - NG + NQ).
-                bulk_wait_read<0>();
-                mbar_arrive(bar(C::B_QEMPTY + (it - NG) % C::NQ));
-            }
             bool ok = mbar_wait(guard, bar(C::B_QFULL + qb), qph, FN_SITE_QFULL, it);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (m0 + r >= qlen) {
                 // A row past q_len: zero it once, so that every later step gives
                 // exactly 0 for it, whatever the caller's buffer holds there.
 #pragma unroll
-                for (int c = 0; c < 16; ++c) st_shared_v4(fn_chunk(sq, r, c), 0u, 0u, 0u, 0u);
+                for (int c = 0; c < 8; ++c) st_shared_v4(fn_chunk(sq, r, hf * 8 + c), 0u, 0u, 0u, 0u);
             }
 
-            // ---- LayerNorm: partial (mean, M2) over this CTA's 128 columns, the
-            //      sums shifted by the row's first value, in packed fp32 pairs.
+            // ---- LayerNorm: partial (mean, M2) over this thread's 64 columns, the
+            //      sums shifted by the half row's first value, in packed fp32 pairs.
             float mean_c, m2_c;
             {
-                const float sh = bf16lo(ld_shared_v4(fn_chunk(sq, r, 0)).x);
+                const float sh = bf16lo(ld_shared_v4(fn_chunk(sq, r, hf * 8)).x);
                 const uint64_t nsh = f2_splat(-sh);
                 uint64_t s1a = 0, s1b = 0, s2a = 0, s2b = 0;  // (0.0f, 0.0f)
 #pragma unroll
-                for (int c = 0; c < 16; c += 2) {
-                    const uint4 w0 = ld_shared_v4(fn_chunk(sq, r, c)), w1 = ld_shared_v4(fn_chunk(sq, r, c + 1));
+                for (int c = 0; c < 8; c += 2) {
+                    const uint4 w0 = ld_shared_v4(fn_chunk(sq, r, hf * 8 + c));
+                    const uint4 w1 = ld_shared_v4(fn_chunk(sq, r, hf * 8 + c + 1));
                     const uint32_t ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {
@@ -378,40 +385,56 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                     }
                 }
                 const float a1 = f2_hsum(f2_add(s1a, s1b)), a2 = f2_hsum(f2_add(s2a, s2b));
-                mean_c = sh + a1 * (1.0f / FN_D);
-                m2_c = fmaxf(fmaf(-a1, a1 * (1.0f / FN_D), a2), 0.0f);
+                mean_c = sh + a1 * (1.0f / 64.0f);
+                m2_c = fmaxf(fmaf(-a1, a1 * (1.0f / 64.0f), a2), 0.0f);
             }
             {
-                // push to slot [rank] of every CTA of the cluster, wait for all H
+                // push to partial [pidx] of every CTA of the cluster, wait for all 2H
                 const uint32_t xb = bar(C::B_X1 + slot);
-                const uint32_t dst = sR1 + static_cast<uint32_t>(((slot * C::MAXH + rank) * FN_ROWS + r) * 8);
+                const uint32_t dst =
+                    sR1 + static_cast<uint32_t>(((slot * 2 * C::MAXH + pidx) * FN_ROWS + r) * 8);
                 for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(dst, p), mean_c, m2_c, mapa_shared(xb, p));
                 ok = mbar_wait<true>(guard, xb, xph, FN_SITE_X1, it);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 if (gw == 0 && lane == 0 && it + C::NSLOT < tiles) mbar_arrive_expect_tx(xb, xbytes);
             }
-            const float* rv1 =
-                reinterpret_cast<const float*>(base_ptr + C::OFF_R1 + (slot * C::MAXH * FN_ROWS + r) * 8);
+            if (it >= NG && lane == 0) {
+                // The output stores of this group's previous tile have read its q
+                // buffer by now: the producer may refill it.
+                bulk_wait_read<0>();
+                mbar_arrive(bar(C::B_QEMPTY + (it - NG) % C::NQ));
+            }
+            // Chan et al. merge of the 2H partials (64 values each); all loads
+            // issued before the first use.
+            float2 pv[2 * C::MAXH];
+            {
+                const uint32_t rb = sR1 + static_cast<uint32_t>((slot * 2 * C::MAXH * FN_ROWS + r) * 8);
+#pragma unroll
+                for (int p = 0; p < 2 * C::MAXH; ++p)
+                    pv[p] = p < 2 * H ? ld_shared_f32x2(rb + static_cast<uint32_t>(p * FN_ROWS * 8)) : make_float2(0.f, 0.f);
+            }
             float msum = 0.0f;
-            for (int p = 0; p < H; ++p) msum += rv1[p * FN_ROWS * 2];
-            const float mean = msum / static_cast<float>(H);
+#pragma unroll
+            for (int p = 0; p < 2 * C::MAXH; ++p) msum += pv[p].x;
+            const float mean = msum / static_cast<float>(2 * H);
             float m2 = 0.0f;
-            for (int p = 0; p < H; ++p) {  // Chan et al. merge, D values per partial
-                const float dm = rv1[p * FN_ROWS * 2] - mean;
-                m2 += rv1[p * FN_ROWS * 2 + 1] + static_cast<float>(FN_D) * dm * dm;
+#pragma unroll
+            for (int p = 0; p < 2 * C::MAXH; ++p) {
+                const float dm = pv[p].x - mean;
+                if (p < 2 * H) m2 += fmaf(64.0f * dm, dm, pv[p].y);
             }
             const float rstd1 = rsqrtf(fmaf(m2, args.inv_hd, args.eps1));
             // ln_q = (q - mean) rstd1 = q rstd1 - mean rstd1, in packed pairs
             const uint64_t rs = f2_splat(rstd1), nmr = f2_splat(-mean * rstd1);
 
-            // ---- bf16(ln_q) as bf16 pairs into TMEM columns tO .. tO + 63 (the first
-            //      MMA's A operand); each 64-column half, once written, releases its
-            //      half of the contraction of S.
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
+            // ---- bf16(ln_q) of this half as bf16 pairs into TMEM columns
+            //      tO + 32hf .. tO + 32hf + 31 (the first MMA's A operand): once the
+            //      four warps of the half have written, that half of the
+            //      contraction of S may run.
+            {
                 uint4 w[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, hh * 8 + k));
+                for (int k = 0; k < 8; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, hf * 8 + k));
                 uint32_t pk[32];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -419,39 +442,34 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) pk[k * 4 + e] = f2_to_bf16x2(f2_fma(bf16x2_to_f2(ww[e]), rs, nmr));
                 }
-                tmem_st32(tO + static_cast<uint32_t>(hh * 32), pk);
+                tmem_st32(tO + static_cast<uint32_t>(hf * 32), pk);
                 tmem_st_wait();
                 tc_fence_before();  // also orders this thread's reads of the last tile's S and O
-                mbar_arrive(bar(b0 + G_AREADY + hh));
+                mbar_arrive(bar(b0 + G_AREADY + hf));
             }
 
-            // ---- P = bf16(act(S)) as bf16 pairs into TMEM columns tS .. tS + 63 (the
-            //      second MMA's A operand, over S's columns already read), per 64-key
-            //      half of S as soon as the MMA has it; each half written releases its
-            //      half of the contraction of O.
-            bool good = true;
-            for (int h = 0; h < 2; ++h) {
-                ok = mbar_wait(guard, bar(b0 + G_SFULL + h), gph, FN_SITE_SFULL, it);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    good = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ts = tS + static_cast<uint32_t>(h * 64), tp = tS + static_cast<uint32_t>(h * 32);
+            // ---- P = bf16(act(S)) for keys 64hf .. 64hf + 63 as bf16 pairs into the
+            //      first 32 of S's TMEM columns for those keys (read just before, by
+            //      this thread): the second MMA's A operand for that half.
+            ok = mbar_wait(guard, bar(b0 + G_SFULL + hf), gph, FN_SITE_SFULL, it);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            {
+                const uint32_t ts = tS + static_cast<uint32_t>(hf * 64);
                 if (args.act == 1)
-                    fn_act_half<1>(ts, tp);
+                    fn_act_half<1>(ts, ts);
                 else if (args.act == 2)
-                    fn_act_half<2>(ts, tp);
+                    fn_act_half<2>(ts, ts);
                 else
-                    fn_act_half<0>(ts, tp);
+                    fn_act_half<0>(ts, ts);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(b0 + G_PREADY + h));
+                mbar_arrive(bar(b0 + G_PREADY + hf));
             }
-            if (!good) break;
 
-            // ---- o = P V + ln_q (residual 1), written back over P V in TMEM, and its
-            //      RMSNorm over all heads (second exchange); out = o rstd2 + q
+            // ---- o = P V + ln_q (residual 1) for this half, written back over P V in
+            //      TMEM, and its RMSNorm over all heads (second exchange);
+            //      out = o rstd2 + q
             ok = mbar_wait(guard, bar(b0 + G_OFULL), gph, FN_SITE_OFULL, it);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
@@ -459,12 +477,13 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
             {
                 uint64_t q0 = 0, q1 = 0;
 #pragma unroll 1
-                for (int seg = 0; seg < 4; ++seg) {
+                for (int seg = 0; seg < 2; ++seg) {
+                    const uint32_t to = tO + static_cast<uint32_t>(hf * 64 + seg * 32);
                     uint32_t v[32];
-                    tmem_ld32(tO + static_cast<uint32_t>(seg * 32), v);
+                    tmem_ld32(to, v);
                     uint4 w[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, seg * 4 + k));
+                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, hf * 8 + seg * 4 + k));
                     tmem_ld_wait(v);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -483,33 +502,40 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                             v[i + 1] = __float_as_uint(o1);
                         }
                     }
-                    tmem_st32(tO + static_cast<uint32_t>(seg * 32), v);
+                    tmem_st32(to, v);
                 }
                 ss = f2_hsum(f2_add(q0, q1));
                 tmem_st_wait();
             }
             {
                 const uint32_t xb = bar(C::B_X2 + slot);
-                const uint32_t dst = sR2 + static_cast<uint32_t>(((slot * C::MAXH + rank) * FN_ROWS + r) * 8);
+                const uint32_t dst =
+                    sR2 + static_cast<uint32_t>(((slot * 2 * C::MAXH + pidx) * FN_ROWS + r) * 8);
                 for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(dst, p), ss, 0.0f, mapa_shared(xb, p));
                 ok = mbar_wait<true>(guard, xb, xph, FN_SITE_X2, it);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 if (gw == 0 && lane == 0 && it + C::NSLOT < tiles) mbar_arrive_expect_tx(xb, xbytes);
             }
-            const float* rv2 =
-                reinterpret_cast<const float*>(base_ptr + C::OFF_R2 + (slot * C::MAXH * FN_ROWS + r) * 8);
             float tot = 0.0f;
-            for (int p = 0; p < H; ++p) tot += rv2[p * FN_ROWS * 2];
+            {
+                const uint32_t rb = sR2 + static_cast<uint32_t>((slot * 2 * C::MAXH * FN_ROWS + r) * 8);
+                float pt[2 * C::MAXH];
+#pragma unroll
+                for (int p = 0; p < 2 * C::MAXH; ++p)
+                    pt[p] = p < 2 * H ? ld_shared_f32(rb + static_cast<uint32_t>(p * FN_ROWS * 8)) : 0.0f;
+#pragma unroll
+                for (int p = 0; p < 2 * C::MAXH; ++p) tot += pt[p];
+            }
             const float rstd2 = rsqrtf(fmaf(tot, args.inv_hd, args.eps2));
             {
                 const uint64_t rr = f2_splat(rstd2);
 #pragma unroll 1
-                for (int seg = 0; seg < 4; ++seg) {
+                for (int seg = 0; seg < 2; ++seg) {
                     uint32_t v[32];
-                    tmem_ld32(tO + static_cast<uint32_t>(seg * 32), v);
+                    tmem_ld32(tO + static_cast<uint32_t>(hf * 64 + seg * 32), v);
                     uint4 w[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, seg * 4 + k));
+                    for (int k = 0; k < 4; ++k) w[k] = ld_shared_v4(fn_chunk(sq, r, hf * 8 + seg * 4 + k));
                     tmem_ld_wait(v);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -520,19 +546,18 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                             pk[e] = f2_to_bf16x2(f2_fma(f2_pack(v[k * 8 + 2 * e], v[k * 8 + 2 * e + 1]), rr,
                                                         bf16x2_to_f2(ww[e])));
                         // q is overwritten in place by out
-                        st_shared_v4(fn_chunk(sq, r, seg * 4 + k), pk[0], pk[1], pk[2], pk[3]);
+                        st_shared_v4(fn_chunk(sq, r, hf * 8 + seg * 4 + k), pk[0], pk[1], pk[2], pk[3]);
                     }
                 }
             }
             fence_proxy_async_smem();  // the TMA store reads the staged rows
             __syncwarp();
             if (lane == 0) {
-                // This warp's 32 rows, two 64-column boxes; none past the batch's
+                // This warp's 32 rows of its 64-column box; none past the batch's
                 // last 32-row group that holds a valid row.
-                if (m0 + gw * 32 < qlen)
-                    for (int half = 0; half < 2; ++half)
-                        tma_store_2d(&tmO, sq + static_cast<uint32_t>(half * FN_HALF_BYTES + gw * 32 * 128),
-                                     col0 + half * 64, static_cast<int32_t>(qrow0 + m0 + gw * 32));
+                if (m0 + q4 * 32 < qlen)
+                    tma_store_2d(&tmO, sq + static_cast<uint32_t>(hf * FN_HALF_BYTES + q4 * 32 * 128),
+                                 col0 + hf * 64, static_cast<int32_t>(qrow0 + m0 + q4 * 32));
                 bulk_commit();
             }
             __syncwarp();
