@@ -96,8 +96,10 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the fused GEMM kernels are built from (not the
+    attention kernel's), which a profile's counters are tied to."""
     from normalization_gemm_gb300 import _build
-    return _build.source_hash()
+    return _build.source_hash(_build.GEMM_SOURCES)
 
 
 def profiled_traffic(workload: str):
@@ -112,7 +114,7 @@ def profiled_traffic(workload: str):
     for line in text.splitlines():
         if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_hash")):
             k, v = line.strip().split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+            vals[k.strip()] = (v.split() or [""])[0].strip("`")
     if vals.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:

@@ -35,11 +35,11 @@ def nvcc() -> str:
     return exe
 
 
-def _stamp(extra_flags) -> str:
+def _stamp(extra_flags, names=None) -> str:
     h = hashlib.sha256()
     for d in (CSRC, INCLUDE):
         for name in sorted(os.listdir(d)):
-            if name.endswith((".cu", ".cuh", ".h")):
+            if name.endswith((".cu", ".cuh", ".h")) and (names is None or name in names):
                 with open(os.path.join(d, name), "rb") as fh:
                     h.update(name.encode() + fh.read())
     # flags without the machine-specific include paths
@@ -48,9 +48,16 @@ def _stamp(extra_flags) -> str:
     return h.hexdigest()
 
 
-def source_hash() -> str:
-    """Short hash of the CUDA sources, headers and flags (path independent)."""
-    return _stamp(())[:16]
+def source_hash(names=None) -> str:
+    """Short hash of the CUDA sources, headers and flags (path independent);
+    with `names`, of those files only (the sources one kernel is built from)."""
+    return _stamp((), names)[:16]
+
+
+# The files the fused GEMM kernels and their launch plans are built from: a
+# profile of one of them stays valid while these are unchanged.
+GEMM_SOURCES = ("nf_api.cu", "nf_gemm_post_ln.cu", "nf_gemm_post_rms.cu", "nf_gemm_pre.cu", "nf_gemm_plain.cu",
+                "nf_gemm_kernel.cuh", "nf_gemm_wide.cuh", "nf_internal.h", "nf_ptx.cuh", "nf.h")
 
 
 def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
