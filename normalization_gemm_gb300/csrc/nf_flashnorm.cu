@@ -10,10 +10,18 @@
 //   out  = RMSNorm(o) + q               over all H x D        (multi-CTA norm 2, residual 2)
 //
 // Layout: Q / Out [B, Lq, H, D], K / V [B, Lkv, H, D], bf16, D = Lkv = 128,
-// seen by TMA as [B*L rows, H*D columns].  The grid is one cluster of H CTAs
-// per batch (as in the blog: the cluster's CTAs share the batch index and take
-// one head each); each CTA keeps its head's K and V in shared memory and walks
-// the batch's 128-row query tiles (ceil(q_len[b] / 128) of them).
+// seen by TMA as [B*L rows, H*D columns].  A cluster of H CTAs works on one
+// batch at a time (as in the blog: the cluster's CTAs share the batch index and
+// take one head each); each CTA keeps its head's K and V in shared memory and
+// walks the batch's 128-row query tiles (ceil(q_len[b] / 128) of them).  The
+// grid is persistent: as many clusters as are resident at once, each taking
+// the next batch from a global counter when it starts the previous one (its
+// rank 0 takes it and writes it into every CTA's batch ring), so set-up,
+// teardown and the first loads are paid once per cluster rather than per batch,
+// and jagged batches balance dynamically.  Query tiles are numbered across
+// batches, so the q prefetch, the exchange slots and all phase parities run on
+// through batch switches; a batch's K and V replace the previous ones once
+// every group is done with them (the kvfree barrier).
 //
 // CTA roles, NG compute groups (NG = 2 for H <= 4; 1 above, where two groups'
 // exchange slots for up to 16 partials per row would crowd out the q buffers):
@@ -29,10 +37,11 @@
 //              (second exchange) and out = o * rstd + q, staged over the q tile
 //              and stored with TMA.  Two groups overlap one tile's exchanges
 //              and MMAs with the other tile's CUDA-core work.
-//   warp 8NG   TMA producer: K and V once, the q tiles into NQ = 4 buffers
-//              (tile it into buffer it mod 4), each refilled once its tile's
-//              output stores have read it, so a group's next tile lands while
-//              it computes the current one.
+//   warp 8NG   TMA producer: the batch sequence, each batch's K and V, the q
+//              tiles into NQ = 4 buffers (tile it into buffer it mod 4, with a
+//              record of its batch, rows and K/V load), each refilled once its
+//              tile's output stores have read it, so a group's next tile lands
+//              while it computes the current one.
 //   warp 8NG+1+g  MMA issuer of group g: S = ln_q K^T (two 64-key halves) and
 //              O = P V (tcgen05.mma, A from TMEM, B from shared memory) in the
 //              group's 256 TMEM columns (S / P 128, O / bf16(ln_q) 128); each
@@ -53,6 +62,8 @@
 //
 // Every wait is bounded; on expiry the kernel records NF_ERR_TIMEOUT with the
 // site in the device status word, drains what it issued and returns.
+#include <mutex>
+
 #include "nf_internal.h"
 #include "nf_ptx.cuh"
 
@@ -84,12 +95,17 @@ struct FnCfg {
     static constexpr int OFF_BAR = OFF_R2 + RECV_BYTES;
     static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;       // barriers + words, 1 KB realignment slack
     static_assert(SMEM_BYTES <= SMEM_OPTIN_LIMIT, "shared memory");
+    static constexpr int NB = 4;                                  // batch ring entries
     // barriers (8 bytes each): kv, qfull[NQ], qempty[NQ], GROUP_BARS per group
-    // (below), x1[NSLOT], x2[NSLOT]
+    // (below), x1[NSLOT], x2[NSLOT], bfull[NB], bempty[NB], kvfree
     static constexpr int B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + NQ, B_GROUP = 1 + 2 * NQ, GROUP_BARS = 8,
-                         B_X1 = B_GROUP + GROUP_BARS * NG, B_X2 = B_X1 + NSLOT, NBAR = B_X2 + NSLOT;
-    static_assert(NBAR * 8 <= 504, "barrier area");
-    static constexpr int OFF_TMEM_HOLDER = 504, OFF_ABORT = 508;
+                         B_X1 = B_GROUP + GROUP_BARS * NG, B_X2 = B_X1 + NSLOT, B_BFULL = B_X2 + NSLOT,
+                         B_BEMPTY = B_BFULL + NB, B_KVFREE = B_BEMPTY + NB, NBAR = B_KVFREE + 1;
+    static_assert(NBAR * 8 <= 320, "barrier area");
+    // words after the barriers: the batch ring (NB int32), the tile records
+    // (NQ x FnTile), the TMEM base, the abort flag
+    static constexpr int OFF_RING = 320, OFF_TILES = 384, OFF_TMEM_HOLDER = 504, OFF_ABORT = 508;
+    static_assert(OFF_TILES + NQ * 20 <= OFF_TMEM_HOLDER, "tile records");
     static constexpr int TMEM_COLS = 256 * NG;     // per group: S 128 columns, O 128
 };
 
@@ -101,8 +117,18 @@ constexpr int G_AREADY = 0, G_SFULL = 2, G_PREADY = 4, G_OFULL = 6, G_MMA_DONE =
 
 enum FnSite : uint32_t {
     FN_SITE_KV = 20, FN_SITE_QFULL = 21, FN_SITE_QEMPTY = 22, FN_SITE_AREADY = 23, FN_SITE_SFULL = 24,
-    FN_SITE_PREADY = 25, FN_SITE_OFULL = 26, FN_SITE_X1 = 27, FN_SITE_X2 = 28,
+    FN_SITE_PREADY = 25, FN_SITE_OFULL = 26, FN_SITE_X1 = 27, FN_SITE_X2 = 28, FN_SITE_BATCH = 29,
+    FN_SITE_BEMPTY = 30, FN_SITE_KVFREE = 31,
 };
+
+// What the producer tells the compute and MMA warps about the query tile in a
+// q buffer: its batch (-1: no more tiles for this group), its first row within
+// the batch, the batch's valid length, which K/V load (0, 1, ...) it uses and
+// whether it is its group's last tile of the batch.
+struct FnTile {
+    int32_t b, m0, qlen, kv, last;
+};
+static_assert(sizeof(FnTile) == 20, "tile record");
 
 struct FnArgs {
     int32_t B, Lq, H;
@@ -110,6 +136,7 @@ struct FnArgs {
     float eps1, eps2;
     float inv_hd;           // 1 / (H * D)
     const int32_t* q_len;  // B entries or null (Lq each)
+    int32_t* sched;        // [0] next batch to hand out, [1] clusters done; zero between launches
     uint32_t* status;
     uint64_t timeout_ns;
 };
@@ -164,10 +191,18 @@ __device__ __forceinline__ void fn_act_half(uint32_t ts, uint32_t tp) {
     }
 }
 
-__device__ __forceinline__ uint32_t fn_cluster_id() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
+// One 32-bit value into a (possibly remote) CTA's shared memory, completing 4
+// bytes of the transaction count of the barrier at the same CTA.
+__device__ __forceinline__ void fn_st_async_s32(uint32_t remote_addr, int32_t v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.s32 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "r"(v), "r"(remote_bar)
+                 : "memory");
+}
+
+// Arrive on a barrier in a (possibly remote) CTA of the cluster, releasing this
+// thread's earlier accesses at cluster scope.
+__device__ __forceinline__ void fn_arrive_remote(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
 // Bounded wait used only while draining: ignores the abort flag, records nothing.
@@ -197,9 +232,11 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
     const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
     const int H = args.H;
     const int rank = static_cast<int>(cluster_ctarank());  // this CTA's head
-    const int bidx = static_cast<int>(fn_cluster_id());     // this cluster's batch
     const uint32_t xbytes = static_cast<uint32_t>(2 * H) * FN_ROWS * 8u;  // one partial per row and column half
     const WaitGuard guard{args.status, abort_flag, args.timeout_ns};
+    const uint32_t sRing = sBar + C::OFF_RING;
+    volatile int32_t* const ring = reinterpret_cast<volatile int32_t*>(base_ptr + C::OFF_BAR + C::OFF_RING);
+    volatile FnTile* const tile_rec = reinterpret_cast<volatile FnTile*>(base_ptr + C::OFF_BAR + C::OFF_TILES);
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmQ);
@@ -225,62 +262,154 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
             mbar_init(bar(C::B_X1 + s), 1);
             mbar_init(bar(C::B_X2 + s), 1);
         }
+        for (int s = 0; s < C::NB; ++s) {
+            mbar_init(bar(C::B_BFULL + s), 1);  // the ring entry, written by the cluster's rank 0
+            mbar_init(bar(C::B_BEMPTY + s), H);  // (rank 0's) every CTA has read the entry
+        }
+        // One phase per K/V load: every group is done with it (an MMA commit
+        // after the group's last tile of the batch, or the producer's arrival for
+        // a group without tiles in it).
+        mbar_init(bar(C::B_KVFREE), NG);
         *abort_flag = 0;
         fence_mbar_init();
+        // Arm the exchange and ring barriers before any peer can write (peers
+        // write only after the cluster barrier below).
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_arrive_expect_tx(bar(C::B_X1 + s), xbytes);
+            mbar_arrive_expect_tx(bar(C::B_X2 + s), xbytes);
+        }
+        for (int s = 0; s < C::NB; ++s) mbar_arrive_expect_tx(bar(C::B_BFULL + s), 4);
     }
     if (warp == C::PRODUCER_WARP) {
         tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
         tmem_relinquish();
     }
-    // Global memory (q_len included) is read only after the preceding grid.
+    // Global memory (the scheduler words and q_len included) is touched only
+    // after the preceding grid.
     griddep_wait();
     griddep_launch_dependents();
-    const int qlen = args.q_len ? min(max(args.q_len[bidx], 0), args.Lq) : args.Lq;
-    const int tiles = (qlen + FN_ROWS - 1) / FN_ROWS;  // the same for every CTA of the cluster
-    if (threadIdx.x == 0) {
-        // Arm the exchange barriers of the first NSLOT tiles before any peer
-        // can send (peers send only after the cluster barrier below).
-        for (int s = 0; s < C::NSLOT && s < tiles; ++s) {
-            mbar_arrive_expect_tx(bar(C::B_X1 + s), xbytes);
-            mbar_arrive_expect_tx(bar(C::B_X2 + s), xbytes);
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     cluster_arrive_release();
     cluster_wait_acquire();
     const uint32_t tmem_base = *tmem_holder;
-    const int64_t qrow0 = static_cast<int64_t>(bidx) * args.Lq;  // the batch's first row in Q / Out
-    const int col0 = rank * FN_D;                                 // this head's first column
+    const int col0 = rank * FN_D;  // this head's first column
 
     if (warp == C::PRODUCER_WARP) {
         // ======================================================== TMA producer
-        if (lane == 0 && tiles > 0) {
-            mbar_arrive_expect_tx(bar(C::B_KV), 2 * FN_TILE_BYTES);
-            const int krow = bidx * FN_LKV;
-            for (int kt = 0; kt < 2; ++kt) {
-                // K: 128 keys x 64 d (K-major B of S); V: 64 keys x 64 d boxes (MN-major B of O)
-                tma_load_2d(sK + kt * FN_HALF_BYTES, &tmK, bar(C::B_KV), col0 + kt * 64, krow);
-                for (int i = 0; i < 2; ++i)
-                    tma_load_2d(sV + kt * FN_HALF_BYTES + i * (FN_HALF_BYTES / 2), &tmV, bar(C::B_KV),
-                                col0 + i * 64, krow + kt * 64);
+        // The cluster walks batches handed out one at a time by a global
+        // counter (the cluster's rank 0 takes them and publishes each in every
+        // CTA's batch ring); the CTAs of a cluster see the same batches, hence
+        // the same sequence of query tiles t = 0, 1, ...
+        if (lane == 0) {
+            int t = 0;          // query tiles issued
+            int kv_loads = 0;   // K/V loads issued (one per batch with tiles)
+            // rank 0: entry k of the ring = the next batch from the counter, or -1
+            auto publish = [&](int k) -> bool {
+                const int s = k % C::NB;
+                if (k >= C::NB && !mbar_wait<true>(guard, bar(C::B_BEMPTY + s), static_cast<uint32_t>(k / C::NB - 1) & 1u,
+                                                   FN_SITE_BEMPTY, k))
+                    return false;
+                const int i = atomicAdd(args.sched, 1);
+                const int b = i < args.B ? i : -1;
+                for (int p = 0; p < H; ++p)
+                    fn_st_async_s32(mapa_shared(sRing + 4u * s, p), b, mapa_shared(bar(C::B_BFULL + s), p));
+                return true;
+            };
+            bool ok = rank != 0 || publish(0);
+            for (int nb = 0; ok; ++nb) {
+                const int s = nb % C::NB;
+                if (!(ok = mbar_wait<true>(guard, bar(C::B_BFULL + s), static_cast<uint32_t>(nb / C::NB) & 1u,
+                                           FN_SITE_BATCH, nb)))
+                    break;
+                const int b = ring[s];
+                mbar_arrive_expect_tx(bar(C::B_BFULL + s), 4);             // for entry nb + NB
+                fn_arrive_remote(mapa_shared(bar(C::B_BEMPTY + s), 0));   // rank 0 may refill the entry
+                if (b < 0) break;
+                if (rank == 0 && !(ok = publish(nb + 1))) break;           // ahead of this batch's loads
+                const int qlen = args.q_len ? min(max(args.q_len[b], 0), args.Lq) : args.Lq;
+                const int tiles = (qlen + FN_ROWS - 1) / FN_ROWS;
+                if (tiles == 0) continue;
+                const int kv = kv_loads;  // this batch's K/V load
+                const int64_t qrow0 = static_cast<int64_t>(b) * args.Lq;
+                const int t_first = t;
+                // q tile m of this batch into the next buffer, with its record
+                auto issue_tile = [&](int m) -> bool {
+                    const int qb = t % C::NQ;
+                    if (!mbar_wait(guard, bar(C::B_QEMPTY + qb), (static_cast<uint32_t>(t / C::NQ) & 1u) ^ 1u,
+                                   FN_SITE_QEMPTY, t))
+                        return false;
+                    tile_rec[qb].b = b;
+                    tile_rec[qb].m0 = m * FN_ROWS;
+                    tile_rec[qb].qlen = qlen;
+                    tile_rec[qb].kv = kv;
+                    tile_rec[qb].last = m + NG >= tiles ? 1 : 0;
+                    const uint32_t fb = bar(C::B_QFULL + qb);
+                    mbar_arrive_expect_tx(fb, FN_TILE_BYTES);  // releases the record with the phase
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_2d(sQ + qb * FN_TILE_BYTES + half * FN_HALF_BYTES, &tmQ, fb, col0 + half * 64,
+                                    static_cast<int32_t>(qrow0 + m * FN_ROWS));
+                    ++t;
+                    return true;
+                };
+                // Tiles whose buffer is already free go out before this batch's K and
+                // V (at most NQ: their buffers were freed by earlier batches' tiles),
+                // so their LayerNorm overlaps the wait below; the rest follow the
+                // K/V load.
+                int m = 0;
+                while (m < tiles && t < t_first + C::NQ &&
+                       mbar_try_wait(bar(C::B_QEMPTY + t % C::NQ), (static_cast<uint32_t>(t / C::NQ) & 1u) ^ 1u))
+                    if (!(ok = issue_tile(m++))) break;
+                if (!ok) break;
+                // K and V are overwritten once every group is done with the previous
+                // load: phase kv - 1 of the kvfree barrier.  (Its phases run in step
+                // with the loads, so the parity test cannot alias: a wait on a
+                // barrier's per-tile phases, seen only at batch switches, could.)
+                if (kv > 0 &&
+                    !(ok = mbar_wait(guard, bar(C::B_KVFREE), static_cast<uint32_t>(kv - 1) & 1u, FN_SITE_KVFREE, t)))
+                    break;
+                mbar_arrive_expect_tx(bar(C::B_KV), 2 * FN_TILE_BYTES);
+                const int krow = b * FN_LKV;
+                for (int kt = 0; kt < 2; ++kt) {
+                    // K: 128 keys x 64 d (K-major B of S); V: 64 keys x 64 d boxes (MN-major B of O)
+                    tma_load_2d(sK + kt * FN_HALF_BYTES, &tmK, bar(C::B_KV), col0 + kt * 64, krow);
+                    for (int i = 0; i < 2; ++i)
+                        tma_load_2d(sV + kt * FN_HALF_BYTES + i * (FN_HALF_BYTES / 2), &tmV, bar(C::B_KV),
+                                    col0 + i * 64, krow + kt * 64);
+                }
+                ++kv_loads;
+                for (int n = tiles; n < NG; ++n) mbar_arrive(bar(C::B_KVFREE));  // each group without a tile here
+                for (; m < tiles && ok; ++m) ok = issue_tile(m);
+                if (!ok) break;
             }
-            for (int it = 0; it < tiles; ++it) {
-                const int qb = it % C::NQ;
-                const uint32_t ph = static_cast<uint32_t>(it / C::NQ) & 1u;
-                if (!mbar_wait(guard, bar(C::B_QEMPTY + qb), ph ^ 1u, FN_SITE_QEMPTY, it)) break;
-                const uint32_t fb = bar(C::B_QFULL + qb);
-                mbar_arrive_expect_tx(fb, FN_TILE_BYTES);
-                for (int half = 0; half < 2; ++half)
-                    tma_load_2d(sQ + qb * FN_TILE_BYTES + half * FN_HALF_BYTES, &tmQ, fb, col0 + half * 64,
-                                static_cast<int32_t>(qrow0 + it * FN_ROWS));
-            }
-            // Every load issued has landed before the CTA may exit.
-            fn_drain(bar(C::B_KV), 0, args.timeout_ns);
-            for (int j = 0; j < C::NQ && j < tiles; ++j) {
-                const int last = j + ((tiles - 1 - j) / C::NQ) * C::NQ;  // the last tile that used buffer j
+            // Every load issued has landed before the CTA may exit (waited here,
+            // before the end records below complete further phases of the q
+            // buffers' barriers).
+            const int loaded = t;  // tiles 0 .. loaded - 1 were loaded, in order
+            if (kv_loads > 0) fn_drain(bar(C::B_KV), static_cast<uint32_t>(kv_loads - 1) & 1u, args.timeout_ns);
+            for (int j = 0; j < C::NQ && j < loaded; ++j) {
+                const int last = j + (loaded - 1 - j) / C::NQ * C::NQ;  // the last tile loaded into buffer j
                 fn_drain(bar(C::B_QFULL + j), static_cast<uint32_t>(last / C::NQ) & 1u, args.timeout_ns);
+            }
+            // One end record per group (its next tile), so every group and MMA warp stops.
+            for (int k = 0; k < NG && ok; ++k, ++t) {
+                const int qb = t % C::NQ;
+                if (!(ok = mbar_wait(guard, bar(C::B_QEMPTY + qb), (static_cast<uint32_t>(t / C::NQ) & 1u) ^ 1u,
+                                     FN_SITE_QEMPTY, t)))
+                    break;
+                tile_rec[qb].b = -1;
+                mbar_arrive(bar(C::B_QFULL + qb));
+            }
+            if (rank == 0) {
+                // This cluster takes no more batches; the last cluster to finish
+                // zeroes the counters for the next launch on this stream.
+                __threadfence();
+                const int clusters = static_cast<int>(gridDim.x) / H;
+                if (atomicAdd(args.sched + 1, 1) == clusters - 1) {
+                    atomicExch(args.sched, 0);
+                    atomicExch(args.sched + 1, 0);
+                }
             }
         }
         __syncwarp();
@@ -288,7 +417,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
         // ======================================================== MMA issuer of group g
         const int g = warp - C::MMA_WARP0;
         const int b0 = C::B_GROUP + g * C::GROUP_BARS;
-        if (lane == 0 && g < tiles) {
+        if (lane == 0) {
             constexpr uint32_t IDESC_S = idesc_bf16_f32(FN_ROWS, FN_LKV / 2, false);  // B = K (K-major), 64 keys
             constexpr uint32_t IDESC_O = idesc_bf16_f32(FN_ROWS, FN_D, true);         // B = V (MN-major)
             const uint32_t tS = tmem_base + static_cast<uint32_t>(g * 256), tO = tS + 128u;
@@ -301,11 +430,18 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                                 smem_desc_sw128(sK + kt * FN_HALF_BYTES + n * (FN_HALF_BYTES / 2) + j * 32, 16, 1024),
                                 IDESC_S, (kt | j) != 0 ? 1u : 0u);
             };
-            bool ok = mbar_wait(guard, bar(C::B_KV), 0, FN_SITE_KV, 0);
-            for (int it = g; it < tiles && ok; it += NG) {
-                const uint32_t ph = static_cast<uint32_t>(it / NG) & 1u;
-                // ln_q columns 0-63 written: the first half of both S halves' contraction
+            bool ok = true;
+            int kv_seen = -1;
+            for (int it = g, k = 0; ok; it += NG, ++k) {
+                const uint32_t ph = static_cast<uint32_t>(k) & 1u;
+                // ln_q columns 0-63 written (or the group's end record seen)
                 if (!(ok = mbar_wait(guard, bar(b0 + G_AREADY), ph, FN_SITE_AREADY, it))) break;
+                const int kv = tile_rec[it % C::NQ].kv, last = tile_rec[it % C::NQ].last;
+                if (tile_rec[it % C::NQ].b < 0) break;
+                if (kv != kv_seen) {  // this tile's batch has its own K and V
+                    if (!(ok = mbar_wait(guard, bar(C::B_KV), static_cast<uint32_t>(kv) & 1u, FN_SITE_KV, it))) break;
+                    kv_seen = kv;
+                }
                 tc_fence_after();
                 mma_s(0, 0);
                 mma_s(1, 0);
@@ -330,6 +466,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit(bar(b0 + G_OFULL));
+                if (last) mma_commit(bar(C::B_KVFREE));  // this group is done with this K and V
             }
             mma_commit(bar(b0 + G_MMA_DONE));
             fn_drain(bar(b0 + G_MMA_DONE), 0, args.timeout_ns);
@@ -345,16 +482,23 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
         const int pidx = rank * 2 + hf;  // this thread's partial in the exchanges
         const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + static_cast<uint32_t>(g * 256);
         const uint32_t tS = t_lane, tO = t_lane + 128u;
-        for (int it = g; it < tiles; it += NG) {
+        for (int it = g, k = 0;; it += NG, ++k) {
             const int qb = it % C::NQ;
             const uint32_t qph = static_cast<uint32_t>(it / C::NQ) & 1u;  // q buffer use count parity
-            const uint32_t gph = static_cast<uint32_t>(it / NG) & 1u;     // this group's tile count parity
+            const uint32_t gph = static_cast<uint32_t>(k) & 1u;            // this group's tile count parity
             const int slot = it % C::NSLOT;
             const uint32_t xph = static_cast<uint32_t>(it / C::NSLOT) & 1u;
-            const int m0 = it * FN_ROWS;
             const uint32_t sq = sQ + static_cast<uint32_t>(qb * FN_TILE_BYTES);
             bool ok = mbar_wait(guard, bar(C::B_QFULL + qb), qph, FN_SITE_QFULL, it);
             if (!__all_sync(0xffffffffu, ok)) break;
+            const int tb = tile_rec[qb].b;
+            if (tb < 0) {
+                // No more tiles for this group; the MMA warp reads the same record.
+                if (hf == 0) mbar_arrive(bar(b0 + G_AREADY));
+                break;
+            }
+            const int m0 = tile_rec[qb].m0, qlen = tile_rec[qb].qlen;
+            const int64_t qrow0 = static_cast<int64_t>(tb) * args.Lq;  // the batch's first row in Q / Out
             if (m0 + r >= qlen) {
                 // A row past q_len: zero it once, so that every later step gives
                 // exactly 0 for it, whatever the caller's buffer holds there.
@@ -396,7 +540,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(dst, p), mean_c, m2_c, mapa_shared(xb, p));
                 ok = mbar_wait<true>(guard, xb, xph, FN_SITE_X1, it);
                 if (!__all_sync(0xffffffffu, ok)) break;
-                if (gw == 0 && lane == 0 && it + C::NSLOT < tiles) mbar_arrive_expect_tx(xb, xbytes);
+                if (gw == 0 && lane == 0) mbar_arrive_expect_tx(xb, xbytes);  // for tile it + NSLOT
             }
             if (it >= NG && lane == 0) {
                 // The output stores of this group's previous tile have read its q
@@ -514,7 +658,7 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 for (int p = 0; p < H; ++p) st_async_f32x2(mapa_shared(dst, p), ss, 0.0f, mapa_shared(xb, p));
                 ok = mbar_wait<true>(guard, xb, xph, FN_SITE_X2, it);
                 if (!__all_sync(0xffffffffu, ok)) break;
-                if (gw == 0 && lane == 0 && it + C::NSLOT < tiles) mbar_arrive_expect_tx(xb, xbytes);
+                if (gw == 0 && lane == 0) mbar_arrive_expect_tx(xb, xbytes);  // for tile it + NSLOT
             }
             float tot = 0.0f;
             {
@@ -577,35 +721,81 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
     }
 }
 
+// Scheduler words of the persistent grid, one pair per (device, stream): zero
+// when the module loads, and zeroed again by the last cluster of every launch,
+// so launches on one stream (which run one after the other) reuse them.
+constexpr int kFnMaxSlots = 64;
+__device__ int32_t g_fn_sched[kFnMaxSlots][2];
+
+struct FnSlot {
+    int device;
+    cudaStream_t stream;
+};
+std::mutex g_fn_mu;
+FnSlot g_fn_slots[kFnMaxSlots];
+int g_fn_nslots = 0;
+
+cudaError_t fn_sched_words(int device, cudaStream_t stream, int32_t** out) {
+    std::lock_guard<std::mutex> lock(g_fn_mu);
+    int idx = -1;
+    for (int i = 0; i < g_fn_nslots && idx < 0; ++i)
+        if (g_fn_slots[i].device == device && g_fn_slots[i].stream == stream) idx = i;
+    if (idx < 0) {
+        if (g_fn_nslots == kFnMaxSlots) return cudaErrorLaunchOutOfResources;  // too many streams
+        idx = g_fn_nslots++;
+        g_fn_slots[idx] = FnSlot{device, stream};
+    }
+    void* base = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&base, g_fn_sched);
+    if (e != cudaSuccess) return e;
+    *out = static_cast<int32_t*>(base) + 2 * idx;
+    return cudaSuccess;
+}
+
+constexpr int kFnMaxDevices = 64;
+
 template <int NG>
-cudaError_t launch_fn(const CUtensorMap* m, const FnArgs& args, bool overlap, cudaStream_t stream) {
+cudaError_t launch_fn(const CUtensorMap* m, FnArgs args, bool overlap, cudaStream_t stream) {
     using C = FnCfg<NG>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(nf_flashnorm_fwd_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    if (device < 0 || device >= kFnMaxDevices) return cudaErrorInvalidDevice;
+    static bool attr_set[kFnMaxDevices] = {};
+    static int max_clusters[kFnMaxDevices][FnCfg<NG>::MAXH + 1] = {};
+    if (!attr_set[device]) {
+        e = cudaFuncSetAttribute(nf_flashnorm_fwd_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[device] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    int n = 0;
-    cfg.gridDim = dim3(static_cast<unsigned>(args.B * args.H));
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(args.H);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = static_cast<unsigned>(args.H);
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-    if (overlap) {
-        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[n].val.programmaticStreamSerializationAllowed = 1;
-        ++n;
-    }
     cfg.attrs = attr;
-    cfg.numAttrs = static_cast<unsigned>(n);
+    cfg.numAttrs = 1;
+    int& maxc = max_clusters[device][args.H];
+    if (maxc == 0) {
+        // A persistent grid: as many clusters as can be resident at once.
+        cfg.gridDim = dim3(static_cast<unsigned>(args.H));
+        e = cudaOccupancyMaxActiveClusters(&maxc, nf_flashnorm_fwd_kernel<NG>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (maxc <= 0) return cudaErrorInvalidConfiguration;
+    }
+    if ((e = fn_sched_words(device, stream, &args.sched)) != cudaSuccess) return e;
+    const int clusters = args.B < maxc ? args.B : maxc;
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * args.H));
+    if (overlap) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, nf_flashnorm_fwd_kernel<NG>, m[0], m[1], m[2], m[3], args);
 }
 
@@ -613,6 +803,7 @@ cudaError_t launch_fn(const CUtensorMap* m, const FnArgs& args, bool overlap, cu
 
 cudaError_t launch_flashnorm_fwd(const void* tmaps, const FlashNormLaunch& a, bool overlap, cudaStream_t stream) {
     const CUtensorMap* m = static_cast<const CUtensorMap*>(tmaps);
+    if (a.B <= 0) return cudaSuccess;
     FnArgs args;
     args.B = a.B;
     args.Lq = a.Lq;
@@ -622,6 +813,7 @@ cudaError_t launch_flashnorm_fwd(const void* tmaps, const FlashNormLaunch& a, bo
     args.eps2 = a.eps2;
     args.inv_hd = 1.0f / static_cast<float>(a.H * FN_D);
     args.q_len = a.q_len;
+    args.sched = nullptr;
     args.status = a.status;
     args.timeout_ns = a.timeout_ns;
     // Two compute groups' exchange slots fit shared memory up to 4 heads per cluster.
