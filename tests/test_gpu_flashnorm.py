@@ -104,3 +104,51 @@ def test_flashnorm_many_clusters(dev, orc):
     got = to_f64(a[torch.from_numpy(pick).to(dev)].reshape(len(pick) * Lq, H * 128)).reshape(len(pick), Lq, H, 128)
     g, w = _valid_rows(got, want, sub["q_len"])
     assert_close(g, w, "FlashNormAttention many clusters")
+
+
+@pytest.mark.parametrize("H", [2, 6], ids=["two_groups", "one_group"])
+def test_flashnorm_persistent_batch_mix(dev, orc, H):
+    """Many more batches than resident clusters with many empty and one-tile
+    batches (a group with no tile in a batch, K/V reloads between one-tile
+    batches), three launches in a row on one stream (the batch counter is
+    reset by each launch): identical bits each time and oracle parity on a
+    sample that includes every length class."""
+    import torch
+    B, Lq = 400, 384
+    inp = nf_inputs.fna_inputs(B, Lq, 128, H, 128, seed=11 + H)
+    classes = np.array([0, 1, 0, 127, 128, 129, 0, 255, 256, 384, 1, 0], np.int32)
+    inp["q_len"] = classes[np.arange(B) % len(classes)]
+    runs = [_run(dev, inp, nf.ACT_SILU, True) for _ in range(3)]
+    for r in runs[1:]:
+        assert torch.equal(torch.nan_to_num(runs[0], nan=7.0), torch.nan_to_num(r, nan=7.0))
+    pick = np.array([0, 1, 3, 4, 5, 7, 8, 9, 10, 200, 397, 399])
+    sub = {k: np.ascontiguousarray(inp[k][pick]) for k in ("Q", "K", "V", "q_len")}
+    want = orc.flashnorm_attn_fwd(sub["Q"], sub["K"], sub["V"], nf.ACT_SILU, 1e-5, 1e-6, q_len=sub["q_len"])
+    got = to_f64(runs[0][torch.from_numpy(pick).to(dev)].reshape(len(pick) * Lq, H * 128)).reshape(len(pick), Lq, H, 128)
+    g, w = _valid_rows(got, want, sub["q_len"])
+    assert_close(g, w, f"FlashNormAttention batch mix H={H}")
+
+
+def test_flashnorm_two_streams(dev):
+    """Two independent problems launched on two streams at once (each stream
+    has its own batch counter) give the same bits as when run one after the
+    other."""
+    import torch
+    H, Lq = 4, 512
+    ia = nf_inputs.fna_inputs(96, Lq, 128, H, 128, seed=21)
+    ib = nf_inputs.fna_inputs(80, Lq, 128, H, 128, seed=22)
+    ref_a = _run(dev, ia, nf.ACT_GELU_TANH, True)
+    ref_b = _run(dev, ib, nf.ACT_GELU_TANH, True)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for inp, s in ((ia, s1), (ib, s2)):
+        q, k, v = _dev4(inp["Q"], dev), _dev4(inp["K"], dev), _dev4(inp["V"], dev)
+        ql = torch.from_numpy(inp["q_len"]).to(dev)
+        out = torch.full_like(q, float("nan"))
+        torch.cuda.synchronize()
+        outs.append((q, k, v, ql, out, s))
+    for q, k, v, ql, out, s in outs:
+        nf.flashnorm_attn_fwd(q, k, v, act=nf.ACT_GELU_TANH, eps1=1e-5, eps2=1e-6, q_len=ql, out=out, stream=s)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.nan_to_num(outs[0][4], nan=7.0), torch.nan_to_num(ref_a, nan=7.0))
+    assert torch.equal(torch.nan_to_num(outs[1][4], nan=7.0), torch.nan_to_num(ref_b, nan=7.0))
