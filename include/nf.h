@@ -165,9 +165,16 @@ nf_status nf_gemm_postnorm_rms_res(const void* X, const void* W, const void* R,
  * 16-byte aligned.  q_len: device int32[B] (4-byte aligned) or NULL (Lq for
  * every batch); rows t >= q_len[b] of Out are left as they were, except those
  * inside the last 32-row group holding a valid row, which are written as 0.
- * Supported: D = Lkv = 128, 1 <= H <= 8 (one thread-block cluster of H CTAs
- * per batch exchanges the row statistics of both norms through distributed
- * shared memory), Lq a multiple of 128; else NF_ERR_UNSUPPORTED_SHAPE.
+ * Supported: D = Lkv = 128, 1 <= H <= 8 (a thread-block cluster of H CTAs
+ * works on one batch at a time and exchanges the row statistics of both norms
+ * through distributed shared memory), Lq a multiple of 128; else
+ * NF_ERR_UNSUPPORTED_SHAPE.
+ * Scheduling: a persistent grid of as many clusters as fit on the device takes
+ * batches one at a time from a counter the library keeps per (device, stream)
+ * in device memory (no allocation; zero again when a launch ends).  Calls on
+ * one stream run one after the other; calls on different streams may overlap.
+ * The counters serve at most 64 (device, stream) pairs per process: a call
+ * from a 65th pair fails with NF_ERR_CUDA.
  */
 #define NF_ACT_IDENTITY 0
 #define NF_ACT_GELU_TANH 1
