@@ -763,12 +763,6 @@ cudaError_t launch_fn(const CUtensorMap* m, FnArgs args, bool overlap, cudaStrea
     if (device < 0 || device >= kFnMaxDevices) return cudaErrorInvalidDevice;
     static bool attr_set[kFnMaxDevices] = {};
     static int max_clusters[kFnMaxDevices][FnCfg<NG>::MAXH + 1] = {};
-    if (!attr_set[device]) {
-        e = cudaFuncSetAttribute(nf_flashnorm_fwd_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set[device] = true;
-    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -780,13 +774,25 @@ cudaError_t launch_fn(const CUtensorMap* m, FnArgs args, bool overlap, cudaStrea
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int& maxc = max_clusters[device][args.H];
-    if (maxc == 0) {
-        // A persistent grid: as many clusters as can be resident at once.
-        cfg.gridDim = dim3(static_cast<unsigned>(args.H));
-        e = cudaOccupancyMaxActiveClusters(&maxc, nf_flashnorm_fwd_kernel<NG>, &cfg);
-        if (e != cudaSuccess) return e;
-        if (maxc <= 0) return cudaErrorInvalidConfiguration;
+    int maxc = 0;
+    {
+        // Per-device set-up, once, under the launcher's lock.
+        std::lock_guard<std::mutex> lock(g_fn_mu);
+        if (!attr_set[device]) {
+            e = cudaFuncSetAttribute(nf_flashnorm_fwd_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            attr_set[device] = true;
+        }
+        int& cached = max_clusters[device][args.H];
+        if (cached == 0) {
+            // A persistent grid: as many clusters as can be resident at once.
+            cfg.gridDim = dim3(static_cast<unsigned>(args.H));
+            e = cudaOccupancyMaxActiveClusters(&cached, nf_flashnorm_fwd_kernel<NG>, &cfg);
+            if (e != cudaSuccess) return e;
+            if (cached <= 0) return cudaErrorInvalidConfiguration;
+        }
+        maxc = cached;
     }
     if ((e = fn_sched_words(device, stream, &args.sched)) != cudaSuccess) return e;
     const int clusters = args.B < maxc ? args.B : maxc;
