@@ -152,3 +152,24 @@ def test_flashnorm_two_streams(dev):
     torch.cuda.synchronize()
     assert torch.equal(torch.nan_to_num(outs[0][4], nan=7.0), torch.nan_to_num(ref_a, nan=7.0))
     assert torch.equal(torch.nan_to_num(outs[1][4], nan=7.0), torch.nan_to_num(ref_b, nan=7.0))
+
+
+def test_flashnorm_all_batches_empty(dev):
+    """Every q_len is 0: no K/V is loaded, no row is written, the call succeeds."""
+    import torch
+    inp = nf_inputs.fna_inputs(5, 256, 128, 4, 128, seed=31)
+    inp["q_len"] = np.zeros(5, np.int32)
+    out = _run(dev, inp, nf.ACT_GELU_TANH, True, sentinel=3.0)
+    assert torch.all(out == 3.0)
+
+
+def test_flashnorm_full_length(dev, orc):
+    """Dense batches of the benchmark's maximum length (8 tiles each, so both
+    compute groups cycle through all four q buffers twice), every row against
+    the oracle."""
+    B, Lq, H = 2, 1024, 4
+    inp = nf_inputs.fna_inputs(B, Lq, 128, H, 128, seed=33, jagged=False)
+    out = _run(dev, inp, nf.ACT_GELU_TANH, False)
+    want = orc.flashnorm_attn_fwd(inp["Q"], inp["K"], inp["V"], nf.ACT_GELU_TANH, 1e-5, 1e-6)
+    got = to_f64(out.reshape(B * Lq, H * 128)).reshape(B, Lq, H, 128)
+    assert_close(got.reshape(B * Lq, -1), want.reshape(B * Lq, -1), "FlashNormAttention full length")
