@@ -356,9 +356,13 @@ __global__ void __launch_bounds__(FnCfg<NG>::THREADS, 1)
                 // Tiles whose buffer is already free go out before this batch's K and
                 // V (at most NQ: their buffers were freed by earlier batches' tiles),
                 // so their LayerNorm overlaps the wait below; the rest follow the
-                // K/V load.
+                // K/V load.  Only once the previous K/V load has landed, though: an
+                // MMA warp whose group had no tile in the previous batch waits for
+                // this batch's load by parity, which is exact only if the load
+                // before it is complete.
                 int m = 0;
                 while (m < tiles && t < t_first + C::NQ &&
+                       (kv == 0 || mbar_try_wait(bar(C::B_KV), static_cast<uint32_t>(kv - 1) & 1u)) &&
                        mbar_try_wait(bar(C::B_QEMPTY + t % C::NQ), (static_cast<uint32_t>(t / C::NQ) & 1u) ^ 1u))
                     if (!(ok = issue_tile(m++))) break;
                 if (!ok) break;

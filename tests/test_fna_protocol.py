@@ -1,0 +1,213 @@
+"""A model of the FlashNormAttention forward kernel's synchronisation, checked
+under random interleavings (CPU only).
+
+The persistent kernel (one CTA of a cluster; the cluster's CTAs run the same
+sequence, so the cross-CTA exchanges add no ordering the model needs) has a
+TMA producer and NG compute groups, each with its MMA warp, that talk through
+mbarriers waited on by phase PARITY.  A parity wait for completion #c is only
+correct if, every time it is evaluated, the barrier has completed c or c + 1
+phases: at c - 1 or fewer the parity reads an older phase as done, at c + 2 or
+more it waits for a phase that may never come.  The model encodes the
+protocol's waits and arrivals in the kernel's order and checks that rule for
+every wait and try-wait, that every arrival counts toward the phase it is meant
+for, that K and V are never replaced under a tile still to use them, and that
+every schedule finishes.
+
+A variant with the first persistent producer's rule (waiting, at a batch
+switch, on each group's per-tile O barrier for its last tile) must be caught.
+"""
+import random
+
+import pytest
+
+NQ = 4          # q tile buffers
+END = None      # end record
+
+
+class Bar:
+    """An mbarrier: completed phases and arrivals in the current phase."""
+
+    def __init__(self, name, count=1):
+        self.name, self.count, self.done, self.arrivals = name, count, 0, 0
+
+    def arrive(self, phase):
+        assert self.done == phase, f"{self.name}: arrival for phase {phase} while at phase {self.done}"
+        self.arrivals += 1
+        if self.arrivals == self.count:
+            self.done += 1
+            self.arrivals = 0
+
+
+class Violation(Exception):
+    pass
+
+
+class State:
+    def __init__(self, ng):
+        self.ng = ng
+        self.qfull = [Bar(f"qfull{j}") for j in range(NQ)]
+        self.qempty = [Bar(f"qempty{j}") for j in range(NQ)]
+        self.kvload = Bar("kv")
+        self.kvfree = Bar("kvfree", count=ng)
+        self.ofull = [Bar(f"ofull{g}") for g in range(ng)]
+        self.rec = [None] * NQ
+        self.kv_in_buffer = -1          # the last K/V load issued into the single buffer
+        self.inflight = {}              # group -> kv of the tile whose MMAs are in flight
+
+
+def check_parity(bar, c):
+    """The rule for a parity wait on completion #c, at evaluation time."""
+    if not (c <= bar.done <= c + 1):
+        raise Violation(f"{bar.name}: parity wait for completion {c} evaluated at {bar.done} completed")
+
+
+def producer(st, batches, rule="current"):
+    ng, t, kv_loads = st.ng, 0, 0
+    for T in batches:
+        if T == 0:
+            continue
+        kv, t_first, m = kv_loads, t, 0
+        # tiles whose buffer is already free go first (non-blocking try-waits),
+        # once the previous K/V load has landed
+        while m < T and t < t_first + NQ and rule != "kv_first":
+            if rule == "current" and kv > 0:
+                check_parity(st.kvload, kv - 1)
+                if st.kvload.done < kv:
+                    break
+            if t >= NQ:
+                bar, c = st.qempty[t % NQ], t // NQ - 1
+                check_parity(bar, c)
+                if bar.done < c + 1:
+                    break
+            st.rec[t % NQ] = (kv, m + ng >= T)
+            yield ("async", ("q", t))
+            t, m = t + 1, m + 1
+        if rule == "per_tile_o":
+            for j in range(t_first - ng, t_first):
+                if j >= 0:
+                    yield ("wait", st.ofull[j % ng], j // ng)
+        elif kv > 0:
+            yield ("wait", st.kvfree, kv - 1)
+        for g, kvt in st.inflight.items():
+            assert kvt >= kv, f"K/V load {kv} issued while group {g} still computes with load {kvt}"
+        st.kv_in_buffer = kv
+        yield ("async", ("kv", kv))
+        kv_loads += 1
+        for _ in range(max(0, ng - T)):
+            st.kvfree.arrive(kv)
+        while m < T:
+            if t >= NQ:
+                yield ("wait", st.qempty[t % NQ], t // NQ - 1)
+            st.rec[t % NQ] = (kv, m + ng >= T)
+            yield ("async", ("q", t))
+            t, m = t + 1, m + 1
+    for _ in range(ng):
+        if t >= NQ:
+            yield ("wait", st.qempty[t % NQ], t // NQ - 1)
+        st.rec[t % NQ] = END
+        st.qfull[t % NQ].arrive(t // NQ)
+        t += 1
+
+
+def group(st, g):
+    ng, it, k, kv_seen = st.ng, g, 0, -1
+    while True:
+        yield ("wait", st.qfull[it % NQ], it // NQ)
+        rec = st.rec[it % NQ]
+        if rec is END:
+            return
+        kv, last = rec
+        if it >= ng:  # at the LayerNorm exchange: the group's previous tile's buffer is free
+            st.qempty[(it - ng) % NQ].arrive((it - ng) // NQ)
+        if kv != kv_seen:
+            yield ("wait", st.kvload, kv)
+            kv_seen = kv
+        assert st.kv_in_buffer == kv, f"group {g} tile {it}: K/V buffer holds load {st.kv_in_buffer}, not {kv}"
+        st.inflight[g] = kv
+        yield ("async", ("o", g, k, kv if last else None))
+        yield ("wait", st.ofull[g], k)
+        it, k = it + ng, k + 1
+
+
+def run(batches, ng, seed, rule="current"):
+    rng = random.Random(seed)
+    st = State(ng)
+    procs = {"p": producer(st, batches, rule)}
+    for g in range(ng):
+        procs[f"g{g}"] = group(st, g)
+    waiting = {}        # name -> (bar, c)
+    events = []         # pending asynchronous completions
+
+    def step(name):
+        try:
+            req = procs[name].send(None)
+        except StopIteration:
+            del procs[name]
+            return
+        if req[0] == "wait":
+            _, bar, c = req
+            check_parity(bar, c)
+            if bar.done < c + 1:
+                waiting[name] = (bar, c)
+        elif req[0] == "async":
+            events.append(req[1])
+
+    for _ in range(200000):
+        if not procs and not events:
+            return
+        ready = [n for n in procs if n not in waiting]
+        choices = [("proc", n) for n in ready] + [("event", i) for i in range(len(events))]
+        if not choices:
+            raise Violation("deadlock: " + ", ".join(f"{n} waits {b.name} #{c}" for n, (b, c) in waiting.items()))
+        kind, x = rng.choice(choices)
+        if kind == "proc":
+            step(x)
+        else:
+            ev = events.pop(x)
+            if ev[0] == "q":
+                st.qfull[ev[1] % NQ].arrive(ev[1] // NQ)
+            elif ev[0] == "kv":
+                st.kvload.arrive(ev[1])
+            else:
+                _, g, k, kv_last = ev
+                st.ofull[g].arrive(k)
+                st.inflight.pop(g, None)
+                if kv_last is not None:
+                    st.kvfree.arrive(kv_last)
+        for n, (bar, c) in list(waiting.items()):
+            check_parity(bar, c)
+            if bar.done >= c + 1:
+                del waiting[n]
+    raise Violation("did not finish")
+
+
+def _batches(rng):
+    n = rng.randint(1, 24)
+    return [rng.choice([0, 0, 1, 1, 2, 3, 4, 5, 8]) for _ in range(n)]
+
+
+@pytest.mark.parametrize("rule", ["current", "kv_first"])
+@pytest.mark.parametrize("ng", [1, 2])
+def test_protocol_random_schedules(ng, rule):
+    """The kernel's rule (a batch's first tiles go out early once the previous
+    K/V load has landed), and the simpler one (every tile after the K/V load)."""
+    rng = random.Random(1234 + ng)
+    for case in range(400):
+        run(_batches(rng), ng, seed=case, rule=rule)
+
+
+@pytest.mark.parametrize("rule", ["per_tile_o", "early_unchecked"])
+def test_protocol_catches_broken_rules(rule):
+    """Two rules that are wrong: waiting at a batch switch on each group's
+    per-tile O barrier for the parity of its last tile (reads a phase two
+    behind as done); and issuing a batch's first tiles before the previous K/V
+    load has landed (a group that had no tile in that batch then waits for the
+    new load two phases ahead of the K/V barrier)."""
+    rng = random.Random(99)
+    caught = 0
+    for case in range(400):
+        try:
+            run(_batches(rng), 2, seed=case, rule=rule)
+        except (Violation, AssertionError):
+            caught += 1
+    assert caught > 0
