@@ -211,3 +211,75 @@ def test_protocol_catches_broken_rules(rule):
         except (Violation, AssertionError):
             caught += 1
     assert caught > 0
+
+
+# ---------------------------------------------------------------- the cluster exchanges
+def exchange_group(cta, g, ng, nslot, tiles, X1, X2, slots1, slots2, H):
+    """One compute group of one CTA: per tile, push its LayerNorm partial to
+    slot it % nslot of every CTA (a send completes transaction bytes on that
+    CTA's barrier), wait for all H partials, read them; later the same for the
+    RMSNorm partial, which the kernel sends only after the tile's O (itself
+    after the LayerNorm exchange)."""
+    for it in range(g, tiles, ng):
+        s = it % nslot
+        for X, slots in ((X1, slots1), (X2, slots2)):
+            for c in range(H):
+                prev = slots[c][s][cta]
+                assert prev is None or prev[1], f"CTA {c} slot {s}: partial of tile {prev[0]} overwritten unread"
+                X[c][s].arrive(it // nslot)
+                slots[c][s][cta] = [it, False]
+            yield ("wait", X[cta][s], it // nslot)
+            for p in range(H):
+                entry = slots[cta][s][p]
+                assert entry[0] == it, f"CTA {cta} tile {it} read tile {entry[0]}'s partial"
+                entry[1] = True
+
+
+def run_exchanges(H, ng, nslot, tiles, seed):
+    rng = random.Random(seed)
+    X1 = [[Bar(f"x1[{c}][{s}]", count=H) for s in range(nslot)] for c in range(H)]
+    X2 = [[Bar(f"x2[{c}][{s}]", count=H) for s in range(nslot)] for c in range(H)]
+    slots1 = [[[None] * H for _ in range(nslot)] for _ in range(H)]
+    slots2 = [[[None] * H for _ in range(nslot)] for _ in range(H)]
+    procs = {(c, g): exchange_group(c, g, ng, nslot, tiles, X1, X2, slots1, slots2, H)
+             for c in range(H) for g in range(ng)}
+    waiting = {}
+    for _ in range(200000):
+        if not procs:
+            return
+        ready = [n for n in procs if n not in waiting]
+        if not ready:
+            raise Violation("deadlock in the exchanges")
+        n = rng.choice(ready)
+        try:
+            _, bar, c = procs[n].send(None)
+            check_parity(bar, c)
+            if bar.done < c + 1:
+                waiting[n] = (bar, c)
+        except StopIteration:
+            del procs[n]
+        for w, (bar, c) in list(waiting.items()):
+            check_parity(bar, c)
+            if bar.done >= c + 1:
+                del waiting[w]
+    raise Violation("did not finish")
+
+
+@pytest.mark.parametrize("H,ng", [(2, 2), (4, 2), (3, 1), (8, 1)])
+def test_exchange_slots_one_per_group(H, ng):
+    """One exchange slot per group (tile it uses slot it mod NG) is never
+    overwritten before it is read, and every send lands in its phase."""
+    for seed in range(150):
+        run_exchanges(H, ng, ng, tiles=9, seed=seed)
+
+
+def test_exchange_model_catches_shared_slot():
+    """Two groups sharing one slot (tiles of both groups on slot 0) overwrite
+    partials before they are read or send into the wrong phase."""
+    caught = 0
+    for seed in range(150):
+        try:
+            run_exchanges(4, 2, 1, tiles=9, seed=seed)
+        except (Violation, AssertionError):
+            caught += 1
+    assert caught > 0
