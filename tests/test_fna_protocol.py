@@ -283,3 +283,76 @@ def test_exchange_model_catches_shared_slot():
         except (Violation, AssertionError):
             caught += 1
     assert caught > 0
+
+
+# ---------------------------------------------------------------- the batch ring
+def ring_cta(rank, H, nb, entries, bfull, bempty, ring, seen, check_empty=True):
+    """One CTA's producer: rank 0 publishes entry k into every CTA's ring slot
+    k % nb (after all H CTAs emptied entry k - nb); every CTA waits for each
+    entry in turn, reads it, re-arms its slot and tells rank 0 the slot is free."""
+    k_pub = 0
+    for k in range(entries):
+        if rank == 0:
+            while k_pub <= min(k + 1, entries - 1):  # publish up to one entry ahead
+                s = k_pub % nb
+                if k_pub >= nb and check_empty:
+                    yield ("wait", bempty[s], k_pub // nb - 1)
+                for c in range(H):
+                    prev = ring[c][s]
+                    assert prev is None or prev[1], f"ring of CTA {c} slot {s}: entry {prev[0]} overwritten unread"
+                    ring[c][s] = [k_pub, False]
+                    bfull[c][s].arrive(k_pub // nb)
+                k_pub += 1
+        s = k % nb
+        yield ("wait", bfull[rank][s], k // nb)
+        assert ring[rank][s][0] == k, f"CTA {rank} read entry {ring[rank][s][0]} for {k}"
+        ring[rank][s][1] = True
+        seen[rank].append(k)
+        bempty[s].arrive(k // nb)
+
+
+def run_ring(H, nb, entries, seed, check_empty=True):
+    rng = random.Random(seed)
+    bfull = [[Bar(f"bfull[{c}][{s}]") for s in range(nb)] for c in range(H)]
+    bempty = [Bar(f"bempty[{s}]", count=H) for s in range(nb)]
+    ring = [[None] * nb for _ in range(H)]
+    seen = [[] for _ in range(H)]
+    procs = {c: ring_cta(c, H, nb, entries, bfull, bempty, ring, seen, check_empty) for c in range(H)}
+    waiting = {}
+    for _ in range(200000):
+        if not procs:
+            assert all(s == list(range(entries)) for s in seen)
+            return
+        ready = [n for n in procs if n not in waiting]
+        if not ready:
+            raise Violation("deadlock in the batch ring")
+        n = rng.choice(ready)
+        try:
+            _, bar, c = procs[n].send(None)
+            check_parity(bar, c)
+            if bar.done < c + 1:
+                waiting[n] = (bar, c)
+        except StopIteration:
+            del procs[n]
+        for w, (bar, c) in list(waiting.items()):
+            check_parity(bar, c)
+            if bar.done >= c + 1:
+                del waiting[w]
+    raise Violation("did not finish")
+
+
+@pytest.mark.parametrize("H", [1, 2, 4, 8])
+def test_batch_ring(H):
+    """Every CTA sees every entry, in order; no entry is overwritten unread."""
+    for seed in range(150):
+        run_ring(H, 4, entries=23, seed=seed)
+
+
+def test_batch_ring_model_catches_missing_empty_wait():
+    caught = 0
+    for seed in range(150):
+        try:
+            run_ring(4, 2, entries=23, seed=seed, check_empty=False)
+        except (Violation, AssertionError):
+            caught += 1
+    assert caught > 0
