@@ -376,9 +376,26 @@ def _golden_cases():
         return json.load(fh)["cases"]
 
 
+def _pin_closed_form_fna(o, case, env):
+    """FlashNormAttention forward on a hand-derived case (inputs exact in bf16)."""
+    arrs = {}
+    for k in ("Q", "K", "V"):
+        a = np.array(case[k], dtype=np.float64)
+        arrs[k] = bf16_round(a)
+        assert np.array_equal(bf16_to_f64(arrs[k]), a), f"{case['name']}: fixture {k} must be exact in bf16"
+    want = np.array([eval(e, env) for e in case["Y"]]).reshape(np.array(case["Q"]).shape)  # noqa: S307
+    got = o.flashnorm_attn_fwd(arrs["Q"], arrs["K"], arrs["V"], int(case["act"]), float(case["eps1"]),
+                               float(case["eps2"]))
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-14), \
+        f"closed form {case['name']}: got {got.ravel().tolist()} want {want.ravel().tolist()}"
+
+
 def pin_closed_forms(o):
     env = {"sqrt": math.sqrt}
     for case in _golden_cases():
+        if case["op"] == "fna":
+            _pin_closed_form_fna(o, case, env)
+            continue
         X = bf16_round(np.array(case["X"], dtype=np.float64))
         assert np.array_equal(bf16_to_f64(X), np.array(case["X"], dtype=np.float64)), \
             f"{case['name']}: fixture X must be exact in bf16"
