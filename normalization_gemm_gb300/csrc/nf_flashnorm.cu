@@ -39,7 +39,8 @@
 //              and MMAs with the other tile's CUDA-core work.
 //   warp 8NG   TMA producer: the batch sequence, each batch's K and V, the q
 //              tiles into NQ = 4 buffers (tile it into buffer it mod 4, with a
-//              record of its batch, rows and K/V load), each refilled once its
+//              record of its batch, rows, K/V load and whether it is its
+//              group's last tile of the batch), each refilled once its
 //              tile's output stores have read it, so a group's next tile lands
 //              while it computes the current one.
 //   warp 8NG+1+g  MMA issuer of group g: S = ln_q K^T (two 64-key halves) and
