@@ -442,17 +442,6 @@ int nfo_prenorm_rms_bwd_db(const uint16_t* A, const double* rstd, const uint16_t
     return 0;
 }
 
-/* x rounded to the nearest bfloat16 (ties to even), from the definition:
- * 8 significant bits; below 2^-126 the spacing stays 2^-133. */
-static double round_bf16(double x) {
-    if (x == 0.0 || isnan(x) || isinf(x)) return x;
-    int e;
-    (void)frexp(x, &e);                 /* |x| in [2^(e-1), 2^e) */
-    if (e < -125) e = -125;             /* subnormal range: fixed spacing */
-    const double q = ldexp(1.0, e - 8); /* spacing of the 8 significant bits */
-    return rint(x / q) * q;             /* rint: nearest, ties to even */
-}
-
 static double activation(double x, int act) {
     if (act == NFO_ACT_GELU_TANH)
         return 0.5 * x * (1.0 + tanh(sqrt(2.0 / 3.14159265358979323846) * (x + 0.044715 * x * x * x)));
@@ -492,14 +481,14 @@ int nfo_flashnorm_attn_fwd(const uint16_t* Q, const uint16_t* K, const uint16_t*
             layernorm_row(q, HD, NULL, NULL, eps1, ln, NULL, NULL);      /* ln_q over all heads */
             for (int64_t h = 0; h < H; ++h) {
                 const double* lh = ln + h * D;
-                for (int64_t j = 0; j < Lkv; ++j) {                      /* s = act(bf16(ln_q_h) . k_j) */
+                for (int64_t j = 0; j < Lkv; ++j) {                      /* p_j = act(ln_q_h . k_j) */
                     const uint16_t* kj = K + ((b * Lkv + j) * H + h) * D;
                     double acc = 0.0;
-                    for (int64_t d = 0; d < D; ++d) acc += round_bf16(lh[d]) * bf16_to_double(kj[d]);
-                    s[j] = round_bf16(activation(acc, act));
+                    for (int64_t d = 0; d < D; ++d) acc += lh[d] * bf16_to_double(kj[d]);
+                    s[j] = activation(acc, act);
                 }
                 for (int64_t d = 0; d < D; ++d) o[h * D + d] = lh[d];    /* residual 1 */
-                for (int64_t j = 0; j < Lkv; ++j) {                      /* + bf16(s) . V */
+                for (int64_t j = 0; j < Lkv; ++j) {                      /* + p . V */
                     const uint16_t* vj = V + ((b * Lkv + j) * H + h) * D;
                     for (int64_t d = 0; d < D; ++d) o[h * D + d] += s[j] * bf16_to_double(vj[d]);
                 }

@@ -121,13 +121,13 @@ int nfo_prenorm_rms_bwd_db(const uint16_t* A, const double* rstd, const uint16_t
 /* FlashNormAttention forward (blog §4, the fused short-K/V GDPA pseudocode):
  * for each batch b and query token t < q_len[b] (q = Q[b, t, :, :], H*D values)
  *   ln_q = LayerNorm(q) over all H*D values (biased variance, eps1, no affine)
- *   for each head h:  s   = act(bf16(ln_q[h]) . K[b, :, h, :]^T)       (Lkv values)
- *                     o_h = bf16(s) . V[b, :, h, :] + ln_q[h]            (residual 1)
+ *   for each head h:  p   = act(ln_q[h] . K[b, :, h, :]^T)             (Lkv values)
+ *                     o_h = p . V[b, :, h, :] + ln_q[h]                  (residual 1)
  *   out = RMSNorm(o) over all H*D values (eps2, no affine) + q          (residual 2)
- * bf16(.) rounds to bfloat16 (nearest, ties to even): the two matmuls take
- * their left operand in bf16, as tensor cores do; the residual uses ln_q as
- * computed.  act: NFO_ACT_IDENTITY, NFO_ACT_GELU_TANH
- * (x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))) or NFO_ACT_SILU (x / (1 + e^-x)).
+ * Every intermediate stays in fp64, as the pseudocode keeps it: nothing is
+ * rounded between the input's bf16 values and the fp64 result.  act:
+ * NFO_ACT_IDENTITY, NFO_ACT_GELU_TANH (x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715
+ * x^3)))) or NFO_ACT_SILU (x / (1 + e^-x)).
  * Q: [B, Lq, H, D], K and V: [B, Lkv, H, D], bf16; q_len: B entries in
  * [0, Lq] (NULL: Lq each).  Out: [B, Lq, H, D] fp64; rows t >= q_len[b] are
  * not written. */

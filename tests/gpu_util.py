@@ -30,13 +30,18 @@ def to_f64(t):
     return nf_inputs.bf16_to_f64(t.detach().view(torch.int16).cpu().numpy().view(np.uint16))
 
 
-def assert_close(got, want, what, atol=ATOL, rtol=RTOL):
+def assert_close(got, want, what, atol=ATOL, rtol=RTOL, extra=None):
+    """|got - want| <= atol + rtol |want| (+ extra, an elementwise term that a
+    test derives for operands the kernel rounds and the definition does not)."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, f"{what}: shape {got.shape} vs {want.shape}"
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - want)
-    bad = err > atol + rtol * np.abs(want)
+    bound = atol + rtol * np.abs(want)
+    if extra is not None:
+        bound = bound + np.asarray(extra, dtype=np.float64)
+    bad = err > bound
     if bad.any():
         idx = tuple(np.argwhere(bad)[0])
         raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} out of bound; first at {idx}: "

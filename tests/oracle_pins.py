@@ -383,6 +383,9 @@ def _pin_closed_form_fna(o, case, env):
         a = np.array(case[k], dtype=np.float64)
         arrs[k] = bf16_round(a)
         assert np.array_equal(bf16_to_f64(arrs[k]), a), f"{case['name']}: fixture {k} must be exact in bf16"
+    env = dict(env)
+    for name, expr in case.get("let", []):
+        env[name] = eval(expr, env)  # noqa: S307
     want = np.array([eval(e, env) for e in case["Y"]]).reshape(np.array(case["Q"]).shape)  # noqa: S307
     got = o.flashnorm_attn_fwd(arrs["Q"], arrs["K"], arrs["V"], int(case["act"]), float(case["eps1"]),
                                float(case["eps2"]))
@@ -391,7 +394,7 @@ def _pin_closed_form_fna(o, case, env):
 
 
 def pin_closed_forms(o):
-    env = {"sqrt": math.sqrt}
+    env = {"sqrt": math.sqrt, "exp": math.exp, "tanh": math.tanh, "pi": math.pi}
     for case in _golden_cases():
         if case["op"] == "fna":
             _pin_closed_form_fna(o, case, env)
@@ -727,9 +730,8 @@ def _fna_case(B, Lq, Lkv, H, D, seed, scale_kv=0.15):
 
 
 def _fna_torch(Q, K, V, act, eps1, eps2):
-    """The blog §4 pseudocode as torch float64 ops, the two matmuls' left
-    operands rounded to bf16 (bf16_round of the input generator, not the
-    oracle's rounding)."""
+    """The blog §4 pseudocode as torch float64 ops, every intermediate kept in
+    float64 (the pseudocode rounds nothing)."""
     import torch
     import torch.nn.functional as F
     B, Lq, H, D = Q.shape
@@ -737,10 +739,8 @@ def _fna_torch(Q, K, V, act, eps1, eps2):
     k = torch.from_numpy(bf16_to_f64(K))
     v = torch.from_numpy(bf16_to_f64(V))
     ln = F.layer_norm(q, (H * D,), eps=eps1).reshape(B, Lq, H, D)
-    lnr = torch.from_numpy(bf16_to_f64(bf16_round(ln.numpy())))
-    s = torch.einsum("bthd,bjhd->bhtj", lnr, k)
-    a = {0: s, 1: F.gelu(s, approximate="tanh"), 2: F.silu(s)}[act]
-    p = torch.from_numpy(bf16_to_f64(bf16_round(a.numpy())))
+    s = torch.einsum("bthd,bjhd->bhtj", ln, k)
+    p = {0: s, 1: F.gelu(s, approximate="tanh"), 2: F.silu(s)}[act]
     o = torch.einsum("bhtj,bjhd->bthd", p, v) + ln
     out = F.rms_norm(o.reshape(B, Lq, H * D), (H * D,), eps=eps2) + q
     return out.reshape(B, Lq, H, D).numpy()
@@ -761,7 +761,6 @@ def pin_fna_bruteforce(o):
     B, Lq, Lkv, H, D = 1, 2, 3, 2, 4
     Q, K, V = _fna_case(B, Lq, Lkv, H, D, seed=3, scale_kv=0.8)
     q, k, v = bf16_to_f64(Q), bf16_to_f64(K), bf16_to_f64(V)
-    rb = lambda x: float(bf16_to_f64(bf16_round(np.array([x])))[0])  # noqa: E731
     for act in (0, 1, 2):
         got = o.flashnorm_attn_fwd(Q, K, V, act, 1e-3, 1e-2)
         for t in range(Lq):
@@ -774,12 +773,12 @@ def pin_fna_bruteforce(o):
             for h in range(H):
                 ps = []
                 for j in range(Lkv):
-                    sj = sum(rb(ln[h * D + d]) * k[0, j, h, d] for d in range(D))
+                    sj = sum(ln[h * D + d] * k[0, j, h, d] for d in range(D))
                     if act == 1:
                         sj = 0.5 * sj * (1 + math.tanh(math.sqrt(2 / math.pi) * (sj + 0.044715 * sj ** 3)))
                     elif act == 2:
                         sj = sj / (1 + math.exp(-sj))
-                    ps.append(rb(sj))
+                    ps.append(sj)
                 for d in range(D):
                     out_o.append(ln[h * D + d] + sum(ps[j] * v[0, j, h, d] for j in range(Lkv)))
             r = 1 / math.sqrt(sum(z * z for z in out_o) / n + 1e-2)

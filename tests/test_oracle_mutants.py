@@ -83,8 +83,14 @@ MUTANTS = [
      "for (int64_t h2 = 0; h2 < H; ++h2) rmsnorm_row(o + h2 * D, D, NULL, eps2, out + h2 * D, NULL);"),
     ("fna_wrong_k_head", "const uint16_t* kj = K + ((b * Lkv + j) * H + h) * D;",
      "const uint16_t* kj = K + ((b * Lkv + j) * H + (h + 1) % H) * D;"),
-    ("fna_p_unrounded", "s[j] = round_bf16(activation(acc, act));", "s[j] = activation(acc, act);"),
-    ("fna_lnq_unrounded", "acc += round_bf16(lh[d]) * bf16_to_double(kj[d]);", "acc += lh[d] * bf16_to_double(kj[d]);"),
+    # a kernel's bf16 tensor-core operands carried into the oracle: p or ln_q
+    # rounded to bf16 (nearest even; normal range) before its matmul
+    ("fna_p_rounded_bf16", "s[j] = activation(acc, act);",
+     "{ const double a_ = activation(acc, act); int e_; (void)frexp(a_, &e_);"
+     " s[j] = a_ == 0.0 ? 0.0 : ldexp(rint(ldexp(a_, 8 - e_)), e_ - 8); }"),
+    ("fna_lnq_rounded_bf16", "acc += lh[d] * bf16_to_double(kj[d]);",
+     "{ int e_; (void)frexp(lh[d], &e_);"
+     " acc += (lh[d] == 0.0 ? 0.0 : ldexp(rint(ldexp(lh[d], 8 - e_)), e_ - 8)) * bf16_to_double(kj[d]); }"),
     ("fna_gelu_coefficient", "(x + 0.044715 * x * x * x)", "(x + 0.04715 * x * x * x)"),
     ("fna_silu_sign", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
     ("fna_v_transposed", "const uint16_t* vj = V + ((b * Lkv + j) * H + h) * D;",
