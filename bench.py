@@ -2,34 +2,42 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {nf,reference}]
 
-Workload: the ads-shaped post-LayerNorm GEMM, Y = LayerNorm(X @ W) over N with
-X 65536 x 128, W 128 x 128 (bf16, fp32 accumulation, eps 1e-5, no affine).
-One step = one call of the fused kernel (nf_gemm_postnorm_ln) on one batch.
+Workload of the headline line: the LLM-shaped configuration, X 8192 x 4096 and
+W 4096 x 4096 (bf16, fp32 accumulation, eps 1e-6, no affine; X ~ N(0, 1),
+W ~ N(0, 1/4096)), on which the two fused operations run: the Lazy Pre-Norm
+GEMM Y1 = RMSNorm(X) @ W and the Multi-CTA post-norm GEMM Y2 = LayerNorm(X @ W)
+over the 4096-column row.  One step = both calls (nf_gemm_prenorm_rms, then
+nf_gemm_postnorm_ln) on one batch, i.e. one pass of the whole hot path:
+2 * 2MNK flops.
 
 Prints ONE JSON line (rank 0):
-  value        fused TFLOP/s (2*M*N*K per step), inputs resident in HBM,
-               timed with CUDA events over exactly K steps.  Successive steps
-               rotate over buffer sets whose footprint exceeds 3x L2, so no
-               step reads its inputs from L2.  The K launches run from CUDA
-               graphs (one graph launch per 1000 steps).
-  roofline     the fused kernel against the HBM roofline (algorithmic bytes
-               X + W + Y per launch over its mean duration), peak from
-               MEASURED_PEAKS.json.
-  norm_hidden_pct  100 * (T_plain + T_norm - T_fused) / T_norm, against this
-               library's own unfused pair (nf_gemm_plain + nf_norm_rows).
+  value        TFLOP/s of the whole job (all ranks' steps), inputs resident in
+               HBM, timed with CUDA events on the launching stream over exactly
+               K steps launched one by one, with an event before each kernel
+               (so each kernel's own mean duration comes from the same timed
+               region).  Successive steps rotate over buffer sets whose
+               footprint exceeds 3x L2.
+  roofline     the dominant kernel of the step (the one with the larger mean
+               duration) against the bf16 tensor peak of MEASURED_PEAKS.json
+               (2MNK per launch over its mean duration); traffic (DRAM read +
+               write bytes per launch) from the committed ncu summary of that
+               kernel when its source hash matches, else null.
+  norm_hidden_pct  100 * (sum of T_plain + T_norm - sum of T_fused) / sum of
+               T_norm over the step's two operations, against this library's
+               own unfused pairs (nf_gemm_plain + nf_norm_rows), every kernel
+               timed the same way (CUDA graphs of back-to-back launches).
   e2e          the same metric through the Python API with host buffers: each
-               step copies X and W from pinned host memory, runs the fused call
-               and reads Y back.
-  cpu_baseline the fp64 oracle on the host cores (a bounded sample).
-  configs      per-workload figures for the other four workloads (not the
-               headline), for the normalization backward fused into the
-               epilogue of the GEMM producing its incoming gradient (post-norm
-               shapes; unfused pair: plain GEMM + row backward kernel), and for
-               the Lazy Pre-Norm backward (pre-norm shapes; unfused: rmsnorm
-               materialized, transposed plain GEMMs, row backward kernel).
+               step copies X and W from pinned host memory, runs both calls and
+               reads both outputs back (pipelined over copy and compute streams).
+  cpu_baseline the fp64 oracle on the host cores (a bounded sample of rows).
+  configs      compact per-workload figures for every other configuration, the
+               backward and residual variants and the FlashNormAttention
+               forward: [fused us, plain us, norm us, fraction of roofline,
+               % of the norm hidden] (context, not the headline).
 --impl reference times the fp64 oracle itself as the reference arm.
-Under torchrun (N > 1) every rank runs its own independent batch of the same
-size (rows shard across GPUs, no collective on the data path; weak scaling).
+Under torchrun (N > 1) the global problem has N * 8192 rows of one seeded X;
+each rank takes its contiguous shard of rows (shard_rows), W is replicated,
+and no collective touches the data path (weak scaling).
 """
 from __future__ import annotations
 
@@ -50,7 +58,7 @@ import numpy as np  # noqa: E402
 
 import nf_inputs  # noqa: E402
 
-WORKLOAD = "post_ln_65536x128x128"
+WORKLOAD = "llm_8192x4096x4096"
 GRAPH_CHUNK = 1000
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -66,11 +74,7 @@ def norm_bytes(rows, cols, affine=0):
     return 4 * rows * cols + 2 * cols * affine
 
 
-def shard_rows(total_rows: int, world: int, rank: int):
-    """Contiguous row range [lo, hi) of `rank` when rows split over `world` GPUs."""
-    base, extra = divmod(total_rows, world)
-    lo = rank * base + min(rank, extra)
-    return lo, lo + base + (1 if rank < extra else 0)
+shard_rows = nf_inputs.shard_rows
 
 
 def max_over_ranks(x: float, dist) -> float:
@@ -102,20 +106,26 @@ def kernel_source_hash() -> str:
     return _build.source_hash(_build.GEMM_SOURCES)
 
 
-def profiled_traffic(workload: str):
-    """Per-launch DRAM bytes of the fused kernel from the committed ncu summary,
-    or None when the summary is missing or the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", f"nf_gemm_postnorm_ln_{workload}.md")
+KERNEL_OF_OP = {"pre_rms": "nf_gemm_prenorm_rms", "post_ln": "nf_gemm_postnorm_ln",
+                "post_rms": "nf_gemm_postnorm_rms", "plain": "nf_gemm_plain"}
+
+
+def profiled_traffic(workload: str, op: str):
+    """Per-launch DRAM bytes (read + write) of the op's fused kernel from the
+    committed ncu summary, or None when the summary is missing, gives no
+    write bytes, or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_OF_OP[op]}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     vals = {}
     for line in text.splitlines():
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_hash")):
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_hash",
+                                                    "traffic_includes_writes")):
             k, v = line.strip().split(":", 1)
             vals[k.strip()] = (v.split() or [""])[0].strip("`")
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    if vals.get("kernel_source_hash") != kernel_source_hash() or vals.get("traffic_includes_writes") != "yes":
         return None
     try:
         return float(vals["traffic_bytes_per_launch"])
@@ -521,24 +531,79 @@ def roofline_time(w, op, hbm_gbs, tflops):
     return max(w.flops / (tflops * 1e12), nbytes / (hbm_gbs * 1e9)), nbytes
 
 
-def e2e_measure(nf, w, dev, stream, steps):
-    """Public API with host buffers: every step copies its X and W from pinned
-    host memory to the device, runs the fused call and copies Y back.  Steps are
-    pipelined over three streams and two buffer sets (the copy of step i+1's
-    inputs and of step i-1's output overlap step i's kernel; host-to-device and
-    device-to-host copies use separate copy engines); every copy of every step is
-    inside the timed region."""
+def call_op(nf, op, X, W, Y, G, B, eps, stream):
+    """One fused call of the step (the public Python API)."""
+    run_op(nf, op, X, W, Y, G, B, eps, stream)
+
+
+def measure_step(nf, w, ops, X0, W0, G, B, dev, stream, steps, warmup, dist=None, sampler=None):
+    """The timed region of the headline: `steps` steps, each one call per op
+    in `ops` on one buffer set (rotating sets > 3x L2), launched one by one on
+    `stream` with a CUDA event before every kernel and one after the last.
+    Returns (seconds of the region (max over ranks), mean seconds per kernel
+    of each op, buffer sets, set bytes)."""
     import torch
-    inp = nf_inputs.workload_inputs(w)
+    Ys = [torch.empty((X0.shape[0], w.N), dtype=torch.bfloat16, device=dev) for _ in ops]
+    set_bytes = X0.numel() * 2 + sum(y.numel() * 2 for y in Ys)
+    sets, nsets = make_sets([X0, *Ys], set_bytes, dev)
+
+    def step(i):
+        x, *ys = sets[i % nsets]
+        for op, y in zip(ops, ys):
+            call_op(nf, op, x, W0, y, G, B, w.eps, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps * len(ops) + 1)]
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    with torch.cuda.stream(stream):
+        k = 0
+        for i in range(steps):
+            x, *ys = sets[i % nsets]
+            for op, y in zip(ops, ys):
+                evs[k].record(stream)
+                call_op(nf, op, x, W0, y, G, B, w.eps, stream)
+                k += 1
+        evs[k].record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.stop()
+    if dist is not None and dist.is_initialized():
+        dist.barrier()
+    total = evs[0].elapsed_time(evs[-1]) / 1e3
+    per_op = {}
+    for j, op in enumerate(ops):
+        d = [evs[i * len(ops) + j].elapsed_time(evs[i * len(ops) + j + 1]) / 1e3 for i in range(steps)]
+        per_op[op] = sum(d) / len(d)
+    del sets, Ys
+    torch.cuda.empty_cache()
+    return max_over_ranks(total, dist), per_op, nsets, set_bytes, step
+
+
+def e2e_measure(nf, w, ops, inp, dev, stream, steps):
+    """Public API with host buffers: every step copies its X and W from pinned
+    host memory to the device, runs the step's fused calls and copies their
+    outputs back.  Steps are pipelined over three streams and two buffer sets
+    (the copy of step i+1's inputs and of step i-1's outputs overlap step i's
+    kernels; host-to-device and device-to-host copies use separate copy
+    engines); every copy of every step is inside the timed region."""
+    import torch
     Xh = torch.from_numpy(inp["X"].view(np.int16)).view(torch.bfloat16).pin_memory()
     Wh = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    Yh = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    M = Xh.shape[0]
+    Yh = [[torch.empty((M, w.N), dtype=torch.bfloat16).pin_memory() for _ in ops] for _ in range(2)]
     Xd = [torch.empty_like(Xh, device=dev) for _ in range(2)]
     Wd = [torch.empty_like(Wh, device=dev) for _ in range(2)]
-    Yd = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    Yd = [[torch.empty((M, w.N), dtype=torch.bfloat16, device=dev) for _ in ops] for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    read_done = [ev(), ev()]   # the kernel of the last step on buffer b has read Xd[b], Wd[b]
+    read_done = [ev(), ev()]   # the kernels of the last step on buffer b have read Xd[b], Wd[b]
     out_done = [ev(), ev()]    # Yd[b] has been copied out
     for b in range(2):
         read_done[b].record(stream)
@@ -555,12 +620,14 @@ def e2e_measure(nf, w, dev, stream, steps):
         with torch.cuda.stream(stream):
             stream.wait_event(in_ready)
             stream.wait_event(out_done[b])
-            nf.gemm_postnorm_ln(Xd[b], Wd[b], w.eps, out=Yd[b], stream=stream)
+            for op, y in zip(ops, Yd[b]):
+                call_op(nf, op, Xd[b], Wd[b], y, None, None, w.eps, stream)
             read_done[b].record(stream)
             y_ready.record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(y_ready)
-            Yh[b].copy_(Yd[b], non_blocking=True)
+            for yh, yd in zip(Yh[b], Yd[b]):
+                yh.copy_(yd, non_blocking=True)
             out_done[b].record(s_out)
 
     for i in range(3):
@@ -576,95 +643,181 @@ def e2e_measure(nf, w, dev, stream, steps):
     t1.record(s_out)
     torch.cuda.synchronize()
     sec = t0.elapsed_time(t1) / 1e3
-    return sec, Xh.numel() * 2 + Wh.numel() * 2, Yh[0].numel() * 2
+    return sec, Xh.numel() * 2 + Wh.numel() * 2, sum(y.numel() * 2 for y in Yh[0])
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_sample(w, op, budget_s, rows_cap=None, seed=0):
-    """Time the fp64 oracle on whole-row samples of the workload for about
-    budget_s seconds; returns (flops_done, seconds, rows_per_pass, threads)."""
+def oracle_rows(orc, inp, w, op, rows):
+    if op == "post_ln":
+        orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, inp.get("gamma"), inp.get("beta"), rows=rows)
+    elif op == "post_rms":
+        orc.gemm_postnorm_rms(inp["X"], inp["W"], w.eps, inp.get("gamma"), rows=rows)
+    else:
+        orc.gemm_prenorm_rms(inp["X"], inp["W"], w.eps, rows=rows)
+
+
+def oracle_sample(w, ops, inp, budget_s, rows_cap):
+    """Time the fp64 oracle on whole-row samples of the step (every op on the
+    same rows) for about budget_s seconds; returns (flops_done, seconds,
+    rows_per_pass, threads)."""
     import oracle
     orc = oracle.get()
-    inp = nf_inputs.workload_inputs(w, seed=seed)
-    rows_per_pass = w.M if rows_cap is None else max(1, min(w.M, rows_cap))
+    M = inp["X"].shape[0]
+    rows_per_pass = max(1, min(M, rows_cap))
     rows = np.arange(rows_per_pass, dtype=np.int64)
-
-    def once():
-        if op == "post_ln":
-            orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, inp.get("gamma"), inp.get("beta"), rows=rows)
-        elif op == "post_rms":
-            orc.gemm_postnorm_rms(inp["X"], inp["W"], w.eps, inp.get("gamma"), rows=rows)
-        else:
-            orc.gemm_prenorm_rms(inp["X"], inp["W"], w.eps, rows=rows)
-
     done = 0
     t0 = time.perf_counter()
     while True:
-        once()
+        for op in ops:
+            oracle_rows(orc, inp, w, op, rows)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     sec = time.perf_counter() - t0
-    return done * 2 * rows_per_pass * w.N * w.K, sec, rows_per_pass, orc.max_threads()
+    return done * len(ops) * 2 * rows_per_pass * w.N * w.K, sec, rows_per_pass, orc.max_threads()
 
 
 def reference_arm(args):
-    """--impl reference: the fp64 CPU oracle, timed as the reference arm."""
+    """--impl reference: the fp64 CPU oracle on the headline's step (every op
+    of the workload on the same rows), timed as the reference arm."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import oracle
-    w = nf_inputs.WORKLOADS[WORKLOAD]
+    w = nf_inputs.WORKLOADS[args.workload]
+    ops = tuple(args.op.split(",")) if args.op else w.ops
     orc = oracle.get()
     inp = nf_inputs.workload_inputs(w)
-    # calibrate rows per second, then size each step so the run stays ~60 s
-    cal_rows = np.arange(min(w.M, 2048), dtype=np.int64)
+    # calibrate seconds per row of a step, then size each step so the run
+    # stays near 60 s
+    cal_rows = np.arange(min(w.M, 32), dtype=np.int64)
     t0 = time.perf_counter()
-    orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, rows=cal_rows)
+    for op in ops:
+        oracle_rows(orc, inp, w, op, cal_rows)
     per_row = (time.perf_counter() - t0) / len(cal_rows)
     total = args.steps + args.warmup
     rows_per_step = int(max(1, min(w.M, 60.0 / max(1, total) / max(per_row, 1e-9))))
     rows = np.arange(rows_per_step, dtype=np.int64)
     for _ in range(args.warmup):
-        orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, rows=rows)
+        for op in ops:
+            oracle_rows(orc, inp, w, op, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, rows=rows)
+        for op in ops:
+            oracle_rows(orc, inp, w, op, rows)
     sec = time.perf_counter() - t0
-    flops = args.steps * 2 * rows_per_step * w.N * w.K
+    flops = args.steps * len(ops) * 2 * rows_per_step * w.N * w.K
     value = flops / sec / 1e12
     line = {
         "impl": "reference", "metric": "fused norm-GEMM TFLOP/s", "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
+        "config": {"workload": w.name, "ops": list(ops), "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
                    "rows_per_step": rows_per_step},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.max_threads(), "kind": "oracle",
-                         "sample": f"{rows_per_step} of {w.M} rows per step (whole rows, fp64 oracle)"},
+                         "sample": f"{rows_per_step} of {w.M} rows per step, every op of the step on them "
+                                   f"(whole rows, fp64 oracle)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
+# ---------------------------------------------------------------- configs
+WL_SHORT = {"pre_rms_256x64x64": "C1", "post_ln_65536x128x128": "C2", "pre_rms_rowscale_32768x512x512": "C3",
+            "post_affine_16384x1024x2048": "C4", "llm_8192x4096x4096": "C5"}
+
+
+def _r(x, nd=3):
+    """Round to nd significant digits (compact JSON)."""
+    if x is None or x == 0 or not np.isfinite(x):
+        return x
+    return float(f"{x:.{nd}g}")
+
+
+def _row(t_fused, t_plain, t_norm, frac):
+    hid = None if t_norm is None else 100.0 * (t_plain + t_norm - t_fused) / t_norm
+    return [_r(t_fused * 1e6), _r(t_plain * 1e6) if t_plain is not None else None,
+            _r(t_norm * 1e6) if t_norm is not None else None, _r(frac, 2), _r(hid, 3)]
+
+
+def config_table(nf, dev, stream, hbm_gbs, bf16_tf):
+    """Every configuration's forward ops, the DSMEM cluster layouts of the
+    wide post-norm rows, the backward and residual variants, and the
+    FlashNormAttention forward: name -> [fused us, plain us, norm us,
+    roofline fraction, % norm hidden]."""
+    import torch
+    rows = {}
+
+    def roof(flops, nbytes, t):
+        return max(flops / (bf16_tf * 1e12), nbytes / (hbm_gbs * 1e9)) / t
+
+    for name in nf_inputs.WORKLOAD_ORDER:
+        cw = nf_inputs.WORKLOADS[name]
+        c = WL_SHORT[name]
+        big = cw.flops > 5e10
+        for cop in cw.ops:
+            r = measure_workload(nf, cw, cop, dev, stream, 200 if big else 1000, 10)
+            tr, _ = roofline_time(cw, cop, hbm_gbs, bf16_tf)
+            rows[f"{c} {cop}"] = _row(r["t_fused"], r["t_plain"], r["t_norm"], tr / r["t_fused"])
+            if cop == "post_ln" and cw.N > 512:
+                # the blog's §3 layout: a thread-block cluster of 256-column
+                # CTAs spans the row, partials through DSMEM
+                nf.set_postnorm_exchange(nf.XCH_CLUSTER)
+                nf.set_postnorm_tile_n(256)
+                try:
+                    rc = measure_workload(nf, cw, cop, dev, stream, 200 if big else 1000, 10, unfused=False)
+                finally:
+                    nf.set_postnorm_exchange(0)
+                    nf.set_postnorm_tile_n(0)
+                rows[f"{c} {cop} cluster{cw.N // 256}x256"] = _row(rc["t_fused"], r["t_plain"], r["t_norm"],
+                                                                    tr / rc["t_fused"])
+            del r
+            torch.cuda.empty_cache()
+        if "pre_rms" in cw.ops:
+            r = measure_prenorm_backward(nf, cw, dev, stream, 100 if big else 500, 10)
+            nb = 6 * cw.M * cw.K + 4 * cw.M * cw.N + 4 * cw.K * cw.N + 8 * cw.M
+            rows[f"{c} pre_rms_bwd"] = _row(r["t_fused"], r["t_plain"], r["t_norm"],
+                                            roof(2 * cw.flops, nb, r["t_fused"]))
+            del r
+        for cop in cw.ops:
+            if cop not in ("post_ln", "post_rms"):
+                continue
+            kind = 0 if cop == "post_ln" else 1
+            r = measure_backward(nf, cw, kind, dev, stream, 200 if big else 1000, 10)
+            rows[f"{c} {cop}_bwd"] = _row(r["t_fused"], r["t_plain"], r["t_norm"],
+                                          roof(cw.flops, backward_bytes(cw, kind), r["t_fused"]))
+            r = measure_residual(nf, cw, kind, dev, stream, 200 if big else 1000, 10)
+            rows[f"{c} {cop}_res"] = _row(r["t_fused"], r["t_plain"], r["t_norm"],
+                                          roof(cw.flops, residual_bytes(cw, kind), r["t_fused"]))
+            del r
+        torch.cuda.empty_cache()
+    r = measure_flashnorm(nf, dev, stream, 50, 5)
+    rows["FNA fwd"] = [_r(r["t_fused"] * 1e6), None, None,
+                       _r(roof(r["flops"], r["bytes"], r["t_fused"]), 2), None, _r(r["t_torch"] * 1e6)]
+    del r
+    torch.cuda.empty_cache()
+    return rows
+
+
 # ---------------------------------------------------------------- main
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["nf", "reference"], default="nf")
     ap.add_argument("--workload", default=WORKLOAD, choices=list(nf_inputs.WORKLOAD_ORDER),
-                    help="workload of the headline line (default: the ads-shaped post-LN GEMM)")
-    ap.add_argument("--op", default=None, help="pre_rms | post_ln | post_rms (default: the workload's first)")
-    ap.add_argument("--eager", action="store_true", help="launch every step from Python (no CUDA graphs)")
+                    help="workload of the headline line (default: the LLM-shaped configuration)")
+    ap.add_argument("--op", default=None,
+                    help="comma-separated ops of a step: pre_rms, post_ln, post_rms (default: the workload's)")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end figure")
-    ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused pair")
+    ap.add_argument("--no-unfused", action="store_true", help="skip timing the unfused pairs")
     ap.add_argument("--no-soak", action="store_true", help="never add a clock-sampling soak")
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--backward", choices=["post_ln", "post_rms", "pre_rms"], default=None,
                     help="time only this op's backward on the workload's shapes and print its figures "
                          "(a profiling aid; not the benchmark line)")
@@ -676,6 +829,11 @@ def main(argv=None):
     ap.add_argument("--residual", choices=["post_ln", "post_rms"], default=None,
                     help="time only this op with a residual add on the workload's shapes and print its "
                          "figures (a profiling aid; not the benchmark line)")
+    ap.add_argument("--single", default=None, choices=["pre_rms", "post_ln", "post_rms", "plain", "norm"],
+                    help="time only this kernel on the workload's shapes, back to back from CUDA graphs, and "
+                         "print its figures (a profiling aid; not the benchmark line)")
+    ap.add_argument("--exchange", default=None, choices=["cluster", "global"],
+                    help="with --single: force the post-norm exchange (cluster: 256-column CTAs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -700,63 +858,93 @@ def main(argv=None):
     nf.clear_device_status()
     stream = torch.cuda.Stream(device=dev)
     hbm_gbs, bf16_tf, bf16_sus, peak_src = measured_peaks()
+    w = nf_inputs.WORKLOADS[args.workload]
     if args.backward:
-        w = nf_inputs.WORKLOADS[args.workload]
         if args.backward == "pre_rms":
-            r = measure_prenorm_backward(nf, w, dev, stream, args.steps, args.warmup, eager=args.eager,
-                                         unfused=not args.no_unfused)
+            r = measure_prenorm_backward(nf, w, dev, stream, args.steps, args.warmup, unfused=not args.no_unfused)
         else:
             r = measure_backward(nf, w, 0 if args.backward == "post_ln" else 1, dev, stream, args.steps,
-                                 args.warmup, eager=args.eager, unfused=not args.no_unfused)
+                                 args.warmup, unfused=not args.no_unfused)
         print(json.dumps({"backward": args.backward, "workload": w.name,
                           **{k: v * 1e6 for k, v in r.items() if k.startswith("t_")}}), flush=True)
         return 0
     if args.flashnorm:
-        r = measure_flashnorm(nf, dev, stream, args.steps, args.warmup, eager=args.eager,
-                              unfused=not args.no_unfused, batch=args.fna_batch)
+        r = measure_flashnorm(nf, dev, stream, args.steps, args.warmup, unfused=not args.no_unfused,
+                              batch=args.fna_batch)
         print(json.dumps({"flashnorm": nf_inputs.FNA_WORKLOAD["name"],
                           **{k: (v * 1e6 if k.startswith("t_") else v) for k, v in r.items()}}), flush=True)
         return 0
     if args.residual:
-        w = nf_inputs.WORKLOADS[args.workload]
         r = measure_residual(nf, w, 0 if args.residual == "post_ln" else 1, dev, stream, args.steps,
-                             args.warmup, eager=args.eager, unfused=not args.no_unfused)
+                             args.warmup, unfused=not args.no_unfused)
         print(json.dumps({"residual": args.residual, "workload": w.name,
                           **{k: v * 1e6 for k, v in r.items() if k.startswith("t_")}}), flush=True)
         return 0
+    if args.single:
+        if args.exchange:
+            nf.set_postnorm_exchange(nf.XCH_CLUSTER if args.exchange == "cluster" else nf.XCH_GLOBAL)
+            if args.exchange == "cluster":
+                nf.set_postnorm_tile_n(256)
+        op = args.single
+        kop = op if op in ("pre_rms", "post_ln", "post_rms") else (w.ops[-1] if op == "norm" else "plain")
+        r = measure_workload(nf, w, kop, dev, stream, args.steps, args.warmup, unfused=op in ("plain", "norm"))
+        key = {"plain": "t_plain", "norm": "t_norm"}.get(op, "t_fused")
+        print(json.dumps({"single": op, "workload": w.name, "us": r[key] * 1e6}), flush=True)
+        return 0
 
-    w = nf_inputs.WORKLOADS[args.workload]
-    op = args.op or w.ops[0]
-    if op not in w.ops:
-        ap.error(f"--op {op} is not run on {w.name} (ops: {w.ops})")
+    ops = tuple(args.op.split(",")) if args.op else w.ops
+    for op in ops:
+        if op not in ("pre_rms", "post_ln", "post_rms"):
+            ap.error(f"--op: unknown op {op}")
+    # rows shard_rows(world * M, world, rank) of one seeded global problem
+    inp = nf_inputs.workload_shard(w, world, rank)
+    lo, hi = inp["rows"]
+    rows_here = hi - lo
+    X0, W0 = _to_dev(inp["X"], dev), _to_dev(inp["W"], dev)
+    G = _to_dev(inp["gamma"], dev) if w.gamma else None
+    B = _to_dev(inp["beta"], dev) if w.beta else None
+    flops_step = len(ops) * 2 * rows_here * w.N * w.K
     sampler = ClockSampler(local_rank)
-    # each rank its own independent batch (seed = rank): weak scaling
-    m = measure_workload(nf, w, op, dev, stream, args.steps, args.warmup, seed=rank, dist=dist,
-                         sampler=sampler, unfused=not args.no_unfused, eager=args.eager)
-    t_step = m["t_fused"]
-    value = world * w.flops / t_step / 1e12
+    sec, per_op, nsets, set_bytes, step_fn = measure_step(nf, w, ops, X0, W0, G, B, dev, stream, args.steps,
+                                                          args.warmup, dist=dist, sampler=sampler)
+    t_step = sec / args.steps
+    value = world * flops_step / t_step / 1e12
     clocks = sampler.summary("timed")
     if clocks["samples"] < 3 and not args.no_soak:
-        # The timed region was shorter than the sampling period: replay the same
-        # fused step for ~1.5 s right after it and sample that instead.
+        # The timed region was shorter than the sampling period: run the same
+        # steps for ~1.5 s right after it and sample that instead.
         soak = ClockSampler(local_rank)
         reps = max(args.steps, int(1.5 / max(t_step, 1e-7)))
-        time_steps(m["fused_fn"], reps, 3, stream, None, sampler=soak)
-        clocks = soak.summary("soak after the timed region (the timed region was shorter than "
-                              "the 50 ms sampling period)")
+        Ys = [torch.empty((rows_here, w.N), dtype=torch.bfloat16, device=dev) for _ in ops]
+        soak.start()
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                for op, y in zip(ops, Ys):
+                    call_op(nf, op, X0, W0, y, G, B, w.eps, stream)
+        torch.cuda.synchronize()
+        soak.stop()
+        del Ys
+        clocks = soak.summary("soak right after the timed region (the timed region was shorter than "
+                              "three 50 ms sampling periods)")
 
-    t_roof, nbytes = roofline_time(w, op, hbm_gbs, bf16_tf)
-    tensor_bound = w.flops / (bf16_tf * 1e12) > nbytes / (hbm_gbs * 1e9)
-    if tensor_bound:
-        achieved = w.flops / t_step / 1e12
+    # the dominant kernel of the step against its roofline
+    dom = max(ops, key=lambda o: per_op[o])
+    kflops = 2 * rows_here * w.N * w.K
+    kbytes = algorithmic_bytes(rows_here, w.N, w.K, gamma=w.gamma and dom != "pre_rms",
+                               beta=w.beta and dom == "post_ln")
+    t_dom = per_op[dom]
+    if kflops / (bf16_tf * 1e12) > kbytes / (hbm_gbs * 1e9):
+        achieved = kflops / t_dom / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
-                "frac": achieved / bf16_tf, "traffic": profiled_traffic(w.name),
-                "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic_flops_per_launch": w.flops}
+                "frac": achieved / bf16_tf, "traffic": profiled_traffic(w.name, dom),
+                "kernel": KERNEL_OF_OP[dom], "peak_source": f"{peak_src} bf16_tflops (burst; of measured)",
+                "algorithmic_flops_per_launch": kflops, "mean_launch_us": t_dom * 1e6}
     else:
-        achieved = nbytes / t_step / 1e9
+        achieved = kbytes / t_dom / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                "frac": achieved / hbm_gbs, "traffic": profiled_traffic(w.name),
-                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": nbytes}
+                "frac": achieved / hbm_gbs, "traffic": profiled_traffic(w.name, dom),
+                "kernel": KERNEL_OF_OP[dom], "peak_source": f"{peak_src} hbm_gbs (of measured)",
+                "algorithmic_bytes_per_launch": kbytes, "mean_launch_us": t_dom * 1e6}
     status, detail = nf.device_status()
 
     line = {
@@ -764,135 +952,57 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "op": op, "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
-                   "gamma": bool(w.gamma and op != "pre_rms"), "beta": bool(w.beta and op == "post_ln"),
-                   "per_gpu_rows": w.M, "parallelism": f"rows x{world}, no collective",
-                   "l2": f"rotating {m['sets']} input/output sets of {m['set_bytes'] / 2**20:.0f} MiB "
-                         f"(> 3x L2 between reuses)",
-                   "launch": "eager" if args.eager else f"CUDA graphs of {min(GRAPH_CHUNK, args.steps)} launches"},
-        "gpu_launches": args.steps,
+        "config": {"workload": w.name, "ops": list(ops), "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
+                   "gamma": bool(w.gamma), "beta": bool(w.beta),
+                   "step": " + ".join(KERNEL_OF_OP[o] for o in ops) + " on one batch",
+                   "per_gpu_rows": rows_here, "parallelism": f"rows x{world} (shard of one seeded problem), "
+                                                            f"no collective",
+                   "l2": f"rotating {nsets} buffer sets of {set_bytes / 2**20:.0f} MiB (> 3x L2 between reuses)",
+                   "launch": "one by one, a CUDA event before each kernel"},
+        "gpu_launches": args.steps * len(ops),
         "roofline": roof,
-        "roofline_frac_of_config_bound": t_roof / t_step,
+        "kernel_us": {KERNEL_OF_OP[o]: per_op[o] * 1e6 for o in ops},
         "clocks": clocks,
         "device_status": int(status),
     }
-    if "t_norm" in m:
-        line["norm_hidden_pct"] = 100.0 * (m["t_plain"] + m["t_norm"] - m["t_fused"]) / m["t_norm"]
-        line["unfused"] = {"t_plain_us": m["t_plain"] * 1e6, "t_norm_us": m["t_norm"] * 1e6,
-                           "t_fused_us": t_step * 1e6}
     if status != 0:
         line["device_status_detail"] = detail
 
     if rank == 0:
-        if not args.no_e2e and op == "post_ln":
+        if not args.no_unfused:
+            tf = tp = tn = 0.0
+            unf = {}
+            for op in ops:
+                m = measure_workload(nf, w, op, dev, stream, 200, 10)
+                tf, tp, tn = tf + m["t_fused"], tp + m["t_plain"], tn + m["t_norm"]
+                unf[op] = {"fused_us": m["t_fused"] * 1e6, "plain_us": m["t_plain"] * 1e6,
+                           "norm_us": m["t_norm"] * 1e6}
+                del m
+                torch.cuda.empty_cache()
+            line["norm_hidden_pct"] = 100.0 * (tp + tn - tf) / tn
+            line["unfused"] = unf
+        if not args.no_e2e:
             e2e_steps = max(1, min(args.e2e_steps, args.steps))
-            sec, hb, db = e2e_measure(nf, w, dev, stream, e2e_steps)
-            line["e2e"] = {"value": world * w.flops * e2e_steps / sec / 1e12, "unit": "TFLOP/s",
+            full = inp if world == 1 else nf_inputs.workload_inputs(w)
+            sec_e, hb, db = e2e_measure(nf, w, ops, full, dev, stream, e2e_steps)
+            line["e2e"] = {"value": world * flops_step * e2e_steps / sec_e / 1e12, "unit": "TFLOP/s",
                            "h2d_bytes_per_step": hb, "d2h_bytes_per_step": db, "steps": e2e_steps}
-        if not args.no_configs:
-            table = []
-            for name in nf_inputs.WORKLOAD_ORDER:
-                cw = nf_inputs.WORKLOADS[name]
-                for cop in cw.ops:
-                    steps = 200 if cw.flops > 5e10 else 1000
-                    r = measure_workload(nf, cw, cop, dev, stream, steps, 10)
-                    tr, nb = roofline_time(cw, cop, hbm_gbs, bf16_tf)
-                    table.append({
-                        "workload": name, "op": cop, "t_fused_us": r["t_fused"] * 1e6,
-                        "tflops": cw.flops / r["t_fused"] / 1e12,
-                        "roofline_frac": tr / r["t_fused"],
-                        "bound": "tensor" if cw.flops / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
-                        "hbm_gbs": nb / r["t_fused"] / 1e9,
-                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
-                        "norm_gbs": norm_bytes(r["norm_rows"], r["norm_cols"]) / r["t_norm"] / 1e9,
-                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
-                    })
-                    del r
-                    torch.cuda.empty_cache()
-                if "pre_rms" in cw.ops:
-                    # Lazy Pre-Norm backward: two GEMMs (4MNK flops); bytes: A read
-                    # twice, dC twice, B, dA, dB, rstd twice
-                    steps = 100 if cw.flops > 5e10 else 500
-                    r = measure_prenorm_backward(nf, cw, dev, stream, steps, 10)
-                    nb = (6 * cw.M * cw.K + 4 * cw.M * cw.N + 4 * cw.K * cw.N + 8 * cw.M)
-                    fl = 2 * cw.flops
-                    tr = max(fl / (bf16_tf * 1e12), nb / (hbm_gbs * 1e9))
-                    table.append({
-                        "workload": name, "op": "pre_rms_bwd", "t_fused_us": r["t_fused"] * 1e6,
-                        "tflops": fl / r["t_fused"] / 1e12, "roofline_frac": tr / r["t_fused"],
-                        "bound": "tensor" if fl / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
-                        "hbm_gbs": nb / r["t_fused"] / 1e9,
-                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
-                        "norm_gbs": (4 * cw.M * cw.K + 6 * cw.M * cw.K) / r["t_norm"] / 1e9,
-                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
-                    })
-                    del r
-                    torch.cuda.empty_cache()
-                # the norm's backward fused into the epilogue of the GEMM that
-                # produces its incoming gradient (same shapes as the forward)
-                for cop in cw.ops:
-                    if cop not in ("post_ln", "post_rms"):
-                        continue
-                    kind = 0 if cop == "post_ln" else 1
-                    steps = 200 if cw.flops > 5e10 else 1000
-                    r = measure_backward(nf, cw, kind, dev, stream, steps, 10)
-                    nb = backward_bytes(cw, kind)
-                    tr = max(cw.flops / (bf16_tf * 1e12), nb / (hbm_gbs * 1e9))
-                    table.append({
-                        "workload": name, "op": cop + "_bwd", "t_fused_us": r["t_fused"] * 1e6,
-                        "tflops": cw.flops / r["t_fused"] / 1e12,
-                        "roofline_frac": tr / r["t_fused"],
-                        "bound": "tensor" if cw.flops / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
-                        "hbm_gbs": nb / r["t_fused"] / 1e9,
-                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
-                        "norm_gbs": 6 * cw.M * cw.N / r["t_norm"] / 1e9,
-                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
-                    })
-                    del r
-                    torch.cuda.empty_cache()
-                # the residual add before the post-norm (H = X W + R, Y = norm(H),
-                # H written back); unfused: plain GEMM + residual-add row norm
-                for cop in cw.ops:
-                    if cop not in ("post_ln", "post_rms"):
-                        continue
-                    kind = 0 if cop == "post_ln" else 1
-                    steps = 200 if cw.flops > 5e10 else 1000
-                    r = measure_residual(nf, cw, kind, dev, stream, steps, 10)
-                    nb = residual_bytes(cw, kind)
-                    tr = max(cw.flops / (bf16_tf * 1e12), nb / (hbm_gbs * 1e9))
-                    table.append({
-                        "workload": name, "op": cop + "_res", "t_fused_us": r["t_fused"] * 1e6,
-                        "tflops": cw.flops / r["t_fused"] / 1e12,
-                        "roofline_frac": tr / r["t_fused"],
-                        "bound": "tensor" if cw.flops / (bf16_tf * 1e12) > nb / (hbm_gbs * 1e9) else "hbm",
-                        "hbm_gbs": nb / r["t_fused"] / 1e9,
-                        "t_plain_us": r["t_plain"] * 1e6, "t_norm_us": r["t_norm"] * 1e6,
-                        "norm_gbs": 8 * cw.M * cw.N / r["t_norm"] / 1e9,
-                        "norm_hidden_pct": 100.0 * (r["t_plain"] + r["t_norm"] - r["t_fused"]) / r["t_norm"],
-                    })
-                    del r
-                    torch.cuda.empty_cache()
-            # FlashNormAttention forward on the blog §4 benchmark shapes
-            r = measure_flashnorm(nf, dev, stream, 50, 5)
-            tr = max(r["flops"] / (bf16_tf * 1e12), r["bytes"] / (hbm_gbs * 1e9))
-            table.append({
-                "workload": nf_inputs.FNA_WORKLOAD["name"], "op": "flashnorm_attn_fwd",
-                "t_fused_us": r["t_fused"] * 1e6, "tflops": r["flops"] / r["t_fused"] / 1e12,
-                "roofline_frac": tr / r["t_fused"],
-                "bound": "tensor" if r["flops"] / (bf16_tf * 1e12) > r["bytes"] / (hbm_gbs * 1e9) else "hbm",
-                "hbm_gbs": r["bytes"] / r["t_fused"] / 1e9, "t_torch_eager_us": r["t_torch"] * 1e6,
-                "valid_rows": r["rows"],
-            })
-            del r
-            torch.cuda.empty_cache()
-            line["configs"] = table
         if not args.no_cpu and world == 1:
-            cap = max(1, int(2e10 // (2 * w.N * w.K)))   # about 20 GFLOP per pass
-            flops, sec, rpp, thr = oracle_sample(w, op, budget_s=10.0, rows_cap=cap)
-            line["cpu_baseline"] = {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": thr,
+            cap = max(1, int(2e10 // (len(ops) * 2 * w.N * w.K)))   # about 20 GFLOP per pass
+            flops, sec_c, rpp, thr = oracle_sample(w, ops, inp, budget_s=10.0, rows_cap=cap)
+            line["cpu_baseline"] = {"value": flops / sec_c / 1e12, "unit": "TFLOP/s", "cores": thr,
                                     "kind": "oracle",
-                                    "sample": f"{rpp} of {w.M} rows of {w.M} x {w.K} x {w.N}, repeated for "
-                                              f"{sec:.1f} s (fp64, OpenMP over rows)"}
+                                    "sample": f"rows 0..{rpp - 1} of {w.M} x {w.K} x {w.N}, every op of the "
+                                              f"step, repeated for {sec_c:.1f} s (fp64, OpenMP over rows)"}
+        if not args.no_configs:
+            line["configs_legend"] = {"C1": "pre_rms_256x64x64", "C2": "post_ln_65536x128x128",
+                                      "C3": "pre_rms_rowscale_32768x512x512",
+                                      "C4": "post_affine_16384x1024x2048", "C5": "llm_8192x4096x4096",
+                                      "row": ["fused_us", "plain_us", "norm_us", "roofline_frac",
+                                              "norm_hidden_pct"],
+                                      "FNA fwd": "FlashNormAttention forward, batch 768, Lq <= 1024, 4 heads: "
+                                                 "[fused_us, -, -, roofline_frac, -, torch_eager_us]"}
+            line["configs"] = config_table(nf, dev, stream, hbm_gbs, bf16_tf)
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

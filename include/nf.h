@@ -19,20 +19,26 @@
  *              fp32 per row.
  *   Memory     Every pointer is DEVICE memory of the current CUDA device,
  *              owned by the caller; the library keeps no reference after the
- *              call returns.  Y must not overlap any input.  The library
- *              allocates nothing per call, with one exception: post-norm
- *              rows wider than 256 columns exchanged through L2 (the default,
- *              see nf_set_postnorm_exchange) use a scratch buffer owned by
- *              the library, one per (device, stream), of about
- *              8 * M * ceil(N / 256) bytes.  The first such call on a stream
- *              (and a call with a larger M * ceil(N / 256) than before)
- *              allocates or grows it, synchronizing that stream; while the
- *              stream is being captured that call fails with
- *              NF_ERR_INVALID_ARG, so make it before capture.  Later calls
- *              reuse the buffer and are capture-safe; a captured graph keeps
- *              the buffer of the stream it was captured on, so replays of it
- *              must not run concurrently with other post-norm work on that
- *              stream's buffer.
+ *              call returns.  Y must not overlap any input.  Scratch memory
+ *              owned by the library, one buffer of each kind per (device,
+ *              stream): post-norm rows wider than 256 columns exchanged
+ *              through L2 (the default, see nf_set_postnorm_exchange) use
+ *              about 8 * M * ceil(N / 256) bytes; GEMMs split over the
+ *              contraction (nf_set_gemm_splitk) use SMs * 128 KB.  Rule: no
+ *              compute call ever synchronizes the host with the device.  A
+ *              call that finds its stream's buffer missing or too small
+ *              allocates a large enough one in stream order (cudaMallocAsync
+ *              and cudaMemsetAsync on `stream`); a buffer it replaces stays
+ *              allocated for the life of the process, because graphs
+ *              captured earlier may still use it.  nf_reserve_scratch sizes
+ *              both buffers up front: after it, calls on that stream with
+ *              shapes within its sizes allocate nothing.  While the stream
+ *              is being captured, a call that would allocate fails with
+ *              NF_ERR_INVALID_ARG; make it (or nf_reserve_scratch) before
+ *              capture.  A captured graph keeps the buffers of the stream it
+ *              was captured on, so its replays must not run concurrently
+ *              with other work on that stream's buffers.
+ *              nf_gemm_postnorm_ln_noalloc allocates nothing at any time.
  *   Alignment  X, W, Y (and in/out of nf_norm_rows) start on a 16-byte
  *              boundary; gamma / beta on 2 bytes; fp32 outputs on 4 bytes.
  *              K and N (cols for nf_norm_rows) are multiples of 8, so that
@@ -175,6 +181,10 @@ nf_status nf_gemm_postnorm_rms_res(const void* X, const void* W, const void* R,
  * one stream run one after the other; calls on different streams may overlap.
  * The counters serve at most 64 (device, stream) pairs per process: a call
  * from a 65th pair fails with NF_ERR_CUDA.
+ * Graphs: a CUDA graph captured from stream S keeps S's counter.  Its
+ * replays must not overlap one another, nor calls made on S (replay it on S,
+ * or order the replays with events); overlapping launches would share the
+ * counter and skip each other's batches.
  */
 #define NF_ACT_IDENTITY 0
 #define NF_ACT_GELU_TANH 1
@@ -237,9 +247,12 @@ nf_status nf_gemm_postnorm_ln(const void* X, const void* W, const void* gamma,
  * nf_gemm_postnorm_ln.  Where that plan exchanges row statistics through L2,
  * the scratch is a fixed device array inside the library (about 4.1 MiB per
  * device, cleared on the first call on each device) instead of the
- * per-stream buffer.  Limits of that array: ceil(M / 128) * ceil(N / 256)
- * <= 4096 and M <= 2^21, else NF_ERR_UNSUPPORTED_SHAPE (only for shapes that
- * use the L2 exchange).
+ * per-stream buffer.  Limit of that array: ceil(M / 128) * ceil(N / 256)
+ * <= 4096 exchange tiles (which implies M <= 2^19), else
+ * NF_ERR_UNSUPPORTED_SHAPE (only for shapes that use the L2 exchange).
+ * The first such call on a device looks the array up and clears it with a
+ * synchronous memset; make it before any stream capture (during a capture
+ * it fails with NF_ERR_INVALID_ARG).
  * Races: the array is one per device, shared by every stream and every
  * thread.  Two calls that may run on the device at the same time (on
  * different streams, or from graphs replayed concurrently) corrupt each
@@ -382,11 +395,20 @@ nf_status nf_set_postnorm_exchange(int mode);
  * (tile, slice) per SM; when a tensor-bound GEMM's last, partial wave holds
  * at most half as many tiles as SMs, only that wave's tiles are split.  Each
  * split unit writes an fp32 partial tile into a per-stream workspace (SMs x
- * 128 KB, allocated by the first such call on a stream, which must not be
- * inside a graph capture), and a second kernel adds the slices in a fixed
- * order and rounds to bf16, so results are reproducible.  mode 1: never
- * split.  Applies to later calls. */
+ * 128 KB, set up by nf_reserve_scratch or by the first such call on a
+ * stream, which must not be inside a graph capture), and a second kernel
+ * adds the slices in a fixed order and rounds to bf16, so results are
+ * reproducible.  mode 1: never split.  Applies to later calls. */
 nf_status nf_set_gemm_splitk(int mode);
+
+/* Scratch set-up for `stream` (see "Memory" above): makes the stream's
+ * post-norm exchange buffer large enough for post-norm calls (forward and
+ * backward) of up to max_rows x max_cols, and sets up its split-K workspace,
+ * both in stream order without synchronizing the host.  Afterwards, calls on
+ * the stream within those sizes allocate nothing and may be captured.
+ * max_cols <= NF_POSTNORM_MAX_N.  Refused (NF_ERR_INVALID_ARG) while the
+ * stream is being captured. */
+nf_status nf_reserve_scratch(int64_t max_rows, int64_t max_cols, nf_stream stream);
 
 /* Self-test of the time limit: launches one CTA that waits on a barrier no
  * thread ever arrives on, with limit `timeout_ns` (1e3..1e10).  After the

@@ -148,6 +148,48 @@ def workload_inputs(w: Workload, seed: int = 0) -> Dict[str, np.ndarray]:
                        gamma=w.gamma, beta=w.beta)
 
 
+def shard_rows(total_rows: int, world: int, rank: int):
+    """Contiguous row range [lo, hi) of `rank` when rows split over `world`
+    processes (sizes differ by at most one)."""
+    base, extra = divmod(total_rows, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def workload_shard(w: Workload, world: int, rank: int, seed: int = 0,
+                   chunk_rows: int = 4096) -> Dict[str, np.ndarray]:
+    """Rows shard_rows(world * w.M, world, rank) of the global problem with
+    world * w.M rows (X drawn exactly as make_inputs would draw it for that
+    many rows: the same streams in the same order, generated in chunks and
+    only the shard kept), with the full W, gamma and beta.  world == 1 gives
+    workload_inputs(w)."""
+    total = world * w.M
+    lo, hi = shard_rows(total, world, rank)
+    g = _streams(seed)
+    parts = []
+    scale = None
+    if w.x_dist == "row_scaled":  # the row scales have a stream of their own
+        scale = np.exp(g["scale"].normal(0.0, 1.0, size=(total, 1)))[lo:hi]
+    elif w.x_dist != "normal":
+        raise ValueError(f"unknown x_dist {w.x_dist!r}")
+    for r0 in range(0, hi, chunk_rows):
+        r1 = min(hi, r0 + chunk_rows)
+        z = _normal(g["X"], (r1 - r0, w.K), 0.0, 1.0)
+        if r1 > lo:
+            parts.append(z[max(lo, r0) - r0:])
+    x = np.concatenate(parts) if parts else np.zeros((0, w.K))
+    if scale is not None:
+        x = x * scale
+    out = {"X": bf16_round(x),
+           "W": bf16_round(_normal(g["W"], (w.K, w.N), 0.0, 1.0 / w.K))}
+    if w.gamma:
+        out["gamma"] = bf16_round(_normal(g["gamma"], (w.N,), 1.0, 0.1))
+    if w.beta:
+        out["beta"] = bf16_round(_normal(g["beta"], (w.N,), 0.0, 0.1))
+    out["rows"] = (lo, hi)
+    return out
+
+
 def sample_rows(M: int, count: int, seed: int = 1, tile_m: int = 128) -> np.ndarray:
     """Rows to check at full size: both ends, every tile edge near them and a
     seeded spread in between (sorted, unique, int64)."""

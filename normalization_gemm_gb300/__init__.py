@@ -85,6 +85,7 @@ _SIGS = {
     "nf_set_postnorm_tile_n": [ctypes.c_int],
     "nf_set_postnorm_exchange": [ctypes.c_int],
     "nf_set_gemm_splitk": [ctypes.c_int],
+    "nf_reserve_scratch": [_I64, _I64, _VP],
     "nf_selftest_wait_timeout": [ctypes.c_uint64, _VP],
     "nf_plan_gemm": [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(NFPlan)],
     "nf_abi_version": [],
@@ -472,6 +473,12 @@ def set_postnorm_exchange(mode: int) -> None:
     """Post-norm rows wider than 256 columns: 0 automatic, XCH_CLUSTER (DSMEM in a
     thread-block cluster) or XCH_GLOBAL (L2 between tiles of a cooperative grid)."""
     _check(lib().nf_set_postnorm_exchange(int(mode)), "nf_set_postnorm_exchange")
+
+
+def reserve_scratch(max_rows: int, max_cols: int, stream=None) -> None:
+    """Size the stream's scratch (post-norm exchange, split-K workspace) for
+    shapes up to max_rows x max_cols; later calls within it allocate nothing."""
+    _check(lib().nf_reserve_scratch(int(max_rows), int(max_cols), _stream(stream)), "nf_reserve_scratch")
 
 
 def selftest_wait_timeout(ns: int, stream=None) -> None:

@@ -94,8 +94,11 @@ DeviceState g_dev[kMaxDevices];
 // Global-exchange scratch, one buffer per (device, stream): launches on one
 // stream run in order, so each buffer is used by one launch at a time.  The
 // buffer holds the header and two counter banks of bank_ints each, then
-// (256-byte aligned) stats_bytes of partial statistics; both capacities only
-// grow.
+// (256-byte aligned) stats_bytes of partial statistics.  A call that needs
+// more replaces the stream's buffer with a larger one, allocated and cleared
+// in stream order (cudaMallocAsync / cudaMemsetAsync: no host
+// synchronization); the smaller one is kept for the life of the process,
+// since a graph captured earlier may still use it.
 struct XScratch {
     int dev = -1;
     cudaStream_t stream = nullptr;
@@ -112,8 +115,8 @@ constexpr int kMaxScratch = 64;
 // Fixed exchange scratch of nf_gemm_postnorm_ln_noalloc: a file-scope device
 // array (header, two counter banks, partial statistics), so that entry point
 // allocates nothing at any time.  Zero when set up on a device.
-constexpr int64_t kNoAllocBankInts = 16384;      // row tiles (M <= 2^21)
-constexpr int64_t kNoAllocStatsBytes = 4 << 20;  // m_tiles * n_tiles <= 4096
+constexpr int64_t kNoAllocBankInts = 16384;      // 4 counters per row tile: m_tiles <= 4096
+constexpr int64_t kNoAllocStatsBytes = 4 << 20;  // m_tiles * n_tiles <= 4096 (binds first: n_tiles >= 3)
 constexpr int64_t kNoAllocStatsOffset = (XCH_CNT0 + 2 * kNoAllocBankInts) * 4;
 constexpr int64_t kNoAllocBytes = kNoAllocStatsOffset + kNoAllocStatsBytes;
 static_assert(kNoAllocStatsOffset % 256 == 0, "statistics region alignment");
@@ -451,9 +454,9 @@ nf_status blocks_per_sm(DeviceState* d, const GemmVariant* v, int* out) {
     return NF_OK;
 }
 
-// The stream's global-exchange scratch for m_tiles x n_tiles tiles.
-// Allocating (first use on a stream, or a larger shape) synchronizes the
-// stream and is refused while the stream is being captured into a graph.
+// The stream's global-exchange scratch for m_tiles x n_tiles tiles.  Set up
+// (or replaced by a larger one) in stream order, without synchronizing the
+// host; refused while the stream is being captured into a graph.
 nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, int32_t* bank, float2** stats) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -473,33 +476,30 @@ nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, 
     if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
     if (cs != cudaStreamCaptureStatusNone)
         return fail(NF_ERR_INVALID_ARG,
-                    "post-norm exchange scratch is set up on the first call per stream (and grown for larger "
-                    "shapes): make that call before capturing the stream");
+                    "post-norm exchange scratch is set up on the first call per stream (and enlarged for larger "
+                    "shapes): make that call, or nf_reserve_scratch, before capturing the stream");
+    if (!x && g_xs_n == kMaxScratch) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many streams with post-norm scratch");
     int64_t bank_ints = need_bank, stats_bytes = need_stats;
-    if (!x) {
-        if (g_xs_n == kMaxScratch) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many streams with post-norm scratch");
-        x = &g_xs[g_xs_n++];
-        x->dev = dev;
-        x->stream = stream;
-    } else {
-        if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
-        cudaFree(x->ptr);
+    if (x) {
         bank_ints = bank_ints > x->bank_ints ? bank_ints : x->bank_ints;
         stats_bytes = stats_bytes > x->stats_bytes ? stats_bytes : x->stats_bytes;
-        x->ptr = nullptr;
-        x->bytes = 0;
-        x->bank_ints = x->stats_bytes = 0;
     }
     // Round both regions up so that modest growth reuses the buffer.
     bank_ints = (bank_ints + 4095) / 4096 * 4096;
     stats_bytes = (stats_bytes + (1 << 20) - 1) >> 20 << 20;
     const size_t bytes = static_cast<size_t>(XScratch::stats_offset(bank_ints) + stats_bytes);
     void* ptr = nullptr;
-    if ((e = cudaMalloc(&ptr, bytes)) != cudaSuccess) return fail_cuda(e, "cudaMalloc(exchange scratch)");
+    if ((e = cudaMallocAsync(&ptr, bytes, stream)) != cudaSuccess) return fail_cuda(e, "cudaMallocAsync(exchange scratch)");
     if ((e = cudaMemsetAsync(ptr, 0, bytes, stream)) != cudaSuccess) {
-        cudaFree(ptr);
+        cudaFreeAsync(ptr, stream);
         return fail_cuda(e, "cudaMemsetAsync(exchange scratch)");
     }
+    if (!x) {
+        x = &g_xs[g_xs_n++];
+        x->dev = dev;
+        x->stream = stream;
+    }
+    // (the previous buffer, if any, stays allocated: see XScratch)
     x->ptr = static_cast<uint8_t*>(ptr);
     x->bytes = bytes;
     x->bank_ints = bank_ints;
@@ -513,7 +513,8 @@ nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, 
 // Split-K workspace, one per (device, stream), sized once for a full wave of
 // 128 x 256 fp32 partial tiles (splitk x M x N <= SMs x 128 x 256).  Every
 // value the reduction reads was written by the GEMM before it, so it needs no
-// clearing.  The first call per stream allocates (refused during capture).
+// clearing.  The first call per stream allocates it in stream order (no host
+// synchronization; refused during capture).
 struct SKScratch {
     int dev = -1;
     cudaStream_t stream = nullptr;
@@ -536,12 +537,12 @@ nf_status splitk_scratch(cudaStream_t stream, int sm_count, float** out) {
     if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
     if (cs != cudaStreamCaptureStatusNone)
         return fail(NF_ERR_INVALID_ARG,
-                    "the split-K workspace is set up on the first split GEMM per stream: make that call before "
-                    "capturing the stream");
+                    "the split-K workspace is set up on the first split GEMM per stream: make that call, or "
+                    "nf_reserve_scratch, before capturing the stream");
     if (g_sk_n == kMaxScratch) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many streams with split-K workspaces");
     void* ptr = nullptr;
     const size_t bytes = static_cast<size_t>(sm_count) * TILE_M * 256 * sizeof(float);
-    if ((e = cudaMalloc(&ptr, bytes)) != cudaSuccess) return fail_cuda(e, "cudaMalloc(split-K workspace)");
+    if ((e = cudaMallocAsync(&ptr, bytes, stream)) != cudaSuccess) return fail_cuda(e, "cudaMallocAsync(split-K workspace)");
     g_sk[g_sk_n].dev = dev;
     g_sk[g_sk_n].stream = stream;
     g_sk[g_sk_n].ptr = static_cast<float*>(ptr);
@@ -551,14 +552,21 @@ nf_status splitk_scratch(cudaStream_t stream, int sm_count, float** out) {
 }
 
 // The current device's fixed no-alloc scratch: address looked up and the
-// array cleared on first use per device.
-nf_status noalloc_scratch(uint8_t** out) {
+// array cleared (synchronously) on first use per device, which is refused
+// while `stream` is being captured.
+nf_status noalloc_scratch(cudaStream_t stream, uint8_t** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(NF_ERR_NO_DEVICE, "device index out of range");
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_noalloc_ptr[dev]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(NF_ERR_INVALID_ARG,
+                        "the no-alloc scratch is cleared by the first call on each device: make that call before "
+                        "capturing the stream");
         void* p = nullptr;
         if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess)
             return fail_cuda(e, "cudaGetSymbolAddress(no-alloc scratch)");
@@ -673,9 +681,9 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
         if (fixed_scratch) {
             if (xch_bank_ints(p.m_tiles) > kNoAllocBankInts || xch_stats_bytes(p.m_tiles, p.n_tiles) > kNoAllocStatsBytes)
                 return fail(NF_ERR_UNSUPPORTED_SHAPE,
-                            "no-alloc post-norm: ceil(M/128) * ceil(N/256) must be <= 4096 and M <= 2^21");
+                            "no-alloc post-norm: ceil(M/128) * ceil(N/256) must be <= 4096 (so M <= 2^19)");
             uint8_t* base = nullptr;
-            if ((st = noalloc_scratch(&base)) != NF_OK) return st;
+            if ((st = noalloc_scratch(stream, &base)) != NF_OK) return st;
             a.xcnt = reinterpret_cast<int*>(base);
             a.xbank = static_cast<int32_t>(kNoAllocBankInts);
             a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
@@ -1051,6 +1059,26 @@ nf_status nf_set_gemm_splitk(int mode) {
     if (mode != 0 && mode != 1) return fail(NF_ERR_INVALID_ARG, "split-K mode: 0 automatic, 1 never");
     g_splitk_mode = mode;
     return NF_OK;
+}
+
+nf_status nf_reserve_scratch(int64_t max_rows, int64_t max_cols, nf_stream stream) {
+    if (max_rows < 0 || max_cols < 0) return fail(NF_ERR_INVALID_ARG, "sizes must be >= 0");
+    if (max_rows > static_cast<int64_t>(INT32_MAX) - TILE_M || max_cols > NF_POSTNORM_MAX_N)
+        return fail(NF_ERR_UNSUPPORTED_SHAPE, "max_rows < 2^31 - 128 and max_cols <= NF_POSTNORM_MAX_N");
+    DeviceState* d = nullptr;
+    nf_status st = device_state(&d);
+    if (st != NF_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (max_rows > 0 && max_cols > 256) {
+        int* cnt = nullptr;
+        int32_t bank = 0;
+        float2* stats = nullptr;
+        const int m_tiles = static_cast<int>((max_rows + TILE_M - 1) / TILE_M);
+        const int n_tiles = static_cast<int>((max_cols + 255) / 256);
+        if ((st = xch_scratch(s, m_tiles, n_tiles, &cnt, &bank, &stats)) != NF_OK) return st;
+    }
+    float* ws = nullptr;
+    return splitk_scratch(s, d->sm_count, &ws);
 }
 
 nf_status nf_set_launch_overlap(int enable) {

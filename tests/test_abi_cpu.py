@@ -305,3 +305,10 @@ def test_splitk_can_be_switched_off(L):
         nf.set_gemm_splitk(0)
     assert nf.plan_gemm(0, 512, 512, 32768, 152)["splitk"] == 19
     assert L.nf_set_gemm_splitk(2) == INVALID
+
+
+def test_reserve_scratch_argument_checks(L):
+    """Sizes are validated before any device work."""
+    assert L.nf_reserve_scratch(-1, 0, None) == INVALID
+    assert L.nf_reserve_scratch(0, -8, None) == INVALID
+    assert L.nf_reserve_scratch(1024, 4104, None) == SHAPE

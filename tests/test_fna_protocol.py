@@ -286,38 +286,78 @@ def test_exchange_model_catches_shared_slot():
 
 
 # ---------------------------------------------------------------- the batch ring
-def ring_cta(rank, H, nb, entries, bfull, bempty, ring, seen, check_empty=True):
-    """One CTA's producer: rank 0 publishes entry k into every CTA's ring slot
-    k % nb (after all H CTAs emptied entry k - nb); every CTA waits for each
-    entry in turn, reads it, re-arms its slot and tells rank 0 the slot is free."""
-    k_pub = 0
+class TxBar(Bar):
+    """An mbarrier that also counts transaction bytes: a phase completes once
+    its arrivals are all in and its expected bytes have all landed (in either
+    order)."""
+
+    def __init__(self, name, count=1):
+        super().__init__(name, count)
+        self.tx = 0
+
+    def arrive_expect(self, phase, nbytes):
+        assert self.done == phase, f"{self.name}: re-arm for phase {phase} while at phase {self.done}"
+        self.tx += nbytes
+        self.arrivals += 1
+        self._complete()
+
+    def complete_tx(self, phase, nbytes):
+        assert self.done == phase, f"{self.name}: bytes for phase {phase} landed at phase {self.done}"
+        self.tx -= nbytes
+        self._complete()
+
+    def _complete(self):
+        if self.arrivals == self.count and self.tx == 0:
+            self.done += 1
+            self.arrivals = 0
+
+
+def ring_cta(rank, H, nb, entries, bfull, bempty, ring, seen, check_empty=True, rearm=True):
+    """One CTA's producer, in the kernel's order.  Rank 0 publishes entry k
+    (the batch from the counter; the last entry is the end mark) with a 4-byte
+    remote write into slot k % nb of every CTA's ring, counted on that CTA's
+    bfull[slot], after waiting on bempty[slot] for every CTA to have read entry
+    k - nb.  Every CTA waits for entry k on bfull, reads it, re-arms bfull for
+    entry k + nb (one arrival expecting 4 bytes), then arrives on rank 0's
+    bempty; rank 0 then publishes entry k + 1 (so it runs one entry ahead of
+    the batch it works on).  A CTA stops after reading the end mark."""
+    def publish(k):
+        s = k % nb
+        if k >= nb and check_empty:
+            yield ("wait", bempty[s], k // nb - 1)
+        for c in range(H):
+            prev = ring[c][s]
+            assert prev is None or prev[1], f"ring of CTA {c} slot {s}: entry {prev[0]} overwritten unread"
+            ring[c][s] = [k, False]
+            bfull[c][s].complete_tx(k // nb, 4)
+
+    if rank == 0:
+        yield from publish(0)
     for k in range(entries):
-        if rank == 0:
-            while k_pub <= min(k + 1, entries - 1):  # publish up to one entry ahead
-                s = k_pub % nb
-                if k_pub >= nb and check_empty:
-                    yield ("wait", bempty[s], k_pub // nb - 1)
-                for c in range(H):
-                    prev = ring[c][s]
-                    assert prev is None or prev[1], f"ring of CTA {c} slot {s}: entry {prev[0]} overwritten unread"
-                    ring[c][s] = [k_pub, False]
-                    bfull[c][s].arrive(k_pub // nb)
-                k_pub += 1
         s = k % nb
         yield ("wait", bfull[rank][s], k // nb)
         assert ring[rank][s][0] == k, f"CTA {rank} read entry {ring[rank][s][0]} for {k}"
         ring[rank][s][1] = True
         seen[rank].append(k)
+        if rearm:
+            bfull[rank][s].arrive_expect(k // nb + 1, 4)
         bempty[s].arrive(k // nb)
+        if k == entries - 1:  # the end mark
+            return
+        if rank == 0:
+            yield from publish(k + 1)
 
 
-def run_ring(H, nb, entries, seed, check_empty=True):
+def run_ring(H, nb, entries, seed, check_empty=True, rearm=True):
     rng = random.Random(seed)
-    bfull = [[Bar(f"bfull[{c}][{s}]") for s in range(nb)] for c in range(H)]
+    bfull = [[TxBar(f"bfull[{c}][{s}]") for s in range(nb)] for c in range(H)]
+    for c in range(H):  # set-up: every slot armed for its first entry
+        for s in range(nb):
+            bfull[c][s].arrive_expect(0, 4)
     bempty = [Bar(f"bempty[{s}]", count=H) for s in range(nb)]
     ring = [[None] * nb for _ in range(H)]
     seen = [[] for _ in range(H)]
-    procs = {c: ring_cta(c, H, nb, entries, bfull, bempty, ring, seen, check_empty) for c in range(H)}
+    procs = {c: ring_cta(c, H, nb, entries, bfull, bempty, ring, seen, check_empty, rearm) for c in range(H)}
     waiting = {}
     for _ in range(200000):
         if not procs:
@@ -356,3 +396,11 @@ def test_batch_ring_model_catches_missing_empty_wait():
         except (Violation, AssertionError):
             caught += 1
     assert caught > 0
+
+
+def test_batch_ring_model_catches_missing_rearm():
+    """Without the re-arm, an entry's bytes land in a phase with no arrival
+    pending: the phase never completes."""
+    for seed in range(20):
+        with pytest.raises(Violation):
+            run_ring(2, 2, entries=9, seed=seed, rearm=False)

@@ -209,6 +209,33 @@ def test_full_size_workloads(dev, orc, name):
             assert float((ms - 1).abs().max()) < 2e-2, f"{name}: row mean square"
 
 
+@pytest.mark.parametrize("tile_n", [256, 512], ids=["cluster16x256", "cluster8x512"])
+def test_llm_post_ln_row_cluster_full_shape(dev, orc, tile_n):
+    """The 8192 x 4096 x 4096 post-LN with the blog §3 layout: a thread-block
+    cluster spans the 4096-column row (16 CTAs of 256 columns, or 8 of 512),
+    partial statistics through DSMEM, at the full shape: sampled rows against
+    the oracle, every row's moments, and the same bits as a second call."""
+    import torch
+    w = nf_inputs.WORKLOADS["llm_8192x4096x4096"]
+    inp = nf_inputs.workload_inputs(w)
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    nf.set_postnorm_exchange(nf.XCH_CLUSTER)
+    nf.set_postnorm_tile_n(tile_n)
+    try:
+        y = nf.gemm_postnorm_ln(X, W, w.eps)
+        y2 = nf.gemm_postnorm_ln(X, W, w.eps)
+        torch.cuda.synchronize()
+    finally:
+        nf.set_postnorm_exchange(0)
+        nf.set_postnorm_tile_n(0)
+    assert torch.equal(y, y2)
+    rows = nf_inputs.sample_rows(w.M, 128, seed=9)
+    ref = orc.gemm_postnorm_ln(inp["X"], inp["W"], w.eps, rows=rows)[0]
+    assert_close(to_f64(y[torch.from_numpy(rows).to(dev)]), ref, f"llm post-LN cluster of {tile_n}-column CTAs")
+    mu, ms = _row_moments(y)
+    assert float(mu.abs().max()) < 2e-2 and float((ms - 1).abs().max()) < 2e-2
+
+
 def test_unfused_pair_matches_fused(dev, orc):
     """Blog §1 baseline pair (GEMM + separate norm kernel) against the fused
     kernels, both against the oracle, on the same inputs."""

@@ -1,5 +1,6 @@
 """The seeded input generator: bf16 rounding and determinism.  CPU only."""
 import numpy as np
+import pytest
 import torch
 
 import nf_inputs
@@ -61,3 +62,20 @@ def test_workloads_match_the_five_configurations():
 def test_sample_rows_cover_edges():
     r = nf_inputs.sample_rows(65536, 64)
     assert r[0] == 0 and r[-1] == 65535 and 127 in r and 128 in r and np.all(np.diff(r) > 0)
+
+
+@pytest.mark.parametrize("x_dist", ["normal", "row_scaled"])
+@pytest.mark.parametrize("world", [1, 2, 3])
+def test_shards_concatenate_to_the_global_problem(world, x_dist):
+    """Rank r's shard is rows shard_rows(world * M, world, r) of exactly the X
+    make_inputs draws for world * M rows; W, gamma and beta are the same."""
+    w = nf_inputs.Workload("t", 150, 72, 40, 1e-5, ("post_ln",), x_dist=x_dist, gamma=True, beta=True)
+    g = nf_inputs.make_inputs(world * w.M, w.K, w.N, seed=3, x_dist=x_dist, gamma=True, beta=True)
+    xs = []
+    for r in range(world):
+        sh = nf_inputs.workload_shard(w, world, r, seed=3, chunk_rows=64)
+        assert sh["rows"] == nf_inputs.shard_rows(world * w.M, world, r)
+        for k in ("W", "gamma", "beta"):
+            assert np.array_equal(sh[k], g[k])
+        xs.append(sh["X"])
+    assert np.array_equal(np.concatenate(xs), g["X"])
