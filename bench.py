@@ -13,12 +13,11 @@ nf_gemm_postnorm_ln) on one batch, i.e. one pass of the whole hot path:
 Prints ONE JSON line (rank 0):
   value        TFLOP/s of the whole job (all ranks' steps), inputs resident in
                HBM, timed with CUDA events on the launching stream over exactly
-               K steps launched one by one, with an event before each kernel
-               (so each kernel's own mean duration comes from the same timed
-               region).  Successive steps rotate over buffer sets whose
-               footprint exceeds 3x L2.
+               K steps replayed from one CUDA graph.  Successive steps rotate
+               over buffer sets whose footprint exceeds 3x L2.
   roofline     the dominant kernel of the step (the one with the larger mean
-               duration) against the bf16 tensor peak of MEASURED_PEAKS.json
+               duration, each timed alone: back-to-back launches from a CUDA
+               graph) against the burst bf16 tensor peak of MEASURED_PEAKS.json
                (2MNK per launch over its mean duration); traffic (DRAM read +
                write bytes per launch) from the committed ncu summary of that
                kernel when its source hash matches, else null.
@@ -537,11 +536,11 @@ def call_op(nf, op, X, W, Y, G, B, eps, stream):
 
 
 def measure_step(nf, w, ops, X0, W0, G, B, dev, stream, steps, warmup, dist=None, sampler=None):
-    """The timed region of the headline: `steps` steps, each one call per op
-    in `ops` on one buffer set (rotating sets > 3x L2), launched one by one on
-    `stream` with a CUDA event before every kernel and one after the last.
-    Returns (seconds of the region (max over ranks), mean seconds per kernel
-    of each op, buffer sets, set bytes)."""
+    """The timed region of the headline: exactly `steps` steps, each one call
+    per op in `ops` on one buffer set (rotating sets > 3x L2), replayed from
+    a CUDA graph of the `steps` steps on `stream` (programmatic dependent
+    launch between the kernels stays on), CUDA events before and after.
+    Returns (seconds (max over ranks), buffer sets, set bytes, step fn)."""
     import torch
     Ys = [torch.empty((X0.shape[0], w.N), dtype=torch.bfloat16, device=dev) for _ in ops]
     set_bytes = X0.numel() * 2 + sum(y.numel() * 2 for y in Ys)
@@ -552,38 +551,22 @@ def measure_step(nf, w, ops, X0, W0, G, B, dev, stream, steps, warmup, dist=None
         for op, y in zip(ops, ys):
             call_op(nf, op, x, W0, y, G, B, w.eps, stream)
 
-    with torch.cuda.stream(stream):
-        for i in range(warmup):
-            step(i)
-    torch.cuda.synchronize()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps * len(ops) + 1)]
-    if dist is not None and dist.is_initialized():
-        dist.barrier()
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.start()
-    with torch.cuda.stream(stream):
-        k = 0
-        for i in range(steps):
-            x, *ys = sets[i % nsets]
-            for op, y in zip(ops, ys):
-                evs[k].record(stream)
-                call_op(nf, op, x, W0, y, G, B, w.eps, stream)
-                k += 1
-        evs[k].record(stream)
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.stop()
-    if dist is not None and dist.is_initialized():
-        dist.barrier()
-    total = evs[0].elapsed_time(evs[-1]) / 1e3
-    per_op = {}
-    for j, op in enumerate(ops):
-        d = [evs[i * len(ops) + j].elapsed_time(evs[i * len(ops) + j + 1]) / 1e3 for i in range(steps)]
-        per_op[op] = sum(d) / len(d)
-    del sets, Ys
+    sec = time_steps(step, steps, warmup, stream, dist, chunk=steps, sampler=sampler)
+    return sec, nsets, set_bytes, step, sets
+
+
+def measure_kernel_alone(nf, w, op, X0, W0, G, B, dev, stream, launches=200, warmup=10):
+    """Mean duration of one op's fused kernel timed alone: `launches`
+    back-to-back calls from a CUDA graph over rotating buffer sets, CUDA
+    events on the launching stream."""
+    import torch
+    Y0 = torch.empty((X0.shape[0], w.N), dtype=torch.bfloat16, device=dev)
+    sets, nsets = make_sets([X0, Y0], X0.numel() * 2 + Y0.numel() * 2, dev)
+    fn = lambda i: call_op(nf, op, sets[i % nsets][0], W0, sets[i % nsets][1], G, B, w.eps, stream)  # noqa: E731
+    t = time_steps(fn, launches, warmup, stream) / launches
+    del sets
     torch.cuda.empty_cache()
-    return max_over_ranks(total, dist), per_op, nsets, set_bytes, step
+    return t
 
 
 def e2e_measure(nf, w, ops, inp, dev, stream, steps):
@@ -905,29 +888,24 @@ def main(argv=None):
     B = _to_dev(inp["beta"], dev) if w.beta else None
     flops_step = len(ops) * 2 * rows_here * w.N * w.K
     sampler = ClockSampler(local_rank)
-    sec, per_op, nsets, set_bytes, step_fn = measure_step(nf, w, ops, X0, W0, G, B, dev, stream, args.steps,
-                                                          args.warmup, dist=dist, sampler=sampler)
+    sec, nsets, set_bytes, step_fn, sets = measure_step(nf, w, ops, X0, W0, G, B, dev, stream, args.steps,
+                                                        args.warmup, dist=dist, sampler=sampler)
     t_step = sec / args.steps
     value = world * flops_step / t_step / 1e12
     clocks = sampler.summary("timed")
     if clocks["samples"] < 3 and not args.no_soak:
-        # The timed region was shorter than the sampling period: run the same
-        # steps for ~1.5 s right after it and sample that instead.
+        # The timed region was shorter than three sampling periods: replay the
+        # same steps for ~1.5 s right after it and sample that instead.
         soak = ClockSampler(local_rank)
         reps = max(args.steps, int(1.5 / max(t_step, 1e-7)))
-        Ys = [torch.empty((rows_here, w.N), dtype=torch.bfloat16, device=dev) for _ in ops]
-        soak.start()
-        with torch.cuda.stream(stream):
-            for _ in range(reps):
-                for op, y in zip(ops, Ys):
-                    call_op(nf, op, X0, W0, y, G, B, w.eps, stream)
-        torch.cuda.synchronize()
-        soak.stop()
-        del Ys
+        time_steps(step_fn, reps, 3, stream, None, chunk=min(reps, 200), sampler=soak)
         clocks = soak.summary("soak right after the timed region (the timed region was shorter than "
                               "three 50 ms sampling periods)")
+    del sets
+    torch.cuda.empty_cache()
 
-    # the dominant kernel of the step against its roofline
+    # each kernel of the step timed alone; the dominant one against its roofline
+    per_op = {op: measure_kernel_alone(nf, w, op, X0, W0, G, B, dev, stream) for op in ops}
     dom = max(ops, key=lambda o: per_op[o])
     kflops = 2 * rows_here * w.N * w.K
     kbytes = algorithmic_bytes(rows_here, w.N, w.K, gamma=w.gamma and dom != "pre_rms",
@@ -937,14 +915,17 @@ def main(argv=None):
         achieved = kflops / t_dom / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
                 "frac": achieved / bf16_tf, "traffic": profiled_traffic(w.name, dom),
-                "kernel": KERNEL_OF_OP[dom], "peak_source": f"{peak_src} bf16_tflops (burst; of measured)",
-                "algorithmic_flops_per_launch": kflops, "mean_launch_us": t_dom * 1e6}
+                "kernel": KERNEL_OF_OP[dom], "peak_source": f"{peak_src} bf16_tflops (burst: the kernel "
+                                                            f"timed alone; of measured)",
+                "algorithmic_flops_per_launch": kflops, "mean_launch_us": t_dom * 1e6,
+                "timing": "200 back-to-back launches from a CUDA graph, rotating buffers, CUDA events"}
     else:
         achieved = kbytes / t_dom / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                 "frac": achieved / hbm_gbs, "traffic": profiled_traffic(w.name, dom),
                 "kernel": KERNEL_OF_OP[dom], "peak_source": f"{peak_src} hbm_gbs (of measured)",
-                "algorithmic_bytes_per_launch": kbytes, "mean_launch_us": t_dom * 1e6}
+                "algorithmic_bytes_per_launch": kbytes, "mean_launch_us": t_dom * 1e6,
+                "timing": "200 back-to-back launches from a CUDA graph, rotating buffers, CUDA events"}
     status, detail = nf.device_status()
 
     line = {
@@ -958,7 +939,7 @@ def main(argv=None):
                    "per_gpu_rows": rows_here, "parallelism": f"rows x{world} (shard of one seeded problem), "
                                                             f"no collective",
                    "l2": f"rotating {nsets} buffer sets of {set_bytes / 2**20:.0f} MiB (> 3x L2 between reuses)",
-                   "launch": "one by one, a CUDA event before each kernel"},
+                   "launch": f"one CUDA graph of the {args.steps} steps"},
         "gpu_launches": args.steps * len(ops),
         "roofline": roof,
         "kernel_us": {KERNEL_OF_OP[o]: per_op[o] * 1e6 for o in ops},

@@ -377,6 +377,12 @@ nf_status nf_set_launch_overlap(int enable);
  * post-norm calls that use the cluster exchange. */
 nf_status nf_set_postnorm_tile_n(int tile_n);
 
+/* Column tile per CTA of plain and Lazy Pre-Norm GEMMs (nf_gemm_plain,
+ * nf_gemm_prenorm_rms): 0 (default) automatic -- the
+ * smallest of 64 / 128 / 256 that covers N, else 256 -- or 64, 128, 256
+ * forced.  Applies to later calls. */
+nf_status nf_set_gemm_tile_n(int tile_n);
+
 /* How post-norm rows wider than 256 columns exchange partial statistics:
  * 0 (default) automatic -- one 512-column CTA per row while N <= 512, else
  * NF_XCH_GLOBAL when K >= 512, else NF_XCH_CLUSTER; NF_XCH_CLUSTER: a

@@ -83,6 +83,7 @@ _SIGS = {
     "nf_set_wait_timeout_ns": [ctypes.c_uint64],
     "nf_set_launch_overlap": [ctypes.c_int],
     "nf_set_postnorm_tile_n": [ctypes.c_int],
+    "nf_set_gemm_tile_n": [ctypes.c_int],
     "nf_set_postnorm_exchange": [ctypes.c_int],
     "nf_set_gemm_splitk": [ctypes.c_int],
     "nf_reserve_scratch": [_I64, _I64, _VP],
@@ -462,6 +463,11 @@ def set_launch_overlap(enable: bool) -> None:
 def set_postnorm_tile_n(tile_n: int) -> None:
     """Post-norm column tile per CTA: 0 automatic, 256 or 512 forced."""
     _check(lib().nf_set_postnorm_tile_n(int(tile_n)), "nf_set_postnorm_tile_n")
+
+
+def set_gemm_tile_n(tile_n: int) -> None:
+    """Column tile of plain and pre-norm GEMMs: 0 automatic, 64, 128 or 256 forced."""
+    _check(lib().nf_set_gemm_tile_n(int(tile_n)), "nf_set_gemm_tile_n")
 
 
 def set_gemm_splitk(mode: int) -> None:

@@ -62,6 +62,8 @@ uint64_t g_timeout_ns = 2000000000ull;
 bool g_overlap = true;
 // Post-norm column tile per CTA of a cluster: 0 = automatic, 256 or 512 forced.
 int g_post_tile = 0;
+// Column tile of plain and pre-norm GEMMs: 0 = automatic, 64, 128 or 256 forced.
+int g_gemm_tile = 0;
 // Post-norm rows wider than 256 columns: 0 = automatic, else an Exchange mode.
 int g_post_xch = 0;
 // A cooperative launch accepted the programmatic-serialization attribute.
@@ -265,6 +267,7 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
     const bool post = op == OP_POST_LN || op == OP_POST_RMS;
     const bool bwd = op == OP_BWD_LN || op == OP_BWD_RMS;
     p->tile_n = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+    if ((op == OP_PLAIN || op == OP_PRE) && ops == 0 && g_gemm_tile != 0) p->tile_n = g_gemm_tile;
     p->xch = XCH_NONE;
     if (bwd && N > 256) {
         // Rows of two tiles: a cluster of 2, which co-resides on every SM.
@@ -1045,6 +1048,13 @@ nf_status nf_set_wait_timeout_ns(uint64_t ns) {
 nf_status nf_set_postnorm_tile_n(int tile_n) {
     if (tile_n != 0 && tile_n != 256 && tile_n != 512) return fail(NF_ERR_INVALID_ARG, "tile_n must be 0, 256 or 512");
     g_post_tile = tile_n;
+    return NF_OK;
+}
+
+nf_status nf_set_gemm_tile_n(int tile_n) {
+    if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256)
+        return fail(NF_ERR_INVALID_ARG, "tile_n must be 0, 64, 128 or 256");
+    g_gemm_tile = tile_n;
     return NF_OK;
 }
 

@@ -8,6 +8,11 @@
 //   * A row of `cols` bf16 is 16-byte chunks; TPR threads (a power of two)
 //     share a row, each holding CPT chunks (CPT * 8 values) in registers, so
 //     the row is read from HBM exactly once and written once.
+//   * Bytes in flight: the next row block's chunks are loaded (raw, 4
+//     registers a chunk) before the current block is reduced, and gamma /
+//     beta are read through the read-only cache where they are used rather
+//     than held in registers, so four CTAs fit on an SM for rows of up to
+//     4096 columns.
 //   * Reductions: xor-shuffles inside a warp; for TPR > 32 a second step
 //     through shared memory across the row's warps.
 //   * LayerNorm takes two passes over the registers (mean, then squared
@@ -51,8 +56,40 @@ __device__ __forceinline__ float group_sum(float x, float* red, int warp, int la
     return x;
 }
 
-template <int TPR, int CPT, int KIND>
-__global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormArgs a) {
+// This thread's CPT 16-byte chunks (t, t + TPR, ...) of `row`, raw; zeros
+// past the row's end or for a row past the last.
+template <int TPR, int CPT, bool STREAM>
+__device__ __forceinline__ void load_row_chunks(const uint4* base, int64_t row, bool live, int t, int chunks,
+                                                uint4 (&q)[CPT]) {
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+        const int c = t + i * TPR;
+        if (live && c < chunks)
+            q[i] = STREAM ? __ldcs(base + row * chunks + c) : __ldcg(base + row * chunks + c);
+        else
+            q[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Occupancy target: 4 CTAs of 256 threads per SM (64 registers a thread)
+// for the plain forward with rows of up to four chunks a thread, 2 for the
+// residual forward and the backward (two tensors' chunks in flight), half
+// that for rows of eight chunks a thread.  Bytes in flight come from the
+// occupancy and from loading the next row block before reducing the current
+// one.
+template <int CPT, bool HEAVY>
+struct NormOcc {
+    static constexpr int MIN_BLOCKS = (HEAVY ? 2 : 4) / (CPT > 4 ? 2 : 1);
+};
+
+// Value e (0..7) of a chunk of 8 packed bf16.
+__device__ __forceinline__ float chunk_val(const uint4& q, int e) {
+    const uint32_t w = (e >> 1) == 0 ? q.x : (e >> 1) == 1 ? q.y : (e >> 1) == 2 ? q.z : q.w;
+    return (e & 1) ? bf16hi(w) : bf16lo(w);
+}
+
+template <int TPR, int CPT, int KIND, bool RES>
+__global__ void __launch_bounds__(NORM_THREADS, (NormOcc<CPT, RES>::MIN_BLOCKS)) nf_norm_rows_kernel(const NormArgs a) {
     constexpr int RPB = NORM_THREADS / TPR;  // rows per block-step
     __shared__ float red[NORM_THREADS / 32];
     const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -61,13 +98,18 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
     const int rg = static_cast<int>(threadIdx.x) / TPR;
     const int chunks = a.cols >> 3;
     const uint4* in = reinterpret_cast<const uint4*>(a.in);
+    const uint4* res = reinterpret_cast<const uint4*>(a.res);
     uint4* out = reinterpret_cast<uint4*>(a.out);
+    uint4* hout = reinterpret_cast<uint4*>(a.h_out);
+    const uint4* gam = reinterpret_cast<const uint4*>(a.gamma);
+    const uint4* bet = reinterpret_cast<const uint4*>(a.beta);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * RPB;
     // Warm L2 with this CTA's first two row blocks while a preceding grid may
     // still be running (a prefetch only fills L2, where that grid's writes
     // land, so the loads after the wait below never see stale data).
     if (threadIdx.x == 0) {
         for (int it = 0; it < 2; ++it) {
-            const int64_t r = (static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(it) * gridDim.x) * RPB;
+            const int64_t r = static_cast<int64_t>(blockIdx.x) * RPB + it * stride;
             if (r < a.rows) {
                 const int64_t nr = a.rows - r < RPB ? a.rows - r : RPB;
                 bulk_prefetch_l2(in + r * chunks, static_cast<uint32_t>(nr * chunks * 16));
@@ -77,57 +119,47 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
     griddep_wait();  // inputs may come from the kernel launched just before
     griddep_launch_dependents();
 
-    // This thread always owns chunks t, t+TPR, ...: load its gamma / beta once.
-    float g[CPT][8], bb[CPT][8];
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-        const int c = t + i * TPR;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            g[i][e] = 1.0f;
-            bb[i][e] = 0.0f;
-        }
-        if (c < chunks) {
-            if (a.gamma) unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma) + c), g[i]);
-            if (KIND == 0 && a.beta) unpack8(__ldg(reinterpret_cast<const uint4*>(a.beta) + c), bb[i]);
-        }
-    }
-
-    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * RPB; r0 < a.rows;
-         r0 += static_cast<int64_t>(gridDim.x) * RPB) {
+    int64_t r0 = static_cast<int64_t>(blockIdx.x) * RPB;
+    // The plain forward keeps its chunks packed (the row block being reduced
+    // in `cur`, the next one loading into `q`) and widens values where they
+    // are used; the residual forward keeps the fp32 sum in v.
+    uint4 q[CPT], qr[RES ? CPT : 1], cur[CPT];
+    load_row_chunks<TPR, CPT, true>(in, r0 + rg, r0 + rg < a.rows, t, chunks, q);
+    if constexpr (RES) load_row_chunks<TPR, CPT, false>(res, r0 + rg, r0 + rg < a.rows, t, chunks, qr);
+    for (; r0 < a.rows; r0 += stride) {
         const int64_t row = r0 + rg;
         const bool live = row < a.rows;
-        float v[CPT][8];
+        float v[RES ? CPT : 1][8];
 #pragma unroll
-        for (int i = 0; i < CPT; ++i) {
-            const int c = t + i * TPR;
-            if (live && c < chunks) {
-                unpack8(__ldcs(in + row * chunks + c), v[i]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[i][e] = 0.0f;
-            }
-        }
-        if (a.res != nullptr) {
+        for (int i = 0; i < CPT; ++i) cur[i] = q[i];
+        if constexpr (RES) {
             // Residual add before the norm; the sum (rounded to bf16) is the
-            // updated residual stream.  The row's chunks of res are read before
-            // this thread writes the same chunks of h_out, so h_out may be res.
-            const uint4* res = reinterpret_cast<const uint4*>(a.res);
-            uint4* hout = reinterpret_cast<uint4*>(a.h_out);
+            // updated residual stream.  The row's chunks of res were read
+            // before this thread writes the same chunks of h_out, so h_out
+            // may be res.
 #pragma unroll
             for (int i = 0; i < CPT; ++i) {
                 const int c = t + i * TPR;
-                if (live && c < chunks) {
-                    float r[8];
-                    unpack8(__ldcg(res + row * chunks + c), r);
+                unpack8(cur[i], v[i]);
+                float r[8];
+                unpack8(qr[i], r);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[i][e] += r[e];
-                    if (hout != nullptr)
-                        __stcs(hout + row * chunks + c,
-                               make_uint4(pack_bf16x2(v[i][0], v[i][1]), pack_bf16x2(v[i][2], v[i][3]),
-                                          pack_bf16x2(v[i][4], v[i][5]), pack_bf16x2(v[i][6], v[i][7])));
-                }
+                for (int e = 0; e < 8; ++e) v[i][e] += r[e];
+                if (hout != nullptr && live && c < chunks)
+                    __stcs(hout + row * chunks + c,
+                           make_uint4(pack_bf16x2(v[i][0], v[i][1]), pack_bf16x2(v[i][2], v[i][3]),
+                                      pack_bf16x2(v[i][4], v[i][5]), pack_bf16x2(v[i][6], v[i][7])));
             }
+        }
+        auto val = [&](int i, int e) -> float {
+            if constexpr (RES) return v[i][e];
+            else return chunk_val(cur[i], e);
+        };
+        // The next row block's loads go out before this block's reductions.
+        {
+            const int64_t nrow = row + stride;
+            load_row_chunks<TPR, CPT, true>(in, nrow, nrow < a.rows, t, chunks, q);
+            if constexpr (RES) load_row_chunks<TPR, CPT, false>(res, nrow, nrow < a.rows, t, chunks, qr);
         }
         float mean = 0.0f, rstd;
         if (KIND == 0) {
@@ -135,7 +167,7 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
 #pragma unroll
             for (int i = 0; i < CPT; ++i)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s += v[i][e];
+                for (int e = 0; e < 8; ++e) s += val(i, e);
             mean = group_sum<TPR>(s, red, warp, lane) * a.inv_cols;
             float d2 = 0.0f;
 #pragma unroll
@@ -143,7 +175,7 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
                 const bool in_row = (t + i * TPR) < chunks;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float d = v[i][e] - mean;
+                    const float d = val(i, e) - mean;
                     d2 += in_row ? d * d : 0.0f;
                 }
             }
@@ -153,7 +185,7 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
 #pragma unroll
             for (int i = 0; i < CPT; ++i)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s = fmaf(v[i][e], v[i][e], s);
+                for (int e = 0; e < 8; ++e) s = fmaf(val(i, e), val(i, e), s);
             rstd = rsqrtf(fmaf(group_sum<TPR>(s, red, warp, lane), a.inv_cols, a.eps));
         }
         if (!live) continue;
@@ -161,15 +193,29 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
         for (int i = 0; i < CPT; ++i) {
             const int c = t + i * TPR;
             if (c < chunks) {
+                // gamma / beta through the read-only cache (every row reuses them)
+                float g[8], b[8];
+                if (gam != nullptr) {
+                    unpack8(__ldg(gam + c), g);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) g[e] = 1.0f;
+                }
+                if (KIND == 0 && bet != nullptr) {
+                    unpack8(__ldg(bet + c), b);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) b[e] = 0.0f;
+                }
                 float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = fmaf((v[i][e] - mean) * rstd, g[i][e], bb[i][e]);
-                uint4 q;
-                q.x = pack_bf16x2(y[0], y[1]);
-                q.y = pack_bf16x2(y[2], y[3]);
-                q.z = pack_bf16x2(y[4], y[5]);
-                q.w = pack_bf16x2(y[6], y[7]);
-                __stcs(out + row * chunks + c, q);
+                for (int e = 0; e < 8; ++e) y[e] = fmaf((val(i, e) - mean) * rstd, g[e], b[e]);
+                uint4 o;
+                o.x = pack_bf16x2(y[0], y[1]);
+                o.y = pack_bf16x2(y[2], y[3]);
+                o.z = pack_bf16x2(y[4], y[5]);
+                o.w = pack_bf16x2(y[6], y[7]);
+                __stcs(out + row * chunks + c, o);
             }
         }
         if (t == 0) {
@@ -185,9 +231,10 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_kernel(const NormAr
 //   g = dY * gamma; xhat = (Z - mean) * rstd (LN) or Z * rstd (RMS);
 //   dZ = rstd * (g - mean(g) - xhat * mean(g * xhat)), mean(g) for LN only.
 // Same layout as the forward kernel: TPR threads per row, CPT 16-byte chunks
-// of dY and of Z per thread in registers, each row read and written once.
+// of dY and of Z per thread in registers (the next row block's loaded ahead),
+// each row read and written once.
 template <int TPR, int CPT, int KIND>
-__global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_bwd_kernel(const NormBwdArgs a) {
+__global__ void __launch_bounds__(NORM_THREADS, (NormOcc<CPT, true>::MIN_BLOCKS)) nf_norm_rows_bwd_kernel(const NormBwdArgs a) {
     constexpr int RPB = NORM_THREADS / TPR;
     __shared__ float red[NORM_THREADS / 32];
     const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -197,7 +244,9 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_bwd_kernel(const No
     const int chunks = a.cols >> 3;
     const uint4* dyp = reinterpret_cast<const uint4*>(a.dy);
     const uint4* zp = reinterpret_cast<const uint4*>(a.z);
+    const uint4* gam = reinterpret_cast<const uint4*>(a.gamma);
     uint4* out = reinterpret_cast<uint4*>(a.dz);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * RPB;
     // Warm L2 with the first row block of dY and Z (see the forward kernel).
     if (threadIdx.x == 0) {
         const int64_t r = static_cast<int64_t>(blockIdx.x) * RPB;
@@ -210,36 +259,40 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_bwd_kernel(const No
     griddep_wait();  // inputs may come from the kernel launched just before
     griddep_launch_dependents();
 
-    float g[CPT][8];
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-        const int c = t + i * TPR;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) g[i][e] = 1.0f;
-        if (c < chunks && a.gamma) unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma) + c), g[i]);
-    }
-
-    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * RPB; r0 < a.rows;
-         r0 += static_cast<int64_t>(gridDim.x) * RPB) {
+    int64_t r0 = static_cast<int64_t>(blockIdx.x) * RPB;
+    uint4 qy[CPT], qz[CPT];
+    load_row_chunks<TPR, CPT, true>(dyp, r0 + rg, r0 + rg < a.rows, t, chunks, qy);
+    load_row_chunks<TPR, CPT, true>(zp, r0 + rg, r0 + rg < a.rows, t, chunks, qz);
+    for (; r0 < a.rows; r0 += stride) {
         const int64_t row = r0 + rg;
         const bool live = row < a.rows;
         float gy[CPT][8], xh[CPT][8];
         const float mu = (KIND == 0 && live) ? a.mean[row] : 0.0f;
         const float rs = live ? a.rstd[row] : 0.0f;
+#pragma unroll
+        for (int i = 0; i < CPT; ++i) {
+            unpack8(qy[i], gy[i]);
+            unpack8(qz[i], xh[i]);
+        }
+        {  // the next row block's loads go out before this block's reductions
+            const int64_t nrow = row + stride;
+            load_row_chunks<TPR, CPT, true>(dyp, nrow, nrow < a.rows, t, chunks, qy);
+            load_row_chunks<TPR, CPT, true>(zp, nrow, nrow < a.rows, t, chunks, qz);
+        }
         float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
             const int c = t + i * TPR;
-            if (live && c < chunks) {
-                unpack8(__ldcs(dyp + row * chunks + c), gy[i]);
-                unpack8(__ldcs(zp + row * chunks + c), xh[i]);
+            float g[8];
+            if (gam != nullptr && c < chunks) {
+                unpack8(__ldg(gam + c), g);
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gy[i][e] = xh[i][e] = 0.0f;
+                for (int e = 0; e < 8; ++e) g[e] = 1.0f;
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                gy[i][e] *= g[i][e];                                   // g = dY * gamma
+                gy[i][e] *= g[e];                                      // g = dY * gamma
                 xh[i][e] = (KIND == 0 ? xh[i][e] - mu : xh[i][e]) * rs;  // xhat
                 s1 += gy[i][e];
                 s2 = fmaf(gy[i][e], xh[i][e], s2);
@@ -255,12 +308,12 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_bwd_kernel(const No
                 float y[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) y[e] = rs * (gy[i][e] - mg - xh[i][e] * mgx);
-                uint4 q;
-                q.x = pack_bf16x2(y[0], y[1]);
-                q.y = pack_bf16x2(y[2], y[3]);
-                q.z = pack_bf16x2(y[4], y[5]);
-                q.w = pack_bf16x2(y[6], y[7]);
-                __stcs(out + row * chunks + c, q);
+                uint4 o;
+                o.x = pack_bf16x2(y[0], y[1]);
+                o.y = pack_bf16x2(y[2], y[3]);
+                o.z = pack_bf16x2(y[4], y[5]);
+                o.w = pack_bf16x2(y[6], y[7]);
+                __stcs(out + row * chunks + c, o);
             }
         }
     }
@@ -268,17 +321,18 @@ __global__ void __launch_bounds__(NORM_THREADS) nf_norm_rows_bwd_kernel(const No
 
 template <int TPR, int CPT, int KIND>
 cudaError_t launch_one(const NormArgs& a, int sm_count, bool overlap, cudaStream_t stream) {
-    auto kern = nf_norm_rows_kernel<TPR, CPT, KIND>;
+    auto kern = a.res != nullptr ? nf_norm_rows_kernel<TPR, CPT, KIND, true> : nf_norm_rows_kernel<TPR, CPT, KIND, false>;
     constexpr int RPB = NORM_THREADS / TPR;
-    static int per_sm = 0;  // occupancy of this variant, queried once
-    if (per_sm == 0) {
+    static int per_sm[2] = {0, 0};  // occupancy of this variant (without, with residual), queried once
+    int& occ = per_sm[a.res != nullptr ? 1 : 0];
+    if (occ == 0) {
         int n = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NORM_THREADS, 0);
         if (e != cudaSuccess) return e;
-        per_sm = n < 1 ? 1 : n;
+        occ = n < 1 ? 1 : n;
     }
     const int64_t steps = (a.rows + RPB - 1) / RPB;
-    const int64_t cap = static_cast<int64_t>(sm_count) * per_sm;
+    const int64_t cap = static_cast<int64_t>(sm_count) * occ;
     const int grid = static_cast<int>(steps < cap ? steps : cap);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
