@@ -383,6 +383,17 @@ nf_status nf_set_postnorm_tile_n(int tile_n);
  * forced.  Applies to later calls. */
 nf_status nf_set_gemm_tile_n(int tile_n);
 
+/* CTA pairs for plain and Lazy Pre-Norm GEMMs: two CTAs of a cluster along M
+ * compute one 256 x 256 output tile with tcgen05 cta_group::2 MMAs, each
+ * loading its own 128 rows of X and half of W's 256 columns; post-norm rows
+ * exchanged through L2 take them too.  mode 0 (default): plain GEMMs of
+ * tensor-bound 256-column tiles (except those with so few tiles that each is
+ * split over the contraction) and post-norm GEMMs with the L2 exchange and
+ * K >= 2048; pre-norm GEMMs keep one CTA per tile (measured no faster in
+ * pairs); 1: never; 2: whenever the tile has 256 columns and M > 128.
+ * Applies to later calls. */
+nf_status nf_set_gemm_pair(int mode);
+
 /* How post-norm rows wider than 256 columns exchange partial statistics:
  * 0 (default) automatic -- one 512-column CTA per row while N <= 512, else
  * NF_XCH_GLOBAL when K >= 512, else NF_XCH_CLUSTER; NF_XCH_CLUSTER: a

@@ -84,6 +84,7 @@ _SIGS = {
     "nf_set_launch_overlap": [ctypes.c_int],
     "nf_set_postnorm_tile_n": [ctypes.c_int],
     "nf_set_gemm_tile_n": [ctypes.c_int],
+    "nf_set_gemm_pair": [ctypes.c_int],
     "nf_set_postnorm_exchange": [ctypes.c_int],
     "nf_set_gemm_splitk": [ctypes.c_int],
     "nf_reserve_scratch": [_I64, _I64, _VP],
@@ -468,6 +469,11 @@ def set_postnorm_tile_n(tile_n: int) -> None:
 def set_gemm_tile_n(tile_n: int) -> None:
     """Column tile of plain and pre-norm GEMMs: 0 automatic, 64, 128 or 256 forced."""
     _check(lib().nf_set_gemm_tile_n(int(tile_n)), "nf_set_gemm_tile_n")
+
+
+def set_gemm_pair(mode: int) -> None:
+    """CTA pairs (cta_group::2) for plain / pre-norm GEMMs: 0 automatic, 1 never, 2 whenever possible."""
+    _check(lib().nf_set_gemm_pair(int(mode)), "nf_set_gemm_pair")
 
 
 def set_gemm_splitk(mode: int) -> None:

@@ -64,10 +64,16 @@ bool g_overlap = true;
 int g_post_tile = 0;
 // Column tile of plain and pre-norm GEMMs: 0 = automatic, 64, 128 or 256 forced.
 int g_gemm_tile = 0;
+// CTA pairs (cta_group::2) for plain and pre-norm GEMMs: 0 = automatic
+// (tensor-bound shapes of 256-column tiles), 1 = never, 2 = whenever the
+// tile allows.
+int g_pair_mode = 0;
 // Post-norm rows wider than 256 columns: 0 = automatic, else an Exchange mode.
 int g_post_xch = 0;
 // A cooperative launch accepted the programmatic-serialization attribute.
 bool g_coop_overlap_ok = true;
+// A cooperative launch of clusters (CTA pairs with the L2 exchange) was accepted.
+bool g_coop_cluster_ok = true;
 // Split-K of plain GEMMs: 0 = automatic, 1 = never.
 int g_splitk_mode = 0;
 std::mutex g_mu;
@@ -200,6 +206,7 @@ nf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 enum Op { OP_PLAIN = 0, OP_PRE = 1, OP_POST_LN = 2, OP_POST_RMS = 3, OP_BWD_LN = 4, OP_BWD_RMS = 5 };
 
 struct Plan {
+    bool pair = false;  // CTA pair along M (cta_group::2), cluster of 2
     int splitk = 1;  // contraction slices of the split tiles (plain GEMM)
     int sk_base = 0, sk_tiles = 0;  // split-K: first split tile, split tiles
     int tile_n = 0;
@@ -213,7 +220,7 @@ struct Plan {
 const GemmVariant* find_variant(int op, int tile_n, int xch, int ops = 0) {
     int n = 0;
     const GemmVariant* t = nullptr;
-    if (ops != 0) {
+    if (ops != 0 && ops != OPS_PAIR) {
         if (op == OP_PLAIN) t = gemm_variants_trans_plain(&n);
         else if (op == OP_BWD_RMS) t = gemm_variants_trans_bwd(&n);
         else if (op == OP_POST_LN && ops == OPS_RESID) t = gemm_variants_res_ln(&n);
@@ -305,6 +312,28 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
     p->cluster = p->clustered ? static_cast<int>((N + p->tile_n - 1) / p->tile_n) : 1;
     p->m_tiles = static_cast<int>((M + TILE_M - 1) / TILE_M);
     p->n_tiles = ((post || bwd) && p->xch != XCH_GLOBAL) ? 1 : static_cast<int>((N + p->tile_n - 1) / p->tile_n);
+    // CTA pair: two CTAs along M share each 256 x 256 tile's B (cta_group::2
+    // MMAs), halving each CTA's B traffic and stage size, for tensor-bound
+    // plain and pre-norm GEMMs of 256-column tiles -- unless a plain GEMM has
+    // so few tiles that every one is split over the contraction (below).
+    // Post-norm rows exchanged through L2 take pairs too (the exchange is
+    // per 128-row tile, whichever CTA computes it).
+    const int64_t tiles_all = static_cast<int64_t>(p->m_tiles) * p->n_tiles;
+    const bool pair_op = ((op == OP_PLAIN || op == OP_PRE) && ops == 0) ||
+                         (post && p->xch == XCH_GLOBAL && ops == 0);
+    // (Automatic plans leave pre-norm GEMMs on single CTAs: measured, the
+    // pre-norm pair's per-stage signal to the peer's sum-of-squares warps
+    // makes it no faster.  Post-norm tiles of a shorter contraction are bound
+    // by their epilogue, which a pair's two CTAs both wait for: K >= 2048.)
+    p->pair = pair_op && p->tile_n == 256 && p->m_tiles >= 2 &&
+              (g_pair_mode == 2 ||
+               (g_pair_mode == 0 && op != OP_PRE && !tile_memory_bound(K, p->tile_n, p->n_tiles) &&
+                (!post || K >= 2048) &&
+                !(op == OP_PLAIN && g_splitk_mode != 1 && 2 * tiles_all <= sms && (K + TILE_K - 1) / TILE_K >= 16)));
+    if (p->pair) {
+        ops = OPS_PAIR;
+        p->cluster = 2;
+    }
     p->v = find_variant(op, p->tile_n, p->xch, ops);
     if (!p->v) return fail(NF_ERR_UNSUPPORTED_SHAPE, "no kernel variant for this shape");
     p->k_tiles = static_cast<int>((K + p->v->tile_k - 1) / p->v->tile_k);
@@ -318,7 +347,7 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
     //     tiles cut that wave into 64-row halves instead, split_last_wave.)
     p->splitk = 1;
     p->sk_base = p->sk_tiles = 0;
-    if (op == OP_PLAIN && g_splitk_mode != 1) {
+    if (op == OP_PLAIN && g_splitk_mode != 1 && !p->pair) {
         const int tiles = p->m_tiles * p->n_tiles;
         const int kmax = p->k_tiles / 8;
         if (2 * tiles <= sms) {
@@ -667,7 +696,34 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     int grid = 0;
     a.units = p.m_tiles * p.n_tiles;
     a.split_base = a.units;
-    if (p.clustered) {
+    if (p.pair) {
+        // Pair tiles of 256 rows, one cluster of two CTAs each, persistent.
+        // With the L2 exchange every cluster is resident at once (cooperative
+        // launch); 2 x clusters >= n_tiles keeps the exchange deadlock free
+        // (the argument of the kernel, per pair tile).
+        int mc = 0;
+        if ((st = max_clusters(d, p.v, 2, &mc)) != NF_OK) return st;
+        a.units = ((p.m_tiles + 1) / 2) * p.n_tiles;
+        a.split_base = a.units;
+        const int clusters = a.units < mc ? a.units : mc;
+        grid = clusters * 2;
+        if (p.xch == XCH_GLOBAL) {
+            if (2 * clusters < p.n_tiles) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too few resident CTA pairs for the exchange");
+            if (fixed_scratch) {
+                if (xch_bank_ints(p.m_tiles) > kNoAllocBankInts ||
+                    xch_stats_bytes(p.m_tiles, p.n_tiles) > kNoAllocStatsBytes)
+                    return fail(NF_ERR_UNSUPPORTED_SHAPE,
+                                "no-alloc post-norm: ceil(M/128) * ceil(N/256) must be <= 4096 (so M <= 2^19)");
+                uint8_t* base = nullptr;
+                if ((st = noalloc_scratch(stream, &base)) != NF_OK) return st;
+                a.xcnt = reinterpret_cast<int*>(base);
+                a.xbank = static_cast<int32_t>(kNoAllocBankInts);
+                a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
+            } else if ((st = xch_scratch(stream, p.m_tiles, p.n_tiles, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
+                return st;
+            }
+        }
+    } else if (p.clustered) {
         int mc = 0;
         if ((st = max_clusters(d, p.v, p.cluster, &mc)) != NF_OK) return st;
         grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;
@@ -708,39 +764,56 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[3];
-    int nattr = 0;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(p.v->threads));
     cfg.dynamicSmemBytes = static_cast<size_t>(p.v->smem_bytes);
     cfg.stream = stream;
-    if (p.clustered) {
-        attr[nattr].id = cudaLaunchAttributeClusterDimension;
-        attr[nattr].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[nattr].val.clusterDim.y = 1;
-        attr[nattr].val.clusterDim.z = 1;
-        ++nattr;
-    }
-    if (p.xch == XCH_GLOBAL) {
-        attr[nattr].id = cudaLaunchAttributeCooperative;
-        attr[nattr].val.cooperative = 1;
-        ++nattr;
-    }
-    const bool overlap = g_overlap && (p.xch != XCH_GLOBAL || g_coop_overlap_ok);
-    if (overlap) {
-        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
-        ++nattr;
-    }
-    cfg.attrs = nattr ? attr : nullptr;
-    cfg.numAttrs = static_cast<unsigned>(nattr);
+    // Attributes: cluster (row cluster or CTA pair), cooperative (the L2
+    // exchange needs every CTA resident), programmatic dependent launch.
+    auto set_attrs = [&](bool coop, bool overlap) {
+        int nattr = 0;
+        if (p.clustered || p.pair) {
+            attr[nattr].id = cudaLaunchAttributeClusterDimension;
+            attr[nattr].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+            attr[nattr].val.clusterDim.y = 1;
+            attr[nattr].val.clusterDim.z = 1;
+            ++nattr;
+        }
+        if (coop) {
+            attr[nattr].id = cudaLaunchAttributeCooperative;
+            attr[nattr].val.cooperative = 1;
+            ++nattr;
+        }
+        if (overlap) {
+            attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+            ++nattr;
+        }
+        cfg.attrs = nattr ? attr : nullptr;
+        cfg.numAttrs = static_cast<unsigned>(nattr);
+    };
+    bool coop = p.xch == XCH_GLOBAL && (!p.pair || g_coop_cluster_ok);
+    bool overlap = g_overlap && (p.xch != XCH_GLOBAL || g_coop_overlap_ok);
+    set_attrs(coop, overlap);
     void* kargs[4] = {&tmX, &tmW, &tmY, &a};
     cudaError_t e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
+    if (e != cudaSuccess && coop && p.pair) {
+        // The runtime refused a cooperative launch of clusters: CTA pairs then
+        // rely on the grid fitting the device at once (it is sized from the
+        // resident cluster count), without the guarantee.
+        (void)cudaGetLastError();
+        g_coop_cluster_ok = false;
+        coop = false;
+        set_attrs(coop, overlap);
+        e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
+    }
     if (e != cudaSuccess && overlap && p.xch == XCH_GLOBAL) {
         // The runtime refused programmatic serialization on a cooperative
         // launch: drop it for these launches from now on.
         (void)cudaGetLastError();
         g_coop_overlap_ok = false;
-        cfg.numAttrs = static_cast<unsigned>(nattr - 1);
+        overlap = false;
+        set_attrs(coop, overlap);
         e = cudaLaunchKernelExC(&cfg, p.v->func, kargs);
     }
     if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
@@ -1058,6 +1131,13 @@ nf_status nf_set_gemm_tile_n(int tile_n) {
     return NF_OK;
 }
 
+nf_status nf_set_gemm_pair(int mode) {
+    if (mode != 0 && mode != 1 && mode != 2)
+        return fail(NF_ERR_INVALID_ARG, "pair mode: 0 automatic, 1 never, 2 whenever the tile allows");
+    g_pair_mode = mode;
+    return NF_OK;
+}
+
 nf_status nf_set_postnorm_exchange(int mode) {
     if (mode != 0 && mode != NF_XCH_CLUSTER && mode != NF_XCH_GLOBAL)
         return fail(NF_ERR_INVALID_ARG, "mode must be 0 (automatic), 1 (cluster) or 2 (global)");
@@ -1143,7 +1223,10 @@ nf_status nf_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int sm_count, nf
     out->exchange = p.xch;
     out->splitk = p.splitk;
     out->split_tiles = p.splitk > 1 ? p.sk_tiles : 0;
-    if (p.clustered) {
+    if (p.pair) {
+        const int units = ((p.m_tiles + 1) / 2) * p.n_tiles, mc = sm_count / 2;
+        out->grid = (units < mc ? units : mc) * 2;
+    } else if (p.clustered) {
         const int mc = sm_count / p.cluster;
         out->grid = (p.m_tiles < mc ? p.m_tiles : mc) * p.cluster;
     } else if (p.splitk > 1) {

@@ -34,6 +34,11 @@
 //   B stage  TILE_N/64 boxes of 64 K-rows x 64 N (MN-major, W is row-major
 //            K x N), box i at i*8 KB, K-row k of a box at k*128 bytes.
 //
+// Waits on barriers that a remote event may complete (a CTA pair's full[s],
+// whose bytes come from both CTAs; the first CTA's commits arriving in the
+// second CTA) poll without the suspend-time hint; the first CTA waits for the
+// peer's once-per-tile relay with test_wait (mbar_wait_remote).
+//
 // Pipeline barriers: full[s] (TMA bytes landed), empty[s] (MMA done with the
 // stage; pre-norm: also all 128 sum-of-squares threads), acc_full[b] (MMA
 // chain of a tile complete), acc_empty[b] (epilogue drained TMEM buffer b),
@@ -41,6 +46,23 @@
 // statistics of the cluster arrived).  Every wait is bounded in time; on
 // expiry the kernel records NF_ERR_TIMEOUT, drains what it issued, frees TMEM
 // and returns.
+//
+// CTA pair (OPS_PAIR, plain and pre-norm GEMMs of 256-column tiles): a
+// cluster of two CTAs along M computes a 256 x 256 tile with tcgen05
+// cta_group::2 MMAs.  Each CTA's producer loads its own 128 rows of A and half
+// of B's 256 columns into its own ring stage (32 KB instead of 48, so six
+// stages fit), counted on the first CTA's full barrier; the first CTA's MMA
+// thread issues the MMAs, which read both CTAs' stages and write each CTA's
+// 128 rows into that CTA's TMEM, and its commits arrive on the barriers of
+// both CTAs.  The second CTA's MMA warp relays its epilogue's "accumulator
+// drained" to the first CTA.  Pre-norm: a sum-of-squares thread of the first
+// CTA, once full[s] shows both CTAs' bytes landed, tells the second CTA's
+// sum-of-squares warps (ardy[s]) with a relaxed remote arrive.  (Measured: the
+// pre-norm pair runs no faster than one CTA per tile -- see the plan, which
+// keeps pre-norm GEMMs on single CTAs -- while a release arrive per stage,
+// or a first CTA summing its peer's rows through distributed shared memory,
+// was three times slower.)  Each
+// CTA's epilogue is unchanged.
 //
 // Post-norm rows wider than one tile exchange partial row statistics between
 // the CTAs that hold the row (XCH):
@@ -271,6 +293,8 @@ struct TileSched {
     int splitk;              // contraction slices of the split tiles
     int k_tiles;
     bool clustered;
+    bool pair;               // CTA pair: unit u is pair tile (u / n_tiles, u % n_tiles), this CTA's rows
+    int pair_rank;           // 0 or 1: the pair tile's first or second 128 rows
     // K-tiles of unit lt and its slice (-1 for a whole tile).
     __device__ __forceinline__ void krange(int lt, int& kt0, int& kt1, int& slice) const {
         const int u = first + lt * step;
@@ -287,6 +311,14 @@ struct TileSched {
     __device__ __forceinline__ void tile(int lt, int& m, int& n, int& row0, int& rows) const {
         int u = first + lt * step;
         if (splitk > 1 && u >= sk_base) u = sk_base + (u - sk_base) % sk_tiles;
+        if (pair) {
+            const int mp = u / n_tiles;
+            n = u - mp * n_tiles;
+            m = 2 * mp + pair_rank;
+            row0 = m * TILE_M;
+            rows = TILE_M;
+            return;
+        }
         if (clustered) {
             m = u;
             n = n_fixed;
@@ -313,6 +345,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     using Cfg = GemmCfg<EPI, TILE_N, XCH, OPS>;
     constexpr bool CLUSTERED = XCH == XCH_CLUSTER;
     constexpr bool GLOBALX = XCH == XCH_GLOBAL;
+    constexpr bool PAIR = Cfg::kPair;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int NBOX = TILE_N / B_BOX_N;
 
@@ -344,6 +377,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     const uint32_t bar_xch0 = bar_ssf0 + 8u * NACC;          // [NACC]
     const uint32_t bar_mma_done = bar_xch0 + 8u * NACC;
     const uint32_t bar_xf0 = sBar + 256u;        // [8] A row scaling: stage s transformed
+    const uint32_t bar_pacc0 = bar_xch0;         // [NACC] CTA pair (first CTA): the peer's epilogue drained buffer b
+    const uint32_t bar_ardy0 = sBar + 256u;      // [8] pre-norm CTA pair (second CTA): its A stage s has landed
+
     const uint32_t bar_afff0 = bar_mma_done + 8u;  // [2] global exchange: a group's affine slot filled
     const uint32_t bar_affe0 = bar_afff0 + 16u;    // [2] global exchange: a group's affine slot free
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS);
@@ -363,7 +399,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     sched.clustered = CLUSTERED;
     sched.n_tiles = args.n_tiles;
     int my_rank = 0;
-    if (CLUSTERED) {
+    sched.pair = PAIR;
+    sched.pair_rank = 0;
+    if (PAIR) {
+        my_rank = static_cast<int>(cluster_ctarank());
+        const int cid = static_cast<int>(cluster_id_x());
+        const int ncl = static_cast<int>(num_clusters_x());
+        const int total = args.units;  // pair tiles
+        sched.first = cid;
+        sched.step = ncl;
+        sched.count = cid < total ? (total - cid + ncl - 1) / ncl : 0;
+        sched.n_fixed = 0;
+        sched.split_base = total;
+        sched.pair_rank = my_rank & 1;
+    } else if (CLUSTERED) {
         my_rank = static_cast<int>(cluster_ctarank());
         const int cid = static_cast<int>(cluster_id_x());
         const int ncl = static_cast<int>(num_clusters_x());
@@ -387,6 +436,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     sched.k_tiles = args.k_tiles;
     const int count = sched.count;
     const int k_tiles = args.k_tiles;
+    const bool lead = !PAIR || (my_rank & 1) == 0;  // CTA pair: the first CTA issues the MMAs
     const uint32_t xch_bytes = static_cast<uint32_t>(args.cluster) * TILE_M * 8u;
 
     // ---- set-up: barriers, TMEM, affine parameters
@@ -398,15 +448,18 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         prefetch_tmap(&tmY);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full0 + 8u * s, 1);
-            mbar_init(bar_empty0 + 8u * s, 1 + (Cfg::kPre ? 128 : 0));
+            mbar_init(bar_empty0 + 8u * s, 1 + (Cfg::kPre ? 128 : 0));  // (pre-norm: and the sum-of-squares threads)
         }
         for (int b = 0; b < NACC; ++b) {
             mbar_init(bar_accf0 + 8u * b, 1);
             mbar_init(bar_acce0 + 8u * b, 128);
             mbar_init(bar_ssf0 + 8u * b, 128);
-            mbar_init(bar_xch0 + 8u * b, 1);
+            mbar_init(bar_xch0 + 8u * b, 1);  // (CTA pair: bar_pacc, one relayed arrival)
         }
+
         mbar_init(bar_mma_done, 1);
+        if (PAIR && Cfg::kPre)
+            for (int st = 0; st < STAGES; ++st) mbar_init(bar_ardy0 + 8u * st, 1);
         if (Cfg::kScaleA)
             for (int st = 0; st < STAGES; ++st) mbar_init(bar_xf0 + 8u * st, 128);  // the transform threads
         for (int g = 0; g < 2; ++g) {
@@ -422,8 +475,13 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         }
     }
     if (warp == Cfg::PRODUCER_WARP) {
-        tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {  // the same columns in both CTAs of the pair
+            tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     // Warm L2 with this CTA's first ring-full of X K-tiles while a preceding
     // grid may still be running.  A prefetch only fills L2 lines, and L2 is
@@ -479,7 +537,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (CLUSTERED) {
+    if (CLUSTERED || PAIR) {  // barriers of every CTA initialised before any remote use
         cluster_arrive_release();
         cluster_wait_acquire();
     }
@@ -507,9 +565,32 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 for (int kt = kt0; kt < kt1; ++kt) {
                     // (a slot's first fill never waits: the ring starts empty)
                     if (issued >= static_cast<uint32_t>(STAGES) &&
-                        !mbar_wait(guard, bar_empty0 + 8u * s, ph ^ 1u, SITE_PROD_EMPTY, lt)) {
+                        !mbar_wait<PAIR>(guard, bar_empty0 + 8u * s, ph ^ 1u, SITE_PROD_EMPTY, lt)) {
                         ok = false;
                         break;
+                    }
+                    if (PAIR) {
+                        // Both CTAs' bytes are counted on the first CTA's full[s].
+                        const uint32_t fl = bar_full0 + 8u * s;
+                        const uint32_t fb = mapa_shared(fl, static_cast<uint32_t>(my_rank & ~1));
+                        if (lead) mbar_arrive_expect_tx(fl, 2u * Cfg::STAGE_BYTES);
+                        tma_load_2d_pair(sA + s * A_STAGE_BYTES, &tmX, fb, kt * TILE_K, row0);
+#pragma unroll
+                        for (int i = 0; i < NBOX / 2; ++i) {
+                            const int col = n * TILE_N + sched.pair_rank * (TILE_N / 2) + i * B_BOX_N;
+                            if (NF_W_EVICT_LAST)
+                                tma_load_2d_pair_hint(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb, col,
+                                                      kt * TILE_K, wpol);
+                            else
+                                tma_load_2d_pair(sB + s * Cfg::B_STAGE_BYTES + i * B_BOX_BYTES, &tmW, fb, col,
+                                                 kt * TILE_K);
+                        }
+                        ++issued;
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
                     }
                     const uint32_t fb = bar_full0 + 8u * s;
                     if (Cfg::kScaleA) {
@@ -555,8 +636,11 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                     }
                 }
             }
-            // Drain: every load issued has landed before the CTA may exit.
-            for (int j = 0; j < STAGES; ++j) {
+            // Drain: every load issued has landed before the CTA may exit.  (A
+            // pair's loads are all counted on the first CTA's barriers, which
+            // its producer drains; the pair meets at a cluster barrier before
+            // either CTA exits.)
+            for (int j = 0; j < STAGES && lead; ++j) {
                 const uint32_t uj = static_cast<uint32_t>(j);
                 if (issued > uj) {
                     const uint32_t fills = (issued - 1u - uj) / STAGES + 1u;
@@ -567,8 +651,17 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         __syncwarp();
     } else if (warp == Cfg::MMA_WARP) {
         // ================================================================ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, TILE_N, !Cfg::kBK, Cfg::kAMN);
+        if (lane == 0 && PAIR && !lead) {
+            // CTA pair, second CTA: relay "this CTA's epilogue drained
+            // accumulator b" to the first CTA, whose MMA writes this CTA's TMEM.
+            for (int lt = NACC; lt < count; ++lt) {
+                const int b = lt % NACC;
+                const uint32_t aph = static_cast<uint32_t>(lt / NACC) & 1u;
+                if (!mbar_wait(guard, bar_acce0 + 8u * b, aph ^ 1u, SITE_MMA_ACC_EMPTY, lt)) break;
+                mbar_arrive_remote(mapa_shared(bar_pacc0 + 8u * b, static_cast<uint32_t>(my_rank & ~1)));
+            }
+        } else if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * TILE_M : TILE_M, TILE_N, !Cfg::kBK, Cfg::kAMN);
             // A transformed in shared memory is consumed after the transform
             // warps released the stage, not when its bytes landed.
             const uint32_t bar_ready0 = Cfg::kScaleA ? bar_xf0 : bar_full0;
@@ -579,12 +672,15 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 const int b = lt % NACC;
                 const uint32_t aph = static_cast<uint32_t>(lt / NACC) & 1u;
                 if (!mbar_wait(guard, bar_acce0 + 8u * b, aph ^ 1u, SITE_MMA_ACC_EMPTY, lt)) break;
+                if (PAIR && !mbar_wait_remote(guard, bar_pacc0 + 8u * b, aph ^ 1u, SITE_MMA_ACC_EMPTY, lt)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(b * TILE_N);
                 int kt0, kt1, slice;
                 sched.krange(lt, kt0, kt1, slice);
                 for (int kt = kt0; kt < kt1; ++kt) {
-                    if (!mbar_wait(guard, bar_ready0 + 8u * s, ph, SITE_MMA_FULL, lt)) {
+                    // (a pair's full[s] also completes by the peer's bytes or
+                    // arrival: polled without the suspend hint)
+                    if (!mbar_wait<PAIR>(guard, bar_ready0 + 8u * s, ph, SITE_MMA_FULL, lt)) {
                         ok = false;
                         break;
                     }
@@ -599,24 +695,38 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                         //    1 KB apart, 64-column boxes 8 KB apart.
                         // (Transposed operands: MN-major A advances 2 KB per 16
                         //  K-rows with its two 64-row boxes 8 KB apart; K-major B
-                        //  advances 32 bytes like A.)
+                        //  advances 32 bytes like A.  CTA pair: the same
+                        //  descriptors address both CTAs' stages.)
                         const uint64_t adesc = Cfg::kAMN ? smem_desc_sw128(a0 + j * 2048, B_BOX_BYTES, 1024)
                                                          : smem_desc_sw128(a0 + j * 32, 16, 1024);
                         const uint64_t bdesc = Cfg::kBK ? smem_desc_sw128(b0 + j * 32, 16, 1024)
                                                         : smem_desc_sw128(b0 + j * 2048, B_BOX_BYTES, 1024);
-                        mma_bf16(d, adesc, bdesc, IDESC, (kt != kt0 || j != 0) ? 1u : 0u);
+                        if (PAIR)
+                            mma_bf16_pair(d, adesc, bdesc, IDESC, (kt != kt0 || j != 0) ? 1u : 0u);
+                        else
+                            mma_bf16(d, adesc, bdesc, IDESC, (kt != kt0 || j != 0) ? 1u : 0u);
                     }
-                    mma_commit(bar_empty0 + 8u * s);  // stage free once these MMAs finish
+                    // stage free (in both CTAs of a pair) once these MMAs finish
+                    if (PAIR)
+                        mma_commit_pair(bar_empty0 + 8u * s);
+                    else
+                        mma_commit(bar_empty0 + 8u * s);
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar_accf0 + 8u * b);  // accumulator b complete
+                if (PAIR)  // accumulator b complete in both CTAs
+                    mma_commit_pair(bar_accf0 + 8u * b);
+                else
+                    mma_commit(bar_accf0 + 8u * b);
             }
             // Everything issued has completed before TMEM can be released.
-            mma_commit(bar_mma_done);
+            if (PAIR)
+                mma_commit_pair_local(bar_mma_done);
+            else
+                mma_commit(bar_mma_done);
             mbar_drain(bar_mma_done, 0, args.timeout_ns);
         }
         __syncwarp();
@@ -703,7 +813,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             // accumulator wait (they do not depend on it).
             const float bmu = (Cfg::kBwdLN && own_row) ? args.mean_in[grow] : 0.0f;
             const float brs = (Cfg::kBwd && own_row) ? args.rstd_in[grow] : 0.0f;
-            ok = mbar_wait(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
+            ok = mbar_wait<PAIR>(guard, bar_accf0 + 8u * b, aph, SITE_EPI_ACC_FULL, lt);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t tacc = t_lane + static_cast<uint32_t>(b * TILE_N);
@@ -1112,6 +1222,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         }
     } else if (Cfg::kPre && warp >= Cfg::SUMSQ_WARP0) {
         // ================================================================ row sums of squares
+        // (CTA pair: both CTAs' bytes are counted on the first CTA's full[s];
+        // one of its sum-of-squares threads then tells the peer's, which wait
+        // on their ardy[s], with a relaxed remote arrive -- it reports an event
+        // the sender has observed.)
         const int row = static_cast<int>(threadIdx.x) - Cfg::SUMSQ_WARP0 * 32;  // 0..127
         int s = 0;
         uint32_t ph = 0;
@@ -1121,10 +1235,14 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             float acc0 = 0.0f, acc1 = 0.0f;
             bool ok = true;
             for (int kt = 0; kt < k_tiles; ++kt) {
-                if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)) {
+                const bool got = (!PAIR || lead) ? mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)
+                                                 : mbar_wait<2>(guard, bar_ardy0 + 8u * s, ph, SITE_SS_FULL, lt);
+                if (!got) {
                     ok = false;
                     break;
                 }
+                if (PAIR && lead && row == 0)
+                    mbar_arrive_remote_relaxed(mapa_shared(bar_ardy0 + 8u * s, static_cast<uint32_t>(my_rank | 1)));
                 // The row's 128 bytes are contiguous whatever the swizzle (it
                 // only permutes 16-byte chunks within the row); start each
                 // thread at a different chunk so the 8 threads of a quarter
@@ -1172,14 +1290,18 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             st_release_gpu(hdr + 2, e + 1);
         }
     }
-    if (CLUSTERED) {
-        // No CTA leaves while a peer may still write into its shared memory.
+    if (CLUSTERED || PAIR) {
+        // No CTA leaves while a peer may still write into its shared memory
+        // (or, in a pair, its TMEM).
         cluster_arrive_release();
         cluster_wait_acquire();
     }
     if (warp == Cfg::PRODUCER_WARP) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
@@ -1190,6 +1312,7 @@ GemmVariant make_variant() {
                        TILE_N,
                        XCH == XCH_CLUSTER,
                        XCH,
+                       Cfg::kPair,
                        OPS,
                        reinterpret_cast<const void*>(&nf_gemm_kernel<EPI, TILE_N, XCH, OPS>),
                        Cfg::THREADS,

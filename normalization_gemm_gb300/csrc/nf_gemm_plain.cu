@@ -7,8 +7,8 @@ namespace nf {
 const GemmVariant* gemm_variants_plain(int* count) {
     static const GemmVariant v[] = {
         make_variant<EPI_PLAIN, 64, XCH_NONE>(), make_variant<EPI_PLAIN, 128, XCH_NONE>(),
-        make_variant<EPI_PLAIN, 256, XCH_NONE>()};
-    *count = 3;
+        make_variant<EPI_PLAIN, 256, XCH_NONE>(), make_variant<EPI_PLAIN, 256, XCH_NONE, OPS_PAIR>()};
+    *count = 4;
     return v;
 }
 

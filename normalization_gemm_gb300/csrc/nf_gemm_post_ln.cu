@@ -9,8 +9,8 @@ const GemmVariant* gemm_variants_post_ln(int* count) {
         make_variant<EPI_POST_LN, 64, XCH_NONE>(), make_variant<EPI_POST_LN, 128, XCH_NONE>(),
         make_variant<EPI_POST_LN, 256, XCH_NONE>(), make_variant<EPI_POST_LN, 256, XCH_CLUSTER>(),
         make_wide_variant<EPI_POST_LN, false>(), make_wide_variant<EPI_POST_LN, true>(),
-        make_variant<EPI_POST_LN, 256, XCH_GLOBAL>()};
-    *count = 7;
+        make_variant<EPI_POST_LN, 256, XCH_GLOBAL>(), make_variant<EPI_POST_LN, 256, XCH_GLOBAL, OPS_PAIR>()};
+    *count = 8;
     return v;
 }
 

@@ -9,8 +9,8 @@ const GemmVariant* gemm_variants_post_rms(int* count) {
         make_variant<EPI_POST_RMS, 64, XCH_NONE>(), make_variant<EPI_POST_RMS, 128, XCH_NONE>(),
         make_variant<EPI_POST_RMS, 256, XCH_NONE>(), make_variant<EPI_POST_RMS, 256, XCH_CLUSTER>(),
         make_wide_variant<EPI_POST_RMS, false>(), make_wide_variant<EPI_POST_RMS, true>(),
-        make_variant<EPI_POST_RMS, 256, XCH_GLOBAL>()};
-    *count = 7;
+        make_variant<EPI_POST_RMS, 256, XCH_GLOBAL>(), make_variant<EPI_POST_RMS, 256, XCH_GLOBAL, OPS_PAIR>()};
+    *count = 8;
     return v;
 }
 

@@ -454,6 +454,7 @@ GemmVariant make_wide_variant() {
                        Cfg::TILE_N,
                        CLUSTERED,
                        CLUSTERED ? XCH_CLUSTER : XCH_NONE,
+                       false,
                        0,
                        reinterpret_cast<const void*>(&nf_gemm_wide_kernel<EPI, CLUSTERED>),
                        Cfg::THREADS,

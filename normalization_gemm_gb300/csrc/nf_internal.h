@@ -66,6 +66,9 @@ enum OperandFlags : int {
                       // memory before the MMA (rmsnorm of the stored matrix rebuilt on the fly)
     OPS_B_K = 4,      // B given as its transpose: W stored N x K row-major (Y = X W^T)
     OPS_RESID = 8,    // post-norm: a residual R (M x N) added to X W before the statistics
+    OPS_PAIR = 16,    // plain / pre-norm / post-norm with the L2 exchange: a cluster of two CTAs along M
+                      // computes a 256-row tile with tcgen05 cta_group::2 MMAs (each CTA loads its 128
+                      // rows of A and half of B)
 };
 
 template <int EPI, int TILE_N, int XCH, int OPS = 0>
@@ -81,12 +84,18 @@ struct GemmCfg {
     static constexpr bool kScaleA = (OPS & OPS_A_SCALE) != 0;
     static constexpr bool kBK = (OPS & OPS_B_K) != 0;
     static constexpr bool kRes = (OPS & OPS_RESID) != 0;
+    static constexpr bool kPair = (OPS & OPS_PAIR) != 0;
+    static_assert(!kPair || (OPS == OPS_PAIR && TILE_N == 256 &&
+                             (((EPI == EPI_PLAIN || EPI == EPI_PRE_RMS) && XCH == XCH_NONE) ||
+                              ((EPI == EPI_POST_LN || EPI == EPI_POST_RMS) && XCH == XCH_GLOBAL))),
+                  "the CTA pair is built for plain and pre-norm GEMMs of 256-column tiles and for "
+                  "post-norm rows exchanged through L2");
     static_assert(!kRes || kPost, "the residual add belongs to the post-norm epilogues");
     static_assert(!kScaleA || (kAMN && EPI == EPI_PLAIN), "row scaling applies to a transposed A, plain epilogue");
     static_assert(TILE_N == 64 || TILE_N == 128 || TILE_N == 256, "tile_n");
     static_assert(XCH == XCH_NONE || (kRow && TILE_N == 256), "row exchange only for post-norm");
 
-    static constexpr int B_STAGE_BYTES = TILE_K * TILE_N * 2;
+    static constexpr int B_STAGE_BYTES = TILE_K * (kPair ? TILE_N / 2 : TILE_N) * 2;  // this CTA's share of B
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     // per-row partial statistics received from every CTA of the cluster,
     // double buffered by tile parity: [2][MAX_CLUSTER][TILE_M] x float2
@@ -106,7 +115,8 @@ struct GemmCfg {
     // A row scaling: each ring stage's 64 rstd values, copied with the stage.
     // (256-column tiles fit four stages at most, narrower ones up to eight.)
     static constexpr int RS_BYTES = kScaleA ? (TILE_N == 256 ? 4 : MAX_STAGES) * TILE_K * 4 : 0;
-    static constexpr int BAR_BYTES = (kScaleA || NACC == 4) ? 320 : 256;  // barriers (+ xformed[8]) + 4 words
+    // barriers (+ xformed[8], or a pre-norm pair's ardy[8]) + 4 words
+    static constexpr int BAR_BYTES = (kScaleA || kPair || NACC == 4) ? 320 : 256;
     // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
     // starts 1 KB aligned in practice; the global-exchange variant, whose
     // fourth pipeline stage needs the room, relies on that (and checks it at
@@ -145,7 +155,8 @@ struct GemmArgs {
     int32_t M, N, K;
     int32_t m_tiles, n_tiles, k_tiles;
     int32_t cluster;        // CTAs per cluster along N (1 = no cluster)
-    int32_t units;          // unclustered: work units (tiles, with the last wave's tiles halved)
+    int32_t units;          // unclustered: work units (tiles, with the last wave's tiles halved);
+                            // CTA pair: 256-row pair tiles (ceil(m_tiles / 2) x n_tiles)
     int32_t split_base;     // unclustered: first half-tile unit (== units when nothing is split)
     float eps;
     float inv_len;          // 1/K (pre-norm) or 1/N (post-norm)
@@ -192,6 +203,7 @@ struct GemmVariant {
     int epi, tile_n;
     bool clustered;  // xch == XCH_CLUSTER
     int xch;
+    bool pair;       // OPS_PAIR: launched in clusters of two CTAs along M
     int ops;         // OperandFlags
     const void* func;
     int threads, smem_bytes, stages, tmem_cols;

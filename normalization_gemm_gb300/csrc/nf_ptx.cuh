@@ -79,6 +79,21 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// CTA-scope test without the suspend hint: for a phase completed by another
+// CTA's relaxed arrival, where the waiter reads only shared memory its own
+// CTA's copies wrote (a cluster-scope acquire per poll and thread costs more).
+__device__ __forceinline__ bool mbar_try_wait_nohint(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Device status word layout: [0] code, [1] wait site, [2] block, [3] tile.
 struct WaitGuard {
     uint32_t* status;           // global status word (4 x u32)
@@ -98,19 +113,59 @@ __device__ __forceinline__ void record_failure(const WaitGuard& g, uint32_t code
 
 // Bounded wait on a phase parity.  Returns false when the CTA is aborting or
 // the time limit passed (which is then recorded).  Never traps.
-template <bool CLUSTER_SCOPE = false>
+// MODE 0 (false): CTA scope with the suspend hint; 1 (true): cluster-scope
+// acquire, no hint; 2: CTA scope, no hint.
+template <int MODE = 0>
+__device__ __forceinline__ bool mbar_try_wait_mode(uint32_t bar, uint32_t parity) {
+    return MODE == 1 ? mbar_try_wait_cluster(bar, parity)
+                     : (MODE == 2 ? mbar_try_wait_nohint(bar, parity) : mbar_try_wait(bar, parity));
+}
+
+template <int MODE = 0>
 __device__ __forceinline__ bool mbar_wait(const WaitGuard& g, uint32_t bar, uint32_t parity,
                                           uint32_t site, uint32_t tile) {
-    if (CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
-        return true;
+    if (mbar_try_wait_mode<MODE>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
-            return true;
+        if (mbar_try_wait_mode<MODE>(bar, parity)) return true;
         if (*g.abort_flag) return false;
         if (globaltimer_ns() - t0 > g.timeout_ns) {
             record_failure(g, 5u /* NF_ERR_TIMEOUT */, site, tile);
             return false;
+        }
+    }
+}
+
+// Non-blocking test of a phase with cluster-scope acquire (never suspends the
+// thread).
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for a phase completed by arrivals that other CTAs' threads
+// send (mbar_arrive_remote): polled with test_wait, which never suspends --
+// measured, a thread suspended in try_wait resumed late after such remote
+// arrivals.
+__device__ __forceinline__ bool mbar_wait_remote(const WaitGuard& g, uint32_t bar, uint32_t parity, uint32_t site,
+                                                 uint32_t tile) {
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait_cluster(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*g.abort_flag) return false;
+            if (globaltimer_ns() - t0 > g.timeout_ns) {
+                record_failure(g, 5u /* NF_ERR_TIMEOUT */, site, tile);
+                return false;
+            }
         }
     }
 }
@@ -288,7 +343,89 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same load for a CTA pair (tcgen05 cta_group::2): the completion is
+// counted on `bar`, which may be in this CTA's shared memory or its peer's
+// (a shared::cluster address); `dst` is this CTA's own shared memory.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                                 int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                      int32_t c0, int32_t c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Arrive once on an mbarrier in another CTA of the cluster (shared::cluster
+// address from mapa_shared), ordered after this thread's earlier accesses at
+// cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// The same without the release: for a signal that only reports an event the
+// sending thread has itself observed complete (bytes a TMA load delivered,
+// seen through an mbarrier phase), where no access of the sender's needs
+// ordering.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
+// Every tcgen05 operation of a kernel uses one CTA group: the cta_group::1
+// forms below, or the cta_group::2 forms of a CTA pair (the *_pair
+// functions), which the warps or threads named in each comment of both CTAs
+// (alloc, relinquish, dealloc) or of the pair's first CTA only (mma, commit)
+// execute.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {  // one warp in each CTA
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {  // one warp in each CTA
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {  // one warp in each CTA
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (+)= A B for the pair's 256-row tile: A's rows 0-127 from the first
+// CTA's shared memory and 128-255 from its peer's (same offsets), B's first
+// and second N halves likewise; D's rows land in each CTA's own TMEM.  Issued
+// by one thread of the pair's first CTA.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the barrier at offset `bar` in both CTAs of the pair when
+// every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+// The same for this CTA's barrier only.
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)

@@ -117,6 +117,8 @@ def test_timeout_setting_range(L):
     (3, 16384, 1024, 512, 256, 1, 2), (2, 16384, 1024, 448, 256, 4, 1),
 ])
 def test_plans(L, op, M, N, K, tile_n, cluster, xch):
+    if xch == 2 and K >= 2048:
+        cluster = 2  # rows exchanged through L2 are computed by CTA pairs (long contractions)
     p = nf.plan_gemm(op, M, N, K, 148)
     assert p["tile_m"] == 128 and p["tile_k"] == (32 if tile_n == 512 else 64)
     assert p["tile_n"] == tile_n and p["cluster"] == cluster and p["exchange"] == xch
@@ -270,7 +272,11 @@ def splitk_slices(k_tiles, splitk):
     (100, 200, 2048, 152, 4),      # one tile, 32 K-tiles: slices of 8
 ])
 def test_splitk_plans(L, M, N, K, sms, splitk):
-    p = nf.plan_gemm(0, M, N, K, sms)
+    nf.set_gemm_pair(1)  # the split-K rules alone (CTA pairs take tensor-bound shapes by default)
+    try:
+        p = nf.plan_gemm(0, M, N, K, sms)
+    finally:
+        nf.set_gemm_pair(0)
     tiles = p["tiles"]
     assert p["splitk"] == splitk
     assert p["grid"] <= sms
@@ -312,3 +318,31 @@ def test_reserve_scratch_argument_checks(L):
     assert L.nf_reserve_scratch(-1, 0, None) == INVALID
     assert L.nf_reserve_scratch(0, -8, None) == INVALID
     assert L.nf_reserve_scratch(1024, 4104, None) == SHAPE
+
+
+@pytest.mark.parametrize("op,M,N,K,pair", [
+    (0, 8192, 4096, 4096, True),    # tensor-bound 256-column tiles
+    (1, 8192, 4096, 4096, False),   # pre-norm GEMMs keep one CTA per tile
+    (0, 4096, 4096, 8192, True),    # pairs instead of splitting the last wave
+    (0, 512, 512, 32768, False),    # 8 tiles: every tile split over the contraction instead
+    (1, 32768, 512, 512, False),    # memory-bound tiles
+    (0, 100, 200, 2048, False),     # a single 128-row tile
+    (0, 4096, 128, 4096, False),    # 128-column tiles
+    (2, 8192, 4096, 4096, True),    # post-norm rows exchanged through L2
+    (3, 16384, 2048, 1024, False),  # ... but not with a short contraction (epilogue-bound tiles)
+    (2, 16384, 2048, 256, False),   # post-norm rows in a DSMEM cluster (K < 512)
+    (2, 65536, 128, 128, False),    # one CTA holds whole rows
+])
+def test_pair_plans(L, op, M, N, K, pair):
+    p = nf.plan_gemm(op, M, N, K, 148)
+    assert (p["cluster"] == 2 and p["exchange"] in (0, 2)) == pair
+    if pair:
+        assert p["tile_n"] == 256 and p["splitk"] == 1 and p["grid"] % 2 == 0
+        pair_tiles = -(-M // 256) * -(-N // 256)
+        assert p["grid"] == 2 * min(pair_tiles, 148 // 2)
+    nf.set_gemm_pair(1)
+    try:
+        assert nf.plan_gemm(op, M, N, K, 148)["cluster"] != 2 or nf.plan_gemm(op, M, N, K, 148)["exchange"] == 1
+    finally:
+        nf.set_gemm_pair(0)
+    assert L.nf_set_gemm_pair(3) == INVALID

@@ -242,6 +242,15 @@ def test_plain_tail_splitk(dev, orc, flags):
     import torch
     M, K, N = 3840, 1024, 4096
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nf.set_gemm_pair(1)  # the plain GEMM would take CTA pairs instead of the split (transposed forms never do)
+    try:
+        _tail_splitk(orc, dev, flags, M, K, N, sms)
+    finally:
+        nf.set_gemm_pair(0)
+
+
+def _tail_splitk(orc, dev, flags, M, K, N, sms):
+    import torch
     p = nf.plan_gemm(0, M, N, K, sms)
     tiles = p["tiles"]
     if tiles % sms == 0 or 2 * (tiles % sms) > sms:
