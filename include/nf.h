@@ -352,8 +352,12 @@ nf_status nf_norm_rows_bwd(const void* dY, const void* Z, const void* gamma,
 
 /* Synchronizes the current device, then returns the status recorded by the
  * kernels since the last clear: NF_OK, or NF_ERR_TIMEOUT when a pipeline wait
- * gave up.  `detail` (may be NULL) receives 4 words: code, wait site, block
- * index, tile index of the first failure. */
+ * gave up (NF_ERR_ALIGNMENT: dynamic shared memory not 1 KB aligned;
+ * NF_ERR_INVALID_ARG: a GEMM kernel found itself in a cluster of a size other
+ * than the one its plan launches it with, as when a tool re-issues the launch
+ * without its attributes, and returned before any work).  `detail` (may be
+ * NULL) receives 4 words: code, wait site, block index, tile index of the
+ * first failure. */
 nf_status nf_get_device_status(uint32_t* detail);
 
 /* Synchronizes the current device, resets its status word to NF_OK and

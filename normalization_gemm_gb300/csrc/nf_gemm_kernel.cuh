@@ -295,6 +295,7 @@ struct TileSched {
     bool clustered;
     bool pair;               // CTA pair: unit u is pair tile (u / n_tiles, u % n_tiles), this CTA's rows
     int pair_rank;           // 0 or 1: the pair tile's first or second 128 rows
+    bool kflip;              // odd local units walk the contraction backwards
     // K-tiles of unit lt and its slice (-1 for a whole tile).
     __device__ __forceinline__ void krange(int lt, int& kt0, int& kt1, int& slice) const {
         const int u = first + lt * step;
@@ -307,6 +308,14 @@ struct TileSched {
         slice = (u - sk_base) / sk_tiles;
         kt0 = static_cast<int>(static_cast<int64_t>(slice) * k_tiles / splitk);
         kt1 = static_cast<int>(static_cast<int64_t>(slice + 1) * k_tiles / splitk);
+    }
+    // Contraction step i of unit lt.  With kflip, every odd local unit walks
+    // its K-tiles from the last down: a CTA's consecutive units are one wave
+    // apart, so the next wave starts on the operand panels the previous one
+    // read last, which L2 still holds.  (All CTAs of a wave walk the same way,
+    // so CTAs sharing a panel still request it in step.)
+    __device__ __forceinline__ int kstep(int lt, int kt0, int kt1, int i) const {
+        return (kflip && (lt & 1)) ? kt1 - 1 - i : kt0 + i;
     }
     __device__ __forceinline__ void tile(int lt, int& m, int& n, int& row0, int& rows) const {
         int u = first + lt * step;
@@ -359,6 +368,19 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         }
         return;
     }
+    if (PAIR || CLUSTERED) {
+        // The pair and row-cluster forms address their peers' shared memory and
+        // (pairs) issue cta_group::2 instructions: a launch whose cluster is not
+        // the one they were planned for leaves, reporting it, before any of that.
+        const uint32_t want = PAIR ? 2u : static_cast<uint32_t>(args.cluster);
+        if (cluster_nctarank() != want) {
+            if (threadIdx.x == 0 && atomicCAS(&args.status[0], 0u, 1u /* NF_ERR_INVALID_ARG */) == 0u) {
+                atomicExch(&args.status[1], SITE_CLUSTER_SHAPE);
+                atomicExch(&args.status[2], blockIdx.x);
+            }
+            return;
+        }
+    }
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
 
@@ -401,6 +423,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     int my_rank = 0;
     sched.pair = PAIR;
     sched.pair_rank = 0;
+    sched.kflip = Cfg::kAMN;
     if (PAIR) {
         my_rank = static_cast<int>(cluster_ctarank());
         const int cid = static_cast<int>(cluster_id_x());
@@ -495,19 +518,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     if (warp == PF_WARP && lane == 0 && count > 0) {
         int lt = 0, kt0, kt1, slice;
         sched.krange(0, kt0, kt1, slice);
-        int kt = kt0;
+        int ki = 0;
         for (int i = 0; i < STAGES && lt < count; ++i) {
             int m, n, row0, rows;
             sched.tile(lt, m, n, row0, rows);
+            const int kt = sched.kstep(lt, kt0, kt1, ki);
             if (Cfg::kAMN) {
                 tma_prefetch_l2_2d(&tmX, row0, kt * TILE_K);
                 tma_prefetch_l2_2d(&tmX, row0 + 64, kt * TILE_K);
             } else {
                 tma_prefetch_l2_2d(&tmX, kt * TILE_K, row0);
             }
-            if (++kt == kt1) {
+            if (++ki == kt1 - kt0) {
                 if (++lt < count) sched.krange(lt, kt0, kt1, slice);
-                kt = kt0;
+                ki = 0;
             }
         }
     }
@@ -562,7 +586,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 int m, n, row0, rows, kt0, kt1, slice;
                 sched.tile(lt, m, n, row0, rows);
                 sched.krange(lt, kt0, kt1, slice);
-                for (int kt = kt0; kt < kt1; ++kt) {
+                for (int ki = 0; ki < kt1 - kt0; ++ki) {
+                    const int kt = sched.kstep(lt, kt0, kt1, ki);
                     // (a slot's first fill never waits: the ring starts empty)
                     if (issued >= static_cast<uint32_t>(STAGES) &&
                         !mbar_wait<PAIR>(guard, bar_empty0 + 8u * s, ph ^ 1u, SITE_PROD_EMPTY, lt)) {
@@ -677,7 +702,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 const uint32_t d = tmem_base + static_cast<uint32_t>(b * TILE_N);
                 int kt0, kt1, slice;
                 sched.krange(lt, kt0, kt1, slice);
-                for (int kt = kt0; kt < kt1; ++kt) {
+                for (int ki = 0; ki < kt1 - kt0; ++ki) {
                     // (a pair's full[s] also completes by the peer's bytes or
                     // arrival: polled without the suspend hint)
                     if (!mbar_wait<PAIR>(guard, bar_ready0 + 8u * s, ph, SITE_MMA_FULL, lt)) {
@@ -702,9 +727,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                         const uint64_t bdesc = Cfg::kBK ? smem_desc_sw128(b0 + j * 32, 16, 1024)
                                                         : smem_desc_sw128(b0 + j * 2048, B_BOX_BYTES, 1024);
                         if (PAIR)
-                            mma_bf16_pair(d, adesc, bdesc, IDESC, (kt != kt0 || j != 0) ? 1u : 0u);
+                            mma_bf16_pair(d, adesc, bdesc, IDESC, (ki != 0 || j != 0) ? 1u : 0u);
                         else
-                            mma_bf16(d, adesc, bdesc, IDESC, (kt != kt0 || j != 0) ? 1u : 0u);
+                            mma_bf16(d, adesc, bdesc, IDESC, (ki != 0 || j != 0) ? 1u : 0u);
                     }
                     // stage free (in both CTAs of a pair) once these MMAs finish
                     if (PAIR)
@@ -1192,7 +1217,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         for (int lt = 0; lt < count && ok; ++lt) {
             int kt0, kt1, slice;
             sched.krange(lt, kt0, kt1, slice);
-            for (int kt = kt0; kt < kt1; ++kt) {
+            for (int ki = 0; ki < kt1 - kt0; ++ki) {
+                const int kt = sched.kstep(lt, kt0, kt1, ki);
                 if (!mbar_wait(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)) {
                     ok = false;
                     break;

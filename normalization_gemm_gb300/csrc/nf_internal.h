@@ -196,6 +196,7 @@ enum WaitSite : uint32_t {
     SITE_EPI_GXCH = 11,
     SITE_EPI_AFF = 12,
     SITE_SMEM_ALIGN = 13,  // code NF_ERR_ALIGNMENT: dynamic shared memory not 1 KB aligned
+    SITE_CLUSTER_SHAPE = 14,  // code NF_ERR_INVALID_ARG: launched with a cluster size the variant does not use
 };
 
 // One compiled GEMM variant.
