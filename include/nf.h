@@ -23,7 +23,9 @@
  *              owned by the library, one buffer of each kind per (device,
  *              stream): post-norm rows wider than 256 columns exchanged
  *              through L2 (the default, see nf_set_postnorm_exchange) use
- *              about 8 * M * ceil(N / 256) bytes; GEMMs split over the
+ *              about 8 * M * ceil(N / 256) bytes, and Lazy Pre-Norm GEMMs
+ *              with split row sums of squares (nf_set_prenorm_split) share
+ *              that buffer, needing 8 * M bytes of it; GEMMs split over the
  *              contraction (nf_set_gemm_splitk) use SMs * 128 KB.  Rule: no
  *              compute call ever synchronizes the host with the device.  A
  *              call that finds its stream's buffer missing or too small
@@ -116,7 +118,10 @@ nf_status nf_gemm_plain_t(const void* X, const void* W, void* Y, int64_t M,
  * shared-memory tiles of X the tensor cores consume, and applied to the fp32
  * accumulator in the epilogue: Y[i,:] = rstd_i * (X[i,:] * W), which equals
  * (rstd_i * X[i,:]) * W (the blog's §2 "Proof").  No gamma and no LayerNorm:
- * the blog's §2 limitations exclude both.
+ * the blog's §2 limitations exclude both.  On tensor-bound shapes with
+ * K >= 2048 and 2..32 column tiles of 256 a row, the tiles of a row share the
+ * sums of squares
+ * (nf_set_prenorm_split) through the stream's exchange scratch ("Memory").
  * rstd_out: optional (may be NULL), M fp32 values.
  * eps: finite and >= 0, else NF_ERR_INVALID_ARG.
  */
@@ -392,11 +397,26 @@ nf_status nf_set_gemm_tile_n(int tile_n);
  * loading its own 128 rows of X and half of W's 256 columns; post-norm rows
  * exchanged through L2 take them too.  mode 0 (default): plain GEMMs of
  * tensor-bound 256-column tiles (except those with so few tiles that each is
- * split over the contraction) and post-norm GEMMs with the L2 exchange and
- * K >= 2048; pre-norm GEMMs keep one CTA per tile (measured no faster in
- * pairs); 1: never; 2: whenever the tile has 256 columns and M > 128.
+ * split over the contraction), pre-norm GEMMs whose row sums of squares are
+ * split (nf_set_prenorm_split) and post-norm GEMMs with the L2 exchange and
+ * K >= 2048; 1: never; 2: whenever the tile has 256 columns and M > 128.
  * Applies to later calls. */
 nf_status nf_set_gemm_pair(int mode);
+
+/* Lazy Pre-Norm row sums of squares, split.  Every CTA of the blog's §2
+ * kernel sums the squares of all of its tile's rows from the shared-memory
+ * stages of X, so the n_tiles = ceil(N / 256) tiles of a row each repeat the
+ * same sums.  Split, tile n of a row tile sums only rows n R .. n R + R - 1
+ * (R = ceil(128 / n_tiles)) over the whole of K, and the row tile's tiles
+ * gather the 128 sums through L2 (scratch memory, see "Memory" above) before
+ * their epilogues scale the accumulators; the tiles then run as a persistent
+ * cooperative grid, like the post-norm L2 exchange.  The sums are the same up
+ * to fp32 summation order.  mode 0 (default): when the 256-column tiles are
+ * tensor-bound (their shared-memory reads would slow the MMA), K >= 2048 and
+ * a row has 2..32 of them; 1: never; 2: whenever a row has 2..32 tiles of 256
+ * columns.
+ * Applies to later calls. */
+nf_status nf_set_prenorm_split(int mode);
 
 /* How post-norm rows wider than 256 columns exchange partial statistics:
  * 0 (default) automatic -- one 512-column CTA per row while N <= 512, else
@@ -423,8 +443,9 @@ nf_status nf_set_postnorm_exchange(int mode);
 nf_status nf_set_gemm_splitk(int mode);
 
 /* Scratch set-up for `stream` (see "Memory" above): makes the stream's
- * post-norm exchange buffer large enough for post-norm calls (forward and
- * backward) of up to max_rows x max_cols, and sets up its split-K workspace,
+ * exchange buffer large enough for post-norm calls (forward and backward) of
+ * up to max_rows x max_cols and Lazy Pre-Norm calls of up to max_rows rows
+ * (any N), and sets up its split-K workspace,
  * both in stream order without synchronizing the host.  Afterwards, calls on
  * the stream within those sizes allocate nothing and may be captured.
  * max_cols <= NF_POSTNORM_MAX_N.  Refused (NF_ERR_INVALID_ARG) while the

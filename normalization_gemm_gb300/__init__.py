@@ -86,6 +86,7 @@ _SIGS = {
     "nf_set_gemm_tile_n": [ctypes.c_int],
     "nf_set_gemm_pair": [ctypes.c_int],
     "nf_set_postnorm_exchange": [ctypes.c_int],
+    "nf_set_prenorm_split": [ctypes.c_int],
     "nf_set_gemm_splitk": [ctypes.c_int],
     "nf_reserve_scratch": [_I64, _I64, _VP],
     "nf_selftest_wait_timeout": [ctypes.c_uint64, _VP],
@@ -479,6 +480,13 @@ def set_gemm_pair(mode: int) -> None:
 def set_gemm_splitk(mode: int) -> None:
     """Split-K of plain GEMMs with few output tiles: 0 automatic (default), 1 never."""
     _check(lib().nf_set_gemm_splitk(int(mode)), "nf_set_gemm_splitk")
+
+
+def set_prenorm_split(mode: int) -> None:
+    """Lazy Pre-Norm row sums of squares split over a row's 256-column tiles and
+    gathered through L2: 0 automatic (tensor-bound tiles, K >= 2048), 1 never,
+    2 whenever a row has 2..32 tiles."""
+    _check(lib().nf_set_prenorm_split(int(mode)), "nf_set_prenorm_split")
 
 
 def set_postnorm_exchange(mode: int) -> None:

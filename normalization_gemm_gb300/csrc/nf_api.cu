@@ -70,6 +70,9 @@ int g_gemm_tile = 0;
 int g_pair_mode = 0;
 // Post-norm rows wider than 256 columns: 0 = automatic, else an Exchange mode.
 int g_post_xch = 0;
+// Lazy Pre-Norm row sums of squares split over a row's tiles: 0 = automatic
+// (tensor-bound tiles), 1 = never, 2 = whenever the shape allows.
+int g_pre_split = 0;
 // A cooperative launch accepted the programmatic-serialization attribute.
 bool g_coop_overlap_ok = true;
 // A cooperative launch of clusters (CTA pairs with the L2 exchange) was accepted.
@@ -308,6 +311,25 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
             if (N <= p->tile_n) p->xch = XCH_NONE;  // one wide CTA covers the row
         }
     }
+    // Lazy Pre-Norm with 2..32 tiles of 256 columns a row: each tile sums the
+    // squares of 1/n_tiles of the rows, and the row tile's tiles gather them
+    // through L2 (the kernel's split sums of squares), instead of every tile
+    // summing every row from its shared-memory stages -- on tensor-bound
+    // tiles those reads take shared-memory bandwidth from the MMA (measured at
+    // 8192 x 4096 x 4096 in CTA pairs: 159 us with every tile summing every
+    // row, 143 us without the reads).  The gather needs the cooperative
+    // persistent grid of the post-norm L2 exchange; <= 32 tiles a row keeps
+    // 2 x resident CTAs (or pairs) >= n_tiles.  Automatic for tensor-bound
+    // tiles with K >= 2048: memory-bound tiles keep the plain form (their last
+    // wave is cut into 64-row units instead), and with a shorter contraction
+    // the gather's latency and the cooperative launch cost about what the
+    // shared reads saved (16384 x 1024 x 2048: 50.4 us split, 49.6 us not).
+    if (op == OP_PRE && ops == 0 && p->tile_n == 256 && g_pre_split != 1) {
+        const int64_t nt = (N + 255) / 256;
+        if (nt >= 2 && nt <= 32 &&
+            (g_pre_split == 2 || (K >= 2048 && !tile_memory_bound(K, 256, static_cast<int>(nt)))))
+            p->xch = XCH_GLOBAL;
+    }
     p->clustered = p->xch == XCH_CLUSTER;
     p->cluster = p->clustered ? static_cast<int>((N + p->tile_n - 1) / p->tile_n) : 1;
     p->m_tiles = static_cast<int>((M + TILE_M - 1) / TILE_M);
@@ -321,13 +343,14 @@ nf_status plan_tiles(int op, int64_t M, int64_t N, int64_t K, int sms, Plan* p, 
     const int64_t tiles_all = static_cast<int64_t>(p->m_tiles) * p->n_tiles;
     const bool pair_op = ((op == OP_PLAIN || op == OP_PRE) && ops == 0) ||
                          (post && p->xch == XCH_GLOBAL && ops == 0);
-    // (Automatic plans leave pre-norm GEMMs on single CTAs: measured, the
-    // pre-norm pair's per-stage signal to the peer's sum-of-squares warps
-    // makes it no faster.  Post-norm tiles of a shorter contraction are bound
-    // by their epilogue, which a pair's two CTAs both wait for: K >= 2048.)
+    // (Automatic plans pair pre-norm GEMMs only with the split sums of
+    // squares: with every tile summing every row, measured no faster in pairs.
+    // Post-norm tiles of a shorter contraction are bound by their epilogue,
+    // which a pair's two CTAs both wait for: K >= 2048.)
     p->pair = pair_op && p->tile_n == 256 && p->m_tiles >= 2 &&
               (g_pair_mode == 2 ||
-               (g_pair_mode == 0 && op != OP_PRE && !tile_memory_bound(K, p->tile_n, p->n_tiles) &&
+               (g_pair_mode == 0 && (op != OP_PRE || p->xch == XCH_GLOBAL) &&
+                !tile_memory_bound(K, p->tile_n, p->n_tiles) &&
                 (!post || K >= 2048) &&
                 !(op == OP_PLAIN && g_splitk_mode != 1 && 2 * tiles_all <= sms && (K + TILE_K - 1) / TILE_K >= 16)));
     if (p->pair) {
@@ -694,6 +717,10 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.h_out = static_cast<uint16_t*>(h_out);
 
     int grid = 0;
+    // Exchange scratch: post-norm partials of every (row tile, column tile);
+    // the pre-norm's split sums of squares, one float per row (the size of a
+    // single column tile's partials, which the scratch holds in any case).
+    const int xnt = op == OP_PRE ? 1 : p.n_tiles;
     a.units = p.m_tiles * p.n_tiles;
     a.split_base = a.units;
     if (p.pair) {
@@ -719,7 +746,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
                 a.xcnt = reinterpret_cast<int*>(base);
                 a.xbank = static_cast<int32_t>(kNoAllocBankInts);
                 a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
-            } else if ((st = xch_scratch(stream, p.m_tiles, p.n_tiles, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
+            } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
                 return st;
             }
         }
@@ -746,7 +773,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
             a.xcnt = reinterpret_cast<int*>(base);
             a.xbank = static_cast<int32_t>(kNoAllocBankInts);
             a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
-        } else if ((st = xch_scratch(stream, p.m_tiles, p.n_tiles, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
+        } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
             return st;
         }
     } else if (p.splitk > 1) {
@@ -1135,6 +1162,13 @@ nf_status nf_set_gemm_pair(int mode) {
     if (mode != 0 && mode != 1 && mode != 2)
         return fail(NF_ERR_INVALID_ARG, "pair mode: 0 automatic, 1 never, 2 whenever the tile allows");
     g_pair_mode = mode;
+    return NF_OK;
+}
+
+nf_status nf_set_prenorm_split(int mode) {
+    if (mode < 0 || mode > 2)
+        return fail(NF_ERR_INVALID_ARG, "pre-norm split: 0 automatic, 1 never, 2 whenever the shape allows");
+    g_pre_split = mode;
     return NF_OK;
 }
 

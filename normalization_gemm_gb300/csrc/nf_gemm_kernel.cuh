@@ -80,6 +80,8 @@
 //                whereas clusters of 8 or 16 co-reside on fewer of them.
 #pragma once
 
+#include <type_traits>
+
 #include "nf_internal.h"
 #include "nf_ptx.cuh"
 
@@ -381,6 +383,15 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             return;
         }
     }
+    if (Cfg::kPre && GLOBALX && args.n_tiles < 2) {
+        // Split sums of squares: two or more tiles a row keep each tile's share
+        // within SPLIT_SS_ITERS loads a lane and stage.
+        if (threadIdx.x == 0 && atomicCAS(&args.status[0], 0u, 1u /* NF_ERR_INVALID_ARG */) == 0u) {
+            atomicExch(&args.status[1], SITE_SPLIT_SS);
+            atomicExch(&args.status[2], blockIdx.x);
+        }
+        return;
+    }
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
 
@@ -404,11 +415,11 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
 
     const uint32_t bar_afff0 = bar_mma_done + 8u;  // [2] global exchange: a group's affine slot filled
     const uint32_t bar_affe0 = bar_afff0 + 16u;    // [2] global exchange: a group's affine slot free
+    const uint32_t bar_sspf0 = bar_afff0;  // [2] pre-norm, split sums: a tile's row sums staged (pre-norm has no affine)
+    const uint32_t bar_sspe0 = bar_affe0;  // [2] pre-norm, split sums: staging slot published, free
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS);
     volatile int* const abort_flag =
         reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 4);
-    volatile int* const epoch_sm =  // global exchange: launch epoch and the last launch's row counters
-        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 8);
     float* const ss_buf = reinterpret_cast<float*>(base_ptr + Cfg::OFF_SS);
     uint16_t* const aff = reinterpret_cast<uint16_t*>(base_ptr + Cfg::OFF_AFF);
 
@@ -471,7 +482,9 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         prefetch_tmap(&tmY);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full0 + 8u * s, 1);
-            mbar_init(bar_empty0 + 8u * s, 1 + (Cfg::kPre ? 128 : 0));  // (pre-norm: and the sum-of-squares threads)
+            // (pre-norm: and the sum-of-squares threads, or, with the sums
+            // split over the row's tiles, its one sum-of-squares warp)
+            mbar_init(bar_empty0 + 8u * s, 1 + (Cfg::kPre ? (GLOBALX ? 1 : 128) : 0));
         }
         for (int b = 0; b < NACC; ++b) {
             mbar_init(bar_accf0 + 8u * b, 1);
@@ -486,8 +499,11 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         if (Cfg::kScaleA)
             for (int st = 0; st < STAGES; ++st) mbar_init(bar_xf0 + 8u * st, 128);  // the transform threads
         for (int g = 0; g < 2; ++g) {
-            mbar_init(bar_afff0 + 8u * g, 4);  // one arrival per warp of the group
-            mbar_init(bar_affe0 + 8u * g, 4);
+            // post-norm: one arrival per warp of the group; pre-norm (split
+            // sums of squares): one from the summing warp (ssp_full), one from
+            // the publishing warp (ssp_empty)
+            mbar_init(bar_afff0 + 8u * g, Cfg::kPre ? 1 : 4);
+            mbar_init(bar_affe0 + 8u * g, Cfg::kPre ? 1 : 4);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -540,13 +556,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     // this (the prefetches above only warm L2).
     griddep_wait();
     griddep_launch_dependents();
-    // Global exchange: count in bank E & 1; clear the other bank, which the
-    // previous launch on this scratch used (it has completed).
-    int* xbank = nullptr;
-    if (GLOBALX && threadIdx.x == 0) {  // shared with the CTA by the barrier below
-        epoch_sm[0] = ld_acquire_gpu(args.xcnt + 2);
-        epoch_sm[1] = ld_acquire_gpu(args.xcnt + 3) * 4;
-    }
+    // Global exchange: launch E counts in bank E & 1.  Only the warps that
+    // count or wait read E (gx_bank, below), after the pipeline has started:
+    // an L2 round trip before the barrier would hold the producer back.  (E is
+    // fixed for the launch: the last CTA to leave advances it, after every
+    // thread's last use.)
+    auto gx_epoch = [&](int* prev_ints) -> int {  // (whole warp; prev_ints: the last launch's counters)
+        int e = 0, pv = 0;
+        if (lane == 0) {
+            e = ld_acquire_gpu(args.xcnt + 2);
+            if (prev_ints) pv = ld_acquire_gpu(args.xcnt + 3) * 4;
+        }
+        if (prev_ints) *prev_ints = __shfl_sync(0xffffffffu, pv, 0);
+        return __shfl_sync(0xffffffffu, e, 0);
+    };
     if (Cfg::kRow && !GLOBALX && threadIdx.x < 128) {
         // This CTA's columns never change: clustered CTAs keep their rank's
         // tile, unclustered post-norm has a single column tile.
@@ -566,13 +589,6 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         cluster_wait_acquire();
     }
     const uint32_t tmem_base = *tmem_holder;
-    if (GLOBALX) {
-        const int e = epoch_sm[0], prev_ints = epoch_sm[1];
-        xbank = args.xcnt + XCH_CNT0 + (e & 1) * args.xbank;
-        int* const other = args.xcnt + XCH_CNT0 + ((e + 1) & 1) * args.xbank;
-        const int stride = static_cast<int>(gridDim.x * blockDim.x);
-        for (int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i < prev_ints; i += stride) other[i] = 0;
-    }
 
     if (warp == Cfg::PRODUCER_WARP) {
         // ================================================================ TMA producer
@@ -757,6 +773,21 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         __syncwarp();
     } else if (warp < EPI_WARPS) {
         // ================================================================ epilogue
+        // Global exchange: this launch's bank, and the other bank cleared --
+        // the previous launch on this scratch counted there (it has completed;
+        // the next launch counts there).  The epilogue warps do it while the
+        // first tile's main loop runs.
+        int* xbank = nullptr;
+        if (GLOBALX) {
+            int prev_ints = 0;
+            const int e = gx_epoch(&prev_ints);
+            xbank = args.xcnt + XCH_CNT0 + (e & 1) * args.xbank;
+            int* const other = args.xcnt + XCH_CNT0 + ((e + 1) & 1) * args.xbank;
+            const int stride = static_cast<int>(gridDim.x) * EPI_WARPS * 32;
+            for (int i = static_cast<int>(blockIdx.x) * EPI_WARPS * 32 + static_cast<int>(threadIdx.x); i < prev_ints;
+                 i += stride)
+                other[i] = 0;
+        }
         // Two warpgroups alternate tiles: group g drains TMEM accumulator g, so
         // each group has two tiles' time for its chain of TMEM reads,
         // statistics, conversion and stores.  Warp (g, qtr) owns TMEM lane
@@ -848,10 +879,22 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
 
 
             if (Cfg::kPre) {
-                ok = mbar_wait(guard, bar_ssf0 + 8u * b, aph, SITE_EPI_SS_FULL, lt);
-                if (!__all_sync(0xffffffffu, ok)) break;
+                float ss = 0.0f;
+                if (GLOBALX) {
+                    // The row's sum of squares, summed by one of the row tile's
+                    // n_tiles tiles and published through L2 once every one of
+                    // them has counted.  (A CTA pair's second CTA past M has no
+                    // rows: nothing to wait for.)
+                    if (m < args.m_tiles) {
+                        if (!gwait_geq(guard, xbank + m * 4, args.n_tiles, SITE_EPI_GXCH, lt)) break;
+                        ss = __ldcg(reinterpret_cast<const float*>(args.xstats) + static_cast<size_t>(m) * TILE_M + row);
+                    }
+                } else {
+                    ok = mbar_wait(guard, bar_ssf0 + 8u * b, aph, SITE_EPI_SS_FULL, lt);
+                    if (!__all_sync(0xffffffffu, ok)) break;
+                    ss = ss_buf[b * TILE_M + row];
+                }
                 // blog §2: rstd = rsqrt(square_sum / K + eps); acc *= rstd[:, None]
-                const float ss = ss_buf[b * TILE_M + row];
                 scale = rsqrtf(fmaf(ss, args.inv_len, args.eps));
                 if (n == 0 && args.rstd_out && own_row) args.rstd_out[grow] = scale;
             }
@@ -912,16 +955,22 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                     }
                 } else if (GLOBALX) {
                     const int nt = args.n_tiles;
-                    float2* const xst = args.xstats + static_cast<size_t>(m) * nt * TILE_M + row;
-                    int* const cnt = xbank + m * 4 + qtr;
-                    __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
-                    __syncwarp();  // the warp's stores precede lane 0's release
-                    if (lane == 0) red_release_gpu_add(cnt, 1);
-                    if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
+                    // A CTA pair's second CTA past M (an odd number of row
+                    // tiles) has no rows: it neither publishes nor waits, and
+                    // touches no counter or partial beyond the row tiles.
+                    const bool real = m < args.m_tiles;
+                    float2* const xst = args.xstats + static_cast<size_t>(real ? m : 0) * nt * TILE_M + row;
+                    if (real) {
+                        int* const cnt = xbank + m * 4 + qtr;
+                        __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
+                        __syncwarp();  // the warp's stores precede lane 0's release
+                        if (lane == 0) red_release_gpu_add(cnt, 1);
+                        if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
+                    }
                     float2 pp[MAX_CLUSTER];
 #pragma unroll
                     for (int p = 0; p < MAX_CLUSTER; ++p)
-                        pp[p] = p < nt ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
+                        pp[p] = (real && p < nt) ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
                     s1 = s2 = 0.0f;
 #pragma unroll
                     for (int p = 0; p < MAX_CLUSTER; ++p) {
@@ -1046,16 +1095,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                     //    all n_tiles column tiles of row tile m have counted,
                     //    read their partials.
                     const int nt = args.n_tiles;
-                    float2* const xst = args.xstats + static_cast<size_t>(m) * nt * TILE_M + row;
-                    int* const cnt = xbank + m * 4 + qtr;
-                    __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
-                    __syncwarp();  // the warp's stores precede lane 0's release
-                    if (lane == 0) red_release_gpu_add(cnt, 1);
-                    if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
+                    // (a CTA pair's second CTA past M: no rows, no exchange)
+                    const bool real = m < args.m_tiles;
+                    float2* const xst = args.xstats + static_cast<size_t>(real ? m : 0) * nt * TILE_M + row;
+                    if (real) {
+                        int* const cnt = xbank + m * 4 + qtr;
+                        __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
+                        __syncwarp();  // the warp's stores precede lane 0's release
+                        if (lane == 0) red_release_gpu_add(cnt, 1);
+                        if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
+                    }
                     float2 pp[MAX_CLUSTER];
 #pragma unroll
                     for (int p = 0; p < MAX_CLUSTER; ++p)
-                        pp[p] = p < nt ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
+                        pp[p] = (real && p < nt) ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
                     if (Cfg::kLN) {
                         // Chan et al. pairwise merge of (count, mean, M2).
                         float msum = 0.0f;
@@ -1244,6 +1297,139 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                     s = 0;
                     ph ^= 1u;
                 }
+            }
+        }
+    } else if (Cfg::kPre && GLOBALX && warp >= Cfg::SUMSQ_WARP0) {
+        // ================================================================ row sums of squares, split
+        // The n_tiles tiles of a row tile share the work on its rows (the
+        // blog's CTAs each sum every row, a redundancy that costs shared-memory
+        // bandwidth the tensor cores need): tile (m, n) sums rows
+        // n R .. n R + R - 1, R = ceil(128 / n_tiles), over the whole
+        // contraction, from the same stages the MMA reads -- one warp reading
+        // 1/n_tiles of each A stage.  A second warp publishes the R sums
+        // through L2 and counts them on row tile m's counter (its release waits
+        // for the stores to land; the summing warp, whose arrivals free the
+        // ring's stages, never waits on L2).  Every tile of row tile m waits in
+        // its epilogue for all n_tiles counts.  Deadlock freedom is that of the
+        // post-norm exchange: a tile's publication needs only its own main
+        // loop, which needs the epilogue of the CTA's tile two before it, which
+        // lies in an earlier row tile (tiles in order, 2 G >= n_tiles).
+        const int nt = args.n_tiles;  // >= 2 (checked at entry): R <= 64
+        const int R = (TILE_M + nt - 1) / nt;
+        if (warp == Cfg::SUMSQ_WARP0) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int lt = 0; lt < count; ++lt) {
+                int m, n, row0, rows;
+                sched.tile(lt, m, n, row0, rows);
+                const int r0 = n * R;
+                const int nchunk = max(0, min(R, TILE_M - r0)) * 8;  // 16-byte chunks of those rows per stage
+                const int nload = (nchunk + 31) >> 5;                   // loads a lane needs per stage (<= 16)
+                // Lane l reads chunk l & 7 of rows (l >> 3) + 4 i, i < NL: a warp
+                // load covers four whole 128-byte rows (no bank conflicts).  A
+                // row past the tile's share reads chunk 0 of its first row
+                // instead and is never published.
+                float acc[SPLIT_SS_ITERS];
+#pragma unroll
+                for (int i = 0; i < SPLIT_SS_ITERS; ++i) acc[i] = 0.0f;
+                // NL loads a lane and stage, fixed at compile time: all are
+                // issued, unconditionally, before any is used, so a stage costs
+                // one shared-memory latency, which the tensor cores' operand
+                // reads stretch to a large part of a stage's MMA time.
+                // (Measured: loads issued under per-load conditions were each
+                // waited for in turn, and this warp fell a ring behind the MMA
+                // and set its pace -- 8192 x 4096 x 4096 in CTA pairs 162 us
+                // against 141 us.)
+                auto tile_sums = [&](auto nl_tag) -> bool {
+                    constexpr int NL = decltype(nl_tag)::value;
+                    uint32_t off[NL > 0 ? NL : 1];
+#pragma unroll
+                    for (int i = 0; i < NL; ++i) {
+                        const int c = lane + 32 * i;
+                        const int cc = c < nchunk ? c : 0;
+                        off[i] = static_cast<uint32_t>(r0 * 128 + (cc >> 3) * 128 + (cc & 7) * 16);
+                    }
+                    for (int kt = 0; kt < k_tiles; ++kt) {
+                        const bool got = (!PAIR || lead)
+                                             ? mbar_wait<2>(guard, bar_full0 + 8u * s, ph, SITE_SS_FULL, lt)
+                                             : mbar_wait<2>(guard, bar_ardy0 + 8u * s, ph, SITE_SS_FULL, lt);
+                        if (!__all_sync(0xffffffffu, got)) return false;
+                        if (PAIR && lead && lane == 0)
+                            mbar_arrive_remote_relaxed(
+                                mapa_shared(bar_ardy0 + 8u * s, static_cast<uint32_t>(my_rank | 1)));
+                        const uint32_t sbase = sA + s * A_STAGE_BYTES;
+                        uint4 w[NL > 0 ? NL : 1];
+#pragma unroll
+                        for (int i = 0; i < NL; ++i) w[i] = ld_shared_v4(sbase + off[i]);
+#pragma unroll
+                        for (int i = 0; i < NL; ++i) {
+                            float x, a = acc[i];
+                            x = bf16lo(w[i].x); a = fmaf(x, x, a);
+                            x = bf16hi(w[i].x); a = fmaf(x, x, a);
+                            x = bf16lo(w[i].y); a = fmaf(x, x, a);
+                            x = bf16hi(w[i].y); a = fmaf(x, x, a);
+                            x = bf16lo(w[i].z); a = fmaf(x, x, a);
+                            x = bf16hi(w[i].z); a = fmaf(x, x, a);
+                            x = bf16lo(w[i].w); a = fmaf(x, x, a);
+                            x = bf16hi(w[i].w); a = fmaf(x, x, a);
+                            acc[i] = a;
+                        }
+                        __syncwarp();  // the warp's reads of the stage precede lane 0's arrival
+                        if (lane == 0) mbar_arrive(bar_empty0 + 8u * s);
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    return true;
+                };
+                // (the wait polls without the suspend hint: measured faster here)
+                bool ok;
+                if (nload == 0) ok = tile_sums(std::integral_constant<int, 0>{});
+                else if (nload <= 1) ok = tile_sums(std::integral_constant<int, 1>{});
+                else if (nload <= 2) ok = tile_sums(std::integral_constant<int, 2>{});
+                else if (nload <= 4) ok = tile_sums(std::integral_constant<int, 4>{});
+                else if (nload <= 8) ok = tile_sums(std::integral_constant<int, 8>{});
+                else ok = tile_sums(std::integral_constant<int, 16>{});
+                if (!ok) break;
+                // Whole rows: add the eight chunks' sums (lanes 8j .. 8j + 7).
+#pragma unroll
+                for (int i = 0; i < SPLIT_SS_ITERS; ++i) {
+                    acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 1);
+                    acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
+                    acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 4);
+                }
+                // Staging slot lt & 1 is free once tile lt - 2's sums are published.
+                const int slot = lt & 1;
+                const uint32_t sph = static_cast<uint32_t>(lt >> 1) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(guard, bar_sspe0 + 8u * slot, sph ^ 1u, SITE_SS_ACC_EMPTY, lt)))
+                    break;
+#pragma unroll
+                for (int i = 0; i < SPLIT_SS_ITERS; ++i) {
+                    const int r = (lane >> 3) + 4 * i;
+                    if ((lane & 7) == 0 && 8 * r < nchunk) ss_buf[slot * TILE_M + r] = acc[i];
+                }
+                __syncwarp();  // the warp's writes precede lane 0's arrival
+                if (lane == 0) mbar_arrive(bar_sspf0 + 8u * slot);
+            }
+        } else if (warp == Cfg::SUMSQ_WARP0 + 1) {
+            int* const xbank = args.xcnt + XCH_CNT0 + (gx_epoch(nullptr) & 1) * args.xbank;
+            for (int lt = 0; lt < count; ++lt) {
+                int m, n, row0, rows;
+                sched.tile(lt, m, n, row0, rows);
+                const int r0 = n * R;
+                const int nrow = max(0, min(R, TILE_M - r0));
+                const int slot = lt & 1;
+                const uint32_t sph = static_cast<uint32_t>(lt >> 1) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(guard, bar_sspf0 + 8u * slot, sph, SITE_SS_FULL, lt))) break;
+                if (m < args.m_tiles) {  // (a CTA pair's second CTA past M: no rows, nothing to publish)
+                    float* const dst = reinterpret_cast<float*>(args.xstats) + static_cast<size_t>(m) * TILE_M + r0;
+                    for (int r = lane; r < nrow; r += 32) __stcg(dst + r, ss_buf[slot * TILE_M + r]);
+                    __syncwarp();  // the warp's stores precede lane 0's release
+                    if (lane == 0) red_release_gpu_add(xbank + m * 4, 1);
+                }
+                __syncwarp();  // the warp's reads of the slot precede lane 0's arrival
+                if (lane == 0) mbar_arrive(bar_sspe0 + 8u * slot);
             }
         }
     } else if (Cfg::kPre && warp >= Cfg::SUMSQ_WARP0) {

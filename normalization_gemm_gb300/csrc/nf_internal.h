@@ -21,6 +21,10 @@ constexpr int STORE_ROWS = 32;
 constexpr int STORE_BUF_BYTES = STORE_COLS * STORE_ROWS * 2;              // 4 KB
 constexpr int STAGING_BYTES = EPI_WARPS * STORE_BUF_BYTES;                 // one box per warp
 constexpr int MAX_CLUSTER = 16;           // post-norm: N <= 256 x 16
+// Pre-norm with the row sums of squares split over a row's n_tiles >= 2 tiles:
+// a tile sums R = ceil(128 / n_tiles) <= 64 rows, 8 R <= 512 16-byte chunks a
+// stage, read by one warp in at most 16 loads a lane.
+constexpr int SPLIT_SS_ITERS = 16;
 constexpr int SMEM_OPTIN_LIMIT = 232448;  // 227 KB of dynamic shared memory per block
 constexpr int MAX_STAGES = 8;
 
@@ -51,7 +55,9 @@ enum Exchange : int {
 //          used: no counter is ever reset while it may be read, and a launch
 //          that gave up part-way leaves nothing behind.
 //   xstats float2 partial (mean, M2) or (sum of squares, 0) per
-//          (row tile, column tile, tile row)
+//          (row tile, column tile, tile row); for the pre-norm's split sums
+//          of squares, one float per row (row tile m's 128 at m * 128), counted
+//          on the first of the row tile's four counters
 constexpr int XCH_CNT0 = 64;  // banks start 256 bytes in
 __host__ __device__ inline int64_t xch_bank_ints(int m_tiles) { return static_cast<int64_t>(m_tiles) * 4; }
 __host__ __device__ inline int64_t xch_stats_bytes(int m_tiles, int n_tiles) {
@@ -86,14 +92,18 @@ struct GemmCfg {
     static constexpr bool kRes = (OPS & OPS_RESID) != 0;
     static constexpr bool kPair = (OPS & OPS_PAIR) != 0;
     static_assert(!kPair || (OPS == OPS_PAIR && TILE_N == 256 &&
-                             (((EPI == EPI_PLAIN || EPI == EPI_PRE_RMS) && XCH == XCH_NONE) ||
+                             ((EPI == EPI_PLAIN && XCH == XCH_NONE) || EPI == EPI_PRE_RMS ||
                               ((EPI == EPI_POST_LN || EPI == EPI_POST_RMS) && XCH == XCH_GLOBAL))),
                   "the CTA pair is built for plain and pre-norm GEMMs of 256-column tiles and for "
                   "post-norm rows exchanged through L2");
     static_assert(!kRes || kPost, "the residual add belongs to the post-norm epilogues");
     static_assert(!kScaleA || (kAMN && EPI == EPI_PLAIN), "row scaling applies to a transposed A, plain epilogue");
     static_assert(TILE_N == 64 || TILE_N == 128 || TILE_N == 256, "tile_n");
-    static_assert(XCH == XCH_NONE || (kRow && TILE_N == 256), "row exchange only for post-norm");
+    // Row exchanges: post-norm partial statistics (cluster or L2), or the
+    // pre-norm's row sums of squares split over the row's tiles (L2).
+    static_assert(XCH == XCH_NONE || (kRow && TILE_N == 256) ||
+                      (kPre && XCH == XCH_GLOBAL && TILE_N == 256 && (OPS == 0 || OPS == OPS_PAIR)),
+                  "row exchange only for post-norm, or the pre-norm's split sums of squares");
 
     static constexpr int B_STAGE_BYTES = TILE_K * (kPair ? TILE_N / 2 : TILE_N) * 2;  // this CTA's share of B
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
@@ -197,6 +207,7 @@ enum WaitSite : uint32_t {
     SITE_EPI_AFF = 12,
     SITE_SMEM_ALIGN = 13,  // code NF_ERR_ALIGNMENT: dynamic shared memory not 1 KB aligned
     SITE_CLUSTER_SHAPE = 14,  // code NF_ERR_INVALID_ARG: launched with a cluster size the variant does not use
+    SITE_SPLIT_SS = 15,  // code NF_ERR_INVALID_ARG: pre-norm split sums of squares with fewer than two tiles a row
 };
 
 // One compiled GEMM variant.

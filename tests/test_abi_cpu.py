@@ -322,7 +322,8 @@ def test_reserve_scratch_argument_checks(L):
 
 @pytest.mark.parametrize("op,M,N,K,pair", [
     (0, 8192, 4096, 4096, True),    # tensor-bound 256-column tiles
-    (1, 8192, 4096, 4096, False),   # pre-norm GEMMs keep one CTA per tile
+    (1, 8192, 4096, 4096, True),    # pre-norm GEMMs whose sums of squares are split over a row's tiles
+    (1, 8192, 256, 4096, False),    # ... but not a row of one tile (every tile sums its own rows)
     (0, 4096, 4096, 8192, True),    # pairs instead of splitting the last wave
     (0, 512, 512, 32768, False),    # 8 tiles: every tile split over the contraction instead
     (1, 32768, 512, 512, False),    # memory-bound tiles
@@ -346,3 +347,28 @@ def test_pair_plans(L, op, M, N, K, pair):
     finally:
         nf.set_gemm_pair(0)
     assert L.nf_set_gemm_pair(3) == INVALID
+
+
+@pytest.mark.parametrize("M,N,K,split", [
+    (8192, 4096, 4096, (2, 0, 2)),    # tensor-bound tiles, 16 a row: split by default
+    (16384, 2048, 2048, (2, 0, 2)),   # 8 a row
+    (16384, 2048, 1024, (0, 0, 2)),   # ... but a contraction shorter than 2048: only on request
+    (32768, 512, 512, (0, 0, 2)),     # memory-bound tiles: only on request
+    (8192, 256, 4096, (0, 0, 0)),     # one tile a row: nothing to share
+    (1024, 8448, 4096, (0, 0, 0)),    # 33 tiles a row: beyond the gather's limit
+    (100, 4096, 4096, (2, 0, 2)),     # a single row tile
+])
+def test_prenorm_split_plans(L, M, N, K, split):
+    """Lazy Pre-Norm with the row sums of squares split over a row's tiles:
+    exchange 2 (the L2 gather) for modes 0 (automatic), 1 (never), 2 (always)."""
+    try:
+        for mode, want in zip((0, 1, 2), split):
+            nf.set_prenorm_split(mode)
+            p = nf.plan_gemm(1, M, N, K, 148)
+            assert p["exchange"] == want, (mode, p)
+            if want:
+                assert p["tile_n"] == 256 and p["splitk"] == 1
+    finally:
+        nf.set_prenorm_split(0)
+    assert L.nf_set_prenorm_split(3) == INVALID
+    assert L.nf_set_prenorm_split(-1) == INVALID

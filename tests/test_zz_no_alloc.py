@@ -5,17 +5,17 @@ import pytest
 
 import nf_inputs
 import normalization_gemm_gb300 as nf
-from gpu_util import to_dev
+from gpu_util import require_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(scope="module")
 def dev():
-    import torch
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    return torch.device("cuda", 0)
+    d = require_gpu()  # fails, like every GPU module, when no device is present
+    from normalization_gemm_gb300 import _build
+    _build.build()
+    return d
 
 
 def _inputs(M, K, N, seed):
