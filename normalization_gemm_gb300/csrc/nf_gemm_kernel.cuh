@@ -422,6 +422,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 4);
     float* const ss_buf = reinterpret_cast<float*>(base_ptr + Cfg::OFF_SS);
     uint16_t* const aff = reinterpret_cast<uint16_t*>(base_ptr + Cfg::OFF_AFF);
+    volatile int* const epoch_sm =  // global exchange: launch epoch and the last launch's counter count
+        reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 8);
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
@@ -561,14 +563,19 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     // an L2 round trip before the barrier would hold the producer back.  (E is
     // fixed for the launch: the last CTA to leave advances it, after every
     // thread's last use.)
-    auto gx_epoch = [&](int* prev_ints) -> int {  // (whole warp; prev_ints: the last launch's counters)
-        int e = 0, pv = 0;
-        if (lane == 0) {
-            e = ld_acquire_gpu(args.xcnt + 2);
-            if (prev_ints) pv = ld_acquire_gpu(args.xcnt + 3) * 4;
+    // One thread of the first epilogue warp reads E (and the last launch's
+    // counter count) into shared memory; the epilogue warps and the
+    // pre-norm's publishing warp meet at a named barrier and take it from
+    // there.  The CTA counts itself in after that barrier, so no warp of a
+    // counted CTA reads E from L2 after the last CTA may have advanced it.
+    constexpr int XWARPS = EPI_WARPS + (Cfg::kPre ? 1 : 0);  // warps meeting at named barrier 1
+    auto gx_epoch = [&]() {
+        if (threadIdx.x == 0) {
+            epoch_sm[0] = ld_acquire_gpu(args.xcnt + 2);
+            epoch_sm[1] = ld_acquire_gpu(args.xcnt + 3) * 4;
         }
-        if (prev_ints) *prev_ints = __shfl_sync(0xffffffffu, pv, 0);
-        return __shfl_sync(0xffffffffu, e, 0);
+        named_bar_sync(1, XWARPS * 32);
+        return epoch_sm[0];
     };
     if (Cfg::kRow && !GLOBALX && threadIdx.x < 128) {
         // This CTA's columns never change: clustered CTAs keep their rank's
@@ -779,14 +786,29 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         // first tile's main loop runs.
         int* xbank = nullptr;
         if (GLOBALX) {
-            int prev_ints = 0;
-            const int e = gx_epoch(&prev_ints);
+            const int e = gx_epoch();
+            const int prev_ints = epoch_sm[1];
             xbank = args.xcnt + XCH_CNT0 + (e & 1) * args.xbank;
             int* const other = args.xcnt + XCH_CNT0 + ((e + 1) & 1) * args.xbank;
             const int stride = static_cast<int>(gridDim.x) * EPI_WARPS * 32;
             for (int i = static_cast<int>(blockIdx.x) * EPI_WARPS * 32 + static_cast<int>(threadIdx.x); i < prev_ints;
                  i += stride)
                 other[i] = 0;
+            if (threadIdx.x == 0) {
+                // Every CTA counts itself in once its warps hold E (the named
+                // barrier above).  The last one resets the count, records how
+                // many counters this launch uses (the next launch clears them)
+                // and advances the epoch, which the next launch reads after
+                // this one has completed.  Done here, in the first main loop's
+                // shadow, not at exit, where its L2 round trips would delay the
+                // kernel's end.
+                int* const hdr = args.xcnt;
+                if (atom_acq_rel_gpu_add(hdr, 1) == static_cast<int>(gridDim.x) - 1) {
+                    hdr[0] = 0;
+                    hdr[3] = args.m_tiles;
+                    st_release_gpu(hdr + 2, e + 1);
+                }
+            }
         }
         // Two warpgroups alternate tiles: group g drains TMEM accumulator g, so
         // each group has two tiles' time for its chain of TMEM reads,
@@ -1413,7 +1435,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 if (lane == 0) mbar_arrive(bar_sspf0 + 8u * slot);
             }
         } else if (warp == Cfg::SUMSQ_WARP0 + 1) {
-            int* const xbank = args.xcnt + XCH_CNT0 + (gx_epoch(nullptr) & 1) * args.xbank;
+            int* const xbank = args.xcnt + XCH_CNT0 + (gx_epoch() & 1) * args.xbank;
             for (int lt = 0; lt < count; ++lt) {
                 int m, n, row0, rows;
                 sched.tile(lt, m, n, row0, rows);
@@ -1490,18 +1512,6 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     // ---- teardown
     tc_fence_before();
     __syncthreads();
-    if (GLOBALX && threadIdx.x == 0) {
-        // Every CTA counts itself out; the last one resets the count, records
-        // how many counters this launch used (the next launch clears them)
-        // and advances the epoch.
-        int* const hdr = args.xcnt;
-        const int e = ld_acquire_gpu(hdr + 2);
-        if (atom_acq_rel_gpu_add(hdr, 1) == static_cast<int>(gridDim.x) - 1) {
-            hdr[0] = 0;
-            hdr[3] = args.m_tiles;
-            st_release_gpu(hdr + 2, e + 1);
-        }
-    }
     if (CLUSTERED || PAIR) {
         // No CTA leaves while a peer may still write into its shared memory
         // (or, in a pair, its TMEM).

@@ -245,6 +245,12 @@ __device__ __forceinline__ bool gwait_geq(const WaitGuard& g, const int* p, int 
     return state == 1;
 }
 
+// Named barrier `id` (1..15) among `nthreads` threads (whole warps) of the
+// CTA; orders their shared-memory accesses like __syncthreads.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------------ programmatic dependent launch
 // Blocks until every grid this one depends on has completed and its memory is
 // visible (a no-op when the launch has no programmatic dependency).
