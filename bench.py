@@ -797,7 +797,8 @@ def config_table(nf, dev, stream, hbm_gbs, bf16_tf):
 
 
 # ---------------------------------------------------------------- main
-def main(argv=None):
+def build_parser() -> argparse.ArgumentParser:
+    """The command line (also used to check the commands quoted in profiles/)."""
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -832,6 +833,11 @@ def main(argv=None):
     ap.add_argument("--gemm-pair", default="auto", choices=["auto", "never"],
                     help="never: no CTA pairs (nf_set_gemm_pair(1)); for profilers that cannot re-issue a "
                          "cooperative launch of clusters")
+    return ap
+
+
+def main(argv=None):
+    ap = build_parser()
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -58,6 +58,13 @@ def source_hash(names=None) -> str:
 # profile of one of them stays valid while these are unchanged.
 GEMM_SOURCES = ("nf_api.cu", "nf_gemm_post_ln.cu", "nf_gemm_post_rms.cu", "nf_gemm_pre.cu", "nf_gemm_plain.cu",
                 "nf_gemm_kernel.cuh", "nf_gemm_wide.cuh", "nf_internal.h", "nf_ptx.cuh", "nf.h")
+# ... and of the backward, residual and transposed-operand GEMMs (their
+# profiles), the row-norm kernels, and the FlashNormAttention kernel.
+GEMM_EXTRA_SOURCES = GEMM_SOURCES + ("nf_gemm_bwd_ln.cu", "nf_gemm_bwd_rms.cu", "nf_gemm_res_ln.cu",
+                                     "nf_gemm_res_rms.cu", "nf_gemm_trans_plain.cu", "nf_gemm_trans_bwd.cu",
+                                     "nf_splitk.cu")
+NORM_SOURCES = ("nf_api.cu", "nf_norm.cu", "nf_internal.h", "nf_ptx.cuh", "nf.h")
+FNA_SOURCES = ("nf_api.cu", "nf_flashnorm.cu", "nf_internal.h", "nf_ptx.cuh", "nf.h")
 
 
 def build(force: bool = False, extra_flags=(), verbose: bool = False) -> str:
