@@ -496,8 +496,9 @@ def set_postnorm_exchange(mode: int) -> None:
 
 
 def reserve_scratch(max_rows: int, max_cols: int, stream=None) -> None:
-    """Size the stream's scratch (post-norm exchange, split-K workspace) for
-    shapes up to max_rows x max_cols; later calls within it allocate nothing."""
+    """Size the stream's scratch (exchange buffer, split-K workspace) for
+    post-norm shapes up to max_rows x max_cols and Lazy Pre-Norm calls of up to
+    max_rows rows; later calls within it allocate nothing."""
     _check(lib().nf_reserve_scratch(int(max_rows), int(max_cols), _stream(stream)), "nf_reserve_scratch")
 
 

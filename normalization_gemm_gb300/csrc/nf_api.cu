@@ -1193,12 +1193,14 @@ nf_status nf_reserve_scratch(int64_t max_rows, int64_t max_cols, nf_stream strea
     nf_status st = device_state(&d);
     if (st != NF_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (max_rows > 0 && max_cols > 256) {
+    if (max_rows > 0) {
+        // Post-norm rows wider than one tile exchange per column tile; the
+        // pre-norm's split sums of squares need one column tile's worth.
         int* cnt = nullptr;
         int32_t bank = 0;
         float2* stats = nullptr;
         const int m_tiles = static_cast<int>((max_rows + TILE_M - 1) / TILE_M);
-        const int n_tiles = static_cast<int>((max_cols + 255) / 256);
+        const int n_tiles = max_cols > 256 ? static_cast<int>((max_cols + 255) / 256) : 1;
         if ((st = xch_scratch(s, m_tiles, n_tiles, &cnt, &bank, &stats)) != NF_OK) return st;
     }
     float* ws = nullptr;

@@ -105,3 +105,42 @@ def test_reserve_then_capture(dev, orc):
         assert torch.equal(y2, want_sk)
     rows = nf_inputs.sample_rows(M, 64, seed=3)
     assert_close(to_f64(y)[rows], orc.gemm_postnorm_ln(inp["X"], inp["W"], 1e-5, rows=rows)[0], "reserved + graph")
+
+
+def test_prenorm_split_scratch_on_a_busy_stream_and_reserved(dev, orc):
+    """The Lazy Pre-Norm with split sums of squares keeps its gathered sums in
+    the same per-stream exchange scratch: its first call on a fresh, busy
+    stream sets the scratch up without waiting for the stream, and after
+    nf_reserve_scratch (rows only; any N) a graph of split calls captures and
+    replays to the eager bits."""
+    import torch
+    M, K, N = 1152, 2048, 2048
+    assert nf.plan_gemm(1, M, N, K, 148)["exchange"] == nf.XCH_GLOBAL
+    inp = nf_inputs.make_inputs(M, K, N, seed=88, x_dist="row_scaled")
+    X, W = to_dev(inp["X"], dev), to_dev(inp["W"], dev)
+    want = nf.gemm_prenorm_rms(X, W, 1e-6)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    y = torch.empty_like(want)
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(400_000_000)
+        nf.gemm_prenorm_rms(X, W, 1e-6, out=y, stream=s)
+        ev = torch.cuda.Event()
+        ev.record(s)
+    assert not ev.query(), "the split pre-norm call waited for the stream"
+    torch.cuda.synchronize()
+    assert torch.equal(y, want)
+    rows = nf_inputs.sample_rows(M, 64, seed=9)
+    assert_close(to_f64(y)[rows], orc.gemm_prenorm_rms(inp["X"], inp["W"], 1e-6, rows=rows)[0],
+                 "split pre-RMS on a busy stream")
+    s2 = torch.cuda.Stream()
+    nf.reserve_scratch(M, 8, stream=s2)
+    y2 = torch.empty_like(want)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s2):
+        nf.gemm_prenorm_rms(X, W, 1e-6, out=y2, stream=s2)
+    for _ in range(2):
+        y2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y2, want)
