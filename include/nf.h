@@ -471,13 +471,16 @@ const char* nf_last_error(void);
 typedef struct nf_plan {
     int32_t tile_m, tile_n, tile_k; /* CTA tile                            */
     int32_t stages;                 /* shared-memory ring depth            */
-    int32_t cluster;                /* CTAs per cluster along N            */
+    int32_t cluster;                /* CTAs per cluster: along N for a row
+                                       cluster, 2 along M for a CTA pair    */
     int32_t grid;                   /* persistent CTAs                      */
     int32_t threads;                /* threads per CTA                     */
     int32_t smem_bytes;             /* dynamic shared memory per CTA       */
     int32_t tmem_cols;              /* tensor-memory columns per CTA       */
     int32_t tiles;                  /* output tiles (M/tile_m x N/tile_n)  */
-    int32_t exchange;               /* 0 none, NF_XCH_CLUSTER, NF_XCH_GLOBAL */
+    int32_t exchange;               /* 0 none, NF_XCH_CLUSTER, NF_XCH_GLOBAL
+                                       (pre-norm: the split row sums of
+                                       squares gathered through L2)        */
     int32_t splitk;                 /* contraction slices (plain GEMM; 1 = none) */
     int32_t split_tiles;            /* tiles split over the contraction (the last ones) */
 } nf_plan;
