@@ -24,8 +24,8 @@
  *              stream): post-norm rows wider than 256 columns exchanged
  *              through L2 (the default, see nf_set_postnorm_exchange) use
  *              about 8 * M * ceil(N / 256) bytes, and Lazy Pre-Norm GEMMs
- *              with split row sums of squares (nf_set_prenorm_split) share
- *              that buffer, needing 8 * M bytes of it; GEMMs split over the
+ *              with split row sums of squares (nf_set_prenorm_split) add
+ *              8 * M bytes of their own to that buffer; GEMMs split over the
  *              contraction (nf_set_gemm_splitk) use SMs * 128 KB.  Rule: no
  *              compute call ever synchronizes the host with the device.  A
  *              call that finds its stream's buffer missing or too small

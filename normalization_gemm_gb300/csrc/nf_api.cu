@@ -117,8 +117,12 @@ struct XScratch {
     size_t bytes = 0;
     int64_t bank_ints = 0;
     int64_t stats_bytes = 0;
+    int64_t tag_bytes = 0;  // the pre-norm's tagged row sums (written by no other kernel)
     int* cnt() const { return reinterpret_cast<int*>(ptr); }
     float2* stats() const { return reinterpret_cast<float2*>(ptr + stats_offset(bank_ints)); }
+    unsigned long long* tags() const {
+        return reinterpret_cast<unsigned long long*>(ptr + stats_offset(bank_ints) + stats_bytes);
+    }
     static int64_t stats_offset(int64_t bank_ints) { return ((XCH_CNT0 + 2 * bank_ints) * 4 + 255) / 256 * 256; }
 };
 constexpr int kMaxScratch = 64;
@@ -512,37 +516,42 @@ nf_status blocks_per_sm(DeviceState* d, const GemmVariant* v, int* out) {
 // The stream's global-exchange scratch for m_tiles x n_tiles tiles.  Set up
 // (or replaced by a larger one) in stream order, without synchronizing the
 // host; refused while the stream is being captured into a graph.
-nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, int32_t* bank, float2** stats) {
+nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, int32_t* bank, float2** stats,
+                      int64_t tag_rows = 0, unsigned long long** tags = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
     const int64_t need_bank = xch_bank_ints(m_tiles), need_stats = xch_stats_bytes(m_tiles, n_tiles);
+    const int64_t need_tags = tag_rows * 8;
     std::lock_guard<std::mutex> lk(g_mu);
     XScratch* x = nullptr;
     for (int i = 0; i < g_xs_n; ++i)
         if (g_xs[i].dev == dev && g_xs[i].stream == stream) x = &g_xs[i];
-    if (x && x->bank_ints >= need_bank && x->stats_bytes >= need_stats) {
+    if (x && x->bank_ints >= need_bank && x->stats_bytes >= need_stats && x->tag_bytes >= need_tags) {
         *cnt = x->cnt();
         *bank = static_cast<int32_t>(x->bank_ints);
         *stats = x->stats();
+        if (tags) *tags = x->tags();
         return NF_OK;
     }
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
     if (cs != cudaStreamCaptureStatusNone)
         return fail(NF_ERR_INVALID_ARG,
-                    "post-norm exchange scratch is set up on the first call per stream (and enlarged for larger "
+                    "exchange scratch is set up on the first call per stream (and enlarged for larger "
                     "shapes): make that call, or nf_reserve_scratch, before capturing the stream");
-    if (!x && g_xs_n == kMaxScratch) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many streams with post-norm scratch");
-    int64_t bank_ints = need_bank, stats_bytes = need_stats;
+    if (!x && g_xs_n == kMaxScratch) return fail(NF_ERR_UNSUPPORTED_SHAPE, "too many streams with exchange scratch");
+    int64_t bank_ints = need_bank, stats_bytes = need_stats, tag_bytes = need_tags;
     if (x) {
         bank_ints = bank_ints > x->bank_ints ? bank_ints : x->bank_ints;
         stats_bytes = stats_bytes > x->stats_bytes ? stats_bytes : x->stats_bytes;
+        tag_bytes = tag_bytes > x->tag_bytes ? tag_bytes : x->tag_bytes;
     }
-    // Round both regions up so that modest growth reuses the buffer.
+    // Round every region up so that modest growth reuses the buffer.
     bank_ints = (bank_ints + 4095) / 4096 * 4096;
     stats_bytes = (stats_bytes + (1 << 20) - 1) >> 20 << 20;
-    const size_t bytes = static_cast<size_t>(XScratch::stats_offset(bank_ints) + stats_bytes);
+    tag_bytes = (tag_bytes + (1 << 20) - 1) >> 20 << 20;
+    const size_t bytes = static_cast<size_t>(XScratch::stats_offset(bank_ints) + stats_bytes + tag_bytes);
     void* ptr = nullptr;
     if ((e = cudaMallocAsync(&ptr, bytes, stream)) != cudaSuccess) return fail_cuda(e, "cudaMallocAsync(exchange scratch)");
     if ((e = cudaMemsetAsync(ptr, 0, bytes, stream)) != cudaSuccess) {
@@ -559,9 +568,11 @@ nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, 
     x->bytes = bytes;
     x->bank_ints = bank_ints;
     x->stats_bytes = stats_bytes;
+    x->tag_bytes = tag_bytes;
     *cnt = x->cnt();
     *bank = static_cast<int32_t>(x->bank_ints);
     *stats = x->stats();
+    if (tags) *tags = x->tags();
     return NF_OK;
 }
 
@@ -708,6 +719,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.xcnt = nullptr;
     a.xbank = 0;
     a.xstats = nullptr;
+    a.sstag = nullptr;
     a.splitk = p.splitk;
     a.sk_base = p.sk_base;
     a.sk_tiles = p.sk_tiles;
@@ -718,9 +730,10 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
 
     int grid = 0;
     // Exchange scratch: post-norm partials of every (row tile, column tile);
-    // the pre-norm's split sums of squares, one float per row (the size of a
-    // single column tile's partials, which the scratch holds in any case).
-    const int xnt = op == OP_PRE ? 1 : p.n_tiles;
+    // the pre-norm's split sums of squares use only the counter header (for
+    // the launch epoch) and their own region of tagged words, one per row.
+    const int xnt = op == OP_PRE ? 0 : p.n_tiles;
+    const int64_t xtag_rows = op == OP_PRE ? static_cast<int64_t>(p.m_tiles) * TILE_M : 0;
     a.units = p.m_tiles * p.n_tiles;
     a.split_base = a.units;
     if (p.pair) {
@@ -746,7 +759,8 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
                 a.xcnt = reinterpret_cast<int*>(base);
                 a.xbank = static_cast<int32_t>(kNoAllocBankInts);
                 a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
-            } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
+            } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats, xtag_rows,
+                                         &a.sstag)) != NF_OK) {
                 return st;
             }
         }
@@ -773,7 +787,8 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
             a.xcnt = reinterpret_cast<int*>(base);
             a.xbank = static_cast<int32_t>(kNoAllocBankInts);
             a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
-        } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats)) != NF_OK) {
+        } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats, xtag_rows,
+                                     &a.sstag)) != NF_OK) {
             return st;
         }
     } else if (p.splitk > 1) {
@@ -1195,13 +1210,16 @@ nf_status nf_reserve_scratch(int64_t max_rows, int64_t max_cols, nf_stream strea
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_rows > 0) {
         // Post-norm rows wider than one tile exchange per column tile; the
-        // pre-norm's split sums of squares need one column tile's worth.
+        // pre-norm's split sums of squares need a tagged word per row.
         int* cnt = nullptr;
         int32_t bank = 0;
         float2* stats = nullptr;
         const int m_tiles = static_cast<int>((max_rows + TILE_M - 1) / TILE_M);
-        const int n_tiles = max_cols > 256 ? static_cast<int>((max_cols + 255) / 256) : 1;
-        if ((st = xch_scratch(s, m_tiles, n_tiles, &cnt, &bank, &stats)) != NF_OK) return st;
+        const int n_tiles = max_cols > 256 ? static_cast<int>((max_cols + 255) / 256) : 0;
+        unsigned long long* tags = nullptr;
+        if ((st = xch_scratch(s, m_tiles, n_tiles, &cnt, &bank, &stats, static_cast<int64_t>(m_tiles) * TILE_M,
+                              &tags)) != NF_OK)
+            return st;
     }
     float* ws = nullptr;
     return splitk_scratch(s, d->sm_count, &ws);

@@ -138,6 +138,26 @@ __device__ __forceinline__ void tmem_load_seg(uint32_t taddr, uint32_t (&v)[NC][
     for (int c = 1; c < NC; ++c) reg_fence(v[c]);
 }
 
+// Bounded per-thread wait for a 64-bit word whose high half is `tag`; the
+// word is returned in `w`.  False when the CTA is aborting or the time limit
+// passed (recorded).
+__device__ __forceinline__ bool tagged_wait(const WaitGuard& g, const unsigned long long* p, unsigned long long tag,
+                                            unsigned long long& w, uint32_t site, uint32_t tile) {
+    w = ld_relaxed_gpu_u64(p);
+    if ((w & 0xffffffff00000000ull) == tag) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        w = ld_relaxed_gpu_u64(p);
+        if ((w & 0xffffffff00000000ull) == tag) return true;
+        if (*g.abort_flag) return false;
+        if (globaltimer_ns() - t0 > g.timeout_ns) {
+            record_failure(g, 5u /* NF_ERR_TIMEOUT */, site, tile);
+            return false;
+        }
+    }
+}
+
 // Where the epilogue finds gamma / beta.
 enum AffSrc : int { AFF_NONE = 0, AFF_SMEM = 1 };
 
@@ -415,8 +435,6 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
 
     const uint32_t bar_afff0 = bar_mma_done + 8u;  // [2] global exchange: a group's affine slot filled
     const uint32_t bar_affe0 = bar_afff0 + 16u;    // [2] global exchange: a group's affine slot free
-    const uint32_t bar_sspf0 = bar_afff0;  // [2] pre-norm, split sums: a tile's row sums staged (pre-norm has no affine)
-    const uint32_t bar_sspe0 = bar_affe0;  // [2] pre-norm, split sums: staging slot published, free
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS);
     volatile int* const abort_flag =
         reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 4);
@@ -501,11 +519,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         if (Cfg::kScaleA)
             for (int st = 0; st < STAGES; ++st) mbar_init(bar_xf0 + 8u * st, 128);  // the transform threads
         for (int g = 0; g < 2; ++g) {
-            // post-norm: one arrival per warp of the group; pre-norm (split
-            // sums of squares): one from the summing warp (ssp_full), one from
-            // the publishing warp (ssp_empty)
-            mbar_init(bar_afff0 + 8u * g, Cfg::kPre ? 1 : 4);
-            mbar_init(bar_affe0 + 8u * g, Cfg::kPre ? 1 : 4);
+            mbar_init(bar_afff0 + 8u * g, 4);  // one arrival per warp of the group
+            mbar_init(bar_affe0 + 8u * g, 4);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -565,7 +580,7 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
     // thread's last use.)
     // One thread of the first epilogue warp reads E (and the last launch's
     // counter count) into shared memory; the epilogue warps and the
-    // pre-norm's publishing warp meet at a named barrier and take it from
+    // pre-norm's summing warp meet at a named barrier and take it from
     // there.  The CTA counts itself in after that barrier, so no warp of a
     // counted CTA reads E from L2 after the last CTA may have advanced it.
     constexpr int XWARPS = EPI_WARPS + (Cfg::kPre ? 1 : 0);  // warps meeting at named barrier 1
@@ -785,8 +800,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         // the next launch counts there).  The epilogue warps do it while the
         // first tile's main loop runs.
         int* xbank = nullptr;
+        unsigned long long xtag = 0;  // pre-norm, split sums: this launch's tag in a word's high half
         if (GLOBALX) {
             const int e = gx_epoch();
+            xtag = static_cast<unsigned long long>(static_cast<uint32_t>(e) + 1u) << 32;
             const int prev_ints = epoch_sm[1];
             xbank = args.xcnt + XCH_CNT0 + (e & 1) * args.xbank;
             int* const other = args.xcnt + XCH_CNT0 + ((e + 1) & 1) * args.xbank;
@@ -904,12 +921,15 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 float ss = 0.0f;
                 if (GLOBALX) {
                     // The row's sum of squares, summed by one of the row tile's
-                    // n_tiles tiles and published through L2 once every one of
-                    // them has counted.  (A CTA pair's second CTA past M has no
+                    // n_tiles tiles: poll the row's word until it carries this
+                    // launch's tag.  (A CTA pair's second CTA past M has no
                     // rows: nothing to wait for.)
                     if (m < args.m_tiles) {
-                        if (!gwait_geq(guard, xbank + m * 4, args.n_tiles, SITE_EPI_GXCH, lt)) break;
-                        ss = __ldcg(reinterpret_cast<const float*>(args.xstats) + static_cast<size_t>(m) * TILE_M + row);
+                        unsigned long long wv = 0;
+                        ok = tagged_wait(guard, args.sstag + static_cast<size_t>(m) * TILE_M + row, xtag, wv,
+                                         SITE_EPI_GXCH, lt);
+                        if (!__all_sync(0xffffffffu, ok)) break;
+                        ss = __uint_as_float(static_cast<uint32_t>(wv));
                     }
                 } else {
                     ok = mbar_wait(guard, bar_ssf0 + 8u * b, aph, SITE_EPI_SS_FULL, lt);
@@ -1328,17 +1348,20 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         // bandwidth the tensor cores need): tile (m, n) sums rows
         // n R .. n R + R - 1, R = ceil(128 / n_tiles), over the whole
         // contraction, from the same stages the MMA reads -- one warp reading
-        // 1/n_tiles of each A stage.  A second warp publishes the R sums
-        // through L2 and counts them on row tile m's counter (its release waits
-        // for the stores to land; the summing warp, whose arrivals free the
-        // ring's stages, never waits on L2).  Every tile of row tile m waits in
-        // its epilogue for all n_tiles counts.  Deadlock freedom is that of the
+        // 1/n_tiles of each A stage -- and stores each sum to L2 as one 64-bit
+        // word carrying this launch's tag (plain stores: the warp, whose
+        // arrivals free the ring's stages, never waits on L2).  The epilogue of
+        // every tile of row tile m polls its row's word until it carries the
+        // tag: one L2 round trip, with no counter, fence or second read (a
+        // counter and a release fence took ~2.8 us from the accumulator's
+        // completion to the sums in hand).  Deadlock freedom is that of the
         // post-norm exchange: a tile's publication needs only its own main
         // loop, which needs the epilogue of the CTA's tile two before it, which
         // lies in an earlier row tile (tiles in order, 2 G >= n_tiles).
         const int nt = args.n_tiles;  // >= 2 (checked at entry): R <= 64
         const int R = (TILE_M + nt - 1) / nt;
         if (warp == Cfg::SUMSQ_WARP0) {
+            const unsigned long long tag = static_cast<unsigned long long>(static_cast<uint32_t>(gx_epoch()) + 1u) << 32;
             int s = 0;
             uint32_t ph = 0;
             for (int lt = 0; lt < count; ++lt) {
@@ -1421,37 +1444,17 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                     acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
                     acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 4);
                 }
-                // Staging slot lt & 1 is free once tile lt - 2's sums are published.
-                const int slot = lt & 1;
-                const uint32_t sph = static_cast<uint32_t>(lt >> 1) & 1u;
-                if (!__all_sync(0xffffffffu, mbar_wait(guard, bar_sspe0 + 8u * slot, sph ^ 1u, SITE_SS_ACC_EMPTY, lt)))
-                    break;
+                // One tagged word per row (a CTA pair's second CTA past M has
+                // no rows: nothing to publish).
+                if (m < args.m_tiles) {
+                    unsigned long long* const dst = args.sstag + static_cast<size_t>(m) * TILE_M + r0;
 #pragma unroll
-                for (int i = 0; i < SPLIT_SS_ITERS; ++i) {
-                    const int r = (lane >> 3) + 4 * i;
-                    if ((lane & 7) == 0 && 8 * r < nchunk) ss_buf[slot * TILE_M + r] = acc[i];
+                    for (int i = 0; i < SPLIT_SS_ITERS; ++i) {
+                        const int r = (lane >> 3) + 4 * i;
+                        if ((lane & 7) == 0 && 8 * r < nchunk)
+                            st_relaxed_gpu_u64(dst + r, tag | __float_as_uint(acc[i]));
+                    }
                 }
-                __syncwarp();  // the warp's writes precede lane 0's arrival
-                if (lane == 0) mbar_arrive(bar_sspf0 + 8u * slot);
-            }
-        } else if (warp == Cfg::SUMSQ_WARP0 + 1) {
-            int* const xbank = args.xcnt + XCH_CNT0 + (gx_epoch() & 1) * args.xbank;
-            for (int lt = 0; lt < count; ++lt) {
-                int m, n, row0, rows;
-                sched.tile(lt, m, n, row0, rows);
-                const int r0 = n * R;
-                const int nrow = max(0, min(R, TILE_M - r0));
-                const int slot = lt & 1;
-                const uint32_t sph = static_cast<uint32_t>(lt >> 1) & 1u;
-                if (!__all_sync(0xffffffffu, mbar_wait(guard, bar_sspf0 + 8u * slot, sph, SITE_SS_FULL, lt))) break;
-                if (m < args.m_tiles) {  // (a CTA pair's second CTA past M: no rows, nothing to publish)
-                    float* const dst = reinterpret_cast<float*>(args.xstats) + static_cast<size_t>(m) * TILE_M + r0;
-                    for (int r = lane; r < nrow; r += 32) __stcg(dst + r, ss_buf[slot * TILE_M + r]);
-                    __syncwarp();  // the warp's stores precede lane 0's release
-                    if (lane == 0) red_release_gpu_add(xbank + m * 4, 1);
-                }
-                __syncwarp();  // the warp's reads of the slot precede lane 0's arrival
-                if (lane == 0) mbar_arrive(bar_sspe0 + 8u * slot);
             }
         }
     } else if (Cfg::kPre && warp >= Cfg::SUMSQ_WARP0) {

@@ -55,9 +55,13 @@ enum Exchange : int {
 //          used: no counter is ever reset while it may be read, and a launch
 //          that gave up part-way leaves nothing behind.
 //   xstats float2 partial (mean, M2) or (sum of squares, 0) per
-//          (row tile, column tile, tile row); for the pre-norm's split sums
-//          of squares, one float per row (row tile m's 128 at m * 128), counted
-//          on the first of the row tile's four counters
+//          (row tile, column tile, tile row)
+//   tags   (pre-norm, split sums of squares) one 64-bit word per row: the
+//          launch's tag E + 1 in the high half, the row's sum of squares in
+//          the low half, stored and polled as one single-copy-atomic word.
+//          Only the pre-norm writes this region and E never repeats on one
+//          scratch buffer, so a word carrying the current tag is this
+//          launch's and needs no counter, fence or clearing.
 constexpr int XCH_CNT0 = 64;  // banks start 256 bytes in
 __host__ __device__ inline int64_t xch_bank_ints(int m_tiles) { return static_cast<int64_t>(m_tiles) * 4; }
 __host__ __device__ inline int64_t xch_stats_bytes(int m_tiles, int n_tiles) {
@@ -186,6 +190,8 @@ struct GemmArgs {
     int32_t sk_base;        // splitk > 1: first split unit (= first split tile); units before it are whole tiles
     int32_t sk_tiles;       // splitk > 1: split tiles (sk_base .. sk_base + sk_tiles - 1), each in splitk units
     float* ws;              // splitk > 1: fp32 partial tiles, [splitk][sk_tiles][TILE_M][TILE_N]
+    unsigned long long* sstag;  // pre-norm, split sums of squares: one word per row, (launch tag << 32) | bits
+                                // of the row's sum of squares, >= m_tiles * 128 words
     uint16_t* xhat_out;     // RMS backward (optional): bf16(Z * rstd), M x N, the rebuilt rmsnorm input
     const uint16_t* resid;  // post-norm (optional): R, M x N bf16, added to X W before the statistics
     uint16_t* h_out;        // with resid (optional): bf16(X W + R), M x N, the updated residual stream

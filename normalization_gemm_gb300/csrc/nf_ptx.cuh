@@ -187,6 +187,17 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
     return v;
 }
 
+// 64-bit GPU-scope relaxed store and load of one aligned word: each is
+// single-copy atomic, so a reader sees the whole old word or the whole new one.
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // GPU-scope acquire-release fence: after a relaxed load that observed a
 // release, makes the releasing side's earlier writes visible (acquire pattern).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }

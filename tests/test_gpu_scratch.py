@@ -59,6 +59,12 @@ def test_compute_calls_never_synchronize(dev, orc):
     sk = nf_inputs.make_inputs(SPLITK[0], SPLITK[1], SPLITK[2], seed=5)
     skx, skw = to_dev(sk["X"], dev), to_dev(sk["W"], dev)
     sky = torch.empty((SPLITK[0], SPLITK[2]), dtype=torch.bfloat16, device=dev)
+    # Load and set up the kernels first, on the default stream (the first use
+    # of a kernel loads its code, which is not what this test is about); the
+    # fresh stream's scratch is untouched.
+    for (inp, X, W), y in zip(cases, ys):
+        nf.gemm_postnorm_ln(X, W, 1e-5, out=y)
+    nf.gemm_plain(skx, skw, out=sky)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         torch.cuda._sleep(400_000_000)  # about 0.2 s of spinning at 2 GHz
