@@ -691,6 +691,15 @@ def oracle_sample(w, ops, inp, budget_s, rows_cap):
     return done * len(ops) * 2 * rows_per_pass * w.N * w.K, sec, rows_per_pass, orc.max_threads()
 
 
+def workload_config(w, ops, world, rows_per_gpu):
+    """The `config` keys that name the workload; both arms print them alike."""
+    return {"workload": w.name, "ops": list(ops), "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
+            "gamma": bool(w.gamma), "beta": bool(w.beta),
+            "step": " + ".join(KERNEL_OF_OP[o] for o in ops) + " on one batch",
+            "per_gpu_rows": rows_per_gpu,
+            "parallelism": f"rows x{world} (shard of one seeded problem), no collective"}
+
+
 def reference_arm(args):
     """--impl reference: the fp64 CPU oracle on the headline's step (every op
     of the workload on the same rows), timed as the reference arm."""
@@ -727,8 +736,7 @@ def reference_arm(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "ops": list(ops), "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
-                   "rows_per_step": rows_per_step},
+        "config": workload_config(w, ops, args.gpus, w.M),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.max_threads(), "kind": "oracle",
                          "sample": f"{rows_per_step} of {w.M} rows per step, every op of the step on them "
                                    f"(whole rows, fp64 oracle)"},
@@ -992,11 +1000,7 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "ops": list(ops), "M": w.M, "K": w.K, "N": w.N, "eps": w.eps,
-                   "gamma": bool(w.gamma), "beta": bool(w.beta),
-                   "step": " + ".join(KERNEL_OF_OP[o] for o in ops) + " on one batch",
-                   "per_gpu_rows": rows_here, "parallelism": f"rows x{world} (shard of one seeded problem), "
-                                                            f"no collective",
+        "config": {**workload_config(w, ops, world, rows_here),
                    "l2": f"rotating {nsets} buffer sets of {set_bytes / 2**20:.0f} MiB (> 3x L2 between reuses)",
                    "launch": f"one CUDA graph of the {args.steps} steps",
                    **({"gemm_pair": "never"} if args.gemm_pair == "never" else {})},
