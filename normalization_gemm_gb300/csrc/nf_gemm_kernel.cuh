@@ -435,6 +435,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
 
     const uint32_t bar_afff0 = bar_mma_done + 8u;  // [2] global exchange: a group's affine slot filled
     const uint32_t bar_affe0 = bar_afff0 + 16u;    // [2] global exchange: a group's affine slot free
+    const uint32_t bar_xpub0 = sBar + 320u;        // [2] global exchange: a group's 4 warps stored their partials
+    const uint32_t bar_xrdy0 = sBar + 336u;        // [2] global exchange: the row tile's partials may be read
     uint32_t* const tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS);
     volatile int* const abort_flag =
         reinterpret_cast<volatile int*>(base_ptr + Cfg::OFF_BAR + 8 * Cfg::NSLOTS + 4);
@@ -521,6 +523,10 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         for (int g = 0; g < 2; ++g) {
             mbar_init(bar_afff0 + 8u * g, 4);  // one arrival per warp of the group
             mbar_init(bar_affe0 + 8u * g, 4);
+            if (GLOBALX) {
+                mbar_init(bar_xpub0 + 8u * g, 4);
+                mbar_init(bar_xrdy0 + 8u * g, 1);
+            }
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -827,6 +833,43 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                 }
             }
         }
+        // The global exchange of one tile's row partials (pa, pb), for the
+        // group's four warps together: each stores its rows' partials for
+        // column tile n; once all four have (xpub, whose arrivals release
+        // those stores at CTA scope), the group's first warp counts the tile
+        // with one GPU-scope release, waits until all n_tiles column tiles of
+        // row tile m have counted, acquires, and lets the four read the
+        // row tile's partials (xrdy).  One fence pair per tile and group: a
+        // pair per warp measured 3.7 us slower at 16384 x 1024 x 2048, each
+        // GPU-scope fence holding back the SM's operand loads.  A CTA pair's
+        // second CTA past M (m >= m_tiles) has no rows: it keeps the group's
+        // barrier phases but stores, counts and reads nothing.  False (for
+        // the whole warp) when a wait gave up.
+        auto xch_global = [&](int m, int n, int qtr, int row, int grp, uint32_t jph, float pa, float pb,
+                              float2 (&pp)[MAX_CLUSTER], int lt) -> bool {
+            const int nt = args.n_tiles;
+            const bool real = m < args.m_tiles;  // (the same for the whole CTA)
+            float2* const xst = args.xstats + static_cast<size_t>(real ? m : 0) * nt * TILE_M + row;
+            if (real) __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_xpub0 + 8u * grp);
+            if (qtr == 0) {
+                bool ok = __all_sync(0xffffffffu, mbar_wait(guard, bar_xpub0 + 8u * grp, jph, SITE_EPI_GXCH, lt));
+                if (ok && real) {
+                    int* const cnt = xbank + m * 4;
+                    if (lane == 0) red_release_gpu_add(cnt, 1);
+                    ok = gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt);
+                }
+                if (!ok) return false;  // (the other warps' xrdy wait then sees the abort flag)
+                if (lane == 0) mbar_arrive(bar_xrdy0 + 8u * grp);
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(guard, bar_xrdy0 + 8u * grp, jph, SITE_EPI_GXCH, lt)))
+                return false;
+#pragma unroll
+            for (int p = 0; p < MAX_CLUSTER; ++p)
+                pp[p] = (real && p < nt) ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
+            return true;
+        };
         // Two warpgroups alternate tiles: group g drains TMEM accumulator g, so
         // each group has two tiles' time for its chain of TMEM reads,
         // statistics, conversion and stores.  Warp (g, qtr) owns TMEM lane
@@ -996,23 +1039,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                         s2 += recv[p * TILE_M * 2 + 1];
                     }
                 } else if (GLOBALX) {
-                    const int nt = args.n_tiles;
-                    // A CTA pair's second CTA past M (an odd number of row
-                    // tiles) has no rows: it neither publishes nor waits, and
-                    // touches no counter or partial beyond the row tiles.
-                    const bool real = m < args.m_tiles;
-                    float2* const xst = args.xstats + static_cast<size_t>(real ? m : 0) * nt * TILE_M + row;
-                    if (real) {
-                        int* const cnt = xbank + m * 4 + qtr;
-                        __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
-                        __syncwarp();  // the warp's stores precede lane 0's release
-                        if (lane == 0) red_release_gpu_add(cnt, 1);
-                        if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
-                    }
                     float2 pp[MAX_CLUSTER];
-#pragma unroll
-                    for (int p = 0; p < MAX_CLUSTER; ++p)
-                        pp[p] = (real && p < nt) ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
+                    if (!xch_global(m, n, qtr, row, grp, jph, pa, pb, pp, lt)) break;
                     s1 = s2 = 0.0f;
 #pragma unroll
                     for (int p = 0; p < MAX_CLUSTER; ++p) {
@@ -1132,25 +1160,12 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
                         for (int p = 0; p < args.cluster; ++p) sq += recv[p * TILE_M * 2];
                     }
                 } else if (GLOBALX) {
-                    // -- exchange through L2: publish this quarter's partials
-                    //    for column tile n, count the publication, wait until
-                    //    all n_tiles column tiles of row tile m have counted,
-                    //    read their partials.
+                    // -- exchange through L2: this row's partials for column
+                    //    tile n out, those of all n_tiles column tiles of row
+                    //    tile m in (xch_global above).
                     const int nt = args.n_tiles;
-                    // (a CTA pair's second CTA past M: no rows, no exchange)
-                    const bool real = m < args.m_tiles;
-                    float2* const xst = args.xstats + static_cast<size_t>(real ? m : 0) * nt * TILE_M + row;
-                    if (real) {
-                        int* const cnt = xbank + m * 4 + qtr;
-                        __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
-                        __syncwarp();  // the warp's stores precede lane 0's release
-                        if (lane == 0) red_release_gpu_add(cnt, 1);
-                        if (!gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt)) break;
-                    }
                     float2 pp[MAX_CLUSTER];
-#pragma unroll
-                    for (int p = 0; p < MAX_CLUSTER; ++p)
-                        pp[p] = (real && p < nt) ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
+                    if (!xch_global(m, n, qtr, row, grp, jph, pa, pb, pp, lt)) break;
                     if (Cfg::kLN) {
                         // Chan et al. pairwise merge of (count, mean, M2).
                         float msum = 0.0f;

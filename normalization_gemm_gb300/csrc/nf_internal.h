@@ -49,11 +49,12 @@ enum Exchange : int {
 // regions whose sizes are fixed when the buffer is set up:
 //   xcnt   int: [0] exit count, [2] launch epoch E (the last CTA to leave a
 //          launch advances it), [3] row tiles of that launch; from XCH_CNT0
-//          two banks of xbank ints, one arrival counter per (row tile,
-//          32-row quarter).  Launch E counts in bank E & 1, which the launch
-//          before it cleared, and clears the other bank, which that launch
-//          used: no counter is ever reset while it may be read, and a launch
-//          that gave up part-way leaves nothing behind.
+//          two banks of xbank ints, 4 per row tile, of which the first
+//          counts the row tile's column tiles.  Launch E counts in bank
+//          E & 1, which the launch before it cleared, and clears the other
+//          bank, which that launch used: no counter is ever reset while it
+//          may be read, and a launch that gave up part-way leaves nothing
+//          behind.
 //   xstats float2 partial (mean, M2) or (sum of squares, 0) per
 //          (row tile, column tile, tile row)
 //   tags   (pre-norm, split sums of squares) one 64-bit word per row: the
@@ -129,8 +130,9 @@ struct GemmCfg {
     // A row scaling: each ring stage's 64 rstd values, copied with the stage.
     // (256-column tiles fit four stages at most, narrower ones up to eight.)
     static constexpr int RS_BYTES = kScaleA ? (TILE_N == 256 ? 4 : MAX_STAGES) * TILE_K * 4 : 0;
-    // barriers (+ xformed[8], or a pre-norm pair's ardy[8]) + 4 words
-    static constexpr int BAR_BYTES = (kScaleA || kPair || NACC == 4) ? 320 : 256;
+    // barriers (+ xformed[8], or a pre-norm pair's ardy[8]) + 4 words; the
+    // global exchange adds xpub[2] and xrdy[2] after those
+    static constexpr int BAR_BYTES = XCH == XCH_GLOBAL ? 352 : ((kScaleA || kPair || NACC == 4) ? 320 : 256);
     // The swizzled buffers need a 1 KB aligned base.  Dynamic shared memory
     // starts 1 KB aligned in practice; the global-exchange variant, whose
     // fourth pipeline stage needs the room, relies on that (and checks it at
