@@ -23,7 +23,7 @@
  *              owned by the library, one buffer of each kind per (device,
  *              stream): post-norm rows wider than 256 columns exchanged
  *              through L2 (the default, see nf_set_postnorm_exchange) use
- *              about 8 * M * ceil(N / 256) bytes, and Lazy Pre-Norm GEMMs
+ *              about 16 * M * ceil(N / 256) bytes, and Lazy Pre-Norm GEMMs
  *              with split row sums of squares (nf_set_prenorm_split) add
  *              8 * M bytes of their own to that buffer; GEMMs split over the
  *              contraction (nf_set_gemm_splitk) use SMs * 128 KB.  Rule: no
@@ -250,7 +250,7 @@ nf_status nf_gemm_postnorm_ln(const void* X, const void* W, const void* gamma,
  * memory at any time, on any call.  The blog has no counterpart: this is a
  * deployment variant.  Same arguments, plan, kernels and results as
  * nf_gemm_postnorm_ln.  Where that plan exchanges row statistics through L2,
- * the scratch is a fixed device array inside the library (about 4.1 MiB per
+ * the scratch is a fixed device array inside the library (about 8.1 MiB per
  * device, cleared on the first call on each device) instead of the
  * per-stream buffer.  Limit of that array: ceil(M / 128) * ceil(N / 256)
  * <= 4096 exchange tiles (which implies M <= 2^19), else

@@ -119,7 +119,9 @@ struct XScratch {
     int64_t stats_bytes = 0;
     int64_t tag_bytes = 0;  // the pre-norm's tagged row sums (written by no other kernel)
     int* cnt() const { return reinterpret_cast<int*>(ptr); }
-    float2* stats() const { return reinterpret_cast<float2*>(ptr + stats_offset(bank_ints)); }
+    unsigned long long* stats() const {
+        return reinterpret_cast<unsigned long long*>(ptr + stats_offset(bank_ints));
+    }
     unsigned long long* tags() const {
         return reinterpret_cast<unsigned long long*>(ptr + stats_offset(bank_ints) + stats_bytes);
     }
@@ -131,7 +133,7 @@ constexpr int kMaxScratch = 64;
 // array (header, two counter banks, partial statistics), so that entry point
 // allocates nothing at any time.  Zero when set up on a device.
 constexpr int64_t kNoAllocBankInts = 16384;      // 4 counters per row tile: m_tiles <= 4096
-constexpr int64_t kNoAllocStatsBytes = 4 << 20;  // m_tiles * n_tiles <= 4096 (binds first: n_tiles >= 3)
+constexpr int64_t kNoAllocStatsBytes = 8 << 20;  // m_tiles * n_tiles <= 4096 (binds first: n_tiles >= 3)
 constexpr int64_t kNoAllocStatsOffset = (XCH_CNT0 + 2 * kNoAllocBankInts) * 4;
 constexpr int64_t kNoAllocBytes = kNoAllocStatsOffset + kNoAllocStatsBytes;
 static_assert(kNoAllocStatsOffset % 256 == 0, "statistics region alignment");
@@ -516,7 +518,8 @@ nf_status blocks_per_sm(DeviceState* d, const GemmVariant* v, int* out) {
 // The stream's global-exchange scratch for m_tiles x n_tiles tiles.  Set up
 // (or replaced by a larger one) in stream order, without synchronizing the
 // host; refused while the stream is being captured into a graph.
-nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, int32_t* bank, float2** stats,
+nf_status xch_scratch(cudaStream_t stream, int m_tiles, int n_tiles, int** cnt, int32_t* bank,
+                      unsigned long long** stats,
                       int64_t tag_rows = 0, unsigned long long** tags = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -718,7 +721,7 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
     a.rstd_in = rstd_in;
     a.xcnt = nullptr;
     a.xbank = 0;
-    a.xstats = nullptr;
+    a.xpart = nullptr;
     a.sstag = nullptr;
     a.splitk = p.splitk;
     a.sk_base = p.sk_base;
@@ -758,8 +761,8 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
                 if ((st = noalloc_scratch(stream, &base)) != NF_OK) return st;
                 a.xcnt = reinterpret_cast<int*>(base);
                 a.xbank = static_cast<int32_t>(kNoAllocBankInts);
-                a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
-            } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats, xtag_rows,
+                a.xpart = reinterpret_cast<unsigned long long*>(base + kNoAllocStatsOffset);
+            } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xpart, xtag_rows,
                                          &a.sstag)) != NF_OK) {
                 return st;
             }
@@ -786,8 +789,8 @@ nf_status run_gemm(int op, const void* X, const void* W, const void* gamma, cons
             if ((st = noalloc_scratch(stream, &base)) != NF_OK) return st;
             a.xcnt = reinterpret_cast<int*>(base);
             a.xbank = static_cast<int32_t>(kNoAllocBankInts);
-            a.xstats = reinterpret_cast<float2*>(base + kNoAllocStatsOffset);
-        } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xstats, xtag_rows,
+            a.xpart = reinterpret_cast<unsigned long long*>(base + kNoAllocStatsOffset);
+        } else if ((st = xch_scratch(stream, p.m_tiles, xnt, &a.xcnt, &a.xbank, &a.xpart, xtag_rows,
                                      &a.sstag)) != NF_OK) {
             return st;
         }
@@ -1213,7 +1216,7 @@ nf_status nf_reserve_scratch(int64_t max_rows, int64_t max_cols, nf_stream strea
         // pre-norm's split sums of squares need a tagged word per row.
         int* cnt = nullptr;
         int32_t bank = 0;
-        float2* stats = nullptr;
+        unsigned long long* stats = nullptr;
         const int m_tiles = static_cast<int>((max_rows + TILE_M - 1) / TILE_M);
         const int n_tiles = max_cols > 256 ? static_cast<int>((max_cols + 255) / 256) : 0;
         unsigned long long* tags = nullptr;

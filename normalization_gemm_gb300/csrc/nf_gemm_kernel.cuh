@@ -834,30 +834,38 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             }
         }
         // The global exchange of one tile's row partials (pa, pb), for the
-        // group's four warps together: each stores its rows' partials for
-        // column tile n; once all four have (xpub, whose arrivals release
-        // those stores at CTA scope), the group's first warp counts the tile
-        // with one GPU-scope release, waits until all n_tiles column tiles of
-        // row tile m have counted, acquires, and lets the four read the
-        // row tile's partials (xrdy).  One fence pair per tile and group: a
-        // pair per warp measured 3.7 us slower at 16384 x 1024 x 2048, each
-        // GPU-scope fence holding back the SM's operand loads.  A CTA pair's
-        // second CTA past M (m >= m_tiles) has no rows: it keeps the group's
-        // barrier phases but stores, counts and reads nothing.  False (for
-        // the whole warp) when a wait gave up.
+        // group's four warps together, without a memory fence.  Each thread
+        // stores its row's partials for column tile n as a pair of tagged
+        // words (each carries this launch's tag beside its float, so a reader
+        // can tell by the word itself whether it is current).  Once all four
+        // warps have (xpub), the group's first warp adds one to row tile m's
+        // count and waits, with relaxed loads, until all n_tiles column tiles
+        // have counted; then (xrdy) every thread reads its row's n_tiles
+        // pairs, again while any still carries an older tag.  The count and
+        // the barriers only say when to look.  (A GPU-scope release on the
+        // count and an acquire after it, one pair per warp, measured 3.7 us
+        // slower at 16384 x 1024 x 2048, and one pair per warpgroup still
+        // 3 us: such fences hold back the SM's operand loads.  Every thread
+        // polling the tagged words alone, without the count, measured slower
+        // still: the L2 traffic of the polling threads does the same.)  A
+        // CTA pair's second CTA past M (m >= m_tiles) has no rows: it keeps
+        // the group's barrier phases but stores, counts and reads nothing.
+        // False (for the whole warp) when a wait gave up.
         auto xch_global = [&](int m, int n, int qtr, int row, int grp, uint32_t jph, float pa, float pb,
                               float2 (&pp)[MAX_CLUSTER], int lt) -> bool {
             const int nt = args.n_tiles;
             const bool real = m < args.m_tiles;  // (the same for the whole CTA)
-            float2* const xst = args.xstats + static_cast<size_t>(real ? m : 0) * nt * TILE_M + row;
-            if (real) __stcg(xst + static_cast<size_t>(n) * TILE_M, make_float2(pa, pb));
+            unsigned long long* const w = args.xpart + (static_cast<size_t>(real ? m : 0) * nt * TILE_M + row) * 2;
+            if (real)
+                st_relaxed_gpu_v2_u64(w + static_cast<size_t>(n) * TILE_M * 2, xtag | __float_as_uint(pa),
+                                      xtag | __float_as_uint(pb));
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_xpub0 + 8u * grp);
             if (qtr == 0) {
                 bool ok = __all_sync(0xffffffffu, mbar_wait(guard, bar_xpub0 + 8u * grp, jph, SITE_EPI_GXCH, lt));
                 if (ok && real) {
                     int* const cnt = xbank + m * 4;
-                    if (lane == 0) red_release_gpu_add(cnt, 1);
+                    if (lane == 0) red_relaxed_gpu_add(cnt, 1);
                     ok = gwait_geq(guard, cnt, nt, SITE_EPI_GXCH, lt);
                 }
                 if (!ok) return false;  // (the other warps' xrdy wait then sees the abort flag)
@@ -866,9 +874,30 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(guard, bar_xrdy0 + 8u * grp, jph, SITE_EPI_GXCH, lt)))
                 return false;
 #pragma unroll
-            for (int p = 0; p < MAX_CLUSTER; ++p)
-                pp[p] = (real && p < nt) ? __ldcg(xst + p * TILE_M) : make_float2(0.0f, 0.0f);
-            return true;
+            for (int p = 0; p < MAX_CLUSTER; ++p) pp[p] = make_float2(0.0f, 0.0f);
+            if (!real) return true;
+            constexpr unsigned long long HI = 0xffffffff00000000ull;
+            uint64_t t0 = 0;
+            for (int round = 0;; ++round) {
+                // All nt pairs each round, loaded before any is looked at.
+                uint32_t stale = 0;
+#pragma unroll
+                for (int p = 0; p < MAX_CLUSTER; ++p)
+                    if (p < nt) {
+                        const ulonglong2 v = ld_relaxed_gpu_v2_u64(w + static_cast<size_t>(p) * TILE_M * 2);
+                        stale |= static_cast<uint32_t>(((v.x & HI) != xtag) | ((v.y & HI) != xtag));
+                        pp[p] = make_float2(__uint_as_float(static_cast<uint32_t>(v.x)),
+                                            __uint_as_float(static_cast<uint32_t>(v.y)));
+                    }
+                if (__all_sync(0xffffffffu, stale == 0)) return true;
+                if (round == 0) t0 = globaltimer_ns();
+                __nanosleep(64);
+                if (*guard.abort_flag) return false;
+                if (globaltimer_ns() - t0 > guard.timeout_ns) {
+                    record_failure(guard, 5u /* NF_ERR_TIMEOUT */, SITE_EPI_GXCH, lt);
+                    return false;
+                }
+            }
         };
         // Two warpgroups alternate tiles: group g drains TMEM accumulator g, so
         // each group has two tiles' time for its chain of TMEM reads,

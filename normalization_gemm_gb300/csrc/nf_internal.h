@@ -54,19 +54,22 @@ enum Exchange : int {
 //          E & 1, which the launch before it cleared, and clears the other
 //          bank, which that launch used: no counter is ever reset while it
 //          may be read, and a launch that gave up part-way leaves nothing
-//          behind.
-//   xstats float2 partial (mean, M2) or (sum of squares, 0) per
-//          (row tile, column tile, tile row)
-//   tags   (pre-norm, split sums of squares) one 64-bit word per row: the
-//          launch's tag E + 1 in the high half, the row's sum of squares in
-//          the low half, stored and polled as one single-copy-atomic word.
-//          Only the pre-norm writes this region and E never repeats on one
-//          scratch buffer, so a word carrying the current tag is this
-//          launch's and needs no counter, fence or clearing.
+//          behind.  A count only says when to look: no fence orders it with
+//          the partials, which tell by their tags whether they are current.
+//   xpart  (post-norm and its backward) two 64-bit words per (row tile,
+//          column tile, tile row), 16-byte aligned: the launch's tag E + 1
+//          in each word's high half and one float of the partial -- (mean,
+//          M2), (sum of squares, 0) or the backward's two sums -- in its low
+//          half.
+//   tags   (pre-norm, split sums of squares) one such word per row, the
+//          row's sum of squares in its low half.
+// Each word is stored and read as one single-copy-atomic access, and E
+// never repeats on one scratch buffer, so a word carrying the current tag is
+// this launch's: it needs no fence and no clearing.
 constexpr int XCH_CNT0 = 64;  // banks start 256 bytes in
 __host__ __device__ inline int64_t xch_bank_ints(int m_tiles) { return static_cast<int64_t>(m_tiles) * 4; }
 __host__ __device__ inline int64_t xch_stats_bytes(int m_tiles, int n_tiles) {
-    return static_cast<int64_t>(m_tiles) * n_tiles * 128 * 8;
+    return static_cast<int64_t>(m_tiles) * n_tiles * 128 * 16;
 }
 
 // Operand layouts (GemmCfg OPS bits).  Default: A K-major (X is M x K
@@ -187,7 +190,7 @@ struct GemmArgs {
     const float* rstd_in;   // backward: saved row rstd (M); OPS_A_SCALE: rstd per contraction row (K)
     int* xcnt;              // global exchange only: XCH_CNT0 + 2 * xbank ints
     int32_t xbank;          // ints per counter bank, >= xch_bank_ints(m_tiles)
-    float2* xstats;         // global exchange only: >= xch_stats_bytes(m_tiles, n_tiles)
+    unsigned long long* xpart;  // post-norm global exchange: >= xch_stats_bytes(m_tiles, n_tiles)
     int32_t splitk;         // plain GEMM: contraction slices of the split tiles (1 = none)
     int32_t sk_base;        // splitk > 1: first split unit (= first split tile); units before it are whole tiles
     int32_t sk_tiles;       // splitk > 1: split tiles (sk_base .. sk_base + sk_tiles - 1), each in splitk units

@@ -197,10 +197,17 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned 
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-
-// GPU-scope acquire-release fence: after a relaxed load that observed a
-// release, makes the releasing side's earlier writes visible (acquire pattern).
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Two 64-bit words at a 16-byte aligned address; each word is single-copy
+// atomic on its own (not the pair).
+__device__ __forceinline__ void st_relaxed_gpu_v2_u64(unsigned long long* p, unsigned long long a,
+                                                      unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_relaxed_gpu_v2_u64(const unsigned long long* p) {
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
 
 // GPU-scope release store.
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
@@ -214,14 +221,15 @@ __device__ __forceinline__ int atom_acq_rel_gpu_add(int* p, int v) {
     return old;
 }
 
-// GPU-scope release add (no return value).
-__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// GPU-scope relaxed add (no return value).
+__device__ __forceinline__ void red_relaxed_gpu_add(int* p, int v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Bounded warp-wide wait until *p >= target.  Lane 0 polls with relaxed
-// loads (backing off with nanosleep); once the target is seen, one fence
-// turns the observation into an acquire for the whole warp.  Gives up like
+// loads (backing off with nanosleep).  Relaxed throughout: seeing the target
+// orders nothing, so what the caller reads next must tell by itself whether
+// it is current (the global exchange's tagged words do).  Gives up like
 // mbar_wait when the CTA aborts or the time limit passes.
 __device__ __forceinline__ bool gwait_geq(const WaitGuard& g, const int* p, int target, uint32_t site,
                                           uint32_t tile) {
@@ -250,9 +258,8 @@ __device__ __forceinline__ bool gwait_geq(const WaitGuard& g, const int* p, int 
                 }
             }
         }
-        if (state == 1) fence_acq_rel_gpu();
     }
-    state = __shfl_sync(0xffffffffu, state, 0);  // orders the other lanes after lane 0's fence
+    state = __shfl_sync(0xffffffffu, state, 0);
     return state == 1;
 }
 
