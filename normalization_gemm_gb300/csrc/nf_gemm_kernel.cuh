@@ -27,7 +27,8 @@
 //   warps 10-13 (pre-norm only) sum of squares of each X row, read from the
 //              same shared-memory stage the tensor cores consume, on CUDA
 //              cores, in parallel with the MMA (blog §2 pseudocode:
-//              square_sum += (tile_A * tile_A).sum(-1)).
+//              square_sum += (tile_A * tile_A).sum(-1)); with the sums split
+//              over a row's tiles, warp 10 alone sums the tile's share of rows.
 //
 // Shared-memory operands (128-byte swizzle, 1 KB aligned):
 //   A stage  128 rows x 64 K, K-major: row r at r*128 bytes.
@@ -47,8 +48,8 @@
 // expiry the kernel records NF_ERR_TIMEOUT, drains what it issued, frees TMEM
 // and returns.
 //
-// CTA pair (OPS_PAIR, plain and pre-norm GEMMs of 256-column tiles): a
-// cluster of two CTAs along M computes a 256 x 256 tile with tcgen05
+// CTA pair (OPS_PAIR: plain, pre-norm and globally exchanging post-norm GEMMs
+// of 256-column tiles): a cluster of two CTAs along M computes a 256 x 256 tile with tcgen05
 // cta_group::2 MMAs.  Each CTA's producer loads its own 128 rows of A and half
 // of B's 256 columns into its own ring stage (32 KB instead of 48, so six
 // stages fit), counted on the first CTA's full barrier; the first CTA's MMA
@@ -57,12 +58,12 @@
 // both CTAs.  The second CTA's MMA warp relays its epilogue's "accumulator
 // drained" to the first CTA.  Pre-norm: a sum-of-squares thread of the first
 // CTA, once full[s] shows both CTAs' bytes landed, tells the second CTA's
-// sum-of-squares warps (ardy[s]) with a relaxed remote arrive.  (Measured: the
-// pre-norm pair runs no faster than one CTA per tile -- see the plan, which
-// keeps pre-norm GEMMs on single CTAs -- while a release arrive per stage,
-// or a first CTA summing its peer's rows through distributed shared memory,
-// was three times slower.)  Each
-// CTA's epilogue is unchanged.
+// sum-of-squares warps (ardy[s]) with a relaxed remote arrive.  (Measured: with
+// every tile summing all its rows the pre-norm pair runs no faster than one CTA
+// per tile -- the plan pairs pre-norm GEMMs only with the split sums -- while a
+// release arrive per stage, or a first CTA summing its peer's rows through
+// distributed shared memory, was three times slower.)  Each CTA's epilogue is
+// unchanged.
 //
 // Post-norm rows wider than one tile exchange partial row statistics between
 // the CTAs that hold the row (XCH):
@@ -71,8 +72,8 @@
 //                in blog §3.
 //   XCH_GLOBAL   the row's tiles are ordinary tiles of a persistent grid whose
 //                CTAs are all resident at once (cooperative launch); partials
-//                go through L2 with an arrival counter per (row tile,
-//                32-row quarter).
+//                go through L2 as tagged words, with an arrival counter per
+//                row tile that only says when to read them (no fence).
 //                Tile t runs on CTA t mod G in order, G >= n_tiles / 2, so a
 //                CTA's tiles t_i and t_{i-2} (which share a TMEM buffer) lie in
 //                different row tiles and every wait points at an earlier row
@@ -911,8 +912,8 @@ __global__ void __launch_bounds__(GemmCfg<EPI, TILE_N, XCH, OPS>::THREADS, 1)
         // to 16 column tiles need those registers, and the residual add, whose
         // staging of R does: those read the segment (X W + R) again from TMEM.
         constexpr bool KEEP_SEG = Cfg::kPost && !GLOBALX && !Cfg::kRes;  // (the backward needs them for Z)
-        // The global exchange's release fence (lane 0) should not wait for
-        // this warp's bulk stores: another lane issues them.
+        // The global exchange's lane 0 counts and polls; another lane issues
+        // the warp's bulk stores.
         constexpr int STORE_LANE = GLOBALX ? 31 : 0;
         constexpr int NC = SEG / 32;
         const int grp = warp >> 2;
